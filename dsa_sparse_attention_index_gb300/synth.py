@@ -1,0 +1,262 @@
+"""Seeded synthetic workloads for the DSA decode path.
+
+This module only *generates inputs*: random draws, their rounding into the
+storage formats (E4M3 bytes, bf16 bits, MXFP4 codes) and their placement in
+the packed paged cache.  It contains none of the method's arithmetic (no
+scoring, selection or attention), and it is the only code that the CUDA path
+and the fp64 oracle both consume.  Every array is produced on the host from
+one ``numpy.random.Generator(PCG64(seed))`` in a fixed draw order.
+
+Cache layout (per block row; the descriptor values below are passed to both
+the library and the oracle, which each read the bytes on their own):
+
+    FP8 index keys   [latent page 64 x 576 B][codes 64 x 128 B][scales 64 x fp32]
+                     row = 36,864 + 8,448 = 45,312 B
+    MXFP4 index keys [latent page 64 x 576 B][codes 64 x 64 B][E8M0 64 x 4 B]
+                     row = 36,864 + 4,352 = 41,216 B
+
+Both row sizes and both page offsets are multiples of 128 B.  The packed
+block row (one contiguous row per cache block holding a layer's latent page
+and index-key page) follows the Kimi K3.1 Pro Day-0 post, section on the KV
+cache that serves three kinds of state; the split of the 132-byte FP8 key
+into a 128-byte code row and a separate fp32 scale keeps every code row
+16-byte aligned.
+"""
+from __future__ import annotations
+
+import dataclasses
+import math
+
+import numpy as np
+
+BLOCK = 64
+IDX_HEADS, IDX_DIM = 32, 128
+MLA_HEADS, LATENT, VALUE = 96, 576, 512
+KEY_FP8, KEY_MXFP4 = 0, 1
+
+LATENT_PAGE = BLOCK * LATENT                      # 36,864 B
+INDEX_PAGE = {KEY_FP8: BLOCK * (IDX_DIM + 4),     # 8,448 B
+              KEY_MXFP4: BLOCK * (IDX_DIM // 2 + 4)}  # 4,352 B
+
+_E2M1_GRID = np.array([0.0, 0.5, 1.0, 1.5, 2.0, 3.0, 4.0, 6.0])
+
+
+@dataclasses.dataclass
+class Case:
+    """One synthetic decode workload, laid out exactly as the cache expects."""
+
+    name: str
+    batch: int
+    nq: int                     # query rows per sequence (speculative draft size)
+    seq_lens: np.ndarray        # int32 [batch], context incl. the current token(s)
+    key_format: int             # KEY_FP8 or KEY_MXFP4
+    topk: int
+    pool: np.ndarray            # uint8 [num_blocks, row_stride]
+    row_stride: int
+    latent_off: int
+    index_off: int
+    latent_scale: float
+    block_table: np.ndarray     # int32 [batch, max_blocks]; -1 = unallocated
+    q_index: np.ndarray         # uint8 (E4M3 codes) [rows, 32, 128]
+    head_w: np.ndarray          # float32 [rows, 32]
+    q_mla: np.ndarray           # uint16 (bf16 bits) [rows, 96, 576]
+    sm_scale: float
+    seed: int = 0
+
+    @property
+    def rows(self) -> int:
+        return self.batch * self.nq
+
+    @property
+    def num_blocks(self) -> int:
+        return int(self.pool.shape[0])
+
+    @property
+    def max_len(self) -> int:
+        return int(self.seq_lens.max()) if self.batch else 0
+
+    def row_lens(self) -> np.ndarray:
+        """Tokens visible to each query row: row j of a sequence with context L
+        and nq draft rows sees L - (nq - 1) + j tokens (causal within the draft)."""
+        L = np.repeat(self.seq_lens.astype(np.int64), self.nq)
+        j = np.tile(np.arange(self.nq, dtype=np.int64), self.batch)
+        return np.maximum(L - (self.nq - 1) + j, 0).astype(np.int32)
+
+    def token_bytes(self) -> int:
+        return 132 if self.key_format == KEY_FP8 else 68
+
+
+# ---------------------------------------------------------------------------
+# storage-format encoders (input rounding only)
+# ---------------------------------------------------------------------------
+
+def e4m3_encode(x: np.ndarray) -> np.ndarray:
+    """Round to OCP E4M3 ('fn') codes, nearest-even, saturating at +-448."""
+    import torch
+
+    t = torch.from_numpy(np.clip(np.asarray(x, dtype=np.float32), -448.0, 448.0))
+    return t.to(torch.float8_e4m3fn).view(torch.uint8).numpy()
+
+
+def bf16_encode(x: np.ndarray) -> np.ndarray:
+    """Round to bfloat16 (nearest-even); returns the raw 16-bit patterns."""
+    import torch
+
+    t = torch.from_numpy(np.ascontiguousarray(x, dtype=np.float32))
+    return t.to(torch.bfloat16).view(torch.int16).numpy().view(np.uint16)
+
+
+def mxfp4_encode(x: np.ndarray):
+    """OCP MX quantisation of rows of 128 values into E2M1 elements with one
+    E8M0 scale per 32 elements.  Shared exponent floor(log2(amax)) - 2 (2 is
+    E2M1's largest exponent), elements rounded to nearest-even and clamped
+    to +-6.  Returns (packed codes uint8 [n, 64], e8m0 uint8 [n, 4]); element
+    2i sits in the low nibble of byte i."""
+    x = np.asarray(x, dtype=np.float64).reshape(-1, IDX_DIM // 32, 32)
+    amax = np.abs(x).max(axis=2)
+    with np.errstate(divide="ignore"):
+        e = np.where(amax > 0, np.floor(np.log2(np.where(amax > 0, amax, 1.0))) - 2, -127)
+    e = np.clip(e, -127, 127).astype(np.int64)
+    scaled = x / np.ldexp(1.0, e)[..., None]
+    mag = np.abs(scaled)
+    d = np.abs(mag[..., None] - _E2M1_GRID)
+    d = d + (np.arange(8) % 2) * 1e-12          # exact ties go to the even code
+    code = np.argmin(d, axis=-1).astype(np.uint8)
+    code = np.where(mag >= 6.0, 7, code).astype(np.uint8)
+    code = code | np.where(scaled < 0, 8, 0).astype(np.uint8)
+    code = code.reshape(-1, IDX_DIM)
+    packed = (code[:, 0::2] | (code[:, 1::2] << 4)).astype(np.uint8)
+    e8m0 = (e + 127).astype(np.uint8).reshape(-1, IDX_DIM // 32)
+    return packed, e8m0
+
+
+# ---------------------------------------------------------------------------
+# workload construction
+# ---------------------------------------------------------------------------
+
+def make_case(name: str, seq_lens, nq: int = 1, key_format: int = KEY_FP8, topk: int = 2048,
+              heavy_tail: float = 0.0, permute_blocks: bool = True, spare_blocks: int = 0,
+              seed: int = 0, chunk_tokens: int = 1 << 16) -> Case:
+    """Build a workload.  Draw order: block permutation, latent scale, then
+    per sequence and per token chunk: index-key values, heavy-tail mask,
+    per-token key scales (FP8 only), latent values; then tail/spare filler
+    bytes; then indexer queries, head weights, MLA queries.
+
+    Distributions: index keys and latents E4M3(N(0,1)); key scales U(0.5, 2);
+    latent scale U(0.5, 2); indexer queries E4M3(N(0,1)) [32, 128]; head
+    weights N(0, 0.1^2) fp32; MLA queries bf16(N(0,1)) [96, 576].  With
+    ``heavy_tail`` = f, a fraction f of tokens have their key values x4 before
+    rounding.  MXFP4 keys quantise the same N(0,1) draws per OCP MX.
+    """
+    rng = np.random.Generator(np.random.PCG64(seed))
+    seq_lens = np.asarray(seq_lens, dtype=np.int32).reshape(-1)
+    batch = int(seq_lens.shape[0])
+    nblk = [max(1, math.ceil(int(L) / BLOCK)) for L in seq_lens]
+    max_blocks = max(nblk) if nblk else 1
+    used = sum(nblk)
+    num_blocks = used + int(spare_blocks)
+    perm = rng.permutation(num_blocks).astype(np.int32)   # drawn in every case: fixed draw order
+    if not permute_blocks:
+        perm = np.arange(num_blocks, dtype=np.int32)
+    latent_scale = float(rng.uniform(0.5, 2.0))
+
+    idx_page = INDEX_PAGE[key_format]
+    row_stride = LATENT_PAGE + idx_page
+    latent_off, index_off = 0, LATENT_PAGE
+    pool = np.zeros((num_blocks, row_stride), dtype=np.uint8)
+    block_table = np.full((batch, max_blocks), -1, dtype=np.int32)
+
+    cursor = 0
+    for b in range(batch):
+        rows_b = perm[cursor:cursor + nblk[b]]
+        cursor += nblk[b]
+        block_table[b, :nblk[b]] = rows_b
+        L = int(seq_lens[b])
+        for t0 in range(0, L, chunk_tokens):
+            n = min(chunk_tokens, L - t0)
+            kv = rng.standard_normal((n, IDX_DIM), dtype=np.float32)
+            if heavy_tail > 0:
+                kv *= np.where(rng.random(n) < heavy_tail, 4.0, 1.0).astype(np.float32)[:, None]
+            if key_format == KEY_FP8:
+                codes = e4m3_encode(kv)
+                scales = rng.uniform(0.5, 2.0, size=n).astype(np.float32)
+            else:
+                codes, e8 = mxfp4_encode(kv)
+            lat = e4m3_encode(rng.standard_normal((n, LATENT), dtype=np.float32))
+            t = np.arange(t0, t0 + n)
+            r = rows_b[t // BLOCK]
+            slot = t % BLOCK
+            # scatter token rows into their pages
+            lat_view = pool[:, latent_off:latent_off + LATENT_PAGE].reshape(num_blocks, BLOCK, LATENT)
+            lat_view[r, slot] = lat
+            if key_format == KEY_FP8:
+                cview = pool[:, index_off:index_off + BLOCK * IDX_DIM].reshape(num_blocks, BLOCK, IDX_DIM)
+                cview[r, slot] = codes
+                sview = pool[:, index_off + BLOCK * IDX_DIM:index_off + idx_page].reshape(num_blocks, BLOCK, 4)
+                sview[r, slot] = scales.view(np.uint8).reshape(n, 4)
+            else:
+                cb = IDX_DIM // 2
+                cview = pool[:, index_off:index_off + BLOCK * cb].reshape(num_blocks, BLOCK, cb)
+                cview[r, slot] = codes
+                eview = pool[:, index_off + BLOCK * cb:index_off + idx_page].reshape(num_blocks, BLOCK, 4)
+                eview[r, slot] = e8
+    # filler: unused tail slots of each last page, and spare rows, get random bytes
+    for b in range(batch):
+        L = int(seq_lens[b])
+        tail = L % BLOCK if L > 0 else 0
+        if tail or L == 0:
+            r = block_table[b, nblk[b] - 1]
+            s0 = tail
+            fill = rng.integers(0, 256, size=(BLOCK - s0, LATENT), dtype=np.uint8)
+            pool[r, latent_off:latent_off + LATENT_PAGE].reshape(BLOCK, LATENT)[s0:] = fill
+            per_tok = idx_page // BLOCK
+            code_b = per_tok - 4
+            codes_view = pool[r, index_off:index_off + BLOCK * code_b].reshape(BLOCK, code_b)
+            codes_view[s0:] = rng.integers(0, 256, size=(BLOCK - s0, code_b), dtype=np.uint8)
+            sc_view = pool[r, index_off + BLOCK * code_b:index_off + idx_page].reshape(BLOCK, 4)
+            sc_view[s0:] = rng.integers(0, 256, size=(BLOCK - s0, 4), dtype=np.uint8)
+    if spare_blocks:
+        spare = perm[used:]
+        pool[spare] = rng.integers(0, 256, size=(len(spare), row_stride), dtype=np.uint8)
+
+    rows = batch * nq
+    q_index = e4m3_encode(rng.standard_normal((rows, IDX_HEADS, IDX_DIM), dtype=np.float32))
+    head_w = (rng.standard_normal((rows, IDX_HEADS)) * 0.1).astype(np.float32)
+    q_mla = bf16_encode(rng.standard_normal((rows, MLA_HEADS, LATENT), dtype=np.float32))
+    return Case(name=name, batch=batch, nq=nq, seq_lens=seq_lens, key_format=key_format, topk=topk,
+                pool=pool, row_stride=row_stride, latent_off=latent_off, index_off=index_off,
+                latent_scale=latent_scale, block_table=block_table, q_index=q_index, head_w=head_w,
+                q_mla=q_mla, sm_scale=1.0 / math.sqrt(LATENT), seed=seed)
+
+
+# ---------------------------------------------------------------------------
+# the named workloads
+# ---------------------------------------------------------------------------
+
+WORKLOADS = {
+    # tiny single decode: batch 1, one query, L = 4096, identity block table
+    "decode_b1_l4096": dict(seq_lens=[4096], nq=1, permute_blocks=False),
+    # speculative verify: 8 sequences x 4 causal draft rows, L = 32,768 each
+    "specdecode_b8x4_l32768": dict(seq_lens=[32768] * 8, nq=4),
+    # long-context batch: 32 sequences, L ~ U(64K, 160K), 10% of keys x4
+    "longctx_b32_l64k-160k": dict(seq_lens=None, nq=1, heavy_tail=0.10),
+    # 1M-token decode with MXFP4 index keys: batch 4
+    "mxfp4_b4_l1m": dict(seq_lens=[1 << 20] * 4, nq=1, key_format=KEY_MXFP4),
+    # chunked-prefill append: 2048 new query rows on a 151,552-token prefix
+    "prefill_q2048_l153600": dict(seq_lens=[153600], nq=2048),
+}
+
+
+def longctx_lengths(seed: int = 0, batch: int = 32, lo: int = 65536, hi: int = 163840) -> np.ndarray:
+    """Context lengths of the long-context batch: integers U[lo, hi], drawn
+    from their own seeded generator so the workload is reproducible."""
+    rng = np.random.Generator(np.random.PCG64(seed + 1000))
+    return rng.integers(lo, hi + 1, size=batch).astype(np.int32)
+
+
+def workload(name: str, seed: int = 0, **overrides) -> Case:
+    spec = dict(WORKLOADS[name])
+    spec.update(overrides)
+    if spec.get("seq_lens") is None:
+        spec["seq_lens"] = longctx_lengths(seed)
+    return make_case(name, seed=seed, **spec)

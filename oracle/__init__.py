@@ -1,0 +1,187 @@
+"""fp64 CPU oracle for the DSA decode hot path — TEST INFRASTRUCTURE ONLY.
+
+Only ``tests/``, ``__graft_entry__.smoke()`` and ``bench.py``'s CPU-baseline
+leg may import this package.  The product path (``dsa_sparse_attention_index_gb300``
+and its CUDA library) never does, and shares no code with it.
+
+The arithmetic lives in ``dsa_oracle.c`` (plain C, double precision); this
+module only compiles it with ``gcc`` and marshals numpy arrays through ctypes.
+Each function's docstring names the passage of the source pages it follows;
+the C file's header lists the pages and the readings taken where they are
+silent.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import subprocess
+import threading
+
+import numpy as np
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_SRC = os.path.join(_HERE, "dsa_oracle.c")
+_LIB = os.path.join(_HERE, "liboracle.so")
+_lock = threading.Lock()
+_lib = None
+
+IDX_HEADS, IDX_DIM = 32, 128
+MLA_HEADS, LATENT, VALUE = 96, 576, 512
+
+
+def build(force: bool = False) -> str:
+    """Compile the oracle into ``oracle/liboracle.so`` (gcc, OpenMP)."""
+    if force or not os.path.exists(_LIB) or os.path.getmtime(_LIB) < os.path.getmtime(_SRC):
+        tmp = _LIB + f".tmp{os.getpid()}"
+        subprocess.check_call(
+            ["gcc", "-O2", "-std=c11", "-fopenmp", "-fPIC", "-shared", _SRC, "-o", tmp, "-lm"]
+        )
+        os.replace(tmp, _LIB)
+    return _LIB
+
+
+def _load():
+    global _lib
+    with _lock:
+        if _lib is None:
+            build()
+            lib = ctypes.CDLL(_LIB)
+            P = ctypes.c_void_p
+            i32, i64, f64 = ctypes.c_int32, ctypes.c_int64, ctypes.c_double
+            lib.oracle_e4m3_to_double.argtypes = [ctypes.c_uint8]
+            lib.oracle_e4m3_to_double.restype = f64
+            lib.oracle_e2m1_to_double.argtypes = [ctypes.c_uint8]
+            lib.oracle_e2m1_to_double.restype = f64
+            lib.oracle_e8m0_to_double.argtypes = [ctypes.c_uint8]
+            lib.oracle_e8m0_to_double.restype = f64
+            lib.oracle_bf16_to_double.argtypes = [ctypes.c_uint16]
+            lib.oracle_bf16_to_double.restype = f64
+            lib.oracle_index_scores.argtypes = [P, i64, i64, i32, i32, P, i32, P, i32, i32, P, P, P, i64]
+            lib.oracle_index_scores.restype = i32
+            lib.oracle_index_score_bounds.argtypes = [P, i64, i64, i32, i32, P, i32, P, i32, i32, P, P, P, i64]
+            lib.oracle_index_score_bounds.restype = i32
+            lib.oracle_topk.argtypes = [P, i64, P, i32, i32, P]
+            lib.oracle_topk.restype = i32
+            lib.oracle_sparse_mla.argtypes = [P, i64, i64, i32, f64, P, i32, P, i32, i32, P, P, i32, f64, P, P]
+            lib.oracle_sparse_mla.restype = i32
+            lib.oracle_num_threads.argtypes = []
+            lib.oracle_num_threads.restype = i32
+            _lib = lib
+    return _lib
+
+
+def _ptr(a: np.ndarray) -> int:
+    assert a.flags["C_CONTIGUOUS"], "oracle inputs must be C-contiguous"
+    return a.ctypes.data
+
+
+class OracleError(RuntimeError):
+    pass
+
+
+def _check(rc: int, what: str) -> None:
+    if rc == 1:
+        raise OracleError(f"{what}: invalid argument")
+    if rc == 3:
+        raise OracleError(f"{what}: block-table entry or token index outside the cache")
+    if rc != 0:
+        raise OracleError(f"{what}: error {rc}")
+
+
+def num_threads() -> int:
+    return int(_load().oracle_num_threads())
+
+
+def e4m3_to_double(code: int) -> float:
+    """OCP E4M3 ('fn') decode from the format definition."""
+    return float(_load().oracle_e4m3_to_double(code))
+
+
+def e2m1_to_double(code: int) -> float:
+    """OCP MX E2M1 decode from the format definition."""
+    return float(_load().oracle_e2m1_to_double(code))
+
+
+def e8m0_to_double(code: int) -> float:
+    """OCP MX E8M0 scale decode: 2^(E-127)."""
+    return float(_load().oracle_e8m0_to_double(code))
+
+
+def bf16_to_double(bits: int) -> float:
+    return float(_load().oracle_bf16_to_double(bits))
+
+
+def _cache_args(case):
+    return (
+        _ptr(case.pool), int(case.row_stride), int(case.index_off), int(case.num_blocks),
+        int(case.key_format), _ptr(case.block_table), int(case.block_table.shape[1]),
+        _ptr(case.seq_lens), int(case.batch), int(case.nq),
+    )
+
+
+def index_scores(case, rows_ld: int | None = None) -> np.ndarray:
+    """Lightning-indexer scores s[row, t] in fp64 for every visible token.
+
+    Follows the Kimi K3.1 Pro Day-0 post, section on sparse attention (32
+    light heads score every prior token with a 132-byte FP8 key) and its AMD
+    MXFP4-indexer section (68-byte keys, FP32 accumulation, weighted head
+    reduction).  Entries beyond a row's visible length are NaN.
+    """
+    ld = int(rows_ld or case.max_len)
+    out = np.full((case.rows, ld), np.nan, dtype=np.float64)
+    q = np.ascontiguousarray(case.q_index)
+    w = np.ascontiguousarray(case.head_w)
+    rc = _load().oracle_index_scores(*_cache_args(case), _ptr(q), _ptr(w), _ptr(out), ld)
+    _check(rc, "index_scores")
+    return out
+
+
+def index_score_bounds(case, rows_ld: int | None = None) -> np.ndarray:
+    """A_t = sum_h |w_h| |scale_t| sum_d |q_hd k_td| — the magnitude that any
+    evaluation order's rounding error of the score is proportional to."""
+    ld = int(rows_ld or case.max_len)
+    out = np.full((case.rows, ld), np.nan, dtype=np.float64)
+    rc = _load().oracle_index_score_bounds(
+        *_cache_args(case), _ptr(np.ascontiguousarray(case.q_index)),
+        _ptr(np.ascontiguousarray(case.head_w)), _ptr(out), ld)
+    _check(rc, "index_score_bounds")
+    return out
+
+
+def topk(scores: np.ndarray, row_lens: np.ndarray, k: int) -> np.ndarray:
+    """Top-k token indices per row: ties to the lower index, ascending output,
+    -1 padding (the Day-0 post keeps the top 2,048 tokens per query)."""
+    s = np.ascontiguousarray(scores, dtype=np.float64)
+    lens = np.ascontiguousarray(row_lens, dtype=np.int32)
+    rows = s.shape[0]
+    out = np.empty((rows, k), dtype=np.int32)
+    rc = _load().oracle_topk(_ptr(s), s.shape[1], _ptr(lens), rows, int(k), _ptr(out))
+    _check(rc, "topk")
+    return out
+
+
+def sparse_mla(case, idx: np.ndarray, k: int | None = None):
+    """Exact absorbed-MLA attention of 96 heads over the selected latents
+    (Day-0 post, sparse-attention section: MLA runs exactly on the kept
+    tokens).  Returns (out [rows, 96, 512] fp64, lse [rows, 96] fp64)."""
+    idx = np.ascontiguousarray(idx, dtype=np.int32)
+    k = int(k or idx.shape[1])
+    out = np.empty((case.rows, MLA_HEADS, VALUE), dtype=np.float64)
+    lse = np.empty((case.rows, MLA_HEADS), dtype=np.float64)
+    q = np.ascontiguousarray(case.q_mla, dtype=np.uint16)
+    rc = _load().oracle_sparse_mla(
+        _ptr(case.pool), int(case.row_stride), int(case.latent_off), int(case.num_blocks),
+        float(case.latent_scale), _ptr(case.block_table), int(case.block_table.shape[1]),
+        _ptr(case.seq_lens), int(case.batch), int(case.nq), _ptr(q), _ptr(idx), k,
+        float(case.sm_scale), _ptr(out), _ptr(lse))
+    _check(rc, "sparse_mla")
+    return out, lse
+
+
+def decode_step(case):
+    """The whole decode hot path: scores -> top-k -> sparse MLA, in fp64.
+    Returns (scores, idx, out, lse)."""
+    s = index_scores(case)
+    idx = topk(s, case.row_lens(), case.topk)
+    out, lse = sparse_mla(case, idx, case.topk)
+    return s, idx, out, lse

@@ -1,0 +1,387 @@
+/*
+ * dsa_oracle.c — plain, slow, fp64 CPU oracle for the DSA decode hot path.
+ *
+ * TEST INFRASTRUCTURE ONLY.  Nothing in the product path (the CUDA library
+ * and its Python binding) may include, link, load or call this file.  Only
+ * the test-suite, the smoke check and the benchmark's CPU-baseline leg use
+ * it.  It shares no code, header, table or constant with the CUDA path: the
+ * number formats are decoded here from their published definitions, and the
+ * paged-cache layout is read from the descriptor values the caller passes.
+ *
+ * Sources (cited by page title and section):
+ *   [K31]  "vLLM 为 Kimi K3.1 Pro 提供 Day-0 支持" (vLLM Day-0 support for
+ *          Kimi K3.1 Pro), sections "K3.1 Pro 中的稀疏注意力" (sparse
+ *          attention), "为三类状态服务的 KV 缓存" (the packed KV cache),
+ *          "量化：原生 MXFP4 索引器" (MXFP4 indexer, AMD section).
+ *   [SUM]  "vLLM 对 Kimi K3.1 Pro 的 Day-0 支持：稀疏注意力、DCP 与零失配强化学习"
+ *          (agentlens summary), architecture table (32 heads x 128 dims,
+ *          FP8 keys, top-2048, NoPE) and the per-token KV byte table.
+ *   Formats: OCP 8-bit floating point (E4M3, "fn" variant without infinities)
+ *   and the OCP Microscaling (MX) specification (E2M1 elements, E8M0 scales).
+ *
+ * What is computed (all arithmetic in double precision):
+ *   index score   s[t] = sum_h w[h] * max(0, scale_t * (q_h . k_t))
+ *                 32 heads x 128 dims; FP8 key + fp32 scale = 132 B per token
+ *                 ([K31] sparse-attention section; [SUM] architecture table).
+ *                 The ReLU/weighted-head form is DeepSeek-V3.2's lightning
+ *                 indexer, which [K31] names as the origin of DSA; the AMD
+ *                 section confirms FP32 accumulation and a weighted reduction
+ *                 across heads.
+ *   MXFP4 keys    k[d] = 2^(E[d/32]-127) * e2m1(code[d]), 128 elements +
+ *                 4 E8M0 scales = 68 B per token, no per-token fp32 scale
+ *                 ([K31] MXFP4 indexer section: 132 B -> 68 B).
+ *   top-k         keep the k highest-scoring visible tokens (k = 2048 in the
+ *                 model, [K31]); ties go to the lower token index; output in
+ *                 ascending token order, padded with -1.
+ *   sparse MLA    exact softmax attention of 96 heads over the selected
+ *                 tokens' 576-wide latents (absorbed MLA: keys are the full
+ *                 576 columns, values the first 512) ([K31] "MLA attention
+ *                 then runs exactly, but only on these 2,048 tokens").
+ *
+ * Paged cache ([K31] packed-cache section): a pool of block rows; a block row
+ * holds, at caller-given byte offsets, the latent page (64 tokens x 576 B
+ * e4m3) and the index-key page.  The FP8 index page stores the 64 codes
+ * rows (64 x 128 B) followed by the 64 fp32 scales; the MXFP4 page stores
+ * 64 x 64 B of packed E2M1 codes followed by 64 x 4 E8M0 scales.  Token t of
+ * sequence b lives in block row block_table[b][t / 64], slot t % 64.
+ *
+ * Visibility: a sequence with nq query rows (speculative-verify draft) and
+ * context length L: query row j (0 <= j < nq) sees the first L - (nq-1) + j
+ * tokens (causal within the draft; nq = 1 gives L).
+ *
+ * Pins (tests/test_oracle_pins.py) tie every function here to something other
+ * than itself: library decoders, exact integer dot products, closed forms,
+ * brute-force selection, and a library softmax on the gathered rows.
+ */
+#include <math.h>
+#include <stdint.h>
+#include <stdlib.h>
+#include <string.h>
+
+#define ORACLE_BLOCK 64          /* tokens per page */
+#define ORACLE_IDX_HEADS 32      /* light indexer heads */
+#define ORACLE_IDX_DIM 128       /* indexer head dimension */
+#define ORACLE_MLA_HEADS 96      /* MLA attention heads */
+#define ORACLE_LATENT 576        /* latent width (keys) */
+#define ORACLE_VALUE 512         /* value width (first 512 latent columns) */
+
+enum { ORACLE_OK = 0, ORACLE_BAD_ARG = 1, ORACLE_BAD_BLOCK = 3 };
+
+/* ------------------------------------------------------------------ */
+/* Number formats, decoded from their definitions.                     */
+/* ------------------------------------------------------------------ */
+
+/* OCP E4M3 ("fn"): 1 sign, 4 exponent (bias 7), 3 mantissa bits; no
+ * infinities; S.1111.111 is NaN; largest finite 448. */
+double oracle_e4m3_to_double(uint8_t c) {
+  int s = (c >> 7) & 1, e = (c >> 3) & 0xF, m = c & 7;
+  double v;
+  if (e == 0xF && m == 7) return NAN;
+  if (e == 0) v = ldexp((double)m / 8.0, -6);
+  else v = ldexp(1.0 + (double)m / 8.0, e - 7);
+  return s ? -v : v;
+}
+
+/* OCP MX E2M1: 1 sign, 2 exponent (bias 1), 1 mantissa bit; no NaN/inf.
+ * Magnitudes {0, 0.5, 1, 1.5, 2, 3, 4, 6}. Only the low 4 bits are used. */
+double oracle_e2m1_to_double(uint8_t c) {
+  int s = (c >> 3) & 1, e = (c >> 1) & 3, m = c & 1;
+  double v;
+  if (e == 0) v = 0.5 * m;
+  else v = ldexp(1.0 + 0.5 * m, e - 1);
+  return s ? -v : v;
+}
+
+/* OCP MX E8M0 scale: 2^(E-127); 0xFF is NaN. */
+double oracle_e8m0_to_double(uint8_t c) {
+  if (c == 0xFF) return NAN;
+  return ldexp(1.0, (int)c - 127);
+}
+
+/* bfloat16: the upper 16 bits of an IEEE binary32. */
+double oracle_bf16_to_double(uint16_t b) {
+  uint32_t u = (uint32_t)b << 16;
+  float f;
+  memcpy(&f, &u, 4);
+  return (double)f;
+}
+
+static float load_f32(const uint8_t* p) {
+  float f;
+  memcpy(&f, p, 4);
+  return f;
+}
+
+/* Visible length of query row j of a sequence with context L and nq rows. */
+static int64_t visible_len(int64_t L, int nq, int j) {
+  int64_t v = L - (nq - 1) + j;
+  return v < 0 ? 0 : v;
+}
+
+/* Address of the block row holding token t of sequence b, or NULL if the
+ * block table entry is outside the pool. */
+static const uint8_t* block_row(const uint8_t* pool, int64_t row_stride, int32_t num_blocks,
+                                const int32_t* block_table, int32_t max_blocks, int b, int64_t t) {
+  int64_t j = t / ORACLE_BLOCK;
+  if (j >= max_blocks) return NULL;
+  int32_t r = block_table[(int64_t)b * max_blocks + j];
+  if (r < 0 || r >= num_blocks) return NULL;
+  return pool + (int64_t)r * row_stride;
+}
+
+/* ------------------------------------------------------------------ */
+/* Lightning indexer scores.                                           */
+/* ------------------------------------------------------------------ */
+
+/* raw[h] = q_h . k_t  for the FP8 key of token t (exact in double: every
+ * e4m3 value is a multiple of 2^-9 below 2^9, so each product is a multiple
+ * of 2^-18 below 2^18 and a 128-term sum stays far inside 53 bits). */
+static void raw_dots_fp8(const uint8_t* q /*[32][128] codes*/, const uint8_t* key /*[128]*/,
+                         double raw[ORACLE_IDX_HEADS]) {
+  double k[ORACLE_IDX_DIM];
+  for (int d = 0; d < ORACLE_IDX_DIM; ++d) k[d] = oracle_e4m3_to_double(key[d]);
+  for (int h = 0; h < ORACLE_IDX_HEADS; ++h) {
+    double acc = 0.0;
+    for (int d = 0; d < ORACLE_IDX_DIM; ++d)
+      acc += oracle_e4m3_to_double(q[h * ORACLE_IDX_DIM + d]) * k[d];
+    raw[h] = acc;
+  }
+}
+
+/* raw[h] = q_h . k_t for an MXFP4 key: 128 E2M1 codes packed two per byte
+ * (element 2i in the low nibble of byte i, element 2i+1 in the high nibble)
+ * and one E8M0 scale per 32 consecutive elements. */
+static void raw_dots_mxfp4(const uint8_t* q, const uint8_t* packed /*[64]*/,
+                           const uint8_t* e8m0 /*[4]*/, double raw[ORACLE_IDX_HEADS]) {
+  double k[ORACLE_IDX_DIM];
+  for (int d = 0; d < ORACLE_IDX_DIM; ++d) {
+    uint8_t byte = packed[d / 2];
+    uint8_t nib = (d % 2 == 0) ? (byte & 0xF) : (byte >> 4);
+    k[d] = oracle_e8m0_to_double(e8m0[d / 32]) * oracle_e2m1_to_double(nib);
+  }
+  for (int h = 0; h < ORACLE_IDX_HEADS; ++h) {
+    double acc = 0.0;
+    for (int d = 0; d < ORACLE_IDX_DIM; ++d)
+      acc += oracle_e4m3_to_double(q[h * ORACLE_IDX_DIM + d]) * k[d];
+    raw[h] = acc;
+  }
+}
+
+/* Scores of every visible token for every query row.
+ *   key_format 0: FP8 page = 64 x 128 B codes, then 64 fp32 scales.
+ *   key_format 1: MXFP4 page = 64 x 64 B packed codes, then 64 x 4 E8M0.
+ * scores[row * ld + t] is written for t < visible length; other entries are
+ * left untouched.  Returns ORACLE_BAD_BLOCK if a visible token's block-table
+ * entry is outside the pool. */
+int oracle_index_scores(const uint8_t* pool, int64_t row_stride, int64_t index_off, int32_t num_blocks,
+                        int32_t key_format, const int32_t* block_table, int32_t max_blocks,
+                        const int32_t* seq_lens, int32_t batch, int32_t nq,
+                        const uint8_t* q_codes /*[batch*nq][32][128]*/, const float* head_w /*[batch*nq][32]*/,
+                        double* scores, int64_t ld) {
+  if (!pool || !block_table || !seq_lens || !q_codes || !head_w || !scores || nq < 1 || batch < 0)
+    return ORACLE_BAD_ARG;
+  if (key_format != 0 && key_format != 1) return ORACLE_BAD_ARG;
+  int bad = 0;
+  int64_t rows = (int64_t)batch * nq;
+  for (int64_t row = 0; row < rows; ++row) {
+    int b = (int)(row / nq), j = (int)(row % nq);
+    int64_t vis = visible_len(seq_lens[b], nq, j);
+    if (vis > ld) return ORACLE_BAD_ARG;
+    const uint8_t* q = q_codes + row * ORACLE_IDX_HEADS * ORACLE_IDX_DIM;
+    const float* w = head_w + row * ORACLE_IDX_HEADS;
+#pragma omp parallel for schedule(static) reduction(| : bad)
+    for (int64_t t = 0; t < vis; ++t) {
+      const uint8_t* rowp = block_row(pool, row_stride, num_blocks, block_table, max_blocks, b, t);
+      if (!rowp) { bad = 1; continue; }
+      const uint8_t* page = rowp + index_off;
+      int slot = (int)(t % ORACLE_BLOCK);
+      double raw[ORACLE_IDX_HEADS];
+      double scale;
+      if (key_format == 0) {
+        raw_dots_fp8(q, page + slot * ORACLE_IDX_DIM, raw);
+        scale = (double)load_f32(page + ORACLE_BLOCK * ORACLE_IDX_DIM + slot * 4);
+      } else {
+        raw_dots_mxfp4(q, page + slot * (ORACLE_IDX_DIM / 2),
+                       page + ORACLE_BLOCK * (ORACLE_IDX_DIM / 2) + slot * 4, raw);
+        scale = 1.0;
+      }
+      double s = 0.0;
+      for (int h = 0; h < ORACLE_IDX_HEADS; ++h) {
+        double x = scale * raw[h];
+        s += (double)w[h] * (x > 0.0 ? x : 0.0);
+      }
+      scores[row * ld + t] = s;
+    }
+  }
+  return bad ? ORACLE_BAD_BLOCK : ORACLE_OK;
+}
+
+/* Per-token magnitude bound A_t = sum_h |w_h| * |scale_t| * sum_d |q_hd * k_td|
+ * (the scale of the rounding error of any evaluation order of the score). */
+int oracle_index_score_bounds(const uint8_t* pool, int64_t row_stride, int64_t index_off, int32_t num_blocks,
+                              int32_t key_format, const int32_t* block_table, int32_t max_blocks,
+                              const int32_t* seq_lens, int32_t batch, int32_t nq,
+                              const uint8_t* q_codes, const float* head_w, double* bounds, int64_t ld) {
+  if (!pool || !block_table || !seq_lens || !q_codes || !head_w || !bounds || nq < 1) return ORACLE_BAD_ARG;
+  int bad = 0;
+  int64_t rows = (int64_t)batch * nq;
+  for (int64_t row = 0; row < rows; ++row) {
+    int b = (int)(row / nq), j = (int)(row % nq);
+    int64_t vis = visible_len(seq_lens[b], nq, j);
+    if (vis > ld) return ORACLE_BAD_ARG;
+    const uint8_t* q = q_codes + row * ORACLE_IDX_HEADS * ORACLE_IDX_DIM;
+    const float* w = head_w + row * ORACLE_IDX_HEADS;
+#pragma omp parallel for schedule(static) reduction(| : bad)
+    for (int64_t t = 0; t < vis; ++t) {
+      const uint8_t* rowp = block_row(pool, row_stride, num_blocks, block_table, max_blocks, b, t);
+      if (!rowp) { bad = 1; continue; }
+      const uint8_t* page = rowp + index_off;
+      int slot = (int)(t % ORACLE_BLOCK);
+      double k[ORACLE_IDX_DIM], scale;
+      if (key_format == 0) {
+        for (int d = 0; d < ORACLE_IDX_DIM; ++d) k[d] = oracle_e4m3_to_double(page[slot * ORACLE_IDX_DIM + d]);
+        scale = (double)load_f32(page + ORACLE_BLOCK * ORACLE_IDX_DIM + slot * 4);
+      } else {
+        const uint8_t* packed = page + slot * (ORACLE_IDX_DIM / 2);
+        const uint8_t* e8 = page + ORACLE_BLOCK * (ORACLE_IDX_DIM / 2) + slot * 4;
+        for (int d = 0; d < ORACLE_IDX_DIM; ++d) {
+          uint8_t nib = (d % 2 == 0) ? (packed[d / 2] & 0xF) : (packed[d / 2] >> 4);
+          k[d] = oracle_e8m0_to_double(e8[d / 32]) * oracle_e2m1_to_double(nib);
+        }
+        scale = 1.0;
+      }
+      double a = 0.0;
+      for (int h = 0; h < ORACLE_IDX_HEADS; ++h) {
+        double acc = 0.0;
+        for (int d = 0; d < ORACLE_IDX_DIM; ++d) acc += fabs(oracle_e4m3_to_double(q[h * ORACLE_IDX_DIM + d]) * k[d]);
+        a += fabs((double)w[h]) * fabs(scale) * acc;
+      }
+      bounds[row * ld + t] = a;
+    }
+  }
+  return bad ? ORACLE_BAD_BLOCK : ORACLE_OK;
+}
+
+/* ------------------------------------------------------------------ */
+/* Top-k selection.                                                    */
+/* ------------------------------------------------------------------ */
+
+typedef struct { double s; int32_t t; } scored_t;
+
+/* Order: higher score first; NaN ranks below every number; -0 equals +0;
+ * equal scores: lower token index first. */
+static int by_score_then_index(const void* pa, const void* pb) {
+  const scored_t* a = (const scored_t*)pa;
+  const scored_t* b = (const scored_t*)pb;
+  int an = isnan(a->s), bn = isnan(b->s);
+  if (an != bn) return an ? 1 : -1;
+  if (!an) {
+    if (a->s > b->s) return -1;
+    if (a->s < b->s) return 1;
+  }
+  return (a->t < b->t) ? -1 : (a->t > b->t);
+}
+
+static int by_index(const void* pa, const void* pb) {
+  int32_t a = *(const int32_t*)pa, b = *(const int32_t*)pb;
+  return (a > b) - (a < b);
+}
+
+/* For each row: the min(k, len) best tokens among t < row_lens[row], in
+ * ascending token order, then -1 up to k entries. Scores are doubles; fp32
+ * scores converted to double keep their exact values and order. */
+int oracle_topk(const double* scores, int64_t ld, const int32_t* row_lens, int32_t rows, int32_t k,
+                int32_t* idx_out /*[rows][k]*/) {
+  if (!scores || !row_lens || !idx_out || k < 1 || rows < 0) return ORACLE_BAD_ARG;
+  int bad = 0;
+#pragma omp parallel for schedule(dynamic) reduction(| : bad)
+  for (int32_t row = 0; row < rows; ++row) {
+    int64_t len = row_lens[row];
+    if (len < 0 || len > ld) { bad = 1; continue; }
+    scored_t* all = (scored_t*)malloc(sizeof(scored_t) * (size_t)(len > 0 ? len : 1));
+    for (int64_t t = 0; t < len; ++t) { all[t].s = scores[(int64_t)row * ld + t]; all[t].t = (int32_t)t; }
+    qsort(all, (size_t)len, sizeof(scored_t), by_score_then_index);
+    int64_t n = len < k ? len : k;
+    int32_t* out = idx_out + (int64_t)row * k;
+    for (int64_t i = 0; i < n; ++i) out[i] = all[i].t;
+    qsort(out, (size_t)n, sizeof(int32_t), by_index);
+    for (int64_t i = n; i < k; ++i) out[i] = -1;
+    free(all);
+  }
+  return bad ? ORACLE_BAD_ARG : ORACLE_OK;
+}
+
+/* ------------------------------------------------------------------ */
+/* Exact sparse MLA attention over the selected tokens.                */
+/* ------------------------------------------------------------------ */
+
+/* For query row `row` (sequence row / nq), head h:
+ *   c_i      = latent_scale * e4m3(latent[t_i])         (576 values)
+ *   l_i      = sm_scale * sum_d q[h][d] * c_i[d]
+ *   out[h][d]= sum_i softmax(l)_i * c_i[d]   for d < 512
+ *   lse[h]   = ln sum_i exp(l_i)             (natural log, scaled logits)
+ * over the entries of idx[row] that are >= 0.  With no valid entry the
+ * output row is 0 and lse is -inf.  An index that is not a visible token of
+ * its sequence, or whose block is outside the pool, is an error. */
+int oracle_sparse_mla(const uint8_t* pool, int64_t row_stride, int64_t latent_off, int32_t num_blocks,
+                      double latent_scale, const int32_t* block_table, int32_t max_blocks,
+                      const int32_t* seq_lens, int32_t batch, int32_t nq,
+                      const uint16_t* q_bf16 /*[rows][96][576]*/, const int32_t* idx /*[rows][k]*/, int32_t k,
+                      double sm_scale, double* out /*[rows][96][512]*/, double* lse /*[rows][96]*/) {
+  if (!pool || !block_table || !seq_lens || !q_bf16 || !idx || !out || !lse || k < 1 || nq < 1)
+    return ORACLE_BAD_ARG;
+  int64_t rows = (int64_t)batch * nq;
+  int bad = 0;
+#pragma omp parallel for schedule(dynamic) collapse(2) reduction(| : bad)
+  for (int64_t row = 0; row < rows; ++row) {
+    for (int h = 0; h < ORACLE_MLA_HEADS; ++h) {
+      int b = (int)(row / nq), j = (int)(row % nq);
+      int64_t vis = visible_len(seq_lens[b], nq, j);
+      const int32_t* sel = idx + row * k;
+      double q[ORACLE_LATENT];
+      for (int d = 0; d < ORACLE_LATENT; ++d)
+        q[d] = oracle_bf16_to_double(q_bf16[(row * ORACLE_MLA_HEADS + h) * ORACLE_LATENT + d]);
+      double* lg = (double*)malloc(sizeof(double) * (size_t)k);
+      const uint8_t** lat = (const uint8_t**)malloc(sizeof(uint8_t*) * (size_t)k);
+      int n = 0;
+      double m = -INFINITY;
+      for (int i = 0; i < k; ++i) {
+        int32_t t = sel[i];
+        if (t < 0) continue;
+        const uint8_t* rowp = (t < vis) ? block_row(pool, row_stride, num_blocks, block_table, max_blocks, b, t) : NULL;
+        if (!rowp) { bad = 1; continue; }
+        const uint8_t* c = rowp + latent_off + (int64_t)(t % ORACLE_BLOCK) * ORACLE_LATENT;
+        double dot = 0.0;
+        for (int d = 0; d < ORACLE_LATENT; ++d) dot += q[d] * (latent_scale * oracle_e4m3_to_double(c[d]));
+        lg[n] = sm_scale * dot;
+        lat[n] = c;
+        if (lg[n] > m) m = lg[n];
+        ++n;
+      }
+      double* o = out + (row * ORACLE_MLA_HEADS + h) * ORACLE_VALUE;
+      for (int d = 0; d < ORACLE_VALUE; ++d) o[d] = 0.0;
+      if (n == 0) {
+        lse[row * ORACLE_MLA_HEADS + h] = -INFINITY;
+      } else {
+        double z = 0.0;
+        for (int i = 0; i < n; ++i) z += exp(lg[i] - m);
+        for (int i = 0; i < n; ++i) {
+          double p = exp(lg[i] - m) / z;
+          for (int d = 0; d < ORACLE_VALUE; ++d) o[d] += p * (latent_scale * oracle_e4m3_to_double(lat[i][d]));
+        }
+        lse[row * ORACLE_MLA_HEADS + h] = m + log(z);
+      }
+      free(lg);
+      free((void*)lat);
+    }
+  }
+  return bad ? ORACLE_BAD_BLOCK : ORACLE_OK;
+}
+
+/* Threads the OpenMP runtime will use (1 when built without OpenMP). */
+#ifdef _OPENMP
+#include <omp.h>
+int oracle_num_threads(void) { return omp_get_max_threads(); }
+#else
+int oracle_num_threads(void) { return 1; }
+#endif

@@ -1,0 +1,315 @@
+"""Pins for the fp64 oracle: each test ties an oracle function to something
+other than itself (a library decoder, exact integer arithmetic, a closed
+form, a brute-force property, or a library softmax), chosen so that a
+plausible mistake (dropped term, wrong sign, wrong index, swapped operand)
+fails at least one of them.  CPU only."""
+import copy
+import math
+from fractions import Fraction
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from dsa_sparse_attention_index_gb300 import synth
+
+
+# --------------------------------------------------------------- formats
+def test_e4m3_decode_matches_torch_for_all_codes():
+    codes = torch.arange(256, dtype=torch.uint8)
+    ref = codes.view(torch.float8_e4m3fn).to(torch.float64).numpy()
+    got = np.array([oracle.e4m3_to_double(c) for c in range(256)])
+    nan = np.isnan(ref)
+    assert np.array_equal(nan, np.isnan(got))
+    assert nan.sum() == 2  # 0x7F and 0xFF
+    assert np.array_equal(ref[~nan], got[~nan])
+    assert np.nanmax(got) == 448.0 and oracle.e4m3_to_double(0x01) == 2.0 ** -9
+
+
+def test_e2m1_decode_is_the_ocp_mx_table():
+    # OCP MX v1.0, FP4 E2M1: exponent bias 1, one mantissa bit, no inf/NaN.
+    mags = [0.0, 0.5, 1.0, 1.5, 2.0, 3.0, 4.0, 6.0]
+    for c in range(16):
+        want = mags[c & 7] * (-1.0 if c & 8 else 1.0)
+        assert oracle.e2m1_to_double(c) == want
+    # torch's own E2M1 container, when present, agrees on the packed nibbles
+    if hasattr(torch, "float4_e2m1fn_x2"):
+        try:
+            packed = torch.arange(256, dtype=torch.uint8).view(torch.float4_e2m1fn_x2)
+            _ = packed.to(torch.float32)  # conversion may be unsupported
+        except Exception:
+            pass
+
+
+def test_e8m0_decode_is_power_of_two():
+    for c in range(255):
+        assert oracle.e8m0_to_double(c) == math.ldexp(1.0, c - 127)
+    assert math.isnan(oracle.e8m0_to_double(255))
+
+
+def test_bf16_decode_matches_torch():
+    rng = np.random.default_rng(5)
+    bits = rng.integers(0, 1 << 16, size=4000, dtype=np.uint16)
+    ref = torch.from_numpy(bits.view(np.int16)).view(torch.bfloat16).to(torch.float64).numpy()
+    got = np.array([oracle.bf16_to_double(int(b)) for b in bits])
+    nan = np.isnan(ref)
+    assert np.array_equal(nan, np.isnan(got))
+    assert np.array_equal(ref[~nan], got[~nan])
+
+
+def test_mxfp4_round_trip_is_nearest_representable():
+    rng = np.random.default_rng(11)
+    x = rng.standard_normal((200, 128))
+    packed, e8 = synth.mxfp4_encode(x)
+    for i in range(0, 200, 17):
+        for d in range(128):
+            nib = packed[i, d // 2] & 0xF if d % 2 == 0 else packed[i, d // 2] >> 4
+            v = oracle.e8m0_to_double(int(e8[i, d // 32])) * oracle.e2m1_to_double(int(nib))
+            scale = oracle.e8m0_to_double(int(e8[i, d // 32]))
+            # quantisation error at most half a grid step (largest step 2 x scale), or clamp
+            assert abs(v - x[i, d]) <= scale * 1.0 + 1e-12 or abs(x[i, d]) > 6 * scale
+
+
+# --------------------------------------------------------------- indexer
+def _decode_key_fp8(case, b, t):
+    r = case.block_table[b, t // 64]
+    page = case.pool[r, case.index_off:]
+    codes = page[(t % 64) * 128:(t % 64) * 128 + 128]
+    scale = page[64 * 128 + (t % 64) * 4:64 * 128 + (t % 64) * 4 + 4].view(np.float32)[0]
+    return codes, float(scale)
+
+
+def _e4m3_int(codes):
+    """E4M3 values times 2^9 as exact Python ints (via torch's decoder)."""
+    v = torch.from_numpy(np.asarray(codes, dtype=np.uint8)).view(torch.float8_e4m3fn).to(torch.float64).numpy()
+    return [int(round(x * 512)) for x in v]
+
+
+@pytest.fixture(scope="module")
+def small_case():
+    return synth.make_case("pin", seq_lens=[200, 75], nq=1, topk=16, seed=3, spare_blocks=2)
+
+
+def test_index_scores_exact_integer_dot(small_case):
+    """With w = e_h the score is max(0, scale * q_h.k_t): check it against an
+    exact integer dot product for every head and several tokens."""
+    c = copy.deepcopy(small_case)
+    for h in (0, 7, 31):
+        c.head_w = np.zeros_like(c.head_w)
+        c.head_w[:, h] = 1.0
+        s = oracle.index_scores(c)
+        for b in range(c.batch):
+            qi = _e4m3_int(c.q_index[b, h])
+            for t in (0, 1, 63, 64, int(c.seq_lens[b]) - 1):
+                codes, scale = _decode_key_fp8(c, b, t)
+                dot = Fraction(sum(a * k for a, k in zip(qi, _e4m3_int(codes))), 512 * 512)
+                want = max(Fraction(0), Fraction(scale) * dot)
+                assert s[b, t] == float(want)
+
+
+def test_index_scores_one_hot_closed_form(small_case):
+    c = copy.deepcopy(small_case)
+    h, d = 5, 77
+    c.q_index = np.zeros_like(c.q_index)
+    c.q_index[:, h, d] = 0x38  # E4M3 code of 1.0
+    c.head_w = np.zeros_like(c.head_w)
+    c.head_w[:, h] = -2.0      # a negative weight keeps the ReLU inside the sum
+    s = oracle.index_scores(c)
+    for b in range(c.batch):
+        for t in range(int(c.seq_lens[b])):
+            codes, scale = _decode_key_fp8(c, b, t)
+            kd = _e4m3_int(codes[d:d + 1])[0] / 512.0
+            assert s[b, t] == -2.0 * max(0.0, scale * kd)
+
+
+def test_index_scores_zero_weights_and_head_permutation(small_case):
+    c = copy.deepcopy(small_case)
+    c.head_w = np.zeros_like(c.head_w)
+    s = oracle.index_scores(c)
+    assert np.all(s[0, :200] == 0) and np.all(s[1, :75] == 0)
+    base = oracle.index_scores(small_case)
+    perm = np.random.default_rng(1).permutation(32)
+    c = copy.deepcopy(small_case)
+    c.q_index = c.q_index[:, perm]
+    c.head_w = c.head_w[:, perm]
+    s = oracle.index_scores(c)
+    np.testing.assert_allclose(s[0, :200], base[0, :200], rtol=1e-14, atol=1e-12)
+    # pairing q_h with a different head's weight would change the scores
+    c.head_w = c.head_w[:, ::-1].copy()
+    assert not np.allclose(oracle.index_scores(c)[0, :200], base[0, :200])
+
+
+def test_index_scores_block_table_permutation_invariance():
+    a = synth.make_case("pa", seq_lens=[300, 130], permute_blocks=False, seed=9)
+    b = synth.make_case("pb", seq_lens=[300, 130], permute_blocks=True, seed=9)
+    # same logical contents, different physical rows
+    sa, sb = oracle.index_scores(a), oracle.index_scores(b)
+    assert np.array_equal(sa[0, :300], sb[0, :300]) and np.array_equal(sa[1, :130], sb[1, :130])
+    assert not np.array_equal(a.block_table, b.block_table)
+
+
+def test_index_scores_visibility_and_scale_sign():
+    c = synth.make_case("vis", seq_lens=[100], nq=4, seed=2)
+    s = oracle.index_scores(c)
+    for j in range(4):
+        n = 100 - 3 + j
+        assert np.all(np.isfinite(s[j, :n])) and np.all(np.isnan(s[j, n:]))
+    # scale inside the ReLU: a negative per-token scale flips which heads pass
+    c1 = copy.deepcopy(c)
+    r = c1.block_table[0, 0]
+    off = c1.index_off + 64 * 128
+    sc = c1.pool[r, off:off + 4].view(np.float32).copy()
+    c1.pool[r, off:off + 4] = (-sc).view(np.uint8)
+    s1 = oracle.index_scores(c1)
+    c1.head_w = np.zeros_like(c1.head_w)
+    c1.head_w[:, 3] = 1.0
+    c2 = copy.deepcopy(c1)
+    c2.pool[r, off:off + 4] = sc.view(np.uint8)
+    one_neg, one_pos = oracle.index_scores(c1)[0, 0], oracle.index_scores(c2)[0, 0]
+    assert (one_neg == 0.0) != (one_pos == 0.0) or (one_neg == 0.0 and one_pos == 0.0)
+    assert s1[0, 1] == s[0, 1]  # other tokens unaffected
+
+
+def test_index_scores_mxfp4_exact_rational():
+    c = synth.make_case("mx", seq_lens=[130], key_format=synth.KEY_MXFP4, seed=4)
+    c.head_w = np.zeros_like(c.head_w)
+    c.head_w[:, 9] = 1.0
+    s = oracle.index_scores(c)
+    qi = _e4m3_int(c.q_index[0, 9])
+    for t in (0, 5, 64, 129):
+        r = c.block_table[0, t // 64]
+        page = c.pool[r, c.index_off:]
+        packed = page[(t % 64) * 64:(t % 64) * 64 + 64]
+        e8 = page[64 * 64 + (t % 64) * 4:64 * 64 + (t % 64) * 4 + 4]
+        two_k = []
+        for d in range(128):
+            nib = packed[d // 2] & 0xF if d % 2 == 0 else packed[d // 2] >> 4
+            mag = [0, 1, 2, 3, 4, 6, 8, 12][nib & 7] * (-1 if nib & 8 else 1)  # 2 x E2M1
+            two_k.append(Fraction(mag, 2) * Fraction(2) ** (int(e8[d // 32]) - 127))
+        dot = sum(Fraction(a, 512) * k for a, k in zip(qi, two_k))
+        assert s[0, t] == float(max(Fraction(0), dot))
+
+
+# --------------------------------------------------------------- top-k
+def _is_valid_topk(scores, n, k, out):
+    sel = [int(i) for i in out if i >= 0]
+    assert len(sel) == min(k, n)
+    assert sel == sorted(sel) and len(set(sel)) == len(sel)
+    assert all(i == -1 for i in out[len(sel):])
+
+    def key(t):
+        v = scores[t]
+        return (0 if np.isnan(v) else 1, 0.0 if np.isnan(v) else v, -t)
+
+    rest = set(range(n)) - set(sel)
+    if sel and rest:
+        assert min(key(t) for t in sel) > max(key(t) for t in rest)
+
+
+def test_topk_brute_force_property_with_ties():
+    rng = np.random.default_rng(0)
+    for trial in range(300):
+        n = int(rng.integers(0, 14))
+        k = int(rng.integers(1, 7))
+        vals = rng.choice([-1.0, 0.0, -0.0, 0.5, 2.0, np.nan], size=n)
+        row = np.full((1, 16), 7.0)
+        row[0, :n] = vals
+        out = oracle.topk(row, np.array([n]), k)[0]
+        _is_valid_topk(row[0], n, k, out)
+
+
+def test_topk_special_cases():
+    s = np.zeros((1, 5000))
+    assert list(oracle.topk(s, np.array([5000]), 2048)[0]) == list(range(2048))
+    s = np.random.default_rng(1).standard_normal((1, 100))
+    out = oracle.topk(s, np.array([100]), 128)[0]
+    assert list(out[:100]) == list(range(100)) and np.all(out[100:] == -1)
+    assert np.all(oracle.topk(s, np.array([0]), 4)[0] == -1)
+    s = np.array([[np.nan, -np.inf, -0.0, 0.0, 1.0]])
+    assert list(oracle.topk(s, np.array([5]), 3)[0]) == [2, 3, 4]
+    assert list(oracle.topk(s, np.array([5]), 4)[0]) == [1, 2, 3, 4]
+
+
+def test_topk_matches_python_sort_on_random_rows():
+    rng = np.random.default_rng(2)
+    s = rng.standard_normal((4, 3000)).astype(np.float32).astype(np.float64)
+    s[:, ::7] = s[:, 3:4]  # heavy duplicates around arbitrary values
+    lens = np.array([3000, 2500, 17, 2049])
+    got = oracle.topk(s, lens, 2048)
+    for r in range(4):
+        n = int(lens[r])
+        want = sorted(sorted(range(n), key=lambda t: (-s[r, t], t))[:2048])
+        assert list(got[r, :len(want)]) == want
+        _is_valid_topk(s[r], n, 2048, got[r])
+
+
+# --------------------------------------------------------------- sparse MLA
+def _latent(case, b, t):
+    r = case.block_table[b, t // 64]
+    row = case.pool[r, case.latent_off + (t % 64) * 576:case.latent_off + (t % 64) * 576 + 576]
+    return torch.from_numpy(row.copy()).view(torch.float8_e4m3fn).to(torch.float64).numpy() * case.latent_scale
+
+
+def _q(case, row):
+    return torch.from_numpy(case.q_mla[row].view(np.int16).copy()).view(torch.bfloat16).to(torch.float64).numpy()
+
+
+@pytest.fixture(scope="module")
+def mla_case():
+    return synth.make_case("mla", seq_lens=[300, 90], nq=1, topk=64, seed=6)
+
+
+def test_sparse_mla_matches_library_softmax(mla_case):
+    c = mla_case
+    rng = np.random.default_rng(3)
+    idx = np.full((2, 64), -1, dtype=np.int32)
+    idx[0] = np.sort(rng.choice(300, 64, replace=False))
+    idx[1, :40] = np.sort(rng.choice(90, 40, replace=False))
+    out, lse = oracle.sparse_mla(c, idx)
+    for row in range(2):
+        sel = [t for t in idx[row] if t >= 0]
+        C = torch.from_numpy(np.stack([_latent(c, row, t) for t in sel]))
+        Q = torch.from_numpy(_q(c, row))
+        logits = (Q @ C.T) * c.sm_scale
+        ref = torch.softmax(logits, dim=-1) @ C[:, :512]
+        np.testing.assert_allclose(out[row], ref.numpy(), rtol=1e-10, atol=1e-12)
+        np.testing.assert_allclose(lse[row], torch.logsumexp(logits, dim=-1).numpy(), rtol=1e-12)
+
+
+def test_sparse_mla_closed_forms(mla_case):
+    c = copy.deepcopy(mla_case)
+    idx = np.full((2, 64), -1, dtype=np.int32)
+    idx[0, 0] = 17          # one selected token: O = its value row, LSE = its logit
+    out, lse = oracle.sparse_mla(c, idx)
+    v = _latent(c, 0, 17)
+    q = _q(c, 0)
+    np.testing.assert_array_equal(out[0], np.broadcast_to(v[:512], (96, 512)))
+    np.testing.assert_allclose(lse[0], c.sm_scale * (q @ v), rtol=1e-13,
+                               atol=1e-14 * c.sm_scale * float(np.max(np.abs(q) @ np.abs(v))))
+    assert np.all(out[1] == 0) and np.all(np.isneginf(lse[1]))   # no valid entry
+    c.q_mla = np.zeros_like(c.q_mla)   # q = 0: uniform weights
+    idx[1, :10] = np.arange(10) * 9
+    out, lse = oracle.sparse_mla(c, idx)
+    mean = np.mean([_latent(c, 1, t)[:512] for t in idx[1, :10]], axis=0)
+    np.testing.assert_allclose(out[1], np.broadcast_to(mean, (96, 512)), rtol=1e-12, atol=1e-14)
+    np.testing.assert_allclose(lse[1], math.log(10), rtol=1e-14)
+
+
+def test_sparse_mla_rejects_invisible_token(mla_case):
+    idx = np.full((2, 64), -1, dtype=np.int32)
+    idx[1, 0] = 95  # sequence 1 has 90 tokens
+    with pytest.raises(oracle.OracleError):
+        oracle.sparse_mla(mla_case, idx)
+
+
+def test_decode_step_composes_the_three_stages():
+    c = synth.make_case("step", seq_lens=[700], nq=2, topk=128, seed=8)
+    s, idx, out, lse = oracle.decode_step(c)
+    assert idx.shape == (2, 128)
+    # row 0 sees 699 tokens, row 1 sees 700
+    assert np.isnan(s[0, 699]) and np.isfinite(s[1, 699])
+    for r in range(2):
+        _is_valid_topk(s[r], int(c.row_lens()[r]), 128, idx[r])
+    o2, l2 = oracle.sparse_mla(c, idx)
+    assert np.array_equal(o2, out) and np.array_equal(l2, lse)
