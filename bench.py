@@ -1,0 +1,363 @@
+#!/usr/bin/env python3
+"""DSA decode layer-step benchmark on GB300.
+
+One step = one layer's full decode hot path over one batch: lightning-indexer
+scores -> top-2048 -> exact sparse MLA, i.e. ``dsa_decode_step`` of libdsa.
+Default workload: the long-context batch (32 sequences, context ~ U(64K,
+160K), 10% heavy-tailed keys, FP8 keys and latents, random block table).
+
+Prints ONE JSON line.  ``value`` is the whole-job algorithmic HBM throughput
+(GB/s): the key bytes (132 B/token, once per sequence), the selected
+latents (576 B/token/row), queries and outputs, divided by the step time.
+The inputs exceed L2 and L2 is also flushed (256 MB write) between timed
+steps, outside the per-step CUDA-event pairs.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME]
+  python bench.py --impl reference ...   # the fp64 CPU oracle on a bounded sample
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import threading
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+from dsa_sparse_attention_index_gb300 import roofline, synth  # noqa: E402
+
+METRIC = "DSA decode µs/layer-step & achieved HBM GB/s (fraction of 8 TB/s) at 1 GB300"
+DEFAULT_WORKLOAD = "longctx_b32_l64k-160k"
+NOMINAL_HBM_GBS = 8000.0
+L2_FLUSH_BYTES = 256 << 20
+
+
+def parse():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", default=DEFAULT_WORKLOAD, choices=sorted(synth.WORKLOADS))
+    ap.add_argument("--seed", type=int, default=0)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-e2e", action="store_true")
+    return ap.parse_args()
+
+
+def peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        d = json.load(open(p))
+        return float(d["hbm_gbs"]), "measured"
+    return 6800.0, "fallback"
+
+
+# ---------------------------------------------------------------- clocks
+class ClockSampler:
+    """nvidia-smi sampling of SM clock and throttle reasons while running."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+        self.path = None
+
+    def __enter__(self):
+        try:
+            fd, self.path = tempfile.mkstemp(suffix=".csv")
+            os.close(fd)
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                 "-lms", "100"], stdout=open(self.path, "w"), stderr=subprocess.DEVNULL)
+        except (OSError, FileNotFoundError):
+            self.proc = None
+        return self
+
+    def __exit__(self, *a):
+        if self.proc:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+
+    def summary(self):
+        if not self.path or not os.path.exists(self.path):
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        sm, smax, reasons = [], None, set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in open(self.path):
+            f = [x.strip() for x in line.split(",")]
+            if len(f) < 9:
+                continue
+            try:
+                sm.append(float(f[1]))
+                smax = float(f[2])
+            except ValueError:
+                continue
+            for n, v in zip(names, f[5:9]):
+                if v.lower() == "active":
+                    reasons.add(n)
+        os.unlink(self.path)
+        busy = [s for s in sm if smax and s > 0.5 * smax] or sm
+        return {"sm_mhz": statistics.median(busy) if busy else None, "sm_max_mhz": smax,
+                "samples": len(sm), "reasons": sorted(reasons)}
+
+
+# ---------------------------------------------------------------- CPU baseline
+def cpu_sample(case, n_rows: int):
+    """Sub-case of the workload: its first sequences (all their draft rows)."""
+    import copy
+
+    nseq = max(1, min(case.batch, n_rows // case.nq))
+    sub = copy.copy(case)
+    sub.seq_lens = case.seq_lens[:nseq].copy()
+    sub.batch = nseq
+    sub.block_table = case.block_table[:nseq].copy()
+    r = nseq * case.nq
+    sub.q_index, sub.head_w, sub.q_mla = case.q_index[:r], case.head_w[:r], case.q_mla[:r]
+    return sub
+
+
+def run_oracle(sub):
+    import oracle
+
+    t0 = time.perf_counter()
+    oracle.decode_step(sub)
+    return time.perf_counter() - t0
+
+
+def cpu_baseline(case, max_rows: int = 4):
+    import oracle
+
+    sub = cpu_sample(case, max_rows)
+    dt = run_oracle(sub)
+    b = roofline.step_bytes(sub.seq_lens, sub.nq, sub.topk, sub.key_format)["total"]
+    return {"value": b / dt / 1e9, "unit": "GB/s", "cores": oracle.num_threads(), "kind": "oracle",
+            "sample": f"{sub.batch} of {case.batch} sequences ({sub.rows} query rows, "
+                      f"{int(sub.seq_lens.sum())} context tokens) of the same workload, fp64 C oracle, "
+                      f"{dt:.2f} s"}
+
+
+# ---------------------------------------------------------------- GPU arm
+def main_ours(args):
+    import torch
+    import torch.distributed as dist
+
+    from dsa_sparse_attention_index_gb300 import binding
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        dist.init_process_group("nccl")
+    torch.cuda.set_device(local)
+    binding.lib()  # fail loudly if the CUDA library is missing
+
+    case = synth.workload(args.workload, seed=args.seed)
+    dc = synth.device_case(case)
+    k = case.topk
+    rows = case.rows
+    ld = (case.max_len + 3) // 4 * 4
+    dev = torch.device("cuda", local)
+    out = torch.empty((rows, 96, 512), dtype=torch.int16, device=dev)
+    lse = torch.empty((rows, 96), dtype=torch.float32, device=dev)
+    scores = torch.empty((rows, ld), dtype=torch.float32, device=dev)
+    idx = torch.empty((rows, k), dtype=torch.int32, device=dev)
+    ws = binding.workspace(binding.workspace_size(dc.batch, k), dev)
+    tk_ws = binding.workspace(binding.topk_workspace_size(rows, case.max_len, k), dev)
+    mla_ws = binding.workspace(binding.sparse_mla_workspace_size(rows, k), dev)
+    status = torch.zeros(1, dtype=torch.int32, device=dev)
+    flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
+    stream = torch.cuda.current_stream()
+
+    def step():
+        binding.decode_step(dc.cache, dc.batch, dc.q_index, dc.head_w, dc.q_mla, k, case.sm_scale, out, lse, ws,
+                            status, stream=stream)
+
+    def barrier():
+        if world > 1:
+            dist.barrier()
+        torch.cuda.synchronize()
+
+    for _ in range(args.warmup):
+        flush.zero_()
+        step()
+    barrier()
+    assert status.item() == 0, binding.status_string(status.item())
+
+    # ---- headline: K fused steps, each bracketed by its own events, L2 flushed in between
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
+    with ClockSampler(local) as clk:
+        barrier()
+        t_wall = time.perf_counter()
+        for e0, e1 in ev:
+            flush.zero_()
+            e0.record(stream)
+            step()
+            e1.record(stream)
+        barrier()
+        t_wall = time.perf_counter() - t_wall
+    clocks = clk.summary()
+    step_ms = [e0.elapsed_time(e1) for e0, e1 in ev]
+    ms = statistics.mean(step_ms)
+    if world > 1:
+        t = torch.tensor([ms], device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        ms = float(t.item())
+    assert status.item() == 0, binding.status_string(status.item())
+
+    # ---- per-stage attribution (same kernels through the three stage entry points)
+    stage = {"index": [], "topk": [], "mla": []}
+    for _ in range(max(3, args.steps // 2)):
+        flush.zero_()
+        e = [torch.cuda.Event(enable_timing=True) for _ in range(4)]
+        e[0].record(stream)
+        binding.index_scores(dc.cache, dc.batch, dc.q_index, dc.head_w, scores, status, stream)
+        e[1].record(stream)
+        binding.topk(scores, dc.row_lens, case.max_len, k, idx, tk_ws, status, stream)
+        e[2].record(stream)
+        binding.sparse_mla_decode(dc.cache, dc.batch, dc.q_mla, idx, case.sm_scale, out, lse, mla_ws, status, stream)
+        e[3].record(stream)
+        torch.cuda.synchronize()
+        stage["index"].append(e[0].elapsed_time(e[1]))
+        stage["topk"].append(e[1].elapsed_time(e[2]))
+        stage["mla"].append(e[2].elapsed_time(e[3]))
+    assert status.item() == 0, binding.status_string(status.item())
+    st_ms = {kk: statistics.mean(v) for kk, v in stage.items()}
+
+    # ---- end to end through the public call, host buffers, copies inside the timed region
+    e2e_ms = []
+    if not args.no_e2e:
+        pin = lambda t: t.cpu().pin_memory()
+        h_in = [pin(dc.q_index), pin(dc.head_w), pin(dc.q_mla), pin(dc.batch.block_table), pin(dc.batch.seq_lens)]
+        d_in = [dc.q_index, dc.head_w, dc.q_mla, dc.batch.block_table, dc.batch.seq_lens]
+        h_out = [torch.empty_like(out, device="cpu").pin_memory(), torch.empty_like(lse, device="cpu").pin_memory()]
+        bi = sum(t.numel() * t.element_size() for t in h_in)
+        bo = sum(t.numel() * t.element_size() for t in h_out)
+        e2e_ms = []
+        for it in range(args.warmup + args.steps):
+            flush.zero_()
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record(stream)
+            for h, d in zip(h_in, d_in):
+                d.copy_(h, non_blocking=True)
+            step()
+            h_out[0].copy_(out, non_blocking=True)
+            h_out[1].copy_(lse, non_blocking=True)
+            e1.record(stream)
+            torch.cuda.synchronize()
+            if it >= args.warmup:
+                e2e_ms.append(e0.elapsed_time(e1))
+        e2e_t = statistics.mean(e2e_ms)
+        if world > 1:
+            t = torch.tensor([e2e_t], device=dev)
+            dist.all_reduce(t, op=dist.ReduceOp.MAX)
+            e2e_t = float(t.item())
+
+    b = roofline.step_bytes(case.seq_lens, case.nq, k, case.key_format)
+    total_bytes = b["total"] * world
+    value = total_bytes / (ms * 1e-3) / 1e9
+    peak, peak_kind = peaks()
+    idx_bytes = roofline.indexer_bytes(case.seq_lens, case.nq, case.key_format)
+    idx_gbs = idx_bytes / (st_ms["index"] * 1e-3) / 1e9
+    traffic = load_traffic(args.workload)
+    line = {
+        "metric": METRIC,
+        "value": round(value, 1),
+        "unit": "GB/s",
+        "n_gpus": world,
+        "steps": args.steps,
+        "warmup": args.warmup,
+        "ms_per_step": round(ms, 5),
+        "us_per_layer_step": round(ms * 1e3, 2),
+        "tokens_per_s": round(rows * world / (ms * 1e-3), 1),
+        "frac_of_8TBps": round(value / world / NOMINAL_HBM_GBS, 4),
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "e4m3 x e4m3 -> fp32 (indexer); bf16 x bf16 -> fp32 (MLA)",
+        "data": "synthetic",
+        "config": {
+            "workload": args.workload, "batch": case.batch, "queries_per_seq": case.nq,
+            "seq_len_mean": float(np.mean(case.seq_lens)), "seq_len_min": int(case.seq_lens.min()),
+            "seq_len_max": int(case.seq_lens.max()), "topk": k, "key_bytes": case.token_bytes(),
+            "latent_bytes": 576, "heads": 96, "index_heads": 32, "block": 64,
+            "algorithmic_bytes_per_step": b["total"], "parallelism": f"replicas x{world}",
+            "l2": "inputs > L2 and 256 MB L2 flush between timed steps (outside the step events)",
+        },
+        "stage_us": {kk: round(v * 1e3, 2) for kk, v in st_ms.items()},
+        "roofline": {"kernel": "indexer_fp8_kernel (dsa_index_scores)", "bound": "hbm",
+                     "achieved": round(idx_gbs, 1), "peak": peak, "peak_kind": peak_kind, "unit": "GB/s",
+                     "frac": round(idx_gbs / peak, 4),
+                     "traffic": traffic, "algorithmic_bytes": idx_bytes,
+                     "step_frac": round(value / world / peak, 4)},
+        "gpu_launches": 6 * args.steps,
+        "clocks": clocks,
+        "wall_s_timed_region": round(t_wall, 4),
+    }
+    if e2e_ms:
+        line["e2e"] = {"value": round(total_bytes / (e2e_t * 1e-3) / 1e9, 1), "unit": "GB/s",
+                       "ms_per_step": round(e2e_t, 5), "h2d_bytes_per_step": bi, "d2h_bytes_per_step": bo}
+    if rank == 0 and not args.no_cpu_baseline:
+        line["cpu_baseline"] = cpu_baseline(case)
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        dist.destroy_process_group()
+
+
+def load_traffic(workload):
+    """DRAM bytes per indexer launch from the committed ncu summary, if any."""
+    p = os.path.join(ROOT, "profiles", "indexer_traffic.json")
+    if os.path.exists(p):
+        d = json.load(open(p))
+        return d.get(workload)
+    return None
+
+
+# ---------------------------------------------------------------- reference arm
+def main_reference(args):
+    rank = int(os.environ.get("RANK", "0"))
+    if rank != 0:
+        return
+    import oracle
+
+    case = synth.workload(args.workload, seed=args.seed)
+    sub = cpu_sample(case, 1)
+    for _ in range(min(args.warmup, 1)):
+        run_oracle(sub)
+    times = [run_oracle(sub) for _ in range(args.steps)]
+    dt = statistics.mean(times)
+    b = roofline.step_bytes(sub.seq_lens, sub.nq, sub.topk, sub.key_format)["total"]
+    v = b / dt / 1e9
+    line = {
+        "impl": "reference", "metric": METRIC, "value": round(v, 4), "unit": "GB/s", "n_gpus": args.gpus,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(dt * 1e3, 3),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": args.workload, "sample": f"{sub.batch} sequence(s), {sub.rows} query row(s)"},
+        "cpu_baseline": {"value": round(v, 4), "unit": "GB/s", "cores": oracle.num_threads(), "kind": "oracle",
+                         "sample": f"first {sub.batch} sequence(s) of the workload per step"},
+        "e2e": {"value": round(v, 4), "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+if __name__ == "__main__":
+    a = parse()
+    if a.impl == "reference":
+        main_reference(a)
+    else:
+        main_ours(a)

@@ -1,0 +1,199 @@
+"""ctypes binding of libdsa.so — argument marshalling only.
+
+Every entry point here forwards torch CUDA tensors (as raw device pointers)
+and the current CUDA stream to the C ABI declared in ``include/dsa.h``; all
+arithmetic happens in the library's kernels.  There is no CPU fallback: if
+the library is missing or fails to load, every call raises.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+from dataclasses import dataclass
+
+import torch
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_HERE, "libdsa.so")
+
+OK, ERR_INVALID_ARG, ERR_UNSUPPORTED, ERR_BOUNDS, ERR_TIMEOUT, ERR_CUDA, ERR_WORKSPACE = range(7)
+KEY_FP8_E4M3, KEY_MXFP4 = 0, 1
+BLOCK, IDX_HEADS, IDX_DIM, MLA_HEADS, LATENT, VALUE, MAX_TOPK = 64, 32, 128, 96, 576, 512, 2048
+
+
+class DsaError(RuntimeError):
+    def __init__(self, code: int, what: str):
+        self.code = code
+        super().__init__(f"{what}: {status_string(code)}")
+
+
+class PagedCacheT(ctypes.Structure):
+    _fields_ = [("base", ctypes.c_void_p), ("row_stride", ctypes.c_int64), ("latent_off", ctypes.c_int64),
+                ("index_off", ctypes.c_int64), ("block_size", ctypes.c_int32), ("num_blocks", ctypes.c_int32),
+                ("key_format", ctypes.c_int32), ("latent_scale", ctypes.c_float)]
+
+
+class BatchT(ctypes.Structure):
+    _fields_ = [("block_table", ctypes.c_void_p), ("seq_lens", ctypes.c_void_p),
+                ("max_blocks_per_seq", ctypes.c_int32), ("batch", ctypes.c_int32),
+                ("queries_per_seq", ctypes.c_int32), ("max_seq_len", ctypes.c_int32)]
+
+
+_lib = None
+
+EXPORTS = ["dsa_api_version", "dsa_status_string", "dsa_translate_pages", "dsa_index_scores",
+           "dsa_topk_workspace_size", "dsa_topk", "sparse_mla_workspace_size", "sparse_mla_decode",
+           "dsa_workspace_size", "dsa_decode_step", "dsa_selftest_wait_timeout"]
+
+
+def lib():
+    """Load libdsa.so (raises if it has not been built)."""
+    global _lib
+    if _lib is None:
+        if not os.path.exists(LIB_PATH):
+            raise RuntimeError(f"libdsa.so not found at {LIB_PATH}: build it with "
+                               "dsa_sparse_attention_index_gb300.build.build()")
+        L = ctypes.CDLL(LIB_PATH)
+        P, i32, i64, sz, f32 = ctypes.c_void_p, ctypes.c_int32, ctypes.c_int64, ctypes.c_size_t, ctypes.c_float
+        pc, pb = ctypes.POINTER(PagedCacheT), ctypes.POINTER(BatchT)
+        sig = {
+            "dsa_api_version": (i32, []),
+            "dsa_status_string": (ctypes.c_char_p, [i32]),
+            "dsa_translate_pages": (i32, [pc, pb, P, P, P, P]),
+            "dsa_index_scores": (i32, [pc, pb, P, P, P, i64, P, P]),
+            "dsa_topk_workspace_size": (sz, [i32, i32, i32]),
+            "dsa_topk": (i32, [P, i64, P, i32, i32, i32, P, P, sz, P, P]),
+            "sparse_mla_workspace_size": (sz, [i32, i32]),
+            "sparse_mla_decode": (i32, [pc, pb, P, P, i32, f32, P, P, P, sz, P, P]),
+            "dsa_workspace_size": (sz, [pb, i32]),
+            "dsa_decode_step": (i32, [pc, pb, P, P, P, i32, f32, P, P, P, i64, P, P, sz, P, P]),
+            "dsa_selftest_wait_timeout": (i32, [i64, P, P]),
+        }
+        for name, (res, args) in sig.items():
+            fn = getattr(L, name)
+            fn.restype = res
+            fn.argtypes = args
+        _lib = L
+    return _lib
+
+
+def status_string(code: int) -> str:
+    return lib().dsa_status_string(int(code)).decode()
+
+
+def _check(code: int, what: str) -> None:
+    if code != OK:
+        raise DsaError(code, what)
+
+
+def _ptr(t) -> int | None:
+    if t is None:
+        return None
+    if not t.is_cuda or not t.is_contiguous():
+        raise ValueError("tensors passed to libdsa must be contiguous CUDA tensors")
+    return t.data_ptr()
+
+
+def _stream(stream) -> int | None:
+    s = stream if stream is not None else torch.cuda.current_stream()
+    return s.cuda_stream
+
+
+@dataclass
+class PagedCache:
+    """One layer's packed paged cache: ``pool`` is a uint8 CUDA tensor
+    [num_blocks, row_stride]; offsets locate the latent and index pages."""
+
+    pool: torch.Tensor
+    row_stride: int
+    latent_off: int
+    index_off: int
+    key_format: int
+    latent_scale: float
+
+    def struct(self) -> PagedCacheT:
+        return PagedCacheT(_ptr(self.pool), self.row_stride, self.latent_off, self.index_off, BLOCK,
+                           int(self.pool.shape[0]), self.key_format, float(self.latent_scale))
+
+
+@dataclass
+class Batch:
+    """block_table int32 [batch, max_blocks] and seq_lens int32 [batch] on the GPU."""
+
+    block_table: torch.Tensor
+    seq_lens: torch.Tensor
+    queries_per_seq: int
+    max_seq_len: int
+
+    @property
+    def batch(self) -> int:
+        return int(self.seq_lens.shape[0])
+
+    @property
+    def rows(self) -> int:
+        return self.batch * self.queries_per_seq
+
+    def struct(self) -> BatchT:
+        return BatchT(_ptr(self.block_table), _ptr(self.seq_lens), int(self.block_table.shape[1]), self.batch,
+                      self.queries_per_seq, int(self.max_seq_len))
+
+
+def translate_pages(cache: PagedCache, batch: Batch, latent_pages, index_pages, status, stream=None):
+    c, b = cache.struct(), batch.struct()
+    _check(lib().dsa_translate_pages(ctypes.byref(c), ctypes.byref(b), _ptr(latent_pages), _ptr(index_pages),
+                                     _ptr(status), _stream(stream)), "dsa_translate_pages")
+
+
+def index_scores(cache: PagedCache, batch: Batch, q_index, head_w, scores, status, stream=None):
+    c, b = cache.struct(), batch.struct()
+    _check(lib().dsa_index_scores(ctypes.byref(c), ctypes.byref(b), _ptr(q_index), _ptr(head_w), _ptr(scores),
+                                  int(scores.shape[1]), _ptr(status), _stream(stream)), "dsa_index_scores")
+
+
+def topk_workspace_size(rows: int, max_row_len: int, k: int) -> int:
+    return int(lib().dsa_topk_workspace_size(rows, max_row_len, k))
+
+
+def topk(scores, row_lens, max_row_len: int, k: int, idx_out, workspace, status, stream=None):
+    rows = int(scores.shape[0])
+    _check(lib().dsa_topk(_ptr(scores), int(scores.shape[1]), _ptr(row_lens), rows, int(max_row_len), int(k),
+                          _ptr(idx_out), _ptr(workspace), workspace.numel() * workspace.element_size(),
+                          _ptr(status), _stream(stream)), "dsa_topk")
+
+
+def sparse_mla_workspace_size(rows: int, k: int) -> int:
+    return int(lib().sparse_mla_workspace_size(rows, k))
+
+
+def sparse_mla_decode(cache: PagedCache, batch: Batch, q_mla, idx, sm_scale: float, out, lse, workspace, status,
+                      stream=None):
+    c, b = cache.struct(), batch.struct()
+    _check(lib().sparse_mla_decode(ctypes.byref(c), ctypes.byref(b), _ptr(q_mla), _ptr(idx), int(idx.shape[1]),
+                                   float(sm_scale), _ptr(out), _ptr(lse), _ptr(workspace),
+                                   workspace.numel() * workspace.element_size(), _ptr(status), _stream(stream)),
+           "sparse_mla_decode")
+
+
+def workspace_size(batch: Batch, k: int) -> int:
+    b = batch.struct()
+    return int(lib().dsa_workspace_size(ctypes.byref(b), int(k)))
+
+
+def decode_step(cache: PagedCache, batch: Batch, q_index, head_w, q_mla, k: int, sm_scale: float, out, lse,
+                workspace, status, scores_out=None, idx_out=None, stream=None):
+    c, b = cache.struct(), batch.struct()
+    ld = int(scores_out.shape[1]) if scores_out is not None else 0
+    _check(lib().dsa_decode_step(ctypes.byref(c), ctypes.byref(b), _ptr(q_index), _ptr(head_w), _ptr(q_mla),
+                                 int(k), float(sm_scale), _ptr(out), _ptr(lse), _ptr(scores_out), ld,
+                                 _ptr(idx_out), _ptr(workspace), workspace.numel() * workspace.element_size(),
+                                 _ptr(status), _stream(stream)), "dsa_decode_step")
+
+
+def selftest_wait_timeout(limit_ns: int, status, stream=None):
+    _check(lib().dsa_selftest_wait_timeout(int(limit_ns), _ptr(status), _stream(stream)),
+           "dsa_selftest_wait_timeout")
+
+
+def workspace(nbytes: int, device="cuda") -> torch.Tensor:
+    """A 256-byte aligned uint8 device buffer (torch's allocator aligns to 512 B)."""
+    return torch.empty(max(int(nbytes), 1), dtype=torch.uint8, device=device)

@@ -1,0 +1,230 @@
+// api.cu — the C ABI of libdsa.so: argument validation, workspace layout and
+// the stream-ordered composition of the kernels.  No allocation, no host
+// synchronisation on any entry point.
+#include <algorithm>
+#include <mutex>
+
+#include "common.cuh"
+#include "internal.h"
+
+namespace dsa {
+
+int num_sms() {
+  static int cache[64] = {};
+  int dev = 0;
+  cudaGetDevice(&dev);
+  if (dev >= 0 && dev < 64 && cache[dev]) return cache[dev];
+  int n = 0;
+  if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0) n = 1;
+  if (dev >= 0 && dev < 64) cache[dev] = n;
+  return n;
+}
+
+namespace {
+
+using EncodeTiledFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
+                                   const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
+                                   CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn encode_fn() {
+  static EncodeTiledFn fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* ptr = nullptr;
+    cudaDriverEntryPointQueryResult q = cudaDriverEntryPointSymbolNotFound;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<EncodeTiledFn>(ptr);
+  });
+  return fn;
+}
+
+inline bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) & (a - 1)) == 0; }
+inline size_t al256(size_t x) { return (x + 255) & ~size_t(255); }
+
+int index_page_bytes(int key_format) {
+  return key_format == DSA_KEY_FP8_E4M3 ? kBlock * (kIdxDim + 4) : kBlock * (kIdxDim / 2 + 4);
+}
+
+dsa_status_t check_cache(const dsa_paged_cache_t* c) {
+  if (!c || !c->base || !aligned(c->base, 128)) return DSA_ERR_INVALID_ARG;
+  if (c->block_size != kBlock) return DSA_ERR_UNSUPPORTED;
+  if (c->key_format != DSA_KEY_FP8_E4M3 && c->key_format != DSA_KEY_MXFP4) return DSA_ERR_INVALID_ARG;
+  if (c->num_blocks <= 0 || c->row_stride <= 0 || (c->row_stride % 128) || (c->latent_off % 128) ||
+      (c->index_off % 128) || c->latent_off < 0 || c->index_off < 0)
+    return DSA_ERR_INVALID_ARG;
+  if (c->latent_off + kBlock * kLatent > c->row_stride) return DSA_ERR_INVALID_ARG;
+  if (c->index_off + index_page_bytes(c->key_format) > c->row_stride) return DSA_ERR_INVALID_ARG;
+  return DSA_OK;
+}
+
+dsa_status_t check_batch(const dsa_batch_t* b) {
+  if (!b || b->batch < 0 || b->max_seq_len < 0 || b->max_blocks_per_seq < 1) return DSA_ERR_INVALID_ARG;
+  if (b->queries_per_seq < 1 || b->queries_per_seq > DSA_MAX_QUERIES_PER_SEQ) return DSA_ERR_UNSUPPORTED;
+  if (b->batch > 0 && (!b->block_table || !b->seq_lens)) return DSA_ERR_INVALID_ARG;
+  if ((int64_t)b->batch * b->queries_per_seq > (1 << 24)) return DSA_ERR_UNSUPPORTED;
+  return DSA_OK;
+}
+
+int64_t round_ld(int max_len) { return ((int64_t)std::max(max_len, 1) + 3) & ~int64_t(3); }
+
+}  // namespace
+
+bool encode_tmap(CUtensorMap* map, CUtensorMapDataType dtype, int rank, const void* base, const uint64_t* dims,
+                 const uint64_t* strides, const uint32_t* box, CUtensorMapSwizzle swizzle) {
+  EncodeTiledFn fn = encode_fn();
+  if (!fn) return false;
+  cuuint64_t d[5], s[4];
+  cuuint32_t bx[5], es[5];
+  for (int i = 0; i < rank; ++i) {
+    d[i] = dims[i];
+    bx[i] = box[i];
+    es[i] = 1;
+  }
+  for (int i = 0; i + 1 < rank; ++i) s[i] = strides[i];
+  return fn(map, dtype, (cuuint32_t)rank, const_cast<void*>(base), d, s, bx, es, CU_TENSOR_MAP_INTERLEAVE_NONE,
+            swizzle, CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+}  // namespace dsa
+
+using namespace dsa;
+
+extern "C" {
+
+int32_t dsa_api_version(void) { return DSA_API_VERSION; }
+
+const char* dsa_status_string(int32_t s) {
+  switch (s) {
+    case DSA_OK: return "DSA_OK";
+    case DSA_ERR_INVALID_ARG: return "DSA_ERR_INVALID_ARG: NULL pointer, bad size or misaligned buffer";
+    case DSA_ERR_UNSUPPORTED: return "DSA_ERR_UNSUPPORTED: valid request not handled by this build";
+    case DSA_ERR_BOUNDS: return "DSA_ERR_BOUNDS: block-table entry or token index outside the cache";
+    case DSA_ERR_TIMEOUT: return "DSA_ERR_TIMEOUT: an in-kernel wait ran out";
+    case DSA_ERR_CUDA: return "DSA_ERR_CUDA: CUDA launch or runtime error";
+    case DSA_ERR_WORKSPACE: return "DSA_ERR_WORKSPACE: workspace missing or too small";
+    default: return "unknown dsa status";
+  }
+}
+
+dsa_status_t dsa_translate_pages(const dsa_paged_cache_t* cache, const dsa_batch_t* batch, int64_t* latent_pages,
+                                 int64_t* index_pages, int32_t* dev_status, void* stream) {
+  dsa_status_t s;
+  if ((s = check_cache(cache)) != DSA_OK) return s;
+  if ((s = check_batch(batch)) != DSA_OK) return s;
+  if (!dev_status) return DSA_ERR_INVALID_ARG;
+  return launch_translate_pages(*cache, *batch, latent_pages, index_pages, dev_status,
+                                static_cast<cudaStream_t>(stream));
+}
+
+dsa_status_t dsa_index_scores(const dsa_paged_cache_t* cache, const dsa_batch_t* batch, const uint8_t* q_index,
+                              const float* head_w, float* scores, int64_t ld_scores, int32_t* dev_status,
+                              void* stream) {
+  dsa_status_t s;
+  if ((s = check_cache(cache)) != DSA_OK) return s;
+  if ((s = check_batch(batch)) != DSA_OK) return s;
+  if (!dev_status) return DSA_ERR_INVALID_ARG;
+  if (batch->batch == 0) return DSA_OK;
+  if (!q_index || !head_w || !scores || !aligned(q_index, 16) || !aligned(head_w, 16) || !aligned(scores, 16))
+    return DSA_ERR_INVALID_ARG;
+  if (ld_scores < batch->max_seq_len || (ld_scores % 4)) return DSA_ERR_INVALID_ARG;
+  if (cache->key_format != DSA_KEY_FP8_E4M3) return DSA_ERR_UNSUPPORTED;
+  return launch_index_scores_fp8(*cache, *batch, q_index, head_w, scores, ld_scores, dev_status,
+                                 static_cast<cudaStream_t>(stream));
+}
+
+size_t dsa_topk_workspace_size(int32_t rows, int32_t max_row_len, int32_t k) {
+  if (rows < 0 || k < 1 || k > DSA_MAX_TOPK) return 0;
+  return topk_workspace_bytes(rows, max_row_len, k);
+}
+
+dsa_status_t dsa_topk(const float* scores, int64_t ld_scores, const int32_t* row_lens, int32_t rows,
+                      int32_t max_row_len, int32_t k, int32_t* idx_out, void* workspace, size_t workspace_bytes,
+                      int32_t* dev_status, void* stream) {
+  if (rows < 0 || k < 1 || k > DSA_MAX_TOPK || max_row_len < 0 || !dev_status) return DSA_ERR_INVALID_ARG;
+  if (rows == 0) return DSA_OK;
+  if (!scores || !row_lens || !idx_out || !aligned(scores, 16) || ld_scores < max_row_len || (ld_scores % 4))
+    return DSA_ERR_INVALID_ARG;
+  if (!workspace || !aligned(workspace, 256) || workspace_bytes < topk_workspace_bytes(rows, max_row_len, k))
+    return DSA_ERR_WORKSPACE;
+  return launch_topk(scores, ld_scores, row_lens, nullptr, 1, rows, max_row_len, k, idx_out, workspace, dev_status,
+                     static_cast<cudaStream_t>(stream));
+}
+
+size_t sparse_mla_workspace_size(int32_t rows, int32_t k) {
+  if (rows < 0 || k < 1 || k > DSA_MAX_TOPK) return 0;
+  return mla_workspace_bytes(rows, k);
+}
+
+dsa_status_t sparse_mla_decode(const dsa_paged_cache_t* cache, const dsa_batch_t* batch, const uint16_t* q_mla,
+                               const int32_t* idx, int32_t k, float sm_scale, uint16_t* out, float* lse,
+                               void* workspace, size_t workspace_bytes, int32_t* dev_status, void* stream) {
+  dsa_status_t s;
+  if ((s = check_cache(cache)) != DSA_OK) return s;
+  if ((s = check_batch(batch)) != DSA_OK) return s;
+  if (k < 1 || k > DSA_MAX_TOPK || !dev_status) return DSA_ERR_INVALID_ARG;
+  const int rows = batch->batch * batch->queries_per_seq;
+  if (rows == 0) return DSA_OK;
+  if (!q_mla || !idx || !out || !lse || !aligned(q_mla, 16) || !aligned(out, 4)) return DSA_ERR_INVALID_ARG;
+  if (!workspace || !aligned(workspace, 256) || workspace_bytes < mla_workspace_bytes(rows, k))
+    return DSA_ERR_WORKSPACE;
+  return launch_sparse_mla(*cache, *batch, q_mla, idx, k, sm_scale, out, lse, workspace, dev_status,
+                           static_cast<cudaStream_t>(stream));
+}
+
+size_t dsa_workspace_size(const dsa_batch_t* batch, int32_t k) {
+  if (!batch || batch->batch < 0 || k < 1 || k > DSA_MAX_TOPK) return 0;
+  const int rows = batch->batch * std::max(1, batch->queries_per_seq);
+  return al256((size_t)rows * round_ld(batch->max_seq_len) * 4) + al256((size_t)rows * k * 4) +
+         al256(topk_workspace_bytes(rows, batch->max_seq_len, k)) + al256(mla_workspace_bytes(rows, k));
+}
+
+dsa_status_t dsa_decode_step(const dsa_paged_cache_t* cache, const dsa_batch_t* batch, const uint8_t* q_index,
+                             const float* head_w, const uint16_t* q_mla, int32_t k, float sm_scale, uint16_t* out,
+                             float* lse, float* scores_out, int64_t ld_scores, int32_t* idx_out, void* workspace,
+                             size_t workspace_bytes, int32_t* dev_status, void* stream) {
+  dsa_status_t s;
+  if ((s = check_cache(cache)) != DSA_OK) return s;
+  if ((s = check_batch(batch)) != DSA_OK) return s;
+  if (k < 1 || k > DSA_MAX_TOPK || !dev_status) return DSA_ERR_INVALID_ARG;
+  const int rows = batch->batch * batch->queries_per_seq;
+  if (rows == 0) return DSA_OK;
+  if (!q_index || !head_w || !q_mla || !out || !lse) return DSA_ERR_INVALID_ARG;
+  if (!aligned(q_index, 16) || !aligned(head_w, 16) || !aligned(q_mla, 16) || !aligned(out, 4))
+    return DSA_ERR_INVALID_ARG;
+  if (!workspace || !aligned(workspace, 256) || workspace_bytes < dsa_workspace_size(batch, k))
+    return DSA_ERR_WORKSPACE;
+  if (cache->key_format != DSA_KEY_FP8_E4M3) return DSA_ERR_UNSUPPORTED;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  uint8_t* w = static_cast<uint8_t*>(workspace);
+  float* scores = scores_out;
+  int64_t ld = ld_scores;
+  const size_t scores_bytes = al256((size_t)rows * round_ld(batch->max_seq_len) * 4);
+  if (!scores) {
+    scores = reinterpret_cast<float*>(w);
+    ld = round_ld(batch->max_seq_len);
+  } else if (!aligned(scores, 16) || ld < batch->max_seq_len || (ld % 4)) {
+    return DSA_ERR_INVALID_ARG;
+  }
+  w += scores_bytes;
+  int32_t* idx = idx_out ? idx_out : reinterpret_cast<int32_t*>(w);
+  w += al256((size_t)rows * k * 4);
+  void* topk_ws = w;
+  w += al256(topk_workspace_bytes(rows, batch->max_seq_len, k));
+  void* mla_ws = w;
+
+  if ((s = launch_index_scores_fp8(*cache, *batch, q_index, head_w, scores, ld, dev_status, st)) != DSA_OK) return s;
+  const int cap = std::min(batch->max_blocks_per_seq * kBlock, batch->max_seq_len);
+  if ((s = launch_topk(scores, ld, nullptr, batch->seq_lens, batch->queries_per_seq, rows, cap, k, idx, topk_ws,
+                       dev_status, st)) != DSA_OK)
+    return s;
+  return launch_sparse_mla(*cache, *batch, q_mla, idx, k, sm_scale, out, lse, mla_ws, dev_status, st);
+}
+
+dsa_status_t dsa_selftest_wait_timeout(int64_t limit_ns, int32_t* dev_status, void* stream) {
+  if (!dev_status) return DSA_ERR_INVALID_ARG;
+  return launch_wait_selftest(limit_ns, dev_status, static_cast<cudaStream_t>(stream));
+}
+
+}  // extern "C"

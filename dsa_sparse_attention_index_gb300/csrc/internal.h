@@ -1,0 +1,36 @@
+// internal.h — launchers and host helpers shared by the library's .cu files.
+#pragma once
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <stddef.h>
+#include <stdint.h>
+
+#include "../../include/dsa.h"
+
+namespace dsa {
+
+// Streaming multiprocessors of the current device (cached per device).
+int num_sms();
+
+// cuTensorMapEncodeTiled through the runtime's driver entry point (no libcuda
+// link dependency).  strides: rank-1 byte strides of dims 1..rank-1.
+bool encode_tmap(CUtensorMap* map, CUtensorMapDataType dtype, int rank, const void* base, const uint64_t* dims,
+                 const uint64_t* strides, const uint32_t* box, CUtensorMapSwizzle swizzle);
+
+dsa_status_t launch_translate_pages(const dsa_paged_cache_t& c, const dsa_batch_t& bt, int64_t* latent_pages,
+                                    int64_t* index_pages, int32_t* status, cudaStream_t st);
+dsa_status_t launch_index_scores_fp8(const dsa_paged_cache_t& c, const dsa_batch_t& bt, const uint8_t* q_index,
+                                     const float* head_w, float* scores, int64_t ld, int32_t* status,
+                                     cudaStream_t st);
+size_t topk_workspace_bytes(int rows, int max_row_len, int k);
+dsa_status_t launch_topk(const float* scores, int64_t ld, const int32_t* row_lens, const int32_t* seq_lens, int nq,
+                         int rows, int max_row_len, int k, int32_t* out, void* workspace, int32_t* status,
+                         cudaStream_t st);
+size_t mla_workspace_bytes(int rows, int k);
+dsa_status_t launch_sparse_mla(const dsa_paged_cache_t& c, const dsa_batch_t& bt, const uint16_t* q_mla,
+                               const int32_t* idx, int k, float sm_scale, uint16_t* out, float* lse,
+                               void* workspace, int32_t* status, cudaStream_t st);
+dsa_status_t launch_wait_selftest(int64_t limit_ns, int32_t* status, cudaStream_t st);
+
+}  // namespace dsa

@@ -1,0 +1,487 @@
+// sparse_mla.cu — exact sparse MLA decode over the selected tokens (stage 3).
+//
+// For every query row and each of the 96 heads: logits over the selected
+// tokens' 576-wide latents (absorbed MLA, keys = all 576 columns, values =
+// the first 512), an exact softmax, and the weighted sum of values, plus the
+// log-sum-exp (vLLM Day-0 post for Kimi K3.1 Pro, sparse-attention section:
+// "MLA attention then runs exactly, but only on these 2,048 tokens"; the
+// prefill section gives the 96 heads).  The selected rows are read straight
+// from the packed paged cache through the block table.
+//
+// GB300 design (one CTA per (query row, token chunk), 13 warps):
+//   * Q [96 x 576] bf16 is loaded once by TMA into shared memory (108 KB,
+//     128-byte swizzle, K-major) and is the A operand of S = Q K^T with the
+//     heads on the MMA's M = 128 rows (rows 96..127 are ignored).
+//   * warps 4..11 gather 32 latent rows per tile (16-byte loads, prefetched a
+//     tile ahead), widen E4M3 -> bf16 exactly in registers and store the tile
+//     once, 128-byte swizzled.  That single tile is the B operand of QK^T
+//     (K-major, N = 32 tokens) and the A operand of P V (MN-major, M = 128
+//     value dims), so V needs no second copy.
+//   * warp 12 issues tcgen05.mma (kind::f16, fp32 accumulation): S into a
+//     double-buffered 32-column TMEM tile, O^T = V^T P^T into 4 x 96 TMEM
+//     columns (dims on lanes, heads on columns: 384 + 2*32 <= 512 columns).
+//     QK of tile i+1 is issued before PV of tile i so the softmax overlaps
+//     the tensor core.
+//   * warps 0..3 (one thread per head) run the online softmax on the S row
+//     in registers (exp2 with the scale folded in), write P as bf16 (64-byte
+//     swizzled rows, the K-major B operand of PV), and rescale O^T only when
+//     a head's running maximum grows by more than 2^8 (exact either way: the
+//     final normalisation uses the same reference maximum).
+//   * Partial (unnormalised O, max, sums) per chunk go to the workspace and
+//     a combine kernel merges the chunks through their log-sum-exp (Day-0
+//     post, DCP section: partial outputs are combined by LSE).
+#include <algorithm>
+#include <cmath>
+
+#include "common.cuh"
+#include "internal.h"
+
+namespace dsa {
+
+namespace {
+
+constexpr int kTileTok = 32;
+constexpr int kDBlocks = kLatent / 64;                 // 9 blocks of 64 dims (128 B of bf16)
+constexpr int kQBlockBytes = kHeads * 128;             // 12,288
+constexpr int kQBytes = kDBlocks * kQBlockBytes;       // 110,592
+constexpr int kTileDBlockBytes = kTileTok * 128;       // 4,096
+constexpr int kTileBytes = kDBlocks * kTileDBlockBytes;  // 36,864
+constexpr int kPBytes = kHeads * kTileTok * 2;         // 6,144
+constexpr int kMaxChunk = 2048;
+constexpr int kThreads = 13 * 32;
+constexpr int kLoaderThreads = 256;
+constexpr int kOCols = 4 * kHeads;                     // 384 TMEM columns of O^T
+constexpr int kSCol = kOCols;                          // S buffers at 384 and 416
+constexpr int kTmemCols = 512;
+constexpr float kRescaleThreshold = 8.0f;              // log2 units
+
+constexpr int kOffQ = 0;
+constexpr int kOffTile = kOffQ + kQBytes;                   // 110,592
+constexpr int kOffP = kOffTile + 2 * kTileBytes;             // 184,320
+constexpr int kOffAlpha = kOffP + 2 * kPBytes;               // 196,608
+constexpr int kOffBars = kOffAlpha + 128 * 4;                // 197,120
+constexpr int kNumBars = 10;
+constexpr int kOffMisc = kOffBars + kNumBars * 8;
+constexpr int kOffTokOff = kOffMisc + 16;                    // int64 per token of the chunk
+constexpr size_t kSmemBytes = 1024 + kOffTokOff + 8 * (size_t)kMaxChunk;
+
+struct MlaParams {
+  const uint8_t* latent_base;  // cache base + latent_off
+  int64_t row_stride;
+  int32_t num_blocks;
+  const int32_t* block_table;
+  int32_t max_blocks;
+  const int32_t* seq_lens;
+  int32_t nq;
+  int32_t cap;
+  const int32_t* idx;
+  int32_t k;
+  int32_t chunk;    // tokens per CTA (multiple of 32)
+  int32_t nsplit;
+  float logit_scale_log2;  // sm_scale * latent_scale * log2(e)
+  float* opart;     // [rows][nsplit][96][512]
+  float* ml;        // [rows][nsplit][96][4]: max (log2), sum of bf16(p), sum of p
+  int32_t* status;
+};
+
+__device__ __forceinline__ bool bar_or_softmax(bool v) {
+  uint32_t r;
+  asm volatile(
+      "{\n .reg .pred p, q;\n setp.ne.u32 q, %1, 0;\n bar.red.or.pred p, 1, 128, q;\n selp.u32 %0, 1, 0, p;\n}\n"
+      : "=r"(r)
+      : "r"((uint32_t)v)
+      : "memory");
+  return r != 0;
+}
+
+__global__ void __launch_bounds__(kThreads, 1)
+    sparse_mla_kernel(const __grid_constant__ CUtensorMap tmap_q, const MlaParams p) {
+  // S = Q K^T: A = Q (K-major), B = latent tile (K-major); M = 128, N = 32.
+  constexpr uint32_t kIdescQK = make_idesc(kFmtBF16, kFmtBF16, 0, 0, 128, kTileTok);
+  // O^T = V^T P^T: A = latent tile (MN-major, M = dims), B = P (K-major); M = 128, N = 96.
+  constexpr uint32_t kIdescPV = make_idesc(kFmtBF16, kFmtBF16, 1, 0, 128, kHeads);
+
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  const uint32_t sbase = smem_u32(smem);
+  const uint32_t bars = sbase + kOffBars;
+  const uint32_t q_full = bars;
+  auto tile_full = [&](int b) { return bars + 8u * (1 + b); };
+  auto tile_empty = [&](int b) { return bars + 8u * (3 + b); };
+  auto s_full = [&](int b) { return bars + 8u * (5 + b); };
+  auto p_full = [&](int b) { return bars + 8u * (7 + b); };
+  const uint32_t pv_done = bars + 8u * 9;
+  // the MMA issuer's teardown barrier reuses q_full's slot after Q has landed
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + kOffMisc);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + kOffMisc + 4);
+  int64_t* tok_off = reinterpret_cast<int64_t*>(smem + kOffTokOff);
+  float* alpha_s = reinterpret_cast<float*>(smem + kOffAlpha);
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int row = blockIdx.y, split = blockIdx.x;
+  const int b_seq = row / p.nq;
+  const int vis = [&] {
+    int len = p.seq_lens[b_seq];
+    len = len < 0 ? 0 : (len > p.cap ? p.cap : len);
+    return visible_len(len, p.nq, row % p.nq);
+  }();
+  const int c0 = split * p.chunk;
+  const int count = max(0, min(p.chunk, p.k - c0));
+  const int ntiles = (count + kTileTok - 1) / kTileTok;
+
+  if (threadIdx.x == 0) {
+    mbar_init(q_full, 1);
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(tile_full(b), kLoaderThreads / 32);
+      mbar_init(tile_empty(b), 1);
+      mbar_init(s_full(b), 1);
+      mbar_init(p_full(b), 4);
+    }
+    mbar_init(pv_done, 1);
+    *abort_flag = 0;
+    fence_mbar_init();
+    prefetch_tmap(&tmap_q);
+  }
+  if (warp == 12) {
+    tmem_alloc(smem_u32(tmem_slot), kTmemCols);
+    tmem_relinquish();
+  }
+  // byte offsets of the chunk's latent rows (-1: masked: -1 index or padding)
+  for (int i = threadIdx.x; i < ntiles * kTileTok; i += kThreads) {
+    int64_t off = -1;
+    if (i < count) {
+      const int t = p.idx[(int64_t)row * p.k + c0 + i];
+      if (t >= 0) {
+        const int r = (t < vis) ? p.block_table[(int64_t)b_seq * p.max_blocks + t / kBlock] : -1;
+        if (r >= 0 && r < p.num_blocks)
+          off = (int64_t)r * p.row_stride + (int64_t)(t % kBlock) * kLatent;
+        else
+          report(p.status, DSA_ERR_BOUNDS);
+      }
+    }
+    tok_off[i] = off;
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+
+  if (ntiles > 0) {
+    if (warp == 12) {
+      if (lane == 0) {
+        // ------------------------------------------------ Q load + MMA issuer
+        mbar_arrive_expect_tx(q_full, kQBytes);
+        for (int kb = 0; kb < kDBlocks; ++kb)
+          tma_load_2d(sbase + kOffQ + kb * kQBlockBytes, &tmap_q, kb * 64, row * kHeads, q_full);
+        bool ok = mbar_wait(q_full, 0, abort_flag, p.status);
+        auto issue_qk = [&](int i) {
+          const int b = i & 1;
+          const uint32_t tile = sbase + kOffTile + b * kTileBytes;
+          for (int kb = 0; kb < kDBlocks; ++kb) {
+#pragma unroll
+            for (int kk = 0; kk < 4; ++kk) {
+              const uint64_t ad = smem_desc(sbase + kOffQ + kb * kQBlockBytes + 32 * kk, 16, 1024, kLayoutSw128);
+              const uint64_t bd = smem_desc(tile + kb * kTileDBlockBytes + 32 * kk, 16, 1024, kLayoutSw128);
+              mma_bf16(tmem + kSCol + kTileTok * b, ad, bd, kIdescQK, (kb | kk) ? 1u : 0u);
+            }
+          }
+          mma_commit(s_full(b));
+        };
+        if (ok) ok = mbar_wait(tile_full(0), 0, abort_flag, p.status);
+        if (ok) {
+          tc_fence_after();
+          issue_qk(0);
+        }
+        for (int i = 0; ok && i < ntiles; ++i) {
+          if (i + 1 < ntiles) {
+            if (!mbar_wait(tile_full((i + 1) & 1), ((i + 1) >> 1) & 1, abort_flag, p.status)) break;
+            tc_fence_after();
+            issue_qk(i + 1);
+          }
+          const int b = i & 1;
+          if (!mbar_wait(p_full(b), (i >> 1) & 1, abort_flag, p.status)) break;
+          tc_fence_after();
+          const uint32_t tile = sbase + kOffTile + b * kTileBytes;
+          const uint32_t pt = sbase + kOffP + b * kPBytes;
+#pragma unroll
+          for (int mb = 0; mb < 4; ++mb) {
+#pragma unroll
+            for (int ks = 0; ks < kTileTok / 16; ++ks) {
+              // A: dims [128 mb, +128) = two 64-dim atoms (LBO apart), tokens [16 ks, +16) = two 8-row groups
+              const uint64_t ad = smem_desc(tile + 2 * mb * kTileDBlockBytes + 2 * ks * 1024, kTileDBlockBytes,
+                                            1024, kLayoutSw128);
+              const uint64_t bd = smem_desc(pt + 32 * ks, 16, 512, kLayoutSw64);
+              mma_bf16(tmem + mb * kHeads, ad, bd, kIdescPV, (i > 0 || ks > 0) ? 1u : 0u);
+            }
+          }
+          mma_commit(tile_empty(b));
+          mma_commit(pv_done);
+        }
+        // wait for every issued MMA before TMEM is released (q_full is free by now)
+        mma_commit(q_full);
+        mbar_wait(q_full, 1, abort_flag, nullptr, 10000000ull);
+      }
+    } else if (warp >= 4) {
+      // ------------------------------------------------ gather + E4M3 -> bf16
+      const int lt = threadIdx.x - 128;       // 0..255
+      const int tok = lt >> 3;                // token row of the tile, 0..31
+      const int g = lt & 7;                   // chunk group: 16-byte chunks g, g+8, ..., < 36
+      const int nch = g < 4 ? 5 : 4;
+      uint4 bufA[5], bufB[5];
+      auto load = [&](int i, uint4 (&buf)[5]) {
+        const int64_t off = tok_off[i * kTileTok + tok];
+#pragma unroll
+        for (int c = 0; c < 5; ++c) {
+          buf[c] = make_uint4(0, 0, 0, 0);
+          if (c < nch && off >= 0)
+            buf[c] = __ldg(reinterpret_cast<const uint4*>(p.latent_base + off) + (g + 8 * c));
+        }
+      };
+      auto store = [&](int i, const uint4 (&buf)[5]) -> bool {
+        const int b = i & 1;
+        const bool ok = mbar_wait(tile_empty(b), ((i >> 1) & 1) ^ 1, abort_flag, p.status);
+        if (!__all_sync(0xffffffffu, ok)) return false;
+        uint8_t* tile = smem + kOffTile + b * kTileBytes;
+#pragma unroll
+        for (int c = 0; c < 5; ++c) {
+          if (c < nch) {
+            const int ch = g + 8 * c;          // 16-byte chunk of the 576-byte row: dims [16 ch, +16)
+            const int dblk = ch >> 2;
+            const uint32_t inner = (uint32_t)((ch & 3) * 32);
+            const uint32_t w[4] = {buf[c].x, buf[c].y, buf[c].z, buf[c].w};
+            uint32_t o[8];
+#pragma unroll
+            for (int q = 0; q < 4; ++q) {
+              o[2 * q] = e4m3x2_to_bf16x2((uint16_t)(w[q] & 0xFFFF));
+              o[2 * q + 1] = e4m3x2_to_bf16x2((uint16_t)(w[q] >> 16));
+            }
+            uint8_t* blk = tile + dblk * kTileDBlockBytes;
+            *reinterpret_cast<uint4*>(blk + swz128(tok * 128 + inner)) = make_uint4(o[0], o[1], o[2], o[3]);
+            *reinterpret_cast<uint4*>(blk + swz128(tok * 128 + inner + 16)) = make_uint4(o[4], o[5], o[6], o[7]);
+          }
+        }
+        fence_proxy_async_smem();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(tile_full(b));
+        return true;
+      };
+      load(0, bufA);
+      for (int i = 0; i < ntiles; i += 2) {
+        if (i + 1 < ntiles) load(i + 1, bufB);
+        if (!store(i, bufA)) break;
+        if (i + 2 < ntiles) load(i + 2, bufA);
+        if (i + 1 < ntiles && !store(i + 1, bufB)) break;
+      }
+    } else {
+      // ------------------------------------------------ softmax (thread = head)
+      const int h = threadIdx.x;  // TMEM lane
+      const bool live = h < kHeads;
+      float m_used = -INFINITY, l_round = 0.f, l_exact = 0.f;
+      bool ok = true;
+      for (int i = 0; i < ntiles; ++i) {
+        const int b = i & 1;
+        ok = mbar_wait(s_full(b), (i >> 1) & 1, abort_flag, p.status);
+        if (bar_or_softmax(!ok)) { ok = false; break; }   // uniform over the 128 softmax threads
+        tc_fence_after();
+        uint32_t r[32];
+        tmem_ld32(tmem + ((uint32_t)(warp * 32) << 16) + kSCol + kTileTok * b, r);
+        tmem_ld_wait();
+        float x[32];
+        float m_tile = -INFINITY;
+#pragma unroll
+        for (int j = 0; j < 32; ++j) {
+          const bool valid = tok_off[i * kTileTok + j] >= 0;
+          x[j] = valid ? __uint_as_float(r[j]) * p.logit_scale_log2 : -INFINITY;
+          m_tile = fmaxf(m_tile, x[j]);
+        }
+        const bool grow = live && m_tile > m_used + kRescaleThreshold;
+        if (bar_or_softmax(grow)) {
+          const float m_new = grow ? m_tile : m_used;
+          const float alpha = (m_used == -INFINITY) ? 0.f : exp2f(m_used - m_new);
+          if (live) alpha_s[h] = alpha;
+          l_round *= alpha;
+          l_exact *= alpha;
+          m_used = m_new;
+          if (i > 0) {
+            // O^T holds tiles 0..i-1: wait for the last PV, then scale column h by alpha[h]
+            ok = mbar_wait(pv_done, (i - 1) & 1, abort_flag, p.status);
+            if (bar_or_softmax(!ok)) { ok = false; break; }   // also publishes alpha_s
+            tc_fence_after();
+#pragma unroll 1
+            for (int c = 0; c < 12; ++c) {  // 4 M-blocks x 3 groups of 32 heads
+              uint32_t o[32];
+              const uint32_t ta = tmem + ((uint32_t)(warp * 32) << 16) + (c / 3) * kHeads + (c % 3) * 32;
+              tmem_ld32(ta, o);
+              tmem_ld_wait();
+#pragma unroll
+              for (int j = 0; j < 32; ++j)
+                o[j] = __float_as_uint(__uint_as_float(o[j]) * alpha_s[(c % 3) * 32 + j]);
+              tmem_st32(ta, o);
+            }
+            tmem_st_wait();
+          }
+        }
+        // probabilities -> bf16 P row h (64 bytes, 64-byte swizzle)
+        uint32_t pk[16];
+        float srnd = 0.f, sex = 0.f;
+#pragma unroll
+        for (int j = 0; j < 32; j += 2) {
+          const float p0 = (m_used == -INFINITY) ? 0.f : exp2f(x[j] - m_used);
+          const float p1 = (m_used == -INFINITY) ? 0.f : exp2f(x[j + 1] - m_used);
+          const __nv_bfloat162 bb = __floats2bfloat162_rn(p0, p1);
+          const float2 back = __bfloat1622float2(bb);
+          srnd += back.x + back.y;
+          sex += p0 + p1;
+          pk[j >> 1] = *reinterpret_cast<const uint32_t*>(&bb);
+        }
+        l_round += srnd;
+        l_exact += sex;
+        if (live) {
+          uint8_t* prow = smem + kOffP + b * kPBytes;
+#pragma unroll
+          for (int c = 0; c < 4; ++c)
+            *reinterpret_cast<uint4*>(prow + swz64(h * 64 + c * 16)) =
+                make_uint4(pk[4 * c], pk[4 * c + 1], pk[4 * c + 2], pk[4 * c + 3]);
+        }
+        fence_proxy_async_smem();
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(p_full(b));
+      }
+      // ---- epilogue: partial results of this chunk
+      if (ok) ok = mbar_wait(pv_done, (ntiles - 1) & 1, abort_flag, p.status);
+      ok = !bar_or_softmax(!ok);
+      if (ok) {
+        tc_fence_after();
+        const int64_t part = (int64_t)row * p.nsplit + split;
+        float* op = p.opart + part * kHeads * kValue;
+        const int dim_in_block = warp * 32 + lane;
+#pragma unroll 1
+        for (int c = 0; c < 12; ++c) {
+          uint32_t o[32];
+          tmem_ld32(tmem + ((uint32_t)(warp * 32) << 16) + (c / 3) * kHeads + (c % 3) * 32, o);
+          tmem_ld_wait();
+          const int dim = (c / 3) * 128 + dim_in_block;
+#pragma unroll
+          for (int j = 0; j < 32; ++j) op[(int64_t)((c % 3) * 32 + j) * kValue + dim] = __uint_as_float(o[j]);
+        }
+        if (live) {
+          float4 v = make_float4(m_used, l_round, l_exact, 0.f);
+          reinterpret_cast<float4*>(p.ml)[part * kHeads + h] = v;
+        }
+      }
+    }
+  } else if (threadIdx.x < kHeads) {
+    // empty chunk: contributes nothing
+    const int64_t part = (int64_t)row * p.nsplit + split;
+    reinterpret_cast<float4*>(p.ml)[part * kHeads + threadIdx.x] = make_float4(-INFINITY, 0.f, 0.f, 0.f);
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  if (warp == 12) tmem_dealloc(tmem, kTmemCols);
+}
+
+// Merge the chunks of one row through their log-sum-exp and write bf16 O and
+// fp32 LSE (natural log).
+__global__ void __launch_bounds__(256) mla_combine_kernel(const float* __restrict__ opart,
+                                                           const float* __restrict__ ml, int nsplit,
+                                                           float latent_scale, uint16_t* out, float* lse) {
+  const int row = blockIdx.y;
+  const int h = blockIdx.x;  // one head per CTA
+  __shared__ float wgt[16];
+  __shared__ float inv_den;
+  const float4* mlr = reinterpret_cast<const float4*>(ml) + (int64_t)row * nsplit * kHeads;
+  if (threadIdx.x == 0) {
+    float M = -INFINITY;
+    for (int s = 0; s < nsplit; ++s) M = fmaxf(M, mlr[s * kHeads + h].x);
+    float den = 0.f, ex = 0.f;
+    for (int s = 0; s < nsplit; ++s) {
+      const float4 v = mlr[s * kHeads + h];
+      const float w = (M == -INFINITY || v.x == -INFINITY) ? 0.f : exp2f(v.x - M);
+      wgt[s] = w;
+      den += w * v.y;
+      ex += w * v.z;
+    }
+    inv_den = den > 0.f ? latent_scale / den : 0.f;
+    lse[(int64_t)row * kHeads + h] = (M == -INFINITY || ex <= 0.f) ? -INFINITY : (M + log2f(ex)) * 0.69314718055994531f;
+  }
+  __syncthreads();
+  for (int d = threadIdx.x * 2; d < kValue; d += 512) {
+    float a0 = 0.f, a1 = 0.f;
+    for (int s = 0; s < nsplit; ++s) {
+      const float w = wgt[s];
+      if (w == 0.f) continue;
+      const float2 v = *reinterpret_cast<const float2*>(opart + (((int64_t)row * nsplit + s) * kHeads + h) * kValue + d);
+      a0 = fmaf(w, v.x, a0);
+      a1 = fmaf(w, v.y, a1);
+    }
+    const __nv_bfloat162 bb = __floats2bfloat162_rn(a0 * inv_den, a1 * inv_den);
+    *reinterpret_cast<__nv_bfloat162*>(out + ((int64_t)row * kHeads + h) * kValue + d) = bb;
+  }
+}
+
+}  // namespace
+
+int mla_nsplit(int rows) { return std::max(1, std::min(16, 160 / std::max(1, rows))); }
+
+size_t mla_workspace_bytes(int rows, int k) {
+  (void)k;
+  auto al = [](size_t x) { return (x + 255) & ~size_t(255); };
+  const size_t parts = (size_t)rows * mla_nsplit(rows);
+  return al(parts * kHeads * kValue * 4) + al(parts * kHeads * 16);
+}
+
+dsa_status_t launch_sparse_mla(const dsa_paged_cache_t& c, const dsa_batch_t& bt, const uint16_t* q_mla,
+                               const int32_t* idx, int k, float sm_scale, uint16_t* out, float* lse,
+                               void* workspace, int32_t* status, cudaStream_t st) {
+  const int rows = bt.batch * bt.queries_per_seq;
+  if (rows == 0) return DSA_OK;
+  CUtensorMap qmap;
+  {
+    const uint64_t dims[2] = {(uint64_t)kLatent, (uint64_t)rows * kHeads};
+    const uint64_t strides[1] = {(uint64_t)kLatent * 2};
+    const uint32_t box[2] = {64, (uint32_t)kHeads};
+    if (!encode_tmap(&qmap, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, q_mla, dims, strides, box,
+                     CU_TENSOR_MAP_SWIZZLE_128B))
+      return DSA_ERR_CUDA;
+  }
+  const int nsplit0 = mla_nsplit(rows);
+  const int tiles = (k + kTileTok - 1) / kTileTok;
+  const int chunk = ((tiles + nsplit0 - 1) / nsplit0) * kTileTok;
+  const int nsplit = (k + chunk - 1) / chunk;
+  auto al = [](size_t x) { return (x + 255) & ~size_t(255); };
+  float* opart = static_cast<float*>(workspace);
+  float* ml = reinterpret_cast<float*>(static_cast<uint8_t*>(workspace) +
+                                       al((size_t)rows * nsplit0 * kHeads * kValue * 4));
+  MlaParams p{static_cast<const uint8_t*>(c.base) + c.latent_off,
+              c.row_stride,
+              c.num_blocks,
+              bt.block_table,
+              bt.max_blocks_per_seq,
+              bt.seq_lens,
+              bt.queries_per_seq,
+              std::min(bt.max_blocks_per_seq * kBlock, bt.max_seq_len),
+              idx,
+              k,
+              chunk,
+              nsplit,
+              sm_scale * c.latent_scale * 1.4426950408889634f,
+              opart,
+              ml,
+              status};
+  static bool attr_set[64] = {};
+  int dev = 0;
+  cudaGetDevice(&dev);
+  if (dev < 64 && !attr_set[dev]) {
+    if (cudaFuncSetAttribute(sparse_mla_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmemBytes) !=
+        cudaSuccess)
+      return DSA_ERR_CUDA;
+    attr_set[dev] = true;
+  }
+  sparse_mla_kernel<<<dim3(nsplit, rows), kThreads, kSmemBytes, st>>>(qmap, p);
+  mla_combine_kernel<<<dim3(kHeads, rows), 256, 0, st>>>(opart, ml, nsplit, c.latent_scale, out, lse);
+  return cudaGetLastError() == cudaSuccess ? DSA_OK : DSA_ERR_CUDA;
+}
+
+}  // namespace dsa

@@ -1,0 +1,398 @@
+// topk.cu — exact per-row top-k selection (stage 2 of DSA).
+//
+// Keeps the k (= 2,048 in the model) highest-scoring visible tokens of each
+// query row (vLLM Day-0 post for Kimi K3.1 Pro, sparse-attention section:
+// "then keep the top 2,048 tokens"; fused-decode section: an exact top-k
+// selection kernel).  Equal scores go to the lower token index, so the
+// selected set is unique; it is written in ascending token order with -1
+// padding when a row has fewer than k tokens.
+//
+// Scores are compared as order-preserving 32-bit keys (integer radix).
+//   1. hist:    multi-CTA per row: 4096-bin histogram of the key's top 12
+//               bits, merged into a per-row global histogram.
+//   2. collect: multi-CTA per row: every CTA finds the threshold bin T
+//               (the bin holding the k-th largest key) from the histogram and
+//               scans its segment: keys above T are selected outright (fewer
+//               than k of them); keys in T become candidates (key, index).
+//   3. final:   one CTA per row: radix-selects the remaining (k - selected)
+//               candidates by (key desc, index asc) on 52 packed bits, then
+//               writes the chosen indices in ascending order through a
+//               shared-memory bitmap of the index range.  If the candidate
+//               buffer overflowed (heavily tied scores) it re-derives the
+//               candidates from the scores directly.
+// The multi-CTA split keeps all SMs busy for the few-long-rows case (4 rows
+// of 1M tokens) as well as for many shorter rows.
+#include <algorithm>
+
+#include "common.cuh"
+#include "internal.h"
+
+namespace dsa {
+
+namespace {
+
+constexpr int kBins = 4096;           // 12-bit first digit
+constexpr int kSeg = 8192;            // tokens per CTA in hist/collect
+constexpr int kThreads = 256;
+constexpr int kCandCap = 8192;        // candidates kept per row
+constexpr int kFinalThreads = 1024;
+constexpr int kWindowBits = 1 << 20;  // bitmap window of the final sort (128 KB)
+
+struct TopkWs {
+  uint32_t* hist;    // [rows][kBins]
+  uint32_t* counts;  // [rows][4]: selected, candidates
+  int32_t* sel;      // [rows][k]
+  uint64_t* cand;    // [rows][kCandCap]
+};
+
+__device__ __forceinline__ int row_len(const int32_t* row_lens, const int32_t* seq_lens, int nq, int r, int cap,
+                                       int32_t* status) {
+  int len = row_lens ? row_lens[r] : visible_len(seq_lens[r / nq], nq, r % nq);
+  if (len < 0 || len > cap) {
+    report(status, DSA_ERR_BOUNDS);
+    len = len < 0 ? 0 : cap;
+  }
+  return len;
+}
+
+// Threshold bin of a row from its 4096-bin histogram: the largest T with
+// sum_{b >= T} hist[b] >= k.  Also returns the count strictly above T.
+// Block-wide; every thread gets the result.
+__device__ void find_threshold(const uint32_t* hist_g, int k, uint32_t* sh_sums, int& T, uint32_t& above) {
+  const int tid = threadIdx.x;
+  constexpr int per = kBins / kThreads;  // 16 bins per thread, thread 0 owns the top bins
+  uint32_t local[per];
+  uint32_t sum = 0;
+#pragma unroll
+  for (int i = 0; i < per; ++i) {
+    local[i] = hist_g[kBins - 1 - (tid * per + i)];  // descending bin order
+    sum += local[i];
+  }
+  sh_sums[tid] = sum;
+  __syncthreads();
+  // inclusive prefix over threads (descending bins)
+  for (int o = 1; o < kThreads; o <<= 1) {
+    uint32_t v = tid >= o ? sh_sums[tid - o] : 0;
+    __syncthreads();
+    sh_sums[tid] += v;
+    __syncthreads();
+  }
+  const uint32_t incl = sh_sums[tid], excl = incl - sum;
+  __shared__ int sh_T;
+  __shared__ uint32_t sh_above;
+  if (excl < (uint32_t)k && incl >= (uint32_t)k) {
+    uint32_t run = excl;
+    for (int i = 0; i < per; ++i) {
+      if (run + local[i] >= (uint32_t)k) {
+        sh_T = kBins - 1 - (tid * per + i);
+        sh_above = run;
+        break;
+      }
+      run += local[i];
+    }
+  }
+  __syncthreads();
+  T = sh_T;
+  above = sh_above;
+}
+
+__global__ void __launch_bounds__(kThreads) topk_hist_kernel(const float* __restrict__ scores, int64_t ld,
+                                                              const int32_t* row_lens, const int32_t* seq_lens,
+                                                              int nq, int cap, int k, TopkWs ws, int32_t* status) {
+  __shared__ uint32_t h[kBins];
+  const int r = blockIdx.y;
+  const int len = row_len(row_lens, seq_lens, nq, r, cap, status);
+  const int64_t t0 = (int64_t)blockIdx.x * kSeg;
+  if (len <= k || t0 >= len) return;
+  for (int i = threadIdx.x; i < kBins; i += kThreads) h[i] = 0;
+  __syncthreads();
+  const int n = (int)std::min<int64_t>(kSeg, len - t0);
+  const float* row = scores + (int64_t)r * ld + t0;
+  const int n4 = n >> 2;
+  const float4* row4 = reinterpret_cast<const float4*>(row);
+  for (int i = threadIdx.x; i < n4; i += kThreads) {
+    float4 v = row4[i];
+    atomicAdd(&h[score_key(v.x) >> 20], 1u);
+    atomicAdd(&h[score_key(v.y) >> 20], 1u);
+    atomicAdd(&h[score_key(v.z) >> 20], 1u);
+    atomicAdd(&h[score_key(v.w) >> 20], 1u);
+  }
+  for (int i = 4 * n4 + threadIdx.x; i < n; i += kThreads) atomicAdd(&h[score_key(row[i]) >> 20], 1u);
+  __syncthreads();
+  uint32_t* g = ws.hist + (int64_t)r * kBins;
+  for (int i = threadIdx.x; i < kBins; i += kThreads)
+    if (h[i]) atomicAdd(&g[i], h[i]);
+}
+
+// Warp-aggregated append: returns this lane's slot (valid only if pred).
+__device__ __forceinline__ uint32_t warp_append(uint32_t* counter, bool pred) {
+  const uint32_t mask = __ballot_sync(0xffffffffu, pred);
+  if (!mask) return 0;
+  const int lane = threadIdx.x & 31;
+  const int leader = __ffs(mask) - 1;
+  uint32_t base = 0;
+  if (lane == leader) base = atomicAdd(counter, (uint32_t)__popc(mask));
+  base = __shfl_sync(0xffffffffu, base, leader);
+  return base + __popc(mask & ((1u << lane) - 1));
+}
+
+__global__ void __launch_bounds__(kThreads) topk_collect_kernel(const float* __restrict__ scores, int64_t ld,
+                                                                 const int32_t* row_lens, const int32_t* seq_lens,
+                                                                 int nq, int cap, int k, TopkWs ws,
+                                                                 int32_t* status) {
+  __shared__ uint32_t sums[kThreads];
+  const int r = blockIdx.y;
+  const int len = row_len(row_lens, seq_lens, nq, r, cap, nullptr);
+  const int64_t t0 = (int64_t)blockIdx.x * kSeg;
+  if (len <= k || t0 >= len) return;
+  int T;
+  uint32_t above;
+  find_threshold(ws.hist + (int64_t)r * kBins, k, sums, T, above);
+  const int n = (int)std::min<int64_t>(kSeg, len - t0);
+  const float* row = scores + (int64_t)r * ld + t0;
+  uint32_t* cnt = ws.counts + 4 * (int64_t)r;
+  int32_t* sel = ws.sel + (int64_t)r * k;
+  uint64_t* cand = ws.cand + (int64_t)r * kCandCap;
+  // whole warps iterate together so the warp-wide appends see every lane
+  for (int base = 0; base < n; base += kThreads) {
+    const int i = base + threadIdx.x;
+    uint32_t key = 0;
+    int bin = -1;
+    if (i < n) {
+      key = score_key(row[i]);
+      bin = (int)(key >> 20);
+    }
+    const bool is_sel = bin > T, is_cand = bin == T;
+    const uint32_t ps = warp_append(&cnt[0], is_sel);
+    if (is_sel && ps < (uint32_t)k) sel[ps] = (int32_t)(t0 + i);
+    const uint32_t pc = warp_append(&cnt[1], is_cand);
+    if (is_cand && pc < (uint32_t)kCandCap)
+      cand[pc] = ((uint64_t)key << 32) | (uint64_t)(0xFFFFFFFFu - (uint32_t)(t0 + i));
+  }
+}
+
+// One radix digit of the final selection: among the values v (52-bit packed
+// (key, ~index) restricted to the prefix found so far), find the digit of
+// the `need`-th largest.  `hist` is a 256-bin shared histogram.
+__device__ __forceinline__ void final_digit(uint32_t* hist, uint32_t* sh, int& digit, uint32_t& need) {
+  // thread t < 256 owns bin 255 - t (descending); exclusive scan over bins
+  const int tid = threadIdx.x;
+  uint32_t c = tid < 256 ? hist[255 - tid] : 0;
+  if (tid < 256) sh[tid] = c;
+  __syncthreads();
+  for (int o = 1; o < 256; o <<= 1) {
+    uint32_t v = (tid < 256 && tid >= o) ? sh[tid - o] : 0;
+    __syncthreads();
+    if (tid < 256) sh[tid] += v;
+    __syncthreads();
+  }
+  __shared__ int s_digit;
+  __shared__ uint32_t s_need;
+  if (tid < 256) {
+    const uint32_t incl = sh[tid], excl = incl - c;
+    if (excl < need && incl >= need) {
+      s_digit = 255 - tid;
+      s_need = need - excl;
+    }
+  }
+  __syncthreads();
+  digit = s_digit;
+  need = s_need;
+}
+
+__global__ void __launch_bounds__(kFinalThreads) topk_final_kernel(const float* __restrict__ scores, int64_t ld,
+                                                                    const int32_t* row_lens,
+                                                                    const int32_t* seq_lens, int nq, int cap, int k,
+                                                                    TopkWs ws, int32_t* out, int32_t* status) {
+  extern __shared__ uint8_t smem_raw[];
+  // layout: chosen[k] int32 | hist[256] | scan[256] | union{ cand[kCandCap] u64, bitmap[kWindowBits/32] u32 }
+  int32_t* chosen = reinterpret_cast<int32_t*>(smem_raw);
+  uint32_t* hist = reinterpret_cast<uint32_t*>(smem_raw + 4 * kMaxTopk);
+  uint32_t* scan = hist + 256;
+  uint8_t* big = smem_raw + 4 * kMaxTopk + 2048 + 1024;
+  uint64_t* cand = reinterpret_cast<uint64_t*>(big);
+  uint32_t* bitmap = reinterpret_cast<uint32_t*>(big);
+  __shared__ uint32_t s_count;
+
+  const int r = blockIdx.x, tid = threadIdx.x;
+  const int len = row_len(row_lens, seq_lens, nq, r, cap, nullptr);
+  int32_t* o = out + (int64_t)r * k;
+  if (len <= k) {
+    for (int i = tid; i < k; i += kFinalThreads) o[i] = i < len ? i : -1;
+    return;
+  }
+  const uint32_t* cnt = ws.counts + 4 * (int64_t)r;
+  const uint32_t n_sel = cnt[0], n_cand = cnt[1];
+  if (n_sel >= (uint32_t)k) {  // cannot happen with a consistent histogram
+    report(status, DSA_ERR_BOUNDS);
+    for (int i = tid; i < k; i += kFinalThreads) o[i] = -1;
+    return;
+  }
+  uint32_t need = (uint32_t)k - n_sel;
+  for (int i = tid; i < (int)n_sel; i += kFinalThreads) chosen[i] = ws.sel[(int64_t)r * k + i];
+
+  // ---- radix-select the `need` best candidates on the packed 52 low bits
+  const bool overflow = n_cand > (uint32_t)kCandCap;
+  int T = 0;
+  const float* row = scores + (int64_t)r * ld;
+  if (!overflow) {
+    for (uint32_t i = tid; i < n_cand; i += kFinalThreads) cand[i] = ws.cand[(int64_t)r * kCandCap + i];
+  } else {
+    // threshold bin = top 12 bits shared by every stored candidate
+    T = (int)(ws.cand[(int64_t)r * kCandCap] >> 52);
+  }
+  __syncthreads();
+  uint64_t prefix = 0, prefix_mask = 0;
+  for (int shift = 48; shift >= 0; shift -= 8) {  // digits of bits [55:0]; bits 55..52 are fixed by T
+    for (int i = tid; i < 256; i += kFinalThreads) hist[i] = 0;
+    __syncthreads();
+    if (!overflow) {
+      for (uint32_t i = tid; i < n_cand; i += kFinalThreads) {
+        const uint64_t v = cand[i];
+        if ((v & prefix_mask) == prefix) atomicAdd(&hist[(v >> shift) & 0xFF], 1u);
+      }
+    } else {
+      for (int t = tid; t < len; t += kFinalThreads) {
+        const uint32_t key = score_key(row[t]);
+        if ((int)(key >> 20) != T) continue;
+        const uint64_t v = ((uint64_t)key << 32) | (uint64_t)(0xFFFFFFFFu - (uint32_t)t);
+        if ((v & prefix_mask) == prefix) atomicAdd(&hist[(v >> shift) & 0xFF], 1u);
+      }
+    }
+    __syncthreads();
+    int digit;
+    final_digit(hist, scan, digit, need);
+    prefix |= (uint64_t)digit << shift;
+    prefix_mask |= 0xFFull << shift;
+    __syncthreads();
+  }
+  // `prefix` (plus the shared top bits) is now the need-th largest packed value:
+  // chosen = candidates whose low 56 bits are >= prefix.
+  if (tid == 0) s_count = n_sel;
+  __syncthreads();
+  if (!overflow) {
+    for (uint32_t i = tid; i < n_cand; i += kFinalThreads) {
+      const uint64_t v = cand[i] & ((1ull << 56) - 1);
+      if (v >= prefix) {
+        const uint32_t pos = atomicAdd(&s_count, 1u);
+        if (pos < (uint32_t)k) chosen[pos] = (int32_t)(0xFFFFFFFFu - (uint32_t)cand[i]);
+      }
+    }
+  } else {
+    for (int t = tid; t < len; t += kFinalThreads) {
+      const uint32_t key = score_key(row[t]);
+      if ((int)(key >> 20) != T) continue;
+      const uint64_t v = (((uint64_t)key << 32) | (uint64_t)(0xFFFFFFFFu - (uint32_t)t)) & ((1ull << 56) - 1);
+      if (v >= prefix) {
+        const uint32_t pos = atomicAdd(&s_count, 1u);
+        if (pos < (uint32_t)k) chosen[pos] = t;
+      }
+    }
+  }
+  __syncthreads();
+  if (s_count != (uint32_t)k) report(status, DSA_ERR_BOUNDS);  // internal consistency check
+  const int nchosen = (int)std::min<uint32_t>(s_count, (uint32_t)k);
+
+  // ---- ascending order through a bitmap of the index range, one window at a time
+  int written = 0;
+  constexpr int kWords = kWindowBits / 32;
+  constexpr int kWordsPerThread = kWords / kFinalThreads;
+  for (int64_t w0 = 0; w0 < len; w0 += kWindowBits) {
+    for (int i = tid; i < kWords; i += kFinalThreads) bitmap[i] = 0;
+    __syncthreads();
+    for (int i = tid; i < nchosen; i += kFinalThreads) {
+      const int64_t t = chosen[i];
+      if (t >= w0 && t < w0 + kWindowBits) atomicOr(&bitmap[(t - w0) >> 5], 1u << ((t - w0) & 31));
+    }
+    __syncthreads();
+    uint32_t c = 0;
+    for (int i = 0; i < kWordsPerThread; ++i) c += __popc(bitmap[tid * kWordsPerThread + i]);
+    // block exclusive scan of c (1024 threads) via warp shuffles + shared
+    uint32_t incl = c;
+    const int lane = tid & 31, wid = tid >> 5;
+#pragma unroll
+    for (int d = 1; d < 32; d <<= 1) {
+      uint32_t v = __shfl_up_sync(0xffffffffu, incl, d);
+      if (lane >= d) incl += v;
+    }
+    if (lane == 31) scan[wid] = incl;
+    __syncthreads();
+    if (wid == 0) {
+      uint32_t v = scan[lane];
+#pragma unroll
+      for (int d = 1; d < 32; d <<= 1) {
+        uint32_t u = __shfl_up_sync(0xffffffffu, v, d);
+        if (lane >= d) v += u;
+      }
+      scan[lane] = v;
+    }
+    __syncthreads();
+    uint32_t pos = written + (wid ? scan[wid - 1] : 0) + incl - c;
+    for (int i = 0; i < kWordsPerThread; ++i) {
+      uint32_t bits = bitmap[tid * kWordsPerThread + i];
+      while (bits) {
+        const int b = __ffs(bits) - 1;
+        bits &= bits - 1;
+        o[pos++] = (int32_t)(w0 + (int64_t)(tid * kWordsPerThread + i) * 32 + b);
+      }
+    }
+    written += scan[31];
+    __syncthreads();
+  }
+  for (int i = written + tid; i < k; i += kFinalThreads) o[i] = -1;
+}
+
+size_t ws_bytes(int rows, int k) {
+  auto al = [](size_t x) { return (x + 255) & ~size_t(255); };
+  return al((size_t)rows * kBins * 4) + al((size_t)rows * 16) + al((size_t)rows * k * 4) +
+         al((size_t)rows * kCandCap * 8);
+}
+
+}  // namespace
+
+size_t topk_workspace_bytes(int rows, int max_row_len, int k) {
+  (void)max_row_len;
+  return ws_bytes(rows, k);
+}
+
+size_t topk_final_smem_bytes() { return 4 * kMaxTopk + 2048 + 1024 + (size_t)kWindowBits / 8; }
+
+dsa_status_t launch_topk(const float* scores, int64_t ld, const int32_t* row_lens, const int32_t* seq_lens, int nq,
+                         int rows, int max_row_len, int k, int32_t* out, void* workspace, int32_t* status,
+                         cudaStream_t st) {
+  if (rows == 0) return DSA_OK;
+  auto al = [](size_t x) { return (x + 255) & ~size_t(255); };
+  uint8_t* w = static_cast<uint8_t*>(workspace);
+  TopkWs ws;
+  ws.hist = reinterpret_cast<uint32_t*>(w);
+  w += al((size_t)rows * kBins * 4);
+  ws.counts = reinterpret_cast<uint32_t*>(w);
+  w += al((size_t)rows * 16);
+  ws.sel = reinterpret_cast<int32_t*>(w);
+  w += al((size_t)rows * k * 4);
+  ws.cand = reinterpret_cast<uint64_t*>(w);
+  // histograms and counters start at zero
+  const size_t zero_bytes = al((size_t)rows * kBins * 4) + al((size_t)rows * 16);
+  if (cudaMemsetAsync(workspace, 0, zero_bytes, st) != cudaSuccess) return DSA_ERR_CUDA;
+  const int cap = max_row_len;
+  const int nseg = std::max(1, (max_row_len + kSeg - 1) / kSeg);
+  if (max_row_len > k) {
+    dim3 grid(nseg, rows);
+    topk_hist_kernel<<<grid, kThreads, 0, st>>>(scores, ld, row_lens, seq_lens, nq, cap, k, ws, status);
+    topk_collect_kernel<<<grid, kThreads, 0, st>>>(scores, ld, row_lens, seq_lens, nq, cap, k, ws, status);
+  }
+  static bool attr_set[64] = {};
+  int dev = 0;
+  cudaGetDevice(&dev);
+  const size_t smem = topk_final_smem_bytes();
+  if (dev < 64 && !attr_set[dev]) {
+    if (cudaFuncSetAttribute(topk_final_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) !=
+        cudaSuccess)
+      return DSA_ERR_CUDA;
+    attr_set[dev] = true;
+  }
+  topk_final_kernel<<<rows, kFinalThreads, smem, st>>>(scores, ld, row_lens, seq_lens, nq, cap, k, ws, out, status);
+  return cudaGetLastError() == cudaSuccess ? DSA_OK : DSA_ERR_CUDA;
+}
+
+}  // namespace dsa

@@ -260,3 +260,33 @@ def workload(name: str, seed: int = 0, **overrides) -> Case:
     if spec.get("seq_lens") is None:
         spec["seq_lens"] = longctx_lengths(seed)
     return make_case(name, seed=seed, **spec)
+
+
+# ---------------------------------------------------------------------------
+# device copies (marshalling only)
+# ---------------------------------------------------------------------------
+
+@dataclasses.dataclass
+class DeviceCase:
+    cache: object        # binding.PagedCache
+    batch: object        # binding.Batch
+    q_index: object      # uint8 [rows, 32, 128]
+    head_w: object       # float32 [rows, 32]
+    q_mla: object        # int16 (bf16 bits) [rows, 96, 576]
+    row_lens: object     # int32 [rows]
+
+
+def device_case(case: Case, device="cuda") -> DeviceCase:
+    """Copy a workload's arrays to the GPU in the layouts libdsa expects."""
+    import torch
+
+    from . import binding
+
+    t = lambda a: torch.from_numpy(np.ascontiguousarray(a)).to(device)
+    cache = binding.PagedCache(pool=t(case.pool), row_stride=case.row_stride, latent_off=case.latent_off,
+                               index_off=case.index_off, key_format=case.key_format,
+                               latent_scale=case.latent_scale)
+    batch = binding.Batch(block_table=t(case.block_table), seq_lens=t(case.seq_lens.astype(np.int32)),
+                          queries_per_seq=case.nq, max_seq_len=max(case.max_len, 0))
+    return DeviceCase(cache=cache, batch=batch, q_index=t(case.q_index), head_w=t(case.head_w),
+                      q_mla=t(case.q_mla.view(np.int16)), row_lens=t(case.row_lens()))

@@ -1,0 +1,203 @@
+/*
+ * dsa.h — C ABI of libdsa.so, the GB300 (sm_103a) DSA decode hot path.
+ *
+ * DSA ("DeepSeek-style sparse attention") as described in the vLLM Day-0
+ * post for Kimi K3.1 Pro, section "K3.1 Pro 中的稀疏注意力" (sparse attention in
+ * K3.1 Pro): a small lightning indexer scores every prior token with 32 light
+ * heads over a 132-byte FP8 key (128 E4M3 codes + fp32 scale), the 2,048
+ * best tokens are kept, and exact MLA attention then runs only over those
+ * tokens' 576-byte FP8 latents.  The indexer score is DeepSeek-V3.2's
+ *     s[t] = sum_h w[h] * max(0, scale_t * (q_h . k_t))
+ * (32 heads x 128 dims, fp32 accumulation and a weighted reduction across
+ * heads — same post, AMD section "量化：原生 MXFP4 索引器").
+ *
+ * The cache is paged and packed ([same post, section "为三类状态服务的 KV 缓存"]):
+ * a pool of block rows, each holding one layer's latent page and index-key
+ * page for 64 tokens; a block table maps (sequence, logical block) to a row,
+ * and the library translates it to page addresses itself on every call.
+ *
+ * Conventions for every entry point
+ *   - All pointers to tensors are DEVICE pointers unless stated otherwise;
+ *     the caller owns every buffer, the workspace and the stream.  The
+ *     library never allocates, frees or synchronises on the hot path.
+ *   - `stream` is a cudaStream_t passed as void* (NULL = legacy default
+ *     stream).  Work is enqueued asynchronously, in stream order.
+ *   - Host-checkable errors (NULL pointers, misalignment, unsupported sizes,
+ *     workspace too small) are returned synchronously and launch nothing.
+ *   - Device-detected errors (a block-table entry or token index outside the
+ *     cache, a bounded wait that ran out) are written to *dev_status (device
+ *     int32) with compare-and-swap from DSA_OK, so the first error wins;
+ *     the caller zeroes it and reads it after synchronising.  Outputs of a
+ *     call that raised a device error are unspecified.
+ *   - A launch failure returns DSA_ERR_CUDA (cudaGetLastError is consumed).
+ *   - Row r = b * queries_per_seq + j is query j of sequence b.  With nq
+ *     queries per sequence (speculative-verify draft rows) and context L,
+ *     row j sees the first L - (nq - 1) + j tokens (causal within the draft).
+ */
+#ifndef DSA_H_
+#define DSA_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define DSA_API_VERSION 1
+#define DSA_BLOCK_SIZE 64        /* tokens per page */
+#define DSA_INDEX_HEADS 32       /* light indexer heads */
+#define DSA_INDEX_DIM 128        /* indexer head dim */
+#define DSA_MLA_HEADS 96         /* attention heads */
+#define DSA_LATENT_DIM 576       /* latent width: keys use all 576 columns */
+#define DSA_VALUE_DIM 512        /* values are the first 512 latent columns */
+#define DSA_MAX_TOPK 2048        /* top-k of the model; also the largest k accepted */
+#define DSA_MAX_QUERIES_PER_SEQ 4
+
+typedef enum dsa_status {
+  DSA_OK = 0,
+  DSA_ERR_INVALID_ARG = 1,   /* NULL pointer, bad size or misaligned buffer */
+  DSA_ERR_UNSUPPORTED = 2,   /* valid request this build does not handle */
+  DSA_ERR_BOUNDS = 3,        /* block-table entry or token index outside the cache (device) */
+  DSA_ERR_TIMEOUT = 4,       /* a bounded in-kernel wait ran out (device) */
+  DSA_ERR_CUDA = 5,          /* CUDA launch or runtime error */
+  DSA_ERR_WORKSPACE = 6      /* workspace NULL or smaller than the *_workspace_size query */
+} dsa_status_t;
+
+typedef enum dsa_key_format {
+  DSA_KEY_FP8_E4M3 = 0,      /* 132 B/token: page = 64 x 128 B E4M3 codes, then 64 fp32 scales */
+  DSA_KEY_MXFP4 = 1          /* 68 B/token: page = 64 x 64 B packed E2M1 (element 2i in the low
+                                nibble of byte i), then 64 x 4 E8M0 scales (one per 32 elements);
+                                no per-token fp32 scale (AMD section: 132 B -> 68 B) */
+} dsa_key_format_t;
+
+/* One layer's view of the packed paged cache. */
+typedef struct dsa_paged_cache {
+  void* base;              /* device address of block row 0; 128-byte aligned */
+  int64_t row_stride;      /* bytes between block rows; multiple of 128 */
+  int64_t latent_off;      /* byte offset of the latent page in a row (64 x 576 E4M3); multiple of 128 */
+  int64_t index_off;       /* byte offset of the index-key page in a row; multiple of 128 */
+  int32_t block_size;      /* tokens per page; must be DSA_BLOCK_SIZE */
+  int32_t num_blocks;      /* block rows in the pool (valid table entries are 0..num_blocks-1) */
+  int32_t key_format;      /* dsa_key_format_t */
+  float latent_scale;      /* per-layer dequantisation scale of the E4M3 latents */
+} dsa_paged_cache_t;
+
+/* The batch of one decode step. */
+typedef struct dsa_batch {
+  const int32_t* block_table;  /* device int32 [batch][max_blocks_per_seq]; entries past a
+                                  sequence's last block are never read */
+  const int32_t* seq_lens;     /* device int32 [batch]: context length incl. the current token(s) */
+  int32_t max_blocks_per_seq;
+  int32_t batch;
+  int32_t queries_per_seq;     /* nq: 1 (plain decode) .. DSA_MAX_QUERIES_PER_SEQ (draft rows) */
+  int32_t max_seq_len;         /* host-known upper bound of seq_lens; sizes grids and scores */
+} dsa_batch_t;
+
+/* Library and status helpers (host only; never fail). */
+int32_t dsa_api_version(void);
+const char* dsa_status_string(int32_t status);
+
+/*
+ * Page translation (Day-0 post, packed-cache section: before every step the
+ * block table and cache slots are turned into kernel page addresses).
+ * Writes, for every sequence b and logical block j < ceil(seq_len_b / 64),
+ * the device byte addresses of its latent page and its index-key page:
+ *   latent_pages[b * max_blocks_per_seq + j] = base + row * row_stride + latent_off
+ * (likewise index_pages); entries past a sequence's blocks are set to 0.
+ * Either output may be NULL.  A table entry outside 0..num_blocks-1 raises
+ * DSA_ERR_BOUNDS in *dev_status and yields address 0.  The other entry points
+ * translate on the fly and do not need this call.
+ */
+dsa_status_t dsa_translate_pages(const dsa_paged_cache_t* cache, const dsa_batch_t* batch,
+                                 int64_t* latent_pages, int64_t* index_pages,
+                                 int32_t* dev_status, void* stream);
+
+/*
+ * Lightning-indexer scores (stage 1).
+ *   q_index  device E4M3 codes [rows][32][128] (16-byte aligned)
+ *   head_w   device fp32 [rows][32]; any query scale is assumed folded into w
+ *   scores   device fp32 [rows][ld_scores]; scores[r][t] is written for every
+ *            visible t of row r and nothing else is touched
+ *   ld_scores >= batch->max_seq_len, multiple of 4
+ * FP8 keys: s[t] = sum_h w[h] * max(0, scale_t * (q_h . k_t)).
+ * MXFP4 keys: q_h . k_t = sum_{blk<4} 2^(E[t,blk]-127) * sum_{d in blk} q_hd * e2m1(k_td),
+ * and scale_t = 1.  Tensor-core accumulation is fp32.
+ */
+dsa_status_t dsa_index_scores(const dsa_paged_cache_t* cache, const dsa_batch_t* batch,
+                              const uint8_t* q_index, const float* head_w,
+                              float* scores, int64_t ld_scores,
+                              int32_t* dev_status, void* stream);
+
+/*
+ * Top-k selection (stage 2): for each row r, the min(k, row_lens[r]) tokens
+ * with the highest scores among t < row_lens[r]; equal scores go to the
+ * lower token index; -0.0 equals +0.0; NaN ranks below every number.
+ * idx_out (device int32 [rows][k]) lists them in ascending token order,
+ * followed by -1 padding.  The result is unique, hence bit-exact.
+ *   scores    device fp32 [rows][ld_scores]
+ *   row_lens  device int32 [rows], each <= max_row_len <= ld_scores
+ *   k         1 .. DSA_MAX_TOPK
+ *   workspace device, >= dsa_topk_workspace_size(rows, max_row_len, k) bytes, 256-B aligned
+ */
+size_t dsa_topk_workspace_size(int32_t rows, int32_t max_row_len, int32_t k);
+dsa_status_t dsa_topk(const float* scores, int64_t ld_scores, const int32_t* row_lens,
+                      int32_t rows, int32_t max_row_len, int32_t k, int32_t* idx_out,
+                      void* workspace, size_t workspace_bytes,
+                      int32_t* dev_status, void* stream);
+
+/*
+ * Exact sparse MLA decode (stage 3; Day-0 post: "MLA attention then runs
+ * exactly, but only on these 2,048 tokens"; absorbed form, 96 heads).
+ * For row r and head h, over the entries i of idx[r] that are >= 0:
+ *   c_i       = latent_scale * e4m3(latent row of token idx[r][i])   (576 values)
+ *   l_i       = sm_scale * (q[r][h] . c_i)
+ *   out[r][h] = sum_i softmax(l)_i * c_i[0:512]        (bf16, round-to-nearest)
+ *   lse[r][h] = ln sum_i exp(l_i)                       (fp32; -inf if no entry)
+ * Every index must be a visible token of its row; otherwise DSA_ERR_BOUNDS.
+ *   q_mla     device bf16 bits [rows][96][576], 16-byte aligned
+ *   idx       device int32 [rows][k], k in 1..DSA_MAX_TOPK
+ *   out       device bf16 bits [rows][96][512];  lse device fp32 [rows][96]
+ *   workspace >= sparse_mla_workspace_size(rows, k) bytes, 256-B aligned
+ * Partial results of token chunks are merged through their log-sum-exp
+ * (Day-0 post, DCP section: partial outputs combined by LSE).
+ */
+size_t sparse_mla_workspace_size(int32_t rows, int32_t k);
+dsa_status_t sparse_mla_decode(const dsa_paged_cache_t* cache, const dsa_batch_t* batch,
+                               const uint16_t* q_mla, const int32_t* idx, int32_t k,
+                               float sm_scale, uint16_t* out, float* lse,
+                               void* workspace, size_t workspace_bytes,
+                               int32_t* dev_status, void* stream);
+
+/*
+ * The fused decode step: page translation, indexer, top-k and sparse MLA on
+ * one stream with no host synchronisation (Day-0 post, fused low-latency
+ * decode section: a key-balanced scorer and an exact top-k in two kernels,
+ * then sparse attention).  Arguments as above; scores_out (fp32
+ * [rows][ld_scores]) and idx_out (int32 [rows][k]) are optional (NULL: kept
+ * in the workspace only).
+ *   workspace >= dsa_workspace_size(batch, k) bytes, 256-B aligned
+ */
+size_t dsa_workspace_size(const dsa_batch_t* batch, int32_t k);
+dsa_status_t dsa_decode_step(const dsa_paged_cache_t* cache, const dsa_batch_t* batch,
+                             const uint8_t* q_index, const float* head_w,
+                             const uint16_t* q_mla, int32_t k, float sm_scale,
+                             uint16_t* out, float* lse,
+                             float* scores_out, int64_t ld_scores, int32_t* idx_out,
+                             void* workspace, size_t workspace_bytes,
+                             int32_t* dev_status, void* stream);
+
+/*
+ * Self-test of the bounded in-kernel wait used by every pipelined kernel:
+ * launches one CTA that waits on a barrier nothing will ever signal, with a
+ * wait limit of `limit_ns` nanoseconds (clamped to 1 ms .. 2 s).  The wait
+ * gives up, the kernel writes DSA_ERR_TIMEOUT to *dev_status and returns;
+ * the CUDA context stays usable.  No GPU fault or hang is involved.
+ */
+dsa_status_t dsa_selftest_wait_timeout(int64_t limit_ns, int32_t* dev_status, void* stream);
+
+#ifdef __cplusplus
+}  /* extern "C" */
+#endif
+
+#endif  /* DSA_H_ */

@@ -1,0 +1,70 @@
+"""The C ABI: the library builds, loads without a GPU and exports every
+entry point include/dsa.h declares; host-side argument checks answer
+synchronously without touching a device."""
+import ctypes
+import os
+import re
+
+import pytest
+
+from dsa_sparse_attention_index_gb300 import binding, build
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    build.build()
+    return binding.lib()
+
+
+def declared_functions():
+    src = open(os.path.join(ROOT, "include", "dsa.h")).read()
+    src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+    return set(re.findall(r"^\s*(?:const\s+)?[a-z_0-9]+\s*\*?\s*([a-z_0-9]+)\s*\(", src, flags=re.M))
+
+
+def test_every_declared_symbol_is_exported(lib):
+    names = declared_functions()
+    assert {"dsa_index_scores", "dsa_topk", "sparse_mla_decode", "dsa_decode_step"} <= names
+    for n in names:
+        assert hasattr(lib, n), f"{n} declared in dsa.h but not exported"
+    assert names == set(binding.EXPORTS)
+
+
+def test_version_and_status_strings(lib):
+    assert lib.dsa_api_version() == 1
+    for code in range(7):
+        assert binding.status_string(code).startswith("DSA_")
+    assert "unknown" in binding.status_string(99)
+
+
+def test_host_validation_without_device(lib):
+    B = binding
+    # null cache / batch descriptors
+    assert lib.dsa_index_scores(None, None, None, None, None, 0, None, None) == B.ERR_INVALID_ARG
+    c = B.PagedCacheT(None, 45312, 0, 36864, 64, 10, 0, 1.0)
+    b = B.BatchT(None, None, 1, 1, 1, 100)
+    assert lib.dsa_index_scores(ctypes.byref(c), ctypes.byref(b), None, None, None, 100, None, None) == B.ERR_INVALID_ARG
+    c.base = 128 * 1000  # fake, aligned, never dereferenced by the host checks
+    c.block_size = 32
+    assert lib.dsa_index_scores(ctypes.byref(c), ctypes.byref(b), None, None, None, 100, None, None) == B.ERR_UNSUPPORTED
+    c.block_size = 64
+    c.row_stride = 45312 + 64  # not a multiple of 128
+    assert lib.sparse_mla_decode(ctypes.byref(c), ctypes.byref(b), None, None, 2048, 1.0, None, None, None, 0, None,
+                                 None) == B.ERR_INVALID_ARG
+    c.row_stride = 45312
+    b.queries_per_seq = 5
+    assert lib.dsa_decode_step(ctypes.byref(c), ctypes.byref(b), None, None, None, 2048, 1.0, None, None, None, 0,
+                               None, None, 0, None, None) == B.ERR_UNSUPPORTED
+    assert lib.dsa_topk(None, 0, None, 1, 10, 0, None, None, 0, None, None) == B.ERR_INVALID_ARG  # k = 0
+    assert lib.dsa_topk(None, 0, None, 1, 10, 4096, None, None, 0, None, None) == B.ERR_INVALID_ARG  # k > 2048
+
+
+def test_workspace_sizes(lib):
+    b = binding.BatchT(None, None, 2560, 32, 1, 163840)
+    ws = lib.dsa_workspace_size(ctypes.byref(b), 2048)
+    assert ws >= 32 * 163840 * 4  # holds the scores
+    assert lib.dsa_topk_workspace_size(4, 1 << 20, 2048) > 0
+    assert lib.sparse_mla_workspace_size(32, 2048) >= 32 * 96 * 512 * 4
+    assert lib.dsa_topk_workspace_size(4, 100, 0) == 0

@@ -1,0 +1,320 @@
+"""GPU parity: every stage of the CUDA path against the fp64 oracle on the
+same seeded inputs, called through the C ABI.
+
+Tolerances (written here, derived in the design doc):
+  scores   |gpu - ref| <= 1e-5 * max(|ref|, A_t), A_t = sum_h |w_h| |scale_t| sum_d |q_hd k_td|
+  top-k    bit-exact (both sides select on the same fp32 scores)
+  MLA      |out - ref| <= 1e-2 (bf16 output), |lse - ref| <= 1e-4
+"""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from dsa_sparse_attention_index_gb300 import binding, synth
+
+pytestmark = pytest.mark.gpu
+
+SCORE_RTOL = 1e-5
+OUT_ATOL = 1e-2
+LSE_ATOL = 1e-4
+SENTINEL = 0x7FC0DEAD  # NaN payload marking never-written score entries
+
+
+def _status():
+    return torch.zeros(1, dtype=torch.int32, device="cuda")
+
+
+def _scores_buf(rows, ld):
+    return torch.full((rows, ld), SENTINEL, dtype=torch.int32, device="cuda").view(torch.float32)
+
+
+def gpu_scores(case, dc, extra=8):
+    ld = (case.max_len + 3) // 4 * 4 + extra
+    s = _scores_buf(case.rows, ld)
+    st = _status()
+    binding.index_scores(dc.cache, dc.batch, dc.q_index, dc.head_w, s, st)
+    torch.cuda.synchronize()
+    assert st.item() == 0, binding.status_string(st.item())
+    return s
+
+
+def check_scores(case, s_gpu):
+    ld = s_gpu.shape[1]
+    ref = oracle.index_scores(case, ld)
+    bound = oracle.index_score_bounds(case, ld)
+    got = s_gpu.cpu().numpy()
+    raw = s_gpu.view(torch.int32).cpu().numpy()
+    for r, vis in enumerate(case.row_lens()):
+        err = np.abs(got[r, :vis].astype(np.float64) - ref[r, :vis])
+        tol = SCORE_RTOL * np.maximum(np.abs(ref[r, :vis]), bound[r, :vis])
+        bad = np.nonzero(err > tol)[0]
+        assert bad.size == 0, f"row {r}: {bad.size} scores out of tolerance, first t={bad[:5]}"
+        assert np.all(raw[r, vis:] == SENTINEL), f"row {r}: wrote past its visible length"
+    return ref
+
+
+@pytest.mark.parametrize("lens,nq", [
+    ([4096], 1),
+    ([1, 63, 64, 65, 127, 128, 129, 200, 1000, 0], 1),
+    ([300, 1031], 2),
+    ([517, 70], 3),
+    ([2000, 64, 4], 4),
+])
+def test_index_scores_match_oracle(lens, nq):
+    case = synth.make_case("idx", seq_lens=lens, nq=nq, seed=len(lens) * 7 + nq, spare_blocks=3)
+    dc = synth.device_case(case)
+    check_scores(case, gpu_scores(case, dc))
+
+
+def test_index_scores_identity_and_permuted_tables_agree():
+    a = synth.make_case("pa", seq_lens=[3000, 777], permute_blocks=False, seed=4)
+    b = synth.make_case("pb", seq_lens=[3000, 777], permute_blocks=True, seed=4)
+    sa = gpu_scores(a, synth.device_case(a))
+    sb = gpu_scores(b, synth.device_case(b))
+    assert torch.equal(sa.view(torch.int32), sb.view(torch.int32))
+
+
+def _gpu_topk(scores, row_lens, k, max_row_len=None):
+    rows = scores.shape[0]
+    max_row_len = int(max_row_len if max_row_len is not None else scores.shape[1])
+    ws = binding.workspace(binding.topk_workspace_size(rows, max_row_len, k))
+    idx = torch.full((rows, k), -7, dtype=torch.int32, device="cuda")
+    st = _status()
+    binding.topk(scores, row_lens, max_row_len, k, idx, ws, st)
+    torch.cuda.synchronize()
+    assert st.item() == 0, binding.status_string(st.item())
+    return idx.cpu().numpy()
+
+
+def test_topk_on_gpu_scores_bit_exact():
+    case = synth.make_case("tk", seq_lens=[9000, 2048, 2049, 100, 20000], nq=1, seed=12)
+    dc = synth.device_case(case)
+    s = gpu_scores(case, dc)
+    k = 2048
+    got = _gpu_topk(s, dc.row_lens, k, case.max_len)
+    ref = oracle.topk(s.cpu().numpy().astype(np.float64), case.row_lens(), k)
+    np.testing.assert_array_equal(got, ref)
+
+
+def _scores_from(rows_np):
+    ld = (max(r.shape[0] for r in rows_np) + 3) // 4 * 4
+    m = np.zeros((len(rows_np), ld), dtype=np.float32)
+    for i, r in enumerate(rows_np):
+        m[i, :r.shape[0]] = r
+    return m, np.array([r.shape[0] for r in rows_np], dtype=np.int32)
+
+
+@pytest.mark.parametrize("k", [2048, 64, 1])
+def test_topk_ties_specials_and_lengths(k):
+    rng = np.random.default_rng(3)
+    rows = [
+        rng.standard_normal(5000).astype(np.float32),
+        rng.integers(0, 3, 7000).astype(np.float32),           # heavy ties
+        np.full(4096, 1.5, dtype=np.float32),                   # all equal
+        np.array([np.nan, -0.0, 0.0, -np.inf, np.inf, 1.0] * 700, dtype=np.float32),
+        rng.standard_normal(k).astype(np.float32),              # exactly k
+        rng.standard_normal(k + 1).astype(np.float32),          # k + 1
+        rng.standard_normal(max(k // 2, 1)).astype(np.float32),  # fewer than k
+        np.zeros(0, dtype=np.float32),                          # empty
+        np.full(20000, -2.0, dtype=np.float32),                 # candidate overflow: 20000 ties
+        np.concatenate([np.full(12000, 3.0), rng.standard_normal(9000)]).astype(np.float32),
+    ]
+    m, lens = _scores_from(rows)
+    got = _gpu_topk(torch.from_numpy(m).cuda(), torch.from_numpy(lens).cuda(), k)
+    ref = oracle.topk(m.astype(np.float64), lens, k)
+    np.testing.assert_array_equal(got, ref)
+
+
+def test_topk_long_rows():
+    rng = np.random.default_rng(5)
+    m = rng.standard_normal((2, 300_001)).astype(np.float32)
+    m[1, ::3] = m[1, 7]                                         # many duplicates of one value
+    lens = np.array([300_001, 250_000], dtype=np.int32)
+    got = _gpu_topk(torch.from_numpy(m).cuda(), torch.from_numpy(lens).cuda(), 2048)
+    np.testing.assert_array_equal(got, oracle.topk(m.astype(np.float64), lens, 2048))
+
+
+def _gpu_mla(case, dc, idx_np):
+    rows, k = idx_np.shape
+    idx = torch.from_numpy(np.ascontiguousarray(idx_np, dtype=np.int32)).cuda()
+    out = torch.empty((rows, 96, 512), dtype=torch.int16, device="cuda")
+    lse = torch.empty((rows, 96), dtype=torch.float32, device="cuda")
+    ws = binding.workspace(binding.sparse_mla_workspace_size(rows, k))
+    st = _status()
+    binding.sparse_mla_decode(dc.cache, dc.batch, dc.q_mla, idx, case.sm_scale, out, lse, ws, st)
+    torch.cuda.synchronize()
+    assert st.item() == 0, binding.status_string(st.item())
+    o = out.view(torch.bfloat16).float().cpu().numpy()
+    return o, lse.cpu().numpy()
+
+
+def check_mla(case, idx_np, o, l):
+    ro, rl = oracle.sparse_mla(case, idx_np)
+    err = np.abs(o - ro).max()
+    assert err <= OUT_ATOL, f"max |out - ref| = {err}"
+    fin = np.isfinite(rl)
+    assert np.array_equal(fin, np.isfinite(l))
+    assert np.all(np.isneginf(l[~fin]))
+    if fin.any():
+        assert np.abs(l[fin] - rl[fin]).max() <= LSE_ATOL
+    assert np.all(o[~fin] == 0)
+
+
+@pytest.mark.parametrize("k", [2048, 100, 1])
+def test_sparse_mla_matches_oracle(k):
+    case = synth.make_case("mla", seq_lens=[6000, 2500, 900], nq=1, seed=21 + k)
+    dc = synth.device_case(case)
+    rng = np.random.default_rng(k)
+    idx = np.full((3, k), -1, dtype=np.int32)
+    for r, L in enumerate(case.row_lens()):
+        n = min(k, int(L))
+        idx[r, :n] = np.sort(rng.choice(int(L), n, replace=False))
+    o, l = _gpu_mla(case, dc, idx)
+    check_mla(case, idx, o, l)
+
+
+def test_sparse_mla_masked_rows_and_scattered_padding():
+    case = synth.make_case("mlm", seq_lens=[3000, 3000], nq=2, seed=5)
+    dc = synth.device_case(case)
+    rng = np.random.default_rng(9)
+    k = 256
+    idx = np.full((4, k), -1, dtype=np.int32)
+    idx[0] = rng.choice(2999, k, replace=False)          # unsorted
+    idx[1, ::3] = rng.choice(3000, len(idx[1, ::3]), replace=False)  # holes anywhere
+    # row 2 stays fully masked
+    idx[3, :5] = [0, 1, 2, 2999, 17]
+    o, l = _gpu_mla(case, dc, idx)
+    check_mla(case, idx, o, l)
+
+
+def test_sparse_mla_large_logits_rescale():
+    # scale the queries up so the running maximum grows many times per row
+    case = synth.make_case("mlr", seq_lens=[4096], seed=8)
+    q = case.q_mla.view(np.uint16).astype(np.uint32) << 16
+    qf = q.view(np.float32) * 8.0
+    case.q_mla = synth.bf16_encode(qf)
+    dc = synth.device_case(case)
+    idx = np.arange(2048, dtype=np.int32)[None] * 2
+    o, l = _gpu_mla(case, dc, idx)
+    check_mla(case, idx, o, l)
+
+
+def _run_step(case, k=None, with_outputs=True):
+    dc = synth.device_case(case)
+    k = k or case.topk
+    rows = case.rows
+    ld = (case.max_len + 3) // 4 * 4
+    scores = _scores_buf(rows, ld)
+    idx = torch.empty((rows, k), dtype=torch.int32, device="cuda")
+    out = torch.empty((rows, 96, 512), dtype=torch.int16, device="cuda")
+    lse = torch.empty((rows, 96), dtype=torch.float32, device="cuda")
+    ws = binding.workspace(binding.workspace_size(dc.batch, k))
+    st = _status()
+    binding.decode_step(dc.cache, dc.batch, dc.q_index, dc.head_w, dc.q_mla, k, case.sm_scale, out, lse, ws, st,
+                        scores_out=scores if with_outputs else None, idx_out=idx if with_outputs else None)
+    torch.cuda.synchronize()
+    assert st.item() == 0, binding.status_string(st.item())
+    return scores, idx.cpu().numpy(), out.view(torch.bfloat16).float().cpu().numpy(), lse.cpu().numpy()
+
+
+@pytest.mark.parametrize("name,kw", [
+    ("decode_b1_l4096", dict(seq_lens=[4096], permute_blocks=False)),
+    ("spec_b2x4", dict(seq_lens=[5000, 2100], nq=4)),
+    ("ragged_b3", dict(seq_lens=[70001, 1500, 2047])),
+    ("heavy_tail_b2", dict(seq_lens=[40000, 33333], heavy_tail=0.1)),
+])
+def test_decode_step_matches_oracle(name, kw):
+    case = synth.make_case(name, seed=17, **kw)
+    scores, idx, o, l = _run_step(case)
+    check_scores(case, scores)
+    s64 = scores.cpu().numpy().astype(np.float64)
+    np.testing.assert_array_equal(idx, oracle.topk(s64, case.row_lens(), case.topk))
+    check_mla(case, idx, o, l)
+    # end to end against the all-fp64 path: selections may differ only at
+    # scores within the score tolerance of the selection threshold
+    ref_s = oracle.index_scores(case, scores.shape[1])
+    bound = oracle.index_score_bounds(case, scores.shape[1])
+    ref_idx = oracle.topk(ref_s, case.row_lens(), case.topk)
+    for r in range(case.rows):
+        a, b = set(idx[r][idx[r] >= 0]), set(ref_idx[r][ref_idx[r] >= 0])
+        if a == b:
+            continue
+        vis = case.row_lens()[r]
+        thr = np.sort(ref_s[r, :vis])[::-1][case.topk - 1]
+        for t in a ^ b:
+            assert abs(ref_s[r, t] - thr) <= 2 * SCORE_RTOL * max(abs(ref_s[r, t]), bound[r, t]), (r, t)
+
+
+def test_decode_step_without_optional_outputs():
+    case = synth.make_case("noout", seq_lens=[5000], seed=2)
+    s1, i1, o1, l1 = _run_step(case)
+    _, _, o2, l2 = _run_step(case, with_outputs=False)
+    assert np.array_equal(o1, o2) and np.array_equal(l1, l2)
+
+
+# ------------------------------------------------------------ device errors
+def test_bad_block_table_entry_reports_bounds():
+    case = synth.make_case("bad", seq_lens=[1000], seed=1)
+    case.block_table[0, 3] = case.num_blocks + 5
+    dc = synth.device_case(case)
+    s = _scores_buf(1, 1004)
+    st = _status()
+    binding.index_scores(dc.cache, dc.batch, dc.q_index, dc.head_w, s, st)
+    torch.cuda.synchronize()
+    assert st.item() == binding.ERR_BOUNDS
+
+
+def test_index_beyond_visible_length_reports_bounds():
+    case = synth.make_case("badidx", seq_lens=[500], seed=1)
+    dc = synth.device_case(case)
+    idx = torch.tensor([[0, 1, 500]], dtype=torch.int32, device="cuda")
+    out = torch.empty((1, 96, 512), dtype=torch.int16, device="cuda")
+    lse = torch.empty((1, 96), dtype=torch.float32, device="cuda")
+    ws = binding.workspace(binding.sparse_mla_workspace_size(1, 3))
+    st = _status()
+    binding.sparse_mla_decode(dc.cache, dc.batch, dc.q_mla, idx, case.sm_scale, out, lse, ws, st)
+    torch.cuda.synchronize()
+    assert st.item() == binding.ERR_BOUNDS
+
+
+def test_seq_len_beyond_table_capacity_reports_bounds():
+    case = synth.make_case("cap", seq_lens=[640], seed=1)
+    dc = synth.device_case(case)
+    dc.batch.seq_lens.fill_(641)  # the table holds 10 blocks = 640 tokens
+    dc.batch.max_seq_len = 641
+    s = _scores_buf(1, 644)
+    st = _status()
+    binding.index_scores(dc.cache, dc.batch, dc.q_index, dc.head_w, s, st)
+    torch.cuda.synchronize()
+    assert st.item() == binding.ERR_BOUNDS
+
+
+def test_bounded_wait_times_out_and_context_survives():
+    st = _status()
+    binding.selftest_wait_timeout(5_000_000, st)
+    torch.cuda.synchronize()
+    assert st.item() == binding.ERR_TIMEOUT
+    case = synth.make_case("after", seq_lens=[300], seed=3)
+    check_scores(case, gpu_scores(case, synth.device_case(case)))
+
+
+def test_translate_pages():
+    case = synth.make_case("tp", seq_lens=[130, 64, 1], seed=3, spare_blocks=2)
+    dc = synth.device_case(case)
+    lat = torch.full(case.block_table.shape, -1, dtype=torch.int64, device="cuda")
+    idx = torch.full(case.block_table.shape, -1, dtype=torch.int64, device="cuda")
+    st = _status()
+    binding.translate_pages(dc.cache, dc.batch, lat, idx, st)
+    torch.cuda.synchronize()
+    assert st.item() == 0
+    base = dc.cache.pool.data_ptr()
+    lat, idx = lat.cpu().numpy(), idx.cpu().numpy()
+    for b, L in enumerate(case.seq_lens):
+        for j in range(case.block_table.shape[1]):
+            if j * 64 < L:
+                r = case.block_table[b, j]
+                assert lat[b, j] == base + r * case.row_stride + case.latent_off
+                assert idx[b, j] == base + r * case.row_stride + case.index_off
+            else:
+                assert lat[b, j] == 0 and idx[b, j] == 0
