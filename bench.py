@@ -9,8 +9,9 @@ Default workload: the long-context batch (32 sequences, context ~ U(64K,
 Prints ONE JSON line.  ``value`` is the whole-job algorithmic HBM throughput
 (GB/s): the key bytes (132 B/token, once per sequence), the selected
 latents (576 B/token/row), queries and outputs, divided by the step time.
-The inputs exceed L2 and L2 is also flushed (256 MB write) between timed
-steps, outside the per-step CUDA-event pairs.
+The inputs exceed L2 and L2 is also flushed (a 256 MB read) between timed
+steps, outside the per-step CUDA-event pairs.  SM clocks are sampled with
+nvidia-smi over a soak of identical steps that ends with the timed region.
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME]
   python bench.py --impl reference ...   # the fp64 CPU oracle on a bounded sample
@@ -37,7 +38,7 @@ from dsa_sparse_attention_index_gb300 import roofline, synth  # noqa: E402
 METRIC = "DSA decode µs/layer-step & achieved HBM GB/s (fraction of 8 TB/s) at 1 GB300"
 DEFAULT_WORKLOAD = "longctx_b32_l64k-160k"
 NOMINAL_HBM_GBS = 8000.0
-L2_FLUSH_BYTES = 256 << 20
+L2_FLUSH_BYTES = 256 << 20   # > 129 MB L2; flushed by READING it (clean lines, no write-back)
 
 
 def parse():
@@ -50,6 +51,7 @@ def parse():
     ap.add_argument("--seed", type=int, default=0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--soak-s", type=float, default=1.5, help="seconds of identical steps before the timed region")
     return ap.parse_args()
 
 
@@ -180,7 +182,15 @@ def main_ours(args):
     tk_ws = binding.workspace(binding.topk_workspace_size(rows, case.max_len, k), dev)
     mla_ws = binding.workspace(binding.sparse_mla_workspace_size(rows, k), dev)
     status = torch.zeros(1, dtype=torch.int32, device=dev)
-    flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
+    flush_buf = torch.ones(L2_FLUSH_BYTES // 8, dtype=torch.int64, device=dev)
+    flush_sink = torch.empty((), dtype=torch.int64, device=dev)
+
+    class _Flush:
+        @staticmethod
+        def zero_():  # read 256 MB: evicts L2 with clean lines, outside the step events
+            flush_sink.copy_(flush_buf.sum())
+
+    flush = _Flush()
     stream = torch.cuda.current_stream()
 
     def step():
@@ -201,6 +211,12 @@ def main_ours(args):
     # ---- headline: K fused steps, each bracketed by its own events, L2 flushed in between
     ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
     with ClockSampler(local) as clk:
+        t_soak = time.perf_counter()
+        while time.perf_counter() - t_soak < args.soak_s:
+            for _ in range(20):
+                flush.zero_()
+                step()
+            torch.cuda.synchronize()
         barrier()
         t_wall = time.perf_counter()
         for e0, e1 in ev:
@@ -296,7 +312,7 @@ def main_ours(args):
             "seq_len_max": int(case.seq_lens.max()), "topk": k, "key_bytes": case.token_bytes(),
             "latent_bytes": 576, "heads": 96, "index_heads": 32, "block": 64,
             "algorithmic_bytes_per_step": b["total"], "parallelism": f"replicas x{world}",
-            "l2": "inputs > L2 and 256 MB L2 flush between timed steps (outside the step events)",
+            "l2": "inputs > L2; L2 flushed by a 256 MB read between timed steps (outside the step events)",
         },
         "stage_us": {kk: round(v * 1e3, 2) for kk, v in st_ms.items()},
         "roofline": {"kernel": "indexer_fp8_kernel (dsa_index_scores)", "bound": "hbm",

@@ -24,7 +24,10 @@ BLOCK, IDX_HEADS, IDX_DIM, MLA_HEADS, LATENT, VALUE, MAX_TOPK = 64, 32, 128, 96,
 class DsaError(RuntimeError):
     def __init__(self, code: int, what: str):
         self.code = code
-        super().__init__(f"{what}: {status_string(code)}")
+        extra = ""
+        if code == ERR_CUDA:
+            extra = f" [{lib().dsa_last_cuda_error().decode()}]"
+        super().__init__(f"{what}: {status_string(code)}{extra}")
 
 
 class PagedCacheT(ctypes.Structure):
@@ -41,7 +44,7 @@ class BatchT(ctypes.Structure):
 
 _lib = None
 
-EXPORTS = ["dsa_api_version", "dsa_status_string", "dsa_translate_pages", "dsa_index_scores",
+EXPORTS = ["dsa_api_version", "dsa_status_string", "dsa_last_cuda_error", "dsa_translate_pages", "dsa_index_scores",
            "dsa_topk_workspace_size", "dsa_topk", "sparse_mla_workspace_size", "sparse_mla_decode",
            "dsa_workspace_size", "dsa_decode_step", "dsa_selftest_wait_timeout"]
 
@@ -59,6 +62,7 @@ def lib():
         sig = {
             "dsa_api_version": (i32, []),
             "dsa_status_string": (ctypes.c_char_p, [i32]),
+            "dsa_last_cuda_error": (ctypes.c_char_p, []),
             "dsa_translate_pages": (i32, [pc, pb, P, P, P, P]),
             "dsa_index_scores": (i32, [pc, pb, P, P, P, i64, P, P]),
             "dsa_topk_workspace_size": (sz, [i32, i32, i32]),

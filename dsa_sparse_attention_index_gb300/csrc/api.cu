@@ -2,6 +2,7 @@
 // the stream-ordered composition of the kernels.  No allocation, no host
 // synchronisation on any entry point.
 #include <algorithm>
+#include <cstdio>
 #include <mutex>
 
 #include "common.cuh"
@@ -18,6 +19,16 @@ int num_sms() {
   if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0) n = 1;
   if (dev >= 0 && dev < 64) cache[dev] = n;
   return n;
+}
+
+namespace {
+thread_local char g_last_cuda_error[256] = "";
+}  // namespace
+
+dsa_status_t cuda_status(cudaError_t e) {
+  if (e == cudaSuccess) return DSA_OK;
+  snprintf(g_last_cuda_error, sizeof(g_last_cuda_error), "%s: %s", cudaGetErrorName(e), cudaGetErrorString(e));
+  return DSA_ERR_CUDA;
 }
 
 namespace {
@@ -83,8 +94,12 @@ bool encode_tmap(CUtensorMap* map, CUtensorMapDataType dtype, int rank, const vo
     es[i] = 1;
   }
   for (int i = 0; i + 1 < rank; ++i) s[i] = strides[i];
-  return fn(map, dtype, (cuuint32_t)rank, const_cast<void*>(base), d, s, bx, es, CU_TENSOR_MAP_INTERLEAVE_NONE,
-            swizzle, CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+  const CUresult r = fn(map, dtype, (cuuint32_t)rank, const_cast<void*>(base), d, s, bx, es,
+                        CU_TENSOR_MAP_INTERLEAVE_NONE, swizzle, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                        CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS)
+    snprintf(g_last_cuda_error, sizeof(g_last_cuda_error), "cuTensorMapEncodeTiled failed with CUresult %d", (int)r);
+  return r == CUDA_SUCCESS;
 }
 
 }  // namespace dsa
@@ -94,6 +109,8 @@ using namespace dsa;
 extern "C" {
 
 int32_t dsa_api_version(void) { return DSA_API_VERSION; }
+
+const char* dsa_last_cuda_error(void) { return g_last_cuda_error; }
 
 const char* dsa_status_string(int32_t s) {
   switch (s) {

@@ -174,38 +174,73 @@ __global__ void __launch_bounds__(kThreads, 1)
   };
 
   if (u_begin < u_end) {
-    if (warp == 0 && lane == 0) {
-      // ------------------------------------------------ TMA producer
-      int cursor = first_seq(u_begin), cur_b = -1;
+    if (warp == 0) {
+      // ------------------------------------------------ TMA producer (one warp)
+      // The lanes resolve the block-table rows of the next 32 units while lane 0
+      // issues the copies of the current 32, so table reads never stall the ring.
+      constexpr unsigned kAll = 0xffffffffu;
+      auto resolve = [&](int64_t g, int& rb, int& rj, int& rnp, int& r0, int& r1) {
+        const int64_t u = g + lane;
+        rb = 0; rj = 0; rnp = 0; r0 = 0; r1 = 0;
+        if (u < u_end) {
+          rb = first_seq(u);
+          rj = (int)(u - prefix[rb]);
+          rnp = (kTileKeys * rj + kBlock < seq_len_of(rb)) ? 2 : 1;
+          const int32_t* bt = p.block_table + (int64_t)rb * p.max_blocks + 2 * rj;
+          r0 = bt[0];
+          r1 = rnp == 2 ? bt[1] : 0;
+        }
+      };
+      int cb, cj, cnp, c0, c1;
+      resolve(u_begin, cb, cj, cnp, c0, c1);
+      int cur_b = -1;
       uint32_t it = 0, qn = 0;
-      for (int64_t u = u_begin; u < u_end; ++u, ++it) {
-        const int b = seq_of_unit(prefix, p.batch, u, cursor);
-        if (b != cur_b) {
-          const int slot = qn & 1;
-          if (!mbar_wait(qe_bar(slot), ((qn >> 1) & 1) ^ 1, abort_flag, p.status)) break;
-          mbar_arrive_expect_tx(qf_bar(slot), L::kQSlot);
-          tma_load_2d(sbase + L::kOffQ + slot * L::kQSlot, &tmap_q, 0, b * N, qf_bar(slot));
-          ++qn;
-          cur_b = b;
-        }
-        const int s = it % kStages;
-        if (!mbar_wait(empty_bar(s), ((it / kStages) & 1) ^ 1, abort_flag, p.status)) break;
-        const int j = (int)(u - prefix[b]);
-        const int len = seq_len_of(b);
-        const int npages = (kTileKeys * j + kBlock < len) ? 2 : 1;
-        mbar_arrive_expect_tx(full_bar(s), npages * (kPageCodeBytes + kPageScaleBytes));
-        for (int pg = 0; pg < npages; ++pg) {
-          int r = p.block_table[(int64_t)b * p.max_blocks + 2 * j + pg];
-          if (r < 0 || r >= p.num_blocks) {
-            report(p.status, DSA_ERR_BOUNDS);
-            r = 0;  // read a valid row instead; the call's results are void
+      bool ok = true;
+      for (int64_t g = u_begin; ok && g < u_end; g += 32) {
+        int nb, nj, nnp, n0, n1;
+        resolve(g + 32, nb, nj, nnp, n0, n1);  // next group's rows, in flight meanwhile
+        const int n = (int)((u_end - g) < 32 ? (u_end - g) : 32);
+        for (int l = 0; l < n; ++l, ++it) {
+          const int b = __shfl_sync(kAll, cb, l);
+          const int j = __shfl_sync(kAll, cj, l);
+          const int npages = __shfl_sync(kAll, cnp, l);
+          const int rr0 = __shfl_sync(kAll, c0, l);
+          const int rr1 = __shfl_sync(kAll, c1, l);
+          if (lane == 0) {
+            if (b != cur_b) {
+              const int slot = qn & 1;
+              ok = mbar_wait(qe_bar(slot), ((qn >> 1) & 1) ^ 1, abort_flag, p.status);
+              if (ok) {
+                mbar_arrive_expect_tx(qf_bar(slot), L::kQSlot);
+                tma_load_2d(sbase + L::kOffQ + slot * L::kQSlot, &tmap_q, 0, b * N, qf_bar(slot));
+                ++qn;
+                cur_b = b;
+              }
+            }
+            const int s = it % kStages;
+            ok = ok && mbar_wait(empty_bar(s), ((it / kStages) & 1) ^ 1, abort_flag, p.status);
+            if (ok) {
+              mbar_arrive_expect_tx(full_bar(s), npages * (kPageCodeBytes + kPageScaleBytes));
+              for (int pg = 0; pg < npages; ++pg) {
+                int r = pg ? rr1 : rr0;
+                if (r < 0 || r >= p.num_blocks) {
+                  report(p.status, DSA_ERR_BOUNDS);
+                  r = 0;  // read a valid row instead; the call's results are void
+                }
+                tma_load_3d(sbase + L::kOffA + s * kATileBytes + pg * kPageCodeBytes, &tmap_keys, 0, 0, r,
+                            full_bar(s));
+                bulk_load(sbase + L::kOffScales + s * 2 * kPageScaleBytes + pg * kPageScaleBytes,
+                          p.index_base + (int64_t)r * p.row_stride + kPageCodeBytes, kPageScaleBytes, full_bar(s));
+              }
+            }
           }
-          tma_load_3d(sbase + L::kOffA + s * kATileBytes + pg * kPageCodeBytes, &tmap_keys, 0, 0, r, full_bar(s));
-          bulk_load(sbase + L::kOffScales + s * 2 * kPageScaleBytes + pg * kPageScaleBytes,
-                    p.index_base + (int64_t)r * p.row_stride + kPageCodeBytes, kPageScaleBytes, full_bar(s));
+          ok = __shfl_sync(kAll, ok, 0);
+          if (!ok) break;
+          (void)j;
         }
+        cb = nb; cj = nj; cnp = nnp; c0 = n0; c1 = n1;
       }
-      if (*abort_flag) {  // let copies already in flight land before the CTA exits
+      if (lane == 0 && *abort_flag) {  // let copies already in flight land before the CTA exits
         for (uint32_t k = (it > kStages ? it - kStages : 0); k < it; ++k)
           mbar_wait(full_bar(k % kStages), (k / kStages) & 1, abort_flag, nullptr, 10000000ull);
       }
@@ -303,15 +338,15 @@ dsa_status_t launch_nq(const IdxParams& p, const CUtensorMap& keys, const CUtens
   cudaGetDevice(&dev);
   const size_t smem = IdxSmem<NQ>::bytes(kMaxBatch);
   if (dev < 64 && !attr_set[dev]) {
-    if (cudaFuncSetAttribute(indexer_fp8_kernel<NQ>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) !=
-        cudaSuccess)
+    if (cuda_status(cudaFuncSetAttribute(indexer_fp8_kernel<NQ>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         (int)smem)) != DSA_OK)
       return DSA_ERR_CUDA;
     attr_set[dev] = true;
   }
   const int64_t units_bound = (int64_t)p.batch * ((p.max_seq_len + kTileKeys - 1) / kTileKeys);
   const int grid = (int)std::max<int64_t>(1, std::min<int64_t>(units_bound, num_sms()));
   indexer_fp8_kernel<NQ><<<grid, kThreads, IdxSmem<NQ>::bytes(p.batch), st>>>(keys, q, p);
-  return cudaGetLastError() == cudaSuccess ? DSA_OK : DSA_ERR_CUDA;
+  return launch_status();
 }
 
 }  // namespace

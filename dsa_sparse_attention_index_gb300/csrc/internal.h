@@ -13,6 +13,12 @@ namespace dsa {
 // Streaming multiprocessors of the current device (cached per device).
 int num_sms();
 
+// Records `e` (if not cudaSuccess) as this thread's last CUDA error and maps
+// it to DSA_OK / DSA_ERR_CUDA.
+dsa_status_t cuda_status(cudaError_t e);
+// cuda_status(cudaGetLastError()): the launch check after a kernel launch.
+inline dsa_status_t launch_status() { return cuda_status(cudaGetLastError()); }
+
 // cuTensorMapEncodeTiled through the runtime's driver entry point (no libcuda
 // link dependency).  strides: rank-1 byte strides of dims 1..rank-1.
 bool encode_tmap(CUtensorMap* map, CUtensorMapDataType dtype, int rank, const void* base, const uint64_t* dims,

@@ -69,14 +69,14 @@ dsa_status_t launch_translate_pages(const dsa_paged_cache_t& c, const dsa_batch_
                                                    c.index_off, c.num_blocks, bt.block_table,
                                                    bt.max_blocks_per_seq, bt.seq_lens, bt.batch, cap, latent_pages,
                                                    index_pages, status);
-  return cudaGetLastError() == cudaSuccess ? DSA_OK : DSA_ERR_CUDA;
+  return launch_status();
 }
 
 dsa_status_t launch_wait_selftest(int64_t limit_ns, int32_t* status, cudaStream_t st) {
   if (limit_ns < 1000000) limit_ns = 1000000;
   if (limit_ns > 2000000000) limit_ns = 2000000000;
   wait_selftest_kernel<<<1, 32, 0, st>>>((uint64_t)limit_ns, status);
-  return cudaGetLastError() == cudaSuccess ? DSA_OK : DSA_ERR_CUDA;
+  return launch_status();
 }
 
 }  // namespace dsa

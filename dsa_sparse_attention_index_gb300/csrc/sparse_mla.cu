@@ -8,16 +8,16 @@
 // prefill section gives the 96 heads).  The selected rows are read straight
 // from the packed paged cache through the block table.
 //
-// GB300 design (one CTA per (query row, token chunk), 13 warps):
+// GB300 design (one CTA per (query row, token chunk), 11 warps):
 //   * Q [96 x 576] bf16 is loaded once by TMA into shared memory (108 KB,
 //     128-byte swizzle, K-major) and is the A operand of S = Q K^T with the
 //     heads on the MMA's M = 128 rows (rows 96..127 are ignored).
-//   * warps 4..11 gather 32 latent rows per tile (16-byte loads, prefetched a
-//     tile ahead), widen E4M3 -> bf16 exactly in registers and store the tile
+//   * warps 4..9 gather 32 latent rows per tile (16-byte loads, four tiles in
+//     flight), widen E4M3 -> bf16 exactly in registers and store the tile
 //     once, 128-byte swizzled.  That single tile is the B operand of QK^T
 //     (K-major, N = 32 tokens) and the A operand of P V (MN-major, M = 128
 //     value dims), so V needs no second copy.
-//   * warp 12 issues tcgen05.mma (kind::f16, fp32 accumulation): S into a
+//   * warp 10 issues tcgen05.mma (kind::f16, fp32 accumulation): S into a
 //     double-buffered 32-column TMEM tile, O^T = V^T P^T into 4 x 96 TMEM
 //     columns (dims on lanes, heads on columns: 384 + 2*32 <= 512 columns).
 //     QK of tile i+1 is issued before PV of tile i so the softmax overlaps
@@ -48,8 +48,12 @@ constexpr int kTileDBlockBytes = kTileTok * 128;       // 4,096
 constexpr int kTileBytes = kDBlocks * kTileDBlockBytes;  // 36,864
 constexpr int kPBytes = kHeads * kTileTok * 2;         // 6,144
 constexpr int kMaxChunk = 2048;
-constexpr int kThreads = 13 * 32;
-constexpr int kLoaderThreads = 256;
+// 11 warps: softmax 0-3, loaders 4-9, MMA issuer 10.  At most 3 warps share a
+// sub-partition's register file, which leaves room for 168 registers a thread.
+constexpr int kThreads = 11 * 32;
+constexpr int kLoaderThreads = 192;
+constexpr int kMmaWarp = 10;
+constexpr int kChunksPerThread = kTileTok * (kLatent / 16) / kLoaderThreads;  // 6 of the 1,152 16-B chunks
 constexpr int kOCols = 4 * kHeads;                     // 384 TMEM columns of O^T
 constexpr int kSCol = kOCols;                          // S buffers at 384 and 416
 constexpr int kTmemCols = 512;
@@ -142,7 +146,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     fence_mbar_init();
     prefetch_tmap(&tmap_q);
   }
-  if (warp == 12) {
+  if (warp == kMmaWarp) {
     tmem_alloc(smem_u32(tmem_slot), kTmemCols);
     tmem_relinquish();
   }
@@ -167,7 +171,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   const uint32_t tmem = *tmem_slot;
 
   if (ntiles > 0) {
-    if (warp == 12) {
+    if (warp == kMmaWarp) {
       if (lane == 0) {
         // ------------------------------------------------ Q load + MMA issuer
         mbar_arrive_expect_tx(q_full, kQBytes);
@@ -223,29 +227,31 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
     } else if (warp >= 4) {
       // ------------------------------------------------ gather + E4M3 -> bf16
-      const int lt = threadIdx.x - 128;       // 0..255
-      const int tok = lt >> 3;                // token row of the tile, 0..31
-      const int g = lt & 7;                   // chunk group: 16-byte chunks g, g+8, ..., < 36
-      const int nch = g < 4 ? 5 : 4;
-      uint4 bufA[5], bufB[5];
-      auto load = [&](int i, uint4 (&buf)[5]) {
+      const int lt = threadIdx.x - 128;                 // 0..191
+      const int tok = lt / kChunksPerThread;             // token row of the tile, 0..31
+      const int g = lt % kChunksPerThread;               // chunks g, g+6, ..., g+30 of the 36
+      // four tiles in flight per thread (a register ring), so the gather of
+      // tile i+3 overlaps the conversion of tile i
+      uint4 buf0[kChunksPerThread], buf1[kChunksPerThread], buf2[kChunksPerThread], buf3[kChunksPerThread];
+      auto load = [&](int i, uint4 (&buf)[kChunksPerThread]) {
+        if (i >= ntiles) return;
         const int64_t off = tok_off[i * kTileTok + tok];
 #pragma unroll
-        for (int c = 0; c < 5; ++c) {
+        for (int c = 0; c < kChunksPerThread; ++c) {
           buf[c] = make_uint4(0, 0, 0, 0);
-          if (c < nch && off >= 0)
-            buf[c] = __ldg(reinterpret_cast<const uint4*>(p.latent_base + off) + (g + 8 * c));
+          if (off >= 0) buf[c] = __ldg(reinterpret_cast<const uint4*>(p.latent_base + off) + (g + kChunksPerThread * c));
         }
       };
-      auto store = [&](int i, const uint4 (&buf)[5]) -> bool {
+      auto store = [&](int i, const uint4 (&buf)[kChunksPerThread]) -> bool {
+        if (i >= ntiles) return true;
         const int b = i & 1;
         const bool ok = mbar_wait(tile_empty(b), ((i >> 1) & 1) ^ 1, abort_flag, p.status);
         if (!__all_sync(0xffffffffu, ok)) return false;
         uint8_t* tile = smem + kOffTile + b * kTileBytes;
 #pragma unroll
-        for (int c = 0; c < 5; ++c) {
-          if (c < nch) {
-            const int ch = g + 8 * c;          // 16-byte chunk of the 576-byte row: dims [16 ch, +16)
+        for (int c = 0; c < kChunksPerThread; ++c) {
+          {
+            const int ch = g + kChunksPerThread * c;  // 16-byte chunk of the 576-byte row: dims [16 ch, +16)
             const int dblk = ch >> 2;
             const uint32_t inner = (uint32_t)((ch & 3) * 32);
             const uint32_t w[4] = {buf[c].x, buf[c].y, buf[c].z, buf[c].w};
@@ -265,12 +271,18 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (lane == 0) mbar_arrive(tile_full(b));
         return true;
       };
-      load(0, bufA);
-      for (int i = 0; i < ntiles; i += 2) {
-        if (i + 1 < ntiles) load(i + 1, bufB);
-        if (!store(i, bufA)) break;
-        if (i + 2 < ntiles) load(i + 2, bufA);
-        if (i + 1 < ntiles && !store(i + 1, bufB)) break;
+      load(0, buf0);
+      load(1, buf1);
+      load(2, buf2);
+      for (int i = 0; i < ntiles; i += 4) {
+        load(i + 3, buf3);
+        if (!store(i, buf0)) break;
+        load(i + 4, buf0);
+        if (!store(i + 1, buf1)) break;
+        load(i + 5, buf1);
+        if (!store(i + 2, buf2)) break;
+        load(i + 6, buf2);
+        if (!store(i + 3, buf3)) break;
       }
     } else {
       // ------------------------------------------------ softmax (thread = head)
@@ -379,7 +391,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
-  if (warp == 12) tmem_dealloc(tmem, kTmemCols);
+  if (warp == kMmaWarp) tmem_dealloc(tmem, kTmemCols);
 }
 
 // Merge the chunks of one row through their log-sum-exp and write bf16 O and
@@ -423,12 +435,15 @@ __global__ void __launch_bounds__(256) mla_combine_kernel(const float* __restric
 
 }  // namespace
 
-int mla_nsplit(int rows) { return std::max(1, std::min(16, 160 / std::max(1, rows))); }
+// Token chunks per row: enough CTAs for one wave over the SMs (one CTA per SM
+// fits), at most 16; the workspace is sized for up to 256 SMs.
+int mla_nsplit_max(int rows) { return std::max(1, std::min(16, 256 / std::max(1, rows))); }
+int mla_nsplit(int rows) { return std::max(1, std::min(mla_nsplit_max(rows), num_sms() / std::max(1, rows))); }
 
 size_t mla_workspace_bytes(int rows, int k) {
   (void)k;
   auto al = [](size_t x) { return (x + 255) & ~size_t(255); };
-  const size_t parts = (size_t)rows * mla_nsplit(rows);
+  const size_t parts = (size_t)rows * mla_nsplit_max(rows);
   return al(parts * kHeads * kValue * 4) + al(parts * kHeads * 16);
 }
 
@@ -453,7 +468,7 @@ dsa_status_t launch_sparse_mla(const dsa_paged_cache_t& c, const dsa_batch_t& bt
   auto al = [](size_t x) { return (x + 255) & ~size_t(255); };
   float* opart = static_cast<float*>(workspace);
   float* ml = reinterpret_cast<float*>(static_cast<uint8_t*>(workspace) +
-                                       al((size_t)rows * nsplit0 * kHeads * kValue * 4));
+                                       al((size_t)rows * mla_nsplit_max(rows) * kHeads * kValue * 4));
   MlaParams p{static_cast<const uint8_t*>(c.base) + c.latent_off,
               c.row_stride,
               c.num_blocks,
@@ -474,14 +489,15 @@ dsa_status_t launch_sparse_mla(const dsa_paged_cache_t& c, const dsa_batch_t& bt
   int dev = 0;
   cudaGetDevice(&dev);
   if (dev < 64 && !attr_set[dev]) {
-    if (cudaFuncSetAttribute(sparse_mla_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmemBytes) !=
-        cudaSuccess)
+    if (cuda_status(cudaFuncSetAttribute(sparse_mla_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         (int)kSmemBytes)) != DSA_OK)
       return DSA_ERR_CUDA;
     attr_set[dev] = true;
   }
   sparse_mla_kernel<<<dim3(nsplit, rows), kThreads, kSmemBytes, st>>>(qmap, p);
+  if (launch_status() != DSA_OK) return DSA_ERR_CUDA;
   mla_combine_kernel<<<dim3(kHeads, rows), 256, 0, st>>>(opart, ml, nsplit, c.latent_scale, out, lse);
-  return cudaGetLastError() == cudaSuccess ? DSA_OK : DSA_ERR_CUDA;
+  return launch_status();
 }
 
 }  // namespace dsa

@@ -35,7 +35,7 @@ constexpr int kBins = 4096;           // 12-bit first digit
 constexpr int kSeg = 8192;            // tokens per CTA in hist/collect
 constexpr int kThreads = 256;
 constexpr int kCandCap = 8192;        // candidates kept per row
-constexpr int kFinalThreads = 1024;
+constexpr int kFinalThreads = 512;
 constexpr int kWindowBits = 1 << 20;  // bitmap window of the final sort (128 KB)
 
 struct TopkWs {
@@ -124,23 +124,13 @@ __global__ void __launch_bounds__(kThreads) topk_hist_kernel(const float* __rest
     if (h[i]) atomicAdd(&g[i], h[i]);
 }
 
-// Warp-aggregated append: returns this lane's slot (valid only if pred).
-__device__ __forceinline__ uint32_t warp_append(uint32_t* counter, bool pred) {
-  const uint32_t mask = __ballot_sync(0xffffffffu, pred);
-  if (!mask) return 0;
-  const int lane = threadIdx.x & 31;
-  const int leader = __ffs(mask) - 1;
-  uint32_t base = 0;
-  if (lane == leader) base = atomicAdd(counter, (uint32_t)__popc(mask));
-  base = __shfl_sync(0xffffffffu, base, leader);
-  return base + __popc(mask & ((1u << lane) - 1));
-}
-
 __global__ void __launch_bounds__(kThreads) topk_collect_kernel(const float* __restrict__ scores, int64_t ld,
                                                                  const int32_t* row_lens, const int32_t* seq_lens,
                                                                  int nq, int cap, int k, TopkWs ws,
                                                                  int32_t* status) {
   __shared__ uint32_t sums[kThreads];
+  __shared__ uint32_t keys[kSeg];
+  __shared__ uint32_t s_cnt[2], s_base[2];
   const int r = blockIdx.y;
   const int len = row_len(row_lens, seq_lens, nq, r, cap, nullptr);
   const int64_t t0 = (int64_t)blockIdx.x * kSeg;
@@ -150,54 +140,123 @@ __global__ void __launch_bounds__(kThreads) topk_collect_kernel(const float* __r
   find_threshold(ws.hist + (int64_t)r * kBins, k, sums, T, above);
   const int n = (int)std::min<int64_t>(kSeg, len - t0);
   const float* row = scores + (int64_t)r * ld + t0;
+  const int lane = threadIdx.x & 31;
+  if (threadIdx.x < 2) s_cnt[threadIdx.x] = 0;
+  __syncthreads();
+  // pass 1: keys into shared memory, count this CTA's selected and candidate entries
+  uint32_t ns = 0, nc = 0;
+  for (int i = threadIdx.x; i < n; i += kThreads) {
+    const uint32_t key = score_key(row[i]);
+    keys[i] = key;
+    const int bin = (int)(key >> 20);
+    ns += bin > T;
+    nc += bin == T;
+  }
+#pragma unroll
+  for (int o = 16; o; o >>= 1) {
+    ns += __shfl_xor_sync(0xffffffffu, ns, o);
+    nc += __shfl_xor_sync(0xffffffffu, nc, o);
+  }
+  if (lane == 0) {
+    if (ns) atomicAdd(&s_cnt[0], ns);
+    if (nc) atomicAdd(&s_cnt[1], nc);
+  }
+  __syncthreads();
   uint32_t* cnt = ws.counts + 4 * (int64_t)r;
+  if (threadIdx.x == 0) {  // one global reservation per counter per CTA
+    s_base[0] = s_cnt[0] ? atomicAdd(&cnt[0], s_cnt[0]) : 0;
+    s_base[1] = s_cnt[1] ? atomicAdd(&cnt[1], s_cnt[1]) : 0;
+    s_cnt[0] = s_cnt[1] = 0;
+  }
+  __syncthreads();
+  // pass 2: write the entries into the reserved ranges (order inside a range is free)
   int32_t* sel = ws.sel + (int64_t)r * k;
   uint64_t* cand = ws.cand + (int64_t)r * kCandCap;
-  // whole warps iterate together so the warp-wide appends see every lane
   for (int base = 0; base < n; base += kThreads) {
     const int i = base + threadIdx.x;
-    uint32_t key = 0;
-    int bin = -1;
-    if (i < n) {
-      key = score_key(row[i]);
-      bin = (int)(key >> 20);
+    const uint32_t key = i < n ? keys[i] : 0u;
+    const int bin = i < n ? (int)(key >> 20) : -1;
+    const uint32_t ms = __ballot_sync(0xffffffffu, bin > T);
+    const uint32_t mc = __ballot_sync(0xffffffffu, bin == T);
+    uint32_t ws_ = 0, wc = 0;
+    if (lane == 0) {
+      if (ms) ws_ = atomicAdd(&s_cnt[0], (uint32_t)__popc(ms));
+      if (mc) wc = atomicAdd(&s_cnt[1], (uint32_t)__popc(mc));
     }
-    const bool is_sel = bin > T, is_cand = bin == T;
-    const uint32_t ps = warp_append(&cnt[0], is_sel);
-    if (is_sel && ps < (uint32_t)k) sel[ps] = (int32_t)(t0 + i);
-    const uint32_t pc = warp_append(&cnt[1], is_cand);
-    if (is_cand && pc < (uint32_t)kCandCap)
-      cand[pc] = ((uint64_t)key << 32) | (uint64_t)(0xFFFFFFFFu - (uint32_t)(t0 + i));
+    ws_ = __shfl_sync(0xffffffffu, ws_, 0);
+    wc = __shfl_sync(0xffffffffu, wc, 0);
+    const uint32_t below = (1u << lane) - 1;
+    if (bin > T) {
+      const uint32_t ps = s_base[0] + ws_ + __popc(ms & below);
+      if (ps < (uint32_t)k) sel[ps] = (int32_t)(t0 + i);
+    } else if (bin == T) {
+      const uint32_t pc = s_base[1] + wc + __popc(mc & below);
+      if (pc < (uint32_t)kCandCap) cand[pc] = ((uint64_t)key << 32) | (uint64_t)(0xFFFFFFFFu - (uint32_t)(t0 + i));
+    }
   }
 }
 
-// One radix digit of the final selection: among the values v (52-bit packed
-// (key, ~index) restricted to the prefix found so far), find the digit of
-// the `need`-th largest.  `hist` is a 256-bin shared histogram.
-__device__ __forceinline__ void final_digit(uint32_t* hist, uint32_t* sh, int& digit, uint32_t& need) {
-  // thread t < 256 owns bin 255 - t (descending); exclusive scan over bins
-  const int tid = threadIdx.x;
-  uint32_t c = tid < 256 ? hist[255 - tid] : 0;
-  if (tid < 256) sh[tid] = c;
-  __syncthreads();
-  for (int o = 1; o < 256; o <<= 1) {
-    uint32_t v = (tid < 256 && tid >= o) ? sh[tid - o] : 0;
-    __syncthreads();
-    if (tid < 256) sh[tid] += v;
-    __syncthreads();
+// Block-wide exclusive scan of one value per thread (kFinalThreads threads).
+__device__ __forceinline__ uint32_t block_excl_scan(uint32_t v, uint32_t* sh, uint32_t& total) {
+  const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5;
+  uint32_t incl = v;
+#pragma unroll
+  for (int d = 1; d < 32; d <<= 1) {
+    const uint32_t u = __shfl_up_sync(0xffffffffu, incl, d);
+    if (lane >= d) incl += u;
   }
+  if (lane == 31) sh[wid] = incl;
+  __syncthreads();
+  if (wid == 0) {
+    uint32_t w = lane < kFinalThreads / 32 ? sh[lane] : 0;
+#pragma unroll
+    for (int d = 1; d < 32; d <<= 1) {
+      const uint32_t u = __shfl_up_sync(0xffffffffu, w, d);
+      if (lane >= d) w += u;
+    }
+    sh[lane] = w;  // inclusive warp totals
+  }
+  __syncthreads();
+  total = sh[kFinalThreads / 32 - 1];
+  const uint32_t r = (wid ? sh[wid - 1] : 0) + incl - v;
+  __syncthreads();
+  return r;
+}
+
+// Finds, in the digit histogram `hist` (nbins bins, larger digit = larger
+// value), the digit holding the need-th largest value; updates `need` to the
+// rank inside that bin and returns the digit and the bin's population.
+__device__ void pick_digit(const uint32_t* hist, int nbins, uint32_t* sh, uint32_t& need, int& digit,
+                           uint32_t& pop) {
+  const int per = (nbins + kFinalThreads - 1) / kFinalThreads;  // bins per thread, descending order
+  uint32_t c = 0;
+  for (int i = 0; i < per; ++i) {
+    const int bin = nbins - 1 - (threadIdx.x * per + i);
+    if (bin >= 0) c += hist[bin];
+  }
+  uint32_t total;
+  const uint32_t excl = block_excl_scan(c, sh, total);
   __shared__ int s_digit;
-  __shared__ uint32_t s_need;
-  if (tid < 256) {
-    const uint32_t incl = sh[tid], excl = incl - c;
-    if (excl < need && incl >= need) {
-      s_digit = 255 - tid;
-      s_need = need - excl;
+  __shared__ uint32_t s_need, s_pop;
+  if (excl < need && excl + c >= need) {
+    uint32_t run = excl;
+    for (int i = 0; i < per; ++i) {
+      const int bin = nbins - 1 - (threadIdx.x * per + i);
+      if (bin < 0) break;
+      if (run + hist[bin] >= need) {
+        s_digit = bin;
+        s_need = need - run;
+        s_pop = hist[bin];
+        break;
+      }
+      run += hist[bin];
     }
   }
   __syncthreads();
   digit = s_digit;
   need = s_need;
+  pop = s_pop;
+  __syncthreads();
 }
 
 __global__ void __launch_bounds__(kFinalThreads) topk_final_kernel(const float* __restrict__ scores, int64_t ld,
@@ -205,11 +264,11 @@ __global__ void __launch_bounds__(kFinalThreads) topk_final_kernel(const float* 
                                                                     const int32_t* seq_lens, int nq, int cap, int k,
                                                                     TopkWs ws, int32_t* out, int32_t* status) {
   extern __shared__ uint8_t smem_raw[];
-  // layout: chosen[k] int32 | hist[256] | scan[256] | union{ cand[kCandCap] u64, bitmap[kWindowBits/32] u32 }
+  // chosen[kMaxTopk] i32 | hist[kBins] u32 | scan[32] u32 | union{ cand[kCandCap] u64, bitmap[kWindowBits/32] }
   int32_t* chosen = reinterpret_cast<int32_t*>(smem_raw);
   uint32_t* hist = reinterpret_cast<uint32_t*>(smem_raw + 4 * kMaxTopk);
-  uint32_t* scan = hist + 256;
-  uint8_t* big = smem_raw + 4 * kMaxTopk + 2048 + 1024;
+  uint32_t* scan = hist + kBins;
+  uint8_t* big = smem_raw + 4 * kMaxTopk + 4 * kBins + 128;
   uint64_t* cand = reinterpret_cast<uint64_t*>(big);
   uint32_t* bitmap = reinterpret_cast<uint32_t*>(big);
   __shared__ uint32_t s_count;
@@ -223,67 +282,72 @@ __global__ void __launch_bounds__(kFinalThreads) topk_final_kernel(const float* 
   }
   const uint32_t* cnt = ws.counts + 4 * (int64_t)r;
   const uint32_t n_sel = cnt[0], n_cand = cnt[1];
-  if (n_sel >= (uint32_t)k) {  // cannot happen with a consistent histogram
+  if (n_sel >= (uint32_t)k || n_cand == 0) {  // impossible with a consistent histogram
     report(status, DSA_ERR_BOUNDS);
     for (int i = tid; i < k; i += kFinalThreads) o[i] = -1;
     return;
   }
   uint32_t need = (uint32_t)k - n_sel;
   for (int i = tid; i < (int)n_sel; i += kFinalThreads) chosen[i] = ws.sel[(int64_t)r * k + i];
-
-  // ---- radix-select the `need` best candidates on the packed 52 low bits
   const bool overflow = n_cand > (uint32_t)kCandCap;
-  int T = 0;
+  const uint64_t* gcand = ws.cand + (int64_t)r * kCandCap;
+  const int T = (int)(gcand[0] >> 52);  // threshold bin: top 12 key bits shared by every candidate
   const float* row = scores + (int64_t)r * ld;
-  if (!overflow) {
-    for (uint32_t i = tid; i < n_cand; i += kFinalThreads) cand[i] = ws.cand[(int64_t)r * kCandCap + i];
-  } else {
-    // threshold bin = top 12 bits shared by every stored candidate
-    T = (int)(ws.cand[(int64_t)r * kCandCap] >> 52);
-  }
+  if (!overflow)
+    for (uint32_t i = tid; i < n_cand; i += kFinalThreads) cand[i] = gcand[i];
   __syncthreads();
-  uint64_t prefix = 0, prefix_mask = 0;
-  for (int shift = 48; shift >= 0; shift -= 8) {  // digits of bits [55:0]; bits 55..52 are fixed by T
-    for (int i = tid; i < 256; i += kFinalThreads) hist[i] = 0;
+
+  // ---- the `need` largest packed values v = (key << 32) | ~index among the
+  //      candidates: 12-bit digits of bits 51..0 (bits 63..52 equal T), stopping
+  //      as soon as the digit's bin is taken whole.
+  auto packed = [&](int t) -> uint64_t {
+    return ((uint64_t)score_key(row[t]) << 32) | (uint64_t)(0xFFFFFFFFu - (uint32_t)t);
+  };
+  uint64_t prefix = 0;
+  int shift = 52;
+  while (shift > 0) {
+    const int bits = shift >= 12 ? 12 : shift;
+    const int nshift = shift - bits;
+    for (int i = tid; i < (1 << bits); i += kFinalThreads) hist[i] = 0;
     __syncthreads();
+    const uint32_t dmask = (1u << bits) - 1;
     if (!overflow) {
       for (uint32_t i = tid; i < n_cand; i += kFinalThreads) {
-        const uint64_t v = cand[i];
-        if ((v & prefix_mask) == prefix) atomicAdd(&hist[(v >> shift) & 0xFF], 1u);
+        const uint64_t v = cand[i] & ((1ull << 52) - 1);
+        if ((v >> shift) == prefix) atomicAdd(&hist[(uint32_t)(v >> nshift) & dmask], 1u);
       }
     } else {
       for (int t = tid; t < len; t += kFinalThreads) {
-        const uint32_t key = score_key(row[t]);
-        if ((int)(key >> 20) != T) continue;
-        const uint64_t v = ((uint64_t)key << 32) | (uint64_t)(0xFFFFFFFFu - (uint32_t)t);
-        if ((v & prefix_mask) == prefix) atomicAdd(&hist[(v >> shift) & 0xFF], 1u);
+        const uint64_t full = packed(t);
+        if ((int)(full >> 52) != T) continue;
+        const uint64_t v = full & ((1ull << 52) - 1);
+        if ((v >> shift) == prefix) atomicAdd(&hist[(uint32_t)(v >> nshift) & dmask], 1u);
       }
     }
     __syncthreads();
     int digit;
-    final_digit(hist, scan, digit, need);
-    prefix |= (uint64_t)digit << shift;
-    prefix_mask |= 0xFFull << shift;
-    __syncthreads();
+    uint32_t pop;
+    pick_digit(hist, 1 << bits, scan, need, digit, pop);
+    prefix = (prefix << bits) | (uint64_t)digit;
+    shift = nshift;
+    if (need == pop) break;  // the whole bin is taken: select by prefix
   }
-  // `prefix` (plus the shared top bits) is now the need-th largest packed value:
-  // chosen = candidates whose low 56 bits are >= prefix.
+  // chosen += candidates whose bits 51..shift are >= prefix
   if (tid == 0) s_count = n_sel;
   __syncthreads();
   if (!overflow) {
     for (uint32_t i = tid; i < n_cand; i += kFinalThreads) {
-      const uint64_t v = cand[i] & ((1ull << 56) - 1);
-      if (v >= prefix) {
+      const uint64_t v = cand[i] & ((1ull << 52) - 1);
+      if ((v >> shift) >= prefix) {
         const uint32_t pos = atomicAdd(&s_count, 1u);
         if (pos < (uint32_t)k) chosen[pos] = (int32_t)(0xFFFFFFFFu - (uint32_t)cand[i]);
       }
     }
   } else {
     for (int t = tid; t < len; t += kFinalThreads) {
-      const uint32_t key = score_key(row[t]);
-      if ((int)(key >> 20) != T) continue;
-      const uint64_t v = (((uint64_t)key << 32) | (uint64_t)(0xFFFFFFFFu - (uint32_t)t)) & ((1ull << 56) - 1);
-      if (v >= prefix) {
+      const uint64_t full = packed(t);
+      if ((int)(full >> 52) != T) continue;
+      if (((full & ((1ull << 52) - 1)) >> shift) >= prefix) {
         const uint32_t pos = atomicAdd(&s_count, 1u);
         if (pos < (uint32_t)k) chosen[pos] = t;
       }
@@ -294,52 +358,40 @@ __global__ void __launch_bounds__(kFinalThreads) topk_final_kernel(const float* 
   const int nchosen = (int)std::min<uint32_t>(s_count, (uint32_t)k);
 
   // ---- ascending order through a bitmap of the index range, one window at a time
-  int written = 0;
-  constexpr int kWords = kWindowBits / 32;
-  constexpr int kWordsPerThread = kWords / kFinalThreads;
+  uint32_t written = 0;
   for (int64_t w0 = 0; w0 < len; w0 += kWindowBits) {
-    for (int i = tid; i < kWords; i += kFinalThreads) bitmap[i] = 0;
+    const int span = (int)std::min<int64_t>(kWindowBits, len - w0);
+    const int words = (span + 31) >> 5;
+    const int per = (words + kFinalThreads - 1) / kFinalThreads;
+    for (int i = tid; i < words; i += kFinalThreads) bitmap[i] = 0;
     __syncthreads();
     for (int i = tid; i < nchosen; i += kFinalThreads) {
       const int64_t t = chosen[i];
-      if (t >= w0 && t < w0 + kWindowBits) atomicOr(&bitmap[(t - w0) >> 5], 1u << ((t - w0) & 31));
+      if (t >= w0 && t < w0 + span) atomicOr(&bitmap[(t - w0) >> 5], 1u << ((t - w0) & 31));
     }
     __syncthreads();
     uint32_t c = 0;
-    for (int i = 0; i < kWordsPerThread; ++i) c += __popc(bitmap[tid * kWordsPerThread + i]);
-    // block exclusive scan of c (1024 threads) via warp shuffles + shared
-    uint32_t incl = c;
-    const int lane = tid & 31, wid = tid >> 5;
-#pragma unroll
-    for (int d = 1; d < 32; d <<= 1) {
-      uint32_t v = __shfl_up_sync(0xffffffffu, incl, d);
-      if (lane >= d) incl += v;
+    for (int i = 0; i < per; ++i) {
+      const int wi = tid * per + i;
+      if (wi < words) c += __popc(bitmap[wi]);
     }
-    if (lane == 31) scan[wid] = incl;
-    __syncthreads();
-    if (wid == 0) {
-      uint32_t v = scan[lane];
-#pragma unroll
-      for (int d = 1; d < 32; d <<= 1) {
-        uint32_t u = __shfl_up_sync(0xffffffffu, v, d);
-        if (lane >= d) v += u;
-      }
-      scan[lane] = v;
-    }
-    __syncthreads();
-    uint32_t pos = written + (wid ? scan[wid - 1] : 0) + incl - c;
-    for (int i = 0; i < kWordsPerThread; ++i) {
-      uint32_t bits = bitmap[tid * kWordsPerThread + i];
+    uint32_t total;
+    uint32_t pos = written + block_excl_scan(c, scan, total);
+    for (int i = 0; i < per; ++i) {
+      const int wi = tid * per + i;
+      if (wi >= words) break;
+      uint32_t bits = bitmap[wi];
       while (bits) {
         const int b = __ffs(bits) - 1;
         bits &= bits - 1;
-        o[pos++] = (int32_t)(w0 + (int64_t)(tid * kWordsPerThread + i) * 32 + b);
+        if (pos < (uint32_t)k) o[pos] = (int32_t)(w0 + (int64_t)wi * 32 + b);
+        ++pos;
       }
     }
-    written += scan[31];
+    written += total;
     __syncthreads();
   }
-  for (int i = written + tid; i < k; i += kFinalThreads) o[i] = -1;
+  for (int i = (int)written + tid; i < k; i += kFinalThreads) o[i] = -1;
 }
 
 size_t ws_bytes(int rows, int k) {
@@ -355,7 +407,7 @@ size_t topk_workspace_bytes(int rows, int max_row_len, int k) {
   return ws_bytes(rows, k);
 }
 
-size_t topk_final_smem_bytes() { return 4 * kMaxTopk + 2048 + 1024 + (size_t)kWindowBits / 8; }
+size_t topk_final_smem_bytes() { return 4 * kMaxTopk + 4 * kBins + 128 + (size_t)kWindowBits / 8; }
 
 dsa_status_t launch_topk(const float* scores, int64_t ld, const int32_t* row_lens, const int32_t* seq_lens, int nq,
                          int rows, int max_row_len, int k, int32_t* out, void* workspace, int32_t* status,
@@ -373,7 +425,7 @@ dsa_status_t launch_topk(const float* scores, int64_t ld, const int32_t* row_len
   ws.cand = reinterpret_cast<uint64_t*>(w);
   // histograms and counters start at zero
   const size_t zero_bytes = al((size_t)rows * kBins * 4) + al((size_t)rows * 16);
-  if (cudaMemsetAsync(workspace, 0, zero_bytes, st) != cudaSuccess) return DSA_ERR_CUDA;
+  if (cuda_status(cudaMemsetAsync(workspace, 0, zero_bytes, st)) != DSA_OK) return DSA_ERR_CUDA;
   const int cap = max_row_len;
   const int nseg = std::max(1, (max_row_len + kSeg - 1) / kSeg);
   if (max_row_len > k) {
@@ -386,13 +438,13 @@ dsa_status_t launch_topk(const float* scores, int64_t ld, const int32_t* row_len
   cudaGetDevice(&dev);
   const size_t smem = topk_final_smem_bytes();
   if (dev < 64 && !attr_set[dev]) {
-    if (cudaFuncSetAttribute(topk_final_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) !=
-        cudaSuccess)
+    if (cuda_status(cudaFuncSetAttribute(topk_final_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         (int)smem)) != DSA_OK)
       return DSA_ERR_CUDA;
     attr_set[dev] = true;
   }
   topk_final_kernel<<<rows, kFinalThreads, smem, st>>>(scores, ld, row_lens, seq_lens, nq, cap, k, ws, out, status);
-  return cudaGetLastError() == cudaSuccess ? DSA_OK : DSA_ERR_CUDA;
+  return launch_status();
 }
 
 }  // namespace dsa

@@ -97,6 +97,9 @@ typedef struct dsa_batch {
 /* Library and status helpers (host only; never fail). */
 int32_t dsa_api_version(void);
 const char* dsa_status_string(int32_t status);
+/* Text of the last CUDA error this thread's calls into the library saw
+ * (the reason behind a DSA_ERR_CUDA), or "" if none. */
+const char* dsa_last_cuda_error(void);
 
 /*
  * Page translation (Day-0 post, packed-cache section: before every step the
