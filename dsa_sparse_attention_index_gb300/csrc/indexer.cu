@@ -9,20 +9,24 @@
 // GB300 design.  Each 132-byte key carries 32*128 multiply-adds, i.e. 62
 // FLOP per byte: at HBM speed that is ~0.4 PFLOP/s, several times what the
 // CUDA cores can issue, so the dot products run on the 5th-gen tensor cores
-// even in decode.  A work unit is one sequence's 128 consecutive tokens (two
+// even in decode.  A work unit is one sequence's 256 consecutive tokens (four
 // 64-token pages).  The grid is persistent (one CTA per SM) and the units of
 // all sequences are split evenly across CTAs ("key-balanced", Day-0 post,
 // fused decode section).  Per CTA:
-//   warp 0  TMA producer: two 64x128 B code pages (128-byte swizzle) and their
-//           fp32 scales per unit into an 8-stage ring; the query tile of the
-//           current sequence into a 2-slot ring;
-//   warp 1  MMA issuer: tcgen05.mma kind::f8f6f4, M = 128 keys, N = 32*NQ
-//           query-heads, K = 128 in four K=32 steps, fp32 accumulator in a
-//           double-buffered TMEM tile;
-//   warps 2-5 epilogue: one thread per key row reads its 32*NQ accumulators
-//           with tcgen05.ld, applies scale, ReLU and the head weights, sums the
-//           heads in registers (no shuffles) and stores one fp32 score per
-//           query row (128-byte coalesced per warp).
+//   warp 0  TMA producer: per unit, four 64 x 128 B code pages (3-D tensor map
+//           over the block pool, 128-byte swizzle) and the four pages' fp32
+//           scale rows in one tile::gather4 copy, into a 5-6 stage ring; the
+//           lanes resolve the block-table rows of the next 32 units while
+//           lane 0 issues; the query tile of the current sequence goes into a
+//           2-slot ring;
+//   warp 1  MMA issuer: tcgen05.mma kind::f8f6f4, two M = 128 key sub-tiles
+//           per unit, N = 32*NQ query-heads, K = 128 in four K=32 steps, fp32
+//           accumulators in a double-buffered TMEM tile;
+//   warps 2-5 epilogue: each thread owns two key rows (one per sub-tile),
+//           reads their 32*NQ accumulators with tcgen05.ld, applies scale,
+//           ReLU and the head weights, sums the heads in registers (no
+//           shuffles) and stores one fp32 score per query row (128-byte
+//           coalesced per warp).
 // All draft rows of a sequence share one key read (AMD section: keys are
 // reused across query rows during speculative verify).
 #include <algorithm>
@@ -34,13 +38,15 @@ namespace dsa {
 
 namespace {
 
-constexpr int kStages = 8;
-constexpr int kTileKeys = 128;
-constexpr int kATileBytes = kTileKeys * kIdxDim;        // 16 KB of E4M3 codes
+constexpr int kUnitKeys = 256;                          // four pages
+constexpr int kPagesPerUnit = kUnitKeys / kBlock;       // 4
+constexpr int kSubTileBytes = 128 * kIdxDim;            // 16 KB: one M = 128 MMA tile
+constexpr int kATileBytes = kUnitKeys * kIdxDim;        // 32 KB of E4M3 codes per unit
 constexpr int kPageCodeBytes = kBlock * kIdxDim;        // 8 KB
 constexpr int kPageScaleBytes = kBlock * 4;             // 256 B
+constexpr int kUnitScaleBytes = kPagesPerUnit * kPageScaleBytes;  // 1 KB (one gather4)
 constexpr int kThreads = 192;
-constexpr int kMaxBatch = 8192;
+constexpr int kMaxBatch = 4096;
 
 struct IdxParams {
   const uint8_t* index_base;  // cache base + index_off
@@ -59,11 +65,12 @@ struct IdxParams {
 
 template <int NQ>
 struct IdxSmem {
+  static constexpr int kStages = NQ == 1 ? 6 : 5;  // keeps the CTA within 227 KB of shared memory
   static constexpr int kQSlot = 32 * NQ * kIdxDim;  // bytes
   static constexpr int kOffA = 0;
   static constexpr int kOffQ = kOffA + kStages * kATileBytes;
   static constexpr int kOffScales = kOffQ + 2 * kQSlot;
-  static constexpr int kOffBars = kOffScales + kStages * 2 * kPageScaleBytes;
+  static constexpr int kOffBars = kOffScales + kStages * kUnitScaleBytes;
   // barriers: full[S], empty[S], acc_full[2], acc_empty[2], q_full[2], q_empty[2], done
   static constexpr int kNumBars = 2 * kStages + 9;
   static constexpr int kOffMisc = kOffBars + kNumBars * 8;  // tmem slot, abort flag
@@ -77,13 +84,23 @@ __device__ __forceinline__ int seq_of_unit(const int32_t* prefix, int batch, int
   return cursor;
 }
 
+__device__ __forceinline__ void tma_gather4(uint32_t dst, const void* map, int c0, int r0, int r1, int r2, int r3,
+                                            uint32_t bar) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.tile::gather4.mbarrier::complete_tx::bytes"
+      " [%0], [%1, {%2, %3, %4, %5, %6}], [%7];"
+      ::"r"(dst), "l"(map), "r"(c0), "r"(r0), "r"(r1), "r"(r2), "r"(r3), "r"(bar)
+      : "memory");
+}
+
 template <int NQ>
 __global__ void __launch_bounds__(kThreads, 1)
-    indexer_fp8_kernel(const __grid_constant__ CUtensorMap tmap_keys, const __grid_constant__ CUtensorMap tmap_q,
-                       const IdxParams p) {
+    indexer_fp8_kernel(const __grid_constant__ CUtensorMap tmap_keys, const __grid_constant__ CUtensorMap tmap_scales,
+                       const __grid_constant__ CUtensorMap tmap_q, const IdxParams p) {
   using L = IdxSmem<NQ>;
+  constexpr int kStages = L::kStages;
   constexpr int N = 32 * NQ;
-  constexpr uint32_t kTmemCols = (2 * N <= 64) ? 64 : (2 * N <= 128 ? 128 : 256);  // power of two
+  constexpr uint32_t kTmemCols = (4 * N <= 128) ? 128 : (4 * N <= 256 ? 256 : 512);  // power of two
   constexpr uint32_t kIdesc = make_idesc(kFmtE4M3, kFmtE4M3, 0, 0, 128, N);
 
   extern __shared__ uint8_t smem_raw[];
@@ -121,6 +138,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     *abort_flag = 0;
     fence_mbar_init();
     prefetch_tmap(&tmap_keys);
+    prefetch_tmap(&tmap_scales);
     prefetch_tmap(&tmap_q);
   }
   if (warp == 1) {
@@ -138,7 +156,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           report(p.status, DSA_ERR_BOUNDS);
           len = len < 0 ? 0 : cap;
         }
-        units = (len + kTileKeys - 1) / kTileKeys;
+        units = (len + kUnitKeys - 1) / kUnitKeys;
       }
       int incl = units;
 #pragma unroll
@@ -179,33 +197,37 @@ __global__ void __launch_bounds__(kThreads, 1)
       // The lanes resolve the block-table rows of the next 32 units while lane 0
       // issues the copies of the current 32, so table reads never stall the ring.
       constexpr unsigned kAll = 0xffffffffu;
-      auto resolve = [&](int64_t g, int& rb, int& rj, int& rnp, int& r0, int& r1) {
+      auto resolve = [&](int64_t g, int& rb, int& rnp, int (&rr)[kPagesPerUnit]) {
         const int64_t u = g + lane;
-        rb = 0; rj = 0; rnp = 0; r0 = 0; r1 = 0;
+        rb = 0;
+        rnp = 0;
+#pragma unroll
+        for (int q = 0; q < kPagesPerUnit; ++q) rr[q] = 0;
         if (u < u_end) {
           rb = first_seq(u);
-          rj = (int)(u - prefix[rb]);
-          rnp = (kTileKeys * rj + kBlock < seq_len_of(rb)) ? 2 : 1;
-          const int32_t* bt = p.block_table + (int64_t)rb * p.max_blocks + 2 * rj;
-          r0 = bt[0];
-          r1 = rnp == 2 ? bt[1] : 0;
+          const int j = (int)(u - prefix[rb]);
+          const int rem = seq_len_of(rb) - kUnitKeys * j;
+          rnp = min(kPagesPerUnit, (rem + kBlock - 1) / kBlock);
+          const int32_t* bt = p.block_table + (int64_t)rb * p.max_blocks + kPagesPerUnit * j;
+#pragma unroll
+          for (int q = 0; q < kPagesPerUnit; ++q) rr[q] = q < rnp ? bt[q] : 0;
         }
       };
-      int cb, cj, cnp, c0, c1;
-      resolve(u_begin, cb, cj, cnp, c0, c1);
+      int cb, cnp, cr[kPagesPerUnit];
+      resolve(u_begin, cb, cnp, cr);
       int cur_b = -1;
       uint32_t it = 0, qn = 0;
       bool ok = true;
       for (int64_t g = u_begin; ok && g < u_end; g += 32) {
-        int nb, nj, nnp, n0, n1;
-        resolve(g + 32, nb, nj, nnp, n0, n1);  // next group's rows, in flight meanwhile
+        int nb, nnp, nr[kPagesPerUnit];
+        resolve(g + 32, nb, nnp, nr);  // next group's rows, in flight meanwhile
         const int n = (int)((u_end - g) < 32 ? (u_end - g) : 32);
         for (int l = 0; l < n; ++l, ++it) {
           const int b = __shfl_sync(kAll, cb, l);
-          const int j = __shfl_sync(kAll, cj, l);
           const int npages = __shfl_sync(kAll, cnp, l);
-          const int rr0 = __shfl_sync(kAll, c0, l);
-          const int rr1 = __shfl_sync(kAll, c1, l);
+          int r[kPagesPerUnit];
+#pragma unroll
+          for (int q = 0; q < kPagesPerUnit; ++q) r[q] = __shfl_sync(kAll, cr[q], l);
           if (lane == 0) {
             if (b != cur_b) {
               const int slot = qn & 1;
@@ -220,25 +242,29 @@ __global__ void __launch_bounds__(kThreads, 1)
             const int s = it % kStages;
             ok = ok && mbar_wait(empty_bar(s), ((it / kStages) & 1) ^ 1, abort_flag, p.status);
             if (ok) {
-              mbar_arrive_expect_tx(full_bar(s), npages * (kPageCodeBytes + kPageScaleBytes));
-              for (int pg = 0; pg < npages; ++pg) {
-                int r = pg ? rr1 : rr0;
-                if (r < 0 || r >= p.num_blocks) {
+#pragma unroll
+              for (int q = 0; q < kPagesPerUnit; ++q) {
+                if (q >= npages) r[q] = r[0];  // gather rows must be valid; unused pages repeat page 0
+                if (r[q] < 0 || r[q] >= p.num_blocks) {
                   report(p.status, DSA_ERR_BOUNDS);
-                  r = 0;  // read a valid row instead; the call's results are void
+                  r[q] = 0;  // read a valid row instead; the call's results are void
                 }
-                tma_load_3d(sbase + L::kOffA + s * kATileBytes + pg * kPageCodeBytes, &tmap_keys, 0, 0, r,
-                            full_bar(s));
-                bulk_load(sbase + L::kOffScales + s * 2 * kPageScaleBytes + pg * kPageScaleBytes,
-                          p.index_base + (int64_t)r * p.row_stride + kPageCodeBytes, kPageScaleBytes, full_bar(s));
               }
+              mbar_arrive_expect_tx(full_bar(s), npages * kPageCodeBytes + kUnitScaleBytes);
+              for (int q = 0; q < npages; ++q)
+                tma_load_3d(sbase + L::kOffA + s * kATileBytes + q * kPageCodeBytes, &tmap_keys, 0, 0, r[q],
+                            full_bar(s));
+              tma_gather4(sbase + L::kOffScales + s * kUnitScaleBytes, &tmap_scales, 0, r[0], r[1], r[2], r[3],
+                          full_bar(s));
             }
           }
           ok = __shfl_sync(kAll, ok, 0);
           if (!ok) break;
-          (void)j;
         }
-        cb = nb; cj = nj; cnp = nnp; c0 = n0; c1 = n1;
+        cb = nb;
+        cnp = nnp;
+#pragma unroll
+        for (int q = 0; q < kPagesPerUnit; ++q) cr[q] = nr[q];
       }
       if (lane == 0 && *abort_flag) {  // let copies already in flight land before the CTA exits
         for (uint32_t k = (it > kStages ? it - kStages : 0); k < it; ++k)
@@ -260,13 +286,16 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (!mbar_wait(full_bar(s), (it / kStages) & 1, abort_flag, p.status)) break;
         if (!mbar_wait(acce_bar(a), ((it >> 1) & 1) ^ 1, abort_flag, p.status)) break;
         tc_fence_after();
-        const uint32_t a_base = sbase + L::kOffA + s * kATileBytes;
         const uint32_t b_base = sbase + L::kOffQ + ((qn - 1) & 1) * L::kQSlot;
 #pragma unroll
-        for (int kk = 0; kk < kIdxDim / 32; ++kk) {
-          const uint64_t ad = smem_desc(a_base + 32 * kk, 16, 1024, kLayoutSw128);
-          const uint64_t bd = smem_desc(b_base + 32 * kk, 16, 1024, kLayoutSw128);
-          mma_f8f6f4(tmem + a * N, ad, bd, kIdesc, kk > 0 ? 1u : 0u);
+        for (int sub = 0; sub < 2; ++sub) {
+          const uint32_t a_base = sbase + L::kOffA + s * kATileBytes + sub * kSubTileBytes;
+#pragma unroll
+          for (int kk = 0; kk < kIdxDim / 32; ++kk) {
+            const uint64_t ad = smem_desc(a_base + 32 * kk, 16, 1024, kLayoutSw128);
+            const uint64_t bd = smem_desc(b_base + 32 * kk, 16, 1024, kLayoutSw128);
+            mma_f8f6f4(tmem + (2 * a + sub) * N, ad, bd, kIdesc, kk > 0 ? 1u : 0u);
+          }
         }
         mma_commit(accf_bar(a));
       }
@@ -276,7 +305,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     } else if (warp >= 2) {
       // ------------------------------------------------ epilogue
       const int quarter = warp & 3;
-      const int row = quarter * 32 + lane;  // key row of the tile = TMEM lane
+      const int row = quarter * 32 + lane;  // TMEM lane = key row of each 128-key sub-tile
       int cursor = first_seq(u_begin), cur_b = -1;
       float w[NQ][kIdxHeads];
       uint32_t it = 0;
@@ -304,17 +333,26 @@ __global__ void __launch_bounds__(kThreads, 1)
         tc_fence_after();
         const int j = (int)(u - prefix[b]);
         const int len = seq_len_of(b);
-        const int t = kTileKeys * j + row;
-        const float scale = scales_smem[s * 2 * kBlock + row];
+        const int t0 = kUnitKeys * j + row, t1 = t0 + 128;
+        const float sc0 = scales_smem[s * (kUnitScaleBytes / 4) + row];
+        const float sc1 = scales_smem[s * (kUnitScaleBytes / 4) + 128 + row];
+        const uint32_t lane_base = tmem + ((uint32_t)(quarter * 32) << 16);
 #pragma unroll
         for (int q = 0; q < NQ; ++q) {
-          uint32_t r[32];
-          tmem_ld32(tmem + ((uint32_t)(quarter * 32) << 16) + a * N + 32 * q, r);
+          uint32_t r0[32], r1[32];
+          tmem_ld32(lane_base + (2 * a) * N + 32 * q, r0);
+          tmem_ld32(lane_base + (2 * a + 1) * N + 32 * q, r1);
           tmem_ld_wait();
-          float sc = 0.f;
+          float s0 = 0.f, s1 = 0.f;
 #pragma unroll
-          for (int h = 0; h < kIdxHeads; ++h) sc = fmaf(w[q][h], fmaxf(scale * __uint_as_float(r[h]), 0.f), sc);
-          if (t < visible_len(len, NQ, q)) p.scores[((int64_t)b * NQ + q) * p.ld + t] = sc;
+          for (int h = 0; h < kIdxHeads; ++h) {
+            s0 = fmaf(w[q][h], fmaxf(sc0 * __uint_as_float(r0[h]), 0.f), s0);
+            s1 = fmaf(w[q][h], fmaxf(sc1 * __uint_as_float(r1[h]), 0.f), s1);
+          }
+          const int vis = visible_len(len, NQ, q);
+          float* out = p.scores + ((int64_t)b * NQ + q) * p.ld;
+          if (t0 < vis) out[t0] = s0;
+          if (t1 < vis) out[t1] = s1;
         }
         tc_fence_before();
         __syncwarp();
@@ -332,7 +370,8 @@ __global__ void __launch_bounds__(kThreads, 1)
 }
 
 template <int NQ>
-dsa_status_t launch_nq(const IdxParams& p, const CUtensorMap& keys, const CUtensorMap& q, cudaStream_t st) {
+dsa_status_t launch_nq(const IdxParams& p, const CUtensorMap& keys, const CUtensorMap& scales,
+                       const CUtensorMap& q, cudaStream_t st) {
   static bool attr_set[64] = {};
   int dev = 0;
   cudaGetDevice(&dev);
@@ -343,9 +382,9 @@ dsa_status_t launch_nq(const IdxParams& p, const CUtensorMap& keys, const CUtens
       return DSA_ERR_CUDA;
     attr_set[dev] = true;
   }
-  const int64_t units_bound = (int64_t)p.batch * ((p.max_seq_len + kTileKeys - 1) / kTileKeys);
+  const int64_t units_bound = (int64_t)p.batch * ((p.max_seq_len + kUnitKeys - 1) / kUnitKeys);
   const int grid = (int)std::max<int64_t>(1, std::min<int64_t>(units_bound, num_sms()));
-  indexer_fp8_kernel<NQ><<<grid, kThreads, IdxSmem<NQ>::bytes(p.batch), st>>>(keys, q, p);
+  indexer_fp8_kernel<NQ><<<grid, kThreads, IdxSmem<NQ>::bytes(p.batch), st>>>(keys, scales, q, p);
   return launch_status();
 }
 
@@ -356,14 +395,23 @@ dsa_status_t launch_index_scores_fp8(const dsa_paged_cache_t& c, const dsa_batch
                                      cudaStream_t st) {
   if (bt.batch > kMaxBatch) return DSA_ERR_UNSUPPORTED;
   const uint8_t* index_base = static_cast<const uint8_t*>(c.base) + c.index_off;
-  CUtensorMap keys, qmap;
-  // keys: the pool as [num_blocks][64 tokens][128 B], one 64x128 box per page
+  CUtensorMap keys, scales, qmap;
+  // codes: the pool as [num_blocks][64 tokens][128 B], one 64 x 128 box per page
   {
     const uint64_t dims[3] = {(uint64_t)kIdxDim, (uint64_t)kBlock, (uint64_t)c.num_blocks};
     const uint64_t strides[2] = {(uint64_t)kIdxDim, (uint64_t)c.row_stride};
     const uint32_t box[3] = {(uint32_t)kIdxDim, (uint32_t)kBlock, 1};
     if (!encode_tmap(&keys, CU_TENSOR_MAP_DATA_TYPE_UINT8, 3, index_base, dims, strides, box,
                      CU_TENSOR_MAP_SWIZZLE_128B))
+      return DSA_ERR_CUDA;
+  }
+  // scales: the pool as [num_blocks][256 B of fp32 scales], one-row boxes for gather4
+  {
+    const uint64_t dims[2] = {(uint64_t)kPageScaleBytes, (uint64_t)c.num_blocks};
+    const uint64_t strides[1] = {(uint64_t)c.row_stride};
+    const uint32_t box[2] = {(uint32_t)kPageScaleBytes, 1};
+    if (!encode_tmap(&scales, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, index_base + kPageCodeBytes, dims, strides, box,
+                     CU_TENSOR_MAP_SWIZZLE_NONE))
       return DSA_ERR_CUDA;
   }
   const int nq = bt.queries_per_seq;
@@ -379,10 +427,10 @@ dsa_status_t launch_index_scores_fp8(const dsa_paged_cache_t& c, const dsa_batch
   IdxParams p{index_base, c.row_stride, c.num_blocks, bt.block_table, bt.max_blocks_per_seq, bt.seq_lens,
               bt.batch, bt.max_seq_len, head_w, scores, ld, status};
   switch (nq) {
-    case 1: return launch_nq<1>(p, keys, qmap, st);
-    case 2: return launch_nq<2>(p, keys, qmap, st);
-    case 3: return launch_nq<3>(p, keys, qmap, st);
-    case 4: return launch_nq<4>(p, keys, qmap, st);
+    case 1: return launch_nq<1>(p, keys, scales, qmap, st);
+    case 2: return launch_nq<2>(p, keys, scales, qmap, st);
+    case 3: return launch_nq<3>(p, keys, scales, qmap, st);
+    case 4: return launch_nq<4>(p, keys, scales, qmap, st);
     default: return DSA_ERR_UNSUPPORTED;
   }
 }

@@ -37,6 +37,7 @@ constexpr int kThreads = 256;
 constexpr int kCandCap = 8192;        // candidates kept per row
 constexpr int kFinalThreads = 512;
 constexpr int kWindowBits = 1 << 20;  // bitmap window of the final sort (128 KB)
+constexpr int kVecPerThread = kSeg / 4 / kThreads;  // float4 loads per thread and segment
 
 struct TopkWs {
   uint32_t* hist;    // [rows][kBins]
@@ -110,12 +111,20 @@ __global__ void __launch_bounds__(kThreads) topk_hist_kernel(const float* __rest
   const float* row = scores + (int64_t)r * ld + t0;
   const int n4 = n >> 2;
   const float4* row4 = reinterpret_cast<const float4*>(row);
-  for (int i = threadIdx.x; i < n4; i += kThreads) {
-    float4 v = row4[i];
-    atomicAdd(&h[score_key(v.x) >> 20], 1u);
-    atomicAdd(&h[score_key(v.y) >> 20], 1u);
-    atomicAdd(&h[score_key(v.z) >> 20], 1u);
-    atomicAdd(&h[score_key(v.w) >> 20], 1u);
+  float4 v[kVecPerThread];  // every load of this thread in flight before the first use
+#pragma unroll
+  for (int c = 0; c < kVecPerThread; ++c) {
+    const int i = threadIdx.x + c * kThreads;
+    v[c] = i < n4 ? row4[i] : make_float4(0.f, 0.f, 0.f, 0.f);
+  }
+#pragma unroll
+  for (int c = 0; c < kVecPerThread; ++c) {
+    if (threadIdx.x + c * kThreads < n4) {
+      atomicAdd(&h[score_key(v[c].x) >> 20], 1u);
+      atomicAdd(&h[score_key(v[c].y) >> 20], 1u);
+      atomicAdd(&h[score_key(v[c].z) >> 20], 1u);
+      atomicAdd(&h[score_key(v[c].w) >> 20], 1u);
+    }
   }
   for (int i = 4 * n4 + threadIdx.x; i < n; i += kThreads) atomicAdd(&h[score_key(row[i]) >> 20], 1u);
   __syncthreads();
@@ -129,7 +138,7 @@ __global__ void __launch_bounds__(kThreads) topk_collect_kernel(const float* __r
                                                                  int nq, int cap, int k, TopkWs ws,
                                                                  int32_t* status) {
   __shared__ uint32_t sums[kThreads];
-  __shared__ uint32_t keys[kSeg];
+  __shared__ __align__(16) uint32_t keys[kSeg];
   __shared__ uint32_t s_cnt[2], s_base[2];
   const int r = blockIdx.y;
   const int len = row_len(row_lens, seq_lens, nq, r, cap, nullptr);
@@ -145,12 +154,35 @@ __global__ void __launch_bounds__(kThreads) topk_collect_kernel(const float* __r
   __syncthreads();
   // pass 1: keys into shared memory, count this CTA's selected and candidate entries
   uint32_t ns = 0, nc = 0;
-  for (int i = threadIdx.x; i < n; i += kThreads) {
-    const uint32_t key = score_key(row[i]);
-    keys[i] = key;
-    const int bin = (int)(key >> 20);
-    ns += bin > T;
-    nc += bin == T;
+  {
+    const int n4 = n >> 2;
+    const float4* row4 = reinterpret_cast<const float4*>(row);
+    float4 v[kVecPerThread];
+#pragma unroll
+    for (int c = 0; c < kVecPerThread; ++c) {
+      const int i = threadIdx.x + c * kThreads;
+      v[c] = i < n4 ? row4[i] : make_float4(0.f, 0.f, 0.f, 0.f);
+    }
+#pragma unroll
+    for (int c = 0; c < kVecPerThread; ++c) {
+      const int i = threadIdx.x + c * kThreads;
+      if (i < n4) {
+        const uint4 kk = make_uint4(score_key(v[c].x), score_key(v[c].y), score_key(v[c].z), score_key(v[c].w));
+        reinterpret_cast<uint4*>(keys)[i] = kk;
+        const uint32_t e[4] = {kk.x, kk.y, kk.z, kk.w};
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+          ns += (int)(e[q] >> 20) > T;
+          nc += (int)(e[q] >> 20) == T;
+        }
+      }
+    }
+    for (int i = 4 * n4 + threadIdx.x; i < n; i += kThreads) {
+      const uint32_t key = score_key(row[i]);
+      keys[i] = key;
+      ns += (int)(key >> 20) > T;
+      nc += (int)(key >> 20) == T;
+    }
   }
 #pragma unroll
   for (int o = 16; o; o >>= 1) {
@@ -288,13 +320,41 @@ __global__ void __launch_bounds__(kFinalThreads) topk_final_kernel(const float* 
     return;
   }
   uint32_t need = (uint32_t)k - n_sel;
-  for (int i = tid; i < (int)n_sel; i += kFinalThreads) chosen[i] = ws.sel[(int64_t)r * k + i];
+  {  // four loads in flight per thread
+    const int32_t* gs = ws.sel + (int64_t)r * k;
+    for (int i0 = 0; i0 < (int)n_sel; i0 += 4 * kFinalThreads) {
+      int32_t v[4];
+#pragma unroll
+      for (int c = 0; c < 4; ++c) {
+        const int i = i0 + c * kFinalThreads + tid;
+        v[c] = i < (int)n_sel ? gs[i] : 0;
+      }
+#pragma unroll
+      for (int c = 0; c < 4; ++c) {
+        const int i = i0 + c * kFinalThreads + tid;
+        if (i < (int)n_sel) chosen[i] = v[c];
+      }
+    }
+  }
   const bool overflow = n_cand > (uint32_t)kCandCap;
   const uint64_t* gcand = ws.cand + (int64_t)r * kCandCap;
   const int T = (int)(gcand[0] >> 52);  // threshold bin: top 12 key bits shared by every candidate
   const float* row = scores + (int64_t)r * ld;
-  if (!overflow)
-    for (uint32_t i = tid; i < n_cand; i += kFinalThreads) cand[i] = gcand[i];
+  if (!overflow) {
+    for (uint32_t i0 = 0; i0 < n_cand; i0 += 4 * kFinalThreads) {
+      uint64_t v[4];
+#pragma unroll
+      for (int c = 0; c < 4; ++c) {
+        const uint32_t i = i0 + c * kFinalThreads + tid;
+        v[c] = i < n_cand ? gcand[i] : 0;
+      }
+#pragma unroll
+      for (int c = 0; c < 4; ++c) {
+        const uint32_t i = i0 + c * kFinalThreads + tid;
+        if (i < n_cand) cand[i] = v[c];
+      }
+    }
+  }
   __syncthreads();
 
   // ---- the `need` largest packed values v = (key << 32) | ~index among the
