@@ -10,11 +10,12 @@
 // Scores are compared as order-preserving 32-bit keys (integer radix).
 //   1. hist:    multi-CTA per row: 4096-bin histogram of the key's top 12
 //               bits, merged into a per-row global histogram.
-//   2. collect: multi-CTA per row: every CTA finds the threshold bin T
-//               (the bin holding the k-th largest key) from the histogram and
-//               scans its segment: keys above T are selected outright (fewer
-//               than k of them); keys in T become candidates (key, index).
-//   3. final:   one CTA per row: radix-selects the remaining (k - selected)
+//   2. threshold: one CTA per row finds the bin T holding the k-th largest
+//               key and the count above it.
+//   3. collect: multi-CTA per row: every CTA scans its segment: keys above T
+//               are selected outright (fewer than k of them); keys in T become
+//               candidates (key, index), reserved with one atomic per CTA.
+//   4. final:   one CTA per row: radix-selects the remaining (k - selected)
 //               candidates by (key desc, index asc) on 52 packed bits, then
 //               writes the chosen indices in ascending order through a
 //               shared-memory bitmap of the index range.  If the candidate
@@ -56,47 +57,6 @@ __device__ __forceinline__ int row_len(const int32_t* row_lens, const int32_t* s
   return len;
 }
 
-// Threshold bin of a row from its 4096-bin histogram: the largest T with
-// sum_{b >= T} hist[b] >= k.  Also returns the count strictly above T.
-// Block-wide; every thread gets the result.
-__device__ void find_threshold(const uint32_t* hist_g, int k, uint32_t* sh_sums, int& T, uint32_t& above) {
-  const int tid = threadIdx.x;
-  constexpr int per = kBins / kThreads;  // 16 bins per thread, thread 0 owns the top bins
-  uint32_t local[per];
-  uint32_t sum = 0;
-#pragma unroll
-  for (int i = 0; i < per; ++i) {
-    local[i] = hist_g[kBins - 1 - (tid * per + i)];  // descending bin order
-    sum += local[i];
-  }
-  sh_sums[tid] = sum;
-  __syncthreads();
-  // inclusive prefix over threads (descending bins)
-  for (int o = 1; o < kThreads; o <<= 1) {
-    uint32_t v = tid >= o ? sh_sums[tid - o] : 0;
-    __syncthreads();
-    sh_sums[tid] += v;
-    __syncthreads();
-  }
-  const uint32_t incl = sh_sums[tid], excl = incl - sum;
-  __shared__ int sh_T;
-  __shared__ uint32_t sh_above;
-  if (excl < (uint32_t)k && incl >= (uint32_t)k) {
-    uint32_t run = excl;
-    for (int i = 0; i < per; ++i) {
-      if (run + local[i] >= (uint32_t)k) {
-        sh_T = kBins - 1 - (tid * per + i);
-        sh_above = run;
-        break;
-      }
-      run += local[i];
-    }
-  }
-  __syncthreads();
-  T = sh_T;
-  above = sh_above;
-}
-
 __global__ void __launch_bounds__(kThreads) topk_hist_kernel(const float* __restrict__ scores, int64_t ld,
                                                               const int32_t* row_lens, const int32_t* seq_lens,
                                                               int nq, int cap, int k, TopkWs ws, int32_t* status) {
@@ -133,97 +93,146 @@ __global__ void __launch_bounds__(kThreads) topk_hist_kernel(const float* __rest
     if (h[i]) atomicAdd(&g[i], h[i]);
 }
 
+// Per row: the threshold bin T of the first digit (the bin holding the k-th
+// largest key) and the count strictly above it, from the row's histogram;
+// T = -1 for rows with at most k tokens.  Written to counts[r][2..3].
+__global__ void __launch_bounds__(kThreads) topk_threshold_kernel(const int32_t* row_lens, const int32_t* seq_lens,
+                                                                   int nq, int cap, int k, TopkWs ws) {
+  __shared__ uint32_t wsum[kThreads / 32];
+  const int r = blockIdx.x, tid = threadIdx.x, lane = tid & 31, wid = tid >> 5;
+  const int len = row_len(row_lens, seq_lens, nq, r, cap, nullptr);
+  uint32_t* cnt = ws.counts + 4 * (int64_t)r;
+  if (len <= k) {
+    if (tid == 0) cnt[2] = 0xFFFFFFFFu;
+    return;
+  }
+  constexpr int per = kBins / kThreads;  // 16 consecutive bins per thread
+  uint32_t h[per];
+  const uint4* src = reinterpret_cast<const uint4*>(ws.hist + (int64_t)r * kBins + tid * per);
+#pragma unroll
+  for (int c = 0; c < per / 4; ++c) {
+    const uint4 v = src[c];
+    h[4 * c] = v.x; h[4 * c + 1] = v.y; h[4 * c + 2] = v.z; h[4 * c + 3] = v.w;
+  }
+  uint32_t sum = 0;
+#pragma unroll
+  for (int i = 0; i < per; ++i) sum += h[i];
+  uint32_t incl = sum;  // inclusive prefix over threads (ascending bins)
+#pragma unroll
+  for (int d = 1; d < 32; d <<= 1) {
+    const uint32_t u = __shfl_up_sync(0xffffffffu, incl, d);
+    if (lane >= d) incl += u;
+  }
+  if (lane == 31) wsum[wid] = incl;
+  __syncthreads();
+  uint32_t before = 0, total = 0;
+  for (int w = 0; w < kThreads / 32; ++w) {
+    if (w < wid) before += wsum[w];
+    total += wsum[w];
+  }
+  incl += before;
+  const uint32_t above_mine = total - incl;  // keys in bins above this thread's range
+  if (above_mine < (uint32_t)k && above_mine + sum >= (uint32_t)k) {
+    uint32_t run = above_mine;
+    for (int i = per - 1; i >= 0; --i) {
+      if (run + h[i] >= (uint32_t)k) {
+        cnt[2] = (uint32_t)(tid * per + i);
+        cnt[3] = run;
+        break;
+      }
+      run += h[i];
+    }
+  }
+}
+
+// Block-wide exclusive scan of one value per thread (kThreads threads).
+__device__ __forceinline__ uint32_t cta_excl_scan(uint32_t v, uint32_t* sh, uint32_t& total) {
+  const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5;
+  uint32_t incl = v;
+#pragma unroll
+  for (int d = 1; d < 32; d <<= 1) {
+    const uint32_t u = __shfl_up_sync(0xffffffffu, incl, d);
+    if (lane >= d) incl += u;
+  }
+  if (lane == 31) sh[wid] = incl;
+  __syncthreads();
+  uint32_t before = 0;
+  total = 0;
+#pragma unroll
+  for (int w = 0; w < kThreads / 32; ++w) {
+    const uint32_t x = sh[w];
+    before += w < wid ? x : 0u;
+    total += x;
+  }
+  return before + incl - v;
+}
+
+// Each thread owns 32 consecutive tokens of the CTA's segment: it loads them
+// (8 x 16 B), keys them in registers, and the CTA places its selected and
+// candidate tokens with two block scans and one global reservation per list.
 __global__ void __launch_bounds__(kThreads) topk_collect_kernel(const float* __restrict__ scores, int64_t ld,
                                                                  const int32_t* row_lens, const int32_t* seq_lens,
                                                                  int nq, int cap, int k, TopkWs ws,
                                                                  int32_t* status) {
-  __shared__ uint32_t sums[kThreads];
-  __shared__ __align__(16) uint32_t keys[kSeg];
-  __shared__ uint32_t s_cnt[2], s_base[2];
+  constexpr int kPer = kSeg / kThreads;  // 32 tokens per thread
+  __shared__ uint32_t sh_s[kThreads / 32], sh_c[kThreads / 32];
+  __shared__ uint32_t s_base[2];
   const int r = blockIdx.y;
   const int len = row_len(row_lens, seq_lens, nq, r, cap, nullptr);
   const int64_t t0 = (int64_t)blockIdx.x * kSeg;
   if (len <= k || t0 >= len) return;
-  int T;
-  uint32_t above;
-  find_threshold(ws.hist + (int64_t)r * kBins, k, sums, T, above);
+  const int T = (int)ws.counts[4 * (int64_t)r + 2];
   const int n = (int)std::min<int64_t>(kSeg, len - t0);
+  const int i0 = threadIdx.x * kPer;  // first token of this thread, relative to t0
   const float* row = scores + (int64_t)r * ld + t0;
-  const int lane = threadIdx.x & 31;
-  if (threadIdx.x < 2) s_cnt[threadIdx.x] = 0;
-  __syncthreads();
-  // pass 1: keys into shared memory, count this CTA's selected and candidate entries
+  uint32_t key[kPer];
+  if (i0 + kPer <= n) {
+    const float4* src = reinterpret_cast<const float4*>(row + i0);
+#pragma unroll
+    for (int c = 0; c < kPer / 4; ++c) {
+      const float4 v = src[c];
+      key[4 * c] = score_key(v.x);
+      key[4 * c + 1] = score_key(v.y);
+      key[4 * c + 2] = score_key(v.z);
+      key[4 * c + 3] = score_key(v.w);
+    }
+  } else {
+#pragma unroll
+    for (int c = 0; c < kPer; ++c) key[c] = (i0 + c < n) ? score_key(row[i0 + c]) : 0u;
+  }
   uint32_t ns = 0, nc = 0;
-  {
-    const int n4 = n >> 2;
-    const float4* row4 = reinterpret_cast<const float4*>(row);
-    float4 v[kVecPerThread];
 #pragma unroll
-    for (int c = 0; c < kVecPerThread; ++c) {
-      const int i = threadIdx.x + c * kThreads;
-      v[c] = i < n4 ? row4[i] : make_float4(0.f, 0.f, 0.f, 0.f);
-    }
-#pragma unroll
-    for (int c = 0; c < kVecPerThread; ++c) {
-      const int i = threadIdx.x + c * kThreads;
-      if (i < n4) {
-        const uint4 kk = make_uint4(score_key(v[c].x), score_key(v[c].y), score_key(v[c].z), score_key(v[c].w));
-        reinterpret_cast<uint4*>(keys)[i] = kk;
-        const uint32_t e[4] = {kk.x, kk.y, kk.z, kk.w};
-#pragma unroll
-        for (int q = 0; q < 4; ++q) {
-          ns += (int)(e[q] >> 20) > T;
-          nc += (int)(e[q] >> 20) == T;
-        }
-      }
-    }
-    for (int i = 4 * n4 + threadIdx.x; i < n; i += kThreads) {
-      const uint32_t key = score_key(row[i]);
-      keys[i] = key;
-      ns += (int)(key >> 20) > T;
-      nc += (int)(key >> 20) == T;
-    }
+  for (int c = 0; c < kPer; ++c) {
+    const bool valid = i0 + c < n;
+    const int bin = (int)(key[c] >> 20);
+    ns += (valid && bin > T);
+    nc += (valid && bin == T);
   }
-#pragma unroll
-  for (int o = 16; o; o >>= 1) {
-    ns += __shfl_xor_sync(0xffffffffu, ns, o);
-    nc += __shfl_xor_sync(0xffffffffu, nc, o);
-  }
-  if (lane == 0) {
-    if (ns) atomicAdd(&s_cnt[0], ns);
-    if (nc) atomicAdd(&s_cnt[1], nc);
-  }
-  __syncthreads();
+  uint32_t tot_s, tot_c;
+  const uint32_t off_s = cta_excl_scan(ns, sh_s, tot_s);
+  const uint32_t off_c = cta_excl_scan(nc, sh_c, tot_c);
   uint32_t* cnt = ws.counts + 4 * (int64_t)r;
-  if (threadIdx.x == 0) {  // one global reservation per counter per CTA
-    s_base[0] = s_cnt[0] ? atomicAdd(&cnt[0], s_cnt[0]) : 0;
-    s_base[1] = s_cnt[1] ? atomicAdd(&cnt[1], s_cnt[1]) : 0;
-    s_cnt[0] = s_cnt[1] = 0;
+  if (threadIdx.x == 0) {  // one global reservation per list per CTA
+    s_base[0] = tot_s ? atomicAdd(&cnt[0], tot_s) : 0u;
+    s_base[1] = tot_c ? atomicAdd(&cnt[1], tot_c) : 0u;
   }
   __syncthreads();
-  // pass 2: write the entries into the reserved ranges (order inside a range is free)
-  int32_t* sel = ws.sel + (int64_t)r * k;
-  uint64_t* cand = ws.cand + (int64_t)r * kCandCap;
-  for (int base = 0; base < n; base += kThreads) {
-    const int i = base + threadIdx.x;
-    const uint32_t key = i < n ? keys[i] : 0u;
-    const int bin = i < n ? (int)(key >> 20) : -1;
-    const uint32_t ms = __ballot_sync(0xffffffffu, bin > T);
-    const uint32_t mc = __ballot_sync(0xffffffffu, bin == T);
-    uint32_t ws_ = 0, wc = 0;
-    if (lane == 0) {
-      if (ms) ws_ = atomicAdd(&s_cnt[0], (uint32_t)__popc(ms));
-      if (mc) wc = atomicAdd(&s_cnt[1], (uint32_t)__popc(mc));
-    }
-    ws_ = __shfl_sync(0xffffffffu, ws_, 0);
-    wc = __shfl_sync(0xffffffffu, wc, 0);
-    const uint32_t below = (1u << lane) - 1;
-    if (bin > T) {
-      const uint32_t ps = s_base[0] + ws_ + __popc(ms & below);
-      if (ps < (uint32_t)k) sel[ps] = (int32_t)(t0 + i);
-    } else if (bin == T) {
-      const uint32_t pc = s_base[1] + wc + __popc(mc & below);
-      if (pc < (uint32_t)kCandCap) cand[pc] = ((uint64_t)key << 32) | (uint64_t)(0xFFFFFFFFu - (uint32_t)(t0 + i));
+  if (ns | nc) {
+    uint32_t ps = s_base[0] + off_s, pc = s_base[1] + off_c;
+    int32_t* sel = ws.sel + (int64_t)r * k;
+    uint64_t* cand = ws.cand + (int64_t)r * kCandCap;
+#pragma unroll
+    for (int c = 0; c < kPer; ++c) {
+      const bool valid = i0 + c < n;
+      const int bin = (int)(key[c] >> 20);
+      const uint32_t t = (uint32_t)(t0 + i0 + c);
+      if (valid && bin > T) {
+        if (ps < (uint32_t)k) sel[ps] = (int32_t)t;
+        ++ps;
+      } else if (valid && bin == T) {
+        if (pc < (uint32_t)kCandCap) cand[pc] = ((uint64_t)key[c] << 32) | (uint64_t)(0xFFFFFFFFu - t);
+        ++pc;
+      }
     }
   }
 }
@@ -296,13 +305,12 @@ __global__ void __launch_bounds__(kFinalThreads) topk_final_kernel(const float* 
                                                                     const int32_t* seq_lens, int nq, int cap, int k,
                                                                     TopkWs ws, int32_t* out, int32_t* status) {
   extern __shared__ uint8_t smem_raw[];
-  // chosen[kMaxTopk] i32 | hist[kBins] u32 | scan[32] u32 | union{ cand[kCandCap] u64, bitmap[kWindowBits/32] }
-  int32_t* chosen = reinterpret_cast<int32_t*>(smem_raw);
-  uint32_t* hist = reinterpret_cast<uint32_t*>(smem_raw + 4 * kMaxTopk);
+  // bitmap[kWindowBits/32] u32 | cand[kCandCap] u64 | chosen[kMaxTopk] i32 | hist[kBins] u32 | scan[32] u32
+  uint32_t* bitmap = reinterpret_cast<uint32_t*>(smem_raw);
+  uint64_t* cand = reinterpret_cast<uint64_t*>(smem_raw + kWindowBits / 8);
+  int32_t* chosen = reinterpret_cast<int32_t*>(smem_raw + kWindowBits / 8 + 8 * kCandCap);
+  uint32_t* hist = reinterpret_cast<uint32_t*>(smem_raw + kWindowBits / 8 + 8 * kCandCap + 4 * kMaxTopk);
   uint32_t* scan = hist + kBins;
-  uint8_t* big = smem_raw + 4 * kMaxTopk + 4 * kBins + 128;
-  uint64_t* cand = reinterpret_cast<uint64_t*>(big);
-  uint32_t* bitmap = reinterpret_cast<uint32_t*>(big);
   __shared__ uint32_t s_count;
 
   const int r = blockIdx.x, tid = threadIdx.x;
@@ -314,34 +322,20 @@ __global__ void __launch_bounds__(kFinalThreads) topk_final_kernel(const float* 
   }
   const uint32_t* cnt = ws.counts + 4 * (int64_t)r;
   const uint32_t n_sel = cnt[0], n_cand = cnt[1];
+  const int T = (int)cnt[2];
   if (n_sel >= (uint32_t)k || n_cand == 0) {  // impossible with a consistent histogram
     report(status, DSA_ERR_BOUNDS);
     for (int i = tid; i < k; i += kFinalThreads) o[i] = -1;
     return;
   }
-  uint32_t need = (uint32_t)k - n_sel;
-  {  // four loads in flight per thread
-    const int32_t* gs = ws.sel + (int64_t)r * k;
-    for (int i0 = 0; i0 < (int)n_sel; i0 += 4 * kFinalThreads) {
-      int32_t v[4];
-#pragma unroll
-      for (int c = 0; c < 4; ++c) {
-        const int i = i0 + c * kFinalThreads + tid;
-        v[c] = i < (int)n_sel ? gs[i] : 0;
-      }
-#pragma unroll
-      for (int c = 0; c < 4; ++c) {
-        const int i = i0 + c * kFinalThreads + tid;
-        if (i < (int)n_sel) chosen[i] = v[c];
-      }
-    }
-  }
+  // rows up to one bitmap window set their bits directly; longer rows collect a list first
+  const bool direct = len <= kWindowBits;
+  const int words0 = direct ? (len + 31) >> 5 : 0;
+  for (int i = tid; i < words0; i += kFinalThreads) bitmap[i] = 0;
   const bool overflow = n_cand > (uint32_t)kCandCap;
   const uint64_t* gcand = ws.cand + (int64_t)r * kCandCap;
-  const int T = (int)(gcand[0] >> 52);  // threshold bin: top 12 key bits shared by every candidate
-  const float* row = scores + (int64_t)r * ld;
   if (!overflow) {
-    for (uint32_t i0 = 0; i0 < n_cand; i0 += 4 * kFinalThreads) {
+    for (uint32_t i0 = 0; i0 < n_cand; i0 += 4 * kFinalThreads) {  // four loads in flight per thread
       uint64_t v[4];
 #pragma unroll
       for (int c = 0; c < 4; ++c) {
@@ -356,6 +350,27 @@ __global__ void __launch_bounds__(kFinalThreads) topk_final_kernel(const float* 
     }
   }
   __syncthreads();
+  {
+    const int32_t* gs = ws.sel + (int64_t)r * k;
+    for (int i0 = 0; i0 < (int)n_sel; i0 += 4 * kFinalThreads) {
+      int32_t v[4];
+#pragma unroll
+      for (int c = 0; c < 4; ++c) {
+        const int i = i0 + c * kFinalThreads + tid;
+        v[c] = i < (int)n_sel ? gs[i] : 0;
+      }
+#pragma unroll
+      for (int c = 0; c < 4; ++c) {
+        const int i = i0 + c * kFinalThreads + tid;
+        if (i < (int)n_sel) {
+          if (direct) atomicOr(&bitmap[v[c] >> 5], 1u << (v[c] & 31));
+          else chosen[i] = v[c];
+        }
+      }
+    }
+  }
+  uint32_t need = (uint32_t)k - n_sel;
+  const float* row = scores + (int64_t)r * ld;
 
   // ---- the `need` largest packed values v = (key << 32) | ~index among the
   //      candidates: 12-bit digits of bits 51..0 (bits 63..52 equal T), stopping
@@ -392,44 +407,48 @@ __global__ void __launch_bounds__(kFinalThreads) topk_final_kernel(const float* 
     shift = nshift;
     if (need == pop) break;  // the whole bin is taken: select by prefix
   }
-  // chosen += candidates whose bits 51..shift are >= prefix
+  // candidates whose bits 51..shift are >= prefix complete the selection
   if (tid == 0) s_count = n_sel;
   __syncthreads();
+  auto take = [&](int32_t t) {
+    if (direct) {
+      atomicOr(&bitmap[t >> 5], 1u << (t & 31));
+    } else {
+      const uint32_t pos = atomicAdd(&s_count, 1u);
+      if (pos < (uint32_t)k) chosen[pos] = t;
+    }
+  };
   if (!overflow) {
     for (uint32_t i = tid; i < n_cand; i += kFinalThreads) {
       const uint64_t v = cand[i] & ((1ull << 52) - 1);
-      if ((v >> shift) >= prefix) {
-        const uint32_t pos = atomicAdd(&s_count, 1u);
-        if (pos < (uint32_t)k) chosen[pos] = (int32_t)(0xFFFFFFFFu - (uint32_t)cand[i]);
-      }
+      if ((v >> shift) >= prefix) take((int32_t)(0xFFFFFFFFu - (uint32_t)cand[i]));
     }
   } else {
     for (int t = tid; t < len; t += kFinalThreads) {
       const uint64_t full = packed(t);
       if ((int)(full >> 52) != T) continue;
-      if (((full & ((1ull << 52) - 1)) >> shift) >= prefix) {
-        const uint32_t pos = atomicAdd(&s_count, 1u);
-        if (pos < (uint32_t)k) chosen[pos] = t;
-      }
+      if (((full & ((1ull << 52) - 1)) >> shift) >= prefix) take(t);
     }
   }
   __syncthreads();
-  if (s_count != (uint32_t)k) report(status, DSA_ERR_BOUNDS);  // internal consistency check
-  const int nchosen = (int)std::min<uint32_t>(s_count, (uint32_t)k);
+  const int nchosen = direct ? k : (int)std::min<uint32_t>(s_count, (uint32_t)k);
+  if (!direct && s_count != (uint32_t)k) report(status, DSA_ERR_BOUNDS);  // internal consistency check
 
-  // ---- ascending order through a bitmap of the index range, one window at a time
+  // ---- ascending order through the bitmap of the index range, one window at a time
   uint32_t written = 0;
   for (int64_t w0 = 0; w0 < len; w0 += kWindowBits) {
     const int span = (int)std::min<int64_t>(kWindowBits, len - w0);
     const int words = (span + 31) >> 5;
     const int per = (words + kFinalThreads - 1) / kFinalThreads;
-    for (int i = tid; i < words; i += kFinalThreads) bitmap[i] = 0;
-    __syncthreads();
-    for (int i = tid; i < nchosen; i += kFinalThreads) {
-      const int64_t t = chosen[i];
-      if (t >= w0 && t < w0 + span) atomicOr(&bitmap[(t - w0) >> 5], 1u << ((t - w0) & 31));
+    if (!direct) {
+      for (int i = tid; i < words; i += kFinalThreads) bitmap[i] = 0;
+      __syncthreads();
+      for (int i = tid; i < nchosen; i += kFinalThreads) {
+        const int64_t t = chosen[i];
+        if (t >= w0 && t < w0 + span) atomicOr(&bitmap[(t - w0) >> 5], 1u << ((t - w0) & 31));
+      }
+      __syncthreads();
     }
-    __syncthreads();
     uint32_t c = 0;
     for (int i = 0; i < per; ++i) {
       const int wi = tid * per + i;
@@ -451,6 +470,7 @@ __global__ void __launch_bounds__(kFinalThreads) topk_final_kernel(const float* 
     written += total;
     __syncthreads();
   }
+  if (direct && written != (uint32_t)k) report(status, DSA_ERR_BOUNDS);  // internal consistency check
   for (int i = (int)written + tid; i < k; i += kFinalThreads) o[i] = -1;
 }
 
@@ -467,7 +487,7 @@ size_t topk_workspace_bytes(int rows, int max_row_len, int k) {
   return ws_bytes(rows, k);
 }
 
-size_t topk_final_smem_bytes() { return 4 * kMaxTopk + 4 * kBins + 128 + (size_t)kWindowBits / 8; }
+size_t topk_final_smem_bytes() { return (size_t)kWindowBits / 8 + 8 * kCandCap + 4 * kMaxTopk + 4 * kBins + 128; }
 
 dsa_status_t launch_topk(const float* scores, int64_t ld, const int32_t* row_lens, const int32_t* seq_lens, int nq,
                          int rows, int max_row_len, int k, int32_t* out, void* workspace, int32_t* status,
@@ -483,14 +503,15 @@ dsa_status_t launch_topk(const float* scores, int64_t ld, const int32_t* row_len
   ws.sel = reinterpret_cast<int32_t*>(w);
   w += al((size_t)rows * k * 4);
   ws.cand = reinterpret_cast<uint64_t*>(w);
-  // histograms and counters start at zero
-  const size_t zero_bytes = al((size_t)rows * kBins * 4) + al((size_t)rows * 16);
-  if (cuda_status(cudaMemsetAsync(workspace, 0, zero_bytes, st)) != DSA_OK) return DSA_ERR_CUDA;
   const int cap = max_row_len;
   const int nseg = std::max(1, (max_row_len + kSeg - 1) / kSeg);
   if (max_row_len > k) {
     dim3 grid(nseg, rows);
+    // histograms and counters start at zero
+    const size_t zero_bytes = al((size_t)rows * kBins * 4) + al((size_t)rows * 16);
+    if (cuda_status(cudaMemsetAsync(workspace, 0, zero_bytes, st)) != DSA_OK) return DSA_ERR_CUDA;
     topk_hist_kernel<<<grid, kThreads, 0, st>>>(scores, ld, row_lens, seq_lens, nq, cap, k, ws, status);
+    topk_threshold_kernel<<<rows, kThreads, 0, st>>>(row_lens, seq_lens, nq, cap, k, ws);
     topk_collect_kernel<<<grid, kThreads, 0, st>>>(scores, ld, row_lens, seq_lens, nq, cap, k, ws, status);
   }
   static bool attr_set[64] = {};
