@@ -183,7 +183,7 @@ dsa_status_t sparse_mla_decode(const dsa_paged_cache_t* cache, const dsa_batch_t
   if (k < 1 || k > DSA_MAX_TOPK || !dev_status) return DSA_ERR_INVALID_ARG;
   const int rows = batch->batch * batch->queries_per_seq;
   if (rows == 0) return DSA_OK;
-  if (!q_mla || !idx || !out || !lse || !aligned(q_mla, 16) || !aligned(out, 4)) return DSA_ERR_INVALID_ARG;
+  if (!q_mla || !idx || !out || !lse || !aligned(q_mla, 16) || !aligned(out, 8)) return DSA_ERR_INVALID_ARG;
   if (!workspace || !aligned(workspace, 256) || workspace_bytes < mla_workspace_bytes(rows, k))
     return DSA_ERR_WORKSPACE;
   return launch_sparse_mla(*cache, *batch, q_mla, idx, k, sm_scale, out, lse, workspace, dev_status,
@@ -208,7 +208,7 @@ dsa_status_t dsa_decode_step(const dsa_paged_cache_t* cache, const dsa_batch_t* 
   const int rows = batch->batch * batch->queries_per_seq;
   if (rows == 0) return DSA_OK;
   if (!q_index || !head_w || !q_mla || !out || !lse) return DSA_ERR_INVALID_ARG;
-  if (!aligned(q_index, 16) || !aligned(head_w, 16) || !aligned(q_mla, 16) || !aligned(out, 4))
+  if (!aligned(q_index, 16) || !aligned(head_w, 16) || !aligned(q_mla, 16) || !aligned(out, 8))
     return DSA_ERR_INVALID_ARG;
   if (!workspace || !aligned(workspace, 256) || workspace_bytes < dsa_workspace_size(batch, k))
     return DSA_ERR_WORKSPACE;

@@ -101,6 +101,29 @@ __device__ __forceinline__ void tma_load_3d(uint32_t dst, const void* map, int c
       ::"r"(dst), "l"(map), "r"(c0), "r"(c1), "r"(c2), "r"(bar)
       : "memory");
 }
+// L2 cache policies: streamed-once data (evict first) and data read again
+// soon by the next kernel (evict last).
+__device__ __forceinline__ uint64_t policy_evict_first() {
+  uint64_t p;
+  asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(p));
+  return p;
+}
+__device__ __forceinline__ uint64_t policy_evict_last() {
+  uint64_t p;
+  asm volatile("createpolicy.fractional.L2::evict_last.b64 %0, 1.0;" : "=l"(p));
+  return p;
+}
+__device__ __forceinline__ void tma_load_3d_hint(uint32_t dst, const void* map, int c0, int c1, int c2, uint32_t bar,
+                                                 uint64_t policy) {
+  asm volatile(
+      "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes.L2::cache_hint"
+      " [%0], [%1, {%2, %3, %4}], [%5], %6;"
+      ::"r"(dst), "l"(map), "r"(c0), "r"(c1), "r"(c2), "r"(bar), "l"(policy)
+      : "memory");
+}
+__device__ __forceinline__ void st_global_hint(float* addr, float v, uint64_t policy) {
+  asm volatile("st.global.L2::cache_hint.f32 [%0], %1, %2;" ::"l"(addr), "f"(v), "l"(policy) : "memory");
+}
 // Plain bulk copy; both addresses 16-byte aligned, bytes a multiple of 16.
 __device__ __forceinline__ void bulk_load(uint32_t dst, const void* src, uint32_t bytes, uint32_t bar) {
   asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];"
@@ -216,6 +239,23 @@ __device__ __forceinline__ uint32_t score_key(float s) {
   if ((u & 0x7FFFFFFFu) > 0x7F800000u) return 0u;
   if (u == 0x80000000u) u = 0u;
   return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
+}
+
+// Four E4M3 bytes -> four bf16, exactly, on full-rate pipes.  An E4M3 value
+// S.EEEE.MMM equals the bf16 with the same sign, exponent field EEEE and
+// mantissa MMM0000 times 2^120, for normal and subnormal codes alike (the
+// bf16 of a zero exponent field is the subnormal 0.MMM * 2^-126); the
+// product is exact.  The NaN codes 0x7F / 0xFF are not special-cased.
+// lo = elements 0 and 1, hi = elements 2 and 3 (low half = lower element).
+__device__ __forceinline__ void e4m3x4_to_bf16x4(uint32_t w, uint32_t& lo, uint32_t& hi) {
+  const uint32_t x0 = __byte_perm(w, 0u, 0x4140);  // [0, b1, 0, b0] as 16-bit lanes
+  const uint32_t x1 = __byte_perm(w, 0u, 0x4342);  // [0, b3, 0, b2]
+  // magnitude bits 6..0 -> 10..4 and sign bit 7 -> 15 of each 16-bit lane (one LOP3 each)
+  const uint32_t f0 = ((x0 << 4) & 0x07F007F0u) | ((x0 << 8) & 0x80008000u);
+  const uint32_t f1 = ((x1 << 4) & 0x07F007F0u) | ((x1 << 8) & 0x80008000u);
+  const uint32_t k2_120 = 0x7B807B80u;  // bf16 2^120 in both halves
+  asm("mul.rn.bf16x2 %0, %1, %2;" : "=r"(lo) : "r"(f0), "r"(k2_120));
+  asm("mul.rn.bf16x2 %0, %1, %2;" : "=r"(hi) : "r"(f1), "r"(k2_120));
 }
 
 // Two E4M3 bytes (low byte = first element) -> two bf16 (low half = first).

@@ -215,6 +215,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       };
       int cb, cnp, cr[kPagesPerUnit];
       resolve(u_begin, cb, cnp, cr);
+      const uint64_t stream_policy = policy_evict_first();  // keys are read once per step
       int cur_b = -1;
       uint32_t it = 0, qn = 0;
       bool ok = true;
@@ -252,8 +253,8 @@ __global__ void __launch_bounds__(kThreads, 1)
               }
               mbar_arrive_expect_tx(full_bar(s), npages * kPageCodeBytes + kUnitScaleBytes);
               for (int q = 0; q < npages; ++q)
-                tma_load_3d(sbase + L::kOffA + s * kATileBytes + q * kPageCodeBytes, &tmap_keys, 0, 0, r[q],
-                            full_bar(s));
+                tma_load_3d_hint(sbase + L::kOffA + s * kATileBytes + q * kPageCodeBytes, &tmap_keys, 0, 0, r[q],
+                                 full_bar(s), stream_policy);
               tma_gather4(sbase + L::kOffScales + s * kUnitScaleBytes, &tmap_scales, 0, r[0], r[1], r[2], r[3],
                           full_bar(s));
             }
@@ -308,6 +309,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int row = quarter * 32 + lane;  // TMEM lane = key row of each 128-key sub-tile
       int cursor = first_seq(u_begin), cur_b = -1;
       float w[NQ][kIdxHeads];
+      const uint64_t keep_policy = policy_evict_last();  // the top-k reads the scores next
       uint32_t it = 0;
       for (int64_t u = u_begin; u < u_end; ++u, ++it) {
         const int b = seq_of_unit(prefix, p.batch, u, cursor);
@@ -351,8 +353,8 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
           const int vis = visible_len(len, NQ, q);
           float* out = p.scores + ((int64_t)b * NQ + q) * p.ld;
-          if (t0 < vis) out[t0] = s0;
-          if (t1 < vis) out[t1] = s1;
+          if (t0 < vis) st_global_hint(out + t0, s0, keep_policy);
+          if (t1 < vis) st_global_hint(out + t1, s1, keep_policy);
         }
         tc_fence_before();
         __syncwarp();

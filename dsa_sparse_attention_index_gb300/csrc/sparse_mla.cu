@@ -67,7 +67,8 @@ constexpr int kOffBars = kOffAlpha + 128 * 4;                // 197,120
 constexpr int kNumBars = 10;
 constexpr int kOffMisc = kOffBars + kNumBars * 8;
 constexpr int kOffTokOff = kOffMisc + 16;                    // int64 per token of the chunk
-constexpr size_t kSmemBytes = 1024 + kOffTokOff + 8 * (size_t)kMaxChunk;
+constexpr int kOffMask = kOffTokOff + 8 * kMaxChunk;         // one validity bit per token
+constexpr size_t kSmemBytes = 1024 + kOffMask + (size_t)kMaxChunk / 8;
 
 struct MlaParams {
   const uint8_t* latent_base;  // cache base + latent_off
@@ -87,6 +88,12 @@ struct MlaParams {
   float* ml;        // [rows][nsplit][96][4]: max (log2), sum of bf16(p), sum of p
   int32_t* status;
 };
+
+__device__ __forceinline__ float ex2(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
 
 __device__ __forceinline__ bool bar_or_softmax(bool v) {
   uint32_t r;
@@ -119,6 +126,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + kOffMisc);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + kOffMisc + 4);
   int64_t* tok_off = reinterpret_cast<int64_t*>(smem + kOffTokOff);
+  uint32_t* tile_mask = reinterpret_cast<uint32_t*>(smem + kOffMask);
   float* alpha_s = reinterpret_cast<float*>(smem + kOffAlpha);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -164,6 +172,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
     }
     tok_off[i] = off;
+    const uint32_t bits = __ballot_sync(0xffffffffu, off >= 0);  // a warp pass covers 32 consecutive tokens
+    if ((threadIdx.x & 31) == 0) tile_mask[i >> 5] = bits;
   }
   tc_fence_before();
   __syncthreads();
@@ -257,10 +267,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             const uint32_t w[4] = {buf[c].x, buf[c].y, buf[c].z, buf[c].w};
             uint32_t o[8];
 #pragma unroll
-            for (int q = 0; q < 4; ++q) {
-              o[2 * q] = e4m3x2_to_bf16x2((uint16_t)(w[q] & 0xFFFF));
-              o[2 * q + 1] = e4m3x2_to_bf16x2((uint16_t)(w[q] >> 16));
-            }
+            for (int q = 0; q < 4; ++q) e4m3x4_to_bf16x4(w[q], o[2 * q], o[2 * q + 1]);
             uint8_t* blk = tile + dblk * kTileDBlockBytes;
             *reinterpret_cast<uint4*>(blk + swz128(tok * 128 + inner)) = make_uint4(o[0], o[1], o[2], o[3]);
             *reinterpret_cast<uint4*>(blk + swz128(tok * 128 + inner + 16)) = make_uint4(o[4], o[5], o[6], o[7]);
@@ -299,17 +306,18 @@ __global__ void __launch_bounds__(kThreads, 1)
         tmem_ld32(tmem + ((uint32_t)(warp * 32) << 16) + kSCol + kTileTok * b, r);
         tmem_ld_wait();
         float x[32];
-        float m_tile = -INFINITY;
+        const uint32_t vmask = tile_mask[i];
+        float m0 = -INFINITY, m1 = -INFINITY;
 #pragma unroll
         for (int j = 0; j < 32; ++j) {
-          const bool valid = tok_off[i * kTileTok + j] >= 0;
-          x[j] = valid ? __uint_as_float(r[j]) * p.logit_scale_log2 : -INFINITY;
-          m_tile = fmaxf(m_tile, x[j]);
+          x[j] = ((vmask >> j) & 1u) ? __uint_as_float(r[j]) * p.logit_scale_log2 : -INFINITY;
+          if (j & 1) m1 = fmaxf(m1, x[j]); else m0 = fmaxf(m0, x[j]);
         }
+        const float m_tile = fmaxf(m0, m1);
         const bool grow = live && m_tile > m_used + kRescaleThreshold;
         if (bar_or_softmax(grow)) {
           const float m_new = grow ? m_tile : m_used;
-          const float alpha = (m_used == -INFINITY) ? 0.f : exp2f(m_used - m_new);
+          const float alpha = (m_used == -INFINITY) ? 0.f : ex2(m_used - m_new);
           if (live) alpha_s[h] = alpha;
           l_round *= alpha;
           l_exact *= alpha;
@@ -336,15 +344,19 @@ __global__ void __launch_bounds__(kThreads, 1)
         // probabilities -> bf16 P row h (64 bytes, 64-byte swizzle)
         uint32_t pk[16];
         float srnd = 0.f, sex = 0.f;
+        if (m_used != -INFINITY) {
 #pragma unroll
-        for (int j = 0; j < 32; j += 2) {
-          const float p0 = (m_used == -INFINITY) ? 0.f : exp2f(x[j] - m_used);
-          const float p1 = (m_used == -INFINITY) ? 0.f : exp2f(x[j + 1] - m_used);
-          const __nv_bfloat162 bb = __floats2bfloat162_rn(p0, p1);
-          const float2 back = __bfloat1622float2(bb);
-          srnd += back.x + back.y;
-          sex += p0 + p1;
-          pk[j >> 1] = *reinterpret_cast<const uint32_t*>(&bb);
+          for (int j = 0; j < 32; j += 2) {
+            const float p0 = ex2(x[j] - m_used), p1 = ex2(x[j + 1] - m_used);  // 2^-inf = 0 when masked
+            const __nv_bfloat162 bb = __floats2bfloat162_rn(p0, p1);
+            const float2 back = __bfloat1622float2(bb);
+            srnd += back.x + back.y;
+            sex += p0 + p1;
+            pk[j >> 1] = *reinterpret_cast<const uint32_t*>(&bb);
+          }
+        } else {
+#pragma unroll
+          for (int j = 0; j < 16; ++j) pk[j] = 0;
         }
         l_round += srnd;
         l_exact += sex;
@@ -395,41 +407,56 @@ __global__ void __launch_bounds__(kThreads, 1)
 }
 
 // Merge the chunks of one row through their log-sum-exp and write bf16 O and
-// fp32 LSE (natural log).
+// fp32 LSE (natural log).  CTA (row, group) covers 8 heads; every split's
+// partial of a float4 is loaded before any is added (loads in flight).
+constexpr int kCombineHeads = 8;
+constexpr int kMaxSplit = 16;
 __global__ void __launch_bounds__(256) mla_combine_kernel(const float* __restrict__ opart,
                                                            const float* __restrict__ ml, int nsplit,
                                                            float latent_scale, uint16_t* out, float* lse) {
-  const int row = blockIdx.y;
-  const int h = blockIdx.x;  // one head per CTA
-  __shared__ float wgt[16];
-  __shared__ float inv_den;
+  const int row = blockIdx.y, h0 = blockIdx.x * kCombineHeads;
+  __shared__ float wgt[kCombineHeads][kMaxSplit];
   const float4* mlr = reinterpret_cast<const float4*>(ml) + (int64_t)row * nsplit * kHeads;
-  if (threadIdx.x == 0) {
+  if (threadIdx.x < kCombineHeads) {
+    const int h = h0 + threadIdx.x;
     float M = -INFINITY;
     for (int s = 0; s < nsplit; ++s) M = fmaxf(M, mlr[s * kHeads + h].x);
     float den = 0.f, ex = 0.f;
+    float w[kMaxSplit];
     for (int s = 0; s < nsplit; ++s) {
       const float4 v = mlr[s * kHeads + h];
-      const float w = (M == -INFINITY || v.x == -INFINITY) ? 0.f : exp2f(v.x - M);
-      wgt[s] = w;
-      den += w * v.y;
-      ex += w * v.z;
+      w[s] = (M == -INFINITY || v.x == -INFINITY) ? 0.f : ex2(v.x - M);
+      den += w[s] * v.y;
+      ex += w[s] * v.z;
     }
-    inv_den = den > 0.f ? latent_scale / den : 0.f;
-    lse[(int64_t)row * kHeads + h] = (M == -INFINITY || ex <= 0.f) ? -INFINITY : (M + log2f(ex)) * 0.69314718055994531f;
+    const float inv = den > 0.f ? latent_scale / den : 0.f;
+    for (int s = 0; s < nsplit; ++s) wgt[threadIdx.x][s] = w[s] * inv;
+    lse[(int64_t)row * kHeads + h] =
+        (M == -INFINITY || ex <= 0.f) ? -INFINITY : (M + log2f(ex)) * 0.69314718055994531f;
   }
   __syncthreads();
-  for (int d = threadIdx.x * 2; d < kValue; d += 512) {
-    float a0 = 0.f, a1 = 0.f;
-    for (int s = 0; s < nsplit; ++s) {
-      const float w = wgt[s];
-      if (w == 0.f) continue;
-      const float2 v = *reinterpret_cast<const float2*>(opart + (((int64_t)row * nsplit + s) * kHeads + h) * kValue + d);
-      a0 = fmaf(w, v.x, a0);
-      a1 = fmaf(w, v.y, a1);
-    }
-    const __nv_bfloat162 bb = __floats2bfloat162_rn(a0 * inv_den, a1 * inv_den);
-    *reinterpret_cast<__nv_bfloat162*>(out + ((int64_t)row * kHeads + h) * kValue + d) = bb;
+  constexpr int kVec = kCombineHeads * kValue / 4;  // 1024 float4s per CTA
+  for (int v = threadIdx.x; v < kVec; v += blockDim.x) {
+    const int hl = v / (kValue / 4), d = (v % (kValue / 4)) * 4;
+    const float* src = opart + ((int64_t)row * nsplit * kHeads + h0 + hl) * kValue + d;
+    float4 x[kMaxSplit];
+#pragma unroll
+    for (int s = 0; s < kMaxSplit; ++s)
+      if (s < nsplit) x[s] = *reinterpret_cast<const float4*>(src + (int64_t)s * kHeads * kValue);
+    float4 a = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+    for (int s = 0; s < kMaxSplit; ++s)
+      if (s < nsplit) {
+        const float w = wgt[hl][s];
+        a.x = fmaf(w, x[s].x, a.x); a.y = fmaf(w, x[s].y, a.y);
+        a.z = fmaf(w, x[s].z, a.z); a.w = fmaf(w, x[s].w, a.w);
+      }
+    const __nv_bfloat162 lo = __floats2bfloat162_rn(a.x, a.y);
+    const __nv_bfloat162 hi = __floats2bfloat162_rn(a.z, a.w);
+    uint2 pk;
+    pk.x = *reinterpret_cast<const uint32_t*>(&lo);
+    pk.y = *reinterpret_cast<const uint32_t*>(&hi);
+    *reinterpret_cast<uint2*>(out + ((int64_t)row * kHeads + h0 + hl) * kValue + d) = pk;
   }
 }
 
@@ -496,7 +523,7 @@ dsa_status_t launch_sparse_mla(const dsa_paged_cache_t& c, const dsa_batch_t& bt
   }
   sparse_mla_kernel<<<dim3(nsplit, rows), kThreads, kSmemBytes, st>>>(qmap, p);
   if (launch_status() != DSA_OK) return DSA_ERR_CUDA;
-  mla_combine_kernel<<<dim3(kHeads, rows), 256, 0, st>>>(opart, ml, nsplit, c.latent_scale, out, lse);
+  mla_combine_kernel<<<dim3(kHeads / kCombineHeads, rows), 256, 0, st>>>(opart, ml, nsplit, c.latent_scale, out, lse);
   return launch_status();
 }
 

@@ -160,7 +160,7 @@ dsa_status_t dsa_topk(const float* scores, int64_t ld_scores, const int32_t* row
  * Every index must be a visible token of its row; otherwise DSA_ERR_BOUNDS.
  *   q_mla     device bf16 bits [rows][96][576], 16-byte aligned
  *   idx       device int32 [rows][k], k in 1..DSA_MAX_TOPK
- *   out       device bf16 bits [rows][96][512];  lse device fp32 [rows][96]
+ *   out       device bf16 bits [rows][96][512], 8-byte aligned;  lse device fp32 [rows][96]
  *   workspace >= sparse_mla_workspace_size(rows, k) bytes, 256-B aligned
  * Partial results of token chunks are merged through their log-sum-exp
  * (Day-0 post, DCP section: partial outputs combined by LSE).

@@ -178,6 +178,24 @@ def test_sparse_mla_matches_oracle(k):
     check_mla(case, idx, o, l, rtol=0.0 if k == 2048 else OUT_RTOL_EDGE)
 
 
+def test_sparse_mla_single_token_is_bit_exact():
+    """One selected token: softmax weight 1, so out = bf16(latent_scale * e4m3(c)) exactly; this pins
+    the E4M3 -> bf16 widening for every code in the row (subnormals, signs, zeros)."""
+    case = synth.make_case("one", seq_lens=[700], nq=1, seed=31)
+    r = case.block_table[0, 3]
+    # put every E4M3 code except the NaNs into token 200's latent row
+    codes = np.array([c for c in range(256) if c not in (0x7F, 0xFF)] * 3, dtype=np.uint8)[:576]
+    off = case.latent_off + (200 % 64) * 576
+    case.pool[r, off:off + 576] = codes
+    dc = synth.device_case(case)
+    idx = np.full((1, 4), -1, dtype=np.int32)
+    idx[0, 0] = 200
+    o, l = _gpu_mla(case, dc, idx)
+    vals = torch.from_numpy(codes[:512].copy()).view(torch.float8_e4m3fn).to(torch.float32) * np.float32(case.latent_scale)
+    want = vals.to(torch.bfloat16).to(torch.float32).numpy()
+    assert np.array_equal(o[0], np.broadcast_to(want, (96, 512)))
+
+
 def test_sparse_mla_masked_rows_and_scattered_padding():
     case = synth.make_case("mlm", seq_lens=[3000, 3000], nq=2, seed=5)
     dc = synth.device_case(case)
