@@ -45,7 +45,8 @@ class BatchT(ctypes.Structure):
 _lib = None
 
 EXPORTS = ["dsa_api_version", "dsa_status_string", "dsa_last_cuda_error", "dsa_translate_pages", "dsa_index_scores",
-           "dsa_topk_workspace_size", "dsa_topk", "sparse_mla_workspace_size", "sparse_mla_decode",
+           "dsa_topk_workspace_size", "dsa_topk", "dsa_topk_noalloc", "sparse_mla_workspace_size",
+           "sparse_mla_decode",
            "dsa_workspace_size", "dsa_decode_step", "dsa_selftest_wait_timeout"]
 
 
@@ -67,6 +68,7 @@ def lib():
             "dsa_index_scores": (i32, [pc, pb, P, P, P, i64, P, P]),
             "dsa_topk_workspace_size": (sz, [i32, i32, i32]),
             "dsa_topk": (i32, [P, i64, P, i32, i32, i32, P, P, sz, P, P]),
+            "dsa_topk_noalloc": (i32, [P, i64, P, i32, i32, i32, P, P, P]),
             "sparse_mla_workspace_size": (sz, [i32, i32]),
             "sparse_mla_decode": (i32, [pc, pb, P, P, i32, f32, P, P, P, sz, P, P]),
             "dsa_workspace_size": (sz, [pb, i32]),
@@ -163,6 +165,13 @@ def topk(scores, row_lens, max_row_len: int, k: int, idx_out, workspace, status,
     _check(lib().dsa_topk(_ptr(scores), int(scores.shape[1]), _ptr(row_lens), rows, int(max_row_len), int(k),
                           _ptr(idx_out), _ptr(workspace), workspace.numel() * workspace.element_size(),
                           _ptr(status), _stream(stream)), "dsa_topk")
+
+
+def topk_noalloc(scores, row_lens, max_row_len: int, k: int, idx_out, status, stream=None):
+    """dsa_topk with the library's built-in scratch: no workspace, no allocation (rows <= 64)."""
+    rows = int(scores.shape[0])
+    _check(lib().dsa_topk_noalloc(_ptr(scores), int(scores.shape[1]), _ptr(row_lens), rows, int(max_row_len),
+                                  int(k), _ptr(idx_out), _ptr(status), _stream(stream)), "dsa_topk_noalloc")
 
 
 def sparse_mla_workspace_size(rows: int, k: int) -> int:

@@ -169,6 +169,17 @@ dsa_status_t dsa_topk(const float* scores, int64_t ld_scores, const int32_t* row
                      static_cast<cudaStream_t>(stream));
 }
 
+dsa_status_t dsa_topk_noalloc(const float* scores, int64_t ld_scores, const int32_t* row_lens, int32_t rows,
+                              int32_t max_row_len, int32_t k, int32_t* idx_out, int32_t* dev_status, void* stream) {
+  if (rows < 0 || k < 1 || k > DSA_MAX_TOPK || max_row_len < 0 || !dev_status) return DSA_ERR_INVALID_ARG;
+  if (rows > DSA_TOPK_NOALLOC_MAX_ROWS) return DSA_ERR_UNSUPPORTED;
+  if (rows == 0) return DSA_OK;
+  if (!scores || !row_lens || !idx_out || !aligned(scores, 16) || ld_scores < max_row_len || (ld_scores % 4))
+    return DSA_ERR_INVALID_ARG;
+  return launch_topk_noalloc(scores, ld_scores, row_lens, rows, max_row_len, k, idx_out, dev_status,
+                             static_cast<cudaStream_t>(stream));
+}
+
 size_t sparse_mla_workspace_size(int32_t rows, int32_t k) {
   if (rows < 0 || k < 1 || k > DSA_MAX_TOPK) return 0;
   return mla_workspace_bytes(rows, k);

@@ -24,6 +24,7 @@
 // The multi-CTA split keeps all SMs busy for the few-long-rows case (4 rows
 // of 1M tokens) as well as for many shorter rows.
 #include <algorithm>
+#include <mutex>
 
 #include "common.cuh"
 #include "internal.h"
@@ -526,6 +527,44 @@ dsa_status_t launch_topk(const float* scores, int64_t ld, const int32_t* row_len
   }
   topk_final_kernel<<<rows, kFinalThreads, smem, st>>>(scores, ld, row_lens, seq_lens, nq, cap, k, ws, out, status);
   return launch_status();
+}
+
+// ---------------------------------------------------------------- top-k with built-in scratch
+// The scratch the top-k needs (histograms, counters, selected and candidate
+// lists) for up to kNoAllocMaxRows rows of any length with k <= 2048, kept in
+// a device array that exists for as long as the library is loaded, so the
+// entry point below never allocates.  Every call reuses it: launch_topk zeroes
+// the histograms and counters at the start of each call, the lists are written
+// before they are read, and calls whose work overlaps on the GPU would race.
+namespace {
+constexpr int kNoAllocMaxRows = DSA_TOPK_NOALLOC_MAX_ROWS;
+constexpr size_t al256c(size_t x) { return (x + 255) & ~size_t(255); }
+constexpr size_t kNoAllocBytes = al256c((size_t)kNoAllocMaxRows * kBins * 4) + al256c((size_t)kNoAllocMaxRows * 16) +
+                                 al256c((size_t)kNoAllocMaxRows * kMaxTopk * 4) +
+                                 al256c((size_t)kNoAllocMaxRows * kCandCap * 8);  // 5.5 MiB
+static __device__ __align__(256) uint8_t g_topk_scratch[kNoAllocBytes];
+std::mutex g_scratch_mu;
+void* g_scratch_addr[64] = {};  // the array's device address, per device, resolved on first use
+}  // namespace
+
+dsa_status_t launch_topk_noalloc(const float* scores, int64_t ld, const int32_t* row_lens, int rows, int max_row_len,
+                                 int k, int32_t* out, int32_t* status, cudaStream_t st) {
+  if (rows > kNoAllocMaxRows || ws_bytes(rows, k) > kNoAllocBytes) return DSA_ERR_UNSUPPORTED;
+  int dev = 0;
+  if (cuda_status(cudaGetDevice(&dev)) != DSA_OK) return DSA_ERR_CUDA;
+  if (dev < 0 || dev >= 64) return DSA_ERR_UNSUPPORTED;
+  void* scratch = nullptr;
+  {
+    std::lock_guard<std::mutex> lock(g_scratch_mu);
+    if (g_scratch_addr[dev] == nullptr) {
+      // the host-side name of the array is not a device address: ask the runtime, with this device current
+      void* addr = nullptr;
+      if (cuda_status(cudaGetSymbolAddress(&addr, g_topk_scratch)) != DSA_OK) return DSA_ERR_CUDA;
+      g_scratch_addr[dev] = addr;
+    }
+    scratch = g_scratch_addr[dev];
+  }
+  return launch_topk(scores, ld, row_lens, nullptr, 1, rows, max_row_len, k, out, scratch, status, st);
 }
 
 }  // namespace dsa

@@ -53,6 +53,7 @@ extern "C" {
 #define DSA_VALUE_DIM 512        /* values are the first 512 latent columns */
 #define DSA_MAX_TOPK 2048        /* top-k of the model; also the largest k accepted */
 #define DSA_MAX_QUERIES_PER_SEQ 4
+#define DSA_TOPK_NOALLOC_MAX_ROWS 64  /* row limit of dsa_topk_noalloc */
 
 typedef enum dsa_status {
   DSA_OK = 0,
@@ -148,6 +149,27 @@ dsa_status_t dsa_topk(const float* scores, int64_t ld_scores, const int32_t* row
                       int32_t rows, int32_t max_row_len, int32_t k, int32_t* idx_out,
                       void* workspace, size_t workspace_bytes,
                       int32_t* dev_status, void* stream);
+
+/*
+ * dsa_topk without a workspace argument and without any allocation.  (The
+ * source pages have no counterpart; this is a convenience of this library.)
+ * Same inputs, outputs, ordering rules and errors as dsa_topk.  It is meant
+ * for callers that cannot call cudaMalloc: a host framework that owns the
+ * device memory pool and forbids allocations from outside it, or a loop where
+ * cudaMalloc/cudaFree must be avoided because they can block or synchronise
+ * the device.  The scratch is a 5.5 MiB array of device memory built into the
+ * library; every GPU that loads the library holds it until the process ends.
+ *   rows <= DSA_TOPK_NOALLOC_MAX_ROWS (64), otherwise DSA_ERR_UNSUPPORTED is
+ *   returned and nothing is launched; any row length; k <= DSA_MAX_TOPK.
+ * The first call on a device looks up the array's device address (a runtime
+ * query, no allocation); make that first call before any stream capture.
+ * All calls on a device share the one array: each call clears the parts that
+ * must start at zero, but calls whose work overlaps on the GPU (different
+ * streams, or concurrent host threads) race and must be serialised.
+ */
+dsa_status_t dsa_topk_noalloc(const float* scores, int64_t ld_scores, const int32_t* row_lens,
+                              int32_t rows, int32_t max_row_len, int32_t k, int32_t* idx_out,
+                              int32_t* dev_status, void* stream);
 
 /*
  * Exact sparse MLA decode (stage 3; Day-0 post: "MLA attention then runs
