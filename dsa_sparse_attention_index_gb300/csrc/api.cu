@@ -146,8 +146,7 @@ dsa_status_t dsa_index_scores(const dsa_paged_cache_t* cache, const dsa_batch_t*
   if (!q_index || !head_w || !scores || !aligned(q_index, 16) || !aligned(head_w, 16) || !aligned(scores, 16))
     return DSA_ERR_INVALID_ARG;
   if (ld_scores < batch->max_seq_len || (ld_scores % 4)) return DSA_ERR_INVALID_ARG;
-  if (cache->key_format != DSA_KEY_FP8_E4M3) return DSA_ERR_UNSUPPORTED;
-  return launch_index_scores_fp8(*cache, *batch, q_index, head_w, scores, ld_scores, dev_status,
+  return launch_index_scores(*cache, *batch, q_index, head_w, scores, ld_scores, dev_status,
                                  static_cast<cudaStream_t>(stream));
 }
 
@@ -223,7 +222,6 @@ dsa_status_t dsa_decode_step(const dsa_paged_cache_t* cache, const dsa_batch_t* 
     return DSA_ERR_INVALID_ARG;
   if (!workspace || !aligned(workspace, 256) || workspace_bytes < dsa_workspace_size(batch, k))
     return DSA_ERR_WORKSPACE;
-  if (cache->key_format != DSA_KEY_FP8_E4M3) return DSA_ERR_UNSUPPORTED;
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   uint8_t* w = static_cast<uint8_t*>(workspace);
   float* scores = scores_out;
@@ -242,7 +240,7 @@ dsa_status_t dsa_decode_step(const dsa_paged_cache_t* cache, const dsa_batch_t* 
   w += al256(topk_workspace_bytes(rows, batch->max_seq_len, k));
   void* mla_ws = w;
 
-  if ((s = launch_index_scores_fp8(*cache, *batch, q_index, head_w, scores, ld, dev_status, st)) != DSA_OK) return s;
+  if ((s = launch_index_scores(*cache, *batch, q_index, head_w, scores, ld, dev_status, st)) != DSA_OK) return s;
   const int cap = std::min(batch->max_blocks_per_seq * kBlock, batch->max_seq_len);
   if ((s = launch_topk(scores, ld, nullptr, batch->seq_lens, batch->queries_per_seq, rows, cap, k, idx, topk_ws,
                        dev_status, st)) != DSA_OK)

@@ -85,6 +85,18 @@ __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, volatil
   }
 }
 
+// Wait for a phase without looking at the abort flag: used when draining
+// copies or MMAs already in flight before a CTA exits or frees TMEM, which
+// must happen even after another role gave up.  Bounded by `limit_ns`.
+__device__ __forceinline__ bool mbar_wait_drain(uint32_t bar, uint32_t parity, uint64_t limit_ns) {
+  if (mbar_try_wait(bar, parity)) return true;
+  const uint64_t t0 = globaltimer();
+  for (uint32_t it = 1;; ++it) {
+    if (mbar_try_wait(bar, parity)) return true;
+    if ((it & 31u) == 0 && globaltimer() - t0 > limit_ns) return false;
+  }
+}
+
 // ---------------------------------------------------------------- copies
 __device__ __forceinline__ void prefetch_tmap(const void* map) {
   asm volatile("prefetch.tensormap [%0];" ::"l"(map) : "memory");
@@ -169,6 +181,19 @@ __device__ __forceinline__ void mma_bf16(uint32_t d, uint64_t a, uint64_t b, uin
       ::"r"(d), "l"(a), "l"(b), "r"(idesc), "r"(accumulate)
       : "memory");
 }
+// D[tmem] (+)= (A * B) with MX block scaling: per 32-element K block, A row m
+// is scaled by 2^(E - 127) with E the byte `sf_id` (instruction descriptor
+// bits [29,31)) of the TMEM word at lane m % 32, column sfa + m / 32; B
+// likewise from `sfb` (descriptor bits [4,6)).  A and B: E2M1 (unpacked byte
+// containers), E4M3, ...; fp32 accumulator.
+__device__ __forceinline__ void mma_mxf8f6f4(uint32_t d, uint64_t a, uint64_t b, uint32_t idesc, uint32_t sfa,
+                                             uint32_t sfb, uint32_t accumulate) {
+  asm volatile(
+      "{\n .reg .pred p;\n setp.ne.b32 p, %6, 0;\n"
+      " tcgen05.mma.cta_group::1.kind::mxf8f6f4.block_scale [%0], %1, %2, %3, [%4], [%5], p;\n}\n"
+      ::"r"(d), "l"(a), "l"(b), "r"(idesc), "r"(sfa), "r"(sfb), "r"(accumulate)
+      : "memory");
+}
 // Arrive once on `bar` when every tcgen05.mma issued so far by this thread completes.
 __device__ __forceinline__ void mma_commit(uint32_t bar) {
   asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar) : "memory");
@@ -201,6 +226,12 @@ __device__ __forceinline__ void tmem_st32(uint32_t taddr, const uint32_t (&r)[32
       DSA_W32(r)
       : "memory");
 }
+// Four consecutive 32-bit TMEM columns of this thread's lane (warp-collective).
+__device__ __forceinline__ void tmem_st4(uint32_t taddr, uint32_t v0, uint32_t v1, uint32_t v2, uint32_t v3) {
+  asm volatile("tcgen05.st.sync.aligned.32x32b.x4.b32 [%0], {%1, %2, %3, %4};" ::"r"(taddr), "r"(v0), "r"(v1),
+               "r"(v2), "r"(v3)
+               : "memory");
+}
 __device__ __forceinline__ void tmem_ld_wait() { asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory"); }
 __device__ __forceinline__ void tmem_st_wait() { asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory"); }
 
@@ -219,6 +250,15 @@ __device__ __forceinline__ uint64_t smem_desc(uint32_t addr, uint32_t lbo, uint3
 // Instruction descriptor (kind::f16 and kind::f8f6f4): fp32 accumulator,
 // operand formats, K-major (0) / MN-major (1) per operand, N >> 3, M >> 4.
 enum : uint32_t { kFmtE4M3 = 0, kFmtE2M1 = 5, kFmtBF16 = 1 };
+// Instruction descriptor of kind::mxf8f6f4.block_scale (fp32 accumulator
+// implied): operand formats, K-major operands, N >> 3, E8M0 scale type (bit
+// 23), M >> 4; the per-MMA scale-factor byte ids are ORed in with mx_sf_ids.
+__host__ __device__ constexpr uint32_t make_idesc_mx(uint32_t a_fmt, uint32_t b_fmt, uint32_t M, uint32_t N) {
+  return (a_fmt << 7) | (b_fmt << 10) | ((N >> 3) << 17) | (1u << 23) | ((M >> 4) << 24);
+}
+__host__ __device__ constexpr uint32_t mx_sf_ids(uint32_t sfa_id, uint32_t sfb_id) {
+  return (sfa_id << 29) | (sfb_id << 4);
+}
 __host__ __device__ constexpr uint32_t make_idesc(uint32_t a_fmt, uint32_t b_fmt, uint32_t a_mn, uint32_t b_mn,
                                                   uint32_t M, uint32_t N) {
   return (1u << 4) | (a_fmt << 7) | (b_fmt << 10) | (a_mn << 15) | (b_mn << 16) | ((N >> 3) << 17) |

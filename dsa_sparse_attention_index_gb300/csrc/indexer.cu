@@ -5,28 +5,39 @@
 // with 32 heads x 128 dims (vLLM Day-0 post for Kimi K3.1 Pro, section
 // "K3.1 Pro 中的稀疏注意力": 32 light heads, a 132-byte FP8 key incl. scale;
 // AMD section: FP32 accumulation and a weighted reduction across heads).
+// MXFP4 keys (68 bytes: 64 bytes of E2M1 codes, four E8M0 block scales) give
+// q[r][h] . k[t] = sum over the four 32-element blocks of 2^(E - 127) times
+// the block's dot product, and scale_t = 1.
 //
-// GB300 design.  Each 132-byte key carries 32*128 multiply-adds, i.e. 62
-// FLOP per byte: at HBM speed that is ~0.4 PFLOP/s, several times what the
-// CUDA cores can issue, so the dot products run on the 5th-gen tensor cores
-// even in decode.  A work unit is one sequence's 256 consecutive tokens (four
+// GB300 design.  Each key carries 32*128 multiply-adds (62 FLOP per FP8 byte,
+// 120 per MXFP4 byte): at HBM speed that is several times what the CUDA
+// cores can issue, so the dot products run on the 5th-gen tensor cores even
+// in decode.  A work unit is one sequence's 256 consecutive tokens (four
 // 64-token pages).  The grid is persistent (one CTA per SM) and the units of
 // all sequences are split evenly across CTAs ("key-balanced", Day-0 post,
 // fused decode section).  Per CTA:
-//   warp 0  TMA producer: per unit, four 64 x 128 B code pages (3-D tensor map
-//           over the block pool, 128-byte swizzle) and the four pages' fp32
-//           scale rows in one tile::gather4 copy, into a 5-6 stage ring; the
-//           lanes resolve the block-table rows of the next 32 units while
-//           lane 0 issues; the query tile of the current sequence goes into a
-//           2-slot ring;
-//   warp 1  MMA issuer: tcgen05.mma kind::f8f6f4, two M = 128 key sub-tiles
-//           per unit, N = 32*NQ query-heads, K = 128 in four K=32 steps, fp32
-//           accumulators in a double-buffered TMEM tile;
+//   warp 0  TMA producer: per unit, four 64-token code pages (3-D tensor map
+//           over the block pool, 128-byte swizzle; MXFP4 nibbles are unpacked
+//           by the copy into byte containers) into a 5-6 stage code ring, and
+//           the four pages' scale rows in one tile::gather4 copy into a
+//           deeper scale ring; the lanes resolve the block-table rows of the
+//           next 32 units, and several lanes issue one unit's copies at once;
+//           the query tile of the current sequence goes into a 2-slot ring;
+//   warp 1  MMA issuer: two M = 128 key sub-tiles per unit, N = 32*NQ
+//           query-heads, K = 128 in four K=32 steps, fp32 accumulators in a
+//           double-buffered TMEM tile.  FP8: tcgen05.mma kind::f8f6f4.
+//           MXFP4: kind::mxf8f6f4.block_scale, E2M1 x E4M3 with the keys'
+//           E8M0 block scales read from TMEM (queries: scale 2^0), so one
+//           accumulator per sub-tile already holds q . k.  The code stage
+//           is released by tcgen05.commit as soon as its MMAs complete;
 //   warps 2-5 epilogue: each thread owns two key rows (one per sub-tile),
-//           reads their 32*NQ accumulators with tcgen05.ld, applies scale,
-//           ReLU and the head weights, sums the heads in registers (no
-//           shuffles) and stores one fp32 score per query row (128-byte
-//           coalesced per warp).
+//           reads their 32*NQ accumulators with tcgen05.ld, applies the FP8
+//           scale, ReLU and the head weights, sums the heads in registers
+//           and stores one fp32 score per query row (coalesced per warp);
+//   warps 6-9 (MXFP4 only) scale staging: per unit, copy the 256 keys' E8M0
+//           words from the scale ring into TMEM, laid out as the
+//           block-scaled MMA reads them (key row m: lane m % 32, column
+//           m / 32, byte = 32-element block).
 // All draft rows of a sequence share one key read (AMD section: keys are
 // reused across query rows during speculative verify).
 #include <algorithm>
@@ -40,13 +51,13 @@ namespace {
 
 constexpr int kUnitKeys = 256;                          // four pages
 constexpr int kPagesPerUnit = kUnitKeys / kBlock;       // 4
-constexpr int kSubTileBytes = 128 * kIdxDim;            // 16 KB: one M = 128 MMA tile
-constexpr int kATileBytes = kUnitKeys * kIdxDim;        // 32 KB of E4M3 codes per unit
-constexpr int kPageCodeBytes = kBlock * kIdxDim;        // 8 KB
+constexpr int kSubTileBytes = 128 * kIdxDim;            // 16 KB: one M = 128 MMA tile (one byte per element)
+constexpr int kATileBytes = kUnitKeys * kIdxDim;        // 32 KB of codes per unit in shared memory
+constexpr int kPageCodeBytes = kBlock * kIdxDim;        // 8 KB in shared memory (MXFP4: 4 KB read)
 constexpr int kPageScaleBytes = kBlock * 4;             // 256 B
 constexpr int kUnitScaleBytes = kPagesPerUnit * kPageScaleBytes;  // 1 KB (one gather4)
-constexpr int kThreads = 192;
 constexpr int kMaxBatch = 4096;
+constexpr uint64_t kDrainNs = 10000000ull;              // bound on draining in-flight work at exit
 
 struct IdxParams {
   const uint8_t* index_base;  // cache base + index_off
@@ -65,18 +76,23 @@ struct IdxParams {
 
 template <int NQ>
 struct IdxSmem {
-  static constexpr int kStages = NQ == 1 ? 6 : 5;  // keeps the CTA within 227 KB of shared memory
-  static constexpr int kQSlot = 32 * NQ * kIdxDim;  // bytes
+  static constexpr int kStages = NQ == 1 ? 6 : 5;       // code ring; keeps the CTA within 227 KB
+  static constexpr int kScaleStages = kStages + 2;      // scale slots are held until the epilogue ends
+  static constexpr int kQSlot = 32 * NQ * kIdxDim;      // bytes
   static constexpr int kOffA = 0;
   static constexpr int kOffQ = kOffA + kStages * kATileBytes;
   static constexpr int kOffScales = kOffQ + 2 * kQSlot;
-  static constexpr int kOffBars = kOffScales + kStages * kUnitScaleBytes;
-  // barriers: full[S], empty[S], acc_full[2], acc_empty[2], q_full[2], q_empty[2], done
-  static constexpr int kNumBars = 2 * kStages + 9;
+  static constexpr int kOffBars = kOffScales + kScaleStages * kUnitScaleBytes;
+  // barriers: code full/empty [S], scale full/empty [SS], acc full/empty [2],
+  // q full/empty [2], scale-factors staged [2], done
+  static constexpr int kNumBars = 2 * kStages + 2 * kScaleStages + 11;
   static constexpr int kOffMisc = kOffBars + kNumBars * 8;  // tmem slot, abort flag
   static constexpr int kOffPrefix = kOffMisc + 16;
   static size_t bytes(int batch) { return 1024 + kOffPrefix + 4 * (size_t)(batch + 1); }
 };
+
+template <bool MX>
+constexpr int idx_threads() { return MX ? 320 : 192; }
 
 // Sequence of unit u, advancing a cursor (units arrive in increasing order).
 __device__ __forceinline__ int seq_of_unit(const int32_t* prefix, int batch, int64_t u, int& cursor) {
@@ -93,15 +109,23 @@ __device__ __forceinline__ void tma_gather4(uint32_t dst, const void* map, int c
       : "memory");
 }
 
-template <int NQ>
-__global__ void __launch_bounds__(kThreads, 1)
-    indexer_fp8_kernel(const __grid_constant__ CUtensorMap tmap_keys, const __grid_constant__ CUtensorMap tmap_scales,
-                       const __grid_constant__ CUtensorMap tmap_q, const IdxParams p) {
+// MX = false: FP8 keys (E4M3 codes + fp32 scale).  MX = true: MXFP4 keys
+// (E2M1 codes + E8M0 block scales, applied by the block-scaled MMA).
+template <int NQ, bool MX>
+__global__ void __launch_bounds__(idx_threads<MX>(), 1)
+    indexer_kernel(const __grid_constant__ CUtensorMap tmap_keys, const __grid_constant__ CUtensorMap tmap_scales,
+                   const __grid_constant__ CUtensorMap tmap_q, const IdxParams p) {
   using L = IdxSmem<NQ>;
+  static_assert(!MX || NQ == 1, "MXFP4 keys: one query row per sequence");
   constexpr int kStages = L::kStages;
+  constexpr int kSS = L::kScaleStages;
   constexpr int N = 32 * NQ;
-  constexpr uint32_t kTmemCols = (4 * N <= 128) ? 128 : (4 * N <= 256 ? 256 : 512);  // power of two
-  constexpr uint32_t kIdesc = make_idesc(kFmtE4M3, kFmtE4M3, 0, 0, 128, N);
+  // TMEM: accumulators [2 slots][2 sub-tiles][N] at column 0; MXFP4 adds the
+  // keys' scale factors (4 columns per sub-tile and slot) and the queries' (2^0)
+  constexpr uint32_t kTmemCols = MX ? 512 : ((4 * N <= 128) ? 128 : (4 * N <= 256 ? 256 : 512));
+  constexpr uint32_t kSfaCol = 256, kSfbCol = 384;
+  constexpr uint32_t kIdesc = MX ? make_idesc_mx(kFmtE2M1, kFmtE4M3, 128, N)
+                                 : make_idesc(kFmtE4M3, kFmtE4M3, 0, 0, 128, N);
 
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -109,15 +133,19 @@ __global__ void __launch_bounds__(kThreads, 1)
   const uint32_t bars = sbase + L::kOffBars;
   auto full_bar = [&](int s) { return bars + 8u * s; };
   auto empty_bar = [&](int s) { return bars + 8u * (kStages + s); };
-  auto accf_bar = [&](int a) { return bars + 8u * (2 * kStages + a); };
-  auto acce_bar = [&](int a) { return bars + 8u * (2 * kStages + 2 + a); };
-  auto qf_bar = [&](int q) { return bars + 8u * (2 * kStages + 4 + q); };
-  auto qe_bar = [&](int q) { return bars + 8u * (2 * kStages + 6 + q); };
-  const uint32_t done_bar = bars + 8u * (2 * kStages + 8);
+  auto scf_bar = [&](int s) { return bars + 8u * (2 * kStages + s); };
+  auto sce_bar = [&](int s) { return bars + 8u * (2 * kStages + kSS + s); };
+  const uint32_t bars2 = bars + 8u * (2 * kStages + 2 * kSS);
+  auto accf_bar = [&](int a) { return bars2 + 8u * a; };
+  auto acce_bar = [&](int a) { return bars2 + 8u * (2 + a); };
+  auto qf_bar = [&](int q) { return bars2 + 8u * (4 + q); };
+  auto qe_bar = [&](int q) { return bars2 + 8u * (6 + q); };
+  auto sfr_bar = [&](int a) { return bars2 + 8u * (8 + a); };
+  const uint32_t done_bar = bars2 + 8u * 10;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + L::kOffMisc);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + L::kOffMisc + 4);
   int32_t* prefix = reinterpret_cast<int32_t*>(smem + L::kOffPrefix);
-  const float* scales_smem = reinterpret_cast<const float*>(smem + L::kOffScales);
+  const uint32_t* scale_words = reinterpret_cast<const uint32_t*>(smem + L::kOffScales);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int cap = min(p.max_blocks * kBlock, p.max_seq_len);
@@ -126,13 +154,18 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (threadIdx.x == 0) {
     for (int s = 0; s < kStages; ++s) {
       mbar_init(full_bar(s), 1);
-      mbar_init(empty_bar(s), 4);
+      mbar_init(empty_bar(s), 1);   // tcgen05.commit of the unit's MMAs
+    }
+    for (int s = 0; s < kSS; ++s) {
+      mbar_init(scf_bar(s), 1);
+      mbar_init(sce_bar(s), 4);     // FP8: the epilogue warps; MXFP4: the scale-staging warps
     }
     for (int a = 0; a < 2; ++a) {
       mbar_init(accf_bar(a), 1);
       mbar_init(acce_bar(a), 4);
       mbar_init(qf_bar(a), 1);
       mbar_init(qe_bar(a), 1);
+      mbar_init(sfr_bar(a), 4);
     }
     mbar_init(done_bar, 1);
     *abort_flag = 0;
@@ -194,8 +227,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (u_begin < u_end) {
     if (warp == 0) {
       // ------------------------------------------------ TMA producer (one warp)
-      // The lanes resolve the block-table rows of the next 32 units while lane 0
-      // issues the copies of the current 32, so table reads never stall the ring.
+      // The lanes resolve the block-table rows of the next 32 units while the
+      // current 32 are issued, so table reads never stall the rings.
       constexpr unsigned kAll = 0xffffffffu;
       auto resolve = [&](int64_t g, int& rb, int& rnp, int (&rr)[kPagesPerUnit]) {
         const int64_t u = g + lane;
@@ -229,6 +262,15 @@ __global__ void __launch_bounds__(kThreads, 1)
           int r[kPagesPerUnit];
 #pragma unroll
           for (int q = 0; q < kPagesPerUnit; ++q) r[q] = __shfl_sync(kAll, cr[q], l);
+#pragma unroll
+          for (int q = 0; q < kPagesPerUnit; ++q) {
+            if (q >= npages) r[q] = r[0];  // gather rows must be valid; unused pages repeat page 0
+            if (r[q] < 0 || r[q] >= p.num_blocks) {
+              if (lane == 0) report(p.status, DSA_ERR_BOUNDS);
+              r[q] = 0;  // read a valid row instead; the call's results are void
+            }
+          }
+          const int s = it % kStages, s2 = it % kSS;
           if (lane == 0) {
             if (b != cur_b) {
               const int slot = qn & 1;
@@ -240,27 +282,26 @@ __global__ void __launch_bounds__(kThreads, 1)
                 cur_b = b;
               }
             }
-            const int s = it % kStages;
             ok = ok && mbar_wait(empty_bar(s), ((it / kStages) & 1) ^ 1, abort_flag, p.status);
+            ok = ok && mbar_wait(sce_bar(s2), ((it / kSS) & 1) ^ 1, abort_flag, p.status);
             if (ok) {
-#pragma unroll
-              for (int q = 0; q < kPagesPerUnit; ++q) {
-                if (q >= npages) r[q] = r[0];  // gather rows must be valid; unused pages repeat page 0
-                if (r[q] < 0 || r[q] >= p.num_blocks) {
-                  report(p.status, DSA_ERR_BOUNDS);
-                  r[q] = 0;  // read a valid row instead; the call's results are void
-                }
-              }
-              mbar_arrive_expect_tx(full_bar(s), npages * kPageCodeBytes + kUnitScaleBytes);
-              for (int q = 0; q < npages; ++q)
-                tma_load_3d_hint(sbase + L::kOffA + s * kATileBytes + q * kPageCodeBytes, &tmap_keys, 0, 0, r[q],
-                                 full_bar(s), stream_policy);
-              tma_gather4(sbase + L::kOffScales + s * kUnitScaleBytes, &tmap_scales, 0, r[0], r[1], r[2], r[3],
-                          full_bar(s));
+              // an unpacking MXFP4 copy counts its packed source bytes (half what it writes)
+              mbar_arrive_expect_tx(full_bar(s), npages * (MX ? kPageCodeBytes / 2 : kPageCodeBytes));
+              mbar_arrive_expect_tx(scf_bar(s2), kUnitScaleBytes);
             }
           }
           ok = __shfl_sync(kAll, ok, 0);
           if (!ok) break;
+          // the copies of one unit go out from several lanes at once: lane q loads page q,
+          // lane kPagesPerUnit gathers the four pages' scale rows
+          if (lane < npages) {
+            const int rq = lane == 0 ? r[0] : (lane == 1 ? r[1] : (lane == 2 ? r[2] : r[3]));
+            tma_load_3d_hint(sbase + L::kOffA + s * kATileBytes + lane * kPageCodeBytes, &tmap_keys, 0, 0, rq,
+                             full_bar(s), stream_policy);
+          } else if (lane == kPagesPerUnit) {
+            tma_gather4(sbase + L::kOffScales + s2 * kUnitScaleBytes, &tmap_scales, 0, r[0], r[1], r[2], r[3],
+                        scf_bar(s2));
+          }
         }
         cb = nb;
         cnp = nnp;
@@ -269,7 +310,9 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       if (lane == 0 && *abort_flag) {  // let copies already in flight land before the CTA exits
         for (uint32_t k = (it > kStages ? it - kStages : 0); k < it; ++k)
-          mbar_wait(full_bar(k % kStages), (k / kStages) & 1, abort_flag, nullptr, 10000000ull);
+          mbar_wait_drain(full_bar(k % kStages), (k / kStages) & 1, kDrainNs);
+        for (uint32_t k = (it > kSS ? it - kSS : 0); k < it; ++k)
+          mbar_wait_drain(scf_bar(k % kSS), (k / kSS) & 1, kDrainNs);
       }
     } else if (warp == 1 && lane == 0) {
       // ------------------------------------------------ MMA issuer
@@ -285,6 +328,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         const int s = it % kStages, a = it & 1;
         if (!mbar_wait(full_bar(s), (it / kStages) & 1, abort_flag, p.status)) break;
+        if (MX && !mbar_wait(sfr_bar(a), (it >> 1) & 1, abort_flag, p.status)) break;
         if (!mbar_wait(acce_bar(a), ((it >> 1) & 1) ^ 1, abort_flag, p.status)) break;
         tc_fence_after();
         const uint32_t b_base = sbase + L::kOffQ + ((qn - 1) & 1) * L::kQSlot;
@@ -295,15 +339,20 @@ __global__ void __launch_bounds__(kThreads, 1)
           for (int kk = 0; kk < kIdxDim / 32; ++kk) {
             const uint64_t ad = smem_desc(a_base + 32 * kk, 16, 1024, kLayoutSw128);
             const uint64_t bd = smem_desc(b_base + 32 * kk, 16, 1024, kLayoutSw128);
-            mma_f8f6f4(tmem + (2 * a + sub) * N, ad, bd, kIdesc, kk > 0 ? 1u : 0u);
+            if constexpr (MX)  // K step kk is E8M0 block kk: scale-factor byte kk
+              mma_mxf8f6f4(tmem + (2 * a + sub) * N, ad, bd, kIdesc | mx_sf_ids(kk, kk),
+                           tmem + kSfaCol + 32 * (2 * a + sub), tmem + kSfbCol, kk > 0 ? 1u : 0u);
+            else
+              mma_f8f6f4(tmem + (2 * a + sub) * N, ad, bd, kIdesc, kk > 0 ? 1u : 0u);
           }
         }
         mma_commit(accf_bar(a));
+        mma_commit(empty_bar(s));   // the code stage is free once these MMAs have read it
       }
       // all issued MMAs must finish before TMEM is released
       mma_commit(done_bar);
-      mbar_wait(done_bar, 0, abort_flag, nullptr, 10000000ull);
-    } else if (warp >= 2) {
+      mbar_wait_drain(done_bar, 0, kDrainNs);
+    } else if (warp >= 2 && warp < 6) {
       // ------------------------------------------------ epilogue
       const int quarter = warp & 3;
       const int row = quarter * 32 + lane;  // TMEM lane = key row of each 128-key sub-tile
@@ -328,17 +377,18 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
           cur_b = b;
         }
-        const int s = it % kStages, a = it & 1;
+        const int s2 = it % kSS, a = it & 1;
         bool ok = mbar_wait(accf_bar(a), (it >> 1) & 1, abort_flag, p.status);
-        ok = ok && mbar_wait(full_bar(s), (it / kStages) & 1, abort_flag, p.status);
+        if (!MX) ok = ok && mbar_wait(scf_bar(s2), (it / kSS) & 1, abort_flag, p.status);
         if (!__all_sync(0xffffffffu, ok)) break;   // warp-uniform: tcgen05.ld below is warp-collective
         tc_fence_after();
         const int j = (int)(u - prefix[b]);
         const int len = seq_len_of(b);
         const int t0 = kUnitKeys * j + row, t1 = t0 + 128;
-        const float sc0 = scales_smem[s * (kUnitScaleBytes / 4) + row];
-        const float sc1 = scales_smem[s * (kUnitScaleBytes / 4) + 128 + row];
         const uint32_t lane_base = tmem + ((uint32_t)(quarter * 32) << 16);
+        // MXFP4: the block scales are inside the accumulators already
+        const float sc0 = MX ? 1.f : __uint_as_float(scale_words[s2 * (kUnitScaleBytes / 4) + row]);
+        const float sc1 = MX ? 1.f : __uint_as_float(scale_words[s2 * (kUnitScaleBytes / 4) + 128 + row]);
 #pragma unroll
         for (int q = 0; q < NQ; ++q) {
           uint32_t r0[32], r1[32];
@@ -348,8 +398,13 @@ __global__ void __launch_bounds__(kThreads, 1)
           float s0 = 0.f, s1 = 0.f;
 #pragma unroll
           for (int h = 0; h < kIdxHeads; ++h) {
-            s0 = fmaf(w[q][h], fmaxf(sc0 * __uint_as_float(r0[h]), 0.f), s0);
-            s1 = fmaf(w[q][h], fmaxf(sc1 * __uint_as_float(r1[h]), 0.f), s1);
+            if constexpr (MX) {
+              s0 = fmaf(w[q][h], fmaxf(__uint_as_float(r0[h]), 0.f), s0);
+              s1 = fmaf(w[q][h], fmaxf(__uint_as_float(r1[h]), 0.f), s1);
+            } else {
+              s0 = fmaf(w[q][h], fmaxf(sc0 * __uint_as_float(r0[h]), 0.f), s0);
+              s1 = fmaf(w[q][h], fmaxf(sc1 * __uint_as_float(r1[h]), 0.f), s1);
+            }
           }
           const int vis = visible_len(len, NQ, q);
           float* out = p.scores + ((int64_t)b * NQ + q) * p.ld;
@@ -360,7 +415,36 @@ __global__ void __launch_bounds__(kThreads, 1)
         __syncwarp();
         if (lane == 0) {
           mbar_arrive(acce_bar(a));
-          mbar_arrive(empty_bar(s));
+          if (!MX) mbar_arrive(sce_bar(s2));
+        }
+      }
+    } else if (MX && warp >= 6) {
+      // ------------------------------------------------ MXFP4 scale staging
+      // Key row m of a sub-tile takes its E8M0 word from TMEM lane m % 32,
+      // column m / 32; every warp writes the same words into its own lane
+      // quarter.  The queries' scale words (2^0 in every byte) are written once.
+      const uint32_t lane_base = tmem + ((uint32_t)((warp & 3) * 32) << 16);
+      tmem_st4(lane_base + kSfbCol, 0x7F7F7F7Fu, 0x7F7F7F7Fu, 0x7F7F7F7Fu, 0x7F7F7F7Fu);
+      uint32_t it = 0;
+      for (int64_t u = u_begin; u < u_end; ++u, ++it) {
+        const int s2 = it % kSS, a = it & 1;
+        bool ok = mbar_wait(scf_bar(s2), (it / kSS) & 1, abort_flag, p.status);
+        // slot a's scale factors were last read by the MMAs of unit it - 2
+        ok = ok && mbar_wait(accf_bar(a), ((it >> 1) & 1) ^ 1, abort_flag, p.status);
+        if (!__all_sync(0xffffffffu, ok)) break;   // tcgen05.st is warp-collective
+        tc_fence_after();
+        const uint32_t* wsrc = scale_words + s2 * (kUnitScaleBytes / 4);
+#pragma unroll
+        for (int sub = 0; sub < 2; ++sub) {
+          const uint32_t* ws = wsrc + 128 * sub + lane;
+          tmem_st4(lane_base + kSfaCol + 32 * (2 * a + sub), ws[0], ws[32], ws[64], ws[96]);
+        }
+        tmem_st_wait();
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) {
+          mbar_arrive(sfr_bar(a));
+          mbar_arrive(sce_bar(s2));
         }
       }
     }
@@ -371,7 +455,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (warp == 1) tmem_dealloc(tmem, kTmemCols);
 }
 
-template <int NQ>
+template <int NQ, bool MX>
 dsa_status_t launch_nq(const IdxParams& p, const CUtensorMap& keys, const CUtensorMap& scales,
                        const CUtensorMap& q, cudaStream_t st) {
   static bool attr_set[64] = {};
@@ -379,44 +463,47 @@ dsa_status_t launch_nq(const IdxParams& p, const CUtensorMap& keys, const CUtens
   cudaGetDevice(&dev);
   const size_t smem = IdxSmem<NQ>::bytes(kMaxBatch);
   if (dev < 64 && !attr_set[dev]) {
-    if (cuda_status(cudaFuncSetAttribute(indexer_fp8_kernel<NQ>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+    if (cuda_status(cudaFuncSetAttribute(indexer_kernel<NQ, MX>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          (int)smem)) != DSA_OK)
       return DSA_ERR_CUDA;
     attr_set[dev] = true;
   }
   const int64_t units_bound = (int64_t)p.batch * ((p.max_seq_len + kUnitKeys - 1) / kUnitKeys);
   const int grid = (int)std::max<int64_t>(1, std::min<int64_t>(units_bound, num_sms()));
-  indexer_fp8_kernel<NQ><<<grid, kThreads, IdxSmem<NQ>::bytes(p.batch), st>>>(keys, scales, q, p);
+  indexer_kernel<NQ, MX><<<grid, idx_threads<MX>(), IdxSmem<NQ>::bytes(p.batch), st>>>(keys, scales, q, p);
   return launch_status();
 }
 
 }  // namespace
 
-dsa_status_t launch_index_scores_fp8(const dsa_paged_cache_t& c, const dsa_batch_t& bt, const uint8_t* q_index,
-                                     const float* head_w, float* scores, int64_t ld, int32_t* status,
-                                     cudaStream_t st) {
+dsa_status_t launch_index_scores(const dsa_paged_cache_t& c, const dsa_batch_t& bt, const uint8_t* q_index,
+                                 const float* head_w, float* scores, int64_t ld, int32_t* status, cudaStream_t st) {
   if (bt.batch > kMaxBatch) return DSA_ERR_UNSUPPORTED;
+  const bool mx = c.key_format == DSA_KEY_MXFP4;
+  const int nq = bt.queries_per_seq;
+  if (mx && nq != 1) return DSA_ERR_UNSUPPORTED;
   const uint8_t* index_base = static_cast<const uint8_t*>(c.base) + c.index_off;
+  const int code_bytes = mx ? kIdxDim / 2 : kIdxDim;  // per token
   CUtensorMap keys, scales, qmap;
-  // codes: the pool as [num_blocks][64 tokens][128 B], one 64 x 128 box per page
+  // codes: the pool as [num_blocks][64 tokens][128 elements], one 64-row box per page; MXFP4
+  // nibbles are unpacked by the copy into one byte per element (8 data + 8 gap bytes per 16)
   {
     const uint64_t dims[3] = {(uint64_t)kIdxDim, (uint64_t)kBlock, (uint64_t)c.num_blocks};
-    const uint64_t strides[2] = {(uint64_t)kIdxDim, (uint64_t)c.row_stride};
+    const uint64_t strides[2] = {(uint64_t)code_bytes, (uint64_t)c.row_stride};
     const uint32_t box[3] = {(uint32_t)kIdxDim, (uint32_t)kBlock, 1};
-    if (!encode_tmap(&keys, CU_TENSOR_MAP_DATA_TYPE_UINT8, 3, index_base, dims, strides, box,
-                     CU_TENSOR_MAP_SWIZZLE_128B))
+    if (!encode_tmap(&keys, mx ? CU_TENSOR_MAP_DATA_TYPE_16U4_ALIGN16B : CU_TENSOR_MAP_DATA_TYPE_UINT8, 3, index_base,
+                     dims, strides, box, CU_TENSOR_MAP_SWIZZLE_128B))
       return DSA_ERR_CUDA;
   }
-  // scales: the pool as [num_blocks][256 B of fp32 scales], one-row boxes for gather4
+  // per-token scales (fp32, or four E8M0 bytes): the pool as [num_blocks][256 B], one-row boxes for gather4
   {
     const uint64_t dims[2] = {(uint64_t)kPageScaleBytes, (uint64_t)c.num_blocks};
     const uint64_t strides[1] = {(uint64_t)c.row_stride};
     const uint32_t box[2] = {(uint32_t)kPageScaleBytes, 1};
-    if (!encode_tmap(&scales, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, index_base + kPageCodeBytes, dims, strides, box,
+    if (!encode_tmap(&scales, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, index_base + kBlock * code_bytes, dims, strides, box,
                      CU_TENSOR_MAP_SWIZZLE_NONE))
       return DSA_ERR_CUDA;
   }
-  const int nq = bt.queries_per_seq;
   {
     const uint64_t rows = (uint64_t)bt.batch * nq * kIdxHeads;
     const uint64_t dims[2] = {(uint64_t)kIdxDim, rows};
@@ -428,11 +515,12 @@ dsa_status_t launch_index_scores_fp8(const dsa_paged_cache_t& c, const dsa_batch
   }
   IdxParams p{index_base, c.row_stride, c.num_blocks, bt.block_table, bt.max_blocks_per_seq, bt.seq_lens,
               bt.batch, bt.max_seq_len, head_w, scores, ld, status};
+  if (mx) return launch_nq<1, true>(p, keys, scales, qmap, st);
   switch (nq) {
-    case 1: return launch_nq<1>(p, keys, scales, qmap, st);
-    case 2: return launch_nq<2>(p, keys, scales, qmap, st);
-    case 3: return launch_nq<3>(p, keys, scales, qmap, st);
-    case 4: return launch_nq<4>(p, keys, scales, qmap, st);
+    case 1: return launch_nq<1, false>(p, keys, scales, qmap, st);
+    case 2: return launch_nq<2, false>(p, keys, scales, qmap, st);
+    case 3: return launch_nq<3, false>(p, keys, scales, qmap, st);
+    case 4: return launch_nq<4, false>(p, keys, scales, qmap, st);
     default: return DSA_ERR_UNSUPPORTED;
   }
 }

@@ -26,9 +26,9 @@ bool encode_tmap(CUtensorMap* map, CUtensorMapDataType dtype, int rank, const vo
 
 dsa_status_t launch_translate_pages(const dsa_paged_cache_t& c, const dsa_batch_t& bt, int64_t* latent_pages,
                                     int64_t* index_pages, int32_t* status, cudaStream_t st);
-dsa_status_t launch_index_scores_fp8(const dsa_paged_cache_t& c, const dsa_batch_t& bt, const uint8_t* q_index,
-                                     const float* head_w, float* scores, int64_t ld, int32_t* status,
-                                     cudaStream_t st);
+// FP8 or MXFP4 keys (MXFP4: one query row per sequence, else DSA_ERR_UNSUPPORTED).
+dsa_status_t launch_index_scores(const dsa_paged_cache_t& c, const dsa_batch_t& bt, const uint8_t* q_index,
+                                 const float* head_w, float* scores, int64_t ld, int32_t* status, cudaStream_t st);
 size_t topk_workspace_bytes(int rows, int max_row_len, int k);
 dsa_status_t launch_topk(const float* scores, int64_t ld, const int32_t* row_lens, const int32_t* seq_lens, int nq,
                          int rows, int max_row_len, int k, int32_t* out, void* workspace, int32_t* status,

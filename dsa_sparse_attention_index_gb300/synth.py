@@ -39,6 +39,7 @@ INDEX_PAGE = {KEY_FP8: BLOCK * (IDX_DIM + 4),     # 8,448 B
               KEY_MXFP4: BLOCK * (IDX_DIM // 2 + 4)}  # 4,352 B
 
 _E2M1_GRID = np.array([0.0, 0.5, 1.0, 1.5, 2.0, 3.0, 4.0, 6.0])
+_E2M1_MID = (_E2M1_GRID[1:] + _E2M1_GRID[:-1]) / 2   # 0.25 0.75 1.25 1.75 2.5 3.5 5
 
 
 @dataclasses.dataclass
@@ -94,7 +95,7 @@ def e4m3_encode(x: np.ndarray) -> np.ndarray:
     """Round to OCP E4M3 ('fn') codes, nearest-even, saturating at +-448."""
     import torch
 
-    t = torch.from_numpy(np.clip(np.asarray(x, dtype=np.float32), -448.0, 448.0))
+    t = torch.from_numpy(np.ascontiguousarray(x, dtype=np.float32)).clamp(-448.0, 448.0)
     return t.to(torch.float8_e4m3fn).view(torch.uint8).numpy()
 
 
@@ -112,20 +113,23 @@ def mxfp4_encode(x: np.ndarray):
     E2M1's largest exponent), elements rounded to nearest-even and clamped
     to +-6.  Returns (packed codes uint8 [n, 64], e8m0 uint8 [n, 4]); element
     2i sits in the low nibble of byte i."""
-    x = np.asarray(x, dtype=np.float64).reshape(-1, IDX_DIM // 32, 32)
-    amax = np.abs(x).max(axis=2)
-    with np.errstate(divide="ignore"):
-        e = np.where(amax > 0, np.floor(np.log2(np.where(amax > 0, amax, 1.0))) - 2, -127)
-    e = np.clip(e, -127, 127).astype(np.int64)
-    scaled = x / np.ldexp(1.0, e)[..., None]
-    mag = np.abs(scaled)
-    d = np.abs(mag[..., None] - _E2M1_GRID)
-    d = d + (np.arange(8) % 2) * 1e-12          # exact ties go to the even code
-    code = np.argmin(d, axis=-1).astype(np.uint8)
-    code = np.where(mag >= 6.0, 7, code).astype(np.uint8)
-    code = code | np.where(scaled < 0, 8, 0).astype(np.uint8)
-    code = code.reshape(-1, IDX_DIM)
+    import torch
+
+    x = torch.from_numpy(np.ascontiguousarray(x, dtype=np.float64)).reshape(-1, IDX_DIM // 32, 32)
+    amax = x.abs().amax(dim=2)
+    _, ex = torch.frexp(amax)                    # amax = m * 2^ex, m in [0.5, 1): floor(log2 amax) = ex - 1
+    e = torch.where(amax > 0, ex.to(torch.int64) - 1 - 2, torch.full_like(ex, -127, dtype=torch.int64))
+    e = e.clamp(-127, 127)
+    scaled = torch.ldexp(x, (-e).unsqueeze(-1).to(torch.float64))   # exact: a power-of-two scaling
+    mag = scaled.abs()
+    # nearest E2M1 magnitude: count the midpoints below |x|; at an exact midpoint
+    # this picks the lower code, so the three midpoints whose upper code is the
+    # even one move up (round half to even); |x| >= 6 lands on code 7 (6.0)
+    code = torch.bucketize(mag, torch.from_numpy(_E2M1_MID), right=False)
+    code = code + ((mag == 0.75) | (mag == 1.75) | (mag == 3.5)).to(code.dtype)
+    code = (code | torch.where(scaled < 0, 8, 0)).to(torch.uint8).reshape(-1, IDX_DIM).numpy()
     packed = (code[:, 0::2] | (code[:, 1::2] << 4)).astype(np.uint8)
+    e = e.numpy()
     e8m0 = (e + 127).astype(np.uint8).reshape(-1, IDX_DIM // 32)
     return packed, e8m0
 
