@@ -20,9 +20,9 @@
 //           over the block pool, 128-byte swizzle; MXFP4 nibbles are unpacked
 //           by the copy into byte containers) into a 5-6 stage code ring, and
 //           the four pages' scale rows in one tile::gather4 copy into a
-//           deeper scale ring; the lanes resolve the block-table rows of the
-//           next 32 units, and several lanes issue one unit's copies at once;
-//           the query tile of the current sequence goes into a 2-slot ring;
+//           deeper scale ring.  The two half-warps issue two units at once;
+//           the lanes resolve the block-table rows of the next 32 units; the
+//           query tiles go into a 2-slot ring, one sequence ahead;
 //   warp 1  MMA issuer: two M = 128 key sub-tiles per unit, N = 32*NQ
 //           query-heads, K = 128 in four K=32 steps, fp32 accumulators in a
 //           double-buffered TMEM tile.  FP8: tcgen05.mma kind::f8f6f4.
@@ -74,6 +74,8 @@ struct IdxParams {
   int32_t* status;
 };
 
+constexpr int kSfSlots = 4;  // MXFP4: TMEM scale-factor slots, decoupled from the accumulators
+
 template <int NQ>
 struct IdxSmem {
   static constexpr int kStages = NQ == 1 ? 6 : 5;       // code ring; keeps the CTA within 227 KB
@@ -84,8 +86,8 @@ struct IdxSmem {
   static constexpr int kOffScales = kOffQ + 2 * kQSlot;
   static constexpr int kOffBars = kOffScales + kScaleStages * kUnitScaleBytes;
   // barriers: code full/empty [S], scale full/empty [SS], acc full/empty [2],
-  // q full/empty [2], scale-factors staged [2], done
-  static constexpr int kNumBars = 2 * kStages + 2 * kScaleStages + 11;
+  // q full/empty [2], done, MXFP4 scale-factor slots staged/free [kSfSlots]
+  static constexpr int kNumBars = 2 * kStages + 2 * kScaleStages + 9 + 2 * kSfSlots;
   static constexpr int kOffMisc = kOffBars + kNumBars * 8;  // tmem slot, abort flag
   static constexpr int kOffPrefix = kOffMisc + 16;
   static size_t bytes(int batch) { return 1024 + kOffPrefix + 4 * (size_t)(batch + 1); }
@@ -121,9 +123,11 @@ __global__ void __launch_bounds__(idx_threads<MX>(), 1)
   constexpr int kSS = L::kScaleStages;
   constexpr int N = 32 * NQ;
   // TMEM: accumulators [2 slots][2 sub-tiles][N] at column 0; MXFP4 adds the
-  // keys' scale factors (4 columns per sub-tile and slot) and the queries' (2^0)
+  // keys' scale factors (4 columns per sub-tile, at 32-column steps, in
+  // kSfSlots slots) and the queries' (2^0)
   constexpr uint32_t kTmemCols = MX ? 512 : ((4 * N <= 128) ? 128 : (4 * N <= 256 ? 256 : 512));
-  constexpr uint32_t kSfaCol = 256, kSfbCol = 384;
+  constexpr uint32_t kSfaCol = 128, kSfbCol = kSfaCol + 64 * kSfSlots;
+  static_assert(!MX || kSfbCol + 4 <= kTmemCols, "TMEM columns");
   constexpr uint32_t kIdesc = MX ? make_idesc_mx(kFmtE2M1, kFmtE4M3, 128, N)
                                  : make_idesc(kFmtE4M3, kFmtE4M3, 0, 0, 128, N);
 
@@ -140,8 +144,9 @@ __global__ void __launch_bounds__(idx_threads<MX>(), 1)
   auto acce_bar = [&](int a) { return bars2 + 8u * (2 + a); };
   auto qf_bar = [&](int q) { return bars2 + 8u * (4 + q); };
   auto qe_bar = [&](int q) { return bars2 + 8u * (6 + q); };
-  auto sfr_bar = [&](int a) { return bars2 + 8u * (8 + a); };
-  const uint32_t done_bar = bars2 + 8u * 10;
+  const uint32_t done_bar = bars2 + 8u * 8;
+  auto sfr_bar = [&](int f) { return bars2 + 8u * (9 + f); };
+  auto sfe_bar = [&](int f) { return bars2 + 8u * (9 + kSfSlots + f); };
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + L::kOffMisc);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + L::kOffMisc + 4);
   int32_t* prefix = reinterpret_cast<int32_t*>(smem + L::kOffPrefix);
@@ -165,7 +170,10 @@ __global__ void __launch_bounds__(idx_threads<MX>(), 1)
       mbar_init(acce_bar(a), 4);
       mbar_init(qf_bar(a), 1);
       mbar_init(qe_bar(a), 1);
-      mbar_init(sfr_bar(a), 4);
+    }
+    for (int f = 0; f < kSfSlots; ++f) {
+      mbar_init(sfr_bar(f), 4);   // the four scale-staging warps
+      mbar_init(sfe_bar(f), 1);   // tcgen05.commit of the MMAs that read the slot
     }
     mbar_init(done_bar, 1);
     *abort_flag = 0;
@@ -227,9 +235,12 @@ __global__ void __launch_bounds__(idx_threads<MX>(), 1)
   if (u_begin < u_end) {
     if (warp == 0) {
       // ------------------------------------------------ TMA producer (one warp)
-      // The lanes resolve the block-table rows of the next 32 units while the
-      // current 32 are issued, so table reads never stall the rings.
+      // Two units per step: half-warp h (lanes 16h .. 16h+15) issues unit
+      // it + h, so the barrier operations and copies of both go out in the
+      // same instructions.  The lanes resolve the block-table rows of the next
+      // 32 units while the current 32 are issued.
       constexpr unsigned kAll = 0xffffffffu;
+      const int half = lane >> 4, hl = lane & 15;
       auto resolve = [&](int64_t g, int& rb, int& rnp, int (&rr)[kPagesPerUnit]) {
         const int64_t u = g + lane;
         rb = 0;
@@ -246,73 +257,97 @@ __global__ void __launch_bounds__(idx_threads<MX>(), 1)
           for (int q = 0; q < kPagesPerUnit; ++q) rr[q] = q < rnp ? bt[q] : 0;
         }
       };
+      // Query tiles go into the 2-slot ring in the order the MMA meets the
+      // sequences.  A load waits (blocking) only for sequences up to `need`,
+      // whose earlier units are all issued; one more is loaded ahead when its
+      // slot is already free.
+      const int q_last = first_seq(u_end - 1);
+      int q_seq = first_seq(u_begin);  // next sequence whose query tile is to be loaded
+      uint32_t qn = 0;                 // query tiles issued
+      auto issue_q = [&](int need) -> bool {
+        while (q_seq <= q_last) {
+          const int slot = qn & 1;
+          const uint32_t par = ((qn >> 1) & 1) ^ 1;
+          if (q_seq <= need) {
+            if (!mbar_wait(qe_bar(slot), par, abort_flag, p.status)) return false;
+          } else if (q_seq > need + 1 || !mbar_try_wait(qe_bar(slot), par)) {
+            break;
+          }
+          mbar_arrive_expect_tx(qf_bar(slot), L::kQSlot);
+          tma_load_2d(sbase + L::kOffQ + slot * L::kQSlot, &tmap_q, 0, q_seq * N, qf_bar(slot));
+          ++qn;
+          do {
+            ++q_seq;  // skip sequences without keys: the MMA never meets them
+          } while (q_seq <= q_last && prefix[q_seq + 1] == prefix[q_seq]);
+        }
+        return true;
+      };
       int cb, cnp, cr[kPagesPerUnit];
       resolve(u_begin, cb, cnp, cr);
       const uint64_t stream_policy = policy_evict_first();  // keys are read once per step
-      int cur_b = -1;
-      uint32_t it = 0, qn = 0;
+      uint32_t it = 0;
       bool ok = true;
       for (int64_t g = u_begin; ok && g < u_end; g += 32) {
         int nb, nnp, nr[kPagesPerUnit];
         resolve(g + 32, nb, nnp, nr);  // next group's rows, in flight meanwhile
         const int n = (int)((u_end - g) < 32 ? (u_end - g) : 32);
-        for (int l = 0; l < n; ++l, ++it) {
-          const int b = __shfl_sync(kAll, cb, l);
-          const int npages = __shfl_sync(kAll, cnp, l);
+        for (int l = 0; l < n; l += 2) {
+          const int lu = l + half;  // this half-warp's unit within the group
+          const bool valid = lu < n;
+          const int src = valid ? lu : l;
+          const int b = __shfl_sync(kAll, cb, src);
+          int npages = __shfl_sync(kAll, cnp, src);
+          if (!valid) npages = 0;
           int r[kPagesPerUnit];
 #pragma unroll
-          for (int q = 0; q < kPagesPerUnit; ++q) r[q] = __shfl_sync(kAll, cr[q], l);
+          for (int q = 0; q < kPagesPerUnit; ++q) r[q] = __shfl_sync(kAll, cr[q], src);
 #pragma unroll
           for (int q = 0; q < kPagesPerUnit; ++q) {
             if (q >= npages) r[q] = r[0];  // gather rows must be valid; unused pages repeat page 0
             if (r[q] < 0 || r[q] >= p.num_blocks) {
-              if (lane == 0) report(p.status, DSA_ERR_BOUNDS);
+              if (hl == 0 && valid) report(p.status, DSA_ERR_BOUNDS);
               r[q] = 0;  // read a valid row instead; the call's results are void
             }
           }
-          const int s = it % kStages, s2 = it % kSS;
-          if (lane == 0) {
-            if (b != cur_b) {
-              const int slot = qn & 1;
-              ok = mbar_wait(qe_bar(slot), ((qn >> 1) & 1) ^ 1, abort_flag, p.status);
-              if (ok) {
-                mbar_arrive_expect_tx(qf_bar(slot), L::kQSlot);
-                tma_load_2d(sbase + L::kOffQ + slot * L::kQSlot, &tmap_q, 0, b * N, qf_bar(slot));
-                ++qn;
-                cur_b = b;
-              }
-            }
-            ok = ok && mbar_wait(empty_bar(s), ((it / kStages) & 1) ^ 1, abort_flag, p.status);
-            ok = ok && mbar_wait(sce_bar(s2), ((it / kSS) & 1) ^ 1, abort_flag, p.status);
-            if (ok) {
+          const uint32_t uit = it + half;
+          const int s = uit % kStages, s2 = uit % kSS;
+          if (lane == 0) ok = issue_q(b);  // lane 0 holds the pair's first unit
+          ok = __shfl_sync(kAll, ok, 0);
+          bool okh = ok;
+          if (ok && hl == 0 && valid) {
+            okh = mbar_wait(empty_bar(s), ((uit / kStages) & 1) ^ 1, abort_flag, p.status) &&
+                  mbar_wait(sce_bar(s2), ((uit / kSS) & 1) ^ 1, abort_flag, p.status);
+            if (okh) {
               // an unpacking MXFP4 copy counts its packed source bytes (half what it writes)
               mbar_arrive_expect_tx(full_bar(s), npages * (MX ? kPageCodeBytes / 2 : kPageCodeBytes));
               mbar_arrive_expect_tx(scf_bar(s2), kUnitScaleBytes);
             }
           }
-          ok = __shfl_sync(kAll, ok, 0);
+          ok = __all_sync(kAll, okh);
           if (!ok) break;
-          // the copies of one unit go out from several lanes at once: lane q loads page q,
-          // lane kPagesPerUnit gathers the four pages' scale rows
-          if (lane < npages) {
-            const int rq = lane == 0 ? r[0] : (lane == 1 ? r[1] : (lane == 2 ? r[2] : r[3]));
-            tma_load_3d_hint(sbase + L::kOffA + s * kATileBytes + lane * kPageCodeBytes, &tmap_keys, 0, 0, rq,
+          // lane hl < npages of each half loads page hl; lane 4 of each half gathers the scale rows
+          if (hl < npages) {
+            const int rq = hl == 0 ? r[0] : (hl == 1 ? r[1] : (hl == 2 ? r[2] : r[3]));
+            tma_load_3d_hint(sbase + L::kOffA + s * kATileBytes + hl * kPageCodeBytes, &tmap_keys, 0, 0, rq,
                              full_bar(s), stream_policy);
-          } else if (lane == kPagesPerUnit) {
+          } else if (hl == kPagesPerUnit && valid) {
             tma_gather4(sbase + L::kOffScales + s2 * kUnitScaleBytes, &tmap_scales, 0, r[0], r[1], r[2], r[3],
                         scf_bar(s2));
           }
+          it += (l + 1 < n) ? 2 : 1;
         }
         cb = nb;
         cnp = nnp;
 #pragma unroll
         for (int q = 0; q < kPagesPerUnit; ++q) cr[q] = nr[q];
       }
+      if (lane == 0 && ok) issue_q(q_last);  // every unit is issued: remaining query tiles may wait
       if (lane == 0 && *abort_flag) {  // let copies already in flight land before the CTA exits
         for (uint32_t k = (it > kStages ? it - kStages : 0); k < it; ++k)
           mbar_wait_drain(full_bar(k % kStages), (k / kStages) & 1, kDrainNs);
         for (uint32_t k = (it > kSS ? it - kSS : 0); k < it; ++k)
           mbar_wait_drain(scf_bar(k % kSS), (k / kSS) & 1, kDrainNs);
+        for (uint32_t k = (qn > 2 ? qn - 2 : 0); k < qn; ++k) mbar_wait_drain(qf_bar(k & 1), (k >> 1) & 1, kDrainNs);
       }
     } else if (warp == 1 && lane == 0) {
       // ------------------------------------------------ MMA issuer
@@ -326,9 +361,9 @@ __global__ void __launch_bounds__(idx_threads<MX>(), 1)
           ++qn;
           cur_b = b;
         }
-        const int s = it % kStages, a = it & 1;
+        const int s = it % kStages, a = it & 1, f = it % kSfSlots;
         if (!mbar_wait(full_bar(s), (it / kStages) & 1, abort_flag, p.status)) break;
-        if (MX && !mbar_wait(sfr_bar(a), (it >> 1) & 1, abort_flag, p.status)) break;
+        if (MX && !mbar_wait(sfr_bar(f), (it / kSfSlots) & 1, abort_flag, p.status)) break;
         if (!mbar_wait(acce_bar(a), ((it >> 1) & 1) ^ 1, abort_flag, p.status)) break;
         tc_fence_after();
         const uint32_t b_base = sbase + L::kOffQ + ((qn - 1) & 1) * L::kQSlot;
@@ -341,13 +376,14 @@ __global__ void __launch_bounds__(idx_threads<MX>(), 1)
             const uint64_t bd = smem_desc(b_base + 32 * kk, 16, 1024, kLayoutSw128);
             if constexpr (MX)  // K step kk is E8M0 block kk: scale-factor byte kk
               mma_mxf8f6f4(tmem + (2 * a + sub) * N, ad, bd, kIdesc | mx_sf_ids(kk, kk),
-                           tmem + kSfaCol + 32 * (2 * a + sub), tmem + kSfbCol, kk > 0 ? 1u : 0u);
+                           tmem + kSfaCol + 32 * (2 * f + sub), tmem + kSfbCol, kk > 0 ? 1u : 0u);
             else
               mma_f8f6f4(tmem + (2 * a + sub) * N, ad, bd, kIdesc, kk > 0 ? 1u : 0u);
           }
         }
         mma_commit(accf_bar(a));
         mma_commit(empty_bar(s));   // the code stage is free once these MMAs have read it
+        if (MX) mma_commit(sfe_bar(f));
       }
       // all issued MMAs must finish before TMEM is released
       mma_commit(done_bar);
@@ -427,23 +463,23 @@ __global__ void __launch_bounds__(idx_threads<MX>(), 1)
       tmem_st4(lane_base + kSfbCol, 0x7F7F7F7Fu, 0x7F7F7F7Fu, 0x7F7F7F7Fu, 0x7F7F7F7Fu);
       uint32_t it = 0;
       for (int64_t u = u_begin; u < u_end; ++u, ++it) {
-        const int s2 = it % kSS, a = it & 1;
+        const int s2 = it % kSS, f = it % kSfSlots;
         bool ok = mbar_wait(scf_bar(s2), (it / kSS) & 1, abort_flag, p.status);
-        // slot a's scale factors were last read by the MMAs of unit it - 2
-        ok = ok && mbar_wait(accf_bar(a), ((it >> 1) & 1) ^ 1, abort_flag, p.status);
+        // slot f's scale factors were last read by the MMAs of unit it - kSfSlots
+        ok = ok && mbar_wait(sfe_bar(f), ((it / kSfSlots) & 1) ^ 1, abort_flag, p.status);
         if (!__all_sync(0xffffffffu, ok)) break;   // tcgen05.st is warp-collective
         tc_fence_after();
         const uint32_t* wsrc = scale_words + s2 * (kUnitScaleBytes / 4);
 #pragma unroll
         for (int sub = 0; sub < 2; ++sub) {
           const uint32_t* ws = wsrc + 128 * sub + lane;
-          tmem_st4(lane_base + kSfaCol + 32 * (2 * a + sub), ws[0], ws[32], ws[64], ws[96]);
+          tmem_st4(lane_base + kSfaCol + 32 * (2 * f + sub), ws[0], ws[32], ws[64], ws[96]);
         }
         tmem_st_wait();
         tc_fence_before();
         __syncwarp();
         if (lane == 0) {
-          mbar_arrive(sfr_bar(a));
+          mbar_arrive(sfr_bar(f));
           mbar_arrive(sce_bar(s2));
         }
       }
