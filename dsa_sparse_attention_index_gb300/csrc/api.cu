@@ -78,6 +78,16 @@ dsa_status_t check_batch(const dsa_batch_t* b) {
   return DSA_OK;
 }
 
+// Row shapes the indexer takes: MXFP4 keys one row per sequence; more than 4
+// rows per sequence (a prefill chunk) in groups of 4, at most 4096 groups.
+dsa_status_t check_index_rows(const dsa_paged_cache_t* c, const dsa_batch_t* b) {
+  const int nq = b->queries_per_seq;
+  if (c->key_format == DSA_KEY_MXFP4 && nq != 1) return DSA_ERR_UNSUPPORTED;
+  if (nq > 4 && nq % 4 != 0) return DSA_ERR_UNSUPPORTED;
+  if ((int64_t)b->batch * (nq > 4 ? nq / 4 : 1) > 4096) return DSA_ERR_UNSUPPORTED;
+  return DSA_OK;
+}
+
 int64_t round_ld(int max_len) { return ((int64_t)std::max(max_len, 1) + 3) & ~int64_t(3); }
 
 }  // namespace
@@ -141,6 +151,7 @@ dsa_status_t dsa_index_scores(const dsa_paged_cache_t* cache, const dsa_batch_t*
   dsa_status_t s;
   if ((s = check_cache(cache)) != DSA_OK) return s;
   if ((s = check_batch(batch)) != DSA_OK) return s;
+  if ((s = check_index_rows(cache, batch)) != DSA_OK) return s;
   if (!dev_status) return DSA_ERR_INVALID_ARG;
   if (batch->batch == 0) return DSA_OK;
   if (!q_index || !head_w || !scores || !aligned(q_index, 16) || !aligned(head_w, 16) || !aligned(scores, 16))
@@ -214,6 +225,7 @@ dsa_status_t dsa_decode_step(const dsa_paged_cache_t* cache, const dsa_batch_t* 
   dsa_status_t s;
   if ((s = check_cache(cache)) != DSA_OK) return s;
   if ((s = check_batch(batch)) != DSA_OK) return s;
+  if ((s = check_index_rows(cache, batch)) != DSA_OK) return s;
   if (k < 1 || k > DSA_MAX_TOPK || !dev_status) return DSA_ERR_INVALID_ARG;
   const int rows = batch->batch * batch->queries_per_seq;
   if (rows == 0) return DSA_OK;

@@ -72,6 +72,13 @@ struct IdxParams {
   float* scores;
   int64_t ld;
   int32_t* status;
+  // A sequence with nq_real query rows runs as `groups` pseudo-sequences of NQ
+  // rows each (decode: groups = 1, nq_real = NQ).  Pseudo-sequence b of real
+  // sequence b / groups has length L - nq_real + NQ * (b % groups + 1), so its
+  // row q sees L - (nq_real - 1) + NQ * (b % groups) + q tokens: the causal
+  // rows of a prefill chunk.
+  int32_t groups;
+  int32_t nq_real;
 };
 
 constexpr int kSfSlots = 4;  // MXFP4: TMEM scale-factor slots, decoupled from the accumulators
@@ -186,18 +193,29 @@ __global__ void __launch_bounds__(idx_threads<MX>(), 1)
     tmem_alloc(smem_u32(tmem_slot), kTmemCols);
     tmem_relinquish();
   }
+  const int nb = p.batch * p.groups;  // pseudo-sequences
+  // length of pseudo-sequence b (the real length clamped to [0, cap], then the
+  // group's causal prefix)
+  const bool grouped = p.groups > 1;
+  auto real_seq = [&](int b) { return grouped ? b / p.groups : b; };
+  auto seq_len_of = [&](int b) {
+    int len = p.seq_lens[real_seq(b)];
+    len = len < 0 ? 0 : (len > cap ? cap : len);
+    if (grouped) {
+      len += NQ * (b % p.groups + 1) - p.nq_real;
+      len = len < 0 ? 0 : len;
+    }
+    return len;
+  };
   if (warp == 0) {
     int run = 0;
-    for (int b0 = 0; b0 < p.batch; b0 += 32) {
+    for (int b0 = 0; b0 < nb; b0 += 32) {
       int b = b0 + lane;
       int units = 0;
-      if (b < p.batch) {
-        int len = p.seq_lens[b];
-        if (len < 0 || len > cap) {
-          report(p.status, DSA_ERR_BOUNDS);
-          len = len < 0 ? 0 : cap;
-        }
-        units = (len + kUnitKeys - 1) / kUnitKeys;
+      if (b < nb) {
+        const int raw = p.seq_lens[real_seq(b)];
+        if (raw < 0 || raw > cap) report(p.status, DSA_ERR_BOUNDS);
+        units = (seq_len_of(b) + kUnitKeys - 1) / kUnitKeys;
       }
       int incl = units;
 #pragma unroll
@@ -205,26 +223,22 @@ __global__ void __launch_bounds__(idx_threads<MX>(), 1)
         int v = __shfl_up_sync(0xffffffffu, incl, o);
         if (lane >= o) incl += v;
       }
-      if (b < p.batch) prefix[b] = run + incl - units;
+      if (b < nb) prefix[b] = run + incl - units;
       run += __shfl_sync(0xffffffffu, incl, 31);
     }
-    if (lane == 0) prefix[p.batch] = run;
+    if (lane == 0) prefix[nb] = run;
   }
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
 
-  const int64_t total = prefix[p.batch];
+  const int64_t total = prefix[nb];
   const int64_t u_begin = total * blockIdx.x / gridDim.x;
   const int64_t u_end = total * (blockIdx.x + 1) / gridDim.x;
 
-  auto seq_len_of = [&](int b) {
-    int len = p.seq_lens[b];
-    return len < 0 ? 0 : (len > cap ? cap : len);
-  };
   auto first_seq = [&](int64_t u) {
-    int lo = 0, hi = p.batch - 1;  // last b with prefix[b] <= u
+    int lo = 0, hi = nb - 1;  // last b with prefix[b] <= u
     while (lo < hi) {
       int mid = (lo + hi + 1) >> 1;
       if (prefix[mid] <= u) lo = mid; else hi = mid - 1;
@@ -252,7 +266,7 @@ __global__ void __launch_bounds__(idx_threads<MX>(), 1)
           const int j = (int)(u - prefix[rb]);
           const int rem = seq_len_of(rb) - kUnitKeys * j;
           rnp = min(kPagesPerUnit, (rem + kBlock - 1) / kBlock);
-          const int32_t* bt = p.block_table + (int64_t)rb * p.max_blocks + kPagesPerUnit * j;
+          const int32_t* bt = p.block_table + (int64_t)real_seq(rb) * p.max_blocks + kPagesPerUnit * j;
 #pragma unroll
           for (int q = 0; q < kPagesPerUnit; ++q) rr[q] = q < rnp ? bt[q] : 0;
         }
@@ -354,7 +368,7 @@ __global__ void __launch_bounds__(idx_threads<MX>(), 1)
       int cursor = first_seq(u_begin), cur_b = -1;
       uint32_t it = 0, qn = 0;
       for (int64_t u = u_begin; u < u_end; ++u, ++it) {
-        const int b = seq_of_unit(prefix, p.batch, u, cursor);
+        const int b = seq_of_unit(prefix, nb, u, cursor);
         if (b != cur_b) {
           if (cur_b >= 0) mma_commit(qe_bar((qn - 1) & 1));
           if (!mbar_wait(qf_bar(qn & 1), (qn >> 1) & 1, abort_flag, p.status)) break;
@@ -397,7 +411,7 @@ __global__ void __launch_bounds__(idx_threads<MX>(), 1)
       const uint64_t keep_policy = policy_evict_last();  // the top-k reads the scores next
       uint32_t it = 0;
       for (int64_t u = u_begin; u < u_end; ++u, ++it) {
-        const int b = seq_of_unit(prefix, p.batch, u, cursor);
+        const int b = seq_of_unit(prefix, nb, u, cursor);
         if (b != cur_b) {
 #pragma unroll
           for (int q = 0; q < NQ; ++q) {
@@ -504,9 +518,9 @@ dsa_status_t launch_nq(const IdxParams& p, const CUtensorMap& keys, const CUtens
       return DSA_ERR_CUDA;
     attr_set[dev] = true;
   }
-  const int64_t units_bound = (int64_t)p.batch * ((p.max_seq_len + kUnitKeys - 1) / kUnitKeys);
+  const int64_t units_bound = (int64_t)p.batch * p.groups * ((p.max_seq_len + kUnitKeys - 1) / kUnitKeys);
   const int grid = (int)std::max<int64_t>(1, std::min<int64_t>(units_bound, num_sms()));
-  indexer_kernel<NQ, MX><<<grid, idx_threads<MX>(), IdxSmem<NQ>::bytes(p.batch), st>>>(keys, scales, q, p);
+  indexer_kernel<NQ, MX><<<grid, idx_threads<MX>(), IdxSmem<NQ>::bytes(p.batch * p.groups), st>>>(keys, scales, q, p);
   return launch_status();
 }
 
@@ -514,10 +528,13 @@ dsa_status_t launch_nq(const IdxParams& p, const CUtensorMap& keys, const CUtens
 
 dsa_status_t launch_index_scores(const dsa_paged_cache_t& c, const dsa_batch_t& bt, const uint8_t* q_index,
                                  const float* head_w, float* scores, int64_t ld, int32_t* status, cudaStream_t st) {
-  if (bt.batch > kMaxBatch) return DSA_ERR_UNSUPPORTED;
   const bool mx = c.key_format == DSA_KEY_MXFP4;
   const int nq = bt.queries_per_seq;
   if (mx && nq != 1) return DSA_ERR_UNSUPPORTED;
+  // more than 4 rows per sequence (a prefill chunk): groups of 4 causal rows
+  if (nq > 4 && nq % 4 != 0) return DSA_ERR_UNSUPPORTED;
+  const int nq_k = nq > 4 ? 4 : nq, groups = nq / nq_k;
+  if ((int64_t)bt.batch * groups > kMaxBatch) return DSA_ERR_UNSUPPORTED;
   const uint8_t* index_base = static_cast<const uint8_t*>(c.base) + c.index_off;
   const int code_bytes = mx ? kIdxDim / 2 : kIdxDim;  // per token
   CUtensorMap keys, scales, qmap;
@@ -544,15 +561,15 @@ dsa_status_t launch_index_scores(const dsa_paged_cache_t& c, const dsa_batch_t& 
     const uint64_t rows = (uint64_t)bt.batch * nq * kIdxHeads;
     const uint64_t dims[2] = {(uint64_t)kIdxDim, rows};
     const uint64_t strides[1] = {(uint64_t)kIdxDim};
-    const uint32_t box[2] = {(uint32_t)kIdxDim, (uint32_t)(kIdxHeads * nq)};
+    const uint32_t box[2] = {(uint32_t)kIdxDim, (uint32_t)(kIdxHeads * nq_k)};
     if (!encode_tmap(&qmap, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, q_index, dims, strides, box,
                      CU_TENSOR_MAP_SWIZZLE_128B))
       return DSA_ERR_CUDA;
   }
   IdxParams p{index_base, c.row_stride, c.num_blocks, bt.block_table, bt.max_blocks_per_seq, bt.seq_lens,
-              bt.batch, bt.max_seq_len, head_w, scores, ld, status};
+              bt.batch, bt.max_seq_len, head_w, scores, ld, status, groups, nq};
   if (mx) return launch_nq<1, true>(p, keys, scales, qmap, st);
-  switch (nq) {
+  switch (nq_k) {
     case 1: return launch_nq<1, false>(p, keys, scales, qmap, st);
     case 2: return launch_nq<2, false>(p, keys, scales, qmap, st);
     case 3: return launch_nq<3, false>(p, keys, scales, qmap, st);

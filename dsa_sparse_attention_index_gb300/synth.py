@@ -246,6 +246,9 @@ WORKLOADS = {
     "longctx_b32_l64k-160k": dict(seq_lens=None, nq=1, heavy_tail=0.10),
     # 1M-token decode with MXFP4 index keys: batch 4
     "mxfp4_b4_l1m": dict(seq_lens=[1 << 20] * 4, nq=1, key_format=KEY_MXFP4),
+    # smaller cases of the same shapes for profiler captures (inputs still larger than L2)
+    "longctx_b32_l64k": dict(seq_lens=[65536] * 32, nq=1, heavy_tail=0.1),
+    "mxfp4_b8_l256k": dict(seq_lens=[1 << 18] * 8, nq=1, key_format=KEY_MXFP4),
     # chunked-prefill append: 2048 new query rows on a 151,552-token prefix
     "prefill_q2048_l153600": dict(seq_lens=[153600], nq=2048),
 }

@@ -52,7 +52,7 @@ extern "C" {
 #define DSA_LATENT_DIM 576       /* latent width: keys use all 576 columns */
 #define DSA_VALUE_DIM 512        /* values are the first 512 latent columns */
 #define DSA_MAX_TOPK 2048        /* top-k of the model; also the largest k accepted */
-#define DSA_MAX_QUERIES_PER_SEQ 4
+#define DSA_MAX_QUERIES_PER_SEQ 2048 /* draft rows (1..4) or a prefill chunk (a multiple of 4) */
 #define DSA_TOPK_NOALLOC_MAX_ROWS 64  /* row limit of dsa_topk_noalloc */
 
 typedef enum dsa_status {
@@ -91,7 +91,10 @@ typedef struct dsa_batch {
   const int32_t* seq_lens;     /* device int32 [batch]: context length incl. the current token(s) */
   int32_t max_blocks_per_seq;
   int32_t batch;
-  int32_t queries_per_seq;     /* nq: 1 (plain decode) .. DSA_MAX_QUERIES_PER_SEQ (draft rows) */
+  int32_t queries_per_seq;     /* nq: 1 (plain decode), 2..4 (speculative-verify draft rows) or,
+                                  for a chunked prefill, a multiple of 4 up to
+                                  DSA_MAX_QUERIES_PER_SEQ; row j of a sequence sees its first
+                                  seq_len - (nq - 1) + j tokens (causal) */
   int32_t max_seq_len;         /* host-known upper bound of seq_lens; sizes grids and scores */
 } dsa_batch_t;
 
@@ -127,6 +130,9 @@ dsa_status_t dsa_translate_pages(const dsa_paged_cache_t* cache, const dsa_batch
  * FP8 keys: s[t] = sum_h w[h] * max(0, scale_t * (q_h . k_t)).
  * MXFP4 keys: q_h . k_t = sum_{blk<4} 2^(E[t,blk]-127) * sum_{d in blk} q_hd * e2m1(k_td),
  * and scale_t = 1.  Tensor-core accumulation is fp32.
+ * rows = batch * queries_per_seq.  MXFP4 keys take one row per sequence, and
+ * more than 4 rows per sequence must be a multiple of 4; otherwise, and when
+ * batch * queries_per_seq / 4 exceeds 4096, DSA_ERR_UNSUPPORTED.
  */
 dsa_status_t dsa_index_scores(const dsa_paged_cache_t* cache, const dsa_batch_t* batch,
                               const uint8_t* q_index, const float* head_w,

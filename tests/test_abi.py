@@ -54,9 +54,17 @@ def test_host_validation_without_device(lib):
     assert lib.sparse_mla_decode(ctypes.byref(c), ctypes.byref(b), None, None, 2048, 1.0, None, None, None, 0, None,
                                  None) == B.ERR_INVALID_ARG
     c.row_stride = 45312
-    b.queries_per_seq = 5
-    assert lib.dsa_decode_step(ctypes.byref(c), ctypes.byref(b), None, None, None, 2048, 1.0, None, None, None, 0,
-                               None, None, 0, None, None) == B.ERR_UNSUPPORTED
+    b.block_table, b.seq_lens = 128 * 2000, 128 * 3000  # fake device pointers, never dereferenced here
+    for nq in (5, 2049, 0):  # > 4 rows must come in groups of 4; at most 2048; at least 1
+        b.queries_per_seq = nq
+        assert lib.dsa_decode_step(ctypes.byref(c), ctypes.byref(b), None, None, None, 2048, 1.0, None, None, None,
+                                   0, None, None, 0, None, None) == B.ERR_UNSUPPORTED
+    b.queries_per_seq = 2
+    c.key_format = B.KEY_MXFP4  # MXFP4 keys: one row per sequence
+    c.row_stride, c.index_off = 41216, 36864
+    assert lib.dsa_index_scores(ctypes.byref(c), ctypes.byref(b), None, None, None, 100, None,
+                                None) == B.ERR_UNSUPPORTED
+    c.key_format, c.row_stride = B.KEY_FP8_E4M3, 45312
     assert lib.dsa_topk(None, 0, None, 1, 10, 0, None, None, 0, None, None) == B.ERR_INVALID_ARG  # k = 0
     assert lib.dsa_topk(None, 0, None, 1, 10, 4096, None, None, 0, None, None) == B.ERR_INVALID_ARG  # k > 2048
 
