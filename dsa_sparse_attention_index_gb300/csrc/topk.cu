@@ -5,9 +5,18 @@
 // "then keep the top 2,048 tokens"; fused-decode section: an exact top-k
 // selection kernel).  Equal scores go to the lower token index, so the
 // selected set is unique; it is written in ascending token order with -1
-// padding when a row has fewer than k tokens.
+// padding when a row has fewer than k tokens.  Scores are compared as
+// order-preserving 32-bit keys (integer radix).
 //
-// Scores are compared as order-preserving 32-bit keys (integer radix).
+// Rows up to 8 x 40,960 tokens: one kernel, a thread-block cluster per row
+// (topk_resident_kernel).  Each CTA of the cluster keeps its slice of the
+// row as keys in shared memory, read once from L2; up to three digit passes
+// (12, 12 and 8 bits) find the k-th key, each pass merging the CTAs'
+// histograms through distributed shared memory; ties on the k-th key go to
+// the lowest indices in CTA-rank and token order; a cluster-wide scan then
+// writes the chosen indices in ascending order.  No workspace is used.
+//
+// Longer rows (the 1M-token rows) take four kernels over a workspace:
 //   1. hist:    multi-CTA per row: 4096-bin histogram of the key's top 12
 //               bits, merged into a per-row global histogram.
 //   2. threshold: one CTA per row finds the bin T holding the k-th largest
@@ -21,10 +30,10 @@
 //               shared-memory bitmap of the index range.  If the candidate
 //               buffer overflowed (heavily tied scores) it re-derives the
 //               candidates from the scores directly.
-// The multi-CTA split keeps all SMs busy for the few-long-rows case (4 rows
-// of 1M tokens) as well as for many shorter rows.
 #include <algorithm>
 #include <mutex>
+
+#include <cooperative_groups.h>
 
 #include "common.cuh"
 #include "internal.h"
@@ -475,6 +484,273 @@ __global__ void __launch_bounds__(kFinalThreads) topk_final_kernel(const float* 
   for (int i = (int)written + tid; i < k; i += kFinalThreads) o[i] = -1;
 }
 
+// ---------------------------------------------------------------- row-resident path
+namespace cg = cooperative_groups;
+
+constexpr int kResKeys = 40960;     // keys per CTA in shared memory (160 KB)
+constexpr int kResThreads = kFinalThreads;
+constexpr int kResWarps = kResThreads / 32;
+constexpr int kResMaxCluster = 8;   // portable cluster size: rows up to 327,680 tokens
+// shared memory: keys[kResKeys] | h1[4096] | h2[4096] | h3[256] | g[4096] | scan[32] | misc[32]
+constexpr size_t kResSmem = 4 * ((size_t)kResKeys + 3 * kBins + 256 + 64);
+
+// Warp-wide exclusive prefix sum of one value per lane; `total` gets the sum.
+__device__ __forceinline__ uint32_t warp_excl_scan(uint32_t v, uint32_t& total) {
+  const int lane = threadIdx.x & 31;
+  uint32_t x = v;
+#pragma unroll
+  for (int d = 1; d < 32; d <<= 1) {
+    const uint32_t u = __shfl_up_sync(0xffffffffu, x, d);
+    if (lane >= d) x += u;
+  }
+  total = __shfl_sync(0xffffffffu, x, 31);
+  return x - v;
+}
+
+template <int C>
+__global__ void __launch_bounds__(kResThreads, 1)
+    topk_resident_kernel(const float* __restrict__ scores, int64_t ld, const int32_t* row_lens,
+                         const int32_t* seq_lens, int nq, int cap, int k, int32_t* out, int32_t* status) {
+  cg::cluster_group cluster = cg::this_cluster();
+  const int c = (int)cluster.block_rank();
+  const int r = blockIdx.x / C, tid = threadIdx.x, lane = tid & 31, wid = tid >> 5;
+  auto csync = [&]() {  // a one-CTA cluster needs only the block barrier
+    if (C == 1) __syncthreads();
+    else cluster.sync();
+  };
+  extern __shared__ __align__(16) uint8_t smem_raw[];
+  uint32_t* keys = reinterpret_cast<uint32_t*>(smem_raw);
+  uint32_t* h1 = keys + kResKeys;
+  uint32_t* h2 = h1 + kBins;
+  uint32_t* h3 = h2 + kBins;  // 256 bins
+  uint32_t* g = h3 + 256;     // the cluster's histogram of the current digit
+  uint32_t* scan = g + kBins;
+  uint32_t* misc = scan + 32;
+
+  const int len = row_len(row_lens, seq_lens, nq, r, cap, c == 0 ? status : nullptr);
+  int32_t* o = out + (int64_t)r * k;
+  if (len <= k) {  // the same branch for every CTA of the cluster
+    if (c == 0)
+      for (int i = tid; i < k; i += kResThreads) o[i] = i < len ? i : -1;
+    return;
+  }
+  // this CTA's slice of the row: S tokens from `start` (S a multiple of 4)
+  const int S = (((len + C - 1) / C) + 3) & ~3;
+  const int start = c * S;
+  const int n = max(0, min(S, len - start));
+  const int n4 = (n + 3) >> 2;  // 4-key groups; the last one is padded with key 0 (below every score)
+
+  // ---- 1. keys into shared memory, histogram of the first digit (bits 31..20)
+  for (int i = tid; i < (2 * kBins + 256) / 4; i += kResThreads) reinterpret_cast<uint4*>(h1)[i] = make_uint4(0, 0, 0, 0);
+  __syncthreads();
+  {
+    const float* row = scores + (int64_t)r * ld + start;
+    const float4* row4 = reinterpret_cast<const float4*>(row);
+    const int full4 = n >> 2;
+    for (int i0 = 0; i0 < n4; i0 += 8 * kResThreads) {
+      float4 v[8];  // eight 16-byte loads in flight per thread
+#pragma unroll
+      for (int u = 0; u < 8; ++u) {
+        const int i = i0 + u * kResThreads + tid;
+        if (i < full4) {
+          v[u] = row4[i];
+        } else if (i < n4) {  // the row's ragged end
+          const int b = 4 * i;
+          v[u].x = row[b];
+          v[u].y = b + 1 < n ? row[b + 1] : __uint_as_float(0x7FC00000u);
+          v[u].z = b + 2 < n ? row[b + 2] : __uint_as_float(0x7FC00000u);
+          v[u].w = b + 3 < n ? row[b + 3] : __uint_as_float(0x7FC00000u);
+        }
+      }
+#pragma unroll
+      for (int u = 0; u < 8; ++u) {
+        const int i = i0 + u * kResThreads + tid;
+        if (i < n4) {
+          const uint4 kk = make_uint4(score_key(v[u].x), score_key(v[u].y), score_key(v[u].z), score_key(v[u].w));
+          reinterpret_cast<uint4*>(keys)[i] = kk;
+          const bool pad = 4 * i + 3 >= n;  // padding keys are not counted
+          atomicAdd(&h1[kk.x >> 20], 1u);
+          if (!pad || 4 * i + 1 < n) atomicAdd(&h1[kk.y >> 20], 1u);
+          if (!pad || 4 * i + 2 < n) atomicAdd(&h1[kk.z >> 20], 1u);
+          if (!pad) atomicAdd(&h1[kk.w >> 20], 1u);
+        }
+      }
+    }
+  }
+  // the cluster-wide histogram: every CTA sums its peers' copies (distributed
+  // shared memory), all C loads of a bin in flight together
+  auto merge = [&](uint32_t* local, int nbins) {
+    csync();
+    for (int i = tid; i < nbins; i += kResThreads) {
+      uint32_t x[C];
+#pragma unroll
+      for (int q = 0; q < C; ++q) x[q] = C == 1 ? local[i] : cluster.map_shared_rank(local, q)[i];
+      uint32_t sum = 0;
+#pragma unroll
+      for (int q = 0; q < C; ++q) sum += x[q];
+      g[i] = sum;
+    }
+    __syncthreads();
+  };
+  merge(h1, kBins);
+  uint32_t need = (uint32_t)k, pop;
+  int digit;
+  pick_digit(g, kBins, scan, need, digit, pop);
+  // Keys whose bits above `shift` exceed `prefix` are taken; keys equal to it on
+  // those bits form the threshold group, taken whole unless `tie` (only on the
+  // full 32 bits), where the first `quota` of them in token order are taken.
+  uint32_t prefix = (uint32_t)digit;
+  int shift = 20;
+  bool tie = false;
+  uint32_t quota = 0;
+  const uint4* keys4 = reinterpret_cast<const uint4*>(keys);
+  if (need != pop) {
+    // ---- 2. second digit (bits 19..8) within the threshold group (keys past
+    //         the slice's end are skipped by index)
+    for (int i = tid; i < n4; i += kResThreads) {
+      const uint4 kk = keys4[i];
+      const uint32_t a[4] = {kk.x, kk.y, kk.z, kk.w};
+#pragma unroll
+      for (int j = 0; j < 4; ++j)
+        if ((a[j] >> 20) == prefix && 4 * i + j < n) atomicAdd(&h2[(a[j] >> 8) & 0xFFFu], 1u);
+    }
+    merge(h2, kBins);
+    pick_digit(g, kBins, scan, need, digit, pop);
+    prefix = (prefix << 12) | (uint32_t)digit;
+    shift = 8;
+    if (need != pop) {
+      // ---- 3. last digit (bits 7..0)
+      for (int i = tid; i < n4; i += kResThreads) {
+        const uint4 kk = keys4[i];
+        const uint32_t a[4] = {kk.x, kk.y, kk.z, kk.w};
+#pragma unroll
+        for (int j = 0; j < 4; ++j)
+          if ((a[j] >> 8) == prefix && 4 * i + j < n) atomicAdd(&h3[a[j] & 0xFFu], 1u);
+      }
+      merge(h3, 256);
+      pick_digit(g, 256, scan, need, digit, pop);
+      prefix = (prefix << 8) | (uint32_t)digit;
+      shift = 0;
+      if (need != pop) {
+        // equal keys: `need` of them, lowest indices first; lower CTA ranks hold lower indices
+        tie = true;
+        uint32_t before = 0;
+#pragma unroll
+        for (int q = 0; q < C; ++q)
+          if (q < c) before += cluster.map_shared_rank(h3, q)[digit];
+        const uint32_t mine = h3[digit];
+        quota = need > before ? min(need - before, mine) : 0u;
+      }
+    }
+  }
+
+  // ---- 4. emit in ascending token order.  Warp w owns a contiguous run of
+  //         4-key groups; each step covers 128 keys (4 per lane, in lane order).
+  const int wg = (n4 + kResWarps - 1) / kResWarps;  // groups per warp
+  const int g0 = min(n4, wid * wg), g1 = min(n4, g0 + wg);
+  auto classify = [&](int i, uint32_t& gt, uint32_t& eq) {  // bit j: key 4i+j above / in the group
+    gt = eq = 0;
+    if (i < g1) {
+      const uint4 kk = keys4[i];
+      const uint32_t a[4] = {kk.x, kk.y, kk.z, kk.w};
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        const uint32_t v = a[j] >> shift;
+        const bool in = 4 * i + j < n;
+        gt |= (uint32_t)(in && v > prefix) << j;
+        eq |= (uint32_t)(in && v == prefix) << j;
+      }
+    }
+  };
+  uint32_t cnt_gt = 0, cnt_eq = 0;
+  for (int i = g0 + lane; i - lane < g1; i += 32) {
+    uint32_t gt, eq;
+    classify(i, gt, eq);
+    cnt_gt += __popc(gt);
+    cnt_eq += __popc(eq);
+  }
+  cnt_gt = __reduce_add_sync(0xffffffffu, cnt_gt);
+  cnt_eq = __reduce_add_sync(0xffffffffu, cnt_eq);
+  if (lane == 0) {
+    scan[wid] = cnt_eq;
+    misc[1 + wid] = cnt_gt;
+  }
+  __syncthreads();
+  uint32_t eq_before = 0, sel_before = 0, sel_total = 0, eq_take = 0;
+  for (int w = 0; w < kResWarps; ++w) {
+    const uint32_t e = scan[w], gtw = misc[1 + w];
+    const uint32_t take_e = !tie ? e : (eq_before >= quota ? 0u : min(e, quota - eq_before));
+    if (w < wid) sel_before += gtw + take_e;
+    if (w == wid) eq_take = take_e;
+    sel_total += gtw + take_e;
+    eq_before += e;
+  }
+  if (tid == 0) misc[0] = sel_total;
+  csync();
+  uint32_t offset = 0, total = 0;
+#pragma unroll
+  for (int q = 0; q < C; ++q) {
+    const uint32_t x = C == 1 ? misc[0] : cluster.map_shared_rank(misc, q)[0];
+    offset += q < c ? x : 0u;
+    total += x;
+  }
+  csync();  // no CTA leaves while a peer may still read its shared memory
+  if (c == 0 && tid == 0 && total != (uint32_t)k) report(status, DSA_ERR_BOUNDS);  // consistency check
+  uint32_t pos = offset + sel_before, eq_seen = 0;
+  for (int i = g0 + lane; i - lane < g1; i += 32) {
+    uint32_t gt, eq;
+    classify(i, gt, eq);
+    uint32_t eq_tot;
+    const uint32_t eq_pre = warp_excl_scan(__popc(eq), eq_tot);  // equal keys before this lane's
+    uint32_t take = gt;
+#pragma unroll
+    for (int j = 0; j < 4; ++j)
+      if ((eq >> j) & 1u) {
+        if (eq_seen + eq_pre + __popc(eq & ((1u << j) - 1u)) < eq_take) take |= 1u << j;
+      }
+    uint32_t t_tot;
+    uint32_t p = pos + warp_excl_scan(__popc(take), t_tot);
+#pragma unroll
+    for (int j = 0; j < 4; ++j)
+      if ((take >> j) & 1u) {
+        if (p < (uint32_t)k) o[p] = start + 4 * i + j;
+        ++p;
+      }
+    pos += t_tot;
+    eq_seen += eq_tot;
+  }
+}
+
+template <int C>
+dsa_status_t launch_resident(const float* scores, int64_t ld, const int32_t* row_lens, const int32_t* seq_lens,
+                             int nq, int rows, int cap, int k, int32_t* out, int32_t* status, cudaStream_t st) {
+  static bool attr_set[64] = {};
+  int dev = 0;
+  cudaGetDevice(&dev);
+  if (dev < 64 && !attr_set[dev]) {
+    if (cuda_status(cudaFuncSetAttribute(topk_resident_kernel<C>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         (int)kResSmem)) != DSA_OK)
+      return DSA_ERR_CUDA;
+    attr_set[dev] = true;
+  }
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3((unsigned)(rows * C));
+  cfg.blockDim = dim3(kResThreads);
+  cfg.dynamicSmemBytes = kResSmem;
+  cfg.stream = st;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = C;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  if (cuda_status(cudaLaunchKernelEx(&cfg, topk_resident_kernel<C>, scores, ld, row_lens, seq_lens, nq, cap, k,
+                                     out, status)) != DSA_OK)
+    return DSA_ERR_CUDA;
+  return launch_status();
+}
+
 size_t ws_bytes(int rows, int k) {
   auto al = [](size_t x) { return (x + 255) & ~size_t(255); };
   return al((size_t)rows * kBins * 4) + al((size_t)rows * 16) + al((size_t)rows * k * 4) +
@@ -494,6 +770,24 @@ dsa_status_t launch_topk(const float* scores, int64_t ld, const int32_t* row_len
                          int rows, int max_row_len, int k, int32_t* out, void* workspace, int32_t* status,
                          cudaStream_t st) {
   if (rows == 0) return DSA_OK;
+  // row-resident path: one cluster per row, enough CTAs to hold the row and,
+  // for few rows, to spread them over the SMs (at least 8,192 keys per CTA)
+  const int c_min = (max_row_len + kResKeys - 1) / kResKeys;
+  const int c_fill = std::min(num_sms() / std::max(rows, 1), max_row_len / 8192);
+  const int cluster = std::min(kResMaxCluster, std::max(c_min, std::max(c_fill, 1)));
+  if (max_row_len > k && c_min <= kResMaxCluster) {
+    // row-resident path: one cluster of `cluster` CTAs per row, no workspace
+    switch (cluster) {
+      case 1: return launch_resident<1>(scores, ld, row_lens, seq_lens, nq, rows, max_row_len, k, out, status, st);
+      case 2: return launch_resident<2>(scores, ld, row_lens, seq_lens, nq, rows, max_row_len, k, out, status, st);
+      case 3: return launch_resident<3>(scores, ld, row_lens, seq_lens, nq, rows, max_row_len, k, out, status, st);
+      case 4: return launch_resident<4>(scores, ld, row_lens, seq_lens, nq, rows, max_row_len, k, out, status, st);
+      case 5: return launch_resident<5>(scores, ld, row_lens, seq_lens, nq, rows, max_row_len, k, out, status, st);
+      case 6: return launch_resident<6>(scores, ld, row_lens, seq_lens, nq, rows, max_row_len, k, out, status, st);
+      case 7: return launch_resident<7>(scores, ld, row_lens, seq_lens, nq, rows, max_row_len, k, out, status, st);
+      default: return launch_resident<8>(scores, ld, row_lens, seq_lens, nq, rows, max_row_len, k, out, status, st);
+    }
+  }
   auto al = [](size_t x) { return (x + 255) & ~size_t(255); };
   uint8_t* w = static_cast<uint8_t*>(workspace);
   TopkWs ws;

@@ -140,6 +140,24 @@ def test_topk_long_rows():
     np.testing.assert_array_equal(got, oracle.topk(m.astype(np.float64), lens, 2048))
 
 
+@pytest.mark.parametrize("n,ties", [(40_960, False), (40_961, True), (120_000, True), (327_680, True),
+                                     (327_681, False), (1_000_000, True)])
+def test_topk_row_lengths_across_paths(n, ties):
+    """Rows held in one CTA, in clusters of 2..8 CTAs (ties on the k-th key
+    spread over every CTA of the cluster), and past 8 x 40,960 tokens (the
+    multi-kernel path)."""
+    rng = np.random.default_rng(n)
+    ld = (n + 3) // 4 * 4
+    m = np.zeros((3, ld), dtype=np.float32)
+    m[0, :n] = rng.integers(0, 50, n) if ties else rng.standard_normal(n)
+    m[1, :n] = 7.0                                  # all equal: the lowest k indices
+    m[2, :n] = rng.standard_normal(n)
+    m[2, n // 3] = np.inf
+    lens = np.array([n, n, n - 5], dtype=np.int32)
+    got = _gpu_topk(torch.from_numpy(m).cuda(), torch.from_numpy(lens).cuda(), 2048)
+    np.testing.assert_array_equal(got, oracle.topk(m.astype(np.float64), lens, 2048))
+
+
 def _gpu_mla(case, dc, idx_np):
     rows, k = idx_np.shape
     idx = torch.from_numpy(np.ascontiguousarray(idx_np, dtype=np.int32)).cuda()
