@@ -240,9 +240,10 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int lt = threadIdx.x - 128;                 // 0..191
       const int tok = lt / kChunksPerThread;             // token row of the tile, 0..31
       const int g = lt % kChunksPerThread;               // chunks g, g+6, ..., g+30 of the 36
-      // four tiles in flight per thread (a register ring), so the gather of
-      // tile i+3 overlaps the conversion of tile i
-      uint4 buf0[kChunksPerThread], buf1[kChunksPerThread], buf2[kChunksPerThread], buf3[kChunksPerThread];
+      // three tiles in flight per thread (a register ring), so the gather of
+      // tile i+3 overlaps the rest; each tile is widened to bf16 in registers
+      // before its buffer is free, so only the shared-memory stores wait
+      uint4 buf0[kChunksPerThread], buf1[kChunksPerThread], buf2[kChunksPerThread];
       auto load = [&](int i, uint4 (&buf)[kChunksPerThread]) {
         if (i >= ntiles) return;
         const int64_t off = tok_off[i * kTileTok + tok];
@@ -254,24 +255,27 @@ __global__ void __launch_bounds__(kThreads, 1)
       };
       auto store = [&](int i, const uint4 (&buf)[kChunksPerThread]) -> bool {
         if (i >= ntiles) return true;
+        uint4 cv[2 * kChunksPerThread];  // the widened chunks: 32 bytes of bf16 each
+#pragma unroll
+        for (int c = 0; c < kChunksPerThread; ++c) {
+          const uint32_t w[4] = {buf[c].x, buf[c].y, buf[c].z, buf[c].w};
+          uint32_t o[8];
+#pragma unroll
+          for (int q = 0; q < 4; ++q) e4m3x4_to_bf16x4(w[q], o[2 * q], o[2 * q + 1]);
+          cv[2 * c] = make_uint4(o[0], o[1], o[2], o[3]);
+          cv[2 * c + 1] = make_uint4(o[4], o[5], o[6], o[7]);
+        }
         const int b = i & 1;
         const bool ok = mbar_wait(tile_empty(b), ((i >> 1) & 1) ^ 1, abort_flag, p.status);
         if (!__all_sync(0xffffffffu, ok)) return false;
         uint8_t* tile = smem + kOffTile + b * kTileBytes;
 #pragma unroll
         for (int c = 0; c < kChunksPerThread; ++c) {
-          {
-            const int ch = g + kChunksPerThread * c;  // 16-byte chunk of the 576-byte row: dims [16 ch, +16)
-            const int dblk = ch >> 2;
-            const uint32_t inner = (uint32_t)((ch & 3) * 32);
-            const uint32_t w[4] = {buf[c].x, buf[c].y, buf[c].z, buf[c].w};
-            uint32_t o[8];
-#pragma unroll
-            for (int q = 0; q < 4; ++q) e4m3x4_to_bf16x4(w[q], o[2 * q], o[2 * q + 1]);
-            uint8_t* blk = tile + dblk * kTileDBlockBytes;
-            *reinterpret_cast<uint4*>(blk + swz128(tok * 128 + inner)) = make_uint4(o[0], o[1], o[2], o[3]);
-            *reinterpret_cast<uint4*>(blk + swz128(tok * 128 + inner + 16)) = make_uint4(o[4], o[5], o[6], o[7]);
-          }
+          const int ch = g + kChunksPerThread * c;  // 16-byte chunk of the 576-byte row: dims [16 ch, +16)
+          uint8_t* blk = tile + (ch >> 2) * kTileDBlockBytes;
+          const uint32_t inner = (uint32_t)((ch & 3) * 32);
+          *reinterpret_cast<uint4*>(blk + swz128(tok * 128 + inner)) = cv[2 * c];
+          *reinterpret_cast<uint4*>(blk + swz128(tok * 128 + inner + 16)) = cv[2 * c + 1];
         }
         fence_proxy_async_smem();
         __syncwarp();
@@ -281,15 +285,13 @@ __global__ void __launch_bounds__(kThreads, 1)
       load(0, buf0);
       load(1, buf1);
       load(2, buf2);
-      for (int i = 0; i < ntiles; i += 4) {
-        load(i + 3, buf3);
+      for (int i = 0; i < ntiles; i += 3) {
         if (!store(i, buf0)) break;
-        load(i + 4, buf0);
+        load(i + 3, buf0);
         if (!store(i + 1, buf1)) break;
-        load(i + 5, buf1);
+        load(i + 4, buf1);
         if (!store(i + 2, buf2)) break;
-        load(i + 6, buf2);
-        if (!store(i + 3, buf3)) break;
+        load(i + 5, buf2);
       }
     } else {
       // ------------------------------------------------ softmax (thread = head)
