@@ -173,8 +173,8 @@ dsa_status_t dsa_topk(const float* scores, int64_t ld_scores, const int32_t* row
   if (rows == 0) return DSA_OK;
   if (!scores || !row_lens || !idx_out || !aligned(scores, 16) || ld_scores < max_row_len || (ld_scores % 4))
     return DSA_ERR_INVALID_ARG;
-  if (!workspace || !aligned(workspace, 256) || workspace_bytes < topk_workspace_bytes(rows, max_row_len, k))
-    return DSA_ERR_WORKSPACE;
+  const size_t need = topk_workspace_bytes(rows, max_row_len, k);
+  if (need && (!workspace || !aligned(workspace, 256) || workspace_bytes < need)) return DSA_ERR_WORKSPACE;
   return launch_topk(scores, ld_scores, row_lens, nullptr, 1, rows, max_row_len, k, idx_out, workspace, dev_status,
                      static_cast<cudaStream_t>(stream));
 }

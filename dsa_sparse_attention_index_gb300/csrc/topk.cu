@@ -760,7 +760,8 @@ size_t ws_bytes(int rows, int k) {
 }  // namespace
 
 size_t topk_workspace_bytes(int rows, int max_row_len, int k) {
-  (void)max_row_len;
+  // rows that fit a cluster's shared memory (or need no selection) use none
+  if (max_row_len <= k || (max_row_len + kResKeys - 1) / kResKeys <= kResMaxCluster) return 0;
   return ws_bytes(rows, k);
 }
 

@@ -148,7 +148,9 @@ dsa_status_t dsa_index_scores(const dsa_paged_cache_t* cache, const dsa_batch_t*
  *   scores    device fp32 [rows][ld_scores]
  *   row_lens  device int32 [rows], each <= max_row_len <= ld_scores
  *   k         1 .. DSA_MAX_TOPK
- *   workspace device, >= dsa_topk_workspace_size(rows, max_row_len, k) bytes, 256-B aligned
+ *   workspace device, >= dsa_topk_workspace_size(rows, max_row_len, k) bytes, 256-B aligned;
+ *             that size is 0 (and NULL is accepted) when max_row_len <= k or the rows fit
+ *             the on-chip path (max_row_len <= 327,680)
  */
 size_t dsa_topk_workspace_size(int32_t rows, int32_t max_row_len, int32_t k);
 dsa_status_t dsa_topk(const float* scores, int64_t ld_scores, const int32_t* row_lens,

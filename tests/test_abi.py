@@ -75,4 +75,5 @@ def test_workspace_sizes(lib):
     assert ws >= 32 * 163840 * 4  # holds the scores
     assert lib.dsa_topk_workspace_size(4, 1 << 20, 2048) > 0
     assert lib.sparse_mla_workspace_size(32, 2048) >= 32 * 96 * 512 * 4
+    assert lib.dsa_topk_workspace_size(32, 163840, 2048) == 0  # rows held in shared memory
     assert lib.dsa_topk_workspace_size(4, 100, 0) == 0
