@@ -181,6 +181,16 @@ __device__ __forceinline__ void mma_bf16(uint32_t d, uint64_t a, uint64_t b, uin
       ::"r"(d), "l"(a), "l"(b), "r"(idesc), "r"(accumulate)
       : "memory");
 }
+// D[tmem] (+)= A[tmem] * B[smem]; 16-bit operands.  A (K-major) sits in TMEM:
+// lane = row, each 32-bit column two consecutive K elements (low half first).
+__device__ __forceinline__ void mma_bf16_tmem_a(uint32_t d, uint32_t a_tmem, uint64_t b, uint32_t idesc,
+                                                uint32_t accumulate) {
+  asm volatile(
+      "{\n .reg .pred p;\n setp.ne.b32 p, %4, 0;\n"
+      " tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n}\n"
+      ::"r"(d), "r"(a_tmem), "l"(b), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
 // D[tmem] (+)= (A * B) with MX block scaling: per 32-element K block, A row m
 // is scaled by 2^(E - 127) with E the byte `sf_id` (instruction descriptor
 // bits [29,31)) of the TMEM word at lane m % 32, column sfa + m / 32; B

@@ -9,9 +9,13 @@
 // from the packed paged cache through the block table.
 //
 // GB300 design (one CTA per (query row, token chunk), 11 warps):
-//   * Q [96 x 576] bf16 is loaded once by TMA into shared memory (108 KB,
-//     128-byte swizzle, K-major) and is the A operand of S = Q K^T with the
-//     heads on the MMA's M = 128 rows (rows 96..127 are ignored).
+//   * Q [96 x 576] bf16 is the A operand of S = Q K^T with the heads on the
+//     MMA's M = 128 rows (rows 96..127 are ignored): dims 0..447 loaded once
+//     by TMA into shared memory (84 KB, 128-byte swizzle, K-major), dims
+//     448..575 written by the softmax warps into TMEM (A from TMEM).  That
+//     leaves room for three latent tile buffers and spares the tensor core
+//     the shared-memory reads of those Q blocks, the limit of these
+//     small-N MMAs.
 //   * warps 4..9 gather 32 latent rows per tile (16-byte loads, four tiles in
 //     flight), widen E4M3 -> bf16 exactly in registers and store the tile
 //     once, 128-byte swizzled.  That single tile is the B operand of QK^T
@@ -42,12 +46,15 @@ namespace {
 
 constexpr int kTileTok = 32;
 constexpr int kDBlocks = kLatent / 64;                 // 9 blocks of 64 dims (128 B of bf16)
+constexpr int kQTmemBlocks = 2;                        // Q dims 448..575 in TMEM
+constexpr int kQSmemBlocks = kDBlocks - kQTmemBlocks;  // Q dims 0..447 in shared memory
 constexpr int kQBlockBytes = kHeads * 128;             // 12,288
-constexpr int kQBytes = kDBlocks * kQBlockBytes;       // 110,592
+constexpr int kQBytes = kQSmemBlocks * kQBlockBytes;   // 86,016
+constexpr int kTileBufs = 3;
 constexpr int kTileDBlockBytes = kTileTok * 128;       // 4,096
 constexpr int kTileBytes = kDBlocks * kTileDBlockBytes;  // 36,864
 constexpr int kPBytes = kHeads * kTileTok * 2;         // 6,144
-constexpr int kMaxChunk = 2048;
+constexpr int kMaxChunk = 1024;                        // tokens per CTA
 // 11 warps: softmax 0-3, loaders 4-9, MMA issuer 10.  At most 3 warps share a
 // sub-partition's register file, which leaves room for 168 registers a thread.
 constexpr int kThreads = 11 * 32;
@@ -56,19 +63,22 @@ constexpr int kMmaWarp = 10;
 constexpr int kChunksPerThread = kTileTok * (kLatent / 16) / kLoaderThreads;  // 6 of the 1,152 16-B chunks
 constexpr int kOCols = 4 * kHeads;                     // 384 TMEM columns of O^T
 constexpr int kSCol = kOCols;                          // S buffers at 384 and 416
+constexpr int kQ8Col = kSCol + 2 * kTileTok;           // Q dims 448..575: 64 columns at 448
 constexpr int kTmemCols = 512;
+static_assert(kQ8Col + 32 * kQTmemBlocks <= kTmemCols, "TMEM columns");
 constexpr float kRescaleThreshold = 8.0f;              // log2 units
 
 constexpr int kOffQ = 0;
-constexpr int kOffTile = kOffQ + kQBytes;                   // 110,592
-constexpr int kOffP = kOffTile + 2 * kTileBytes;             // 184,320
-constexpr int kOffAlpha = kOffP + 2 * kPBytes;               // 196,608
-constexpr int kOffBars = kOffAlpha + 128 * 4;                // 197,120
-constexpr int kNumBars = 10;
+constexpr int kOffTile = kOffQ + kQBytes;                    // 86,016
+constexpr int kOffP = kOffTile + kTileBufs * kTileBytes;     // 196,608
+constexpr int kOffAlpha = kOffP + 2 * kPBytes;               // 208,896
+constexpr int kOffBars = kOffAlpha + 128 * 4;                // 209,408
+constexpr int kNumBars = 2 + 2 * kTileBufs + 4 + 1;          // q, q8, tiles full/empty, s, p, pv_done
 constexpr int kOffMisc = kOffBars + kNumBars * 8;
-constexpr int kOffTokOff = kOffMisc + 16;                    // int64 per token of the chunk
-constexpr int kOffMask = kOffTokOff + 8 * kMaxChunk;         // one validity bit per token
+constexpr int kOffTok = kOffMisc + 16;                       // int32 per token: block row * 64 + slot, or -1
+constexpr int kOffMask = kOffTok + 4 * kMaxChunk;            // one validity bit per token
 constexpr size_t kSmemBytes = 1024 + kOffMask + (size_t)kMaxChunk / 8;
+static_assert(kSmemBytes <= 232448, "shared memory");
 
 struct MlaParams {
   const uint8_t* latent_base;  // cache base + latent_off
@@ -84,6 +94,7 @@ struct MlaParams {
   int32_t chunk;    // tokens per CTA (multiple of 32)
   int32_t nsplit;
   float logit_scale_log2;  // sm_scale * latent_scale * log2(e)
+  const uint16_t* q_mla;   // bf16 [rows][96][576]
   float* opart;     // [rows][nsplit][96][512]
   float* ml;        // [rows][nsplit][96][4]: max (log2), sum of bf16(p), sum of p
   int32_t* status;
@@ -117,15 +128,16 @@ __global__ void __launch_bounds__(kThreads, 1)
   const uint32_t sbase = smem_u32(smem);
   const uint32_t bars = sbase + kOffBars;
   const uint32_t q_full = bars;
-  auto tile_full = [&](int b) { return bars + 8u * (1 + b); };
-  auto tile_empty = [&](int b) { return bars + 8u * (3 + b); };
-  auto s_full = [&](int b) { return bars + 8u * (5 + b); };
-  auto p_full = [&](int b) { return bars + 8u * (7 + b); };
-  const uint32_t pv_done = bars + 8u * 9;
+  const uint32_t q8_full = bars + 8u;  // Q dims 448..575 written to TMEM by the softmax warps
+  auto tile_full = [&](int b) { return bars + 8u * (2 + b); };
+  auto tile_empty = [&](int b) { return bars + 8u * (2 + kTileBufs + b); };
+  auto s_full = [&](int b) { return bars + 8u * (2 + 2 * kTileBufs + b); };
+  auto p_full = [&](int b) { return bars + 8u * (4 + 2 * kTileBufs + b); };
+  const uint32_t pv_done = bars + 8u * (6 + 2 * kTileBufs);
   // the MMA issuer's teardown barrier reuses q_full's slot after Q has landed
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + kOffMisc);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + kOffMisc + 4);
-  int64_t* tok_off = reinterpret_cast<int64_t*>(smem + kOffTokOff);
+  int32_t* tok_phys = reinterpret_cast<int32_t*>(smem + kOffTok);
   uint32_t* tile_mask = reinterpret_cast<uint32_t*>(smem + kOffMask);
   float* alpha_s = reinterpret_cast<float*>(smem + kOffAlpha);
 
@@ -143,9 +155,12 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   if (threadIdx.x == 0) {
     mbar_init(q_full, 1);
-    for (int b = 0; b < 2; ++b) {
+    mbar_init(q8_full, 4);
+    for (int b = 0; b < kTileBufs; ++b) {
       mbar_init(tile_full(b), kLoaderThreads / 32);
       mbar_init(tile_empty(b), 1);
+    }
+    for (int b = 0; b < 2; ++b) {
       mbar_init(s_full(b), 1);
       mbar_init(p_full(b), 4);
     }
@@ -158,21 +173,22 @@ __global__ void __launch_bounds__(kThreads, 1)
     tmem_alloc(smem_u32(tmem_slot), kTmemCols);
     tmem_relinquish();
   }
-  // byte offsets of the chunk's latent rows (-1: masked: -1 index or padding)
+  // physical slots of the chunk's latent rows, block row * 64 + slot (-1: a -1
+  // index or padding)
   for (int i = threadIdx.x; i < ntiles * kTileTok; i += kThreads) {
-    int64_t off = -1;
+    int32_t phys = -1;
     if (i < count) {
       const int t = p.idx[(int64_t)row * p.k + c0 + i];
       if (t >= 0) {
         const int r = (t < vis) ? p.block_table[(int64_t)b_seq * p.max_blocks + t / kBlock] : -1;
         if (r >= 0 && r < p.num_blocks)
-          off = (int64_t)r * p.row_stride + (int64_t)(t % kBlock) * kLatent;
+          phys = r * kBlock + t % kBlock;
         else
           report(p.status, DSA_ERR_BOUNDS);
       }
     }
-    tok_off[i] = off;
-    const uint32_t bits = __ballot_sync(0xffffffffu, off >= 0);  // a warp pass covers 32 consecutive tokens
+    tok_phys[i] = phys;
+    const uint32_t bits = __ballot_sync(0xffffffffu, phys >= 0);  // a warp pass covers 32 consecutive tokens
     if ((threadIdx.x & 31) == 0) tile_mask[i >> 5] = bits;
   }
   tc_fence_before();
@@ -185,19 +201,26 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (lane == 0) {
         // ------------------------------------------------ Q load + MMA issuer
         mbar_arrive_expect_tx(q_full, kQBytes);
-        for (int kb = 0; kb < kDBlocks; ++kb)
+        for (int kb = 0; kb < kQSmemBlocks; ++kb)
           tma_load_2d(sbase + kOffQ + kb * kQBlockBytes, &tmap_q, kb * 64, row * kHeads, q_full);
         bool ok = mbar_wait(q_full, 0, abort_flag, p.status);
+        ok = ok && mbar_wait(q8_full, 0, abort_flag, p.status);
         auto issue_qk = [&](int i) {
           const int b = i & 1;
-          const uint32_t tile = sbase + kOffTile + b * kTileBytes;
-          for (int kb = 0; kb < kDBlocks; ++kb) {
+          const uint32_t tile = sbase + kOffTile + (i % kTileBufs) * kTileBytes;
+          for (int kb = 0; kb < kQSmemBlocks; ++kb) {
 #pragma unroll
             for (int kk = 0; kk < 4; ++kk) {
               const uint64_t ad = smem_desc(sbase + kOffQ + kb * kQBlockBytes + 32 * kk, 16, 1024, kLayoutSw128);
               const uint64_t bd = smem_desc(tile + kb * kTileDBlockBytes + 32 * kk, 16, 1024, kLayoutSw128);
               mma_bf16(tmem + kSCol + kTileTok * b, ad, bd, kIdescQK, (kb | kk) ? 1u : 0u);
             }
+          }
+#pragma unroll
+          for (int kk = 0; kk < 4 * kQTmemBlocks; ++kk) {  // dims 448..575: A from TMEM, 8 columns per K = 16 step
+            const uint64_t bd = smem_desc(tile + (kQSmemBlocks + kk / 4) * kTileDBlockBytes + 32 * (kk % 4), 16,
+                                          1024, kLayoutSw128);
+            mma_bf16_tmem_a(tmem + kSCol + kTileTok * b, tmem + kQ8Col + 8 * kk, bd, kIdescQK, 1u);
           }
           mma_commit(s_full(b));
         };
@@ -208,14 +231,14 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         for (int i = 0; ok && i < ntiles; ++i) {
           if (i + 1 < ntiles) {
-            if (!mbar_wait(tile_full((i + 1) & 1), ((i + 1) >> 1) & 1, abort_flag, p.status)) break;
+            if (!mbar_wait(tile_full((i + 1) % kTileBufs), ((i + 1) / kTileBufs) & 1, abort_flag, p.status)) break;
             tc_fence_after();
             issue_qk(i + 1);
           }
           const int b = i & 1;
           if (!mbar_wait(p_full(b), (i >> 1) & 1, abort_flag, p.status)) break;
           tc_fence_after();
-          const uint32_t tile = sbase + kOffTile + b * kTileBytes;
+          const uint32_t tile = sbase + kOffTile + (i % kTileBufs) * kTileBytes;
           const uint32_t pt = sbase + kOffP + b * kPBytes;
 #pragma unroll
           for (int mb = 0; mb < 4; ++mb) {
@@ -228,7 +251,7 @@ __global__ void __launch_bounds__(kThreads, 1)
               mma_bf16(tmem + mb * kHeads, ad, bd, kIdescPV, (i > 0 || ks > 0) ? 1u : 0u);
             }
           }
-          mma_commit(tile_empty(b));
+          mma_commit(tile_empty(i % kTileBufs));
           mma_commit(pv_done);
         }
         // wait for every issued MMA before TMEM is released (q_full is free by now)
@@ -246,11 +269,12 @@ __global__ void __launch_bounds__(kThreads, 1)
       uint4 buf0[kChunksPerThread], buf1[kChunksPerThread], buf2[kChunksPerThread];
       auto load = [&](int i, uint4 (&buf)[kChunksPerThread]) {
         if (i >= ntiles) return;
-        const int64_t off = tok_off[i * kTileTok + tok];
+        const int32_t phys = tok_phys[i * kTileTok + tok];
+        const int64_t off = (int64_t)(phys >> 6) * p.row_stride + (phys & (kBlock - 1)) * kLatent;
 #pragma unroll
         for (int c = 0; c < kChunksPerThread; ++c) {
           buf[c] = make_uint4(0, 0, 0, 0);
-          if (off >= 0) buf[c] = __ldg(reinterpret_cast<const uint4*>(p.latent_base + off) + (g + kChunksPerThread * c));
+          if (phys >= 0) buf[c] = __ldg(reinterpret_cast<const uint4*>(p.latent_base + off) + (g + kChunksPerThread * c));
         }
       };
       auto store = [&](int i, const uint4 (&buf)[kChunksPerThread]) -> bool {
@@ -265,8 +289,8 @@ __global__ void __launch_bounds__(kThreads, 1)
           cv[2 * c] = make_uint4(o[0], o[1], o[2], o[3]);
           cv[2 * c + 1] = make_uint4(o[4], o[5], o[6], o[7]);
         }
-        const int b = i & 1;
-        const bool ok = mbar_wait(tile_empty(b), ((i >> 1) & 1) ^ 1, abort_flag, p.status);
+        const int b = i % kTileBufs;
+        const bool ok = mbar_wait(tile_empty(b), ((i / kTileBufs) & 1) ^ 1, abort_flag, p.status);
         if (!__all_sync(0xffffffffu, ok)) return false;
         uint8_t* tile = smem + kOffTile + b * kTileBytes;
 #pragma unroll
@@ -297,6 +321,25 @@ __global__ void __launch_bounds__(kThreads, 1)
       // ------------------------------------------------ softmax (thread = head)
       const int h = threadIdx.x;  // TMEM lane
       const bool live = h < kHeads;
+      {
+        // Q dims 448..575 of head h into TMEM (the A operand of the last eight
+        // QK steps), 8 columns (16 dims) at a time
+        const uint4* src = reinterpret_cast<const uint4*>(p.q_mla + ((int64_t)row * kHeads + h) * kLatent +
+                                                          64 * kQSmemBlocks);
+#pragma unroll 1
+        for (int c = 0; c < 4 * kQTmemBlocks; ++c) {
+          const uint4 v0 = live ? __ldg(src + 2 * c) : make_uint4(0, 0, 0, 0);
+          const uint4 v1 = live ? __ldg(src + 2 * c + 1) : make_uint4(0, 0, 0, 0);
+          asm volatile("tcgen05.st.sync.aligned.32x32b.x8.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8};"
+                       ::"r"(tmem + ((uint32_t)(warp * 32) << 16) + kQ8Col + 8 * c), "r"(v0.x), "r"(v0.y),
+                       "r"(v0.z), "r"(v0.w), "r"(v1.x), "r"(v1.y), "r"(v1.z), "r"(v1.w)
+                       : "memory");
+        }
+        tmem_st_wait();
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(q8_full);
+      }
       float m_used = -INFINITY, l_round = 0.f, l_exact = 0.f;
       bool ok = true;
       for (int i = 0; i < ntiles; ++i) {
@@ -466,13 +509,17 @@ __global__ void __launch_bounds__(256) mla_combine_kernel(const float* __restric
 
 // Token chunks per row: enough CTAs for one wave over the SMs (one CTA per SM
 // fits), at most 16; the workspace is sized for up to 256 SMs.
-int mla_nsplit_max(int rows) { return std::max(1, std::min(16, 256 / std::max(1, rows))); }
-int mla_nsplit(int rows) { return std::max(1, std::min(mla_nsplit_max(rows), num_sms() / std::max(1, rows))); }
+int mla_nsplit_max(int rows, int k) {
+  return std::max((k + kMaxChunk - 1) / kMaxChunk, std::min(16, 256 / std::max(1, rows)));
+}
+int mla_nsplit(int rows, int k) {
+  return std::max((k + kMaxChunk - 1) / kMaxChunk,
+                  std::min(mla_nsplit_max(rows, k), num_sms() / std::max(1, rows)));
+}
 
 size_t mla_workspace_bytes(int rows, int k) {
-  (void)k;
   auto al = [](size_t x) { return (x + 255) & ~size_t(255); };
-  const size_t parts = (size_t)rows * mla_nsplit_max(rows);
+  const size_t parts = (size_t)rows * mla_nsplit_max(rows, k);
   return al(parts * kHeads * kValue * 4) + al(parts * kHeads * 16);
 }
 
@@ -490,14 +537,14 @@ dsa_status_t launch_sparse_mla(const dsa_paged_cache_t& c, const dsa_batch_t& bt
                      CU_TENSOR_MAP_SWIZZLE_128B))
       return DSA_ERR_CUDA;
   }
-  const int nsplit0 = mla_nsplit(rows);
+  const int nsplit0 = mla_nsplit(rows, k);
   const int tiles = (k + kTileTok - 1) / kTileTok;
   const int chunk = ((tiles + nsplit0 - 1) / nsplit0) * kTileTok;
   const int nsplit = (k + chunk - 1) / chunk;
   auto al = [](size_t x) { return (x + 255) & ~size_t(255); };
   float* opart = static_cast<float*>(workspace);
   float* ml = reinterpret_cast<float*>(static_cast<uint8_t*>(workspace) +
-                                       al((size_t)rows * mla_nsplit_max(rows) * kHeads * kValue * 4));
+                                       al((size_t)rows * mla_nsplit_max(rows, k) * kHeads * kValue * 4));
   MlaParams p{static_cast<const uint8_t*>(c.base) + c.latent_off,
               c.row_stride,
               c.num_blocks,
@@ -511,6 +558,7 @@ dsa_status_t launch_sparse_mla(const dsa_paged_cache_t& c, const dsa_batch_t& bt
               chunk,
               nsplit,
               sm_scale * c.latent_scale * 1.4426950408889634f,
+              q_mla,
               opart,
               ml,
               status};
