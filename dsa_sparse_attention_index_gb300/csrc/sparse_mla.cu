@@ -21,11 +21,11 @@
 //     once, 128-byte swizzled.  That single tile is the B operand of QK^T
 //     (K-major, N = 32 tokens) and the A operand of P V (MN-major, M = 128
 //     value dims), so V needs no second copy.
-//   * warp 10 issues tcgen05.mma (kind::f16, fp32 accumulation): S into a
-//     double-buffered 32-column TMEM tile, O^T = V^T P^T into 4 x 96 TMEM
-//     columns (dims on lanes, heads on columns: 384 + 2*32 <= 512 columns).
-//     QK of tile i+1 is issued before PV of tile i so the softmax overlaps
-//     the tensor core.
+//   * two warps issue tcgen05.mma (kind::f16, fp32 accumulation): warp 10
+//     S = Q K^T into a double-buffered 32-column TMEM tile, warp 11
+//     O^T = V^T P^T into 4 x 96 TMEM columns (dims on lanes, heads on
+//     columns).  The two products of neighbouring tiles are issued at the
+//     same time, and the softmax of tile i overlaps both.
 //   * warps 0..3 (one thread per head) run the online softmax on the S row
 //     in registers (exp2 with the scale folded in), write P as bf16 (64-byte
 //     swizzled rows, the K-major B operand of PV), and rescale O^T only when
@@ -55,11 +55,12 @@ constexpr int kTileDBlockBytes = kTileTok * 128;       // 4,096
 constexpr int kTileBytes = kDBlocks * kTileDBlockBytes;  // 36,864
 constexpr int kPBytes = kHeads * kTileTok * 2;         // 6,144
 constexpr int kMaxChunk = 1024;                        // tokens per CTA
-// 11 warps: softmax 0-3, loaders 4-9, MMA issuer 10.  At most 3 warps share a
-// sub-partition's register file, which leaves room for 168 registers a thread.
-constexpr int kThreads = 11 * 32;
+// 12 warps: softmax 0-3, loaders 4-9, QK issuer 10, PV issuer 11.  Three warps
+// share a sub-partition's register file: room for 168 registers a thread.
+constexpr int kThreads = 12 * 32;
 constexpr int kLoaderThreads = 192;
 constexpr int kMmaWarp = 10;
+constexpr int kPvWarp = 11;
 constexpr int kChunksPerThread = kTileTok * (kLatent / 16) / kLoaderThreads;  // 6 of the 1,152 16-B chunks
 constexpr int kOCols = 4 * kHeads;                     // 384 TMEM columns of O^T
 constexpr int kSCol = kOCols;                          // S buffers at 384 and 416
@@ -73,7 +74,8 @@ constexpr int kOffTile = kOffQ + kQBytes;                    // 86,016
 constexpr int kOffP = kOffTile + kTileBufs * kTileBytes;     // 196,608
 constexpr int kOffAlpha = kOffP + 2 * kPBytes;               // 208,896
 constexpr int kOffBars = kOffAlpha + 128 * 4;                // 209,408
-constexpr int kNumBars = 2 + 2 * kTileBufs + 4 + 1;          // q, q8, tiles full/empty, s, p, pv_done
+// q, q8, tiles full/empty, s full/empty, p full, PV done per P buffer, PV drain
+constexpr int kNumBars = 2 + 2 * kTileBufs + 2 + 2 + 2 + 2 + 1;
 constexpr int kOffMisc = kOffBars + kNumBars * 8;
 constexpr int kOffTok = kOffMisc + 16;                       // int32 per token: block row * 64 + slot, or -1
 constexpr int kOffMask = kOffTok + 4 * kMaxChunk;            // one validity bit per token
@@ -132,8 +134,10 @@ __global__ void __launch_bounds__(kThreads, 1)
   auto tile_full = [&](int b) { return bars + 8u * (2 + b); };
   auto tile_empty = [&](int b) { return bars + 8u * (2 + kTileBufs + b); };
   auto s_full = [&](int b) { return bars + 8u * (2 + 2 * kTileBufs + b); };
-  auto p_full = [&](int b) { return bars + 8u * (4 + 2 * kTileBufs + b); };
-  const uint32_t pv_done = bars + 8u * (6 + 2 * kTileBufs);
+  auto s_empty = [&](int b) { return bars + 8u * (4 + 2 * kTileBufs + b); };
+  auto p_full = [&](int b) { return bars + 8u * (6 + 2 * kTileBufs + b); };
+  auto pv_done = [&](int b) { return bars + 8u * (8 + 2 * kTileBufs + b); };  // PV of the tiles using P buffer b
+  const uint32_t pv_drain = bars + 8u * (10 + 2 * kTileBufs);
   // the MMA issuer's teardown barrier reuses q_full's slot after Q has landed
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + kOffMisc);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + kOffMisc + 4);
@@ -162,9 +166,11 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     for (int b = 0; b < 2; ++b) {
       mbar_init(s_full(b), 1);
+      mbar_init(s_empty(b), 4);
       mbar_init(p_full(b), 4);
+      mbar_init(pv_done(b), 1);
     }
-    mbar_init(pv_done, 1);
+    mbar_init(pv_drain, 1);
     *abort_flag = 0;
     fence_mbar_init();
     prefetch_tmap(&tmap_q);
@@ -224,17 +230,22 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
           mma_commit(s_full(b));
         };
-        if (ok) ok = mbar_wait(tile_full(0), 0, abort_flag, p.status);
-        if (ok) {
-          tc_fence_after();
-          issue_qk(0);
-        }
         for (int i = 0; ok && i < ntiles; ++i) {
-          if (i + 1 < ntiles) {
-            if (!mbar_wait(tile_full((i + 1) % kTileBufs), ((i + 1) / kTileBufs) & 1, abort_flag, p.status)) break;
-            tc_fence_after();
-            issue_qk(i + 1);
-          }
+          // tile i landed; S buffer i & 1 read out by the softmax of tile i - 2
+          ok = mbar_wait(tile_full(i % kTileBufs), (i / kTileBufs) & 1, abort_flag, p.status) &&
+               mbar_wait(s_empty(i & 1), ((i >> 1) & 1) ^ 1, abort_flag, p.status);
+          if (!ok) break;
+          tc_fence_after();
+          issue_qk(i);
+        }
+        // wait for every issued MMA before TMEM is released (q_full is free by now)
+        mma_commit(q_full);
+        mbar_wait_drain(q_full, 1, 10000000ull);
+      }
+    } else if (warp == kPvWarp) {
+      if (lane == 0) {
+        // ------------------------------------------------ PV issuer
+        for (int i = 0; i < ntiles; ++i) {
           const int b = i & 1;
           if (!mbar_wait(p_full(b), (i >> 1) & 1, abort_flag, p.status)) break;
           tc_fence_after();
@@ -251,12 +262,12 @@ __global__ void __launch_bounds__(kThreads, 1)
               mma_bf16(tmem + mb * kHeads, ad, bd, kIdescPV, (i > 0 || ks > 0) ? 1u : 0u);
             }
           }
+          // QK of tile i completed before its P existed, so the tile is free after these
           mma_commit(tile_empty(i % kTileBufs));
-          mma_commit(pv_done);
+          mma_commit(pv_done(b));
         }
-        // wait for every issued MMA before TMEM is released (q_full is free by now)
-        mma_commit(q_full);
-        mbar_wait(q_full, 1, abort_flag, nullptr, 10000000ull);
+        mma_commit(pv_drain);
+        mbar_wait_drain(pv_drain, 0, 10000000ull);
       }
     } else if (warp >= 4) {
       // ------------------------------------------------ gather + E4M3 -> bf16
@@ -350,6 +361,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         uint32_t r[32];
         tmem_ld32(tmem + ((uint32_t)(warp * 32) << 16) + kSCol + kTileTok * b, r);
         tmem_ld_wait();
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(s_empty(b));  // the QK issuer may overwrite this S buffer
         float x[32];
         const uint32_t vmask = tile_mask[i];
         float m0 = -INFINITY, m1 = -INFINITY;
@@ -369,7 +383,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           m_used = m_new;
           if (i > 0) {
             // O^T holds tiles 0..i-1: wait for the last PV, then scale column h by alpha[h]
-            ok = mbar_wait(pv_done, (i - 1) & 1, abort_flag, p.status);
+            ok = mbar_wait(pv_done((i - 1) & 1), ((i - 1) >> 1) & 1, abort_flag, p.status);
             if (bar_or_softmax(!ok)) { ok = false; break; }   // also publishes alpha_s
             tc_fence_after();
 #pragma unroll 1
@@ -405,6 +419,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         l_round += srnd;
         l_exact += sex;
+        // P buffer b was last read by the PV of tile i - 2
+        ok = mbar_wait(pv_done(b), ((i >> 1) & 1) ^ 1, abort_flag, p.status);
+        if (bar_or_softmax(!ok)) { ok = false; break; }
         if (live) {
           uint8_t* prow = smem + kOffP + b * kPBytes;
 #pragma unroll
@@ -418,7 +435,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (lane == 0) mbar_arrive(p_full(b));
       }
       // ---- epilogue: partial results of this chunk
-      if (ok) ok = mbar_wait(pv_done, (ntiles - 1) & 1, abort_flag, p.status);
+      if (ok) ok = mbar_wait(pv_done((ntiles - 1) & 1), ((ntiles - 1) >> 1) & 1, abort_flag, p.status);
       ok = !bar_or_softmax(!ok);
       if (ok) {
         tc_fence_after();
