@@ -487,12 +487,17 @@ __global__ void __launch_bounds__(kFinalThreads) topk_final_kernel(const float* 
 // ---------------------------------------------------------------- row-resident path
 namespace cg = cooperative_groups;
 
-constexpr int kResKeys = 40960;     // keys per CTA in shared memory (160 KB)
+constexpr int kResKeys = 40960;     // most keys a CTA holds in shared memory (160 KB)
+constexpr int kResPairKeys = 20480; // keys per CTA that still let two CTAs share an SM
 constexpr int kResThreads = kFinalThreads;
 constexpr int kResWarps = kResThreads / 32;
 constexpr int kResMaxCluster = 8;   // portable cluster size: rows up to 327,680 tokens
-// shared memory: keys[kResKeys] | h1[4096] | h2[4096] | h3[256] | g[4096] | scan[32] | misc[32]
-constexpr size_t kResSmem = 4 * ((size_t)kResKeys + 3 * kBins + 256 + 64);
+// digits of the 32-bit key: bits 31..21, 20..10, 9..0
+constexpr int kD1 = 11, kD2 = 11, kD3 = 10;
+constexpr int kB1 = 1 << kD1, kB2 = 1 << kD2, kB3 = 1 << kD3;
+// shared memory: keys[slice] | h1[kB1] | h2[kB2] | h3[kB3] | g[kB1] | scan[32] | misc[32]
+constexpr size_t kResFixed = 4 * ((size_t)kB1 + kB2 + kB3 + kB1 + 64);
+size_t res_smem(int slice) { return 4 * (size_t)slice + kResFixed; }
 
 // Warp-wide exclusive prefix sum of one value per lane; `total` gets the sum.
 __device__ __forceinline__ uint32_t warp_excl_scan(uint32_t v, uint32_t& total) {
@@ -508,9 +513,10 @@ __device__ __forceinline__ uint32_t warp_excl_scan(uint32_t v, uint32_t& total) 
 }
 
 template <int C>
-__global__ void __launch_bounds__(kResThreads, 1)
+__global__ void __launch_bounds__(kResThreads, 2)  // two CTAs of 512 threads per SM: at most 64 registers
     topk_resident_kernel(const float* __restrict__ scores, int64_t ld, const int32_t* row_lens,
-                         const int32_t* seq_lens, int nq, int cap, int k, int32_t* out, int32_t* status) {
+                         const int32_t* seq_lens, int nq, int cap, int k, int32_t* out, int32_t* status,
+                         int slice_cap) {
   cg::cluster_group cluster = cg::this_cluster();
   const int c = (int)cluster.block_rank();
   const int r = blockIdx.x / C, tid = threadIdx.x, lane = tid & 31, wid = tid >> 5;
@@ -520,11 +526,11 @@ __global__ void __launch_bounds__(kResThreads, 1)
   };
   extern __shared__ __align__(16) uint8_t smem_raw[];
   uint32_t* keys = reinterpret_cast<uint32_t*>(smem_raw);
-  uint32_t* h1 = keys + kResKeys;
-  uint32_t* h2 = h1 + kBins;
-  uint32_t* h3 = h2 + kBins;  // 256 bins
-  uint32_t* g = h3 + 256;     // the cluster's histogram of the current digit
-  uint32_t* scan = g + kBins;
+  uint32_t* h1 = keys + slice_cap;  // slice_cap: a multiple of 4 (16-byte aligned histograms)
+  uint32_t* h2 = h1 + kB1;
+  uint32_t* h3 = h2 + kB2;
+  uint32_t* g = h3 + kB3;     // the cluster's histogram of the current digit
+  uint32_t* scan = g + kB1;
   uint32_t* misc = scan + 32;
 
   const int len = row_len(row_lens, seq_lens, nq, r, cap, c == 0 ? status : nullptr);
@@ -540,8 +546,8 @@ __global__ void __launch_bounds__(kResThreads, 1)
   const int n = max(0, min(S, len - start));
   const int n4 = (n + 3) >> 2;  // 4-key groups; the last one is padded with key 0 (below every score)
 
-  // ---- 1. keys into shared memory, histogram of the first digit (bits 31..20)
-  for (int i = tid; i < (2 * kBins + 256) / 4; i += kResThreads) reinterpret_cast<uint4*>(h1)[i] = make_uint4(0, 0, 0, 0);
+  // ---- 1. keys into shared memory, histogram of the first digit (bits 31..21)
+  for (int i = tid; i < (kB1 + kB2 + kB3) / 4; i += kResThreads) reinterpret_cast<uint4*>(h1)[i] = make_uint4(0, 0, 0, 0);
   __syncthreads();
   {
     const float* row = scores + (int64_t)r * ld + start;
@@ -569,10 +575,10 @@ __global__ void __launch_bounds__(kResThreads, 1)
           const uint4 kk = make_uint4(score_key(v[u].x), score_key(v[u].y), score_key(v[u].z), score_key(v[u].w));
           reinterpret_cast<uint4*>(keys)[i] = kk;
           const bool pad = 4 * i + 3 >= n;  // padding keys are not counted
-          atomicAdd(&h1[kk.x >> 20], 1u);
-          if (!pad || 4 * i + 1 < n) atomicAdd(&h1[kk.y >> 20], 1u);
-          if (!pad || 4 * i + 2 < n) atomicAdd(&h1[kk.z >> 20], 1u);
-          if (!pad) atomicAdd(&h1[kk.w >> 20], 1u);
+          atomicAdd(&h1[kk.x >> (32 - kD1)], 1u);
+          if (!pad || 4 * i + 1 < n) atomicAdd(&h1[kk.y >> (32 - kD1)], 1u);
+          if (!pad || 4 * i + 2 < n) atomicAdd(&h1[kk.z >> (32 - kD1)], 1u);
+          if (!pad) atomicAdd(&h1[kk.w >> (32 - kD1)], 1u);
         }
       }
     }
@@ -592,44 +598,44 @@ __global__ void __launch_bounds__(kResThreads, 1)
     }
     __syncthreads();
   };
-  merge(h1, kBins);
+  merge(h1, kB1);
   uint32_t need = (uint32_t)k, pop;
   int digit;
-  pick_digit(g, kBins, scan, need, digit, pop);
+  pick_digit(g, kB1, scan, need, digit, pop);
   // Keys whose bits above `shift` exceed `prefix` are taken; keys equal to it on
   // those bits form the threshold group, taken whole unless `tie` (only on the
   // full 32 bits), where the first `quota` of them in token order are taken.
   uint32_t prefix = (uint32_t)digit;
-  int shift = 20;
+  int shift = 32 - kD1;
   bool tie = false;
   uint32_t quota = 0;
   const uint4* keys4 = reinterpret_cast<const uint4*>(keys);
   if (need != pop) {
-    // ---- 2. second digit (bits 19..8) within the threshold group (keys past
+    // ---- 2. second digit (bits 20..10) within the threshold group (keys past
     //         the slice's end are skipped by index)
     for (int i = tid; i < n4; i += kResThreads) {
       const uint4 kk = keys4[i];
       const uint32_t a[4] = {kk.x, kk.y, kk.z, kk.w};
 #pragma unroll
       for (int j = 0; j < 4; ++j)
-        if ((a[j] >> 20) == prefix && 4 * i + j < n) atomicAdd(&h2[(a[j] >> 8) & 0xFFFu], 1u);
+        if ((a[j] >> (32 - kD1)) == prefix && 4 * i + j < n) atomicAdd(&h2[(a[j] >> kD3) & (kB2 - 1)], 1u);
     }
-    merge(h2, kBins);
-    pick_digit(g, kBins, scan, need, digit, pop);
-    prefix = (prefix << 12) | (uint32_t)digit;
-    shift = 8;
+    merge(h2, kB2);
+    pick_digit(g, kB2, scan, need, digit, pop);
+    prefix = (prefix << kD2) | (uint32_t)digit;
+    shift = kD3;
     if (need != pop) {
-      // ---- 3. last digit (bits 7..0)
+      // ---- 3. last digit (bits 9..0)
       for (int i = tid; i < n4; i += kResThreads) {
         const uint4 kk = keys4[i];
         const uint32_t a[4] = {kk.x, kk.y, kk.z, kk.w};
 #pragma unroll
         for (int j = 0; j < 4; ++j)
-          if ((a[j] >> 8) == prefix && 4 * i + j < n) atomicAdd(&h3[a[j] & 0xFFu], 1u);
+          if ((a[j] >> kD3) == prefix && 4 * i + j < n) atomicAdd(&h3[a[j] & (kB3 - 1)], 1u);
       }
-      merge(h3, 256);
-      pick_digit(g, 256, scan, need, digit, pop);
-      prefix = (prefix << 8) | (uint32_t)digit;
+      merge(h3, kB3);
+      pick_digit(g, kB3, scan, need, digit, pop);
+      prefix = (prefix << kD3) | (uint32_t)digit;
       shift = 0;
       if (need != pop) {
         // equal keys: `need` of them, lowest indices first; lower CTA ranks hold lower indices
@@ -729,14 +735,16 @@ dsa_status_t launch_resident(const float* scores, int64_t ld, const int32_t* row
   cudaGetDevice(&dev);
   if (dev < 64 && !attr_set[dev]) {
     if (cuda_status(cudaFuncSetAttribute(topk_resident_kernel<C>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         (int)kResSmem)) != DSA_OK)
+                                         (int)res_smem(kResKeys))) != DSA_OK)
       return DSA_ERR_CUDA;
     attr_set[dev] = true;
   }
+  // each CTA's slice of the longest row, rounded up to 4 keys
+  const int slice = (((cap + C - 1) / C) + 3) & ~3;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3((unsigned)(rows * C));
   cfg.blockDim = dim3(kResThreads);
-  cfg.dynamicSmemBytes = kResSmem;
+  cfg.dynamicSmemBytes = res_smem(slice);
   cfg.stream = st;
   cudaLaunchAttribute attr[1];
   attr[0].id = cudaLaunchAttributeClusterDimension;
@@ -746,7 +754,7 @@ dsa_status_t launch_resident(const float* scores, int64_t ld, const int32_t* row
   cfg.attrs = attr;
   cfg.numAttrs = 1;
   if (cuda_status(cudaLaunchKernelEx(&cfg, topk_resident_kernel<C>, scores, ld, row_lens, seq_lens, nq, cap, k,
-                                     out, status)) != DSA_OK)
+                                     out, status, slice)) != DSA_OK)
     return DSA_ERR_CUDA;
   return launch_status();
 }
@@ -771,11 +779,13 @@ dsa_status_t launch_topk(const float* scores, int64_t ld, const int32_t* row_len
                          int rows, int max_row_len, int k, int32_t* out, void* workspace, int32_t* status,
                          cudaStream_t st) {
   if (rows == 0) return DSA_OK;
-  // row-resident path: one cluster per row, enough CTAs to hold the row and,
-  // for few rows, to spread them over the SMs (at least 8,192 keys per CTA)
+  // row-resident path: one cluster per row, enough CTAs to hold the row, small
+  // enough slices for two CTAs per SM where a cluster of 8 allows it, and for
+  // few rows enough CTAs to spread them over the SMs (at least 8,192 keys per CTA)
   const int c_min = (max_row_len + kResKeys - 1) / kResKeys;
+  const int c_pair = std::min(kResMaxCluster, (max_row_len + kResPairKeys - 1) / kResPairKeys);
   const int c_fill = std::min(num_sms() / std::max(rows, 1), max_row_len / 8192);
-  const int cluster = std::min(kResMaxCluster, std::max(c_min, std::max(c_fill, 1)));
+  const int cluster = std::min(kResMaxCluster, std::max(std::max(c_min, c_pair), std::max(c_fill, 1)));
   if (max_row_len > k && c_min <= kResMaxCluster) {
     // row-resident path: one cluster of `cluster` CTAs per row, no workspace
     switch (cluster) {
