@@ -97,6 +97,15 @@ __device__ __forceinline__ bool mbar_wait_drain(uint32_t bar, uint32_t parity, u
   }
 }
 
+// ---------------------------------------------------------------- programmatic dependent launch
+// A kernel launched with programmatic stream serialization may start while the
+// previous kernel in the stream is still running; grid_dep_wait() blocks until
+// that kernel has completed and its memory is visible (it returns at once for
+// an ordinary launch).  grid_dep_launch() lets this grid's dependent launch as
+// soon as every CTA of this grid has issued it.
+__device__ __forceinline__ void grid_dep_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void grid_dep_launch() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+
 // ---------------------------------------------------------------- copies
 __device__ __forceinline__ void prefetch_tmap(const void* map) {
   asm volatile("prefetch.tensormap [%0];" ::"l"(map) : "memory");

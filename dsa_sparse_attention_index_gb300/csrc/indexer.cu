@@ -232,6 +232,7 @@ __global__ void __launch_bounds__(idx_threads<MX>(), 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
+  grid_dep_launch();  // the top-k may launch and wait for this grid on its own
 
   const int64_t total = prefix[nb];
   const int64_t u_begin = total * blockIdx.x / gridDim.x;

@@ -179,6 +179,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     tmem_alloc(smem_u32(tmem_slot), kTmemCols);
     tmem_relinquish();
   }
+  grid_dep_wait();    // the indices come from the previous kernel
+  grid_dep_launch();
   // physical slots of the chunk's latent rows, block row * 64 + slot (-1: a -1
   // index or padding)
   for (int i = threadIdx.x; i < ntiles * kTileTok; i += kThreads) {
@@ -478,6 +480,7 @@ __global__ void __launch_bounds__(256) mla_combine_kernel(const float* __restric
                                                            float latent_scale, uint16_t* out, float* lse) {
   const int row = blockIdx.y, h0 = blockIdx.x * kCombineHeads;
   __shared__ float wgt[kCombineHeads][kMaxSplit];
+  grid_dep_wait();  // the partials come from the previous kernel
   const float4* mlr = reinterpret_cast<const float4*>(ml) + (int64_t)row * nsplit * kHeads;
   if (threadIdx.x < kCombineHeads) {
     const int h = h0 + threadIdx.x;
@@ -588,9 +591,25 @@ dsa_status_t launch_sparse_mla(const dsa_paged_cache_t& c, const dsa_batch_t& bt
       return DSA_ERR_CUDA;
     attr_set[dev] = true;
   }
-  sparse_mla_kernel<<<dim3(nsplit, rows), kThreads, kSmemBytes, st>>>(qmap, p);
-  if (launch_status() != DSA_OK) return DSA_ERR_CUDA;
-  mla_combine_kernel<<<dim3(kHeads / kCombineHeads, rows), 256, 0, st>>>(opart, ml, nsplit, c.latent_scale, out, lse);
+  // both launches may overlap the previous kernel's tail; each waits for its inputs
+  cudaLaunchAttribute pdl[1];
+  pdl[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  pdl[0].val.programmaticStreamSerializationAllowed = 1;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3((unsigned)nsplit, (unsigned)rows);
+  cfg.blockDim = dim3(kThreads);
+  cfg.dynamicSmemBytes = kSmemBytes;
+  cfg.stream = st;
+  cfg.attrs = pdl;
+  cfg.numAttrs = 1;
+  if (cuda_status(cudaLaunchKernelEx(&cfg, sparse_mla_kernel, qmap, p)) != DSA_OK) return DSA_ERR_CUDA;
+  cudaLaunchConfig_t cfg2 = cfg;
+  cfg2.gridDim = dim3(kHeads / kCombineHeads, (unsigned)rows);
+  cfg2.blockDim = dim3(256);
+  cfg2.dynamicSmemBytes = 0;
+  if (cuda_status(cudaLaunchKernelEx(&cfg2, mla_combine_kernel, (const float*)opart, (const float*)ml, nsplit,
+                                     c.latent_scale, out, lse)) != DSA_OK)
+    return DSA_ERR_CUDA;
   return launch_status();
 }
 

@@ -535,6 +535,8 @@ __global__ void __launch_bounds__(kResThreads, 2)  // two CTAs of 512 threads pe
 
   const int len = row_len(row_lens, seq_lens, nq, r, cap, c == 0 ? status : nullptr);
   int32_t* o = out + (int64_t)r * k;
+  grid_dep_wait();  // the scores come from the previous kernel, which may still read `out`
+  grid_dep_launch();
   if (len <= k) {  // the same branch for every CTA of the cluster
     if (c == 0)
       for (int i = tid; i < k; i += kResThreads) o[i] = i < len ? i : -1;
@@ -746,13 +748,15 @@ dsa_status_t launch_resident(const float* scores, int64_t ld, const int32_t* row
   cfg.blockDim = dim3(kResThreads);
   cfg.dynamicSmemBytes = res_smem(slice);
   cfg.stream = st;
-  cudaLaunchAttribute attr[1];
+  cudaLaunchAttribute attr[2];
   attr[0].id = cudaLaunchAttributeClusterDimension;
   attr[0].val.clusterDim.x = C;
   attr[0].val.clusterDim.y = 1;
   attr[0].val.clusterDim.z = 1;
+  attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;  // overlaps the indexer's tail
+  attr[1].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
-  cfg.numAttrs = 1;
+  cfg.numAttrs = 2;
   if (cuda_status(cudaLaunchKernelEx(&cfg, topk_resident_kernel<C>, scores, ld, row_lens, seq_lens, nq, cap, k,
                                      out, status, slice)) != DSA_OK)
     return DSA_ERR_CUDA;
