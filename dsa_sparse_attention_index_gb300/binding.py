@@ -47,7 +47,8 @@ _lib = None
 EXPORTS = ["dsa_api_version", "dsa_status_string", "dsa_last_cuda_error", "dsa_translate_pages", "dsa_index_scores",
            "dsa_topk_workspace_size", "dsa_topk", "dsa_topk_noalloc", "sparse_mla_workspace_size",
            "sparse_mla_decode",
-           "dsa_workspace_size", "dsa_decode_step", "dsa_selftest_wait_timeout"]
+           "dsa_workspace_size", "dsa_decode_step", "dsa_cache_append", "dsa_quantize_index_query",
+           "dsa_selftest_wait_timeout"]
 
 
 def lib():
@@ -73,6 +74,8 @@ def lib():
             "sparse_mla_decode": (i32, [pc, pb, P, P, i32, f32, P, P, P, sz, P, P]),
             "dsa_workspace_size": (sz, [pb, i32]),
             "dsa_decode_step": (i32, [pc, pb, P, P, P, i32, f32, P, P, P, i64, P, P, sz, P, P]),
+            "dsa_cache_append": (i32, [pc, pb, P, P, P, P]),
+            "dsa_quantize_index_query": (i32, [P, P, i32, P, P, P]),
             "dsa_selftest_wait_timeout": (i32, [i64, P, P]),
         }
         for name, (res, args) in sig.items():
@@ -200,6 +203,21 @@ def decode_step(cache: PagedCache, batch: Batch, q_index, head_w, q_mla, k: int,
                                  int(k), float(sm_scale), _ptr(out), _ptr(lse), _ptr(scores_out), ld,
                                  _ptr(idx_out), _ptr(workspace), workspace.numel() * workspace.element_size(),
                                  _ptr(status), _stream(stream)), "dsa_decode_step")
+
+
+def cache_append(cache: PagedCache, batch: Batch, new_latent, new_index_key, status, stream=None):
+    """Write every sequence's queries_per_seq new tokens (bf16 bits, [rows, 576] and
+    [rows, 128]) into their pages."""
+    c, b = cache.struct(), batch.struct()
+    _check(lib().dsa_cache_append(ctypes.byref(c), ctypes.byref(b), _ptr(new_latent), _ptr(new_index_key),
+                                  _ptr(status), _stream(stream)), "dsa_cache_append")
+
+
+def quantize_index_query(q_bf16, head_w, q_index, head_w_out, stream=None):
+    """FP8 indexer query per (row, head), its scale folded into the head weight."""
+    rows = int(q_bf16.shape[0])
+    _check(lib().dsa_quantize_index_query(_ptr(q_bf16), _ptr(head_w), rows, _ptr(q_index), _ptr(head_w_out),
+                                          _stream(stream)), "dsa_quantize_index_query")
 
 
 def selftest_wait_timeout(limit_ns: int, status, stream=None):

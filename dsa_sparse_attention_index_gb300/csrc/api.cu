@@ -260,6 +260,28 @@ dsa_status_t dsa_decode_step(const dsa_paged_cache_t* cache, const dsa_batch_t* 
   return launch_sparse_mla(*cache, *batch, q_mla, idx, k, sm_scale, out, lse, mla_ws, dev_status, st);
 }
 
+dsa_status_t dsa_cache_append(const dsa_paged_cache_t* cache, const dsa_batch_t* batch, const uint16_t* new_latent,
+                              const uint16_t* new_index_key, int32_t* dev_status, void* stream) {
+  dsa_status_t s;
+  if ((s = check_cache(cache)) != DSA_OK) return s;
+  if ((s = check_batch(batch)) != DSA_OK) return s;
+  if (!dev_status) return DSA_ERR_INVALID_ARG;
+  if (batch->batch == 0) return DSA_OK;
+  if (!new_latent || !new_index_key || !aligned(new_latent, 2) || !aligned(new_index_key, 2))
+    return DSA_ERR_INVALID_ARG;
+  return launch_cache_append(*cache, *batch, new_latent, new_index_key, dev_status,
+                             static_cast<cudaStream_t>(stream));
+}
+
+dsa_status_t dsa_quantize_index_query(const uint16_t* q_bf16, const float* head_w, int32_t rows, uint8_t* q_index,
+                                      float* head_w_out, void* stream) {
+  if (rows < 0) return DSA_ERR_INVALID_ARG;
+  if (rows == 0) return DSA_OK;
+  if (!q_bf16 || !head_w || !q_index || !head_w_out || !aligned(q_bf16, 8) || !aligned(q_index, 4))
+    return DSA_ERR_INVALID_ARG;
+  return launch_quantize_query(q_bf16, head_w, rows, q_index, head_w_out, static_cast<cudaStream_t>(stream));
+}
+
 dsa_status_t dsa_selftest_wait_timeout(int64_t limit_ns, int32_t* dev_status, void* stream) {
   if (!dev_status) return DSA_ERR_INVALID_ARG;
   return launch_wait_selftest(limit_ns, dev_status, static_cast<cudaStream_t>(stream));

@@ -41,5 +41,9 @@ dsa_status_t launch_sparse_mla(const dsa_paged_cache_t& c, const dsa_batch_t& bt
                                const int32_t* idx, int k, float sm_scale, uint16_t* out, float* lse,
                                void* workspace, int32_t* status, cudaStream_t st);
 dsa_status_t launch_wait_selftest(int64_t limit_ns, int32_t* status, cudaStream_t st);
+dsa_status_t launch_cache_append(const dsa_paged_cache_t& c, const dsa_batch_t& bt, const uint16_t* new_latent,
+                                 const uint16_t* new_key, int32_t* status, cudaStream_t st);
+dsa_status_t launch_quantize_query(const uint16_t* q, const float* w, int rows, uint8_t* codes, float* w_out,
+                                   cudaStream_t st);
 
 }  // namespace dsa

@@ -221,6 +221,43 @@ dsa_status_t dsa_decode_step(const dsa_paged_cache_t* cache, const dsa_batch_t* 
                              int32_t* dev_status, void* stream);
 
 /*
+ * New-token cache write: the front end of the fused decode path (Day-0 post,
+ * section on the fused low-latency decode path: each step writes the new
+ * token's index key and latent into the cache; packed-cache section for the
+ * page layout).  For every sequence b and new row j < queries_per_seq, token
+ * t = seq_len_b - queries_per_seq + j (the context includes the new tokens)
+ * goes to block row block_table[b][t / 64], slot t % 64:
+ *   latent (576 values)  codes e4m3(x / latent_scale)
+ *   FP8 index key (128)  s = amax / 448 in fp32 (1 if all zero), codes e4m3(x / s),
+ *                        s stored as the token's fp32 scale
+ *   MXFP4 index key      per 32 elements E = floor(log2 amax) - 2 in [-127, 127]
+ *                        (-127 if all zero), codes e2m1(x * 2^-E) packed two per
+ *                        byte (element 2i in the low nibble), byte E + 127
+ * Rounding: nearest, ties to even; finite values past the largest code saturate.
+ *   new_latent     device bf16 bits [batch * queries_per_seq][576]
+ *   new_index_key  device bf16 bits [batch * queries_per_seq][128]
+ * A table entry outside 0..num_blocks-1 or a length outside the table raises
+ * DSA_ERR_BOUNDS in *dev_status and that row is not written.  Rows whose token
+ * would precede the sequence start are skipped.
+ */
+dsa_status_t dsa_cache_append(const dsa_paged_cache_t* cache, const dsa_batch_t* batch,
+                              const uint16_t* new_latent, const uint16_t* new_index_key,
+                              int32_t* dev_status, void* stream);
+
+/*
+ * Indexer query in FP8 (Day-0 post, fused-decode section: the indexer's query
+ * is quantised with its scale folded into the head weights).  Per row r and
+ * head h: s = amax_d |q[r][h][d]| / 448 in fp32 (1 if all zero),
+ * q_index[r][h][d] = e4m3(q / s), head_w_out[r][h] = head_w[r][h] * s.  Since
+ * max(0, s * x) = s * max(0, x) for s > 0, the scores of dsa_index_scores on
+ * (q_index, head_w_out) are those of the bf16 query up to its FP8 rounding.
+ *   q_bf16 device bf16 bits [rows][32][128], 8-byte aligned
+ *   head_w / head_w_out device fp32 [rows][32];  q_index device [rows][32][128], 4-byte aligned
+ */
+dsa_status_t dsa_quantize_index_query(const uint16_t* q_bf16, const float* head_w, int32_t rows,
+                                      uint8_t* q_index, float* head_w_out, void* stream);
+
+/*
  * Self-test of the bounded in-kernel wait used by every pipelined kernel:
  * launches one CTA that waits on a barrier nothing will ever signal, with a
  * wait limit of `limit_ns` nanoseconds (clamped to 1 ms .. 2 s).  The wait

@@ -66,6 +66,14 @@ def _load():
             lib.oracle_sparse_mla.restype = i32
             lib.oracle_num_threads.argtypes = []
             lib.oracle_num_threads.restype = i32
+            lib.oracle_e4m3_encode.argtypes = [f64]
+            lib.oracle_e4m3_encode.restype = ctypes.c_uint8
+            lib.oracle_e2m1_encode.argtypes = [f64]
+            lib.oracle_e2m1_encode.restype = ctypes.c_uint8
+            lib.oracle_cache_append.argtypes = [P, i64, i64, i64, i32, i32, ctypes.c_float, P, i32, P, i32, i32, P, P]
+            lib.oracle_cache_append.restype = i32
+            lib.oracle_quantize_query.argtypes = [P, P, i32, P, P]
+            lib.oracle_quantize_query.restype = i32
             _lib = lib
     return _lib
 
@@ -185,3 +193,42 @@ def decode_step(case):
     idx = topk(s, case.row_lens(), case.topk)
     out, lse = sparse_mla(case, idx, case.topk)
     return s, idx, out, lse
+
+
+def e4m3_encode(x: float) -> int:
+    """OCP E4M3 ('fn') encode: nearest code, ties to even, saturating at 448."""
+    return int(_load().oracle_e4m3_encode(float(x)))
+
+
+def e2m1_encode(x: float) -> int:
+    """OCP MX E2M1 encode: nearest code, ties to even, saturating at 6."""
+    return int(_load().oracle_e2m1_encode(float(x)))
+
+
+def cache_append(case, new_latent: np.ndarray, new_key: np.ndarray) -> np.ndarray:
+    """The pool after writing every sequence's nq new tokens (bf16 bits
+    new_latent [rows, 576], new_key [rows, 128]) into their pages, following
+    the Day-0 post's fused-decode section (the step writes the new token's
+    index key and latent into the packed cache).  Returns a new pool array."""
+    pool = np.array(case.pool, copy=True)
+    lat = np.ascontiguousarray(new_latent, dtype=np.uint16)
+    key = np.ascontiguousarray(new_key, dtype=np.uint16)
+    rc = _load().oracle_cache_append(
+        _ptr(pool), int(case.row_stride), int(case.latent_off), int(case.index_off), int(case.num_blocks),
+        int(case.key_format), float(case.latent_scale), _ptr(case.block_table), int(case.block_table.shape[1]),
+        _ptr(case.seq_lens), int(case.batch), int(case.nq), _ptr(lat), _ptr(key))
+    _check(rc, "cache_append")
+    return pool
+
+
+def quantize_query(q_bf16: np.ndarray, head_w: np.ndarray):
+    """FP8 indexer query per (row, head) with its scale folded into the head
+    weight (Day-0 post, fused-decode section).  Returns (codes uint8
+    [rows, 32, 128], w float32 [rows, 32])."""
+    q = np.ascontiguousarray(q_bf16, dtype=np.uint16)
+    w = np.ascontiguousarray(head_w, dtype=np.float32)
+    rows = q.shape[0]
+    codes = np.empty((rows, IDX_HEADS, IDX_DIM), dtype=np.uint8)
+    w_out = np.empty((rows, IDX_HEADS), dtype=np.float32)
+    _check(_load().oracle_quantize_query(_ptr(q), _ptr(w), rows, _ptr(codes), _ptr(w_out)), "quantize_query")
+    return codes, w_out

@@ -385,3 +385,137 @@ int oracle_num_threads(void) { return omp_get_max_threads(); }
 #else
 int oracle_num_threads(void) { return 1; }
 #endif
+
+/* ------------------------------------------------------------------ */
+/* New-token cache write and indexer-query quantisation.               */
+/* ------------------------------------------------------------------ */
+/*
+ * The fused decode path of [K31] ("低延迟解码：融合的 DSA 解码路径": the
+ * new token's index key and latent are written into the paged cache each
+ * step, and the indexer's query is FP8 with its scale folded into the head
+ * weights, "为三类状态服务的 KV 缓存" for the packed pages).  Encodings follow
+ * their definitions: round to the nearest representable value, ties to the
+ * even code, finite inputs beyond the largest magnitude saturate to it, the
+ * sign (of zero too) is kept.  Scales are computed in single precision, as
+ * the cache stores them: amax / 448 for an FP8 key or query head, and for an
+ * MXFP4 block the OCP MX shared exponent floor(log2 amax) - 2 (E8M0 byte
+ * exponent + 127; an all-zero block takes byte 0).
+ */
+
+/* nearest code by search over the non-negative codes, ties to the even code */
+static uint8_t nearest_code(double a, double (*decode)(uint8_t), int ncodes, double maxmag) {
+  if (a >= maxmag) {
+    for (int c = ncodes - 1; c >= 0; --c)
+      if (decode((uint8_t)c) == maxmag) return (uint8_t)c;
+  }
+  int best = 0;
+  double bd = fabs(a - decode(0));
+  for (int c = 1; c < ncodes; ++c) {
+    const double v = decode((uint8_t)c);
+    if (isnan(v)) continue;
+    const double d = fabs(a - v);
+    if (d < bd || (d == bd && (c & 1) == 0 && (best & 1) == 1)) {
+      best = c;
+      bd = d;
+    }
+  }
+  return (uint8_t)best;
+}
+
+/* OCP E4M3 ("fn") encode; NaN -> 0x7F. */
+uint8_t oracle_e4m3_encode(double x) {
+  if (isnan(x)) return 0x7F;
+  const uint8_t mag = nearest_code(fabs(x), oracle_e4m3_to_double, 0x7F, 448.0);
+  return (uint8_t)(mag | (signbit(x) ? 0x80 : 0));
+}
+
+/* OCP MX E2M1 encode (4 bits). */
+uint8_t oracle_e2m1_encode(double x) {
+  const uint8_t mag = nearest_code(fabs(x), oracle_e2m1_to_double, 8, 6.0);
+  return (uint8_t)(mag | (signbit(x) ? 0x8 : 0));
+}
+
+/* float amax / 448 in single precision; 1 for an all-zero vector */
+static float fp8_scale(const float* x, int n) {
+  float amax = 0.f;
+  for (int i = 0; i < n; ++i) {
+    const float a = fabsf(x[i]);
+    if (a > amax) amax = a;
+  }
+  return amax > 0.f ? amax / 448.0f : 1.0f;
+}
+
+/*
+ * Writes the nq new tokens of every sequence (context L includes them: token
+ * L - nq + j is new row j) into the pool: latent codes e4m3(x / latent_scale)
+ * and the index key (FP8: codes e4m3(x / s) with s = amax/448 stored as fp32;
+ * MXFP4: per 32 elements E = floor(log2 amax) - 2 clamped to [-127, 127],
+ * codes e2m1(x * 2^-E), byte E + 127).  Inputs are bf16 bits:
+ * new_latent [batch*nq][576], new_key [batch*nq][128].  Returns 3 for a
+ * block-table entry outside the pool.
+ */
+int oracle_cache_append(uint8_t* pool, int64_t row_stride, int64_t latent_off, int64_t index_off,
+                        int32_t num_blocks, int32_t key_format, float latent_scale, const int32_t* block_table,
+                        int32_t max_blocks, const int32_t* seq_lens, int32_t batch, int32_t nq,
+                        const uint16_t* new_latent, const uint16_t* new_key) {
+  for (int b = 0; b < batch; ++b) {
+    for (int j = 0; j < nq; ++j) {
+      const int64_t t = (int64_t)seq_lens[b] - nq + j;
+      if (t < 0) continue;
+      const int32_t r = block_table[(int64_t)b * max_blocks + t / ORACLE_BLOCK];
+      if (r < 0 || r >= num_blocks) return ORACLE_BAD_BLOCK;
+      const int slot = (int)(t % ORACLE_BLOCK);
+      uint8_t* row = pool + (int64_t)r * row_stride;
+      const int64_t nr = (int64_t)b * nq + j;
+      const uint16_t* lat = new_latent + nr * ORACLE_LATENT;
+      for (int d = 0; d < ORACLE_LATENT; ++d) {
+        const float x = (float)oracle_bf16_to_double(lat[d]);
+        row[latent_off + (int64_t)slot * ORACLE_LATENT + d] = oracle_e4m3_encode((double)(x / latent_scale));
+      }
+      float k[ORACLE_IDX_DIM];
+      for (int d = 0; d < ORACLE_IDX_DIM; ++d) k[d] = (float)oracle_bf16_to_double(new_key[nr * ORACLE_IDX_DIM + d]);
+      uint8_t* page = row + index_off;
+      if (key_format == 0) {
+        const float s = fp8_scale(k, ORACLE_IDX_DIM);
+        for (int d = 0; d < ORACLE_IDX_DIM; ++d)
+          page[(int64_t)slot * ORACLE_IDX_DIM + d] = oracle_e4m3_encode((double)(k[d] / s));
+        memcpy(page + ORACLE_BLOCK * ORACLE_IDX_DIM + 4 * slot, &s, 4);
+      } else {
+        for (int blk = 0; blk < ORACLE_IDX_DIM / 32; ++blk) {
+          double amax = 0.0;
+          for (int d = 0; d < 32; ++d) amax = fmax(amax, fabs((double)k[32 * blk + d]));
+          int e = -127;
+          if (amax > 0.0) {
+            int ex;
+            frexp(amax, &ex);  /* amax = m * 2^ex, m in [0.5, 1): floor(log2 amax) = ex - 1 */
+            e = ex - 1 - 2;
+            if (e < -127) e = -127;
+            if (e > 127) e = 127;
+          }
+          uint8_t codes[32];
+          for (int d = 0; d < 32; ++d) codes[d] = oracle_e2m1_encode(ldexp((double)k[32 * blk + d], -e));
+          for (int d = 0; d < 32; d += 2)
+            page[(int64_t)slot * (ORACLE_IDX_DIM / 2) + 16 * blk + d / 2] = (uint8_t)(codes[d] | (codes[d + 1] << 4));
+          page[ORACLE_BLOCK * (ORACLE_IDX_DIM / 2) + 4 * slot + blk] = (uint8_t)(e + 127);
+        }
+      }
+    }
+  }
+  return ORACLE_OK;
+}
+
+/*
+ * Indexer query in FP8 per (row, head): s = amax/448 (fp32), codes
+ * e4m3(q / s), and the scale folded into the head weight, w_out = w * s
+ * (ReLU is positively homogeneous: w max(0, t q.k) = w s max(0, t (q/s).k)).
+ */
+int oracle_quantize_query(const uint16_t* q, const float* w, int32_t rows, uint8_t* codes, float* w_out) {
+  for (int64_t rh = 0; rh < (int64_t)rows * ORACLE_IDX_HEADS; ++rh) {
+    float x[ORACLE_IDX_DIM];
+    for (int d = 0; d < ORACLE_IDX_DIM; ++d) x[d] = (float)oracle_bf16_to_double(q[rh * ORACLE_IDX_DIM + d]);
+    const float s = fp8_scale(x, ORACLE_IDX_DIM);
+    for (int d = 0; d < ORACLE_IDX_DIM; ++d) codes[rh * ORACLE_IDX_DIM + d] = oracle_e4m3_encode((double)(x[d] / s));
+    w_out[rh] = w[rh] * s;
+  }
+  return ORACLE_OK;
+}

@@ -313,3 +313,105 @@ def test_decode_step_composes_the_three_stages():
         _is_valid_topk(s[r], int(c.row_lens()[r]), 128, idx[r])
     o2, l2 = oracle.sparse_mla(c, idx)
     assert np.array_equal(o2, out) and np.array_equal(l2, lse)
+
+
+# ---------------------------------------------------------------- new-token write and FP8 query
+def _bf16_bits(x):
+    return torch.from_numpy(np.ascontiguousarray(x, dtype=np.float32)).to(torch.bfloat16).view(torch.int16).numpy().view(np.uint16)
+
+
+def _bf16_value(bits):
+    return (np.asarray(bits, dtype=np.uint32) << 16).view(np.float32)
+
+
+def _torch_e4m3(x):
+    t = torch.from_numpy(np.clip(np.asarray(x, dtype=np.float32), -448.0, 448.0))
+    return t.to(torch.float8_e4m3fn).view(torch.uint8).numpy()
+
+
+_E2M1_MAG = np.array([0.0, 0.5, 1.0, 1.5, 2.0, 3.0, 4.0, 6.0])
+
+
+def _e2m1_brute(x):
+    """Nearest E2M1 code by search, ties to the even code, saturating at 6."""
+    a = min(abs(x), 6.0)
+    d = np.abs(_E2M1_MAG - a)
+    best = [c for c in range(8) if d[c] == d.min()]
+    c = min(best, key=lambda c: (c % 2, c))
+    return c | (8 if np.signbit(x) else 0)
+
+
+def test_e4m3_encode_matches_torch():
+    rng = np.random.default_rng(11)
+    x = np.concatenate([
+        rng.standard_normal(4000) * np.exp(rng.uniform(-14, 7, 4000)),
+        [0.0, -0.0, 448.0, 449.0, 464.0, 1e6, -1e6, 2.0 ** -9, 2.0 ** -10, 3 * 2.0 ** -11],
+        # exact midpoints between neighbouring codes (ties to even)
+        [(oracle.e4m3_to_double(c) + oracle.e4m3_to_double(c + 1)) / 2 for c in range(0, 0x7E)],
+    ]).astype(np.float32)
+    got = np.array([oracle.e4m3_encode(float(v)) for v in x], dtype=np.uint8)
+    np.testing.assert_array_equal(got, _torch_e4m3(x))
+
+
+def test_e2m1_encode_is_nearest_ties_even():
+    vals = list(np.arange(-9, 9, 1 / 64)) + [0.25, 0.75, 1.25, 1.75, 2.5, 3.5, 5.0, -0.0, 6.0, 7.0, 100.0]
+    for v in vals:
+        assert oracle.e2m1_encode(float(v)) == _e2m1_brute(float(v)), v
+
+
+@pytest.mark.parametrize("fmt", [synth.KEY_FP8, synth.KEY_MXFP4])
+def test_cache_append_writes_nearest_codes(fmt):
+    case = synth.make_case("app", seq_lens=[130, 64], nq=3, key_format=fmt, seed=4)
+    rng = np.random.default_rng(5)
+    lat = rng.standard_normal((case.rows, 576)).astype(np.float32) * 3
+    key = rng.standard_normal((case.rows, 128)).astype(np.float32)
+    key[1] = 0.0                               # an all-zero key
+    key[2, :32] *= 1e-30                       # a block of tiny values
+    lat[0, :5] = [1e6, -1e6, 0.0, -0.0, 1e-30]
+    lat_b, key_b = _bf16_bits(lat), _bf16_bits(key)
+    lat, key = _bf16_value(lat_b), _bf16_value(key_b)
+    pool = oracle.cache_append(case, lat_b, key_b)
+    changed = np.zeros_like(pool, dtype=bool)
+    for b in range(case.batch):
+        for j in range(case.nq):
+            nr = b * case.nq + j
+            t = int(case.seq_lens[b]) - case.nq + j
+            r = case.block_table[b, t // 64]
+            slot = t % 64
+            lat_codes = pool[r, case.latent_off + slot * 576:case.latent_off + (slot + 1) * 576]
+            np.testing.assert_array_equal(lat_codes, _torch_e4m3(lat[nr] / np.float32(case.latent_scale)))
+            changed[r, case.latent_off + slot * 576:case.latent_off + (slot + 1) * 576] = True
+            page = pool[r, case.index_off:]
+            if fmt == synth.KEY_FP8:
+                amax = np.float32(np.abs(key[nr]).max())
+                s = amax / np.float32(448.0) if amax > 0 else np.float32(1.0)
+                np.testing.assert_array_equal(page[slot * 128:(slot + 1) * 128], _torch_e4m3(key[nr] / s))
+                assert page[64 * 128 + 4 * slot:64 * 128 + 4 * slot + 4].view(np.float32)[0] == s
+                changed[r, case.index_off + slot * 128:case.index_off + (slot + 1) * 128] = True
+                changed[r, case.index_off + 64 * 128 + 4 * slot:case.index_off + 64 * 128 + 4 * slot + 4] = True
+            else:
+                for blk in range(4):
+                    xs = key[nr, 32 * blk:32 * blk + 32].astype(np.float64)
+                    amax = np.abs(xs).max()
+                    e = -127 if amax == 0 else max(-127, min(127, int(np.floor(np.log2(amax))) - 2))
+                    assert page[64 * 64 + 4 * slot + blk] == e + 127
+                    packed = page[slot * 64 + 16 * blk:slot * 64 + 16 * blk + 16]
+                    codes = np.stack([packed & 0xF, packed >> 4], axis=1).reshape(-1)
+                    assert [int(c) for c in codes] == [_e2m1_brute(float(v) * 2.0 ** -e) for v in xs]
+                changed[r, case.index_off + slot * 64:case.index_off + (slot + 1) * 64] = True
+                changed[r, case.index_off + 64 * 64 + 4 * slot:case.index_off + 64 * 64 + 4 * slot + 4] = True
+    np.testing.assert_array_equal(pool[~changed], case.pool[~changed])  # nothing else is touched
+
+
+def test_quantize_query_folds_the_scale():
+    rng = np.random.default_rng(8)
+    q = rng.standard_normal((3, 32, 128)).astype(np.float32) * np.exp(rng.uniform(-3, 3, (3, 32, 1)))
+    q[0, 5] = 0.0
+    q_b = _bf16_bits(q)
+    q = _bf16_value(q_b)
+    w = rng.standard_normal((3, 32)).astype(np.float32)
+    codes, w_out = oracle.quantize_query(q_b, w)
+    amax = np.abs(q).max(axis=2)
+    s = np.where(amax > 0, amax / np.float32(448.0), np.float32(1.0)).astype(np.float32)
+    np.testing.assert_array_equal(codes, _torch_e4m3(q / s[..., None]))
+    np.testing.assert_array_equal(w_out, (w * s).astype(np.float32))
