@@ -381,9 +381,11 @@ def main_ours(args):
 
 
 def launches_per_step(case):
-    """Kernels of libdsa one dsa_decode_step launches: indexer; top-k histogram, threshold, collect
-    (rows longer than k only) and final; sparse MLA and its split combine."""
-    return 1 + (4 if case.max_len > case.topk else 1) + 2
+    """Kernels of libdsa one dsa_decode_step launches: the indexer; the top-k (one cluster kernel
+    for rows up to 8 x 40,960 tokens, else histogram, threshold, collect and final); the sparse
+    MLA and its chunk combine."""
+    long_rows = case.max_len > case.topk and (case.max_len + 40959) // 40960 > 8
+    return 1 + (4 if long_rows else 1) + 2
 
 
 def load_traffic(workload):
