@@ -239,11 +239,13 @@ def main_ours(args):
             torch.cuda.synchronize()
         barrier()
         t_wall = time.perf_counter()
+        n_launch0 = binding.kernel_launches()
         for e0, e1 in ev:
             flush.zero_()
             e0.record(stream)
             step()
             e1.record(stream)
+        n_launches = binding.kernel_launches() - n_launch0
         barrier()
         t_wall = time.perf_counter() - t_wall
     clocks = clk.summary()
@@ -365,7 +367,7 @@ def main_ours(args):
         "stage_us": {kk: round(v * 1e3, 2) for kk, v in st_ms.items()},
         "stages": stages,
         "roofline": roof,
-        "gpu_launches": launches_per_step(case) * args.steps,
+        "gpu_launches": n_launches,
         "clocks": clocks,
         "wall_s_timed_region": round(t_wall, 4),
     }
@@ -378,14 +380,6 @@ def main_ours(args):
         print(json.dumps(line), flush=True)
     if world > 1:
         dist.destroy_process_group()
-
-
-def launches_per_step(case):
-    """Kernels of libdsa one dsa_decode_step launches: the indexer; the top-k (one cluster kernel
-    for rows up to 8 x 40,960 tokens, else histogram, threshold, collect and final); the sparse
-    MLA and its chunk combine."""
-    long_rows = case.max_len > case.topk and (case.max_len + 40959) // 40960 > 8
-    return 1 + (4 if long_rows else 1) + 2
 
 
 def load_traffic(workload):

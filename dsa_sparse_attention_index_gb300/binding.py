@@ -44,8 +44,9 @@ class BatchT(ctypes.Structure):
 
 _lib = None
 
-EXPORTS = ["dsa_api_version", "dsa_status_string", "dsa_last_cuda_error", "dsa_translate_pages", "dsa_index_scores",
-           "dsa_topk_workspace_size", "dsa_topk", "dsa_topk_noalloc", "sparse_mla_workspace_size",
+EXPORTS = ["dsa_api_version", "dsa_status_string", "dsa_last_cuda_error", "dsa_kernel_launches",
+           "dsa_translate_pages", "dsa_index_scores",
+           "dsa_topk_workspace_size", "dsa_topk", "dsa_topk_noalloc", "dsa_topk_force_multipass", "sparse_mla_workspace_size",
            "sparse_mla_decode",
            "dsa_workspace_size", "dsa_decode_step", "dsa_cache_append", "dsa_quantize_index_query",
            "dsa_selftest_wait_timeout"]
@@ -65,11 +66,13 @@ def lib():
             "dsa_api_version": (i32, []),
             "dsa_status_string": (ctypes.c_char_p, [i32]),
             "dsa_last_cuda_error": (ctypes.c_char_p, []),
+            "dsa_kernel_launches": (ctypes.c_uint64, []),
             "dsa_translate_pages": (i32, [pc, pb, P, P, P, P]),
             "dsa_index_scores": (i32, [pc, pb, P, P, P, i64, P, P]),
             "dsa_topk_workspace_size": (sz, [i32, i32, i32]),
             "dsa_topk": (i32, [P, i64, P, i32, i32, i32, P, P, sz, P, P]),
             "dsa_topk_noalloc": (i32, [P, i64, P, i32, i32, i32, P, P, P]),
+            "dsa_topk_force_multipass": (i32, [i32]),
             "sparse_mla_workspace_size": (sz, [i32, i32]),
             "sparse_mla_decode": (i32, [pc, pb, P, P, i32, f32, P, P, P, sz, P, P]),
             "dsa_workspace_size": (sz, [pb, i32]),
@@ -84,6 +87,17 @@ def lib():
             fn.argtypes = args
         _lib = L
     return _lib
+
+
+def topk_force_multipass(on: bool) -> bool:
+    """Route rows longer than 327,680 tokens through the four-kernel top-k
+    (True) or the automatic choice (False); returns the previous setting."""
+    return bool(lib().dsa_topk_force_multipass(int(bool(on))))
+
+
+def kernel_launches() -> int:
+    """Kernels libdsa has launched in this process so far."""
+    return int(lib().dsa_kernel_launches())
 
 
 def status_string(code: int) -> str:

@@ -2,6 +2,7 @@
 // the stream-ordered composition of the kernels.  No allocation, no host
 // synchronisation on any entry point.
 #include <algorithm>
+#include <atomic>
 #include <cstdio>
 #include <mutex>
 
@@ -23,7 +24,10 @@ int num_sms() {
 
 namespace {
 thread_local char g_last_cuda_error[256] = "";
+std::atomic<uint64_t> g_launches{0};
 }  // namespace
+
+void count_launches(int n) { g_launches.fetch_add((uint64_t)n, std::memory_order_relaxed); }
 
 dsa_status_t cuda_status(cudaError_t e) {
   if (e == cudaSuccess) return DSA_OK;
@@ -121,6 +125,10 @@ extern "C" {
 int32_t dsa_api_version(void) { return DSA_API_VERSION; }
 
 const char* dsa_last_cuda_error(void) { return g_last_cuda_error; }
+
+int32_t dsa_topk_force_multipass(int32_t on) { return dsa::topk_force_multipass(on); }
+
+uint64_t dsa_kernel_launches(void) { return dsa::g_launches.load(std::memory_order_relaxed); }
 
 const char* dsa_status_string(int32_t s) {
   switch (s) {

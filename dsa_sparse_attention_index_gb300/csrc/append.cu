@@ -112,6 +112,7 @@ dsa_status_t launch_cache_append(const dsa_paged_cache_t& c, const dsa_batch_t& 
   if (rows == 0) return DSA_OK;
   uint8_t* base = static_cast<uint8_t*>(c.base);
   const int cap = std::min(bt.max_blocks_per_seq * kBlock, bt.max_seq_len);
+  count_launches(1);
   cache_append_kernel<<<rows, kAppendThreads, 0, st>>>(base + c.latent_off, base + c.index_off, c.row_stride,
                                                        c.num_blocks, c.key_format, c.latent_scale, bt.block_table,
                                                        bt.max_blocks_per_seq, bt.seq_lens, bt.queries_per_seq, cap,
@@ -123,6 +124,7 @@ dsa_status_t launch_quantize_query(const uint16_t* q, const float* w, int rows, 
                                    cudaStream_t st) {
   const int64_t pairs = (int64_t)rows * kIdxHeads;
   if (pairs == 0) return DSA_OK;
+  count_launches(1);
   quantize_query_kernel<<<(unsigned)((pairs + 3) / 4), 128, 0, st>>>(q, w, pairs, codes, w_out);
   return launch_status();
 }

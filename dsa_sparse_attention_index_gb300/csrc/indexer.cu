@@ -521,6 +521,7 @@ dsa_status_t launch_nq(const IdxParams& p, const CUtensorMap& keys, const CUtens
   }
   const int64_t units_bound = (int64_t)p.batch * p.groups * ((p.max_seq_len + kUnitKeys - 1) / kUnitKeys);
   const int grid = (int)std::max<int64_t>(1, std::min<int64_t>(units_bound, num_sms()));
+  count_launches(1);
   indexer_kernel<NQ, MX><<<grid, idx_threads<MX>(), IdxSmem<NQ>::bytes(p.batch * p.groups), st>>>(keys, scales, q, p);
   return launch_status();
 }

@@ -19,6 +19,10 @@ dsa_status_t cuda_status(cudaError_t e);
 // cuda_status(cudaGetLastError()): the launch check after a kernel launch.
 inline dsa_status_t launch_status() { return cuda_status(cudaGetLastError()); }
 
+// Adds n to the count of kernel launches the library has issued (process-wide,
+// read through dsa_kernel_launches).
+void count_launches(int n);
+
 // cuTensorMapEncodeTiled through the runtime's driver entry point (no libcuda
 // link dependency).  strides: rank-1 byte strides of dims 1..rank-1.
 bool encode_tmap(CUtensorMap* map, CUtensorMapDataType dtype, int rank, const void* base, const uint64_t* dims,
@@ -30,6 +34,8 @@ dsa_status_t launch_translate_pages(const dsa_paged_cache_t& c, const dsa_batch_
 dsa_status_t launch_index_scores(const dsa_paged_cache_t& c, const dsa_batch_t& bt, const uint8_t* q_index,
                                  const float* head_w, float* scores, int64_t ld, int32_t* status, cudaStream_t st);
 size_t topk_workspace_bytes(int rows, int max_row_len, int k);
+// Process-wide choice of the four-kernel top-k for rows too long for shared memory.
+int topk_force_multipass(int on);
 dsa_status_t launch_topk(const float* scores, int64_t ld, const int32_t* row_lens, const int32_t* seq_lens, int nq,
                          int rows, int max_row_len, int k, int32_t* out, void* workspace, int32_t* status,
                          cudaStream_t st);

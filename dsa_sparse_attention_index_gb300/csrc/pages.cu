@@ -65,6 +65,7 @@ dsa_status_t launch_translate_pages(const dsa_paged_cache_t& c, const dsa_batch_
   const int threads = 256;
   const int grid = (int)std::min<int64_t>((n + threads - 1) / threads, 4 * (int64_t)num_sms());
   const int cap = std::min(bt.max_blocks_per_seq * kBlock, bt.max_seq_len);
+  count_launches(1);
   translate_pages_kernel<<<grid, threads, 0, st>>>(static_cast<const uint8_t*>(c.base), c.row_stride, c.latent_off,
                                                    c.index_off, c.num_blocks, bt.block_table,
                                                    bt.max_blocks_per_seq, bt.seq_lens, bt.batch, cap, latent_pages,
@@ -75,6 +76,7 @@ dsa_status_t launch_translate_pages(const dsa_paged_cache_t& c, const dsa_batch_
 dsa_status_t launch_wait_selftest(int64_t limit_ns, int32_t* status, cudaStream_t st) {
   if (limit_ns < 1000000) limit_ns = 1000000;
   if (limit_ns > 2000000000) limit_ns = 2000000000;
+  count_launches(1);
   wait_selftest_kernel<<<1, 32, 0, st>>>((uint64_t)limit_ns, status);
   return launch_status();
 }

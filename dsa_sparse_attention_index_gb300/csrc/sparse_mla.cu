@@ -602,11 +602,13 @@ dsa_status_t launch_sparse_mla(const dsa_paged_cache_t& c, const dsa_batch_t& bt
   cfg.stream = st;
   cfg.attrs = pdl;
   cfg.numAttrs = 1;
+  count_launches(1);
   if (cuda_status(cudaLaunchKernelEx(&cfg, sparse_mla_kernel, qmap, p)) != DSA_OK) return DSA_ERR_CUDA;
   cudaLaunchConfig_t cfg2 = cfg;
   cfg2.gridDim = dim3(kHeads / kCombineHeads, (unsigned)rows);
   cfg2.blockDim = dim3(256);
   cfg2.dynamicSmemBytes = 0;
+  count_launches(1);
   if (cuda_status(cudaLaunchKernelEx(&cfg2, mla_combine_kernel, (const float*)opart, (const float*)ml, nsplit,
                                      c.latent_scale, out, lse)) != DSA_OK)
     return DSA_ERR_CUDA;

@@ -9,14 +9,18 @@
 // order-preserving 32-bit keys (integer radix).
 //
 // Rows up to 8 x 40,960 tokens: one kernel, a thread-block cluster per row
-// (topk_resident_kernel).  Each CTA of the cluster keeps its slice of the
+// (topk_cluster_kernel).  Each CTA of the cluster keeps its slice of the
 // row as keys in shared memory, read once from L2; up to three digit passes
-// (12, 12 and 8 bits) find the k-th key, each pass merging the CTAs'
+// (11, 11 and 10 bits) find the k-th key, each pass merging the CTAs'
 // histograms through distributed shared memory; ties on the k-th key go to
 // the lowest indices in CTA-rank and token order; a cluster-wide scan then
 // writes the chosen indices in ascending order.  No workspace is used.
 //
-// Longer rows (the 1M-token rows) take four kernels over a workspace:
+// Longer rows (the 1M-token rows) take the same kernel in its streaming form:
+// a cluster of 16 CTAs per row (8 where the device cannot schedule 16) that
+// reads its slice again from L2 in every pass and keeps only the histograms
+// in shared memory.  Where neither cluster can be scheduled, four kernels
+// over a workspace do the selection:
 //   1. hist:    multi-CTA per row: 4096-bin histogram of the key's top 12
 //               bits, merged into a per-row global histogram.
 //   2. threshold: one CTA per row finds the bin T holding the k-th largest
@@ -31,6 +35,8 @@
 //               buffer overflowed (heavily tied scores) it re-derives the
 //               candidates from the scores directly.
 #include <algorithm>
+#include <atomic>
+#include <type_traits>
 #include <mutex>
 
 #include <cooperative_groups.h>
@@ -497,26 +503,104 @@ constexpr int kD1 = 11, kD2 = 11, kD3 = 10;
 constexpr int kB1 = 1 << kD1, kB2 = 1 << kD2, kB3 = 1 << kD3;
 // shared memory: keys[slice] | h1[kB1] | h2[kB2] | h3[kB3] | g[kB1] | scan[32] | misc[32]
 constexpr size_t kResFixed = 4 * ((size_t)kB1 + kB2 + kB3 + kB1 + 64);
+constexpr int kRangeTotal = 24;  // misc slot: the total of this CTA's bin range in a merge
+constexpr int kOverflow = 25;    // misc slot: a warp took more indices than it can stage
+constexpr int kStageCap = (kB1 + kB2) / kResWarps;  // indices a warp stages in h1/h2 (256)
 size_t res_smem(int slice) { return 4 * (size_t)slice + kResFixed; }
 
-// Warp-wide exclusive prefix sum of one value per lane; `total` gets the sum.
-__device__ __forceinline__ uint32_t warp_excl_scan(uint32_t v, uint32_t& total) {
-  const int lane = threadIdx.x & 31;
-  uint32_t x = v;
-#pragma unroll
-  for (int d = 1; d < 32; d <<= 1) {
-    const uint32_t u = __shfl_up_sync(0xffffffffu, x, d);
-    if (lane >= d) x += u;
-  }
-  total = __shfl_sync(0xffffffffu, x, 31);
-  return x - v;
+// Warp-wide exclusive prefix sum of one value 0..7 per lane, from three
+// ballots of its bits; `total` gets the sum.
+__device__ __forceinline__ uint32_t warp_excl_scan_small(uint32_t v, uint32_t lanes_below, uint32_t& total) {
+  const uint32_t b0 = __ballot_sync(0xffffffffu, v & 1u), b1 = __ballot_sync(0xffffffffu, v & 2u),
+                 b2 = __ballot_sync(0xffffffffu, v & 4u);
+  total = __popc(b0) + 2u * __popc(b1) + 4u * __popc(b2);
+  return __popc(b0 & lanes_below) + 2u * __popc(b1 & lanes_below) + 4u * __popc(b2 & lanes_below);
 }
 
-template <int C>
+// A key range [klo, khi] of score_key order as scores, so that the streaming
+// passes compare scores without converting them: a score's key lies in the
+// range iff lo <= s <= hi, and above it iff s > hi.  The compares are IEEE (the
+// library is built without flush-to-zero), so -0 == +0 as in score_key.  NaN
+// scores (key 0) fail every compare; a range that starts at key 0 holds
+// exactly the NaN scores (no score has a key in 1..0x7FFFFE), flagged by
+// `nan`, and then every other score is above it.  Ranges chosen by a digit
+// pass always hold a key that occurs, so khi never falls in 1..0x7FFFFE.
+struct ScoreRange {
+  float lo, hi;
+  bool nan;
+};
+
+__device__ __forceinline__ float key_score(uint32_t key) {  // the score of a key that occurs
+  return __uint_as_float((key & 0x80000000u) ? (key & 0x7FFFFFFFu) : ~key);
+}
+
+__device__ __forceinline__ ScoreRange score_range(uint32_t klo, uint32_t khi) {
+  ScoreRange r;
+  r.nan = klo == 0u;
+  r.lo = klo <= 0x007FFFFFu ? __uint_as_float(0xFF800000u) : key_score(klo);  // key of -inf: 0x007FFFFF
+  r.hi = khi >= 0xFF800000u   ? __uint_as_float(0x7F800000u)                  // key of +inf: 0xFF800000
+         : khi == 0x7FFFFFFFu ? __uint_as_float(0x80000001u)  // just below the zeros' key: -denorm_min
+                              : key_score(khi);
+  return r;
+}
+
+// A threshold range in both forms: keys [klo, klo + span] and their scores.
+struct KeyRange {
+  uint32_t klo, span;
+  ScoreRange s;
+};
+
+__device__ __forceinline__ KeyRange key_range(uint32_t prefix, int shift) {
+  KeyRange r;
+  r.klo = prefix << shift;
+  r.span = (1u << shift) - 1u;
+  r.s = score_range(r.klo, r.klo + r.span);
+  return r;
+}
+
+// Bit j: element j of a group (keys, or scores when streaming) lies in the
+// range / above it.
+__device__ __forceinline__ uint32_t bits_in(const uint4& v, const KeyRange& r) {
+  return (uint32_t)(v.x - r.klo <= r.span) | ((uint32_t)(v.y - r.klo <= r.span) << 1) |
+         ((uint32_t)(v.z - r.klo <= r.span) << 2) | ((uint32_t)(v.w - r.klo <= r.span) << 3);
+}
+__device__ __forceinline__ uint32_t bits_above(const uint4& v, const KeyRange& r) {
+  const uint32_t hi = r.klo + r.span;
+  return (uint32_t)(v.x > hi) | ((uint32_t)(v.y > hi) << 1) | ((uint32_t)(v.z > hi) << 2) | ((uint32_t)(v.w > hi) << 3);
+}
+__device__ __forceinline__ uint32_t bits_in(const float4& v, const KeyRange& r) {
+  const ScoreRange& s = r.s;
+  if (s.nan)
+    return (uint32_t)(v.x != v.x) | ((uint32_t)(v.y != v.y) << 1) | ((uint32_t)(v.z != v.z) << 2) |
+           ((uint32_t)(v.w != v.w) << 3);
+  return (uint32_t)(v.x >= s.lo && v.x <= s.hi) | ((uint32_t)(v.y >= s.lo && v.y <= s.hi) << 1) |
+         ((uint32_t)(v.z >= s.lo && v.z <= s.hi) << 2) | ((uint32_t)(v.w >= s.lo && v.w <= s.hi) << 3);
+}
+__device__ __forceinline__ uint32_t bits_above(const float4& v, const KeyRange& r) {
+  const ScoreRange& s = r.s;
+  if (s.nan)
+    return (uint32_t)(v.x == v.x) | ((uint32_t)(v.y == v.y) << 1) | ((uint32_t)(v.z == v.z) << 2) |
+           ((uint32_t)(v.w == v.w) << 3);
+  return (uint32_t)(v.x > s.hi) | ((uint32_t)(v.y > s.hi) << 1) | ((uint32_t)(v.z > s.hi) << 2) |
+         ((uint32_t)(v.w > s.hi) << 3);
+}
+__device__ __forceinline__ uint32_t elem_key(const uint4& v, int j) {
+  return j == 0 ? v.x : j == 1 ? v.y : j == 2 ? v.z : v.w;
+}
+__device__ __forceinline__ uint32_t elem_key(const float4& v, int j) {
+  return score_key(j == 0 ? v.x : j == 1 ? v.y : j == 2 ? v.z : v.w);
+}
+
+// kStream = false: each CTA keeps its slice of the row as keys in shared
+// memory.  kStream = true (rows too long for that): every pass reads the
+// slice's scores again from global memory (L2), and shared memory holds only
+// the histograms.
+template <int C, bool kStream>
 __global__ void __launch_bounds__(kResThreads, 2)  // two CTAs of 512 threads per SM: at most 64 registers
-    topk_resident_kernel(const float* __restrict__ scores, int64_t ld, const int32_t* row_lens,
-                         const int32_t* seq_lens, int nq, int cap, int k, int32_t* out, int32_t* status,
-                         int slice_cap) {
+    topk_cluster_kernel(const float* __restrict__ scores, int64_t ld, const int32_t* row_lens,
+                        const int32_t* seq_lens, int nq, int cap, int k, int32_t* out, int32_t* status,
+                        int slice_cap) {
+  using G = typename std::conditional<kStream, float4, uint4>::type;  // a group of 4 elements
   cg::cluster_group cluster = cg::this_cluster();
   const int c = (int)cluster.block_rank();
   const int r = blockIdx.x / C, tid = threadIdx.x, lane = tid & 31, wid = tid >> 5;
@@ -525,11 +609,11 @@ __global__ void __launch_bounds__(kResThreads, 2)  // two CTAs of 512 threads pe
     else cluster.sync();
   };
   extern __shared__ __align__(16) uint8_t smem_raw[];
-  uint32_t* keys = reinterpret_cast<uint32_t*>(smem_raw);
-  uint32_t* h1 = keys + slice_cap;  // slice_cap: a multiple of 4 (16-byte aligned histograms)
+  uint4* keys4 = reinterpret_cast<uint4*>(smem_raw);  // the slice's keys (resident form)
+  uint32_t* h1 = reinterpret_cast<uint32_t*>(smem_raw) + (kStream ? 0 : slice_cap);  // slice_cap: a multiple of 4
   uint32_t* h2 = h1 + kB1;
   uint32_t* h3 = h2 + kB2;
-  uint32_t* g = h3 + kB3;     // the cluster's histogram of the current digit
+  uint32_t* g = h3 + kB3;  // the cluster's histogram of the current digit (the ranges this CTA reads)
   uint32_t* scan = g + kB1;
   uint32_t* misc = scan + 32;
 
@@ -546,64 +630,107 @@ __global__ void __launch_bounds__(kResThreads, 2)  // two CTAs of 512 threads pe
   const int S = (((len + C - 1) / C) + 3) & ~3;
   const int start = c * S;
   const int n = max(0, min(S, len - start));
-  const int n4 = (n + 3) >> 2;  // 4-key groups; the last one is padded with key 0 (below every score)
+  const int n4 = (n + 3) >> 2;  // groups of 4; the last one is padded with NaN / key 0 (never counted)
+  const float* row = scores + (int64_t)r * ld + start;
+  const float4* row4 = reinterpret_cast<const float4*>(row);
+  const int full4 = n >> 2;
+  auto score_group = [&](int i) -> float4 {  // scores 4i..4i+3 from global memory
+    if (i < full4) return row4[i];
+    const int b = 4 * i;  // the slice's ragged last group
+    const float nan = __uint_as_float(0x7FC00000u);
+    return make_float4(row[b], b + 1 < n ? row[b + 1] : nan, b + 2 < n ? row[b + 2] : nan,
+                       b + 3 < n ? row[b + 3] : nan);
+  };
+  auto load_group = [&](int i) -> G {
+    if constexpr (kStream) return score_group(i);
+    else return keys4[i];
+  };
+  // the valid elements of group i (padding past the slice's end excluded)
+  auto valid_bits = [&](int i) -> uint32_t { return 4 * i + 4 > n ? (1u << (n - 4 * i)) - 1u : 0xFu; };
 
-  // ---- 1. keys into shared memory, histogram of the first digit (bits 31..21)
+  // ---- 1. the slice into shared memory as keys, histogram of the first digit (bits 31..21)
   for (int i = tid; i < (kB1 + kB2 + kB3) / 4; i += kResThreads) reinterpret_cast<uint4*>(h1)[i] = make_uint4(0, 0, 0, 0);
+  if (tid == 0) misc[kOverflow] = 0u;
   __syncthreads();
-  {
-    const float* row = scores + (int64_t)r * ld + start;
-    const float4* row4 = reinterpret_cast<const float4*>(row);
-    const int full4 = n >> 2;
-    for (int i0 = 0; i0 < n4; i0 += 8 * kResThreads) {
-      float4 v[8];  // eight 16-byte loads in flight per thread
+  for (int i0 = 0; i0 < n4; i0 += 8 * kResThreads) {
+    float4 v[8];  // eight 16-byte loads in flight per thread
 #pragma unroll
-      for (int u = 0; u < 8; ++u) {
-        const int i = i0 + u * kResThreads + tid;
-        if (i < full4) {
-          v[u] = row4[i];
-        } else if (i < n4) {  // the row's ragged end
-          const int b = 4 * i;
-          v[u].x = row[b];
-          v[u].y = b + 1 < n ? row[b + 1] : __uint_as_float(0x7FC00000u);
-          v[u].z = b + 2 < n ? row[b + 2] : __uint_as_float(0x7FC00000u);
-          v[u].w = b + 3 < n ? row[b + 3] : __uint_as_float(0x7FC00000u);
-        }
-      }
+    for (int u = 0; u < 8; ++u) {
+      const int i = i0 + u * kResThreads + tid;
+      if (i < n4) v[u] = score_group(i);
+    }
 #pragma unroll
-      for (int u = 0; u < 8; ++u) {
-        const int i = i0 + u * kResThreads + tid;
-        if (i < n4) {
-          const uint4 kk = make_uint4(score_key(v[u].x), score_key(v[u].y), score_key(v[u].z), score_key(v[u].w));
-          reinterpret_cast<uint4*>(keys)[i] = kk;
-          const bool pad = 4 * i + 3 >= n;  // padding keys are not counted
-          atomicAdd(&h1[kk.x >> (32 - kD1)], 1u);
-          if (!pad || 4 * i + 1 < n) atomicAdd(&h1[kk.y >> (32 - kD1)], 1u);
-          if (!pad || 4 * i + 2 < n) atomicAdd(&h1[kk.z >> (32 - kD1)], 1u);
-          if (!pad) atomicAdd(&h1[kk.w >> (32 - kD1)], 1u);
-        }
+    for (int u = 0; u < 8; ++u) {
+      const int i = i0 + u * kResThreads + tid;
+      if (i < n4) {
+        const uint4 kk = make_uint4(score_key(v[u].x), score_key(v[u].y), score_key(v[u].z), score_key(v[u].w));
+        if (!kStream) keys4[i] = kk;
+        const bool pad = 4 * i + 3 >= n;  // padding keys are not counted
+        atomicAdd(&h1[kk.x >> (32 - kD1)], 1u);
+        if (!pad || 4 * i + 1 < n) atomicAdd(&h1[kk.y >> (32 - kD1)], 1u);
+        if (!pad || 4 * i + 2 < n) atomicAdd(&h1[kk.z >> (32 - kD1)], 1u);
+        if (!pad) atomicAdd(&h1[kk.w >> (32 - kD1)], 1u);
       }
     }
   }
-  // the cluster-wide histogram: every CTA sums its peers' copies (distributed
-  // shared memory), all C loads of a bin in flight together
-  auto merge = [&](uint32_t* local, int nbins) {
-    csync();
-    for (int i = tid; i < nbins; i += kResThreads) {
-      uint32_t x[C];
+  // The cluster-wide choice of a digit from the CTAs' histograms `local`
+  // (nbins bins each).  CTA q sums bin range q of every CTA's copy (distributed
+  // shared memory) into its own g and publishes the range's total; every CTA
+  // then finds, from the C totals, the range holding the need-th largest key,
+  // copies that range's sums and picks the digit within it.  Each CTA loads
+  // about 2 * nbins peer values, whatever the cluster size.
+  auto merge_pick = [&](uint32_t* local, int nbins, uint32_t& need, int& digit, uint32_t& pop) {
+    if constexpr (C == 1) {
+      __syncthreads();
+      pick_digit(local, nbins, scan, need, digit, pop);
+    } else {
+      const int per = (nbins + C - 1) / C;
+      csync();  // every CTA's histogram is complete
+      {
+        const int lo = min(nbins, c * per), hi = min(nbins, lo + per);
+        uint32_t part = 0;
+        for (int b = lo + tid; b < hi; b += kResThreads) {
+          uint32_t sum = 0;
 #pragma unroll
-      for (int q = 0; q < C; ++q) x[q] = C == 1 ? local[i] : cluster.map_shared_rank(local, q)[i];
-      uint32_t sum = 0;
-#pragma unroll
-      for (int q = 0; q < C; ++q) sum += x[q];
-      g[i] = sum;
+          for (int q = 0; q < C; ++q) sum += cluster.map_shared_rank(local, q)[b];
+          g[b] = sum;
+          part += sum;
+        }
+        part = __reduce_add_sync(0xffffffffu, part);
+        if (lane == 0) scan[wid] = part;
+        __syncthreads();
+        if (tid == 0) {
+          uint32_t t = 0;
+          for (int w = 0; w < kResWarps; ++w) t += scan[w];
+          misc[kRangeTotal] = t;
+        }
+      }
+      csync();  // every range is summed
+      if (tid < C) scan[tid] = cluster.map_shared_rank(misc, tid)[kRangeTotal];
+      __syncthreads();
+      int owner = 0;
+      uint32_t above = 0;
+      for (int q = C - 1; q >= 0; --q) {  // high bins first
+        if (above + scan[q] >= need) {
+          owner = q;
+          break;
+        }
+        above += scan[q];
+      }
+      const int lo = min(nbins, owner * per), hi = min(nbins, lo + per);
+      if (owner != c) {
+        const uint32_t* src = cluster.map_shared_rank(g, owner);
+        for (int b = lo + tid; b < hi; b += kResThreads) g[b] = src[b];
+      }
+      __syncthreads();
+      need -= above;
+      pick_digit(g + lo, hi - lo, scan, need, digit, pop);
+      digit += lo;
     }
-    __syncthreads();
   };
-  merge(h1, kB1);
   uint32_t need = (uint32_t)k, pop;
   int digit;
-  pick_digit(g, kB1, scan, need, digit, pop);
+  merge_pick(h1, kB1, need, digit, pop);
   // Keys whose bits above `shift` exceed `prefix` are taken; keys equal to it on
   // those bits form the threshold group, taken whole unless `tie` (only on the
   // full 32 bits), where the first `quota` of them in token order are taken.
@@ -611,32 +738,47 @@ __global__ void __launch_bounds__(kResThreads, 2)  // two CTAs of 512 threads pe
   int shift = 32 - kD1;
   bool tie = false;
   uint32_t quota = 0;
-  const uint4* keys4 = reinterpret_cast<const uint4*>(keys);
-  if (need != pop) {
-    // ---- 2. second digit (bits 20..10) within the threshold group (keys past
-    //         the slice's end are skipped by index)
-    for (int i = tid; i < n4; i += kResThreads) {
-      const uint4 kk = keys4[i];
-      const uint32_t a[4] = {kk.x, kk.y, kk.z, kk.w};
+  // U groups loaded ahead per thread (more when they come from L2)
+  constexpr int U = kStream ? (C > 8 ? 8 : 6) : 4;
+  auto for_my_groups = [&](auto&& body) {  // body(i, group) for groups i = tid + j * kResThreads
+    for (int i0 = tid; i0 < n4; i0 += U * kResThreads) {
+      G v[U];
 #pragma unroll
-      for (int j = 0; j < 4; ++j)
-        if ((a[j] >> (32 - kD1)) == prefix && 4 * i + j < n) atomicAdd(&h2[(a[j] >> kD3) & (kB2 - 1)], 1u);
+      for (int u = 0; u < U; ++u) {
+        const int i = i0 + u * kResThreads;
+        if (i < n4) v[u] = load_group(i);
+      }
+#pragma unroll
+      for (int u = 0; u < U; ++u)
+        if (i0 + u * kResThreads < n4) body(i0 + u * kResThreads, v[u]);
     }
-    merge(h2, kB2);
-    pick_digit(g, kB2, scan, need, digit, pop);
+  };
+  if (need != pop) {
+    // ---- 2. second digit (bits 20..10) within the threshold group
+    const KeyRange rg = key_range(prefix, shift);
+    for_my_groups([&](int i, const G& v) {
+      const uint32_t m = bits_in(v, rg) & valid_bits(i);
+      if (m) {
+#pragma unroll
+        for (int j = 0; j < 4; ++j)
+          if ((m >> j) & 1u) atomicAdd(&h2[(elem_key(v, j) >> kD3) & (kB2 - 1)], 1u);
+      }
+    });
+    merge_pick(h2, kB2, need, digit, pop);
     prefix = (prefix << kD2) | (uint32_t)digit;
     shift = kD3;
     if (need != pop) {
       // ---- 3. last digit (bits 9..0)
-      for (int i = tid; i < n4; i += kResThreads) {
-        const uint4 kk = keys4[i];
-        const uint32_t a[4] = {kk.x, kk.y, kk.z, kk.w};
+      const KeyRange rg3 = key_range(prefix, shift);
+      for_my_groups([&](int i, const G& v) {
+        const uint32_t m = bits_in(v, rg3) & valid_bits(i);
+        if (m) {
 #pragma unroll
-        for (int j = 0; j < 4; ++j)
-          if ((a[j] >> kD3) == prefix && 4 * i + j < n) atomicAdd(&h3[a[j] & (kB3 - 1)], 1u);
-      }
-      merge(h3, kB3);
-      pick_digit(g, kB3, scan, need, digit, pop);
+          for (int j = 0; j < 4; ++j)
+            if ((m >> j) & 1u) atomicAdd(&h3[elem_key(v, j) & (kB3 - 1)], 1u);
+        }
+      });
+      merge_pick(h3, kB3, need, digit, pop);
       prefix = (prefix << kD3) | (uint32_t)digit;
       shift = 0;
       if (need != pop) {
@@ -651,48 +793,74 @@ __global__ void __launch_bounds__(kResThreads, 2)  // two CTAs of 512 threads pe
       }
     }
   }
+  const KeyRange fin = key_range(prefix, shift);  // the threshold group
 
   // ---- 4. emit in ascending token order.  Warp w owns a contiguous run of
-  //         4-key groups; each step covers 128 keys (4 per lane, in lane order).
+  //         groups; each step covers 128 elements (4 per lane, in lane order).
   const int wg = (n4 + kResWarps - 1) / kResWarps;  // groups per warp
   const int g0 = min(n4, wid * wg), g1 = min(n4, g0 + wg);
-  auto classify = [&](int i, uint32_t& gt, uint32_t& eq) {  // bit j: key 4i+j above / in the group
-    gt = eq = 0;
-    if (i < g1) {
-      const uint4 kk = keys4[i];
-      const uint32_t a[4] = {kk.x, kk.y, kk.z, kk.w};
+  // the warp's groups in order, 32 per step (one per lane), U steps loaded ahead;
+  // body(i, group) runs for every lane while the step's first group is in range
+  auto for_warp_groups = [&](auto&& body) {
+    for (int b0 = g0; b0 < g1; b0 += 32 * U) {
+      G v[U];
 #pragma unroll
-      for (int j = 0; j < 4; ++j) {
-        const uint32_t v = a[j] >> shift;
-        const bool in = 4 * i + j < n;
-        gt |= (uint32_t)(in && v > prefix) << j;
-        eq |= (uint32_t)(in && v == prefix) << j;
+      for (int u = 0; u < U; ++u) {
+        const int i = b0 + 32 * u + lane;
+        if (i < g1) v[u] = load_group(i);
       }
+#pragma unroll
+      for (int u = 0; u < U; ++u)
+        if (b0 + 32 * u < g1) body(b0 + 32 * u + lane, v[u]);  // the same for the whole warp
     }
   };
-  uint32_t cnt_gt = 0, cnt_eq = 0;
-  for (int i = g0 + lane; i - lane < g1; i += 32) {
+  auto classify = [&](int i, const G& v, uint32_t& gt, uint32_t& eq) {  // bit j: element 4i+j above / in the group
+    gt = eq = 0;
+    if (i < g1) {
+      const uint32_t valid = valid_bits(i);
+      gt = bits_above(v, fin) & valid;
+      eq = bits_in(v, fin) & valid;
+    }
+  };
+  const uint32_t lanes_below = (1u << lane) - 1u;
+  // 4a. one pass: each warp counts what it takes and stages the slice-local
+  //     indices in token order (bit 31: a key of the threshold group) in its
+  //     share of h1/h2, free once the last merge is done
+  uint32_t* stage = h1 + wid * kStageCap;
+  uint32_t n_sel = 0, n_eq = 0;  // the warp's candidates and threshold-group keys among them
+  for_warp_groups([&](int i, const G& v) {
     uint32_t gt, eq;
-    classify(i, gt, eq);
-    cnt_gt += __popc(gt);
-    cnt_eq += __popc(eq);
-  }
-  cnt_gt = __reduce_add_sync(0xffffffffu, cnt_gt);
-  cnt_eq = __reduce_add_sync(0xffffffffu, cnt_eq);
+    classify(i, v, gt, eq);
+    const uint32_t sel = gt | eq;
+    if (__any_sync(0xffffffffu, sel != 0)) {  // most steps select nothing
+      uint32_t tot;
+      uint32_t p = n_sel + warp_excl_scan_small(__popc(sel), lanes_below, tot);
+#pragma unroll
+      for (int j = 0; j < 4; ++j)
+        if ((sel >> j) & 1u) {
+          if (p < (uint32_t)kStageCap) stage[p] = (uint32_t)(4 * i + j) | (((eq >> j) & 1u) << 31);
+          ++p;
+        }
+      n_sel += tot;
+      if (tie) n_eq += __reduce_add_sync(0xffffffffu, __popc(eq));
+    }
+  });
   if (lane == 0) {
-    scan[wid] = cnt_eq;
-    misc[1 + wid] = cnt_gt;
+    scan[wid] = tie ? n_eq : 0u;             // threshold-group keys that need a quota
+    misc[1 + wid] = tie ? n_sel - n_eq : n_sel;  // taken outright
+    if (n_sel > (uint32_t)kStageCap) misc[kOverflow] = 1u;
   }
   __syncthreads();
   uint32_t eq_before = 0, sel_before = 0, sel_total = 0, eq_take = 0;
   for (int w = 0; w < kResWarps; ++w) {
     const uint32_t e = scan[w], gtw = misc[1 + w];
-    const uint32_t take_e = !tie ? e : (eq_before >= quota ? 0u : min(e, quota - eq_before));
+    const uint32_t take_e = eq_before >= quota ? 0u : min(e, quota - eq_before);
     if (w < wid) sel_before += gtw + take_e;
     if (w == wid) eq_take = take_e;
     sel_total += gtw + take_e;
     eq_before += e;
   }
+  const bool overflow = misc[kOverflow] != 0u;
   if (tid == 0) misc[0] = sel_total;
   csync();
   uint32_t offset = 0, total = 0;
@@ -704,40 +872,76 @@ __global__ void __launch_bounds__(kResThreads, 2)  // two CTAs of 512 threads pe
   }
   csync();  // no CTA leaves while a peer may still read its shared memory
   if (c == 0 && tid == 0 && total != (uint32_t)k) report(status, DSA_ERR_BOUNDS);  // consistency check
-  uint32_t pos = offset + sel_before, eq_seen = 0;
-  for (int i = g0 + lane; i - lane < g1; i += 32) {
-    uint32_t gt, eq;
-    classify(i, gt, eq);
-    uint32_t eq_tot;
-    const uint32_t eq_pre = warp_excl_scan(__popc(eq), eq_tot);  // equal keys before this lane's
-    uint32_t take = gt;
-#pragma unroll
-    for (int j = 0; j < 4; ++j)
-      if ((eq >> j) & 1u) {
-        if (eq_seen + eq_pre + __popc(eq & ((1u << j) - 1u)) < eq_take) take |= 1u << j;
+  uint32_t pos = offset + sel_before;
+  if (!overflow) {
+    // 4b. the staged indices out, 32 at a time; threshold-group keys past the
+    //     warp's quota are dropped
+    uint32_t eq_seen = 0;
+    for (uint32_t t0 = 0; t0 < n_sel; t0 += 32) {
+      const uint32_t t = t0 + lane;
+      const uint32_t e = t < n_sel ? stage[t] : 0u;
+      bool take = t < n_sel;
+      if (tie) {
+        const bool is_eq = take && (e >> 31);
+        const uint32_t eq_mask = __ballot_sync(0xffffffffu, is_eq);
+        if (is_eq) take = eq_seen + __popc(eq_mask & lanes_below) < eq_take;
+        eq_seen += __popc(eq_mask);
       }
-    uint32_t t_tot;
-    uint32_t p = pos + warp_excl_scan(__popc(take), t_tot);
-#pragma unroll
-    for (int j = 0; j < 4; ++j)
-      if ((take >> j) & 1u) {
-        if (p < (uint32_t)k) o[p] = start + 4 * i + j;
-        ++p;
-      }
-    pos += t_tot;
-    eq_seen += eq_tot;
+      const uint32_t take_mask = __ballot_sync(0xffffffffu, take);
+      const uint32_t p = pos + __popc(take_mask & lanes_below);
+      if (take && p < (uint32_t)k) o[p] = start + (int)(e & 0x7FFFFFFFu);
+      pos += __popc(take_mask);
+    }
+    return;
   }
+  // 4b'. a warp took more than it can stage (many keys of one warp's run at the
+  //      top, or a large tie): classify the slice again and write as it goes
+  uint32_t eq_seen = 0;
+  for_warp_groups([&](int i, const G& v) {
+    uint32_t gt, eq;
+    classify(i, v, gt, eq);
+    uint32_t take = gt;
+    if (!tie) {
+      take |= eq;
+    } else if (__any_sync(0xffffffffu, eq != 0)) {
+      // the group's keys in token order until the warp's quota
+      uint32_t eq_tot;
+      const uint32_t eq_pre = warp_excl_scan_small(__popc(eq), lanes_below, eq_tot);
+#pragma unroll
+      for (int j = 0; j < 4; ++j)
+        if ((eq >> j) & 1u) {
+          if (eq_seen + eq_pre + __popc(eq & ((1u << j) - 1u)) < eq_take) take |= 1u << j;
+        }
+      eq_seen += eq_tot;
+    }
+    if (__any_sync(0xffffffffu, take != 0)) {
+      uint32_t t_tot;
+      uint32_t p = pos + warp_excl_scan_small(__popc(take), lanes_below, t_tot);
+#pragma unroll
+      for (int j = 0; j < 4; ++j)
+        if ((take >> j) & 1u) {
+          if (p < (uint32_t)k) o[p] = start + 4 * i + j;
+          ++p;
+        }
+      pos += t_tot;
+    }
+  });
 }
 
-template <int C>
-dsa_status_t launch_resident(const float* scores, int64_t ld, const int32_t* row_lens, const int32_t* seq_lens,
-                             int nq, int rows, int cap, int k, int32_t* out, int32_t* status, cudaStream_t st) {
+template <int C, bool kStream>
+dsa_status_t launch_cluster(const float* scores, int64_t ld, const int32_t* row_lens, const int32_t* seq_lens,
+                            int nq, int rows, int cap, int k, int32_t* out, int32_t* status, cudaStream_t st) {
   static bool attr_set[64] = {};
   int dev = 0;
   cudaGetDevice(&dev);
   if (dev < 64 && !attr_set[dev]) {
-    if (cuda_status(cudaFuncSetAttribute(topk_resident_kernel<C>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         (int)res_smem(kResKeys))) != DSA_OK)
+    if (cuda_status(cudaFuncSetAttribute(topk_cluster_kernel<C, kStream>,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         (int)res_smem(kStream ? 0 : kResKeys))) != DSA_OK)
+      return DSA_ERR_CUDA;
+    if (C > kResMaxCluster &&
+        cuda_status(cudaFuncSetAttribute(topk_cluster_kernel<C, kStream>,
+                                         cudaFuncAttributeNonPortableClusterSizeAllowed, 1)) != DSA_OK)
       return DSA_ERR_CUDA;
     attr_set[dev] = true;
   }
@@ -746,7 +950,7 @@ dsa_status_t launch_resident(const float* scores, int64_t ld, const int32_t* row
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3((unsigned)(rows * C));
   cfg.blockDim = dim3(kResThreads);
-  cfg.dynamicSmemBytes = res_smem(slice);
+  cfg.dynamicSmemBytes = res_smem(kStream ? 0 : slice);
   cfg.stream = st;
   cudaLaunchAttribute attr[2];
   attr[0].id = cudaLaunchAttributeClusterDimension;
@@ -757,10 +961,41 @@ dsa_status_t launch_resident(const float* scores, int64_t ld, const int32_t* row
   attr[1].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 2;
-  if (cuda_status(cudaLaunchKernelEx(&cfg, topk_resident_kernel<C>, scores, ld, row_lens, seq_lens, nq, cap, k,
-                                     out, status, slice)) != DSA_OK)
+  count_launches(1);
+  if (cuda_status(cudaLaunchKernelEx(&cfg, topk_cluster_kernel<C, kStream>, scores, ld, row_lens, seq_lens, nq, cap,
+                                     k, out, status, slice)) != DSA_OK)
     return DSA_ERR_CUDA;
   return launch_status();
+}
+
+// Whether clusters of C streaming CTAs can be resident at all on this device
+// (asked once per device; a cluster of 16 needs the non-portable size).
+template <int C>
+bool stream_cluster_ok() {
+  static int known[64] = {};  // 0 unknown, 1 yes, 2 no
+  int dev = 0;
+  cudaGetDevice(&dev);
+  if (dev >= 64) return false;
+  if (known[dev] == 0) {
+    bool ok = cudaFuncSetAttribute(topk_cluster_kernel<C, true>, cudaFuncAttributeNonPortableClusterSizeAllowed,
+                                   C > kResMaxCluster ? 1 : 0) == cudaSuccess;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(C);
+    cfg.blockDim = dim3(kResThreads);
+    cfg.dynamicSmemBytes = res_smem(0);
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = C;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    int n = 0;
+    ok = ok && cudaOccupancyMaxActiveClusters(&n, topk_cluster_kernel<C, true>, &cfg) == cudaSuccess && n > 0;
+    cudaGetLastError();  // a refused query leaves no error behind
+    known[dev] = ok ? 1 : 2;
+  }
+  return known[dev] == 1;
 }
 
 size_t ws_bytes(int rows, int k) {
@@ -777,6 +1012,12 @@ size_t topk_workspace_bytes(int rows, int max_row_len, int k) {
   return ws_bytes(rows, k);
 }
 
+namespace {
+std::atomic<int> g_force_multipass{0};
+}  // namespace
+
+int topk_force_multipass(int on) { return g_force_multipass.exchange(on ? 1 : 0); }
+
 size_t topk_final_smem_bytes() { return (size_t)kWindowBits / 8 + 8 * kCandCap + 4 * kMaxTopk + 4 * kBins + 128; }
 
 dsa_status_t launch_topk(const float* scores, int64_t ld, const int32_t* row_lens, const int32_t* seq_lens, int nq,
@@ -787,21 +1028,31 @@ dsa_status_t launch_topk(const float* scores, int64_t ld, const int32_t* row_len
   // enough slices for two CTAs per SM where a cluster of 8 allows it, and for
   // few rows enough CTAs to spread them over the SMs (at least 8,192 keys per CTA)
   const int c_min = (max_row_len + kResKeys - 1) / kResKeys;
-  const int c_pair = std::min(kResMaxCluster, (max_row_len + kResPairKeys - 1) / kResPairKeys);
+  // two CTAs per SM pay off only while the grid stays within one wave
+  int c_pair = std::min(kResMaxCluster, (max_row_len + kResPairKeys - 1) / kResPairKeys);
+  if ((int64_t)rows * c_pair > 2 * (int64_t)num_sms()) c_pair = 1;
   const int c_fill = std::min(num_sms() / std::max(rows, 1), max_row_len / 8192);
   const int cluster = std::min(kResMaxCluster, std::max(std::max(c_min, c_pair), std::max(c_fill, 1)));
   if (max_row_len > k && c_min <= kResMaxCluster) {
     // row-resident path: one cluster of `cluster` CTAs per row, no workspace
     switch (cluster) {
-      case 1: return launch_resident<1>(scores, ld, row_lens, seq_lens, nq, rows, max_row_len, k, out, status, st);
-      case 2: return launch_resident<2>(scores, ld, row_lens, seq_lens, nq, rows, max_row_len, k, out, status, st);
-      case 3: return launch_resident<3>(scores, ld, row_lens, seq_lens, nq, rows, max_row_len, k, out, status, st);
-      case 4: return launch_resident<4>(scores, ld, row_lens, seq_lens, nq, rows, max_row_len, k, out, status, st);
-      case 5: return launch_resident<5>(scores, ld, row_lens, seq_lens, nq, rows, max_row_len, k, out, status, st);
-      case 6: return launch_resident<6>(scores, ld, row_lens, seq_lens, nq, rows, max_row_len, k, out, status, st);
-      case 7: return launch_resident<7>(scores, ld, row_lens, seq_lens, nq, rows, max_row_len, k, out, status, st);
-      default: return launch_resident<8>(scores, ld, row_lens, seq_lens, nq, rows, max_row_len, k, out, status, st);
+      case 1: return launch_cluster<1, false>(scores, ld, row_lens, seq_lens, nq, rows, max_row_len, k, out, status, st);
+      case 2: return launch_cluster<2, false>(scores, ld, row_lens, seq_lens, nq, rows, max_row_len, k, out, status, st);
+      case 3: return launch_cluster<3, false>(scores, ld, row_lens, seq_lens, nq, rows, max_row_len, k, out, status, st);
+      case 4: return launch_cluster<4, false>(scores, ld, row_lens, seq_lens, nq, rows, max_row_len, k, out, status, st);
+      case 5: return launch_cluster<5, false>(scores, ld, row_lens, seq_lens, nq, rows, max_row_len, k, out, status, st);
+      case 6: return launch_cluster<6, false>(scores, ld, row_lens, seq_lens, nq, rows, max_row_len, k, out, status, st);
+      case 7: return launch_cluster<7, false>(scores, ld, row_lens, seq_lens, nq, rows, max_row_len, k, out, status, st);
+      default: return launch_cluster<8, false>(scores, ld, row_lens, seq_lens, nq, rows, max_row_len, k, out, status, st);
     }
+  }
+  if (max_row_len > k && !g_force_multipass.load(std::memory_order_relaxed)) {
+    // rows too long to hold on chip: the streaming cluster kernel, 16 CTAs per
+    // row where the device schedules such clusters, else 8
+    if (stream_cluster_ok<16>())
+      return launch_cluster<16, true>(scores, ld, row_lens, seq_lens, nq, rows, max_row_len, k, out, status, st);
+    if (stream_cluster_ok<8>())
+      return launch_cluster<8, true>(scores, ld, row_lens, seq_lens, nq, rows, max_row_len, k, out, status, st);
   }
   auto al = [](size_t x) { return (x + 255) & ~size_t(255); };
   uint8_t* w = static_cast<uint8_t*>(workspace);
@@ -820,6 +1071,7 @@ dsa_status_t launch_topk(const float* scores, int64_t ld, const int32_t* row_len
     // histograms and counters start at zero
     const size_t zero_bytes = al((size_t)rows * kBins * 4) + al((size_t)rows * 16);
     if (cuda_status(cudaMemsetAsync(workspace, 0, zero_bytes, st)) != DSA_OK) return DSA_ERR_CUDA;
+    count_launches(3);
     topk_hist_kernel<<<grid, kThreads, 0, st>>>(scores, ld, row_lens, seq_lens, nq, cap, k, ws, status);
     topk_threshold_kernel<<<rows, kThreads, 0, st>>>(row_lens, seq_lens, nq, cap, k, ws);
     topk_collect_kernel<<<grid, kThreads, 0, st>>>(scores, ld, row_lens, seq_lens, nq, cap, k, ws, status);
@@ -834,6 +1086,7 @@ dsa_status_t launch_topk(const float* scores, int64_t ld, const int32_t* row_len
       return DSA_ERR_CUDA;
     attr_set[dev] = true;
   }
+  count_launches(1);
   topk_final_kernel<<<rows, kFinalThreads, smem, st>>>(scores, ld, row_lens, seq_lens, nq, cap, k, ws, out, status);
   return launch_status();
 }

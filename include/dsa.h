@@ -104,6 +104,10 @@ const char* dsa_status_string(int32_t status);
 /* Text of the last CUDA error this thread's calls into the library saw
  * (the reason behind a DSA_ERR_CUDA), or "" if none. */
 const char* dsa_last_cuda_error(void);
+/* Kernels the library has launched in this process so far (all threads and
+ * devices; a memset is not a kernel).  Subtracting two readings around a call
+ * gives the kernels that call launched. */
+uint64_t dsa_kernel_launches(void);
 
 /*
  * Page translation (Day-0 post, packed-cache section: before every step the
@@ -157,6 +161,18 @@ dsa_status_t dsa_topk(const float* scores, int64_t ld_scores, const int32_t* row
                       int32_t rows, int32_t max_row_len, int32_t k, int32_t* idx_out,
                       void* workspace, size_t workspace_bytes,
                       int32_t* dev_status, void* stream);
+
+/*
+ * Which top-k kernels serve rows longer than 327,680 tokens.  By default
+ * (on = 0) such rows take one launch of a thread-block cluster per row (16
+ * CTAs, or 8 where the device cannot schedule 16) and the workspace goes
+ * unused; where neither cluster can be scheduled, four kernels over the
+ * workspace do the selection.  on != 0 selects the four-kernel path for every
+ * later call in this process (all threads and devices), for testing it or for
+ * a device shared with work that clusters would contend with.  Both paths give
+ * the same indices.  Returns the previous setting; never fails.
+ */
+int32_t dsa_topk_force_multipass(int32_t on);
 
 /*
  * dsa_topk without a workspace argument and without any allocation.  (The

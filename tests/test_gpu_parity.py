@@ -124,6 +124,9 @@ def test_topk_ties_specials_and_lengths(k):
         np.zeros(0, dtype=np.float32),                          # empty
         np.full(20000, -2.0, dtype=np.float32),                 # candidate overflow: 20000 ties
         np.concatenate([np.full(12000, 3.0), rng.standard_normal(9000)]).astype(np.float32),
+        # the top 2,500 in one run of the row: more than one warp's share of it
+        np.concatenate([rng.standard_normal(5000), 10 + rng.standard_normal(2500),
+                        rng.standard_normal(5000)]).astype(np.float32),
     ]
     m, lens = _scores_from(rows)
     got = _gpu_topk(torch.from_numpy(m).cuda(), torch.from_numpy(lens).cuda(), k)
@@ -145,7 +148,7 @@ def test_topk_long_rows():
 def test_topk_row_lengths_across_paths(n, ties):
     """Rows held in one CTA, in clusters of 2..8 CTAs (ties on the k-th key
     spread over every CTA of the cluster), and past 8 x 40,960 tokens (the
-    multi-kernel path)."""
+    streaming cluster kernel)."""
     rng = np.random.default_rng(n)
     ld = (n + 3) // 4 * 4
     m = np.zeros((3, ld), dtype=np.float32)
@@ -156,6 +159,48 @@ def test_topk_row_lengths_across_paths(n, ties):
     lens = np.array([n, n, n - 5], dtype=np.int32)
     got = _gpu_topk(torch.from_numpy(m).cuda(), torch.from_numpy(lens).cuda(), 2048)
     np.testing.assert_array_equal(got, oracle.topk(m.astype(np.float64), lens, 2048))
+
+
+@pytest.mark.parametrize("multipass", [False, True])
+@pytest.mark.parametrize("n", [327_681, 1_000_000, 2_000_003])
+def test_topk_long_rows_on_both_paths(n, multipass):
+    """Rows past 8 x 40,960 tokens: the streaming cluster kernel (one launch)
+    and the four-kernel path (forced), bit-exact against the oracle, with rows
+    of mixed lengths in one call (one shorter than k, one far shorter than
+    the longest) and heavy ties on the k-th key."""
+    rng = np.random.default_rng(n + multipass)
+    ld = (n + 3) // 4 * 4
+    m = np.zeros((6, ld), dtype=np.float32)
+    m[0, :n] = rng.integers(0, 50, n)                 # ties on the k-th key
+    m[1, :n] = 7.0                                  # all equal: the lowest k indices
+    m[2, :n] = rng.standard_normal(n)
+    m[2, n // 3] = np.inf
+    m[2, n - 9] = -np.inf
+    m[3, :] = rng.standard_normal(ld)
+    m[4, :] = rng.standard_normal(ld)
+    m[5, :n] = -rng.exponential(1.0, n)             # all negative, top at the row's end
+    m[5, n - 2048:n] = 1.0 + rng.random(2048)
+    lens = np.array([n, n, n - 5, 1000, 50_001, n - 3], dtype=np.int32)
+    prev = binding.topk_force_multipass(multipass)
+    try:
+        n0 = binding.kernel_launches()
+        got = _gpu_topk(torch.from_numpy(m).cuda(), torch.from_numpy(lens).cuda(), 2048, max_row_len=n)
+        launches = binding.kernel_launches() - n0
+    finally:
+        binding.topk_force_multipass(prev)
+    assert launches == (4 if multipass else 1)
+    np.testing.assert_array_equal(got, oracle.topk(m.astype(np.float64), lens, 2048))
+
+
+def test_decode_step_launches_four_kernels():
+    """A fused decode step is four launches (indexer, top-k, sparse MLA, chunk
+    combine) for rows that fit the on-chip top-k and for rows that take the
+    streaming cluster top-k."""
+    for lens in ([9000, 130], [400_000]):
+        case = synth.make_case("cnt", seq_lens=lens, nq=1, seed=3)
+        n0 = binding.kernel_launches()
+        _run_step(case)
+        assert binding.kernel_launches() - n0 == 4
 
 
 def _gpu_mla(case, dc, idx_np):
