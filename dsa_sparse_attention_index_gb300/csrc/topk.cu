@@ -8,13 +8,17 @@
 // padding when a row has fewer than k tokens.  Scores are compared as
 // order-preserving 32-bit keys (integer radix).
 //
-// Rows up to 8 x 40,960 tokens: one kernel, a thread-block cluster per row
-// (topk_cluster_kernel).  Each CTA of the cluster keeps its slice of the
-// row as keys in shared memory, read once from L2; up to three digit passes
-// (11, 11 and 10 bits) find the k-th key, each pass merging the CTAs'
-// histograms through distributed shared memory; ties on the k-th key go to
-// the lowest indices in CTA-rank and token order; a cluster-wide scan then
-// writes the chosen indices in ascending order.  No workspace is used.
+// Rows up to 8 x 30,720 tokens: one kernel, a thread-block cluster per row
+// (topk_cluster_kernel).  Each CTA of the cluster keeps its slice of the row
+// as keys in shared memory (bulk copies from L2).  The first digit (11 bits)
+// is picked from the CTAs' histograms, merged through distributed shared
+// memory.  One more pass over the keys then marks, per lane run, the keys
+// above that digit's bin (taken whatever follows) and moves the keys in the
+// bin to the front of the run; the second and third digits (11 and 10 bits)
+// and the output use only those candidates.  Ties on the k-th key go to the
+// lowest indices in CTA-rank and token order; each lane writes its run's
+// chosen indices in ascending order at a place from warp and cluster scans.
+// No workspace is used.
 //
 // Longer rows (the 1M-token rows) take the same kernel in its streaming form:
 // a cluster of 16 CTAs per row (8 where the device cannot schedule 16) that
@@ -493,19 +497,24 @@ __global__ void __launch_bounds__(kFinalThreads) topk_final_kernel(const float* 
 // ---------------------------------------------------------------- row-resident path
 namespace cg = cooperative_groups;
 
-constexpr int kResKeys = 40960;     // most keys a CTA holds in shared memory (160 KB)
+constexpr int kResKeys = 30720;     // most keys a CTA holds in shared memory (120 KB): a lane's
+                                    // run of a 16-warp CTA is then at most 15 groups of 4 (60 bits)
+static_assert((kResKeys / 4 + 15) / 16 <= 15 * 32, "lane runs must fit a 64-bit mask");
 constexpr int kResPairKeys = 20480; // keys per CTA that still let two CTAs share an SM
 constexpr int kResThreads = kFinalThreads;
 constexpr int kResWarps = kResThreads / 32;
-constexpr int kResMaxCluster = 8;   // portable cluster size: rows up to 327,680 tokens
+constexpr int kResMaxCluster = 8;   // portable cluster size: rows up to 245,760 tokens
 // digits of the 32-bit key: bits 31..21, 20..10, 9..0
 constexpr int kD1 = 11, kD2 = 11, kD3 = 10;
 constexpr int kB1 = 1 << kD1, kB2 = 1 << kD2, kB3 = 1 << kD3;
-// shared memory: keys[slice] | h1[kB1] | h2[kB2] | h3[kB3] | g[kB1] | scan[32] | misc[32]
-constexpr size_t kResFixed = 4 * ((size_t)kB1 + kB2 + kB3 + kB1 + 64);
-constexpr int kRangeTotal = 24;  // misc slot: the total of this CTA's bin range in a merge
+// shared memory (32-bit words): keys[slice] | h1[kB1] | h2[kB2] | h3[kB3] |
+// stage[kB1] | coarse[3][64] | scan[32] | misc[32] | 4 mbarriers
+constexpr int kCoarse = 64;      // super-bins of 32 bins per digit level
+constexpr int kLoadChunks = 4;   // bulk copies of a resident slice, each with its own mbarrier
+constexpr size_t kResFixed = 4 * ((size_t)kB1 + kB2 + kB3 + kB1 + 3 * kCoarse + 32 + 32 + 2 * kLoadChunks);
 constexpr int kOverflow = 25;    // misc slot: a warp took more indices than it can stage
-constexpr int kStageCap = (kB1 + kB2) / kResWarps;  // indices a warp stages in h1/h2 (256)
+constexpr int kPick = 26;        // misc slots 26..28: the merge's digit, need and pop
+constexpr int kStageCap = kB1 / kResWarps;  // indices a warp stages (128)
 size_t res_smem(int slice) { return 4 * (size_t)slice + kResFixed; }
 
 // Warp-wide exclusive prefix sum of one value 0..7 per lane, from three
@@ -591,12 +600,27 @@ __device__ __forceinline__ uint32_t elem_key(const float4& v, int j) {
   return score_key(j == 0 ? v.x : j == 1 ? v.y : j == 2 ? v.z : v.w);
 }
 
+
+// Warp-wide exclusive prefix sum of one value per lane; `total` gets the sum.
+__device__ __forceinline__ uint32_t warp_excl_scan(uint32_t v, uint32_t& total) {
+  const int lane = threadIdx.x & 31;
+  uint32_t x = v;
+#pragma unroll
+  for (int d = 1; d < 32; d <<= 1) {
+    const uint32_t u = __shfl_up_sync(0xffffffffu, x, d);
+    if (lane >= d) x += u;
+  }
+  total = __shfl_sync(0xffffffffu, x, 31);
+  return x - v;
+}
+
 // kStream = false: each CTA keeps its slice of the row as keys in shared
 // memory.  kStream = true (rows too long for that): every pass reads the
 // slice's scores again from global memory (L2), and shared memory holds only
-// the histograms.
+// the histograms.  Resident: two CTAs of 512 threads per SM (at most 64
+// registers); streaming: one.
 template <int C, bool kStream>
-__global__ void __launch_bounds__(kResThreads, 2)  // two CTAs of 512 threads per SM: at most 64 registers
+__global__ void __launch_bounds__(kResThreads, kStream ? 1 : 2)
     topk_cluster_kernel(const float* __restrict__ scores, int64_t ld, const int32_t* row_lens,
                         const int32_t* seq_lens, int nq, int cap, int k, int32_t* out, int32_t* status,
                         int slice_cap) {
@@ -613,9 +637,11 @@ __global__ void __launch_bounds__(kResThreads, 2)  // two CTAs of 512 threads pe
   uint32_t* h1 = reinterpret_cast<uint32_t*>(smem_raw) + (kStream ? 0 : slice_cap);  // slice_cap: a multiple of 4
   uint32_t* h2 = h1 + kB1;
   uint32_t* h3 = h2 + kB2;
-  uint32_t* g = h3 + kB3;  // the cluster's histogram of the current digit (the ranges this CTA reads)
-  uint32_t* scan = g + kB1;
+  uint32_t* stage = h3 + kB3;  // the warps' taken indices, kStageCap each
+  uint32_t* coarse = stage + kB1;  // per digit level: sums of 32 consecutive bins
+  uint32_t* scan = coarse + 3 * kCoarse;
   uint32_t* misc = scan + 32;
+  const uint32_t load_bars = smem_u32(misc + 32);  // kLoadChunks mbarriers, 8 bytes each
 
   const int len = row_len(row_lens, seq_lens, nq, r, cap, c == 0 ? status : nullptr);
   int32_t* o = out + (int64_t)r * k;
@@ -647,90 +673,143 @@ __global__ void __launch_bounds__(kResThreads, 2)  // two CTAs of 512 threads pe
   };
   // the valid elements of group i (padding past the slice's end excluded)
   auto valid_bits = [&](int i) -> uint32_t { return 4 * i + 4 > n ? (1u << (n - 4 * i)) - 1u : 0xFu; };
+  // the first digit's histogram entries of group i's keys
+  auto count_first = [&](int i, const uint4& kk) {
+    const bool pad = 4 * i + 3 >= n;  // padding keys are not counted
+    atomicAdd(&h1[kk.x >> (32 - kD1)], 1u);
+    if (!pad || 4 * i + 1 < n) atomicAdd(&h1[kk.y >> (32 - kD1)], 1u);
+    if (!pad || 4 * i + 2 < n) atomicAdd(&h1[kk.z >> (32 - kD1)], 1u);
+    if (!pad) atomicAdd(&h1[kk.w >> (32 - kD1)], 1u);
+  };
+  auto to_keys = [](const float4& v) {
+    return make_uint4(score_key(v.x), score_key(v.y), score_key(v.z), score_key(v.w));
+  };
 
-  // ---- 1. the slice into shared memory as keys, histogram of the first digit (bits 31..21)
+  // ---- 1. histogram of the first digit (bits 31..21); resident: the slice
+  //         into shared memory as keys
   for (int i = tid; i < (kB1 + kB2 + kB3) / 4; i += kResThreads) reinterpret_cast<uint4*>(h1)[i] = make_uint4(0, 0, 0, 0);
-  if (tid == 0) misc[kOverflow] = 0u;
-  __syncthreads();
-  for (int i0 = 0; i0 < n4; i0 += 8 * kResThreads) {
-    float4 v[8];  // eight 16-byte loads in flight per thread
-#pragma unroll
-    for (int u = 0; u < 8; ++u) {
-      const int i = i0 + u * kResThreads + tid;
-      if (i < n4) v[u] = score_group(i);
+  if (tid == 0) {
+    misc[kOverflow] = 0u;
+    if (!kStream) {
+      for (int q = 0; q < kLoadChunks; ++q) mbar_init(load_bars + 8 * q, 1);
+      fence_mbar_init();
     }
+  }
+  __syncthreads();
+  if constexpr (!kStream) {
+    // the slice's whole groups by bulk copies in kLoadChunks pieces, converted to
+    // keys in place as each lands; the ragged last group by plain loads
+    const int per = (full4 + kLoadChunks - 1) / kLoadChunks;
+    if (tid == 0) {
 #pragma unroll
-    for (int u = 0; u < 8; ++u) {
-      const int i = i0 + u * kResThreads + tid;
-      if (i < n4) {
-        const uint4 kk = make_uint4(score_key(v[u].x), score_key(v[u].y), score_key(v[u].z), score_key(v[u].w));
-        if (!kStream) keys4[i] = kk;
-        const bool pad = 4 * i + 3 >= n;  // padding keys are not counted
-        atomicAdd(&h1[kk.x >> (32 - kD1)], 1u);
-        if (!pad || 4 * i + 1 < n) atomicAdd(&h1[kk.y >> (32 - kD1)], 1u);
-        if (!pad || 4 * i + 2 < n) atomicAdd(&h1[kk.z >> (32 - kD1)], 1u);
-        if (!pad) atomicAdd(&h1[kk.w >> (32 - kD1)], 1u);
+      for (int q = 0; q < kLoadChunks; ++q) {
+        const int a = min(full4, q * per), b = min(full4, a + per);
+        mbar_arrive_expect_tx(load_bars + 8 * q, (uint32_t)(b - a) * 16u);
+        if (b > a) bulk_load(smem_u32(keys4 + a), row4 + a, (uint32_t)(b - a) * 16u, load_bars + 8 * q);
+      }
+    }
+    if (full4 < n4 && tid == kResThreads - 1) {
+      const uint4 kk = to_keys(score_group(full4));
+      keys4[full4] = kk;
+      count_first(full4, kk);
+    }
+#pragma unroll 1
+    for (int q = 0; q < kLoadChunks; ++q) {
+      const int a = min(full4, q * per), b = min(full4, a + per);
+      if (!mbar_wait_drain(load_bars + 8 * q, 0, 1000000000ull)) report(status, DSA_ERR_TIMEOUT);
+      for (int i = a + tid; i < b; i += kResThreads) {
+        const uint4 raw = keys4[i];
+        const uint4 kk = to_keys(make_float4(__uint_as_float(raw.x), __uint_as_float(raw.y),
+                                             __uint_as_float(raw.z), __uint_as_float(raw.w)));
+        keys4[i] = kk;
+        count_first(i, kk);
+      }
+    }
+  } else {
+    for (int i0 = 0; i0 < n4; i0 += 8 * kResThreads) {
+      float4 v[8];  // eight 16-byte loads in flight per thread
+#pragma unroll
+      for (int u = 0; u < 8; ++u) {
+        const int i = i0 + u * kResThreads + tid;
+        if (i < n4) v[u] = score_group(i);
+      }
+#pragma unroll
+      for (int u = 0; u < 8; ++u) {
+        const int i = i0 + u * kResThreads + tid;
+        if (i < n4) count_first(i, to_keys(v[u]));
       }
     }
   }
   // The cluster-wide choice of a digit from the CTAs' histograms `local`
-  // (nbins bins each).  CTA q sums bin range q of every CTA's copy (distributed
-  // shared memory) into its own g and publishes the range's total; every CTA
-  // then finds, from the C totals, the range holding the need-th largest key,
-  // copies that range's sums and picks the digit within it.  Each CTA loads
-  // about 2 * nbins peer values, whatever the cluster size.
-  auto merge_pick = [&](uint32_t* local, int nbins, uint32_t& need, int& digit, uint32_t& pop) {
-    if constexpr (C == 1) {
-      __syncthreads();
-      pick_digit(local, nbins, scan, need, digit, pop);
-    } else {
-      const int per = (nbins + C - 1) / C;
-      csync();  // every CTA's histogram is complete
-      {
-        const int lo = min(nbins, c * per), hi = min(nbins, lo + per);
-        uint32_t part = 0;
-        for (int b = lo + tid; b < hi; b += kResThreads) {
-          uint32_t sum = 0;
-#pragma unroll
-          for (int q = 0; q < C; ++q) sum += cluster.map_shared_rank(local, q)[b];
-          g[b] = sum;
-          part += sum;
-        }
-        part = __reduce_add_sync(0xffffffffu, part);
-        if (lane == 0) scan[wid] = part;
-        __syncthreads();
-        if (tid == 0) {
-          uint32_t t = 0;
-          for (int w = 0; w < kResWarps; ++w) t += scan[w];
-          misc[kRangeTotal] = t;
-        }
-      }
-      csync();  // every range is summed
-      if (tid < C) scan[tid] = cluster.map_shared_rank(misc, tid)[kRangeTotal];
-      __syncthreads();
-      int owner = 0;
-      uint32_t above = 0;
-      for (int q = C - 1; q >= 0; --q) {  // high bins first
-        if (above + scan[q] >= need) {
-          owner = q;
-          break;
-        }
-        above += scan[q];
-      }
-      const int lo = min(nbins, owner * per), hi = min(nbins, lo + per);
-      if (owner != c) {
-        const uint32_t* src = cluster.map_shared_rank(g, owner);
-        for (int b = lo + tid; b < hi; b += kResThreads) g[b] = src[b];
-      }
-      __syncthreads();
-      need -= above;
-      pick_digit(g + lo, hi - lo, scan, need, digit, pop);
-      digit += lo;
+  // (nbins = 32 * nc bins each, nc <= 64) with one cluster barrier: each CTA
+  // sums its histogram in nc super-bins of 32 bins (`cs`), then warp 0 adds up
+  // every CTA's super-bins (distributed shared memory), finds the one holding
+  // the need-th largest key counting from the top, adds up the 32 bins of that
+  // super-bin over the CTAs and picks the bin.  The peers' arrays are only read
+  // after the barrier and never written again in this launch.
+  auto merge_pick = [&](const uint32_t* local, int nc, uint32_t* cs, uint32_t& need, int& digit, uint32_t& pop) {
+    __syncthreads();  // this CTA's histogram is complete
+    for (int sb = wid; sb < nc; sb += kResWarps) {
+      const uint32_t v = __reduce_add_sync(0xffffffffu, local[sb * 32 + lane]);
+      if (lane == 0) cs[sb] = v;
     }
+    csync();  // every CTA's histogram and super-bins are complete
+    if (wid == 0) {
+      // lane l: super-bins l (lo) and 32 + l (hi)
+      uint32_t lo = 0, hi = 0;
+#pragma unroll
+      for (int q = 0; q < C; ++q) {
+        const uint32_t* pc = C == 1 ? cs : cluster.map_shared_rank(cs, q);
+        lo += pc[lane];
+        if (nc > 32) hi += pc[32 + lane];
+      }
+      // inclusive sums from the top: super-bins above and including each
+      uint32_t shi = hi, slo = lo;
+#pragma unroll
+      for (int d = 1; d < 32; d <<= 1) {
+        const uint32_t a = __shfl_down_sync(0xffffffffu, shi, d), b = __shfl_down_sync(0xffffffffu, slo, d);
+        if (lane + d < 32) {
+          shi += a;
+          slo += b;
+        }
+      }
+      const uint32_t tot_hi = __shfl_sync(0xffffffffu, shi, 0);
+      slo += tot_hi;
+      // the super-bin where the running count from the top first reaches need
+      const bool in_hi = shi - hi < need && need <= shi;
+      const bool in_lo = slo - lo < need && need <= slo;
+      const uint32_t m_hi = __ballot_sync(0xffffffffu, in_hi), m_lo = __ballot_sync(0xffffffffu, in_lo);
+      // exactly one lane qualifies (the clamp only keeps indices in range if the
+      // counts were inconsistent)
+      const int sb = max(0, m_hi ? 32 + __ffs(m_hi) - 1 : __ffs(m_lo) - 1);
+      const uint32_t above = __shfl_sync(0xffffffffu, m_hi ? shi - hi : slo - lo, (sb & 31));
+      // the 32 bins of super-bin sb over the cluster
+      uint32_t f = 0;
+#pragma unroll
+      for (int q = 0; q < C; ++q) f += (C == 1 ? local : cluster.map_shared_rank(local, q))[sb * 32 + lane];
+      uint32_t sf = f;
+#pragma unroll
+      for (int d = 1; d < 32; d <<= 1) {
+        const uint32_t a = __shfl_down_sync(0xffffffffu, sf, d);
+        if (lane + d < 32) sf += a;
+      }
+      const uint32_t want = need - above;
+      const uint32_t mb = __ballot_sync(0xffffffffu, sf - f < want && want <= sf);
+      const int l = max(0, __ffs(mb) - 1);
+      if (lane == l) {
+        misc[kPick] = (uint32_t)(sb * 32 + l);
+        misc[kPick + 1] = want - (sf - f);
+        misc[kPick + 2] = f;
+      }
+    }
+    __syncthreads();
+    digit = (int)misc[kPick];
+    need = misc[kPick + 1];
+    pop = misc[kPick + 2];
   };
   uint32_t need = (uint32_t)k, pop;
   int digit;
-  merge_pick(h1, kB1, need, digit, pop);
+  merge_pick(h1, kB1 / 32, coarse, need, digit, pop);
   // Keys whose bits above `shift` exceed `prefix` are taken; keys equal to it on
   // those bits form the threshold group, taken whole unless `tie` (only on the
   // full 32 bits), where the first `quota` of them in token order are taken.
@@ -738,8 +817,148 @@ __global__ void __launch_bounds__(kResThreads, 2)  // two CTAs of 512 threads pe
   int shift = 32 - kD1;
   bool tie = false;
   uint32_t quota = 0;
-  // U groups loaded ahead per thread (more when they come from L2)
-  constexpr int U = kStream ? (C > 8 ? 8 : 6) : 4;
+  auto tie_quota = [&]() {  // equal keys: `need` of them, lowest indices first (lower CTA ranks hold lower indices)
+    tie = true;
+    uint32_t before = 0;
+#pragma unroll
+    for (int q = 0; q < C; ++q)
+      if (q < c) before += cluster.map_shared_rank(h3, q)[digit];
+    const uint32_t mine = h3[digit];
+    quota = need > before ? min(need - before, mine) : 0u;
+  };
+  // Warp w owns the contiguous run of groups [g0, g1) of the slice.
+  const int wg = (n4 + kResWarps - 1) / kResWarps;
+  const int g0 = min(n4, wid * wg), g1 = min(n4, g0 + wg);
+  const uint32_t lanes_below = (1u << lane) - 1u;
+  // The warp's place in the row's output from its counts: `n_sel` taken or in
+  // the threshold group, `n_eq` of those in the group when it is tied.  Returns
+  // the first output position and the warp's share of the group quota.
+  auto place = [&](uint32_t n_sel, uint32_t n_eq, bool stage_overflow, uint32_t& eq_take, bool& overflow) {
+    if (lane == 0) {
+      scan[wid] = tie ? n_eq : 0u;                 // threshold-group keys that need a quota
+      misc[1 + wid] = tie ? n_sel - n_eq : n_sel;  // taken outright
+      if (stage_overflow) misc[kOverflow] = 1u;
+    }
+    __syncthreads();
+    uint32_t eq_before = 0, sel_before = 0, sel_total = 0;
+    eq_take = 0;
+    for (int w = 0; w < kResWarps; ++w) {
+      const uint32_t e = scan[w], gtw = misc[1 + w];
+      const uint32_t take_e = eq_before >= quota ? 0u : min(e, quota - eq_before);
+      if (w < wid) sel_before += gtw + take_e;
+      if (w == wid) eq_take = take_e;
+      sel_total += gtw + take_e;
+      eq_before += e;
+    }
+    overflow = misc[kOverflow] != 0u;
+    if (tid == 0) misc[0] = sel_total;
+    csync();
+    uint32_t offset = 0, total = 0;
+#pragma unroll
+    for (int q = 0; q < C; ++q) {
+      const uint32_t x = C == 1 ? misc[0] : cluster.map_shared_rank(misc, q)[0];
+      offset += q < c ? x : 0u;
+      total += x;
+    }
+    csync();  // no CTA leaves while a peer may still read its shared memory
+    if (c == 0 && tid == 0 && total != (uint32_t)k) report(status, DSA_ERR_BOUNDS);  // consistency check
+    return offset + sel_before;
+  };
+
+  if constexpr (!kStream) {
+    // Lane l owns the contiguous groups [q0, q1) of its warp's run: an odd
+    // number, at most 15 (slices of at most kResKeys keys), so a warp's
+    // 16-byte loads fall in distinct banks and the run fits a 64-bit mask.
+    const int wl = ((g1 - g0 + 31) / 32) | 1;
+    const int q0 = min(g1, g0 + lane * wl), q1 = min(g1, q0 + wl);
+    uint32_t* run = reinterpret_cast<uint32_t*>(keys4) + 4 * q0;  // the run's keys, then its candidates
+    // ---- 2. one pass over the run: keys above the first digit's bin are taken
+    //         whatever follows (bit set in `above`); keys in the bin are the
+    //         candidates (bit set in `cand`), moved to the front of the run in
+    //         token order and counted for the second digit
+    const bool count2 = need != pop;
+    uint64_t above = 0, cand = 0;
+    int nc = 0;
+    for (int i = q0; i < q1; ++i) {
+      const uint4 kk = keys4[i];
+      const uint32_t valid = valid_bits(i);
+      const uint32_t a[4] = {kk.x, kk.y, kk.z, kk.w};
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        const uint32_t bin = a[j] >> (32 - kD1);
+        const int b = 4 * (i - q0) + j;
+        if (((valid >> j) & 1u) && bin >= prefix) {
+          if (bin > prefix) {
+            above |= 1ull << b;
+          } else {
+            cand |= 1ull << b;
+            run[nc++] = a[j];  // never past the key just read
+            if (count2) atomicAdd(&h2[(a[j] >> kD3) & (kB2 - 1)], 1u);
+          }
+        }
+      }
+    }
+    if (count2) {
+      merge_pick(h2, kB2 / 32, coarse + kCoarse, need, digit, pop);
+      prefix = (prefix << kD2) | (uint32_t)digit;
+      shift = kD3;
+      if (need != pop) {
+        // ---- 3. last digit (bits 9..0), over the candidates only
+        for (int t = 0; t < nc; ++t) {
+          const uint32_t key = run[t];
+          if ((key >> kD3) == prefix) atomicAdd(&h3[key & (kB3 - 1)], 1u);
+        }
+        merge_pick(h3, kB3 / 32, coarse + 2 * kCoarse, need, digit, pop);
+        prefix = (prefix << kD3) | (uint32_t)digit;
+        shift = 0;
+        if (need != pop) tie_quota();
+      }
+    }
+    // ---- 4. emit in ascending token order
+    const KeyRange fin = key_range(prefix, shift);  // the threshold group
+    const uint32_t fin_hi = fin.klo + fin.span;
+    uint32_t c_gt = (uint32_t)__popcll(above), c_eq = 0;
+    for (int t = 0; t < nc; ++t) {
+      const uint32_t key = run[t];
+      c_gt += key > fin_hi;
+      c_eq += key - fin.klo <= fin.span;
+    }
+    const uint32_t n_eq = __reduce_add_sync(0xffffffffu, c_eq);
+    const uint32_t n_sel = __reduce_add_sync(0xffffffffu, c_gt) + n_eq;
+    uint32_t eq_take;
+    bool overflow;
+    const uint32_t pos = place(n_sel, n_eq, false, eq_take, overflow);
+    // this lane's place in the warp: the lanes below took their keys above the
+    // group and, up to the warp's quota, their keys in it
+    uint32_t eq_tot, taken_tot;
+    const uint32_t eq_before_lane = warp_excl_scan(c_eq, eq_tot);
+    const uint32_t eq_mine = !tie ? c_eq : (eq_before_lane >= eq_take ? 0u : min(c_eq, eq_take - eq_before_lane));
+    uint32_t p = pos + warp_excl_scan(c_gt + eq_mine, taken_tot);
+    uint32_t eq_left = eq_mine;
+    int t = 0;
+    for (uint64_t m = above | cand; m; m &= m - 1) {
+      const int b = __ffsll((long long)m) - 1;
+      bool take = (above >> b) & 1ull;
+      if (!take) {  // the t-th candidate
+        const uint32_t key = run[t++];
+        if (key > fin_hi) {
+          take = true;
+        } else if (key - fin.klo <= fin.span && eq_left) {
+          take = true;
+          --eq_left;
+        }
+      }
+      if (take) {
+        if (p < (uint32_t)k) o[p] = start + 4 * q0 + b;
+        ++p;
+      }
+    }
+    return;
+  }
+
+  // ---------------------------------------------------------------- streaming
+  // U groups loaded ahead per thread
+  constexpr int U = 8;
   auto for_my_groups = [&](auto&& body) {  // body(i, group) for groups i = tid + j * kResThreads
     for (int i0 = tid; i0 < n4; i0 += U * kResThreads) {
       G v[U];
@@ -764,7 +983,7 @@ __global__ void __launch_bounds__(kResThreads, 2)  // two CTAs of 512 threads pe
           if ((m >> j) & 1u) atomicAdd(&h2[(elem_key(v, j) >> kD3) & (kB2 - 1)], 1u);
       }
     });
-    merge_pick(h2, kB2, need, digit, pop);
+    merge_pick(h2, kB2 / 32, coarse + kCoarse, need, digit, pop);
     prefix = (prefix << kD2) | (uint32_t)digit;
     shift = kD3;
     if (need != pop) {
@@ -778,30 +997,17 @@ __global__ void __launch_bounds__(kResThreads, 2)  // two CTAs of 512 threads pe
             if ((m >> j) & 1u) atomicAdd(&h3[elem_key(v, j) & (kB3 - 1)], 1u);
         }
       });
-      merge_pick(h3, kB3, need, digit, pop);
+      merge_pick(h3, kB3 / 32, coarse + 2 * kCoarse, need, digit, pop);
       prefix = (prefix << kD3) | (uint32_t)digit;
       shift = 0;
-      if (need != pop) {
-        // equal keys: `need` of them, lowest indices first; lower CTA ranks hold lower indices
-        tie = true;
-        uint32_t before = 0;
-#pragma unroll
-        for (int q = 0; q < C; ++q)
-          if (q < c) before += cluster.map_shared_rank(h3, q)[digit];
-        const uint32_t mine = h3[digit];
-        quota = need > before ? min(need - before, mine) : 0u;
-      }
+      if (need != pop) tie_quota();
     }
   }
   const KeyRange fin = key_range(prefix, shift);  // the threshold group
 
-  // ---- 4. emit in ascending token order.  Warp w owns a contiguous run of
-  //         groups; each step covers 128 elements (4 per lane, in lane order).
-  const int wg = (n4 + kResWarps - 1) / kResWarps;  // groups per warp
-  const int g0 = min(n4, wid * wg), g1 = min(n4, g0 + wg);
-  // the warp's groups in order, 32 per step (one per lane), U steps loaded ahead;
-  // body(i, group) runs for every lane while the step's first group is in range
-  auto for_warp_groups = [&](auto&& body) {
+  // ---- 4. emit in ascending token order, 128 scores per warp step (a 16-byte
+  //         group per lane)
+  auto for_warp_groups = [&](auto&& body) {  // body(i, group) for i = g0 + 32 s + lane while g0 + 32 s < g1
     for (int b0 = g0; b0 < g1; b0 += 32 * U) {
       G v[U];
 #pragma unroll
@@ -822,12 +1028,10 @@ __global__ void __launch_bounds__(kResThreads, 2)  // two CTAs of 512 threads pe
       eq = bits_in(v, fin) & valid;
     }
   };
-  const uint32_t lanes_below = (1u << lane) - 1u;
-  // 4a. one pass: each warp counts what it takes and stages the slice-local
-  //     indices in token order (bit 31: a key of the threshold group) in its
-  //     share of h1/h2, free once the last merge is done
-  uint32_t* stage = h1 + wid * kStageCap;
-  uint32_t n_sel = 0, n_eq = 0;  // the warp's candidates and threshold-group keys among them
+  // 4a. one pass: the warp counts what it takes and stages the slice-local
+  //     indices in token order (bit 31: a key of the threshold group)
+  uint32_t* my_stage = stage + wid * kStageCap;
+  uint32_t n_sel = 0, n_eq = 0;
   for_warp_groups([&](int i, const G& v) {
     uint32_t gt, eq;
     classify(i, v, gt, eq);
@@ -838,48 +1042,23 @@ __global__ void __launch_bounds__(kResThreads, 2)  // two CTAs of 512 threads pe
 #pragma unroll
       for (int j = 0; j < 4; ++j)
         if ((sel >> j) & 1u) {
-          if (p < (uint32_t)kStageCap) stage[p] = (uint32_t)(4 * i + j) | (((eq >> j) & 1u) << 31);
+          if (p < (uint32_t)kStageCap) my_stage[p] = (uint32_t)(4 * i + j) | (((eq >> j) & 1u) << 31);
           ++p;
         }
       n_sel += tot;
       if (tie) n_eq += __reduce_add_sync(0xffffffffu, __popc(eq));
     }
   });
-  if (lane == 0) {
-    scan[wid] = tie ? n_eq : 0u;             // threshold-group keys that need a quota
-    misc[1 + wid] = tie ? n_sel - n_eq : n_sel;  // taken outright
-    if (n_sel > (uint32_t)kStageCap) misc[kOverflow] = 1u;
-  }
-  __syncthreads();
-  uint32_t eq_before = 0, sel_before = 0, sel_total = 0, eq_take = 0;
-  for (int w = 0; w < kResWarps; ++w) {
-    const uint32_t e = scan[w], gtw = misc[1 + w];
-    const uint32_t take_e = eq_before >= quota ? 0u : min(e, quota - eq_before);
-    if (w < wid) sel_before += gtw + take_e;
-    if (w == wid) eq_take = take_e;
-    sel_total += gtw + take_e;
-    eq_before += e;
-  }
-  const bool overflow = misc[kOverflow] != 0u;
-  if (tid == 0) misc[0] = sel_total;
-  csync();
-  uint32_t offset = 0, total = 0;
-#pragma unroll
-  for (int q = 0; q < C; ++q) {
-    const uint32_t x = C == 1 ? misc[0] : cluster.map_shared_rank(misc, q)[0];
-    offset += q < c ? x : 0u;
-    total += x;
-  }
-  csync();  // no CTA leaves while a peer may still read its shared memory
-  if (c == 0 && tid == 0 && total != (uint32_t)k) report(status, DSA_ERR_BOUNDS);  // consistency check
-  uint32_t pos = offset + sel_before;
+  uint32_t eq_take;
+  bool overflow;
+  uint32_t pos = place(n_sel, n_eq, n_sel > (uint32_t)kStageCap, eq_take, overflow);
   if (!overflow) {
     // 4b. the staged indices out, 32 at a time; threshold-group keys past the
     //     warp's quota are dropped
     uint32_t eq_seen = 0;
     for (uint32_t t0 = 0; t0 < n_sel; t0 += 32) {
       const uint32_t t = t0 + lane;
-      const uint32_t e = t < n_sel ? stage[t] : 0u;
+      const uint32_t e = t < n_sel ? my_stage[t] : 0u;
       bool take = t < n_sel;
       if (tie) {
         const bool is_eq = take && (e >> 31);
@@ -895,37 +1074,39 @@ __global__ void __launch_bounds__(kResThreads, 2)  // two CTAs of 512 threads pe
     return;
   }
   // 4b'. a warp took more than it can stage (many keys of one warp's run at the
-  //      top, or a large tie): classify the slice again and write as it goes
+  //      top, or a large tie): classify the run again and write as it goes
   uint32_t eq_seen = 0;
-  for_warp_groups([&](int i, const G& v) {
-    uint32_t gt, eq;
-    classify(i, v, gt, eq);
-    uint32_t take = gt;
-    if (!tie) {
-      take |= eq;
-    } else if (__any_sync(0xffffffffu, eq != 0)) {
-      // the group's keys in token order until the warp's quota
-      uint32_t eq_tot;
-      const uint32_t eq_pre = warp_excl_scan_small(__popc(eq), lanes_below, eq_tot);
+  {
+    for_warp_groups([&](int i, const G& v) {
+      uint32_t gt, eq;
+      classify(i, v, gt, eq);
+      uint32_t take = gt;
+      if (!tie) {
+        take |= eq;
+      } else if (__any_sync(0xffffffffu, eq != 0)) {
+        // the group's keys in token order until the warp's quota
+        uint32_t eq_tot;
+        const uint32_t eq_pre = warp_excl_scan_small(__popc(eq), lanes_below, eq_tot);
 #pragma unroll
-      for (int j = 0; j < 4; ++j)
-        if ((eq >> j) & 1u) {
-          if (eq_seen + eq_pre + __popc(eq & ((1u << j) - 1u)) < eq_take) take |= 1u << j;
-        }
-      eq_seen += eq_tot;
-    }
-    if (__any_sync(0xffffffffu, take != 0)) {
-      uint32_t t_tot;
-      uint32_t p = pos + warp_excl_scan_small(__popc(take), lanes_below, t_tot);
+        for (int j = 0; j < 4; ++j)
+          if ((eq >> j) & 1u) {
+            if (eq_seen + eq_pre + __popc(eq & ((1u << j) - 1u)) < eq_take) take |= 1u << j;
+          }
+        eq_seen += eq_tot;
+      }
+      if (__any_sync(0xffffffffu, take != 0)) {
+        uint32_t t_tot;
+        uint32_t p = pos + warp_excl_scan_small(__popc(take), lanes_below, t_tot);
 #pragma unroll
-      for (int j = 0; j < 4; ++j)
-        if ((take >> j) & 1u) {
-          if (p < (uint32_t)k) o[p] = start + 4 * i + j;
-          ++p;
-        }
-      pos += t_tot;
-    }
-  });
+        for (int j = 0; j < 4; ++j)
+          if ((take >> j) & 1u) {
+            if (p < (uint32_t)k) o[p] = start + 4 * i + j;
+            ++p;
+          }
+        pos += t_tot;
+      }
+    });
+  }
 }
 
 template <int C, bool kStream>

@@ -154,7 +154,7 @@ dsa_status_t dsa_index_scores(const dsa_paged_cache_t* cache, const dsa_batch_t*
  *   k         1 .. DSA_MAX_TOPK
  *   workspace device, >= dsa_topk_workspace_size(rows, max_row_len, k) bytes, 256-B aligned;
  *             that size is 0 (and NULL is accepted) when max_row_len <= k or the rows fit
- *             the on-chip path (max_row_len <= 327,680)
+ *             the on-chip path (max_row_len <= 245,760)
  */
 size_t dsa_topk_workspace_size(int32_t rows, int32_t max_row_len, int32_t k);
 dsa_status_t dsa_topk(const float* scores, int64_t ld_scores, const int32_t* row_lens,
@@ -163,7 +163,7 @@ dsa_status_t dsa_topk(const float* scores, int64_t ld_scores, const int32_t* row
                       int32_t* dev_status, void* stream);
 
 /*
- * Which top-k kernels serve rows longer than 327,680 tokens.  By default
+ * Which top-k kernels serve rows longer than 245,760 tokens.  By default
  * (on = 0) such rows take one launch of a thread-block cluster per row (16
  * CTAs, or 8 where the device cannot schedule 16) and the workspace goes
  * unused; where neither cluster can be scheduled, four kernels over the

@@ -143,11 +143,11 @@ def test_topk_long_rows():
     np.testing.assert_array_equal(got, oracle.topk(m.astype(np.float64), lens, 2048))
 
 
-@pytest.mark.parametrize("n,ties", [(40_960, False), (40_961, True), (120_000, True), (327_680, True),
-                                     (327_681, False), (1_000_000, True)])
+@pytest.mark.parametrize("n,ties", [(30_720, False), (30_721, True), (120_000, True), (245_760, True),
+                                     (245_761, False), (327_681, True), (1_000_000, True)])
 def test_topk_row_lengths_across_paths(n, ties):
     """Rows held in one CTA, in clusters of 2..8 CTAs (ties on the k-th key
-    spread over every CTA of the cluster), and past 8 x 40,960 tokens (the
+    spread over every CTA of the cluster), and past 8 x 30,720 tokens (the
     streaming cluster kernel)."""
     rng = np.random.default_rng(n)
     ld = (n + 3) // 4 * 4
@@ -162,9 +162,9 @@ def test_topk_row_lengths_across_paths(n, ties):
 
 
 @pytest.mark.parametrize("multipass", [False, True])
-@pytest.mark.parametrize("n", [327_681, 1_000_000, 2_000_003])
+@pytest.mark.parametrize("n", [245_761, 1_000_000, 2_000_003])
 def test_topk_long_rows_on_both_paths(n, multipass):
-    """Rows past 8 x 40,960 tokens: the streaming cluster kernel (one launch)
+    """Rows past 8 x 30,720 tokens: the streaming cluster kernel (one launch)
     and the four-kernel path (forced), bit-exact against the oracle, with rows
     of mixed lengths in one call (one shorter than k, one far shorter than
     the longest) and heavy ties on the k-th key."""
