@@ -851,17 +851,15 @@ __global__ void __launch_bounds__(kResThreads, kStream ? 1 : 2)
       eq_before += e;
     }
     overflow = misc[kOverflow] != 0u;
-    if (tid == 0) misc[0] = sel_total;
+    // each CTA's total into slot c of every higher-ranked CTA (distributed
+    // shared memory), so that after the barrier the offsets are read locally
+    // and no CTA's shared memory is read by a peer any more
+    if (tid > c && tid < C) cluster.map_shared_rank(scan + 16, tid)[c] = sel_total;
     csync();
-    uint32_t offset = 0, total = 0;
+    uint32_t offset = 0;
 #pragma unroll
-    for (int q = 0; q < C; ++q) {
-      const uint32_t x = C == 1 ? misc[0] : cluster.map_shared_rank(misc, q)[0];
-      offset += q < c ? x : 0u;
-      total += x;
-    }
-    csync();  // no CTA leaves while a peer may still read its shared memory
-    if (c == 0 && tid == 0 && total != (uint32_t)k) report(status, DSA_ERR_BOUNDS);  // consistency check
+    for (int q = 0; q < C; ++q) offset += q < c ? scan[16 + q] : 0u;
+    if (c == C - 1 && tid == 0 && offset + sel_total != (uint32_t)k) report(status, DSA_ERR_BOUNDS);  // consistency check
     return offset + sel_before;
   };
 
