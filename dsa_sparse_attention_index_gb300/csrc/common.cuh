@@ -266,6 +266,9 @@ __device__ __forceinline__ uint64_t smem_desc(uint32_t addr, uint32_t lbo, uint3
          (static_cast<uint64_t>((sbo >> 4) & 0x3FFFu) << 32) | (1ull << 46) | (layout << 61);
 }
 
+// A descriptor from its two 32-bit words.
+__device__ __forceinline__ uint64_t desc64(uint32_t lo, uint32_t hi) { return ((uint64_t)hi << 32) | lo; }
+
 // Instruction descriptor (kind::f16 and kind::f8f6f4): fp32 accumulator,
 // operand formats, K-major (0) / MN-major (1) per operand, N >> 3, M >> 4.
 enum : uint32_t { kFmtE4M3 = 0, kFmtE2M1 = 5, kFmtBF16 = 1 };

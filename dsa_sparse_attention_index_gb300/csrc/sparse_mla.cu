@@ -213,23 +213,29 @@ __global__ void __launch_bounds__(kThreads, 1)
           tma_load_2d(sbase + kOffQ + kb * kQBlockBytes, &tmap_q, kb * 64, row * kHeads, q_full);
         bool ok = mbar_wait(q_full, 0, abort_flag, p.status);
         ok = ok && mbar_wait(q8_full, 0, abort_flag, p.status);
+        // Shared-memory descriptors: the start address is the low 14 bits (in
+        // 16-byte units) of the low word, so an offset inside shared memory is
+        // added to the low word alone; the high word (stride, layout) is fixed.
+        const uint64_t q_desc = smem_desc(sbase + kOffQ, 16, 1024, kLayoutSw128);
+        const uint32_t q_lo = (uint32_t)q_desc, sw128_hi = (uint32_t)(q_desc >> 32);
+        const uint32_t t_lo0 = (uint32_t)smem_desc(sbase + kOffTile, 16, 1024, kLayoutSw128);
         auto issue_qk = [&](int i) {
           const int b = i & 1;
-          const uint32_t tile = sbase + kOffTile + (i % kTileBufs) * kTileBytes;
+          const uint32_t d = tmem + kSCol + kTileTok * b;
+          const uint32_t t_lo = t_lo0 + (uint32_t)((i % kTileBufs) * kTileBytes / 16);
+#pragma unroll
           for (int kb = 0; kb < kQSmemBlocks; ++kb) {
 #pragma unroll
-            for (int kk = 0; kk < 4; ++kk) {
-              const uint64_t ad = smem_desc(sbase + kOffQ + kb * kQBlockBytes + 32 * kk, 16, 1024, kLayoutSw128);
-              const uint64_t bd = smem_desc(tile + kb * kTileDBlockBytes + 32 * kk, 16, 1024, kLayoutSw128);
-              mma_bf16(tmem + kSCol + kTileTok * b, ad, bd, kIdescQK, (kb | kk) ? 1u : 0u);
-            }
+            for (int kk = 0; kk < 4; ++kk)
+              mma_bf16(d, desc64(q_lo + (kb * kQBlockBytes + 32 * kk) / 16, sw128_hi),
+                       desc64(t_lo + (kb * kTileDBlockBytes + 32 * kk) / 16, sw128_hi), kIdescQK,
+                       (kb | kk) ? 1u : 0u);
           }
 #pragma unroll
-          for (int kk = 0; kk < 4 * kQTmemBlocks; ++kk) {  // dims 448..575: A from TMEM, 8 columns per K = 16 step
-            const uint64_t bd = smem_desc(tile + (kQSmemBlocks + kk / 4) * kTileDBlockBytes + 32 * (kk % 4), 16,
-                                          1024, kLayoutSw128);
-            mma_bf16_tmem_a(tmem + kSCol + kTileTok * b, tmem + kQ8Col + 8 * kk, bd, kIdescQK, 1u);
-          }
+          for (int kk = 0; kk < 4 * kQTmemBlocks; ++kk)  // dims 448..575: A from TMEM, 8 columns per K = 16 step
+            mma_bf16_tmem_a(d, tmem + kQ8Col + 8 * kk,
+                            desc64(t_lo + ((kQSmemBlocks + kk / 4) * kTileDBlockBytes + 32 * (kk % 4)) / 16, sw128_hi),
+                            kIdescQK, 1u);
           mma_commit(s_full(b));
         };
         for (int i = 0; ok && i < ntiles; ++i) {
@@ -247,21 +253,24 @@ __global__ void __launch_bounds__(kThreads, 1)
     } else if (warp == kPvWarp) {
       if (lane == 0) {
         // ------------------------------------------------ PV issuer
+        // descriptors as in the QK issuer: offsets go to the low word
+        const uint64_t a_desc = smem_desc(sbase + kOffTile, kTileDBlockBytes, 1024, kLayoutSw128);
+        const uint32_t a_lo0 = (uint32_t)a_desc, a_hi = (uint32_t)(a_desc >> 32);
+        const uint64_t p_desc = smem_desc(sbase + kOffP, 16, 512, kLayoutSw64);
+        const uint32_t p_lo0 = (uint32_t)p_desc, p_hi = (uint32_t)(p_desc >> 32);
         for (int i = 0; i < ntiles; ++i) {
           const int b = i & 1;
           if (!mbar_wait(p_full(b), (i >> 1) & 1, abort_flag, p.status)) break;
           tc_fence_after();
-          const uint32_t tile = sbase + kOffTile + (i % kTileBufs) * kTileBytes;
-          const uint32_t pt = sbase + kOffP + b * kPBytes;
+          const uint32_t a_lo = a_lo0 + (uint32_t)((i % kTileBufs) * kTileBytes / 16);
+          const uint32_t b_lo = p_lo0 + (uint32_t)(b * kPBytes / 16);
 #pragma unroll
           for (int mb = 0; mb < 4; ++mb) {
 #pragma unroll
             for (int ks = 0; ks < kTileTok / 16; ++ks) {
               // A: dims [128 mb, +128) = two 64-dim atoms (LBO apart), tokens [16 ks, +16) = two 8-row groups
-              const uint64_t ad = smem_desc(tile + 2 * mb * kTileDBlockBytes + 2 * ks * 1024, kTileDBlockBytes,
-                                            1024, kLayoutSw128);
-              const uint64_t bd = smem_desc(pt + 32 * ks, 16, 512, kLayoutSw64);
-              mma_bf16(tmem + mb * kHeads, ad, bd, kIdescPV, (i > 0 || ks > 0) ? 1u : 0u);
+              mma_bf16(tmem + mb * kHeads, desc64(a_lo + (2 * mb * kTileDBlockBytes + 2 * ks * 1024) / 16, a_hi),
+                       desc64(b_lo + 32 * ks / 16, p_hi), kIdescPV, (i > 0 || ks > 0) ? 1u : 0u);
             }
           }
           // QK of tile i completed before its P existed, so the tile is free after these
@@ -436,33 +445,44 @@ __global__ void __launch_bounds__(kThreads, 1)
         __syncwarp();
         if (lane == 0) mbar_arrive(p_full(b));
       }
-      // ---- epilogue: partial results of this chunk
-      if (ok) ok = mbar_wait(pv_done((ntiles - 1) & 1), ((ntiles - 1) >> 1) & 1, abort_flag, p.status);
+      // ---- this chunk's running max and sums per head
       ok = !bar_or_softmax(!ok);
-      if (ok) {
-        tc_fence_after();
+      if (ok && live) {
         const int64_t part = (int64_t)row * p.nsplit + split;
-        float* op = p.opart + part * kHeads * kValue;
-        const int dim_in_block = warp * 32 + lane;
-#pragma unroll 1
-        for (int c = 0; c < 12; ++c) {
-          uint32_t o[32];
-          tmem_ld32(tmem + ((uint32_t)(warp * 32) << 16) + (c / 3) * kHeads + (c % 3) * 32, o);
-          tmem_ld_wait();
-          const int dim = (c / 3) * 128 + dim_in_block;
-#pragma unroll
-          for (int j = 0; j < 32; ++j) op[(int64_t)((c % 3) * 32 + j) * kValue + dim] = __uint_as_float(o[j]);
-        }
-        if (live) {
-          float4 v = make_float4(m_used, l_round, l_exact, 0.f);
-          reinterpret_cast<float4*>(p.ml)[part * kHeads + h] = v;
-        }
+        reinterpret_cast<float4*>(p.ml)[part * kHeads + h] = make_float4(m_used, l_round, l_exact, 0.f);
       }
     }
   } else if (threadIdx.x < kHeads) {
     // empty chunk: contributes nothing
     const int64_t part = (int64_t)row * p.nsplit + split;
     reinterpret_cast<float4*>(p.ml)[part * kHeads + threadIdx.x] = make_float4(-INFINITY, 0.f, 0.f, 0.f);
+  }
+  // ---- epilogue: the chunk's unnormalised O^T to the workspace, by all twelve
+  //      warps.  Every MMA has completed: both issuers waited for theirs before
+  //      this barrier.  Warp w reads TMEM lanes 32 (w % 4) .. + 31 (dims of each
+  //      128-dim block) and the 32-head column groups w / 4 of the four blocks,
+  //      two groups in flight.
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  if (ntiles > 0 && *abort_flag == 0) {
+    const int64_t part = (int64_t)row * p.nsplit + split;
+    float* op = p.opart + part * kHeads * kValue;
+    const int quarter = warp & 3, hg = warp >> 2;
+    const uint32_t lane_base = tmem + ((uint32_t)(quarter * 32) << 16) + hg * 32;
+    const int dim_in_block = quarter * 32 + lane;
+#pragma unroll 1
+    for (int mb = 0; mb < 4; mb += 2) {
+      uint32_t o0[32], o1[32];
+      tmem_ld32(lane_base + mb * kHeads, o0);
+      tmem_ld32(lane_base + (mb + 1) * kHeads, o1);
+      tmem_ld_wait();
+#pragma unroll
+      for (int j = 0; j < 32; ++j) {
+        op[(int64_t)(hg * 32 + j) * kValue + mb * 128 + dim_in_block] = __uint_as_float(o0[j]);
+        op[(int64_t)(hg * 32 + j) * kValue + (mb + 1) * 128 + dim_in_block] = __uint_as_float(o1[j]);
+      }
+    }
   }
   tc_fence_before();
   __syncthreads();
