@@ -37,6 +37,8 @@
 #include <algorithm>
 #include <cmath>
 
+#include <cooperative_groups.h>
+
 #include "common.cuh"
 #include "internal.h"
 
@@ -55,6 +57,8 @@ constexpr int kTileDBlockBytes = kTileTok * 128;       // 4,096
 constexpr int kTileBytes = kDBlocks * kTileDBlockBytes;  // 36,864
 constexpr int kPBytes = kHeads * kTileTok * 2;         // 6,144
 constexpr int kMaxChunk = 1024;                        // tokens per CTA
+constexpr int kMaxSplit = 16;                          // chunks per row
+constexpr int kMaxFusedSplit = 8;                      // chunks combined inside the kernel (a portable cluster)
 // 12 warps: softmax 0-3, loaders 4-9, QK issuer 10, PV issuer 11.  Three warps
 // share a sub-partition's register file: room for 168 registers a thread.
 constexpr int kThreads = 12 * 32;
@@ -100,6 +104,11 @@ struct MlaParams {
   float* opart;     // [rows][nsplit][96][512]
   float* ml;        // [rows][nsplit][96][4]: max (log2), sum of bf16(p), sum of p
   int32_t* status;
+  // combining in the kernel: a row's nsplit CTAs form a cluster (fuse = 1)
+  int32_t fuse;
+  float latent_scale;
+  uint16_t* out;    // bf16 [rows][96][512]
+  float* lse;       // [rows][96]
 };
 
 __device__ __forceinline__ float ex2(float x) {
@@ -488,13 +497,66 @@ __global__ void __launch_bounds__(kThreads, 1)
   __syncthreads();
   tc_fence_after();
   if (warp == kMmaWarp) tmem_dealloc(tmem, kTmemCols);
+  if (p.fuse) {
+    // ---- the row's chunks are the cluster: once every chunk's partials are
+    //      written (the cluster barrier orders them), each CTA merges a share of
+    //      the row's outputs through the chunks' log-sum-exp, as the combine
+    //      kernel does
+    cooperative_groups::this_cluster().sync();
+    const float4* mlr = reinterpret_cast<const float4*>(p.ml) + (int64_t)row * p.nsplit * kHeads;
+    float* wgt = reinterpret_cast<float*>(smem + kOffTile);  // [96][kMaxFusedSplit]; the tiles are free
+    if (threadIdx.x < kHeads) {
+      const int h = threadIdx.x;
+      float M = -INFINITY;
+      for (int s = 0; s < p.nsplit; ++s) M = fmaxf(M, mlr[s * kHeads + h].x);
+      float den = 0.f, ex = 0.f;
+      for (int s = 0; s < p.nsplit; ++s) {
+        const float4 v = mlr[s * kHeads + h];
+        const float w = (M == -INFINITY || v.x == -INFINITY) ? 0.f : ex2(v.x - M);
+        den += w * v.y;
+        ex += w * v.z;
+        wgt[h * kMaxFusedSplit + s] = w;
+      }
+      const float inv = den > 0.f ? p.latent_scale / den : 0.f;
+      for (int s = 0; s < p.nsplit; ++s) wgt[h * kMaxFusedSplit + s] *= inv;
+      if (split == 0)
+        p.lse[(int64_t)row * kHeads + h] =
+            (M == -INFINITY || ex <= 0.f) ? -INFINITY : (M + log2f(ex)) * 0.69314718055994531f;
+    }
+    __syncthreads();
+    constexpr int kVec = kHeads * kValue / 4;  // float4s of the row's output
+    const int v0 = (int)((int64_t)kVec * split / p.nsplit), v1 = (int)((int64_t)kVec * (split + 1) / p.nsplit);
+    for (int v = v0 + (int)threadIdx.x; v < v1; v += kThreads) {
+      const int hh = v / (kValue / 4), d = (v % (kValue / 4)) * 4;
+      const float* src = p.opart + ((int64_t)row * p.nsplit * kHeads + hh) * kValue + d;
+      float4 x[kMaxFusedSplit];
+#pragma unroll
+      for (int s = 0; s < kMaxFusedSplit; ++s)
+        if (s < p.nsplit) x[s] = *reinterpret_cast<const float4*>(src + (int64_t)s * kHeads * kValue);
+      float4 a = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+      for (int s = 0; s < kMaxFusedSplit; ++s)
+        if (s < p.nsplit) {
+          const float w = wgt[hh * kMaxFusedSplit + s];
+          a.x = fmaf(w, x[s].x, a.x);
+          a.y = fmaf(w, x[s].y, a.y);
+          a.z = fmaf(w, x[s].z, a.z);
+          a.w = fmaf(w, x[s].w, a.w);
+        }
+      const __nv_bfloat162 lo = __floats2bfloat162_rn(a.x, a.y);
+      const __nv_bfloat162 hi = __floats2bfloat162_rn(a.z, a.w);
+      uint2 pk;
+      pk.x = *reinterpret_cast<const uint32_t*>(&lo);
+      pk.y = *reinterpret_cast<const uint32_t*>(&hi);
+      *reinterpret_cast<uint2*>(p.out + ((int64_t)row * kHeads + hh) * kValue + d) = pk;
+    }
+  }
 }
 
 // Merge the chunks of one row through their log-sum-exp and write bf16 O and
 // fp32 LSE (natural log).  CTA (row, group) covers 8 heads; every split's
 // partial of a float4 is loaded before any is added (loads in flight).
 constexpr int kCombineHeads = 8;
-constexpr int kMaxSplit = 16;
 __global__ void __launch_bounds__(256) mla_combine_kernel(const float* __restrict__ opart,
                                                            const float* __restrict__ ml, int nsplit,
                                                            float latent_scale, uint16_t* out, float* lse) {
@@ -546,6 +608,35 @@ __global__ void __launch_bounds__(256) mla_combine_kernel(const float* __restric
 }
 
 }  // namespace
+
+// Whether clusters of `nsplit` CTAs of the MLA kernel can be resident on this
+// device (asked once per device and size).
+bool fused_cluster_ok(int nsplit) {
+  static int known[64][kMaxFusedSplit + 1] = {};  // 0 unknown, 1 yes, 2 no
+  int dev = 0;
+  cudaGetDevice(&dev);
+  if (dev < 0 || dev >= 64 || nsplit < 1 || nsplit > kMaxFusedSplit) return false;
+  if (known[dev][nsplit] == 0) {
+    bool ok = cudaFuncSetAttribute(sparse_mla_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                   (int)kSmemBytes) == cudaSuccess;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)nsplit);
+    cfg.blockDim = dim3(kThreads);
+    cfg.dynamicSmemBytes = kSmemBytes;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = (unsigned)nsplit;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    int n = 0;
+    ok = ok && cudaOccupancyMaxActiveClusters(&n, sparse_mla_kernel, &cfg) == cudaSuccess && n > 0;
+    cudaGetLastError();  // a refused query leaves no error behind
+    known[dev][nsplit] = ok ? 1 : 2;
+  }
+  return known[dev][nsplit] == 1;
+}
 
 // Token chunks per row: enough CTAs for one wave over the SMs (one CTA per SM
 // fits), at most 16; the workspace is sized for up to 256 SMs.
@@ -601,7 +692,11 @@ dsa_status_t launch_sparse_mla(const dsa_paged_cache_t& c, const dsa_batch_t& bt
               q_mla,
               opart,
               ml,
-              status};
+              status,
+              0,
+              c.latent_scale,
+              out,
+              lse};
   static bool attr_set[64] = {};
   int dev = 0;
   cudaGetDevice(&dev);
@@ -611,20 +706,29 @@ dsa_status_t launch_sparse_mla(const dsa_paged_cache_t& c, const dsa_batch_t& bt
       return DSA_ERR_CUDA;
     attr_set[dev] = true;
   }
-  // both launches may overlap the previous kernel's tail; each waits for its inputs
-  cudaLaunchAttribute pdl[1];
-  pdl[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-  pdl[0].val.programmaticStreamSerializationAllowed = 1;
+  // Up to kMaxFusedSplit chunks per row: the row's CTAs form a cluster and
+  // merge the chunks themselves; more chunks take the combine kernel.
+  p.fuse = nsplit <= kMaxFusedSplit && fused_cluster_ok(nsplit) ? 1 : 0;
+  // the launches may overlap the previous kernel's tail; each waits for its inputs
+  cudaLaunchAttribute attrs[2];
+  attrs[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attrs[0].val.programmaticStreamSerializationAllowed = 1;
+  attrs[1].id = cudaLaunchAttributeClusterDimension;
+  attrs[1].val.clusterDim.x = (unsigned)nsplit;
+  attrs[1].val.clusterDim.y = 1;
+  attrs[1].val.clusterDim.z = 1;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3((unsigned)nsplit, (unsigned)rows);
   cfg.blockDim = dim3(kThreads);
   cfg.dynamicSmemBytes = kSmemBytes;
   cfg.stream = st;
-  cfg.attrs = pdl;
-  cfg.numAttrs = 1;
+  cfg.attrs = attrs;
+  cfg.numAttrs = p.fuse ? 2 : 1;
   count_launches(1);
   if (cuda_status(cudaLaunchKernelEx(&cfg, sparse_mla_kernel, qmap, p)) != DSA_OK) return DSA_ERR_CUDA;
+  if (p.fuse) return launch_status();
   cudaLaunchConfig_t cfg2 = cfg;
+  cfg2.numAttrs = 1;
   cfg2.gridDim = dim3(kHeads / kCombineHeads, (unsigned)rows);
   cfg2.blockDim = dim3(256);
   cfg2.dynamicSmemBytes = 0;

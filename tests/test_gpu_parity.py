@@ -192,15 +192,19 @@ def test_topk_long_rows_on_both_paths(n, multipass):
     np.testing.assert_array_equal(got, oracle.topk(m.astype(np.float64), lens, 2048))
 
 
-def test_decode_step_launches_four_kernels():
-    """A fused decode step is four launches (indexer, top-k, sparse MLA, chunk
-    combine) for rows that fit the on-chip top-k and for rows that take the
-    streaming cluster top-k."""
-    for lens in ([9000, 130], [400_000]):
-        case = synth.make_case("cnt", seq_lens=lens, nq=1, seed=3)
-        n0 = binding.kernel_launches()
-        _run_step(case)
-        assert binding.kernel_launches() - n0 == 4
+@pytest.mark.parametrize("lens,launches", [
+    ([3000] * 32, 3),        # 4 chunks per row: the MLA merges them itself (a cluster per row)
+    ([9000, 130], 4),        # 16 chunks per row: plus the combine kernel
+    ([400_000], 4),          # the streaming cluster top-k, 16 chunks
+])
+def test_decode_step_launch_count(lens, launches):
+    """A fused decode step launches the indexer, the top-k and the sparse MLA,
+    plus the chunk combine when a row has more than 8 chunks."""
+    case = synth.make_case("cnt", seq_lens=lens, nq=1, seed=3)
+    n0 = binding.kernel_launches()
+    scores, idx, o, l = _run_step(case)
+    assert binding.kernel_launches() - n0 == launches
+    check_mla(case, idx, o, l)
 
 
 def _gpu_mla(case, dc, idx_np):
