@@ -161,6 +161,24 @@ def test_topk_row_lengths_across_paths(n, ties):
     np.testing.assert_array_equal(got, oracle.topk(m.astype(np.float64), lens, 2048))
 
 
+@pytest.mark.parametrize("n", [10_000, 20_000, 45_000, 50_000, 60_000])
+def test_topk_cluster_sizes(n):
+    """Three rows of lengths that give clusters of 1, 2, 5, 6 and 7 CTAs per row
+    (with heavy ties, all-equal scores and specials), bit-exact."""
+    rng = np.random.default_rng(n + 1)
+    ld = (n + 3) // 4 * 4
+    m = np.zeros((3, ld), dtype=np.float32)
+    m[0, :n] = rng.integers(0, 40, n)
+    m[1, :n] = -3.0
+    m[2, :n] = rng.standard_normal(n)
+    m[2, 7] = np.nan
+    m[2, n // 2] = -np.inf
+    m[2, n - 1] = np.inf
+    lens = np.array([n, n - 1, n - 2], dtype=np.int32)
+    got = _gpu_topk(torch.from_numpy(m).cuda(), torch.from_numpy(lens).cuda(), 2048, max_row_len=n)
+    np.testing.assert_array_equal(got, oracle.topk(m.astype(np.float64), lens, 2048))
+
+
 @pytest.mark.parametrize("multipass", [False, True])
 @pytest.mark.parametrize("n", [245_761, 1_000_000, 2_000_003])
 def test_topk_long_rows_on_both_paths(n, multipass):
@@ -244,6 +262,22 @@ def test_sparse_mla_matches_oracle(k):
         idx[r, :n] = np.sort(rng.choice(int(L), n, replace=False))
     o, l = _gpu_mla(case, dc, idx)
     check_mla(case, idx, o, l, rtol=0.0 if k == 2048 else OUT_RTOL_EDGE)
+
+
+@pytest.mark.parametrize("rows", [50, 30, 25, 21])
+def test_sparse_mla_chunks_merged_in_cluster(rows):
+    """Row counts that give 3, 5, 6 and 7 chunks per row (k = 2048, 152 SMs):
+    the row's CTAs merge their chunks as a cluster of that size."""
+    case = synth.make_case("mlc", seq_lens=[2600] * rows, nq=1, seed=rows)
+    dc = synth.device_case(case)
+    rng = np.random.default_rng(rows)
+    k = 2048
+    idx = np.stack([np.sort(rng.choice(2600, k, replace=False)) for _ in range(rows)]).astype(np.int32)
+    idx[1, 100:900] = -1                                  # a row with a masked run
+    n0 = binding.kernel_launches()
+    o, l = _gpu_mla(case, dc, idx)
+    assert binding.kernel_launches() - n0 == 1            # no separate combine
+    check_mla(case, idx, o, l)
 
 
 def test_sparse_mla_single_token_is_bit_exact():
