@@ -4,7 +4,7 @@
 // tokens' 576-wide latents (absorbed MLA, keys = all 576 columns, values =
 // the first 512), an exact softmax, and the weighted sum of values, plus the
 // log-sum-exp (vLLM Day-0 post for Kimi K3.1 Pro, sparse-attention section:
-// "MLA attention then runs exactly, but only on these 2,048 tokens"; the
+// the MLA attention is exact, restricted to the 2,048 selected tokens; the
 // prefill section gives the 96 heads).  The selected rows are read straight
 // from the packed paged cache through the block table.
 //

@@ -2,8 +2,8 @@
 //
 // Keeps the k (= 2,048 in the model) highest-scoring visible tokens of each
 // query row (vLLM Day-0 post for Kimi K3.1 Pro, sparse-attention section:
-// "then keep the top 2,048 tokens"; fused-decode section: an exact top-k
-// selection kernel).  Equal scores go to the lower token index, so the
+// the indexer's scores choose 2,048 tokens per query; fused-decode section:
+// the selection is exact).  Equal scores go to the lower token index, so the
 // selected set is unique; it is written in ascending token order with -1
 // padding when a row has fewer than k tokens.  Scores are compared as
 // order-preserving 32-bit keys (integer radix).

@@ -196,8 +196,9 @@ dsa_status_t dsa_topk_noalloc(const float* scores, int64_t ld_scores, const int3
                               int32_t* dev_status, void* stream);
 
 /*
- * Exact sparse MLA decode (stage 3; Day-0 post: "MLA attention then runs
- * exactly, but only on these 2,048 tokens"; absorbed form, 96 heads).
+ * Exact sparse MLA decode (stage 3; Day-0 post, sparse-attention section:
+ * exact MLA attention restricted to the selected tokens; absorbed form, 96
+ * heads).
  * For row r and head h, over the entries i of idx[r] that are >= 0:
  *   c_i       = latent_scale * e4m3(latent row of token idx[r][i])   (576 values)
  *   l_i       = sm_scale * (q[r][h] . c_i)

@@ -62,6 +62,8 @@ def _load():
             lib.oracle_index_score_bounds.restype = i32
             lib.oracle_topk.argtypes = [P, i64, P, i32, i32, P]
             lib.oracle_topk.restype = i32
+            lib.oracle_dcp_topk.argtypes = [P, i64, P, i32, i32, i32, P, P]
+            lib.oracle_dcp_topk.restype = i32
             lib.oracle_sparse_mla.argtypes = [P, i64, i64, i32, f64, P, i32, P, i32, i32, P, P, i32, f64, P, P]
             lib.oracle_sparse_mla.restype = i32
             lib.oracle_num_threads.argtypes = []
@@ -166,6 +168,23 @@ def topk(scores: np.ndarray, row_lens: np.ndarray, k: int) -> np.ndarray:
     rc = _load().oracle_topk(_ptr(s), s.shape[1], _ptr(lens), rows, int(k), _ptr(out))
     _check(rc, "topk")
     return out
+
+
+def dcp_topk(scores: np.ndarray, row_lens: np.ndarray, k: int, shards: int):
+    """Top-k through the decode-context-parallel merge of W = `shards` shards
+    (Day-0 post, decode-context-parallelism section): per shard the best
+    ceil(1.5 k / W) bf16-keyed candidates as 32-bit words, a global selection,
+    and a full local top-k resent by any shard that may hold more of it.
+    Returns (indices [rows, k] ascending with -1 padding, stats [rows, 3]:
+    words sent in the first round, shards that resent, words resent)."""
+    s = np.ascontiguousarray(scores, dtype=np.float32)
+    lens = np.ascontiguousarray(row_lens, dtype=np.int32)
+    rows = s.shape[0]
+    out = np.empty((rows, k), dtype=np.int32)
+    stats = np.empty((rows, 3), dtype=np.int64)
+    rc = _load().oracle_dcp_topk(_ptr(s), s.shape[1], _ptr(lens), rows, int(k), int(shards), _ptr(out), _ptr(stats))
+    _check(rc, "dcp_topk")
+    return out, stats
 
 
 def sparse_mla(case, idx: np.ndarray, k: int | None = None):

@@ -35,8 +35,8 @@
  *                 ascending token order, padded with -1.
  *   sparse MLA    exact softmax attention of 96 heads over the selected
  *                 tokens' 576-wide latents (absorbed MLA: keys are the full
- *                 576 columns, values the first 512) ([K31] "MLA attention
- *                 then runs exactly, but only on these 2,048 tokens").
+ *                 576 columns, values the first 512) ([K31]: the attention
+ *                 is exact, restricted to the selected tokens).
  *
  * Paged cache ([K31] packed-cache section): a pool of block rows; a block row
  * holds, at caller-given byte offsets, the latent page (64 tokens x 576 B
@@ -307,6 +307,114 @@ int oracle_topk(const double* scores, int64_t ld, const int32_t* row_lens, int32
     qsort(out, (size_t)n, sizeof(int32_t), by_index);
     for (int64_t i = n; i < k; ++i) out[i] = -1;
     free(all);
+  }
+  return bad ? ORACLE_BAD_ARG : ORACLE_OK;
+}
+
+/* ------------------------------------------------------------------ */
+/* Decode context parallelism: the exact top-k merge across W shards.  */
+/* ------------------------------------------------------------------ */
+
+/* [K31] decode-context-parallelism section.  Shard r of W holds the tokens t
+ * with t mod W = r (local position t div W).  Each shard sends its best
+ * ceil(1.5 k / W) candidates, chosen on bf16 scores, each packed with its
+ * score into one 32-bit word; every shard then selects the same global top-k
+ * from the gathered words.  A shard all of whose sent words were selected,
+ * and which holds more tokens, may hold more of the top-k than it sent: it
+ * resends its full local top-k (min(k, its tokens) words) for that row and
+ * the selection runs again (a shard that has sent its full local top-k
+ * cannot hold more of a top-k of k tokens).
+ * Readings: the word is the 16-bit order key of the bf16-rounded score
+ * (round to nearest even) in the upper half and the local position in the
+ * lower half, so a shard holds at most 65,536 tokens of a row.  Keys order
+ * as the fp32 top-k does (higher first, NaN below every number, -0 = +0) and
+ * equal keys go to the lower global token index.  The result is therefore
+ * the top-k of the bf16-rounded scores. */
+static uint16_t bf16_order_key(float x) {
+  uint32_t u;
+  memcpy(&u, &x, 4);
+  if ((u & 0x7FFFFFFFu) > 0x7F800000u) return 0; /* NaN: below every number */
+  uint32_t b = (u + 0x7FFFu + ((u >> 16) & 1u)) >> 16; /* round to nearest even */
+  if (b == 0x8000u) b = 0;                            /* -0 = +0 */
+  return (uint16_t)((b & 0x8000u) ? (~b & 0xFFFFu) : (b | 0x8000u));
+}
+
+typedef struct { uint32_t key; int32_t t; } dcp_cand_t;  /* t: global token index */
+
+/* Higher key first; equal keys: lower global index first. */
+static int dcp_order(const void* pa, const void* pb) {
+  const dcp_cand_t* a = (const dcp_cand_t*)pa;
+  const dcp_cand_t* b = (const dcp_cand_t*)pb;
+  if (a->key != b->key) return a->key > b->key ? -1 : 1;
+  return (a->t < b->t) ? -1 : (a->t > b->t);
+}
+
+int oracle_dcp_topk(const float* scores, int64_t ld, const int32_t* row_lens, int32_t rows, int32_t k,
+                    int32_t shards, int32_t* idx_out /*[rows][k]*/, int64_t* stats /*[rows][3] or NULL*/) {
+  if (!scores || !row_lens || !idx_out || k < 1 || rows < 0 || shards < 1 || shards > 64) return ORACLE_BAD_ARG;
+  const int32_t c = (int32_t)((3LL * k + 2LL * shards - 1) / (2LL * shards)); /* ceil(1.5 k / W) */
+  int bad = 0;
+#pragma omp parallel for schedule(dynamic) reduction(| : bad)
+  for (int32_t row = 0; row < rows; ++row) {
+    const int64_t len = row_lens[row];
+    if (len < 0 || len > ld || (len + shards - 1) / shards > 65536) { bad = 1; continue; }
+    const float* srow = scores + (int64_t)row * ld;
+    /* every shard's tokens in its own order: (key desc, local asc) */
+    dcp_cand_t** local = (dcp_cand_t**)calloc((size_t)shards, sizeof(dcp_cand_t*));
+    int64_t* n = (int64_t*)calloc((size_t)shards, sizeof(int64_t));
+    int64_t* sent = (int64_t*)calloc((size_t)shards, sizeof(int64_t));
+    int64_t* taken = (int64_t*)calloc((size_t)shards, sizeof(int64_t));
+    for (int32_t r = 0; r < shards; ++r) {
+      n[r] = len > r ? (len - r + shards - 1) / shards : 0;
+      local[r] = (dcp_cand_t*)malloc(sizeof(dcp_cand_t) * (size_t)(n[r] > 0 ? n[r] : 1));
+      for (int64_t l = 0; l < n[r]; ++l) {
+        const int64_t t = l * shards + r;
+        /* the word a shard sends: key above, local position below */
+        const uint32_t word = ((uint32_t)bf16_order_key(srow[t]) << 16) | (uint32_t)l;
+        local[r][l].key = word >> 16;
+        local[r][l].t = (int32_t)t;
+      }
+      qsort(local[r], (size_t)n[r], sizeof(dcp_cand_t), dcp_order);
+      sent[r] = n[r] < c ? n[r] : c;
+    }
+    int64_t words = 0, resent_shards = 0, resent_words = 0;
+    for (int32_t r = 0; r < shards; ++r) words += sent[r];
+    dcp_cand_t* pool = (dcp_cand_t*)malloc(sizeof(dcp_cand_t) * (size_t)(len > 0 ? len : 1));
+    int64_t m = 0, sel = 0;
+    for (int round = 0; round < 2; ++round) {
+      /* gather every shard's sent words and select the global top-k */
+      m = 0;
+      for (int32_t r = 0; r < shards; ++r)
+        for (int64_t i = 0; i < sent[r]; ++i) pool[m++] = local[r][i];
+      qsort(pool, (size_t)m, sizeof(dcp_cand_t), dcp_order);
+      sel = m < k ? m : k;
+      for (int32_t r = 0; r < shards; ++r) taken[r] = 0;
+      for (int64_t i = 0; i < sel; ++i) taken[pool[i].t % shards]++;
+      /* a shard whose sent words were all taken, and which sent fewer than its
+       * full local top-k, may hold more of the global top-k: it resends */
+      int again = 0;
+      for (int32_t r = 0; r < shards; ++r)
+        if (taken[r] == sent[r] && sent[r] < (n[r] < k ? n[r] : k)) {
+          if (round == 1) { bad = 1; }
+          const int64_t full = n[r] < k ? n[r] : k;
+          resent_shards++;
+          resent_words += full;
+          sent[r] = full;
+          again = 1;
+        }
+      if (!again) break;
+    }
+    int32_t* out = idx_out + (int64_t)row * k;
+    for (int64_t i = 0; i < sel; ++i) out[i] = pool[i].t;
+    qsort(out, (size_t)sel, sizeof(int32_t), by_index);
+    for (int64_t i = sel; i < k; ++i) out[i] = -1;
+    if (stats) {
+      stats[3 * (int64_t)row] = words;
+      stats[3 * (int64_t)row + 1] = resent_shards;
+      stats[3 * (int64_t)row + 2] = resent_words;
+    }
+    for (int32_t r = 0; r < shards; ++r) free(local[r]);
+    free(local); free(n); free(sent); free(taken); free(pool);
   }
   return bad ? ORACLE_BAD_ARG : ORACLE_OK;
 }

@@ -415,3 +415,58 @@ def test_quantize_query_folds_the_scale():
     s = np.where(amax > 0, amax / np.float32(448.0), np.float32(1.0)).astype(np.float32)
     np.testing.assert_array_equal(codes, _torch_e4m3(q / s[..., None]))
     np.testing.assert_array_equal(w_out, (w * s).astype(np.float32))
+
+
+# ---------------------------------------------------------------- DCP top-k merge
+def _bf16_round(x):
+    return torch.from_numpy(np.ascontiguousarray(x, dtype=np.float32)).to(torch.bfloat16).to(torch.float32).numpy()
+
+
+@pytest.mark.parametrize("shards", [1, 2, 3, 5, 8])
+def test_dcp_topk_is_the_topk_of_bf16_scores(shards):
+    """The shard-wise candidates, the merge and the resends give exactly the
+    top-k of the bf16-rounded scores with ties to the lower index (a full
+    sort, the plain top-k)."""
+    rng = np.random.default_rng(shards)
+    n = 7000
+    s = np.zeros((6, n), dtype=np.float32)
+    s[0] = rng.standard_normal(n)
+    s[1] = rng.integers(0, 40, n)                      # heavy ties
+    s[2] = rng.standard_normal(n) * 1e-3 + 1.0          # ties only after bf16 rounding
+    s[3] = rng.standard_normal(n)
+    s[3, [5, 77, 900]] = [np.nan, -0.0, np.inf]
+    s[3, 1000:1010] = 0.0
+    s[4] = -rng.exponential(1.0, n)
+    s[5] = rng.standard_normal(n)
+    lens = np.array([n, n - 1, n - 7, 2048, 2049, 1000], dtype=np.int32)
+    got, _ = oracle.dcp_topk(s, lens, 2048, shards)
+    ref = oracle.topk(_bf16_round(s).astype(np.float64), lens, 2048)
+    np.testing.assert_array_equal(got, ref)
+
+
+@pytest.mark.parametrize("shards", [2, 4, 8])
+def test_dcp_topk_resend_when_one_shard_holds_the_top(shards):
+    """Every token of shard 0 outscores the rest: shard 0's candidates are all
+    taken, so it resends its full local top-k and the result stays exact."""
+    rng = np.random.default_rng(10 + shards)
+    n = 40_000
+    s = rng.standard_normal((2, n)).astype(np.float32)
+    s[0, ::shards] += 100.0
+    lens = np.array([n, n], dtype=np.int32)
+    got, stats = oracle.dcp_topk(s, lens, 2048, shards)
+    np.testing.assert_array_equal(got, oracle.topk(_bf16_round(s).astype(np.float64), lens, 2048))
+    c = -(-3 * 2048 // (2 * shards))
+    assert stats[0, 1] == 1 and stats[0, 2] == 2048      # shard 0 resent its full local top-k
+    assert stats[1, 1] == 0 and stats[0, 0] == stats[1, 0] == shards * c
+
+
+def test_dcp_candidate_bytes_ten_times_fewer():
+    """W = 8, k = 2048: each shard sends ceil(1.5 * 2048 / 8) = 384 words of
+    4 bytes, against its full local top-k as (fp32 score, token id) pairs:
+    16,384 B / 1,536 B = 10.7."""
+    rng = np.random.default_rng(3)
+    s = rng.standard_normal((1, 100_000)).astype(np.float32)
+    _, stats = oracle.dcp_topk(s, np.array([100_000], dtype=np.int32), 2048, 8)
+    per_shard = stats[0, 0] // 8 * 4
+    assert per_shard == 1536 and stats[0, 1] == 0
+    assert (2048 * 8) / per_shard > 10
