@@ -46,7 +46,8 @@ _lib = None
 
 EXPORTS = ["dsa_api_version", "dsa_status_string", "dsa_last_cuda_error", "dsa_kernel_launches",
            "dsa_translate_pages", "dsa_index_scores",
-           "dsa_topk_workspace_size", "dsa_topk", "dsa_topk_noalloc", "dsa_topk_force_multipass", "sparse_mla_workspace_size",
+           "dsa_topk_workspace_size", "dsa_topk", "dsa_topk_noalloc", "dsa_topk_force_multipass",
+           "dsa_dcp_topk_workspace_size", "dsa_dcp_topk", "sparse_mla_workspace_size",
            "sparse_mla_decode",
            "dsa_workspace_size", "dsa_decode_step", "dsa_cache_append", "dsa_quantize_index_query",
            "dsa_selftest_wait_timeout"]
@@ -73,6 +74,8 @@ def lib():
             "dsa_topk": (i32, [P, i64, P, i32, i32, i32, P, P, sz, P, P]),
             "dsa_topk_noalloc": (i32, [P, i64, P, i32, i32, i32, P, P, P]),
             "dsa_topk_force_multipass": (i32, [i32]),
+            "dsa_dcp_topk_workspace_size": (sz, [i32, i32, i32]),
+            "dsa_dcp_topk": (i32, [P, i64, P, i32, i32, i32, i32, P, P, P, sz, P, P]),
             "sparse_mla_workspace_size": (sz, [i32, i32]),
             "sparse_mla_decode": (i32, [pc, pb, P, P, i32, f32, P, P, P, sz, P, P]),
             "dsa_workspace_size": (sz, [pb, i32]),
@@ -189,6 +192,21 @@ def topk_noalloc(scores, row_lens, max_row_len: int, k: int, idx_out, status, st
     rows = int(scores.shape[0])
     _check(lib().dsa_topk_noalloc(_ptr(scores), int(scores.shape[1]), _ptr(row_lens), rows, int(max_row_len),
                                   int(k), _ptr(idx_out), _ptr(status), _stream(stream)), "dsa_topk_noalloc")
+
+
+def dcp_topk_workspace_size(rows: int, k: int, shards: int) -> int:
+    return int(lib().dsa_dcp_topk_workspace_size(rows, k, shards))
+
+
+def dcp_topk(scores, row_lens, max_row_len: int, k: int, shards: int, idx_out, workspace, status, stats_out=None,
+             stream=None):
+    """The decode-context-parallel top-k merge of `shards` token shards (bf16-keyed candidates, global
+    selection, resends); stats_out: optional int32 [rows, 3] (words sent, shards that resent, words resent)."""
+    rows = int(scores.shape[0])
+    _check(lib().dsa_dcp_topk(_ptr(scores), int(scores.shape[1]), _ptr(row_lens), rows, int(max_row_len), int(k),
+                              int(shards), _ptr(idx_out), _ptr(stats_out), _ptr(workspace),
+                              workspace.numel() * workspace.element_size(), _ptr(status), _stream(stream)),
+           "dsa_dcp_topk")
 
 
 def sparse_mla_workspace_size(rows: int, k: int) -> int:

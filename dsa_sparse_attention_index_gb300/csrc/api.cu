@@ -198,6 +198,26 @@ dsa_status_t dsa_topk_noalloc(const float* scores, int64_t ld_scores, const int3
                              static_cast<cudaStream_t>(stream));
 }
 
+size_t dsa_dcp_topk_workspace_size(int32_t rows, int32_t k, int32_t shards) {
+  if (rows < 0 || k < 1 || k > DSA_MAX_TOPK || shards < 1 || shards > DSA_DCP_MAX_SHARDS) return 0;
+  return dcp_workspace_bytes(rows, k, shards);
+}
+
+dsa_status_t dsa_dcp_topk(const float* scores, int64_t ld_scores, const int32_t* row_lens, int32_t rows,
+                          int32_t max_row_len, int32_t k, int32_t shards, int32_t* idx_out, int32_t* stats_out,
+                          void* workspace, size_t workspace_bytes, int32_t* dev_status, void* stream) {
+  if (rows < 0 || k < 1 || k > DSA_MAX_TOPK || max_row_len < 0 || shards < 1 || !dev_status)
+    return DSA_ERR_INVALID_ARG;
+  if (shards > DSA_DCP_MAX_SHARDS || (int64_t)max_row_len > (int64_t)DSA_DCP_MAX_SHARD_TOKENS * shards)
+    return DSA_ERR_UNSUPPORTED;
+  if (rows == 0) return DSA_OK;
+  if (!scores || !row_lens || !idx_out || !aligned(scores, 4) || ld_scores < max_row_len) return DSA_ERR_INVALID_ARG;
+  const size_t need = dcp_workspace_bytes(rows, k, shards);
+  if (!workspace || !aligned(workspace, 256) || workspace_bytes < need) return DSA_ERR_WORKSPACE;
+  return launch_dcp_topk(scores, ld_scores, row_lens, rows, max_row_len, k, shards, idx_out, stats_out, workspace,
+                         dev_status, static_cast<cudaStream_t>(stream));
+}
+
 size_t sparse_mla_workspace_size(int32_t rows, int32_t k) {
   if (rows < 0 || k < 1 || k > DSA_MAX_TOPK) return 0;
   return mla_workspace_bytes(rows, k);

@@ -42,6 +42,11 @@ dsa_status_t launch_topk(const float* scores, int64_t ld, const int32_t* row_len
 // The same top-k with its scratch in a file-scope device array (no allocation).
 dsa_status_t launch_topk_noalloc(const float* scores, int64_t ld, const int32_t* row_lens, int rows, int max_row_len,
                                  int k, int32_t* out, int32_t* status, cudaStream_t st);
+// Decode-context-parallel top-k merge of `shards` token shards, emulated on one GPU.
+size_t dcp_workspace_bytes(int rows, int k, int shards);
+dsa_status_t launch_dcp_topk(const float* scores, int64_t ld, const int32_t* row_lens, int rows, int max_row_len,
+                             int k, int shards, int32_t* out, int32_t* stats, void* workspace, int32_t* status,
+                             cudaStream_t st);
 size_t mla_workspace_bytes(int rows, int k);
 dsa_status_t launch_sparse_mla(const dsa_paged_cache_t& c, const dsa_batch_t& bt, const uint16_t* q_mla,
                                const int32_t* idx, int k, float sm_scale, uint16_t* out, float* lse,

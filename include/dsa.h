@@ -54,6 +54,8 @@ extern "C" {
 #define DSA_MAX_TOPK 2048        /* top-k of the model; also the largest k accepted */
 #define DSA_MAX_QUERIES_PER_SEQ 2048 /* draft rows (1..4) or a prefill chunk (a multiple of 4) */
 #define DSA_TOPK_NOALLOC_MAX_ROWS 64  /* row limit of dsa_topk_noalloc */
+#define DSA_DCP_MAX_SHARDS 8          /* shards of dsa_dcp_topk */
+#define DSA_DCP_MAX_SHARD_TOKENS 65536 /* tokens of one row a shard may hold (16-bit local position) */
 
 typedef enum dsa_status {
   DSA_OK = 0,
@@ -194,6 +196,36 @@ int32_t dsa_topk_force_multipass(int32_t on);
 dsa_status_t dsa_topk_noalloc(const float* scores, int64_t ld_scores, const int32_t* row_lens,
                               int32_t rows, int32_t max_row_len, int32_t k, int32_t* idx_out,
                               int32_t* dev_status, void* stream);
+
+/*
+ * Decode context parallelism, the exact top-k merge (Day-0 post,
+ * decode-context-parallelism section), emulated on one GPU with `shards` = W
+ * token shards: shard r holds the tokens t with t mod W = r.
+ *   1. Each shard sends its best ceil(1.5 k / W) tokens, ranked on
+ *      bf16-rounded scores, as 32-bit words (the 16-bit order key of the bf16
+ *      score above the 16-bit local position t div W).
+ *   2. The global top-k is selected from the gathered words by (bf16 key
+ *      descending, global token index ascending).
+ *   3. A shard whose words were all taken, and which has not sent its full
+ *      local top-k, resends its full local top-k, and the selection runs again.
+ * The result is the top-k of the bf16-rounded scores (NaN below every number,
+ * -0 = +0, ties to the lower index), in ascending token order with -1
+ * padding, as from dsa_topk; it differs from dsa_topk's fp32 selection only
+ * where scores tie after rounding to bf16.
+ *   scores, ld_scores, row_lens, rows, max_row_len, k as for dsa_topk (scores
+ *             4-byte aligned; ld_scores >= max_row_len)
+ *   shards    1 .. DSA_DCP_MAX_SHARDS; max_row_len <= DSA_DCP_MAX_SHARD_TOKENS
+ *             * shards, else DSA_ERR_UNSUPPORTED
+ *   stats_out device int32 [rows][3] or NULL: words sent in the first round,
+ *             shards that resent, words resent
+ *   workspace >= dsa_dcp_topk_workspace_size(rows, k, shards) bytes, 256-B aligned
+ * Four launches (candidates, merge, resend candidates, second merge); rows
+ * without a resend are written by the first merge.
+ */
+size_t dsa_dcp_topk_workspace_size(int32_t rows, int32_t k, int32_t shards);
+dsa_status_t dsa_dcp_topk(const float* scores, int64_t ld_scores, const int32_t* row_lens, int32_t rows,
+                          int32_t max_row_len, int32_t k, int32_t shards, int32_t* idx_out, int32_t* stats_out,
+                          void* workspace, size_t workspace_bytes, int32_t* dev_status, void* stream);
 
 /*
  * Exact sparse MLA decode (stage 3; Day-0 post, sparse-attention section:

@@ -67,6 +67,13 @@ def test_host_validation_without_device(lib):
     c.key_format, c.row_stride = B.KEY_FP8_E4M3, 45312
     assert lib.dsa_topk(None, 0, None, 1, 10, 0, None, None, 0, None, None) == B.ERR_INVALID_ARG  # k = 0
     assert lib.dsa_topk(None, 0, None, 1, 10, 4096, None, None, 0, None, None) == B.ERR_INVALID_ARG  # k > 2048
+    st = 128 * 4000  # fake device status pointer
+    # DCP merge: at most 8 shards, at most 65,536 tokens per shard and row
+    assert lib.dsa_dcp_topk(None, 0, None, 1, 10, 2048, 9, None, None, None, 0, st, None) == B.ERR_UNSUPPORTED
+    assert lib.dsa_dcp_topk(None, 0, None, 1, 2 * 65536 + 1, 2048, 2, None, None, None, 0, st,
+                            None) == B.ERR_UNSUPPORTED
+    assert lib.dsa_dcp_topk(None, 0, None, 1, 10, 2048, 0, None, None, None, 0, st, None) == B.ERR_INVALID_ARG
+    assert lib.dsa_dcp_topk(128, 16, 256, 1, 10, 2048, 8, 512, None, None, 0, st, None) == B.ERR_WORKSPACE
 
 
 def test_workspace_sizes(lib):
@@ -77,3 +84,7 @@ def test_workspace_sizes(lib):
     assert lib.sparse_mla_workspace_size(32, 2048) >= 32 * 96 * 512 * 4
     assert lib.dsa_topk_workspace_size(32, 163840, 2048) == 0  # rows held in shared memory
     assert lib.dsa_topk_workspace_size(4, 100, 0) == 0
+    # DCP: one candidate slot of max(ceil(1.5 k / W), k) words per (row, shard), plus counters
+    assert lib.dsa_dcp_topk_workspace_size(32, 2048, 8) >= 32 * 8 * 2048 * 4
+    assert lib.dsa_dcp_topk_workspace_size(4, 2048, 1) >= 4 * 3072 * 4
+    assert lib.dsa_dcp_topk_workspace_size(4, 2048, 9) == 0
