@@ -278,6 +278,32 @@ def main_ours(args):
     assert status.item() == 0, binding.status_string(status.item())
     st_ms = {kk: statistics.median(v) for kk, v in stage.items()}
 
+    # ---- the decode-context-parallel top-k merge of 8 shards on the step's scores
+    #      (L2-resident after the indexer, as in a step): time and words sent
+    dcp = None
+    shards = 8
+    if case.max_len <= 65536 * shards and rank == 0:
+        dcp_ws = binding.workspace(binding.dcp_topk_workspace_size(rows, k, shards), dev)
+        dcp_idx = torch.empty((rows, k), dtype=torch.int32, device=dev)
+        dcp_stats = torch.empty((rows, 3), dtype=torch.int32, device=dev)
+        dev_ = [[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(n_att)]
+        for e in dev_:
+            flush.zero_()
+            binding.index_scores(dc.cache, dc.batch, dc.q_index, dc.head_w, scores, status, stream)
+            e[0].record(stream)
+            binding.dcp_topk(scores, dc.row_lens, case.max_len, k, shards, dcp_idx, dcp_ws, status,
+                             stats_out=dcp_stats, stream=stream)
+            e[1].record(stream)
+        torch.cuda.synchronize()
+        assert status.item() == 0, binding.status_string(status.item())
+        stt = dcp_stats.cpu().numpy()
+        words = float(stt[:, 0].mean())
+        per_shard = words / shards * 4
+        dcp = {"shards": shards, "us": round(statistics.median(e[0].elapsed_time(e[1]) for e in dev_) * 1e3, 2),
+               "launches": 4, "words_per_row": round(words, 1), "rows_with_resend": int((stt[:, 1] > 0).sum()),
+               "bytes_per_shard_and_row": round(per_shard, 1),
+               "vs_full_local_topk_pairs": round(k * 8 / per_shard, 2)}
+
     # ---- end to end through the public call, host buffers, copies inside the timed region
     e2e_ms = []
     if not args.no_e2e:
@@ -368,6 +394,7 @@ def main_ours(args):
         "stages": stages,
         "roofline": roof,
         "gpu_launches": n_launches,
+        "dcp_topk": dcp,
         "clocks": clocks,
         "wall_s_timed_region": round(t_wall, 4),
     }
