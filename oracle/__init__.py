@@ -251,3 +251,50 @@ def quantize_query(q_bf16: np.ndarray, head_w: np.ndarray):
     w_out = np.empty((rows, IDX_HEADS), dtype=np.float32)
     _check(_load().oracle_quantize_query(_ptr(q), _ptr(w), rows, _ptr(codes), _ptr(w_out)), "quantize_query")
     return codes, w_out
+
+
+def round_bf16(x: np.ndarray) -> np.ndarray:
+    """Round fp64 values to the nearest bf16 value, ties to even, exactly (8
+    significant bits; subnormal spacing 2^-133; no overflow handling, the
+    values here are far from the bf16 range's end).  Zeros, infinities and
+    NaN pass through."""
+    x = np.asarray(x, dtype=np.float64)
+    out = x.copy()
+    fin = np.isfinite(x) & (x != 0.0)
+    _, e = np.frexp(x[fin])                    # |x| = m 2^e, m in [0.5, 1)
+    quantum = np.ldexp(1.0, np.maximum(e - 8, -133))
+    out[fin] = np.rint(x[fin] / quantum) * quantum  # exact: a power-of-two scale, then round half to even
+    return out
+
+
+def dcp_sparse_mla(case, idx: np.ndarray, shards: int, k: int | None = None, partial: str = "bf16"):
+    """Sparse MLA under decode context parallelism (Day-0 post,
+    decode-context-parallelism section): shard w of W holds the tokens t
+    with t mod W = w and attends over the selected tokens it holds; the
+    partial outputs are merged through their log-sum-exp:
+        lse = ln sum_w exp(LSE_w),  out = sum_w exp(LSE_w - lse) O_w.
+    partial = "bf16": each O_w is rounded to bf16 before the merge (the
+    exchanged format; the post's combine kernels move BF16 outputs);
+    "f64": no rounding, so the result is the unsharded attention.
+    Returns (out [rows, 96, 512], lse [rows, 96], O [W, rows, 96, 512],
+    LSE [W, rows, 96]), all fp64."""
+    if partial not in ("bf16", "f64"):
+        raise ValueError("partial must be 'bf16' or 'f64'")
+    idx = np.ascontiguousarray(idx, dtype=np.int32)
+    W = int(shards)
+    parts_o, parts_l = [], []
+    for w in range(W):
+        own = np.where((idx >= 0) & (idx % W == w), idx, -1).astype(np.int32)
+        o, l = sparse_mla(case, own, k)
+        parts_o.append(round_bf16(o) if partial == "bf16" else o)
+        parts_l.append(l)
+    O = np.stack(parts_o)                      # [W, rows, 96, 512]
+    L = np.stack(parts_l)                      # [W, rows, 96]
+    m = L.max(axis=0)                          # -inf where no shard holds a token
+    safe_m = np.where(np.isfinite(m), m, 0.0)
+    wexp = np.where(np.isfinite(L), np.exp(L - safe_m), 0.0)
+    tot = wexp.sum(axis=0)
+    lse = np.where(tot > 0, safe_m + np.log(np.where(tot > 0, tot, 1.0)), -np.inf)
+    wgt = np.where(tot > 0, wexp / np.where(tot > 0, tot, 1.0), 0.0)   # exp(LSE_w - lse)
+    out = (wgt[..., None] * O).sum(axis=0)
+    return out, lse, O, L

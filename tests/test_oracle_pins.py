@@ -470,3 +470,81 @@ def test_dcp_candidate_bytes_ten_times_fewer():
     per_shard = stats[0, 0] // 8 * 4
     assert per_shard == 1536 and stats[0, 1] == 0
     assert (2048 * 8) / per_shard > 10
+
+
+# ---------------------------------------------------------------- DCP LSE combine
+def _bf16_bits_round(x):
+    """fp64 -> nearest bf16 by integer rounding of the IEEE bits (keep the top
+    16 of 64 bits' worth of significand: drop 45 bits, ties to even); valid
+    for normal values, an independent route to the oracle's rounding."""
+    b = np.ascontiguousarray(x, dtype=np.float64).view(np.uint64)
+    lsb = (b >> np.uint64(45)) & np.uint64(1)
+    b = (b + np.uint64((1 << 44) - 1) + lsb) & ~np.uint64((1 << 45) - 1)
+    return b.view(np.float64)
+
+
+def test_round_bf16_matches_torch_and_bit_rounding():
+    ties = np.array([1.0 + 2.0**-8, 1.0 + 3 * 2.0**-8, -(1.0 + 2.0**-8), 3.0 * 2.0**-9 + 1.0])
+    np.testing.assert_array_equal(oracle.round_bf16(ties), [1.0, 1.0 + 2.0**-6, -1.0, 1.0 + 2.0**-7])
+    rng = np.random.default_rng(5)
+    x32 = (rng.standard_normal(200_000) * np.exp(rng.uniform(-20, 20, 200_000))).astype(np.float32)
+    ref = torch.from_numpy(x32).to(torch.bfloat16).to(torch.float64).numpy()
+    np.testing.assert_array_equal(oracle.round_bf16(x32.astype(np.float64)), ref)
+    x64 = rng.standard_normal(200_000) * np.exp(rng.uniform(-20, 20, 200_000))
+    np.testing.assert_array_equal(oracle.round_bf16(x64), _bf16_bits_round(x64))
+
+
+@pytest.fixture(scope="module")
+def dcp_case():
+    c = synth.make_case("dcpmla", seq_lens=[300, 90], nq=1, topk=64, seed=11)
+    rng = np.random.default_rng(12)
+    idx = np.full((2, 64), -1, dtype=np.int32)
+    idx[0] = np.sort(rng.choice(300, 64, replace=False))
+    idx[1, :37] = np.sort(rng.choice(90, 37, replace=False))
+    return c, idx
+
+
+@pytest.mark.parametrize("shards", [1, 2, 3, 8])
+def test_dcp_sparse_mla_exact_partials_give_the_unsharded_softmax(dcp_case, shards):
+    """With unrounded partials the LSE combine is an identity: the merged
+    output and LSE are the softmax attention over all selected tokens
+    (torch's softmax and logsumexp in fp64), and shard w's LSE is the
+    logsumexp over the selected tokens t with t mod W = w."""
+    c, idx = dcp_case
+    out, lse, O, L = oracle.dcp_sparse_mla(c, idx, shards, partial="f64")
+    for row in range(2):
+        sel = np.array([t for t in idx[row] if t >= 0])
+        C = torch.from_numpy(np.stack([_latent(c, row, t) for t in sel]))
+        Q = torch.from_numpy(_q(c, row))
+        logits = (Q @ C.T) * c.sm_scale
+        np.testing.assert_allclose(out[row], (torch.softmax(logits, dim=-1) @ C[:, :512]).numpy(),
+                                   rtol=1e-10, atol=1e-12)
+        np.testing.assert_allclose(lse[row], torch.logsumexp(logits, dim=-1).numpy(), rtol=1e-12)
+        for w in range(shards):
+            own = torch.from_numpy(sel % shards == w)
+            if own.any():
+                np.testing.assert_allclose(L[w, row], torch.logsumexp(logits[:, own], dim=-1).numpy(), rtol=1e-12)
+            else:
+                assert np.all(np.isneginf(L[w, row])) and np.all(O[w, row] == 0)
+
+
+def test_dcp_sparse_mla_bf16_partials(dcp_case):
+    """W = 1: the one partial is the whole output, so the result is the
+    unsharded output rounded to bf16.  A shard that holds no selected token
+    sends LSE = -inf and weighs nothing: with every selected token in shard
+    0 the result is shard 0's rounded output."""
+    c, idx = dcp_case
+    ref_out, ref_lse = oracle.sparse_mla(c, idx)
+    out, lse, _, _ = oracle.dcp_sparse_mla(c, idx, 1)
+    np.testing.assert_array_equal(out, oracle.round_bf16(ref_out))
+    np.testing.assert_array_equal(lse, ref_lse)
+    only0 = np.where(idx % 4 == 0, idx, -1).astype(np.int32)
+    out, lse, O, L = oracle.dcp_sparse_mla(c, only0, 4)
+    o0, l0 = oracle.sparse_mla(c, only0)
+    np.testing.assert_array_equal(out, oracle.round_bf16(o0))
+    np.testing.assert_array_equal(lse, l0)
+    assert np.all(np.isneginf(L[1:])) and np.all(O[1:] == 0)
+    # the bf16 partials move the output by at most about one bf16 step of the largest |O_w|
+    out8, _, O8, _ = oracle.dcp_sparse_mla(c, idx, 8)
+    exact, _, _, _ = oracle.dcp_sparse_mla(c, idx, 8, partial="f64")
+    assert np.all(np.abs(out8 - exact) <= 2.0**-8 * np.abs(O8).max(axis=0) + 1e-300)
