@@ -303,6 +303,27 @@ def main_ours(args):
                "launches": 4, "words_per_row": round(words, 1), "rows_with_resend": int((stt[:, 1] > 0).sum()),
                "bytes_per_shard_and_row": round(per_shard, 1),
                "vs_full_local_topk_pairs": round(k * 8 / per_shard, 2)}
+        # the partial attention of the 8 shards over the merged selection and the
+        # LSE combine of their bf16 outputs (L2 flushed before each call)
+        cm_ws = binding.workspace(binding.dcp_sparse_mla_workspace_size(rows, k, shards), dev)
+        cm_out = torch.empty_like(out)
+        cm_lse = torch.empty_like(lse)
+        evc = [[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(n_att)]
+        for e in evc:
+            flush.zero_()
+            e[0].record(stream)
+            binding.dcp_sparse_mla(dc.cache, dc.batch, dc.q_mla, dcp_idx, shards, case.sm_scale, cm_out, cm_lse,
+                                   cm_ws, status, stream=stream)
+            e[1].record(stream)
+        binding.sparse_mla_decode(dc.cache, dc.batch, dc.q_mla, dcp_idx, case.sm_scale, out, lse, mla_ws, status,
+                                  stream)
+        torch.cuda.synchronize()
+        assert status.item() == 0, binding.status_string(status.item())
+        diff = (cm_out.view(torch.bfloat16).float() - out.view(torch.bfloat16).float()).abs().max().item()
+        dcp["lse_combine"] = {
+            "us": round(statistics.median(e[0].elapsed_time(e[1]) for e in evc) * 1e3, 2), "launches": 3,
+            "partial_bytes_per_shard_and_row": 96 * 512 * 2 + 96 * 4,
+            "max_abs_vs_unsharded": round(diff, 5)}
 
     # ---- end to end through the public call, host buffers, copies inside the timed region
     e2e_ms = []

@@ -48,7 +48,7 @@ EXPORTS = ["dsa_api_version", "dsa_status_string", "dsa_last_cuda_error", "dsa_k
            "dsa_translate_pages", "dsa_index_scores",
            "dsa_topk_workspace_size", "dsa_topk", "dsa_topk_noalloc", "dsa_topk_force_multipass",
            "dsa_dcp_topk_workspace_size", "dsa_dcp_topk", "sparse_mla_workspace_size",
-           "sparse_mla_decode",
+           "sparse_mla_decode", "dsa_dcp_sparse_mla_workspace_size", "dsa_dcp_sparse_mla",
            "dsa_workspace_size", "dsa_decode_step", "dsa_cache_append", "dsa_quantize_index_query",
            "dsa_selftest_wait_timeout"]
 
@@ -78,6 +78,8 @@ def lib():
             "dsa_dcp_topk": (i32, [P, i64, P, i32, i32, i32, i32, P, P, P, sz, P, P]),
             "sparse_mla_workspace_size": (sz, [i32, i32]),
             "sparse_mla_decode": (i32, [pc, pb, P, P, i32, f32, P, P, P, sz, P, P]),
+            "dsa_dcp_sparse_mla_workspace_size": (sz, [i32, i32, i32]),
+            "dsa_dcp_sparse_mla": (i32, [pc, pb, P, P, i32, i32, f32, P, P, P, P, P, sz, P, P]),
             "dsa_workspace_size": (sz, [pb, i32]),
             "dsa_decode_step": (i32, [pc, pb, P, P, P, i32, f32, P, P, P, i64, P, P, sz, P, P]),
             "dsa_cache_append": (i32, [pc, pb, P, P, P, P]),
@@ -220,6 +222,23 @@ def sparse_mla_decode(cache: PagedCache, batch: Batch, q_mla, idx, sm_scale: flo
                                    float(sm_scale), _ptr(out), _ptr(lse), _ptr(workspace),
                                    workspace.numel() * workspace.element_size(), _ptr(status), _stream(stream)),
            "sparse_mla_decode")
+
+
+def dcp_sparse_mla_workspace_size(rows: int, k: int, shards: int) -> int:
+    return int(lib().dsa_dcp_sparse_mla_workspace_size(rows, k, shards))
+
+
+def dcp_sparse_mla(cache: PagedCache, batch: Batch, q_mla, idx, shards: int, sm_scale: float, out, lse, workspace,
+                   status, part_out=None, part_lse=None, stream=None):
+    """Sparse MLA as `shards` token shards would compute it: per-shard partial attention over the selected
+    tokens each holds, bf16 partial outputs and fp32 LSEs, merged through their log-sum-exp.  part_out
+    (bf16 [shards, rows, 96, 512]) and part_lse (fp32 [shards, rows, 96]) optionally receive the partials."""
+    c, b = cache.struct(), batch.struct()
+    _check(lib().dsa_dcp_sparse_mla(ctypes.byref(c), ctypes.byref(b), _ptr(q_mla), _ptr(idx), int(idx.shape[1]),
+                                    int(shards), float(sm_scale), _ptr(out), _ptr(lse), _ptr(part_out),
+                                    _ptr(part_lse), _ptr(workspace), workspace.numel() * workspace.element_size(),
+                                    _ptr(status), _stream(stream)),
+           "dsa_dcp_sparse_mla")
 
 
 def workspace_size(batch: Batch, k: int) -> int:

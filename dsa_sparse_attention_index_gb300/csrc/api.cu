@@ -218,6 +218,31 @@ dsa_status_t dsa_dcp_topk(const float* scores, int64_t ld_scores, const int32_t*
                          dev_status, static_cast<cudaStream_t>(stream));
 }
 
+size_t dsa_dcp_sparse_mla_workspace_size(int32_t rows, int32_t k, int32_t shards) {
+  if (rows < 0 || k < 1 || k > DSA_MAX_TOPK || shards < 1 || shards > DSA_DCP_MAX_SHARDS) return 0;
+  return dcp_mla_workspace_bytes(rows, k, shards);
+}
+
+dsa_status_t dsa_dcp_sparse_mla(const dsa_paged_cache_t* cache, const dsa_batch_t* batch, const uint16_t* q_mla,
+                                const int32_t* idx, int32_t k, int32_t shards, float sm_scale, uint16_t* out,
+                                float* lse, uint16_t* part_out, float* part_lse, void* workspace,
+                                size_t workspace_bytes, int32_t* dev_status, void* stream) {
+  dsa_status_t s;
+  if ((s = check_cache(cache)) != DSA_OK) return s;
+  if ((s = check_batch(batch)) != DSA_OK) return s;
+  if (k < 1 || k > DSA_MAX_TOPK || shards < 1 || !dev_status) return DSA_ERR_INVALID_ARG;
+  if (shards > DSA_DCP_MAX_SHARDS) return DSA_ERR_UNSUPPORTED;
+  const int rows = batch->batch * batch->queries_per_seq;
+  if (rows == 0) return DSA_OK;
+  if (!q_mla || !idx || !out || !lse || !aligned(q_mla, 16) || !aligned(out, 8) ||
+      (part_out && !aligned(part_out, 8)))
+    return DSA_ERR_INVALID_ARG;
+  if (!workspace || !aligned(workspace, 256) || workspace_bytes < dcp_mla_workspace_bytes(rows, k, shards))
+    return DSA_ERR_WORKSPACE;
+  return launch_dcp_sparse_mla(*cache, *batch, q_mla, idx, k, shards, sm_scale, out, lse, part_out, part_lse,
+                               workspace, dev_status, static_cast<cudaStream_t>(stream));
+}
+
 size_t sparse_mla_workspace_size(int32_t rows, int32_t k) {
   if (rows < 0 || k < 1 || k > DSA_MAX_TOPK) return 0;
   return mla_workspace_bytes(rows, k);

@@ -324,6 +324,166 @@ __global__ void __launch_bounds__(kDcpThreads, 1)
   grid_dep_launch();
 }
 
+
+// ---------------------------------------------------------------- LSE combine
+// The second half of the DCP exchange (same section): every shard attends
+// only over the selected tokens it holds, and the shards' partial outputs are
+// merged through their log-sum-exp.  Emulated here with the shard's token
+// groups as chunks of the MLA kernel:
+//   1. dcp_group_kernel, one CTA per row: the row's selected indices grouped
+//      by shard (t mod W), in their original order inside a shard, each
+//      shard's group cut into P pieces of at most the MLA kernel's chunk;
+//   2. the MLA kernel over those pieces (unnormalised partials, max and sums);
+//   3. dcp_combine_kernel: per shard, the output it would send (its pieces
+//      merged: bf16 O_r and fp32 LSE_r, the exchanged format), then the LSE
+//      combine of the W shards from those rounded values.
+
+// Selected indices of row `row` grouped by shard; seg[row][r * P + j] is where
+// piece j of shard r starts in gidx[row], seg[row][W * P] the number of
+// entries >= 0; the rest of gidx[row] is -1.
+__global__ void __launch_bounds__(kDcpThreads) dcp_group_kernel(const int32_t* __restrict__ idx, int k, int W,
+                                                                int P, int32_t* __restrict__ gidx,
+                                                                int32_t* __restrict__ seg) {
+  __shared__ uint32_t sh[32];
+  constexpr int kPer = (kMaxTopk + kDcpThreads - 1) / kDcpThreads;
+  const int row = blockIdx.x;
+  const int per = (k + kDcpThreads - 1) / kDcpThreads;
+  const int i0 = (int)threadIdx.x * per;
+  int32_t t[kPer];
+#pragma unroll
+  for (int j = 0; j < kPer; ++j) t[j] = (j < per && i0 + j < k) ? idx[(int64_t)row * k + i0 + j] : -1;
+  int32_t* g = gidx + (int64_t)row * k;
+  int32_t* sg = seg + (int64_t)row * (W * P + 1);
+  uint32_t base = 0;
+  for (int r = 0; r < W; ++r) {
+    uint32_t c = 0;
+#pragma unroll
+    for (int j = 0; j < kPer; ++j) c += (t[j] >= 0 && t[j] % W == r) ? 1u : 0u;
+    uint32_t n;
+    uint32_t pos = base + dcp_block_scan(c, sh, n);
+#pragma unroll
+    for (int j = 0; j < kPer; ++j)
+      if (t[j] >= 0 && t[j] % W == r) g[pos++] = t[j];
+    if (threadIdx.x == 0) {
+      const uint32_t q = (n + (uint32_t)P - 1) / (uint32_t)P;
+      for (int j = 0; j < P; ++j) sg[r * P + j] = (int32_t)(base + min(n, (uint32_t)j * q));
+    }
+    base += n;
+  }
+  for (int i = (int)base + (int)threadIdx.x; i < k; i += kDcpThreads) g[i] = -1;
+  if (threadIdx.x == 0) sg[W * P] = (int32_t)base;
+}
+
+__device__ __forceinline__ float dcp_ex2(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+
+constexpr int kDcpCombineHeads = 8;
+constexpr int kDcpMaxPieces = 16;
+
+// Per (row, 8 heads): each shard's output from its pieces, as the MLA's own
+// chunk merge forms it (max, weights 2^(m - M), output normalised by the sum of
+// the rounded probabilities, LSE from the exact sum), rounded to bf16; then
+// out = sum_r 2^(LSE_r - LSE) * O_r with LSE = log2 sum_r 2^LSE_r (log2 units
+// inside, natural log stored).  part_out / part_lse (nullable) receive the
+// shards' outputs, [W][rows][96][512] bf16 and [W][rows][96] fp32.
+template <int P>
+__global__ void __launch_bounds__(256) dcp_combine_kernel(const float* __restrict__ opart,
+                                                           const float* __restrict__ ml, int W, int rows,
+                                                           float latent_scale, uint16_t* __restrict__ out,
+                                                           float* __restrict__ lse, uint16_t* __restrict__ part_out,
+                                                           float* __restrict__ part_lse) {
+  const int row = blockIdx.y, h0 = blockIdx.x * kDcpCombineHeads;
+  const int nseg = W * P;
+  __shared__ float wgt[kDcpCombineHeads][kDcpMaxPieces];      // a piece's weight inside its shard
+  __shared__ float swt[kDcpCombineHeads][DSA_DCP_MAX_SHARDS];  // a shard's weight in the output
+  grid_dep_wait();  // the partials come from the previous kernel
+  const float4* mlr = reinterpret_cast<const float4*>(ml) + (int64_t)row * nseg * kHeads;
+  constexpr float kLn2 = 0.69314718055994531f;
+  if (threadIdx.x < kDcpCombineHeads) {
+    const int hl = threadIdx.x, h = h0 + hl;
+    float lse2[DSA_DCP_MAX_SHARDS];
+    float G = -INFINITY;
+#pragma unroll
+    for (int r = 0; r < DSA_DCP_MAX_SHARDS; ++r) {
+      lse2[r] = -INFINITY;
+      if (r >= W) continue;
+      float M = -INFINITY;
+      for (int j = 0; j < P; ++j) M = fmaxf(M, mlr[(r * P + j) * kHeads + h].x);
+      float den = 0.f, ex = 0.f;
+      for (int j = 0; j < P; ++j) {
+        const float4 v = mlr[(r * P + j) * kHeads + h];
+        const float w = (M == -INFINITY || v.x == -INFINITY) ? 0.f : dcp_ex2(v.x - M);
+        den += w * v.y;
+        ex += w * v.z;
+        wgt[hl][r * P + j] = w;
+      }
+      const float inv = den > 0.f ? latent_scale / den : 0.f;
+      for (int j = 0; j < P; ++j) wgt[hl][r * P + j] *= inv;
+      lse2[r] = (M == -INFINITY || ex <= 0.f) ? -INFINITY : M + log2f(ex);
+      G = fmaxf(G, lse2[r]);
+      if (part_lse) part_lse[((int64_t)r * rows + row) * kHeads + h] = lse2[r] * kLn2;
+    }
+    float U = 0.f;
+#pragma unroll
+    for (int r = 0; r < DSA_DCP_MAX_SHARDS; ++r) {
+      const float u = (lse2[r] == -INFINITY) ? 0.f : dcp_ex2(lse2[r] - G);  // 0 past the W shards
+      swt[hl][r] = u;
+      U += u;
+    }
+    const float invU = U > 0.f ? 1.f / U : 0.f;
+#pragma unroll
+    for (int r = 0; r < DSA_DCP_MAX_SHARDS; ++r) swt[hl][r] *= invU;
+    lse[(int64_t)row * kHeads + h] = (G == -INFINITY) ? -INFINITY : (G + log2f(U)) * kLn2;
+  }
+  __syncthreads();
+  constexpr int kVec = kDcpCombineHeads * kValue / 4;  // 1024 float4s per CTA
+  for (int v = threadIdx.x; v < kVec; v += blockDim.x) {
+    const int hl = v / (kValue / 4), d = (v % (kValue / 4)) * 4;
+    const float* src = opart + ((int64_t)row * nseg * kHeads + h0 + hl) * kValue + d;
+    // an empty piece wrote no partial: only pieces with weight are read
+    float4 x[DSA_DCP_MAX_SHARDS * P];
+#pragma unroll
+    for (int s = 0; s < DSA_DCP_MAX_SHARDS * P; ++s)
+      if (s < nseg && wgt[hl][s] != 0.f) x[s] = *reinterpret_cast<const float4*>(src + (int64_t)s * kHeads * kValue);
+    float4 a = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+    for (int r = 0; r < DSA_DCP_MAX_SHARDS; ++r) {
+      if (r >= W) break;
+      float4 o = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+      for (int j = 0; j < P; ++j) {
+        const int s = r * P + j;
+        const float w = wgt[hl][s];
+        if (w != 0.f) {
+          o.x = fmaf(w, x[s].x, o.x); o.y = fmaf(w, x[s].y, o.y);
+          o.z = fmaf(w, x[s].z, o.z); o.w = fmaf(w, x[s].w, o.w);
+        }
+      }
+      const __nv_bfloat162 lo = __floats2bfloat162_rn(o.x, o.y);
+      const __nv_bfloat162 hi = __floats2bfloat162_rn(o.z, o.w);
+      if (part_out) {
+        uint2 pk;
+        pk.x = *reinterpret_cast<const uint32_t*>(&lo);
+        pk.y = *reinterpret_cast<const uint32_t*>(&hi);
+        *reinterpret_cast<uint2*>(part_out + (((int64_t)r * rows + row) * kHeads + h0 + hl) * kValue + d) = pk;
+      }
+      const float2 l2 = __bfloat1622float2(lo), h2 = __bfloat1622float2(hi);
+      const float u = swt[hl][r];
+      a.x = fmaf(u, l2.x, a.x); a.y = fmaf(u, l2.y, a.y);
+      a.z = fmaf(u, h2.x, a.z); a.w = fmaf(u, h2.y, a.w);
+    }
+    const __nv_bfloat162 lo = __floats2bfloat162_rn(a.x, a.y);
+    const __nv_bfloat162 hi = __floats2bfloat162_rn(a.z, a.w);
+    uint2 pk;
+    pk.x = *reinterpret_cast<const uint32_t*>(&lo);
+    pk.y = *reinterpret_cast<const uint32_t*>(&hi);
+    *reinterpret_cast<uint2*>(out + ((int64_t)row * kHeads + h0 + hl) * kValue + d) = pk;
+  }
+}
+
 }  // namespace
 
 size_t dcp_workspace_bytes(int rows, int k, int shards) {
@@ -388,6 +548,59 @@ dsa_status_t launch_dcp_topk(const float* scores, int64_t ld, const int32_t* row
                                                          ws, status);
   dcp_merge_kernel<<<rows, kDcpThreads, smem2, st>>>(row_lens, max_row_len, k, W, true, len_cap, m_cap, ws, out,
                                                      stats, status);
+  return launch_status();
+}
+
+// Pieces per shard: a shard may hold all k selected tokens, and a piece is at
+// most one MLA chunk.
+static int dcp_pieces(int k) { return (k + mla_max_chunk() - 1) / mla_max_chunk(); }
+
+size_t dcp_mla_workspace_bytes(int rows, int k, int shards) {
+  auto al = [](size_t x) { return (x + 255) & ~size_t(255); };
+  const size_t nseg = (size_t)shards * dcp_pieces(k);
+  return al((size_t)rows * k * 4) + al((size_t)rows * (nseg + 1) * 4) + al((size_t)rows * nseg * kHeads * kValue * 4) +
+         al((size_t)rows * nseg * kHeads * 16);
+}
+
+dsa_status_t launch_dcp_sparse_mla(const dsa_paged_cache_t& c, const dsa_batch_t& bt, const uint16_t* q_mla,
+                                   const int32_t* idx, int k, int shards, float sm_scale, uint16_t* out, float* lse,
+                                   uint16_t* part_out, float* part_lse, void* workspace, int32_t* status,
+                                   cudaStream_t st) {
+  const int rows = bt.batch * bt.queries_per_seq;
+  if (rows == 0) return DSA_OK;
+  const int W = shards, P = dcp_pieces(k), nseg = W * P;
+  if (P > 2) return DSA_ERR_UNSUPPORTED;  // k <= 2,048 and chunks of 1,024 tokens
+  auto al = [](size_t x) { return (x + 255) & ~size_t(255); };
+  uint8_t* w = static_cast<uint8_t*>(workspace);
+  int32_t* gidx = reinterpret_cast<int32_t*>(w);
+  w += al((size_t)rows * k * 4);
+  int32_t* seg = reinterpret_cast<int32_t*>(w);
+  w += al((size_t)rows * (nseg + 1) * 4);
+  float* opart = reinterpret_cast<float*>(w);
+  w += al((size_t)rows * nseg * kHeads * kValue * 4);
+  float* ml = reinterpret_cast<float*>(w);
+  count_launches(1);
+  dcp_group_kernel<<<rows, kDcpThreads, 0, st>>>(idx, k, W, P, gidx, seg);
+  dsa_status_t s = launch_status();
+  if (s != DSA_OK) return s;
+  s = launch_sparse_mla_partials(c, bt, q_mla, gidx, k, seg, nseg, sm_scale, opart, ml, status, st);
+  if (s != DSA_OK) return s;
+  cudaLaunchAttribute attrs[1];
+  attrs[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attrs[0].val.programmaticStreamSerializationAllowed = 1;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(kHeads / kDcpCombineHeads, (unsigned)rows);
+  cfg.blockDim = dim3(256);
+  cfg.stream = st;
+  cfg.attrs = attrs;
+  cfg.numAttrs = 1;
+  count_launches(1);
+  const cudaError_t e =
+      P == 1 ? cudaLaunchKernelEx(&cfg, dcp_combine_kernel<1>, (const float*)opart, (const float*)ml, W, rows,
+                                  c.latent_scale, out, lse, part_out, part_lse)
+             : cudaLaunchKernelEx(&cfg, dcp_combine_kernel<2>, (const float*)opart, (const float*)ml, W, rows,
+                                  c.latent_scale, out, lse, part_out, part_lse);
+  if (cuda_status(e) != DSA_OK) return DSA_ERR_CUDA;
   return launch_status();
 }
 

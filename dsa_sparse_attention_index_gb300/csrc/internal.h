@@ -47,7 +47,22 @@ size_t dcp_workspace_bytes(int rows, int k, int shards);
 dsa_status_t launch_dcp_topk(const float* scores, int64_t ld, const int32_t* row_lens, int rows, int max_row_len,
                              int k, int shards, int32_t* out, int32_t* stats, void* workspace, int32_t* status,
                              cudaStream_t st);
+// Decode-context-parallel sparse MLA: per-shard partial attention and the LSE combine.
+size_t dcp_mla_workspace_bytes(int rows, int k, int shards);
+dsa_status_t launch_dcp_sparse_mla(const dsa_paged_cache_t& c, const dsa_batch_t& bt, const uint16_t* q_mla,
+                                   const int32_t* idx, int k, int shards, float sm_scale, uint16_t* out, float* lse,
+                                   uint16_t* part_out, float* part_lse, void* workspace, int32_t* status,
+                                   cudaStream_t st);
 size_t mla_workspace_bytes(int rows, int k);
+// Tokens of idx one MLA chunk may hold.
+int mla_max_chunk();
+// The MLA kernel alone over per-row chunk tables: nseg chunks per row,
+// boundaries seg[row][0..nseg] in idx[row], each at most mla_max_chunk()
+// tokens; unnormalised partials to opart [rows][nseg][96][512] and (max, sum
+// of rounded p, sum of p) to ml [rows][nseg][96][4].
+dsa_status_t launch_sparse_mla_partials(const dsa_paged_cache_t& c, const dsa_batch_t& bt, const uint16_t* q_mla,
+                                        const int32_t* idx, int k, const int32_t* seg, int nseg, float sm_scale,
+                                        float* opart, float* ml, int32_t* status, cudaStream_t st);
 dsa_status_t launch_sparse_mla(const dsa_paged_cache_t& c, const dsa_batch_t& bt, const uint16_t* q_mla,
                                const int32_t* idx, int k, float sm_scale, uint16_t* out, float* lse,
                                void* workspace, int32_t* status, cudaStream_t st);

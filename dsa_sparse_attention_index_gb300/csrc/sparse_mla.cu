@@ -109,6 +109,10 @@ struct MlaParams {
   float latent_scale;
   uint16_t* out;    // bf16 [rows][96][512]
   float* lse;       // [rows][96]
+  // chunk boundaries per row, [rows][nsplit + 1] offsets into idx[row] (chunk
+  // `split` is [seg[split], seg[split + 1]), at most `chunk` long), or null:
+  // chunk `split` is [split * chunk, (split + 1) * chunk)
+  const int32_t* seg;
 };
 
 __device__ __forceinline__ float ex2(float x) {
@@ -162,9 +166,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     len = len < 0 ? 0 : (len > p.cap ? p.cap : len);
     return visible_len(len, p.nq, row % p.nq);
   }();
-  const int c0 = split * p.chunk;
-  const int count = max(0, min(p.chunk, p.k - c0));
-  const int ntiles = (count + kTileTok - 1) / kTileTok;
+  int c0 = split * p.chunk;
+  int count = max(0, min(p.chunk, p.k - c0));
 
   if (threadIdx.x == 0) {
     mbar_init(q_full, 1);
@@ -190,6 +193,12 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
   grid_dep_wait();    // the indices come from the previous kernel
   grid_dep_launch();
+  if (p.seg) {
+    const int32_t* sg = p.seg + (int64_t)row * (p.nsplit + 1) + split;
+    c0 = min(max(sg[0], 0), p.k);
+    count = max(0, min(min(sg[1] - c0, p.chunk), p.k - c0));
+  }
+  const int ntiles = (count + kTileTok - 1) / kTileTok;
   // physical slots of the chunk's latent rows, block row * 64 + slot (-1: a -1
   // index or padding)
   for (int i = threadIdx.x; i < ntiles * kTileTok; i += kThreads) {
@@ -654,20 +663,89 @@ size_t mla_workspace_bytes(int rows, int k) {
   return al(parts * kHeads * kValue * 4) + al(parts * kHeads * 16);
 }
 
+namespace {
+
+// The Q tensor map and the kernel's parameters for `rows` query rows and
+// `nsplit` chunks of `chunk` tokens; false if the tensor map cannot be made or
+// the shared-memory size cannot be set.
+bool mla_setup(const dsa_paged_cache_t& c, const dsa_batch_t& bt, const uint16_t* q_mla, const int32_t* idx, int k,
+               int chunk, int nsplit, float sm_scale, float* opart, float* ml, uint16_t* out, float* lse,
+               int32_t* status, CUtensorMap* qmap, MlaParams* p) {
+  const int rows = bt.batch * bt.queries_per_seq;
+  const uint64_t dims[2] = {(uint64_t)kLatent, (uint64_t)rows * kHeads};
+  const uint64_t strides[1] = {(uint64_t)kLatent * 2};
+  const uint32_t box[2] = {64, (uint32_t)kHeads};
+  if (!encode_tmap(qmap, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, q_mla, dims, strides, box, CU_TENSOR_MAP_SWIZZLE_128B))
+    return false;
+  *p = MlaParams{static_cast<const uint8_t*>(c.base) + c.latent_off,
+                 c.row_stride,
+                 c.num_blocks,
+                 bt.block_table,
+                 bt.max_blocks_per_seq,
+                 bt.seq_lens,
+                 bt.queries_per_seq,
+                 std::min(bt.max_blocks_per_seq * kBlock, bt.max_seq_len),
+                 idx,
+                 k,
+                 chunk,
+                 nsplit,
+                 sm_scale * c.latent_scale * 1.4426950408889634f,
+                 q_mla,
+                 opart,
+                 ml,
+                 status,
+                 0,
+                 c.latent_scale,
+                 out,
+                 lse,
+                 nullptr};
+  static bool attr_set[64] = {};
+  int dev = 0;
+  cudaGetDevice(&dev);
+  if (dev < 64 && !attr_set[dev]) {
+    if (cuda_status(cudaFuncSetAttribute(sparse_mla_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         (int)kSmemBytes)) != DSA_OK)
+      return false;
+    attr_set[dev] = true;
+  }
+  return true;
+}
+
+}  // namespace
+
+int mla_max_chunk() { return kMaxChunk; }
+
+dsa_status_t launch_sparse_mla_partials(const dsa_paged_cache_t& c, const dsa_batch_t& bt, const uint16_t* q_mla,
+                                        const int32_t* idx, int k, const int32_t* seg, int nseg, float sm_scale,
+                                        float* opart, float* ml, int32_t* status, cudaStream_t st) {
+  const int rows = bt.batch * bt.queries_per_seq;
+  if (rows == 0) return DSA_OK;
+  if (nseg < 1 || nseg > kMaxSplit) return DSA_ERR_UNSUPPORTED;
+  CUtensorMap qmap;
+  MlaParams p;
+  if (!mla_setup(c, bt, q_mla, idx, k, kMaxChunk, nseg, sm_scale, opart, ml, nullptr, nullptr, status, &qmap, &p))
+    return DSA_ERR_CUDA;
+  p.seg = seg;
+  cudaLaunchAttribute attrs[1];
+  attrs[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attrs[0].val.programmaticStreamSerializationAllowed = 1;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3((unsigned)nseg, (unsigned)rows);
+  cfg.blockDim = dim3(kThreads);
+  cfg.dynamicSmemBytes = kSmemBytes;
+  cfg.stream = st;
+  cfg.attrs = attrs;
+  cfg.numAttrs = 1;
+  count_launches(1);
+  if (cuda_status(cudaLaunchKernelEx(&cfg, sparse_mla_kernel, qmap, p)) != DSA_OK) return DSA_ERR_CUDA;
+  return launch_status();
+}
+
 dsa_status_t launch_sparse_mla(const dsa_paged_cache_t& c, const dsa_batch_t& bt, const uint16_t* q_mla,
                                const int32_t* idx, int k, float sm_scale, uint16_t* out, float* lse,
                                void* workspace, int32_t* status, cudaStream_t st) {
   const int rows = bt.batch * bt.queries_per_seq;
   if (rows == 0) return DSA_OK;
-  CUtensorMap qmap;
-  {
-    const uint64_t dims[2] = {(uint64_t)kLatent, (uint64_t)rows * kHeads};
-    const uint64_t strides[1] = {(uint64_t)kLatent * 2};
-    const uint32_t box[2] = {64, (uint32_t)kHeads};
-    if (!encode_tmap(&qmap, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, q_mla, dims, strides, box,
-                     CU_TENSOR_MAP_SWIZZLE_128B))
-      return DSA_ERR_CUDA;
-  }
   const int nsplit0 = mla_nsplit(rows, k);
   const int tiles = (k + kTileTok - 1) / kTileTok;
   const int chunk = ((tiles + nsplit0 - 1) / nsplit0) * kTileTok;
@@ -676,36 +754,10 @@ dsa_status_t launch_sparse_mla(const dsa_paged_cache_t& c, const dsa_batch_t& bt
   float* opart = static_cast<float*>(workspace);
   float* ml = reinterpret_cast<float*>(static_cast<uint8_t*>(workspace) +
                                        al((size_t)rows * mla_nsplit_max(rows, k) * kHeads * kValue * 4));
-  MlaParams p{static_cast<const uint8_t*>(c.base) + c.latent_off,
-              c.row_stride,
-              c.num_blocks,
-              bt.block_table,
-              bt.max_blocks_per_seq,
-              bt.seq_lens,
-              bt.queries_per_seq,
-              std::min(bt.max_blocks_per_seq * kBlock, bt.max_seq_len),
-              idx,
-              k,
-              chunk,
-              nsplit,
-              sm_scale * c.latent_scale * 1.4426950408889634f,
-              q_mla,
-              opart,
-              ml,
-              status,
-              0,
-              c.latent_scale,
-              out,
-              lse};
-  static bool attr_set[64] = {};
-  int dev = 0;
-  cudaGetDevice(&dev);
-  if (dev < 64 && !attr_set[dev]) {
-    if (cuda_status(cudaFuncSetAttribute(sparse_mla_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         (int)kSmemBytes)) != DSA_OK)
-      return DSA_ERR_CUDA;
-    attr_set[dev] = true;
-  }
+  CUtensorMap qmap;
+  MlaParams p;
+  if (!mla_setup(c, bt, q_mla, idx, k, chunk, nsplit, sm_scale, opart, ml, out, lse, status, &qmap, &p))
+    return DSA_ERR_CUDA;
   // Up to kMaxFusedSplit chunks per row: the row's CTAs form a cluster and
   // merge the chunks themselves; more chunks take the combine kernel.
   p.fuse = nsplit <= kMaxFusedSplit && fused_cluster_ok(nsplit) ? 1 : 0;

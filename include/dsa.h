@@ -54,7 +54,7 @@ extern "C" {
 #define DSA_MAX_TOPK 2048        /* top-k of the model; also the largest k accepted */
 #define DSA_MAX_QUERIES_PER_SEQ 2048 /* draft rows (1..4) or a prefill chunk (a multiple of 4) */
 #define DSA_TOPK_NOALLOC_MAX_ROWS 64  /* row limit of dsa_topk_noalloc */
-#define DSA_DCP_MAX_SHARDS 8          /* shards of dsa_dcp_topk */
+#define DSA_DCP_MAX_SHARDS 8          /* shards of dsa_dcp_topk and dsa_dcp_sparse_mla */
 #define DSA_DCP_MAX_SHARD_TOKENS 65536 /* tokens of one row a shard may hold (16-bit local position) */
 
 typedef enum dsa_status {
@@ -250,6 +250,33 @@ dsa_status_t sparse_mla_decode(const dsa_paged_cache_t* cache, const dsa_batch_t
                                float sm_scale, uint16_t* out, float* lse,
                                void* workspace, size_t workspace_bytes,
                                int32_t* dev_status, void* stream);
+
+/*
+ * Decode context parallelism, the partial-attention exchange (Day-0 post,
+ * decode-context-parallelism section: each GPU attends over its own token
+ * shard and the partial outputs are merged through their log-sum-exp),
+ * emulated on one GPU with `shards` = W token shards; shard r holds the
+ * tokens t with t mod W = r.  For row r and head h, with S_w the entries of
+ * idx[r] that are >= 0 and held by shard w:
+ *   O_w, LSE_w = the sparse MLA output and LSE over S_w alone (as
+ *                sparse_mla_decode defines them), O_w rounded to bf16: what
+ *                shard w sends (O_w = 0, LSE_w = -inf for an empty S_w)
+ *   lse[r][h]  = ln sum_w exp(LSE_w)
+ *   out[r][h]  = sum_w exp(LSE_w - lse[r][h]) * O_w      (bf16, round-to-nearest)
+ * This is sparse_mla_decode's result up to the rounding of the O_w to bf16.
+ *   cache, batch, q_mla, idx, k, sm_scale, out, lse as for sparse_mla_decode
+ *   shards    1 .. DSA_DCP_MAX_SHARDS, else DSA_ERR_UNSUPPORTED
+ *   part_out  device bf16 bits [shards][rows][96][512] or NULL: the O_w
+ *   part_lse  device fp32 [shards][rows][96] or NULL: the LSE_w
+ *   workspace >= dsa_dcp_sparse_mla_workspace_size(rows, k, shards) bytes, 256-B aligned
+ * Three launches: grouping of the indices by shard, the MLA kernel over the
+ * shards' token groups, and the combine.
+ */
+size_t dsa_dcp_sparse_mla_workspace_size(int32_t rows, int32_t k, int32_t shards);
+dsa_status_t dsa_dcp_sparse_mla(const dsa_paged_cache_t* cache, const dsa_batch_t* batch, const uint16_t* q_mla,
+                                const int32_t* idx, int32_t k, int32_t shards, float sm_scale, uint16_t* out,
+                                float* lse, uint16_t* part_out, float* part_lse, void* workspace,
+                                size_t workspace_bytes, int32_t* dev_status, void* stream);
 
 /*
  * The fused decode step: page translation, indexer, top-k and sparse MLA on

@@ -74,6 +74,15 @@ def test_host_validation_without_device(lib):
                             None) == B.ERR_UNSUPPORTED
     assert lib.dsa_dcp_topk(None, 0, None, 1, 10, 2048, 0, None, None, None, 0, st, None) == B.ERR_INVALID_ARG
     assert lib.dsa_dcp_topk(128, 16, 256, 1, 10, 2048, 8, 512, None, None, 0, st, None) == B.ERR_WORKSPACE
+    # DCP LSE combine: 1..8 shards, aligned pointers, a workspace of the stated size
+    b.queries_per_seq = 1
+    dm = lambda shards, q, out, ws, n: lib.dsa_dcp_sparse_mla(ctypes.byref(c), ctypes.byref(b), q, 256, 2048, shards,
+                                                              1.0, out, 512, None, None, ws, n, st, None)
+    assert dm(9, 1024, 2048, None, 0) == B.ERR_UNSUPPORTED
+    assert dm(0, 1024, 2048, None, 0) == B.ERR_INVALID_ARG
+    assert dm(8, 1032, 2048, None, 0) == B.ERR_INVALID_ARG        # q_mla not 16-byte aligned
+    assert dm(8, 1024, 2052, None, 0) == B.ERR_INVALID_ARG        # out not 8-byte aligned
+    assert dm(8, 1024, 2048, 4096, 100) == B.ERR_WORKSPACE
 
 
 def test_workspace_sizes(lib):
@@ -88,3 +97,7 @@ def test_workspace_sizes(lib):
     assert lib.dsa_dcp_topk_workspace_size(32, 2048, 8) >= 32 * 8 * 2048 * 4
     assert lib.dsa_dcp_topk_workspace_size(4, 2048, 1) >= 4 * 3072 * 4
     assert lib.dsa_dcp_topk_workspace_size(4, 2048, 9) == 0
+    # DCP LSE combine: the grouped indices plus fp32 partials of 2 pieces per shard (k = 2048)
+    assert lib.dsa_dcp_sparse_mla_workspace_size(32, 2048, 8) >= 32 * 16 * 96 * 512 * 4 + 32 * 2048 * 4
+    assert lib.dsa_dcp_sparse_mla_workspace_size(4, 1024, 3) >= 4 * 3 * 96 * 512 * 4
+    assert lib.dsa_dcp_sparse_mla_workspace_size(4, 2048, 9) == 0
