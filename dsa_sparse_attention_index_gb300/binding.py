@@ -48,7 +48,7 @@ EXPORTS = ["dsa_api_version", "dsa_status_string", "dsa_last_cuda_error", "dsa_k
            "dsa_translate_pages", "dsa_index_scores",
            "dsa_topk_workspace_size", "dsa_topk", "dsa_topk_noalloc", "dsa_topk_force_multipass",
            "dsa_dcp_topk_workspace_size", "dsa_dcp_topk", "sparse_mla_workspace_size",
-           "sparse_mla_decode", "dsa_dcp_sparse_mla_workspace_size", "dsa_dcp_sparse_mla",
+           "sparse_mla_decode", "dsa_dcp_sparse_mla_workspace_size", "dsa_dcp_sparse_mla", "dsa_batch_invariant",
            "dsa_workspace_size", "dsa_decode_step", "dsa_cache_append", "dsa_quantize_index_query",
            "dsa_selftest_wait_timeout"]
 
@@ -79,6 +79,7 @@ def lib():
             "sparse_mla_workspace_size": (sz, [i32, i32]),
             "sparse_mla_decode": (i32, [pc, pb, P, P, i32, f32, P, P, P, sz, P, P]),
             "dsa_dcp_sparse_mla_workspace_size": (sz, [i32, i32, i32]),
+            "dsa_batch_invariant": (i32, [i32]),
             "dsa_dcp_sparse_mla": (i32, [pc, pb, P, P, i32, i32, f32, P, P, P, P, P, sz, P, P]),
             "dsa_workspace_size": (sz, [pb, i32]),
             "dsa_decode_step": (i32, [pc, pb, P, P, P, i32, f32, P, P, P, i64, P, P, sz, P, P]),
@@ -222,6 +223,11 @@ def sparse_mla_decode(cache: PagedCache, batch: Batch, q_mla, idx, sm_scale: flo
                                    float(sm_scale), _ptr(out), _ptr(lse), _ptr(workspace),
                                    workspace.numel() * workspace.element_size(), _ptr(status), _stream(stream)),
            "sparse_mla_decode")
+
+
+def batch_invariant(on: bool) -> bool:
+    """Switch the process-wide batch-invariant mode (fixed 512-token MLA chunks); returns the previous one."""
+    return bool(lib().dsa_batch_invariant(1 if on else 0))
 
 
 def dcp_sparse_mla_workspace_size(rows: int, k: int, shards: int) -> int:

@@ -243,6 +243,8 @@ dsa_status_t dsa_dcp_sparse_mla(const dsa_paged_cache_t* cache, const dsa_batch_
                                workspace, dev_status, static_cast<cudaStream_t>(stream));
 }
 
+int32_t dsa_batch_invariant(int32_t on) { return dsa::mla_batch_invariant(on); }
+
 size_t sparse_mla_workspace_size(int32_t rows, int32_t k) {
   if (rows < 0 || k < 1 || k > DSA_MAX_TOPK) return 0;
   return mla_workspace_bytes(rows, k);

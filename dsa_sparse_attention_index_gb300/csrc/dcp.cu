@@ -330,48 +330,56 @@ __global__ void __launch_bounds__(kDcpThreads, 1)
 // only over the selected tokens it holds, and the shards' partial outputs are
 // merged through their log-sum-exp.  Emulated here with the shard's token
 // groups as chunks of the MLA kernel:
-//   1. dcp_group_kernel, one CTA per row: the row's selected indices grouped
+//   1. dcp_group_kernel, one CTA per (shard, row): the row's selected indices grouped
 //      by shard (t mod W), in their original order inside a shard, each
-//      shard's group cut into P pieces of at most the MLA kernel's chunk;
+//      shard's group cut into P pieces of the MLA kernel's chunk (1,024
+//      tokens; P = 2 covers a shard that holds all 2,048);
 //   2. the MLA kernel over those pieces (unnormalised partials, max and sums);
 //   3. dcp_combine_kernel: per shard, the output it would send (its pieces
 //      merged: bf16 O_r and fp32 LSE_r, the exchanged format), then the LSE
 //      combine of the W shards from those rounded values.
 
-// Selected indices of row `row` grouped by shard; seg[row][r * P + j] is where
-// piece j of shard r starts in gidx[row], seg[row][W * P] the number of
-// entries >= 0; the rest of gidx[row] is -1.
+// Selected indices of a row grouped by shard, one CTA per (shard r, row):
+// seg[row][r * P + j] is where piece j of shard r starts in gidx[row],
+// seg[row][W * P] the number of entries >= 0; the rest of gidx[row] is -1.
+// Pieces are `piece` tokens long from the group's start, so a group of at
+// most `piece` tokens leaves its later pieces empty (their CTAs of the MLA
+// kernel return at once).  One block scan of packed counts places the group:
+// the low 16 bits count shard r's entries, the high 16 bits those of shards
+// below r (each at most 2,048, so no carry crosses).
 __global__ void __launch_bounds__(kDcpThreads) dcp_group_kernel(const int32_t* __restrict__ idx, int k, int W,
-                                                                int P, int32_t* __restrict__ gidx,
+                                                                int P, int piece, int32_t* __restrict__ gidx,
                                                                 int32_t* __restrict__ seg) {
   __shared__ uint32_t sh[32];
   constexpr int kPer = (kMaxTopk + kDcpThreads - 1) / kDcpThreads;
-  const int row = blockIdx.x;
+  const int r = blockIdx.x, row = blockIdx.y;
   const int per = (k + kDcpThreads - 1) / kDcpThreads;
   const int i0 = (int)threadIdx.x * per;
   int32_t t[kPer];
+  uint32_t c = 0;
 #pragma unroll
-  for (int j = 0; j < kPer; ++j) t[j] = (j < per && i0 + j < k) ? idx[(int64_t)row * k + i0 + j] : -1;
+  for (int j = 0; j < kPer; ++j) {
+    t[j] = (j < per && i0 + j < k) ? idx[(int64_t)row * k + i0 + j] : -1;
+    if (t[j] >= 0) {
+      const int s = t[j] % W;
+      c += s == r ? 1u : (s < r ? 0x10000u : 0u);
+    }
+  }
+  uint32_t tot;
+  const uint32_t e = dcp_block_scan(c, sh, tot);
+  const uint32_t base = tot >> 16, n = tot & 0xFFFFu;
   int32_t* g = gidx + (int64_t)row * k;
   int32_t* sg = seg + (int64_t)row * (W * P + 1);
-  uint32_t base = 0;
-  for (int r = 0; r < W; ++r) {
-    uint32_t c = 0;
+  uint32_t pos = base + (e & 0xFFFFu);
 #pragma unroll
-    for (int j = 0; j < kPer; ++j) c += (t[j] >= 0 && t[j] % W == r) ? 1u : 0u;
-    uint32_t n;
-    uint32_t pos = base + dcp_block_scan(c, sh, n);
-#pragma unroll
-    for (int j = 0; j < kPer; ++j)
-      if (t[j] >= 0 && t[j] % W == r) g[pos++] = t[j];
-    if (threadIdx.x == 0) {
-      const uint32_t q = (n + (uint32_t)P - 1) / (uint32_t)P;
-      for (int j = 0; j < P; ++j) sg[r * P + j] = (int32_t)(base + min(n, (uint32_t)j * q));
-    }
-    base += n;
+  for (int j = 0; j < kPer; ++j)
+    if (t[j] >= 0 && t[j] % W == r) g[pos++] = t[j];
+  if (threadIdx.x == 0)
+    for (int j = 0; j < P; ++j) sg[r * P + j] = (int32_t)(base + min(n, (uint32_t)(j * piece)));
+  if (r == W - 1) {  // the last group ends where the entries end: pad the rest
+    for (int i = (int)(base + n) + (int)threadIdx.x; i < k; i += kDcpThreads) g[i] = -1;
+    if (threadIdx.x == 0) sg[W * P] = (int32_t)(base + n);
   }
-  for (int i = (int)base + (int)threadIdx.x; i < k; i += kDcpThreads) g[i] = -1;
-  if (threadIdx.x == 0) sg[W * P] = (int32_t)base;
 }
 
 __device__ __forceinline__ float dcp_ex2(float x) {
@@ -580,7 +588,8 @@ dsa_status_t launch_dcp_sparse_mla(const dsa_paged_cache_t& c, const dsa_batch_t
   w += al((size_t)rows * nseg * kHeads * kValue * 4);
   float* ml = reinterpret_cast<float*>(w);
   count_launches(1);
-  dcp_group_kernel<<<rows, kDcpThreads, 0, st>>>(idx, k, W, P, gidx, seg);
+  dcp_group_kernel<<<dim3((unsigned)W, (unsigned)rows), kDcpThreads, 0, st>>>(idx, k, W, P, mla_max_chunk(), gidx,
+                                                                             seg);
   dsa_status_t s = launch_status();
   if (s != DSA_OK) return s;
   s = launch_sparse_mla_partials(c, bt, q_mla, gidx, k, seg, nseg, sm_scale, opart, ml, status, st);

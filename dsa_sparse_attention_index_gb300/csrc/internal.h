@@ -54,6 +54,8 @@ dsa_status_t launch_dcp_sparse_mla(const dsa_paged_cache_t& c, const dsa_batch_t
                                    uint16_t* part_out, float* part_lse, void* workspace, int32_t* status,
                                    cudaStream_t st);
 size_t mla_workspace_bytes(int rows, int k);
+// Process-wide batch-invariant mode of the MLA chunking; returns the previous setting.
+int mla_batch_invariant(int on);
 // Tokens of idx one MLA chunk may hold.
 int mla_max_chunk();
 // The MLA kernel alone over per-row chunk tables: nseg chunks per row,

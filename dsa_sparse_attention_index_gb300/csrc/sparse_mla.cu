@@ -35,6 +35,7 @@
 //     a combine kernel merges the chunks through their log-sum-exp (Day-0
 //     post, DCP section: partial outputs are combined by LSE).
 #include <algorithm>
+#include <atomic>
 #include <cmath>
 
 #include <cooperative_groups.h>
@@ -57,6 +58,7 @@ constexpr int kTileDBlockBytes = kTileTok * 128;       // 4,096
 constexpr int kTileBytes = kDBlocks * kTileDBlockBytes;  // 36,864
 constexpr int kPBytes = kHeads * kTileTok * 2;         // 6,144
 constexpr int kMaxChunk = 1024;                        // tokens per CTA
+constexpr int kInvariantChunk = 512;                   // tokens per CTA in the batch-invariant mode
 constexpr int kMaxSplit = 16;                          // chunks per row
 constexpr int kMaxFusedSplit = 8;                      // chunks combined inside the kernel (a portable cluster)
 // 12 warps: softmax 0-3, loaders 4-9, QK issuer 10, PV issuer 11.  Three warps
@@ -647,19 +649,30 @@ bool fused_cluster_ok(int nsplit) {
   return known[dev][nsplit] == 1;
 }
 
+namespace {
+std::atomic<int> g_batch_invariant{0};
+}  // namespace
+
+int mla_batch_invariant(int on) { return g_batch_invariant.exchange(on ? 1 : 0); }
+
 // Token chunks per row: enough CTAs for one wave over the SMs (one CTA per SM
-// fits), at most 16; the workspace is sized for up to 256 SMs.
-int mla_nsplit_max(int rows, int k) {
-  return std::max((k + kMaxChunk - 1) / kMaxChunk, std::min(16, 256 / std::max(1, rows)));
+// fits), at most 16; the workspace is sized for up to 256 SMs.  In the
+// batch-invariant mode the chunks are kInvariantChunk tokens whatever the
+// number of rows, so a row's arithmetic does not depend on its batch.
+static int mla_nsplit_max(int rows, int k, bool inv) {
+  const int n = std::max((k + kMaxChunk - 1) / kMaxChunk, std::min(16, 256 / std::max(1, rows)));
+  return inv ? std::max(n, (k + kInvariantChunk - 1) / kInvariantChunk) : n;
 }
-int mla_nsplit(int rows, int k) {
+static int mla_nsplit(int rows, int k, bool inv) {
+  if (inv) return (k + kInvariantChunk - 1) / kInvariantChunk;
   return std::max((k + kMaxChunk - 1) / kMaxChunk,
-                  std::min(mla_nsplit_max(rows, k), num_sms() / std::max(1, rows)));
+                  std::min(mla_nsplit_max(rows, k, false), num_sms() / std::max(1, rows)));
 }
+static bool batch_invariant() { return g_batch_invariant.load(std::memory_order_relaxed) != 0; }
 
 size_t mla_workspace_bytes(int rows, int k) {
   auto al = [](size_t x) { return (x + 255) & ~size_t(255); };
-  const size_t parts = (size_t)rows * mla_nsplit_max(rows, k);
+  const size_t parts = (size_t)rows * mla_nsplit_max(rows, k, batch_invariant());
   return al(parts * kHeads * kValue * 4) + al(parts * kHeads * 16);
 }
 
@@ -746,14 +759,15 @@ dsa_status_t launch_sparse_mla(const dsa_paged_cache_t& c, const dsa_batch_t& bt
                                void* workspace, int32_t* status, cudaStream_t st) {
   const int rows = bt.batch * bt.queries_per_seq;
   if (rows == 0) return DSA_OK;
-  const int nsplit0 = mla_nsplit(rows, k);
+  const bool inv = batch_invariant();  // read once: the split and the workspace layout agree
+  const int nsplit0 = mla_nsplit(rows, k, inv);
   const int tiles = (k + kTileTok - 1) / kTileTok;
   const int chunk = ((tiles + nsplit0 - 1) / nsplit0) * kTileTok;
   const int nsplit = (k + chunk - 1) / chunk;
   auto al = [](size_t x) { return (x + 255) & ~size_t(255); };
   float* opart = static_cast<float*>(workspace);
   float* ml = reinterpret_cast<float*>(static_cast<uint8_t*>(workspace) +
-                                       al((size_t)rows * mla_nsplit_max(rows, k) * kHeads * kValue * 4));
+                                       al((size_t)rows * mla_nsplit_max(rows, k, inv) * kHeads * kValue * 4));
   CUtensorMap qmap;
   MlaParams p;
   if (!mla_setup(c, bt, q_mla, idx, k, chunk, nsplit, sm_scale, opart, ml, out, lse, status, &qmap, &p))

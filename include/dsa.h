@@ -252,6 +252,22 @@ dsa_status_t sparse_mla_decode(const dsa_paged_cache_t* cache, const dsa_batch_t
                                int32_t* dev_status, void* stream);
 
 /*
+ * Batch-invariant mode (Day-0 post, section on RL without train/rollout
+ * mismatch: with batch-invariant kernels a token's log-prob does not depend
+ * on the batch it is computed in).  The indexer and the top-k already give
+ * each row the same result whatever the batch; the sparse MLA splits a row's
+ * tokens into chunks whose number depends on the number of rows (to fill the
+ * SMs), and the merge of the chunks rounds differently for a different split.
+ * on != 0 fixes the chunks at 512 tokens for every later call in this process
+ * (all threads and devices), so out and lse of a row are bitwise the same in
+ * any batch, at the cost of fewer CTAs for small batches.  The workspace
+ * sizes reported by sparse_mla_workspace_size and dsa_workspace_size follow
+ * the mode at the time of the query: set the mode first, and do not change it
+ * while other threads launch.  Returns the previous setting; never fails.
+ */
+int32_t dsa_batch_invariant(int32_t on);
+
+/*
  * Decode context parallelism, the partial-attention exchange (Day-0 post,
  * decode-context-parallelism section: each GPU attends over its own token
  * shard and the partial outputs are merged through their log-sum-exp),

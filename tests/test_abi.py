@@ -101,3 +101,10 @@ def test_workspace_sizes(lib):
     assert lib.dsa_dcp_sparse_mla_workspace_size(32, 2048, 8) >= 32 * 16 * 96 * 512 * 4 + 32 * 2048 * 4
     assert lib.dsa_dcp_sparse_mla_workspace_size(4, 1024, 3) >= 4 * 3 * 96 * 512 * 4
     assert lib.dsa_dcp_sparse_mla_workspace_size(4, 2048, 9) == 0
+    # batch-invariant mode: 512-token chunks, so the partials of 200 rows need 4 slots a row
+    assert lib.dsa_batch_invariant(1) == 0
+    try:
+        assert lib.sparse_mla_workspace_size(200, 2048) >= 200 * 4 * 96 * 512 * 4
+    finally:
+        assert lib.dsa_batch_invariant(0) == 1
+    assert lib.sparse_mla_workspace_size(200, 2048) < 200 * 4 * 96 * 512 * 4
