@@ -278,6 +278,37 @@ def main_ours(args):
     assert status.item() == 0, binding.status_string(status.item())
     st_ms = {kk: statistics.median(v) for kk, v in stage.items()}
 
+    # ---- the same step with bf16 scores between the indexer and the top-k: the
+    #      fused call, its two first stages, and how often the selection moves
+    b16 = None
+    if rank == 0:
+        ld16 = (case.max_len + 7) // 8 * 8
+        s16 = torch.empty((rows, ld16), dtype=torch.int16, device=dev)
+        idx16 = torch.empty((rows, k), dtype=torch.int32, device=dev)
+        evf = [[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(n_att)]
+        for e in evf:
+            flush.zero_()
+            e[0].record(stream)
+            binding.decode_step_bf16(dc.cache, dc.batch, dc.q_index, dc.head_w, dc.q_mla, k, case.sm_scale, out,
+                                     lse, ws, status, stream=stream)
+            e[1].record(stream)
+        evb = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(n_att)]
+        for e in evb:
+            flush.zero_()
+            e[0].record(stream)
+            binding.index_scores_bf16(dc.cache, dc.batch, dc.q_index, dc.head_w, s16, status, stream)
+            e[1].record(stream)
+            binding.topk_bf16(s16, dc.row_lens, case.max_len, k, idx16, status, stream)
+            e[2].record(stream)
+        torch.cuda.synchronize()
+        assert status.item() == 0, binding.status_string(status.item())
+        med = lambda evs, a, b_: round(statistics.median(e[a].elapsed_time(e[b_]) for e in evs) * 1e3, 2)
+        same = int((idx16 == idx).all(dim=1).sum().item())  # `idx` holds the fp32 selection of the same step
+        n_scores = int(case.row_lens().astype(np.int64).sum())
+        b16 = {"step_us": med(evf, 0, 1), "index_us": med(evb, 0, 1), "topk_us": med(evb, 1, 2),
+               "score_bytes_per_step": 2 * n_scores, "fp32_score_bytes_per_step": 4 * n_scores,
+               "rows_with_the_fp32_selection": same, "rows": rows}
+
     # ---- the decode-context-parallel top-k merge of 8 shards on the step's scores
     #      (L2-resident after the indexer, as in a step): time and words sent
     dcp = None
@@ -416,6 +447,7 @@ def main_ours(args):
         "roofline": roof,
         "gpu_launches": n_launches,
         "dcp_topk": dcp,
+        "bf16_scores": b16,
         "clocks": clocks,
         "wall_s_timed_region": round(t_wall, 4),
     }

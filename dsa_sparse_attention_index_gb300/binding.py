@@ -45,7 +45,8 @@ class BatchT(ctypes.Structure):
 _lib = None
 
 EXPORTS = ["dsa_api_version", "dsa_status_string", "dsa_last_cuda_error", "dsa_kernel_launches",
-           "dsa_translate_pages", "dsa_index_scores",
+           "dsa_translate_pages", "dsa_index_scores", "dsa_index_scores_bf16", "dsa_topk_bf16",
+           "dsa_decode_step_bf16",
            "dsa_topk_workspace_size", "dsa_topk", "dsa_topk_noalloc", "dsa_topk_force_multipass",
            "dsa_dcp_topk_workspace_size", "dsa_dcp_topk", "sparse_mla_workspace_size",
            "sparse_mla_decode", "dsa_dcp_sparse_mla_workspace_size", "dsa_dcp_sparse_mla", "dsa_batch_invariant",
@@ -83,6 +84,9 @@ def lib():
             "dsa_dcp_sparse_mla": (i32, [pc, pb, P, P, i32, i32, f32, P, P, P, P, P, sz, P, P]),
             "dsa_workspace_size": (sz, [pb, i32]),
             "dsa_decode_step": (i32, [pc, pb, P, P, P, i32, f32, P, P, P, i64, P, P, sz, P, P]),
+            "dsa_decode_step_bf16": (i32, [pc, pb, P, P, P, i32, f32, P, P, P, i64, P, P, sz, P, P]),
+            "dsa_index_scores_bf16": (i32, [pc, pb, P, P, P, i64, P, P]),
+            "dsa_topk_bf16": (i32, [P, i64, P, i32, i32, i32, P, P, P]),
             "dsa_cache_append": (i32, [pc, pb, P, P, P, P]),
             "dsa_quantize_index_query": (i32, [P, P, i32, P, P, P]),
             "dsa_selftest_wait_timeout": (i32, [i64, P, P]),
@@ -179,6 +183,20 @@ def index_scores(cache: PagedCache, batch: Batch, q_index, head_w, scores, statu
                                   int(scores.shape[1]), _ptr(status), _stream(stream)), "dsa_index_scores")
 
 
+def index_scores_bf16(cache: PagedCache, batch: Batch, q_index, head_w, scores, status, stream=None):
+    """Indexer scores rounded to bf16; `scores` holds the bits (int16 or bfloat16 [rows, ld], ld % 8 == 0)."""
+    c, b = cache.struct(), batch.struct()
+    _check(lib().dsa_index_scores_bf16(ctypes.byref(c), ctypes.byref(b), _ptr(q_index), _ptr(head_w), _ptr(scores),
+                                       int(scores.shape[1]), _ptr(status), _stream(stream)), "dsa_index_scores_bf16")
+
+
+def topk_bf16(scores, row_lens, max_row_len: int, k: int, idx_out, status, stream=None):
+    """Top-k over bf16 scores (bits [rows, ld], ld % 8 == 0); no workspace."""
+    rows = int(scores.shape[0])
+    _check(lib().dsa_topk_bf16(_ptr(scores), int(scores.shape[1]), _ptr(row_lens), rows, int(max_row_len), int(k),
+                               _ptr(idx_out), _ptr(status), _stream(stream)), "dsa_topk_bf16")
+
+
 def topk_workspace_size(rows: int, max_row_len: int, k: int) -> int:
     return int(lib().dsa_topk_workspace_size(rows, max_row_len, k))
 
@@ -260,6 +278,17 @@ def decode_step(cache: PagedCache, batch: Batch, q_index, head_w, q_mla, k: int,
                                  int(k), float(sm_scale), _ptr(out), _ptr(lse), _ptr(scores_out), ld,
                                  _ptr(idx_out), _ptr(workspace), workspace.numel() * workspace.element_size(),
                                  _ptr(status), _stream(stream)), "dsa_decode_step")
+
+
+def decode_step_bf16(cache: PagedCache, batch: Batch, q_index, head_w, q_mla, k: int, sm_scale: float, out, lse,
+                     workspace, status, scores_out=None, idx_out=None, stream=None):
+    """The fused step with bf16 scores between the indexer and the top-k."""
+    c, b = cache.struct(), batch.struct()
+    ld = int(scores_out.shape[1]) if scores_out is not None else 0
+    _check(lib().dsa_decode_step_bf16(ctypes.byref(c), ctypes.byref(b), _ptr(q_index), _ptr(head_w), _ptr(q_mla),
+                                      int(k), float(sm_scale), _ptr(out), _ptr(lse), _ptr(scores_out), ld,
+                                      _ptr(idx_out), _ptr(workspace), workspace.numel() * workspace.element_size(),
+                                      _ptr(status), _stream(stream)), "dsa_decode_step_bf16")
 
 
 def cache_append(cache: PagedCache, batch: Batch, new_latent, new_index_key, status, stream=None):

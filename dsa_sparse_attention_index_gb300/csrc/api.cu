@@ -92,7 +92,7 @@ dsa_status_t check_index_rows(const dsa_paged_cache_t* c, const dsa_batch_t* b) 
   return DSA_OK;
 }
 
-int64_t round_ld(int max_len) { return ((int64_t)std::max(max_len, 1) + 3) & ~int64_t(3); }
+int64_t round_ld(int max_len) { return ((int64_t)std::max(max_len, 1) + 7) & ~int64_t(7); }
 
 }  // namespace
 
@@ -165,8 +165,24 @@ dsa_status_t dsa_index_scores(const dsa_paged_cache_t* cache, const dsa_batch_t*
   if (!q_index || !head_w || !scores || !aligned(q_index, 16) || !aligned(head_w, 16) || !aligned(scores, 16))
     return DSA_ERR_INVALID_ARG;
   if (ld_scores < batch->max_seq_len || (ld_scores % 4)) return DSA_ERR_INVALID_ARG;
-  return launch_index_scores(*cache, *batch, q_index, head_w, scores, ld_scores, dev_status,
-                                 static_cast<cudaStream_t>(stream));
+  return launch_index_scores(*cache, *batch, q_index, head_w, scores, false, ld_scores, dev_status,
+                             static_cast<cudaStream_t>(stream));
+}
+
+dsa_status_t dsa_index_scores_bf16(const dsa_paged_cache_t* cache, const dsa_batch_t* batch, const uint8_t* q_index,
+                                   const float* head_w, uint16_t* scores, int64_t ld_scores, int32_t* dev_status,
+                                   void* stream) {
+  dsa_status_t s;
+  if ((s = check_cache(cache)) != DSA_OK) return s;
+  if ((s = check_batch(batch)) != DSA_OK) return s;
+  if ((s = check_index_rows(cache, batch)) != DSA_OK) return s;
+  if (!dev_status) return DSA_ERR_INVALID_ARG;
+  if (batch->batch == 0) return DSA_OK;
+  if (!q_index || !head_w || !scores || !aligned(q_index, 16) || !aligned(head_w, 16) || !aligned(scores, 16))
+    return DSA_ERR_INVALID_ARG;
+  if (ld_scores < batch->max_seq_len || (ld_scores % 8)) return DSA_ERR_INVALID_ARG;
+  return launch_index_scores(*cache, *batch, q_index, head_w, scores, true, ld_scores, dev_status,
+                             static_cast<cudaStream_t>(stream));
 }
 
 size_t dsa_topk_workspace_size(int32_t rows, int32_t max_row_len, int32_t k) {
@@ -185,6 +201,16 @@ dsa_status_t dsa_topk(const float* scores, int64_t ld_scores, const int32_t* row
   if (need && (!workspace || !aligned(workspace, 256) || workspace_bytes < need)) return DSA_ERR_WORKSPACE;
   return launch_topk(scores, ld_scores, row_lens, nullptr, 1, rows, max_row_len, k, idx_out, workspace, dev_status,
                      static_cast<cudaStream_t>(stream));
+}
+
+dsa_status_t dsa_topk_bf16(const uint16_t* scores, int64_t ld_scores, const int32_t* row_lens, int32_t rows,
+                           int32_t max_row_len, int32_t k, int32_t* idx_out, int32_t* dev_status, void* stream) {
+  if (rows < 0 || k < 1 || k > DSA_MAX_TOPK || max_row_len < 0 || !dev_status) return DSA_ERR_INVALID_ARG;
+  if (rows == 0) return DSA_OK;
+  if (!scores || !row_lens || !idx_out || !aligned(scores, 16) || ld_scores < max_row_len || (ld_scores % 8))
+    return DSA_ERR_INVALID_ARG;
+  return launch_topk_bf16(scores, ld_scores, row_lens, nullptr, 1, rows, max_row_len, k, idx_out, dev_status,
+                          static_cast<cudaStream_t>(stream));
 }
 
 dsa_status_t dsa_topk_noalloc(const float* scores, int64_t ld_scores, const int32_t* row_lens, int32_t rows,
@@ -273,10 +299,12 @@ size_t dsa_workspace_size(const dsa_batch_t* batch, int32_t k) {
          al256(topk_workspace_bytes(rows, batch->max_seq_len, k)) + al256(mla_workspace_bytes(rows, k));
 }
 
-dsa_status_t dsa_decode_step(const dsa_paged_cache_t* cache, const dsa_batch_t* batch, const uint8_t* q_index,
-                             const float* head_w, const uint16_t* q_mla, int32_t k, float sm_scale, uint16_t* out,
-                             float* lse, float* scores_out, int64_t ld_scores, int32_t* idx_out, void* workspace,
-                             size_t workspace_bytes, int32_t* dev_status, void* stream) {
+namespace {
+
+dsa_status_t decode_step_impl(const dsa_paged_cache_t* cache, const dsa_batch_t* batch, const uint8_t* q_index,
+                              const float* head_w, const uint16_t* q_mla, int32_t k, float sm_scale, uint16_t* out,
+                              float* lse, void* scores_out, bool bf16, int64_t ld_scores, int32_t* idx_out,
+                              void* workspace, size_t workspace_bytes, int32_t* dev_status, void* stream) {
   dsa_status_t s;
   if ((s = check_cache(cache)) != DSA_OK) return s;
   if ((s = check_batch(batch)) != DSA_OK) return s;
@@ -291,13 +319,13 @@ dsa_status_t dsa_decode_step(const dsa_paged_cache_t* cache, const dsa_batch_t* 
     return DSA_ERR_WORKSPACE;
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   uint8_t* w = static_cast<uint8_t*>(workspace);
-  float* scores = scores_out;
+  void* scores = scores_out;
   int64_t ld = ld_scores;
   const size_t scores_bytes = al256((size_t)rows * round_ld(batch->max_seq_len) * 4);
   if (!scores) {
-    scores = reinterpret_cast<float*>(w);
-    ld = round_ld(batch->max_seq_len);
-  } else if (!aligned(scores, 16) || ld < batch->max_seq_len || (ld % 4)) {
+    scores = w;
+    ld = round_ld(batch->max_seq_len);  // a multiple of 8
+  } else if (!aligned(scores, 16) || ld < batch->max_seq_len || (ld % (bf16 ? 8 : 4))) {
     return DSA_ERR_INVALID_ARG;
   }
   w += scores_bytes;
@@ -307,12 +335,36 @@ dsa_status_t dsa_decode_step(const dsa_paged_cache_t* cache, const dsa_batch_t* 
   w += al256(topk_workspace_bytes(rows, batch->max_seq_len, k));
   void* mla_ws = w;
 
-  if ((s = launch_index_scores(*cache, *batch, q_index, head_w, scores, ld, dev_status, st)) != DSA_OK) return s;
-  const int cap = std::min(batch->max_blocks_per_seq * kBlock, batch->max_seq_len);
-  if ((s = launch_topk(scores, ld, nullptr, batch->seq_lens, batch->queries_per_seq, rows, cap, k, idx, topk_ws,
-                       dev_status, st)) != DSA_OK)
+  if ((s = launch_index_scores(*cache, *batch, q_index, head_w, scores, bf16, ld, dev_status, st)) != DSA_OK)
     return s;
+  const int cap = std::min(batch->max_blocks_per_seq * kBlock, batch->max_seq_len);
+  if (bf16)
+    s = launch_topk_bf16(static_cast<const uint16_t*>(scores), ld, nullptr, batch->seq_lens,
+                         batch->queries_per_seq, rows, cap, k, idx, dev_status, st);
+  else
+    s = launch_topk(static_cast<const float*>(scores), ld, nullptr, batch->seq_lens, batch->queries_per_seq, rows,
+                    cap, k, idx, topk_ws, dev_status, st);
+  if (s != DSA_OK) return s;
   return launch_sparse_mla(*cache, *batch, q_mla, idx, k, sm_scale, out, lse, mla_ws, dev_status, st);
+}
+
+}  // namespace
+
+dsa_status_t dsa_decode_step(const dsa_paged_cache_t* cache, const dsa_batch_t* batch, const uint8_t* q_index,
+                             const float* head_w, const uint16_t* q_mla, int32_t k, float sm_scale, uint16_t* out,
+                             float* lse, float* scores_out, int64_t ld_scores, int32_t* idx_out, void* workspace,
+                             size_t workspace_bytes, int32_t* dev_status, void* stream) {
+  return decode_step_impl(cache, batch, q_index, head_w, q_mla, k, sm_scale, out, lse, scores_out, false, ld_scores,
+                          idx_out, workspace, workspace_bytes, dev_status, stream);
+}
+
+dsa_status_t dsa_decode_step_bf16(const dsa_paged_cache_t* cache, const dsa_batch_t* batch, const uint8_t* q_index,
+                                  const float* head_w, const uint16_t* q_mla, int32_t k, float sm_scale,
+                                  uint16_t* out, float* lse, uint16_t* scores_out, int64_t ld_scores,
+                                  int32_t* idx_out, void* workspace, size_t workspace_bytes, int32_t* dev_status,
+                                  void* stream) {
+  return decode_step_impl(cache, batch, q_index, head_w, q_mla, k, sm_scale, out, lse, scores_out, true, ld_scores,
+                          idx_out, workspace, workspace_bytes, dev_status, stream);
 }
 
 dsa_status_t dsa_cache_append(const dsa_paged_cache_t* cache, const dsa_batch_t* batch, const uint16_t* new_latent,

@@ -145,6 +145,9 @@ __device__ __forceinline__ void tma_load_3d_hint(uint32_t dst, const void* map, 
 __device__ __forceinline__ void st_global_hint(float* addr, float v, uint64_t policy) {
   asm volatile("st.global.L2::cache_hint.f32 [%0], %1, %2;" ::"l"(addr), "f"(v), "l"(policy) : "memory");
 }
+__device__ __forceinline__ void st_global_hint(uint16_t* addr, uint16_t v, uint64_t policy) {
+  asm volatile("st.global.L2::cache_hint.b16 [%0], %1, %2;" ::"l"(addr), "h"(v), "l"(policy) : "memory");
+}
 // Plain bulk copy; both addresses 16-byte aligned, bytes a multiple of 16.
 __device__ __forceinline__ void bulk_load(uint32_t dst, const void* src, uint32_t bytes, uint32_t bar) {
   asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];"

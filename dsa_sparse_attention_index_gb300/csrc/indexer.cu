@@ -42,6 +42,8 @@
 // reused across query rows during speculative verify).
 #include <algorithm>
 
+#include <cuda_bf16.h>
+
 #include "common.cuh"
 #include "internal.h"
 
@@ -79,6 +81,7 @@ struct IdxParams {
   // rows of a prefill chunk.
   int32_t groups;
   int32_t nq_real;
+  int32_t score_bf16;  // scores are bf16 (round to nearest even) at (uint16_t*)scores, else fp32
 };
 
 constexpr int kSfSlots = 4;  // MXFP4: TMEM scale-factor slots, decoupled from the accumulators
@@ -458,9 +461,16 @@ __global__ void __launch_bounds__(idx_threads<MX>(), 1)
             }
           }
           const int vis = visible_len(len, NQ, q);
-          float* out = p.scores + ((int64_t)b * NQ + q) * p.ld;
-          if (t0 < vis) st_global_hint(out + t0, s0, keep_policy);
-          if (t1 < vis) st_global_hint(out + t1, s1, keep_policy);
+          const int64_t ro = ((int64_t)b * NQ + q) * p.ld;
+          if (p.score_bf16) {
+            uint16_t* out = reinterpret_cast<uint16_t*>(p.scores) + ro;
+            if (t0 < vis) st_global_hint(out + t0, __bfloat16_as_ushort(__float2bfloat16_rn(s0)), keep_policy);
+            if (t1 < vis) st_global_hint(out + t1, __bfloat16_as_ushort(__float2bfloat16_rn(s1)), keep_policy);
+          } else {
+            float* out = p.scores + ro;
+            if (t0 < vis) st_global_hint(out + t0, s0, keep_policy);
+            if (t1 < vis) st_global_hint(out + t1, s1, keep_policy);
+          }
         }
         tc_fence_before();
         __syncwarp();
@@ -529,7 +539,8 @@ dsa_status_t launch_nq(const IdxParams& p, const CUtensorMap& keys, const CUtens
 }  // namespace
 
 dsa_status_t launch_index_scores(const dsa_paged_cache_t& c, const dsa_batch_t& bt, const uint8_t* q_index,
-                                 const float* head_w, float* scores, int64_t ld, int32_t* status, cudaStream_t st) {
+                                 const float* head_w, void* scores, bool bf16, int64_t ld, int32_t* status,
+                                 cudaStream_t st) {
   const bool mx = c.key_format == DSA_KEY_MXFP4;
   const int nq = bt.queries_per_seq;
   if (mx && nq != 1) return DSA_ERR_UNSUPPORTED;
@@ -569,7 +580,8 @@ dsa_status_t launch_index_scores(const dsa_paged_cache_t& c, const dsa_batch_t& 
       return DSA_ERR_CUDA;
   }
   IdxParams p{index_base, c.row_stride, c.num_blocks, bt.block_table, bt.max_blocks_per_seq, bt.seq_lens,
-              bt.batch, bt.max_seq_len, head_w, scores, ld, status, groups, nq};
+              bt.batch, bt.max_seq_len, head_w, static_cast<float*>(scores), ld, status, groups, nq,
+              bf16 ? 1 : 0};
   if (mx) return launch_nq<1, true>(p, keys, scales, qmap, st);
   switch (nq_k) {
     case 1: return launch_nq<1, false>(p, keys, scales, qmap, st);

@@ -31,14 +31,21 @@ bool encode_tmap(CUtensorMap* map, CUtensorMapDataType dtype, int rank, const vo
 dsa_status_t launch_translate_pages(const dsa_paged_cache_t& c, const dsa_batch_t& bt, int64_t* latent_pages,
                                     int64_t* index_pages, int32_t* status, cudaStream_t st);
 // FP8 or MXFP4 keys (MXFP4: one query row per sequence, else DSA_ERR_UNSUPPORTED).
+// scores: fp32, or bf16 bits when bf16 (ld in elements either way).
 dsa_status_t launch_index_scores(const dsa_paged_cache_t& c, const dsa_batch_t& bt, const uint8_t* q_index,
-                                 const float* head_w, float* scores, int64_t ld, int32_t* status, cudaStream_t st);
+                                 const float* head_w, void* scores, bool bf16, int64_t ld, int32_t* status,
+                                 cudaStream_t st);
 size_t topk_workspace_bytes(int rows, int max_row_len, int k);
 // Process-wide choice of the four-kernel top-k for rows too long for shared memory.
 int topk_force_multipass(int on);
 dsa_status_t launch_topk(const float* scores, int64_t ld, const int32_t* row_lens, const int32_t* seq_lens, int nq,
                          int rows, int max_row_len, int k, int32_t* out, void* workspace, int32_t* status,
                          cudaStream_t st);
+// The same top-k over bf16 scores (bits, widened exactly): the cluster paths
+// only (DSA_ERR_UNSUPPORTED where no cluster can be scheduled); no workspace.
+dsa_status_t launch_topk_bf16(const uint16_t* scores, int64_t ld, const int32_t* row_lens, const int32_t* seq_lens,
+                              int nq, int rows, int max_row_len, int k, int32_t* out, int32_t* status,
+                              cudaStream_t st);
 // The same top-k with its scratch in a file-scope device array (no allocation).
 dsa_status_t launch_topk_noalloc(const float* scores, int64_t ld, const int32_t* row_lens, int rows, int max_row_len,
                                  int k, int32_t* out, int32_t* status, cudaStream_t st);

@@ -619,11 +619,14 @@ __device__ __forceinline__ uint32_t warp_excl_scan(uint32_t v, uint32_t& total) 
 // slice's scores again from global memory (L2), and shared memory holds only
 // the histograms.  Resident: two CTAs of 512 threads per SM (at most 64
 // registers); streaming: one.
-template <int C, bool kStream>
+// In: the score element, float or uint16_t (bf16 bits, widened exactly to
+// fp32 as they are read; the selection is then the fp32 one).
+template <int C, bool kStream, typename In>
 __global__ void __launch_bounds__(kResThreads, kStream ? 1 : 2)
-    topk_cluster_kernel(const float* __restrict__ scores, int64_t ld, const int32_t* row_lens,
+    topk_cluster_kernel(const In* __restrict__ scores, int64_t ld, const int32_t* row_lens,
                         const int32_t* seq_lens, int nq, int cap, int k, int32_t* out, int32_t* status,
                         int slice_cap) {
+  constexpr bool kF32 = std::is_same<In, float>::value;
   using G = typename std::conditional<kStream, float4, uint4>::type;  // a group of 4 elements
   cg::cluster_group cluster = cg::this_cluster();
   const int c = (int)cluster.block_rank();
@@ -657,15 +660,26 @@ __global__ void __launch_bounds__(kResThreads, kStream ? 1 : 2)
   const int start = c * S;
   const int n = max(0, min(S, len - start));
   const int n4 = (n + 3) >> 2;  // groups of 4; the last one is padded with NaN / key 0 (never counted)
-  const float* row = scores + (int64_t)r * ld + start;
-  const float4* row4 = reinterpret_cast<const float4*>(row);
+  const In* row = scores + (int64_t)r * ld + start;
   const int full4 = n >> 2;
+  auto widen = [](In x) -> float {
+    if constexpr (kF32) return x;
+    else return __uint_as_float((uint32_t)x << 16);
+  };
   auto score_group = [&](int i) -> float4 {  // scores 4i..4i+3 from global memory
-    if (i < full4) return row4[i];
+    if (i < full4) {
+      if constexpr (kF32) {
+        return reinterpret_cast<const float4*>(row)[i];
+      } else {
+        const uint2 w = reinterpret_cast<const uint2*>(row)[i];
+        return make_float4(__uint_as_float(w.x << 16), __uint_as_float(w.x & 0xFFFF0000u),
+                           __uint_as_float(w.y << 16), __uint_as_float(w.y & 0xFFFF0000u));
+      }
+    }
     const int b = 4 * i;  // the slice's ragged last group
     const float nan = __uint_as_float(0x7FC00000u);
-    return make_float4(row[b], b + 1 < n ? row[b + 1] : nan, b + 2 < n ? row[b + 2] : nan,
-                       b + 3 < n ? row[b + 3] : nan);
+    return make_float4(widen(row[b]), b + 1 < n ? widen(row[b + 1]) : nan, b + 2 < n ? widen(row[b + 2]) : nan,
+                       b + 3 < n ? widen(row[b + 3]) : nan);
   };
   auto load_group = [&](int i) -> G {
     if constexpr (kStream) return score_group(i);
@@ -696,9 +710,17 @@ __global__ void __launch_bounds__(kResThreads, kStream ? 1 : 2)
     }
   }
   __syncthreads();
-  if constexpr (!kStream) {
+  if constexpr (!kStream && !kF32) {
+    // bf16 scores: 8-byte loads widened to keys (half the bytes of fp32)
+    for (int i = tid; i < n4; i += kResThreads) {
+      const uint4 kk = to_keys(score_group(i));
+      keys4[i] = kk;
+      count_first(i, kk);
+    }
+  } else if constexpr (!kStream) {
     // the slice's whole groups by bulk copies in kLoadChunks pieces, converted to
     // keys in place as each lands; the ragged last group by plain loads
+    const float4* row4 = reinterpret_cast<const float4*>(row);
     const int per = (full4 + kLoadChunks - 1) / kLoadChunks;
     if (tid == 0) {
 #pragma unroll
@@ -1107,19 +1129,19 @@ __global__ void __launch_bounds__(kResThreads, kStream ? 1 : 2)
   }
 }
 
-template <int C, bool kStream>
-dsa_status_t launch_cluster(const float* scores, int64_t ld, const int32_t* row_lens, const int32_t* seq_lens,
+template <int C, bool kStream, typename In>
+dsa_status_t launch_cluster(const In* scores, int64_t ld, const int32_t* row_lens, const int32_t* seq_lens,
                             int nq, int rows, int cap, int k, int32_t* out, int32_t* status, cudaStream_t st) {
   static bool attr_set[64] = {};
   int dev = 0;
   cudaGetDevice(&dev);
   if (dev < 64 && !attr_set[dev]) {
-    if (cuda_status(cudaFuncSetAttribute(topk_cluster_kernel<C, kStream>,
+    if (cuda_status(cudaFuncSetAttribute(topk_cluster_kernel<C, kStream, In>,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          (int)res_smem(kStream ? 0 : kResKeys))) != DSA_OK)
       return DSA_ERR_CUDA;
     if (C > kResMaxCluster &&
-        cuda_status(cudaFuncSetAttribute(topk_cluster_kernel<C, kStream>,
+        cuda_status(cudaFuncSetAttribute(topk_cluster_kernel<C, kStream, In>,
                                          cudaFuncAttributeNonPortableClusterSizeAllowed, 1)) != DSA_OK)
       return DSA_ERR_CUDA;
     attr_set[dev] = true;
@@ -1141,7 +1163,7 @@ dsa_status_t launch_cluster(const float* scores, int64_t ld, const int32_t* row_
   cfg.attrs = attr;
   cfg.numAttrs = 2;
   count_launches(1);
-  if (cuda_status(cudaLaunchKernelEx(&cfg, topk_cluster_kernel<C, kStream>, scores, ld, row_lens, seq_lens, nq, cap,
+  if (cuda_status(cudaLaunchKernelEx(&cfg, topk_cluster_kernel<C, kStream, In>, scores, ld, row_lens, seq_lens, nq, cap,
                                      k, out, status, slice)) != DSA_OK)
     return DSA_ERR_CUDA;
   return launch_status();
@@ -1149,14 +1171,14 @@ dsa_status_t launch_cluster(const float* scores, int64_t ld, const int32_t* row_
 
 // Whether clusters of C streaming CTAs can be resident at all on this device
 // (asked once per device; a cluster of 16 needs the non-portable size).
-template <int C>
+template <int C, typename In>
 bool stream_cluster_ok() {
   static int known[64] = {};  // 0 unknown, 1 yes, 2 no
   int dev = 0;
   cudaGetDevice(&dev);
   if (dev >= 64) return false;
   if (known[dev] == 0) {
-    bool ok = cudaFuncSetAttribute(topk_cluster_kernel<C, true>, cudaFuncAttributeNonPortableClusterSizeAllowed,
+    bool ok = cudaFuncSetAttribute(topk_cluster_kernel<C, true, In>, cudaFuncAttributeNonPortableClusterSizeAllowed,
                                    C > kResMaxCluster ? 1 : 0) == cudaSuccess;
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(C);
@@ -1170,7 +1192,7 @@ bool stream_cluster_ok() {
     cfg.attrs = attr;
     cfg.numAttrs = 1;
     int n = 0;
-    ok = ok && cudaOccupancyMaxActiveClusters(&n, topk_cluster_kernel<C, true>, &cfg) == cudaSuccess && n > 0;
+    ok = ok && cudaOccupancyMaxActiveClusters(&n, topk_cluster_kernel<C, true, In>, &cfg) == cudaSuccess && n > 0;
     cudaGetLastError();  // a refused query leaves no error behind
     known[dev] = ok ? 1 : 2;
   }
@@ -1199,10 +1221,13 @@ int topk_force_multipass(int on) { return g_force_multipass.exchange(on ? 1 : 0)
 
 size_t topk_final_smem_bytes() { return (size_t)kWindowBits / 8 + 8 * kCandCap + 4 * kMaxTopk + 4 * kBins + 128; }
 
-dsa_status_t launch_topk(const float* scores, int64_t ld, const int32_t* row_lens, const int32_t* seq_lens, int nq,
-                         int rows, int max_row_len, int k, int32_t* out, void* workspace, int32_t* status,
-                         cudaStream_t st) {
-  if (rows == 0) return DSA_OK;
+namespace {
+
+// The cluster paths: true with *res set when one of them took the rows.
+template <typename In>
+bool launch_topk_cluster(const In* scores, int64_t ld, const int32_t* row_lens, const int32_t* seq_lens, int nq,
+                         int rows, int max_row_len, int k, int32_t* out, int32_t* status, cudaStream_t st,
+                         dsa_status_t* res) {
   // row-resident path: one cluster per row, enough CTAs to hold the row, small
   // enough slices for two CTAs per SM where a cluster of 8 allows it, and for
   // few rows enough CTAs to spread them over the SMs (at least 8,192 keys per CTA)
@@ -1214,25 +1239,58 @@ dsa_status_t launch_topk(const float* scores, int64_t ld, const int32_t* row_len
   const int cluster = std::min(kResMaxCluster, std::max(std::max(c_min, c_pair), std::max(c_fill, 1)));
   if (max_row_len > k && c_min <= kResMaxCluster) {
     // row-resident path: one cluster of `cluster` CTAs per row, no workspace
+#define DSA_RES(C) launch_cluster<C, false, In>(scores, ld, row_lens, seq_lens, nq, rows, max_row_len, k, out, status, st)
     switch (cluster) {
-      case 1: return launch_cluster<1, false>(scores, ld, row_lens, seq_lens, nq, rows, max_row_len, k, out, status, st);
-      case 2: return launch_cluster<2, false>(scores, ld, row_lens, seq_lens, nq, rows, max_row_len, k, out, status, st);
-      case 3: return launch_cluster<3, false>(scores, ld, row_lens, seq_lens, nq, rows, max_row_len, k, out, status, st);
-      case 4: return launch_cluster<4, false>(scores, ld, row_lens, seq_lens, nq, rows, max_row_len, k, out, status, st);
-      case 5: return launch_cluster<5, false>(scores, ld, row_lens, seq_lens, nq, rows, max_row_len, k, out, status, st);
-      case 6: return launch_cluster<6, false>(scores, ld, row_lens, seq_lens, nq, rows, max_row_len, k, out, status, st);
-      case 7: return launch_cluster<7, false>(scores, ld, row_lens, seq_lens, nq, rows, max_row_len, k, out, status, st);
-      default: return launch_cluster<8, false>(scores, ld, row_lens, seq_lens, nq, rows, max_row_len, k, out, status, st);
+      case 1: *res = DSA_RES(1); break;
+      case 2: *res = DSA_RES(2); break;
+      case 3: *res = DSA_RES(3); break;
+      case 4: *res = DSA_RES(4); break;
+      case 5: *res = DSA_RES(5); break;
+      case 6: *res = DSA_RES(6); break;
+      case 7: *res = DSA_RES(7); break;
+      default: *res = DSA_RES(8); break;
     }
+#undef DSA_RES
+    return true;
   }
   if (max_row_len > k && !g_force_multipass.load(std::memory_order_relaxed)) {
     // rows too long to hold on chip: the streaming cluster kernel, 16 CTAs per
     // row where the device schedules such clusters, else 8
-    if (stream_cluster_ok<16>())
-      return launch_cluster<16, true>(scores, ld, row_lens, seq_lens, nq, rows, max_row_len, k, out, status, st);
-    if (stream_cluster_ok<8>())
-      return launch_cluster<8, true>(scores, ld, row_lens, seq_lens, nq, rows, max_row_len, k, out, status, st);
+    if (stream_cluster_ok<16, In>()) {
+      *res = launch_cluster<16, true, In>(scores, ld, row_lens, seq_lens, nq, rows, max_row_len, k, out, status, st);
+      return true;
+    }
+    if (stream_cluster_ok<8, In>()) {
+      *res = launch_cluster<8, true, In>(scores, ld, row_lens, seq_lens, nq, rows, max_row_len, k, out, status, st);
+      return true;
+    }
   }
+  return false;
+}
+
+}  // namespace
+
+dsa_status_t launch_topk_bf16(const uint16_t* scores, int64_t ld, const int32_t* row_lens, const int32_t* seq_lens,
+                              int nq, int rows, int max_row_len, int k, int32_t* out, int32_t* status,
+                              cudaStream_t st) {
+  if (rows == 0) return DSA_OK;
+  dsa_status_t res = DSA_OK;
+  if (max_row_len <= k)  // nothing to select: the kernel writes 0..len-1 and the padding, reading no score
+    return launch_cluster<1, false, uint16_t>(scores, ld, row_lens, seq_lens, nq, rows, max_row_len, k, out, status,
+                                              st);
+  if (launch_topk_cluster(scores, ld, row_lens, seq_lens, nq, rows, max_row_len, k, out, status, st, &res))
+    return res;
+  // long rows with the four-kernel path forced, or no cluster schedulable: that path reads fp32 scores only
+  return DSA_ERR_UNSUPPORTED;
+}
+
+dsa_status_t launch_topk(const float* scores, int64_t ld, const int32_t* row_lens, const int32_t* seq_lens, int nq,
+                         int rows, int max_row_len, int k, int32_t* out, void* workspace, int32_t* status,
+                         cudaStream_t st) {
+  if (rows == 0) return DSA_OK;
+  dsa_status_t res = DSA_OK;
+  if (launch_topk_cluster(scores, ld, row_lens, seq_lens, nq, rows, max_row_len, k, out, status, st, &res))
+    return res;
   auto al = [](size_t x) { return (x + 255) & ~size_t(255); };
   uint8_t* w = static_cast<uint8_t*>(workspace);
   TopkWs ws;

@@ -313,6 +313,40 @@ dsa_status_t dsa_decode_step(const dsa_paged_cache_t* cache, const dsa_batch_t* 
                              int32_t* dev_status, void* stream);
 
 /*
+ * BF16 scores (Day-0 post, decode-context-parallelism section: candidates
+ * are picked straight from BF16 scores, and BF16 halves the bytes of the
+ * score rows the top-k reads).
+ * dsa_index_scores_bf16 is dsa_index_scores with each score rounded to bf16
+ * (nearest, ties to even) from the same fp32 value; scores holds bf16 bits
+ * [rows][ld_scores].  dsa_topk_bf16 is dsa_topk over bf16 scores (bits),
+ * with the same rules: equal scores go to the lower token index, -0 = +0,
+ * NaN ranks below every number.  bf16 keeps 8 significant bits, so scores
+ * that differ in fp32 can tie in bf16, and a tie at the k-th score goes to
+ * the lowest indices: the set can differ from dsa_topk's selection over the
+ * fp32 scores wherever a score lies within a bf16 rounding step of the k-th.
+ * dsa_decode_step_bf16 is dsa_decode_step with bf16 scores between the
+ * indexer and the top-k (scores_out, if not NULL, receives them).
+ *   scores    16-byte aligned; ld_scores >= max_row_len (batch->max_seq_len)
+ *             and a multiple of 8
+ *   dsa_topk_bf16 needs no workspace.  Rows longer than 245,760 tokens take
+ *   a cluster of 16 (or 8) CTAs per row; where neither can be scheduled, or
+ *   with dsa_topk_force_multipass on, such rows give DSA_ERR_UNSUPPORTED.
+ */
+dsa_status_t dsa_index_scores_bf16(const dsa_paged_cache_t* cache, const dsa_batch_t* batch,
+                                   const uint8_t* q_index, const float* head_w,
+                                   uint16_t* scores, int64_t ld_scores,
+                                   int32_t* dev_status, void* stream);
+dsa_status_t dsa_topk_bf16(const uint16_t* scores, int64_t ld_scores, const int32_t* row_lens, int32_t rows,
+                           int32_t max_row_len, int32_t k, int32_t* idx_out, int32_t* dev_status, void* stream);
+dsa_status_t dsa_decode_step_bf16(const dsa_paged_cache_t* cache, const dsa_batch_t* batch,
+                                  const uint8_t* q_index, const float* head_w,
+                                  const uint16_t* q_mla, int32_t k, float sm_scale,
+                                  uint16_t* out, float* lse,
+                                  uint16_t* scores_out, int64_t ld_scores, int32_t* idx_out,
+                                  void* workspace, size_t workspace_bytes,
+                                  int32_t* dev_status, void* stream);
+
+/*
  * New-token cache write: the front end of the fused decode path (Day-0 post,
  * section on the fused low-latency decode path: each step writes the new
  * token's index key and latent into the cache; packed-cache section for the

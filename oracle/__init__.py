@@ -298,3 +298,10 @@ def dcp_sparse_mla(case, idx: np.ndarray, shards: int, k: int | None = None, par
     wgt = np.where(tot > 0, wexp / np.where(tot > 0, tot, 1.0), 0.0)   # exp(LSE_w - lse)
     out = (wgt[..., None] * O).sum(axis=0)
     return out, lse, O, L
+
+
+def index_scores_bf16(case, rows_ld: int | None = None) -> np.ndarray:
+    """Indexer scores rounded to bf16, nearest with ties to even (Day-0 post,
+    decode-context-parallelism section: the top-k candidates come straight
+    from BF16 scores).  The fp64 scores of index_scores, rounded."""
+    return round_bf16(index_scores(case, rows_ld))

@@ -74,6 +74,11 @@ def test_host_validation_without_device(lib):
                             None) == B.ERR_UNSUPPORTED
     assert lib.dsa_dcp_topk(None, 0, None, 1, 10, 2048, 0, None, None, None, 0, st, None) == B.ERR_INVALID_ARG
     assert lib.dsa_dcp_topk(128, 16, 256, 1, 10, 2048, 8, 512, None, None, 0, st, None) == B.ERR_WORKSPACE
+    # bf16 scores: rows of a multiple of 8 elements
+    assert lib.dsa_topk_bf16(128, 12, 256, 1, 10, 2048, 512, st, None) == B.ERR_INVALID_ARG
+    assert lib.dsa_topk_bf16(128, 16, 256, 1, 10, 0, 512, st, None) == B.ERR_INVALID_ARG
+    assert lib.dsa_index_scores_bf16(ctypes.byref(c), ctypes.byref(b), 1024, 2048, 4096, 100, st,
+                                     None) == B.ERR_INVALID_ARG
     # DCP LSE combine: 1..8 shards, aligned pointers, a workspace of the stated size
     b.queries_per_seq = 1
     dm = lambda shards, q, out, ws, n: lib.dsa_dcp_sparse_mla(ctypes.byref(c), ctypes.byref(b), q, 256, 2048, shards,
