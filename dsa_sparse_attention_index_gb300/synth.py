@@ -33,8 +33,11 @@ BLOCK = 64
 IDX_HEADS, IDX_DIM = 32, 128
 MLA_HEADS, LATENT, VALUE = 96, 576, 512
 KEY_FP8, KEY_MXFP4 = 0, 1
+LATENT_FP8, LATENT_NVFP4 = 0, 1
 
-LATENT_PAGE = BLOCK * LATENT                      # 36,864 B
+LATENT_RECORD = {LATENT_FP8: LATENT,              # 576 B: E4M3 codes
+                 LATENT_NVFP4: VALUE // 2 + VALUE // 16 + (LATENT - VALUE)}  # 352 B: E2M1 + E4M3 scales + E4M3 tail
+LATENT_PAGE = BLOCK * LATENT                      # 36,864 B (FP8 latents)
 INDEX_PAGE = {KEY_FP8: BLOCK * (IDX_DIM + 4),     # 8,448 B
               KEY_MXFP4: BLOCK * (IDX_DIM // 2 + 4)}  # 4,352 B
 
@@ -63,6 +66,7 @@ class Case:
     q_mla: np.ndarray           # uint16 (bf16 bits) [rows, 96, 576]
     sm_scale: float
     seed: int = 0
+    latent_format: int = LATENT_FP8  # LATENT_FP8 or LATENT_NVFP4
 
     @property
     def rows(self) -> int:
@@ -85,6 +89,9 @@ class Case:
 
     def token_bytes(self) -> int:
         return 132 if self.key_format == KEY_FP8 else 68
+
+    def latent_bytes(self) -> int:
+        return LATENT_RECORD[self.latent_format]
 
 
 # ---------------------------------------------------------------------------
@@ -121,17 +128,48 @@ def mxfp4_encode(x: np.ndarray):
     e = torch.where(amax > 0, ex.to(torch.int64) - 1 - 2, torch.full_like(ex, -127, dtype=torch.int64))
     e = e.clamp(-127, 127)
     scaled = torch.ldexp(x, (-e).unsqueeze(-1).to(torch.float64))   # exact: a power-of-two scaling
-    mag = scaled.abs()
-    # nearest E2M1 magnitude: count the midpoints below |x|; at an exact midpoint
-    # this picks the lower code, so the three midpoints whose upper code is the
-    # even one move up (round half to even); |x| >= 6 lands on code 7 (6.0)
-    code = torch.bucketize(mag, torch.from_numpy(_E2M1_MID), right=False)
-    code = code + ((mag == 0.75) | (mag == 1.75) | (mag == 3.5)).to(code.dtype)
-    code = (code | torch.where(scaled < 0, 8, 0)).to(torch.uint8).reshape(-1, IDX_DIM).numpy()
+    code = e2m1_codes(scaled).to(torch.uint8).reshape(-1, IDX_DIM).numpy()
     packed = (code[:, 0::2] | (code[:, 1::2] << 4)).astype(np.uint8)
     e = e.numpy()
     e8m0 = (e + 127).astype(np.uint8).reshape(-1, IDX_DIM // 32)
     return packed, e8m0
+
+
+def e2m1_codes(mag_signed: "torch.Tensor") -> "torch.Tensor":
+    """Nearest E2M1 codes (ties to even, |x| >= 6 -> 6) of a float64 tensor,
+    as int64 nibbles with the sign in bit 3."""
+    import torch
+
+    mag = mag_signed.abs()
+    # count the midpoints below |x|; at an exact midpoint this picks the lower
+    # code, so the three midpoints whose upper code is the even one move up
+    # (round half to even); |x| >= 6 lands on code 7 (6.0)
+    code = torch.bucketize(mag, torch.from_numpy(_E2M1_MID), right=False)
+    code = code + ((mag == 0.75) | (mag == 1.75) | (mag == 3.5)).to(code.dtype)
+    return code | torch.where(mag_signed < 0, 8, 0)
+
+
+def nvfp4_latent_encode(x: np.ndarray, latent_scale: float) -> np.ndarray:
+    """NVFP4 latent records [n, 352] of [n, 576] values: per 16 dims of
+    0..511 a block scale e4m3(amax / (6 latent_scale)) and E2M1 codes of
+    x / (latent_scale * scale) (element 2i in the low nibble of byte i); dims
+    512..575 as e4m3(x / latent_scale)."""
+    import torch
+
+    x = np.ascontiguousarray(x, dtype=np.float32)
+    n = x.shape[0]
+    ls = np.float32(latent_scale)
+    head = x[:, :VALUE].reshape(n, VALUE // 16, 16)
+    amax = np.abs(head).max(axis=2)
+    sc = e4m3_encode(amax / (np.float32(6.0) * ls))                       # [n, 32] codes
+    sdec = torch.from_numpy(sc.copy()).view(torch.float8_e4m3fn).to(torch.float32).numpy()
+    step = (ls * sdec).astype(np.float32)
+    with np.errstate(divide="ignore", invalid="ignore"):
+        q = np.where(sdec[..., None] > 0, head / step[..., None], np.float32(0.0)).astype(np.float32)
+    codes = e2m1_codes(torch.from_numpy(q.astype(np.float64))).to(torch.uint8).numpy().reshape(n, VALUE)
+    packed = (codes[:, 0::2] | (codes[:, 1::2] << 4)).astype(np.uint8)
+    tail = e4m3_encode(x[:, VALUE:] / ls)
+    return np.concatenate([packed, sc, tail], axis=1)
 
 
 # ---------------------------------------------------------------------------
@@ -140,7 +178,7 @@ def mxfp4_encode(x: np.ndarray):
 
 def make_case(name: str, seq_lens, nq: int = 1, key_format: int = KEY_FP8, topk: int = 2048,
               heavy_tail: float = 0.0, permute_blocks: bool = True, spare_blocks: int = 0,
-              seed: int = 0, chunk_tokens: int = 1 << 16) -> Case:
+              seed: int = 0, chunk_tokens: int = 1 << 16, latent_format: int = LATENT_FP8) -> Case:
     """Build a workload.  Draw order: block permutation, latent scale, then
     per sequence and per token chunk: index-key values, heavy-tail mask,
     per-token key scales (FP8 only), latent values; then tail/spare filler
@@ -150,7 +188,8 @@ def make_case(name: str, seq_lens, nq: int = 1, key_format: int = KEY_FP8, topk:
     latent scale U(0.5, 2); indexer queries E4M3(N(0,1)) [32, 128]; head
     weights N(0, 0.1^2) fp32; MLA queries bf16(N(0,1)) [96, 576].  With
     ``heavy_tail`` = f, a fraction f of tokens have their key values x4 before
-    rounding.  MXFP4 keys quantise the same N(0,1) draws per OCP MX.
+    rounding.  MXFP4 keys quantise the same N(0,1) draws per OCP MX; NVFP4
+    latents quantise the same latent draws as ``nvfp4_latent_encode``.
     """
     rng = np.random.Generator(np.random.PCG64(seed))
     seq_lens = np.asarray(seq_lens, dtype=np.int32).reshape(-1)
@@ -165,8 +204,10 @@ def make_case(name: str, seq_lens, nq: int = 1, key_format: int = KEY_FP8, topk:
     latent_scale = float(rng.uniform(0.5, 2.0))
 
     idx_page = INDEX_PAGE[key_format]
-    row_stride = LATENT_PAGE + idx_page
-    latent_off, index_off = 0, LATENT_PAGE
+    rec = LATENT_RECORD[latent_format]
+    lat_page = BLOCK * rec
+    row_stride = lat_page + idx_page
+    latent_off, index_off = 0, lat_page
     pool = np.zeros((num_blocks, row_stride), dtype=np.uint8)
     block_table = np.full((batch, max_blocks), -1, dtype=np.int32)
 
@@ -186,12 +227,13 @@ def make_case(name: str, seq_lens, nq: int = 1, key_format: int = KEY_FP8, topk:
                 scales = rng.uniform(0.5, 2.0, size=n).astype(np.float32)
             else:
                 codes, e8 = mxfp4_encode(kv)
-            lat = e4m3_encode(rng.standard_normal((n, LATENT), dtype=np.float32))
+            lat_x = rng.standard_normal((n, LATENT), dtype=np.float32)
+            lat = e4m3_encode(lat_x) if latent_format == LATENT_FP8 else nvfp4_latent_encode(lat_x, latent_scale)
             t = np.arange(t0, t0 + n)
             r = rows_b[t // BLOCK]
             slot = t % BLOCK
             # scatter token rows into their pages
-            lat_view = pool[:, latent_off:latent_off + LATENT_PAGE].reshape(num_blocks, BLOCK, LATENT)
+            lat_view = pool[:, latent_off:latent_off + lat_page].reshape(num_blocks, BLOCK, rec)
             lat_view[r, slot] = lat
             if key_format == KEY_FP8:
                 cview = pool[:, index_off:index_off + BLOCK * IDX_DIM].reshape(num_blocks, BLOCK, IDX_DIM)
@@ -211,8 +253,8 @@ def make_case(name: str, seq_lens, nq: int = 1, key_format: int = KEY_FP8, topk:
         if tail or L == 0:
             r = block_table[b, nblk[b] - 1]
             s0 = tail
-            fill = rng.integers(0, 256, size=(BLOCK - s0, LATENT), dtype=np.uint8)
-            pool[r, latent_off:latent_off + LATENT_PAGE].reshape(BLOCK, LATENT)[s0:] = fill
+            fill = rng.integers(0, 256, size=(BLOCK - s0, rec), dtype=np.uint8)
+            pool[r, latent_off:latent_off + lat_page].reshape(BLOCK, rec)[s0:] = fill
             per_tok = idx_page // BLOCK
             code_b = per_tok - 4
             codes_view = pool[r, index_off:index_off + BLOCK * code_b].reshape(BLOCK, code_b)
@@ -230,7 +272,7 @@ def make_case(name: str, seq_lens, nq: int = 1, key_format: int = KEY_FP8, topk:
     return Case(name=name, batch=batch, nq=nq, seq_lens=seq_lens, key_format=key_format, topk=topk,
                 pool=pool, row_stride=row_stride, latent_off=latent_off, index_off=index_off,
                 latent_scale=latent_scale, block_table=block_table, q_index=q_index, head_w=head_w,
-                q_mla=q_mla, sm_scale=1.0 / math.sqrt(LATENT), seed=seed)
+                q_mla=q_mla, sm_scale=1.0 / math.sqrt(LATENT), seed=seed, latent_format=latent_format)
 
 
 # ---------------------------------------------------------------------------
@@ -246,6 +288,10 @@ WORKLOADS = {
     "longctx_b32_l64k-160k": dict(seq_lens=None, nq=1, heavy_tail=0.10),
     # 1M-token decode with MXFP4 index keys: batch 4
     "mxfp4_b4_l1m": dict(seq_lens=[1 << 20] * 4, nq=1, key_format=KEY_MXFP4),
+    # the long-context batch in the 10,080 B/token configuration: NVFP4
+    # latents (352 B) and MXFP4 keys (68 B), 420 B a token and layer
+    "longctx_b32_l64k-160k_nvfp4": dict(seq_lens=None, nq=1, heavy_tail=0.10, key_format=KEY_MXFP4,
+                                        latent_format=LATENT_NVFP4),
     # smaller cases of the same shapes for profiler captures (inputs still larger than L2)
     "longctx_b32_l64k": dict(seq_lens=[65536] * 32, nq=1, heavy_tail=0.1),
     "mxfp4_b8_l256k": dict(seq_lens=[1 << 18] * 8, nq=1, key_format=KEY_MXFP4),
@@ -292,7 +338,7 @@ def device_case(case: Case, device="cuda") -> DeviceCase:
     t = lambda a: torch.from_numpy(np.ascontiguousarray(a)).to(device)
     cache = binding.PagedCache(pool=t(case.pool), row_stride=case.row_stride, latent_off=case.latent_off,
                                index_off=case.index_off, key_format=case.key_format,
-                               latent_scale=case.latent_scale)
+                               latent_scale=case.latent_scale, latent_format=case.latent_format)
     batch = binding.Batch(block_table=t(case.block_table), seq_lens=t(case.seq_lens.astype(np.int32)),
                           queries_per_seq=case.nq, max_seq_len=max(case.max_len, 0))
     return DeviceCase(cache=cache, batch=batch, q_index=t(case.q_index), head_w=t(case.head_w),

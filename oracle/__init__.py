@@ -64,7 +64,7 @@ def _load():
             lib.oracle_topk.restype = i32
             lib.oracle_dcp_topk.argtypes = [P, i64, P, i32, i32, i32, P, P]
             lib.oracle_dcp_topk.restype = i32
-            lib.oracle_sparse_mla.argtypes = [P, i64, i64, i32, f64, P, i32, P, i32, i32, P, P, i32, f64, P, P]
+            lib.oracle_sparse_mla.argtypes = [P, i64, i64, i32, f64, P, i32, P, i32, i32, P, P, i32, f64, P, P, i32]
             lib.oracle_sparse_mla.restype = i32
             lib.oracle_num_threads.argtypes = []
             lib.oracle_num_threads.restype = i32
@@ -72,7 +72,8 @@ def _load():
             lib.oracle_e4m3_encode.restype = ctypes.c_uint8
             lib.oracle_e2m1_encode.argtypes = [f64]
             lib.oracle_e2m1_encode.restype = ctypes.c_uint8
-            lib.oracle_cache_append.argtypes = [P, i64, i64, i64, i32, i32, ctypes.c_float, P, i32, P, i32, i32, P, P]
+            lib.oracle_cache_append.argtypes = [P, i64, i64, i64, i32, i32, ctypes.c_float, P, i32, P, i32, i32, P, P,
+                                                i32]
             lib.oracle_cache_append.restype = i32
             lib.oracle_quantize_query.argtypes = [P, P, i32, P, P]
             lib.oracle_quantize_query.restype = i32
@@ -200,7 +201,7 @@ def sparse_mla(case, idx: np.ndarray, k: int | None = None):
         _ptr(case.pool), int(case.row_stride), int(case.latent_off), int(case.num_blocks),
         float(case.latent_scale), _ptr(case.block_table), int(case.block_table.shape[1]),
         _ptr(case.seq_lens), int(case.batch), int(case.nq), _ptr(q), _ptr(idx), k,
-        float(case.sm_scale), _ptr(out), _ptr(lse))
+        float(case.sm_scale), _ptr(out), _ptr(lse), int(getattr(case, "latent_format", 0)))
     _check(rc, "sparse_mla")
     return out, lse
 
@@ -235,7 +236,8 @@ def cache_append(case, new_latent: np.ndarray, new_key: np.ndarray) -> np.ndarra
     rc = _load().oracle_cache_append(
         _ptr(pool), int(case.row_stride), int(case.latent_off), int(case.index_off), int(case.num_blocks),
         int(case.key_format), float(case.latent_scale), _ptr(case.block_table), int(case.block_table.shape[1]),
-        _ptr(case.seq_lens), int(case.batch), int(case.nq), _ptr(lat), _ptr(key))
+        _ptr(case.seq_lens), int(case.batch), int(case.nq), _ptr(lat), _ptr(key),
+        int(getattr(case, "latent_format", 0)))
     _check(rc, "cache_append")
     return pool
 

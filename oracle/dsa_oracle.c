@@ -38,9 +38,16 @@
  *                 576 columns, values the first 512) ([K31]: the attention
  *                 is exact, restricted to the selected tokens).
  *
+ * NVFP4 latents ([K31] packed-cache section: 352 B per token instead of 576;
+ *                 the layout within the record is a reading of that size):
+ *                 dims 0..511 as E2M1 codes with one E4M3 scale per 16 dims
+ *                 (256 B + 32 B), dims 512..575 as E4M3 codes (64 B);
+ *                 value = latent_scale * e4m3(scale) * e2m1(code), resp.
+ *                 latent_scale * e4m3(code).
+ *
  * Paged cache ([K31] packed-cache section): a pool of block rows; a block row
  * holds, at caller-given byte offsets, the latent page (64 tokens x 576 B
- * e4m3) and the index-key page.  The FP8 index page stores the 64 codes
+ * e4m3, or 64 x 352 B NVFP4 records) and the index-key page.  The FP8 index page stores the 64 codes
  * rows (64 x 128 B) followed by the 64 fp32 scales; the MXFP4 page stores
  * 64 x 64 B of packed E2M1 codes followed by 64 x 4 E8M0 scales.  Token t of
  * sequence b lives in block row block_table[b][t / 64], slot t % 64.
@@ -64,6 +71,7 @@
 #define ORACLE_MLA_HEADS 96      /* MLA attention heads */
 #define ORACLE_LATENT 576        /* latent width (keys) */
 #define ORACLE_VALUE 512         /* value width (first 512 latent columns) */
+#define ORACLE_NVFP4_RECORD 352  /* bytes per token of an NVFP4 latent record */
 
 enum { ORACLE_OK = 0, ORACLE_BAD_ARG = 1, ORACLE_BAD_BLOCK = 3 };
 
@@ -423,8 +431,21 @@ int oracle_dcp_topk(const float* scores, int64_t ld, const int32_t* row_lens, in
 /* Exact sparse MLA attention over the selected tokens.                */
 /* ------------------------------------------------------------------ */
 
+/* Latent column d of a record, before the per-layer scale: e4m3 for FP8
+ * records; for NVFP4 records, dims 0..511 are e4m3(block scale d/16) times
+ * e2m1(nibble d: the low nibble of byte d/2 for even d), dims 512..575
+ * e4m3 codes after the 256 code bytes and 32 scale bytes. */
+static double latent_code_value(const uint8_t* rec, int32_t latent_format, int d) {
+  if (latent_format == 0) return oracle_e4m3_to_double(rec[d]);
+  if (d < ORACLE_VALUE) {
+    const uint8_t nib = (uint8_t)((rec[d / 2] >> (4 * (d & 1))) & 0xF);
+    return oracle_e4m3_to_double(rec[ORACLE_VALUE / 2 + d / 16]) * oracle_e2m1_to_double(nib);
+  }
+  return oracle_e4m3_to_double(rec[ORACLE_VALUE / 2 + ORACLE_VALUE / 16 + (d - ORACLE_VALUE)]);
+}
+
 /* For query row `row` (sequence row / nq), head h:
- *   c_i      = latent_scale * e4m3(latent[t_i])         (576 values)
+ *   c_i      = latent_scale * value(latent record of t_i)  (576 values; e4m3, or NVFP4)
  *   l_i      = sm_scale * sum_d q[h][d] * c_i[d]
  *   out[h][d]= sum_i softmax(l)_i * c_i[d]   for d < 512
  *   lse[h]   = ln sum_i exp(l_i)             (natural log, scaled logits)
@@ -435,9 +456,12 @@ int oracle_sparse_mla(const uint8_t* pool, int64_t row_stride, int64_t latent_of
                       double latent_scale, const int32_t* block_table, int32_t max_blocks,
                       const int32_t* seq_lens, int32_t batch, int32_t nq,
                       const uint16_t* q_bf16 /*[rows][96][576]*/, const int32_t* idx /*[rows][k]*/, int32_t k,
-                      double sm_scale, double* out /*[rows][96][512]*/, double* lse /*[rows][96]*/) {
-  if (!pool || !block_table || !seq_lens || !q_bf16 || !idx || !out || !lse || k < 1 || nq < 1)
+                      double sm_scale, double* out /*[rows][96][512]*/, double* lse /*[rows][96]*/,
+                      int32_t latent_format) {
+  if (!pool || !block_table || !seq_lens || !q_bf16 || !idx || !out || !lse || k < 1 || nq < 1 ||
+      (latent_format != 0 && latent_format != 1))
     return ORACLE_BAD_ARG;
+  const int64_t rec_bytes = latent_format == 0 ? ORACLE_LATENT : ORACLE_NVFP4_RECORD;
   int64_t rows = (int64_t)batch * nq;
   int bad = 0;
 #pragma omp parallel for schedule(dynamic) collapse(2) reduction(| : bad)
@@ -458,9 +482,9 @@ int oracle_sparse_mla(const uint8_t* pool, int64_t row_stride, int64_t latent_of
         if (t < 0) continue;
         const uint8_t* rowp = (t < vis) ? block_row(pool, row_stride, num_blocks, block_table, max_blocks, b, t) : NULL;
         if (!rowp) { bad = 1; continue; }
-        const uint8_t* c = rowp + latent_off + (int64_t)(t % ORACLE_BLOCK) * ORACLE_LATENT;
+        const uint8_t* c = rowp + latent_off + (int64_t)(t % ORACLE_BLOCK) * rec_bytes;
         double dot = 0.0;
-        for (int d = 0; d < ORACLE_LATENT; ++d) dot += q[d] * (latent_scale * oracle_e4m3_to_double(c[d]));
+        for (int d = 0; d < ORACLE_LATENT; ++d) dot += q[d] * (latent_scale * latent_code_value(c, latent_format, d));
         lg[n] = sm_scale * dot;
         lat[n] = c;
         if (lg[n] > m) m = lg[n];
@@ -475,7 +499,7 @@ int oracle_sparse_mla(const uint8_t* pool, int64_t row_stride, int64_t latent_of
         for (int i = 0; i < n; ++i) z += exp(lg[i] - m);
         for (int i = 0; i < n; ++i) {
           double p = exp(lg[i] - m) / z;
-          for (int d = 0; d < ORACLE_VALUE; ++d) o[d] += p * (latent_scale * oracle_e4m3_to_double(lat[i][d]));
+          for (int d = 0; d < ORACLE_VALUE; ++d) o[d] += p * (latent_scale * latent_code_value(lat[i], latent_format, d));
         }
         lse[row * ORACLE_MLA_HEADS + h] = m + log(z);
       }
@@ -561,11 +585,19 @@ static float fp8_scale(const float* x, int n) {
  * codes e2m1(x * 2^-E), byte E + 127).  Inputs are bf16 bits:
  * new_latent [batch*nq][576], new_key [batch*nq][128].  Returns 3 for a
  * block-table entry outside the pool.
+ * NVFP4 latents (latent_format 1; the scale rule is a reading, the pages give
+ * only the record size): per 16 dims of 0..511 the block scale code is
+ * e4m3(amax / (6 * latent_scale)) (fp32 quotient; the block's largest
+ * magnitude maps to E2M1's largest, 6), the codes are
+ * e2m1(x / (latent_scale * e4m3(scale code))) (fp32 product, fp32 quotient),
+ * and a block whose scale decodes to 0 gets zero codes; dims 512..575 are
+ * e4m3(x / latent_scale) as for FP8 latents.
  */
 int oracle_cache_append(uint8_t* pool, int64_t row_stride, int64_t latent_off, int64_t index_off,
                         int32_t num_blocks, int32_t key_format, float latent_scale, const int32_t* block_table,
                         int32_t max_blocks, const int32_t* seq_lens, int32_t batch, int32_t nq,
-                        const uint16_t* new_latent, const uint16_t* new_key) {
+                        const uint16_t* new_latent, const uint16_t* new_key, int32_t latent_format) {
+  if (latent_format != 0 && latent_format != 1) return ORACLE_BAD_ARG;
   for (int b = 0; b < batch; ++b) {
     for (int j = 0; j < nq; ++j) {
       const int64_t t = (int64_t)seq_lens[b] - nq + j;
@@ -576,9 +608,31 @@ int oracle_cache_append(uint8_t* pool, int64_t row_stride, int64_t latent_off, i
       uint8_t* row = pool + (int64_t)r * row_stride;
       const int64_t nr = (int64_t)b * nq + j;
       const uint16_t* lat = new_latent + nr * ORACLE_LATENT;
-      for (int d = 0; d < ORACLE_LATENT; ++d) {
-        const float x = (float)oracle_bf16_to_double(lat[d]);
-        row[latent_off + (int64_t)slot * ORACLE_LATENT + d] = oracle_e4m3_encode((double)(x / latent_scale));
+      if (latent_format == 0) {
+        for (int d = 0; d < ORACLE_LATENT; ++d) {
+          const float x = (float)oracle_bf16_to_double(lat[d]);
+          row[latent_off + (int64_t)slot * ORACLE_LATENT + d] = oracle_e4m3_encode((double)(x / latent_scale));
+        }
+      } else {
+        uint8_t* rec = row + latent_off + (int64_t)slot * ORACLE_NVFP4_RECORD;
+        for (int blk = 0; blk < ORACLE_VALUE / 16; ++blk) {
+          float x[16], amax = 0.f;
+          for (int d = 0; d < 16; ++d) {
+            x[d] = (float)oracle_bf16_to_double(lat[16 * blk + d]);
+            if (fabsf(x[d]) > amax) amax = fabsf(x[d]);
+          }
+          const uint8_t sc = oracle_e4m3_encode((double)(amax / (6.0f * latent_scale)));
+          const float sdec = (float)oracle_e4m3_to_double(sc);
+          const float step = latent_scale * sdec;
+          uint8_t codes[16];
+          for (int d = 0; d < 16; ++d) codes[d] = sdec > 0.f ? oracle_e2m1_encode((double)(x[d] / step)) : 0;
+          for (int d = 0; d < 16; d += 2) rec[8 * blk + d / 2] = (uint8_t)(codes[d] | (codes[d + 1] << 4));
+          rec[ORACLE_VALUE / 2 + blk] = sc;
+        }
+        for (int d = ORACLE_VALUE; d < ORACLE_LATENT; ++d) {
+          const float x = (float)oracle_bf16_to_double(lat[d]);
+          rec[ORACLE_VALUE / 2 + ORACLE_VALUE / 16 + (d - ORACLE_VALUE)] = oracle_e4m3_encode((double)(x / latent_scale));
+        }
       }
       float k[ORACLE_IDX_DIM];
       for (int d = 0; d < ORACLE_IDX_DIM; ++d) k[d] = (float)oracle_bf16_to_double(new_key[nr * ORACLE_IDX_DIM + d]);

@@ -548,3 +548,102 @@ def test_dcp_sparse_mla_bf16_partials(dcp_case):
     out8, _, O8, _ = oracle.dcp_sparse_mla(c, idx, 8)
     exact, _, _, _ = oracle.dcp_sparse_mla(c, idx, 8, partial="f64")
     assert np.all(np.abs(out8 - exact) <= 2.0**-8 * np.abs(O8).max(axis=0) + 1e-300)
+
+
+# ---------------------------------------------------------------- NVFP4 latents
+def _nvfp4_record_values(rec):
+    """The 576 values (before latent_scale) of a 352-byte record, from torch's
+    E4M3 decoder and the OCP E2M1 table: dims 0..511 scale x element, the
+    rest E4M3 codes."""
+    codes = np.stack([rec[:256] & 0xF, rec[:256] >> 4], axis=1).reshape(-1)
+    e2m1 = np.where(codes & 8, -1.0, 1.0) * _E2M1_MAG[codes & 7]
+    scale = torch.from_numpy(rec[256:288].copy()).view(torch.float8_e4m3fn).to(torch.float64).numpy()
+    tail = torch.from_numpy(rec[288:352].copy()).view(torch.float8_e4m3fn).to(torch.float64).numpy()
+    return np.concatenate([e2m1 * np.repeat(scale, 16), tail])
+
+
+def test_sparse_mla_nvfp4_single_token_closed_form():
+    """One selected token: O is its value row exactly and LSE its logit;
+    the record holds every E2M1 code in both nibbles, scales across the E4M3
+    range (subnormal to 448) and E4M3 tail codes."""
+    c = synth.make_case("nv1", seq_lens=[200, 90], nq=1, topk=8, seed=13, latent_format=synth.LATENT_NVFP4)
+    rec = np.zeros(352, dtype=np.uint8)
+    rec[:256] = [(i % 16) | (((7 * i + 3) % 16) << 4) for i in range(256)]
+    rec[256:288] = [0x01, 0x07, 0x08, 0x30, 0x38, 0x40, 0x55, 0x7E, 0x81, 0xB8, 0xFE, 0x00, 0x02] + list(range(0x10, 0x80, 6))
+    rec[288:352] = [(5 * i + 1) % 256 for i in range(64)]
+    rec[288:352][rec[288:352] % 128 == 0x7F] = 0x11       # no NaN codes
+    r = c.block_table[0, 17 // 64]
+    off = c.latent_off + (17 % 64) * 352
+    c.pool[r, off:off + 352] = rec
+    idx = np.full((2, 8), -1, dtype=np.int32)
+    idx[0, 0] = 17
+    out, lse = oracle.sparse_mla(c, idx)
+    v = _nvfp4_record_values(rec) * c.latent_scale
+    np.testing.assert_array_equal(out[0], np.broadcast_to(v[:512], (96, 512)))
+    q = _q(c, 0)
+    np.testing.assert_allclose(lse[0], c.sm_scale * (q @ v), rtol=1e-13,
+                               atol=1e-14 * c.sm_scale * float(np.max(np.abs(q) @ np.abs(v))))
+
+
+def test_sparse_mla_nvfp4_matches_library_softmax():
+    c = synth.make_case("nv2", seq_lens=[300, 90], nq=1, topk=64, seed=14, latent_format=synth.LATENT_NVFP4)
+    rng = np.random.default_rng(4)
+    idx = np.full((2, 64), -1, dtype=np.int32)
+    idx[0] = np.sort(rng.choice(300, 64, replace=False))
+    idx[1, :33] = np.sort(rng.choice(90, 33, replace=False))
+    out, lse = oracle.sparse_mla(c, idx)
+    for row in range(2):
+        sel = [t for t in idx[row] if t >= 0]
+        recs = []
+        for t in sel:
+            r = c.block_table[row, t // 64]
+            o = c.latent_off + (t % 64) * 352
+            recs.append(_nvfp4_record_values(c.pool[r, o:o + 352]) * c.latent_scale)
+        C = torch.from_numpy(np.stack(recs))
+        Q = torch.from_numpy(_q(c, row))
+        logits = (Q @ C.T) * c.sm_scale
+        np.testing.assert_allclose(out[row], (torch.softmax(logits, dim=-1) @ C[:, :512]).numpy(),
+                                   rtol=1e-10, atol=1e-12)
+        np.testing.assert_allclose(lse[row], torch.logsumexp(logits, dim=-1).numpy(), rtol=1e-12)
+
+
+def test_cache_append_nvfp4_latents():
+    """Block scale = torch's E4M3 of amax / (6 latent_scale) in fp32; codes =
+    the brute-force nearest E2M1 of x / (latent_scale * scale); an all-zero
+    block gets scale 0 and zero codes; the tail = torch's E4M3 of
+    x / latent_scale; nothing else in the pool changes."""
+    case = synth.make_case("appnv", seq_lens=[130, 64], nq=2, key_format=synth.KEY_MXFP4, seed=6,
+                           latent_format=synth.LATENT_NVFP4)
+    rng = np.random.default_rng(6)
+    lat = rng.standard_normal((case.rows, 576)).astype(np.float32) * np.exp(rng.uniform(-4, 4, (case.rows, 36, 1))).repeat(16, axis=2).reshape(case.rows, 576).astype(np.float32)
+    lat[0, 16:32] = 0.0                              # an all-zero block
+    lat[1, :3] = [1e6, -1e6, 1e-30]                  # saturation and a tiny value
+    key = rng.standard_normal((case.rows, 128)).astype(np.float32)
+    lat_b, key_b = _bf16_bits(lat), _bf16_bits(key)
+    lat = _bf16_value(lat_b)
+    pool = oracle.cache_append(case, lat_b, key_b)
+    ls = np.float32(case.latent_scale)
+    changed = np.zeros_like(pool, dtype=bool)
+    for b in range(case.batch):
+        for j in range(case.nq):
+            nr = b * case.nq + j
+            t = int(case.seq_lens[b]) - case.nq + j
+            r = case.block_table[b, t // 64]
+            slot = t % 64
+            o = case.latent_off + slot * 352
+            rec = pool[r, o:o + 352]
+            for blk in range(32):
+                xs = lat[nr, 16 * blk:16 * blk + 16]
+                sc = _torch_e4m3(np.array([np.abs(xs).max() / (np.float32(6.0) * ls)], dtype=np.float32))[0]
+                assert rec[256 + blk] == sc
+                sdec = np.float32(torch.from_numpy(np.array([sc], dtype=np.uint8)).view(torch.float8_e4m3fn).float().item())
+                step = np.float32(ls * sdec)
+                packed = rec[8 * blk:8 * blk + 8]
+                codes = np.stack([packed & 0xF, packed >> 4], axis=1).reshape(-1)
+                want = [_e2m1_brute(float(np.float32(v / step))) if sdec > 0 else 0 for v in xs]
+                assert [int(c) for c in codes] == want, (nr, blk)
+            np.testing.assert_array_equal(rec[288:], _torch_e4m3(lat[nr, 512:] / ls))
+            changed[r, o:o + 352] = True
+            changed[r, case.index_off + slot * 64:case.index_off + (slot + 1) * 64] = True
+            changed[r, case.index_off + 64 * 64 + 4 * slot:case.index_off + 64 * 64 + 4 * slot + 4] = True
+    np.testing.assert_array_equal(pool[~changed], case.pool[~changed])
