@@ -8,7 +8,7 @@ Default workload: the long-context batch (32 sequences, context ~ U(64K,
 
 Prints ONE JSON line.  ``value`` is the whole-job algorithmic HBM throughput
 (GB/s): the key bytes (132 B/token, once per sequence), the selected
-latents (576 B/token/row), queries and outputs, divided by the step time.
+latents (576 B/token/row, 352 with NVFP4 latents), queries and outputs, divided by the step time.
 The inputs exceed L2 and L2 is also flushed (a 256 MB read) between timed
 steps, outside the per-step CUDA-event pairs.  SM clocks are sampled with
 nvidia-smi over a soak of identical steps that ends with the timed region.
@@ -166,7 +166,7 @@ def cpu_baseline(case, max_rows: int = 4):
 
     sub = cpu_sample(case, max_rows)
     dt = run_oracle(sub)
-    b = roofline.step_bytes(sub.seq_lens, sub.nq, sub.topk, sub.key_format)["total"]
+    b = roofline.step_bytes(sub.seq_lens, sub.nq, sub.topk, sub.key_format, sub.latent_format)["total"]
     return {"value": b / dt / 1e9, "unit": "GB/s", "cores": oracle.num_threads(), "kind": "oracle",
             "sample": f"{sub.batch} of {case.batch} sequences ({sub.rows} query rows, "
                       f"{int(sub.seq_lens.sum())} context tokens) of the same workload, fp64 C oracle, "
@@ -385,7 +385,7 @@ def main_ours(args):
             dist.all_reduce(t, op=dist.ReduceOp.MAX)
             e2e_t = float(t.item())
 
-    b = roofline.step_bytes(case.seq_lens, case.nq, k, case.key_format)
+    b = roofline.step_bytes(case.seq_lens, case.nq, k, case.key_format, case.latent_format)
     total_bytes = b["total"] * world
     value = total_bytes / (ms * 1e-3) / 1e9
     peak, peak_kind = peaks()
@@ -395,7 +395,7 @@ def main_ours(args):
     bf16_peak, bf16_kind = tensor_peak()
     idx_tf = roofline.indexer_flops(case.seq_lens, case.nq) / (st_ms["index"] * 1e-3) / 1e12
     mla_tf = roofline.mla_flops(case.seq_lens, case.nq, k) / (st_ms["mla"] * 1e-3) / 1e12
-    mla_gbs = roofline.mla_bytes(case.seq_lens, case.nq, k) / (st_ms["mla"] * 1e-3) / 1e9
+    mla_gbs = roofline.mla_bytes(case.seq_lens, case.nq, k, case.latent_format) / (st_ms["mla"] * 1e-3) / 1e9
     stages = {"index": {"us": round(st_ms["index"] * 1e3, 2), "GB/s": round(idx_gbs, 1), "TFLOP/s": round(idx_tf, 1)},
               "topk": {"us": round(st_ms["topk"] * 1e3, 2)},
               "mla": {"us": round(st_ms["mla"] * 1e3, 2), "GB/s": round(mla_gbs, 1), "TFLOP/s": round(mla_tf, 1)}}
@@ -438,7 +438,7 @@ def main_ours(args):
             "workload": args.workload, "batch": case.batch, "queries_per_seq": case.nq,
             "seq_len_mean": float(np.mean(case.seq_lens)), "seq_len_min": int(case.seq_lens.min()),
             "seq_len_max": int(case.seq_lens.max()), "topk": k, "key_bytes": case.token_bytes(),
-            "latent_bytes": 576, "heads": 96, "index_heads": 32, "block": 64,
+            "latent_bytes": case.latent_bytes(), "heads": 96, "index_heads": 32, "block": 64,
             "algorithmic_bytes_per_step": b["total"], "parallelism": f"replicas x{world}",
             "l2": "inputs > L2; L2 flushed by a 256 MB read between timed steps (outside the step events)",
         },
@@ -484,7 +484,7 @@ def main_reference(args):
         run_oracle(sub)
     times = [run_oracle(sub) for _ in range(args.steps)]
     dt = statistics.mean(times)
-    b = roofline.step_bytes(sub.seq_lens, sub.nq, sub.topk, sub.key_format)["total"]
+    b = roofline.step_bytes(sub.seq_lens, sub.nq, sub.topk, sub.key_format, sub.latent_format)["total"]
     v = b / dt / 1e9
     line = {
         "impl": "reference", "metric": METRIC, "value": round(v, 4), "unit": "GB/s", "n_gpus": args.gpus,

@@ -18,6 +18,7 @@ LIB_PATH = os.path.join(_HERE, "libdsa.so")
 
 OK, ERR_INVALID_ARG, ERR_UNSUPPORTED, ERR_BOUNDS, ERR_TIMEOUT, ERR_CUDA, ERR_WORKSPACE = range(7)
 KEY_FP8_E4M3, KEY_MXFP4 = 0, 1
+LATENT_FP8_E4M3, LATENT_NVFP4 = 0, 1
 BLOCK, IDX_HEADS, IDX_DIM, MLA_HEADS, LATENT, VALUE, MAX_TOPK = 64, 32, 128, 96, 576, 512, 2048
 
 
@@ -33,7 +34,7 @@ class DsaError(RuntimeError):
 class PagedCacheT(ctypes.Structure):
     _fields_ = [("base", ctypes.c_void_p), ("row_stride", ctypes.c_int64), ("latent_off", ctypes.c_int64),
                 ("index_off", ctypes.c_int64), ("block_size", ctypes.c_int32), ("num_blocks", ctypes.c_int32),
-                ("key_format", ctypes.c_int32), ("latent_scale", ctypes.c_float)]
+                ("key_format", ctypes.c_int32), ("latent_scale", ctypes.c_float), ("latent_format", ctypes.c_int32)]
 
 
 class BatchT(ctypes.Structure):
@@ -143,10 +144,12 @@ class PagedCache:
     index_off: int
     key_format: int
     latent_scale: float
+    latent_format: int = 0
 
     def struct(self) -> PagedCacheT:
         return PagedCacheT(_ptr(self.pool), self.row_stride, self.latent_off, self.index_off, BLOCK,
-                           int(self.pool.shape[0]), self.key_format, float(self.latent_scale))
+                           int(self.pool.shape[0]), self.key_format, float(self.latent_scale),
+                           int(self.latent_format))
 
 
 @dataclass

@@ -58,6 +58,8 @@ EncodeTiledFn encode_fn() {
 inline bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) & (a - 1)) == 0; }
 inline size_t al256(size_t x) { return (x + 255) & ~size_t(255); }
 
+int latent_record_bytes(int latent_format) { return latent_format == DSA_LATENT_NVFP4 ? 352 : kLatent; }
+
 int index_page_bytes(int key_format) {
   return key_format == DSA_KEY_FP8_E4M3 ? kBlock * (kIdxDim + 4) : kBlock * (kIdxDim / 2 + 4);
 }
@@ -66,10 +68,11 @@ dsa_status_t check_cache(const dsa_paged_cache_t* c) {
   if (!c || !c->base || !aligned(c->base, 128)) return DSA_ERR_INVALID_ARG;
   if (c->block_size != kBlock) return DSA_ERR_UNSUPPORTED;
   if (c->key_format != DSA_KEY_FP8_E4M3 && c->key_format != DSA_KEY_MXFP4) return DSA_ERR_INVALID_ARG;
+  if (c->latent_format != DSA_LATENT_FP8_E4M3 && c->latent_format != DSA_LATENT_NVFP4) return DSA_ERR_INVALID_ARG;
   if (c->num_blocks <= 0 || c->row_stride <= 0 || (c->row_stride % 128) || (c->latent_off % 128) ||
       (c->index_off % 128) || c->latent_off < 0 || c->index_off < 0)
     return DSA_ERR_INVALID_ARG;
-  if (c->latent_off + kBlock * kLatent > c->row_stride) return DSA_ERR_INVALID_ARG;
+  if (c->latent_off + kBlock * latent_record_bytes(c->latent_format) > c->row_stride) return DSA_ERR_INVALID_ARG;
   if (c->index_off + index_page_bytes(c->key_format) > c->row_stride) return DSA_ERR_INVALID_ARG;
   return DSA_OK;
 }

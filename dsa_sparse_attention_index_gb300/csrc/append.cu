@@ -9,12 +9,18 @@
 // Encodings: round to nearest, ties to even, finite values beyond the largest
 // magnitude saturate (CUDA's FP8/FP4 conversions).  Scales in fp32:
 //   latent    code = e4m3(x / latent_scale)
+//   NVFP4     per 16 dims of 0..511: scale code c = e4m3(amax / (6 latent_scale)),
+//   latent    codes e2m1(x / (latent_scale * e4m3(c))) (0 where that scale is 0),
+//             element 2i in the low nibble of byte i; dims 512..575 as above
+//             (the record layout and this rule are readings of the packed-cache
+//             section's 352 B NVFP4 latent)
 //   FP8 key   s = amax / 448 (1 for an all-zero key), code = e4m3(x / s), s stored
 //   MXFP4 key per 32 elements E = floor(log2 amax) - 2 clamped to [-127, 127]
 //             (-127 for an all-zero block), code = e2m1(x * 2^-E), byte E + 127
 //   query     per (row, head) s = amax / 448, code = e4m3(q / s), w' = w * s
 //             (ReLU is positively homogeneous, so the score is unchanged).
 #include <cuda_bf16.h>
+#include <cuda_fp16.h>
 #include <cuda_fp4.h>
 #include <cuda_fp8.h>
 
@@ -42,7 +48,8 @@ __device__ __forceinline__ float warp_max(float v) {
 // One CTA per new token row nr = b * nq + j (token L_b - nq + j).
 __global__ void __launch_bounds__(kAppendThreads)
     cache_append_kernel(uint8_t* latent_base, uint8_t* index_base, int64_t row_stride, int32_t num_blocks,
-                        int32_t key_format, float latent_scale, const int32_t* block_table, int32_t max_blocks,
+                        int32_t key_format, int32_t latent_format, float latent_scale,
+                        const int32_t* block_table, int32_t max_blocks,
                         const int32_t* seq_lens, int32_t nq, int32_t cap, const uint16_t* new_latent,
                         const uint16_t* new_key, int32_t* status) {
   __shared__ float warp_amax[kAppendThreads / 32];
@@ -60,10 +67,35 @@ __global__ void __launch_bounds__(kAppendThreads)
     return;
   }
   const int slot = t % kBlock;
-  // latent: 576 codes
   const uint16_t* lat = new_latent + (int64_t)nr * kLatent;
-  uint8_t* lat_dst = latent_base + (int64_t)r * row_stride + (int64_t)slot * kLatent;
-  for (int d = tid; d < kLatent; d += kAppendThreads) lat_dst[d] = e4m3(bf16_bits_to_float(lat[d]) / latent_scale);
+  if (latent_format == DSA_LATENT_FP8_E4M3) {
+    // latent: 576 codes
+    uint8_t* lat_dst = latent_base + (int64_t)r * row_stride + (int64_t)slot * kLatent;
+    for (int d = tid; d < kLatent; d += kAppendThreads) lat_dst[d] = e4m3(bf16_bits_to_float(lat[d]) / latent_scale);
+  } else {
+    // NVFP4 record: thread tid owns dims 4 tid .. 4 tid + 3, four threads a 16-dim block
+    constexpr int kRec = kValue / 2 + kValue / 16 + (kLatent - kValue);
+    uint8_t* rec = latent_base + (int64_t)r * row_stride + (int64_t)slot * kRec;
+    float v[4];
+#pragma unroll
+    for (int q = 0; q < 4; ++q) v[q] = bf16_bits_to_float(lat[4 * tid + q]);
+    float amax = fmaxf(fmaxf(fabsf(v[0]), fabsf(v[1])), fmaxf(fabsf(v[2]), fabsf(v[3])));
+    amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 1));
+    amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 2));
+    const uint8_t sc = e4m3(amax / (6.0f * latent_scale));
+    const __half_raw hr = __nv_cvt_fp8_to_halfraw((__nv_fp8_storage_t)sc, __NV_E4M3);
+    const float sdec = __half2float(*reinterpret_cast<const __half*>(&hr));
+    const float step = latent_scale * sdec;
+    uint32_t code[4];
+#pragma unroll
+    for (int q = 0; q < 4; ++q)
+      code[q] = sdec > 0.f ? (uint32_t)__nv_cvt_float_to_fp4(v[q] / step, __NV_E2M1, cudaRoundNearest) & 0xFu : 0u;
+    const uint16_t two = (uint16_t)((code[0] | (code[1] << 4)) | ((code[2] | (code[3] << 4)) << 8));
+    *reinterpret_cast<uint16_t*>(rec + 2 * tid) = two;
+    if ((tid & 3) == 0) rec[kValue / 2 + tid / 4] = sc;
+    if (tid < kLatent - kValue)
+      rec[kValue / 2 + kValue / 16 + tid] = e4m3(bf16_bits_to_float(lat[kValue + tid]) / latent_scale);
+  }
   // index key: thread tid owns element tid
   const float x = bf16_bits_to_float(new_key[(int64_t)nr * kIdxDim + tid]);
   uint8_t* page = index_base + (int64_t)r * row_stride;
@@ -114,7 +146,8 @@ dsa_status_t launch_cache_append(const dsa_paged_cache_t& c, const dsa_batch_t& 
   const int cap = std::min(bt.max_blocks_per_seq * kBlock, bt.max_seq_len);
   count_launches(1);
   cache_append_kernel<<<rows, kAppendThreads, 0, st>>>(base + c.latent_off, base + c.index_off, c.row_stride,
-                                                       c.num_blocks, c.key_format, c.latent_scale, bt.block_table,
+                                                       c.num_blocks, c.key_format, c.latent_format,
+                                                       c.latent_scale, bt.block_table,
                                                        bt.max_blocks_per_seq, bt.seq_lens, bt.queries_per_seq, cap,
                                                        new_latent, new_key, status);
   return launch_status();

@@ -323,6 +323,30 @@ __device__ __forceinline__ void e4m3x4_to_bf16x4(uint32_t w, uint32_t& lo, uint3
   asm("mul.rn.bf16x2 %0, %1, %2;" : "=r"(hi) : "r"(f1), "r"(k2_120));
 }
 
+// 16 E2M1 codes (w0, w1: element 2i in the low nibble of byte i) times one
+// E4M3 block scale -> 16 bf16 (o[j]: elements 2j, 2j + 1), exactly: an E2M1
+// value has 2 significant bits and an E4M3 scale 4, so the product fits
+// bf16's 8.  Each nibble's exponent and mantissa bits go to bf16's lowest
+// exponent bits and top mantissa bit, so the bf16 reads 2^-126 times the E2M1
+// value (E2M1's zero exponent lands on bf16 subnormals the same way); one
+// multiply by 2^126 and one by the scale (itself widened as E4M3 is above).
+__device__ __forceinline__ void nvfp4x16_to_bf16x16(uint32_t w0, uint32_t w1, uint32_t scale_byte,
+                                                    uint32_t (&o)[8]) {
+  const uint32_t sx = scale_byte * 0x00010001u;
+  const uint32_t sf = ((sx << 4) & 0x07F007F0u) | ((sx << 8) & 0x80008000u);
+  uint32_t s2;
+  asm("mul.rn.bf16x2 %0, %1, %2;" : "=r"(s2) : "r"(sf), "r"(0x7B807B80u));  // 2^120: E4M3's bias
+#pragma unroll
+  for (int j = 0; j < 8; ++j) {
+    const uint32_t byte = ((j < 4 ? w0 : w1) >> (8 * (j & 3))) & 0xFFu;
+    const uint32_t y = (byte & 0x0Fu) | ((byte & 0xF0u) << 12);  // the two nibbles in the two 16-bit lanes
+    const uint32_t f = ((y << 6) & 0x01C001C0u) | ((y << 12) & 0x80008000u);
+    uint32_t v;
+    asm("mul.rn.bf16x2 %0, %1, %2;" : "=r"(v) : "r"(f), "r"(0x7E807E80u));  // 2^126
+    asm("mul.rn.bf16x2 %0, %1, %2;" : "=r"(o[j]) : "r"(v), "r"(s2));
+  }
+}
+
 // Two E4M3 bytes (low byte = first element) -> two bf16 (low half = first).
 __device__ __forceinline__ uint32_t e4m3x2_to_bf16x2(uint16_t v) {
   __half2_raw h = __nv_cvt_fp8x2_to_halfraw2(static_cast<__nv_fp8x2_storage_t>(v), __NV_E4M3);

@@ -59,6 +59,8 @@ constexpr int kTileBytes = kDBlocks * kTileDBlockBytes;  // 36,864
 constexpr int kPBytes = kHeads * kTileTok * 2;         // 6,144
 constexpr int kMaxChunk = 1024;                        // tokens per CTA
 constexpr int kInvariantChunk = 512;                   // tokens per CTA in the batch-invariant mode
+constexpr int kNvRecord = kValue / 2 + kValue / 16 + (kLatent - kValue);  // 352 B: NVFP4 latent record
+constexpr int kNvUnits = kValue / 16;                  // 16-dim units of E2M1 codes (the rest are E4M3)
 constexpr int kMaxSplit = 16;                          // chunks per row
 constexpr int kMaxFusedSplit = 8;                      // chunks combined inside the kernel (a portable cluster)
 // 12 warps: softmax 0-3, loaders 4-9, QK issuer 10, PV issuer 11.  Three warps
@@ -133,8 +135,13 @@ __device__ __forceinline__ bool bar_or_softmax(bool v) {
   return r != 0;
 }
 
+// kNV: NVFP4 latent records (352 B: E2M1 dims 0..511 with an E4M3 scale per
+// 16 dims, E4M3 dims 512..575), else E4M3 records (576 B).  Both are widened
+// to the same bf16 tile, exactly.
+template <bool kNV>
 __global__ void __launch_bounds__(kThreads, 1)
     sparse_mla_kernel(const __grid_constant__ CUtensorMap tmap_q, const MlaParams p) {
+  constexpr int kRec = kNV ? kNvRecord : kLatent;  // bytes per token record
   // S = Q K^T: A = Q (K-major), B = latent tile (K-major); M = 128, N = 32.
   constexpr uint32_t kIdescQK = make_idesc(kFmtBF16, kFmtBF16, 0, 0, 128, kTileTok);
   // O^T = V^T P^T: A = latent tile (MN-major, M = dims), B = P (K-major); M = 128, N = 96.
@@ -309,25 +316,41 @@ __global__ void __launch_bounds__(kThreads, 1)
       // tile i+3 overlaps the rest; each tile is widened to bf16 in registers
       // before its buffer is free, so only the shared-memory stores wait
       uint4 buf0[kChunksPerThread], buf1[kChunksPerThread], buf2[kChunksPerThread];
+      // A unit is 16 dims (32 bytes of bf16 in the tile): for E4M3 records the
+      // 16 code bytes; for NVFP4 units below kNvUnits the 8 code bytes (.x, .y)
+      // and the scale byte (.z), above them the 16 E4M3 tail bytes.
       auto load = [&](int i, uint4 (&buf)[kChunksPerThread]) {
         if (i >= ntiles) return;
         const int32_t phys = tok_phys[i * kTileTok + tok];
-        const int64_t off = (int64_t)(phys >> 6) * p.row_stride + (phys & (kBlock - 1)) * kLatent;
+        const uint8_t* rec = p.latent_base + (int64_t)(phys >> 6) * p.row_stride + (phys & (kBlock - 1)) * kRec;
 #pragma unroll
         for (int c = 0; c < kChunksPerThread; ++c) {
+          const int u = g + kChunksPerThread * c;
           buf[c] = make_uint4(0, 0, 0, 0);
-          if (phys >= 0) buf[c] = __ldg(reinterpret_cast<const uint4*>(p.latent_base + off) + (g + kChunksPerThread * c));
+          if (phys < 0) continue;
+          if (!kNV) {
+            buf[c] = __ldg(reinterpret_cast<const uint4*>(rec) + u);
+          } else if (u < kNvUnits) {
+            const uint2 w = __ldg(reinterpret_cast<const uint2*>(rec) + u);
+            buf[c] = make_uint4(w.x, w.y, (uint32_t)__ldg(rec + kValue / 2 + u), 0u);
+          } else {
+            buf[c] = __ldg(reinterpret_cast<const uint4*>(rec + kValue / 2 + kValue / 16) + (u - kNvUnits));
+          }
         }
       };
       auto store = [&](int i, const uint4 (&buf)[kChunksPerThread]) -> bool {
         if (i >= ntiles) return true;
-        uint4 cv[2 * kChunksPerThread];  // the widened chunks: 32 bytes of bf16 each
+        uint4 cv[2 * kChunksPerThread];  // the widened units: 32 bytes of bf16 each
 #pragma unroll
         for (int c = 0; c < kChunksPerThread; ++c) {
-          const uint32_t w[4] = {buf[c].x, buf[c].y, buf[c].z, buf[c].w};
           uint32_t o[8];
+          if (kNV && g + kChunksPerThread * c < kNvUnits) {
+            nvfp4x16_to_bf16x16(buf[c].x, buf[c].y, buf[c].z, o);
+          } else {
+            const uint32_t w[4] = {buf[c].x, buf[c].y, buf[c].z, buf[c].w};
 #pragma unroll
-          for (int q = 0; q < 4; ++q) e4m3x4_to_bf16x4(w[q], o[2 * q], o[2 * q + 1]);
+            for (int q = 0; q < 4; ++q) e4m3x4_to_bf16x4(w[q], o[2 * q], o[2 * q + 1]);
+          }
           cv[2 * c] = make_uint4(o[0], o[1], o[2], o[3]);
           cv[2 * c + 1] = make_uint4(o[4], o[5], o[6], o[7]);
         }
@@ -622,13 +645,14 @@ __global__ void __launch_bounds__(256) mla_combine_kernel(const float* __restric
 
 // Whether clusters of `nsplit` CTAs of the MLA kernel can be resident on this
 // device (asked once per device and size).
+template <bool kNV>
 bool fused_cluster_ok(int nsplit) {
   static int known[64][kMaxFusedSplit + 1] = {};  // 0 unknown, 1 yes, 2 no
   int dev = 0;
   cudaGetDevice(&dev);
   if (dev < 0 || dev >= 64 || nsplit < 1 || nsplit > kMaxFusedSplit) return false;
   if (known[dev][nsplit] == 0) {
-    bool ok = cudaFuncSetAttribute(sparse_mla_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+    bool ok = cudaFuncSetAttribute(sparse_mla_kernel<kNV>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                    (int)kSmemBytes) == cudaSuccess;
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3((unsigned)nsplit);
@@ -642,7 +666,7 @@ bool fused_cluster_ok(int nsplit) {
     cfg.attrs = attr;
     cfg.numAttrs = 1;
     int n = 0;
-    ok = ok && cudaOccupancyMaxActiveClusters(&n, sparse_mla_kernel, &cfg) == cudaSuccess && n > 0;
+    ok = ok && cudaOccupancyMaxActiveClusters(&n, sparse_mla_kernel<kNV>, &cfg) == cudaSuccess && n > 0;
     cudaGetLastError();  // a refused query leaves no error behind
     known[dev][nsplit] = ok ? 1 : 2;
   }
@@ -716,12 +740,19 @@ bool mla_setup(const dsa_paged_cache_t& c, const dsa_batch_t& bt, const uint16_t
   int dev = 0;
   cudaGetDevice(&dev);
   if (dev < 64 && !attr_set[dev]) {
-    if (cuda_status(cudaFuncSetAttribute(sparse_mla_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+    if (cuda_status(cudaFuncSetAttribute(sparse_mla_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         (int)kSmemBytes)) != DSA_OK ||
+        cuda_status(cudaFuncSetAttribute(sparse_mla_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          (int)kSmemBytes)) != DSA_OK)
       return false;
     attr_set[dev] = true;
   }
   return true;
+}
+
+using MlaKernel = void (*)(const CUtensorMap, const MlaParams);
+MlaKernel mla_kernel_for(const dsa_paged_cache_t& c) {
+  return c.latent_format == DSA_LATENT_NVFP4 ? sparse_mla_kernel<true> : sparse_mla_kernel<false>;
 }
 
 }  // namespace
@@ -750,7 +781,7 @@ dsa_status_t launch_sparse_mla_partials(const dsa_paged_cache_t& c, const dsa_ba
   cfg.attrs = attrs;
   cfg.numAttrs = 1;
   count_launches(1);
-  if (cuda_status(cudaLaunchKernelEx(&cfg, sparse_mla_kernel, qmap, p)) != DSA_OK) return DSA_ERR_CUDA;
+  if (cuda_status(cudaLaunchKernelEx(&cfg, mla_kernel_for(c), qmap, p)) != DSA_OK) return DSA_ERR_CUDA;
   return launch_status();
 }
 
@@ -774,7 +805,8 @@ dsa_status_t launch_sparse_mla(const dsa_paged_cache_t& c, const dsa_batch_t& bt
     return DSA_ERR_CUDA;
   // Up to kMaxFusedSplit chunks per row: the row's CTAs form a cluster and
   // merge the chunks themselves; more chunks take the combine kernel.
-  p.fuse = nsplit <= kMaxFusedSplit && fused_cluster_ok(nsplit) ? 1 : 0;
+  const bool nv = c.latent_format == DSA_LATENT_NVFP4;
+  p.fuse = nsplit <= kMaxFusedSplit && (nv ? fused_cluster_ok<true>(nsplit) : fused_cluster_ok<false>(nsplit)) ? 1 : 0;
   // the launches may overlap the previous kernel's tail; each waits for its inputs
   cudaLaunchAttribute attrs[2];
   attrs[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
@@ -791,7 +823,7 @@ dsa_status_t launch_sparse_mla(const dsa_paged_cache_t& c, const dsa_batch_t& bt
   cfg.attrs = attrs;
   cfg.numAttrs = p.fuse ? 2 : 1;
   count_launches(1);
-  if (cuda_status(cudaLaunchKernelEx(&cfg, sparse_mla_kernel, qmap, p)) != DSA_OK) return DSA_ERR_CUDA;
+  if (cuda_status(cudaLaunchKernelEx(&cfg, mla_kernel_for(c), qmap, p)) != DSA_OK) return DSA_ERR_CUDA;
   if (p.fuse) return launch_status();
   cudaLaunchConfig_t cfg2 = cfg;
   cfg2.numAttrs = 1;

@@ -6,7 +6,8 @@ the chip for one layer-step, independent of how the kernels are written:
 * index keys: every visible token's key once per sequence — 132 B (128 E4M3
   codes + fp32 scale) or 68 B (128 E2M1 + 4 E8M0) — all draft rows of a
   sequence share one read;
-* latents: 576 B for each selected token of each query row (up to top-k);
+* latents: 576 B (E4M3) or 352 B (NVFP4) for each selected token of each
+  query row (up to top-k);
 * queries and head weights in, attention output (bf16 [96, 512]) and LSE
   (fp32 [96]) out.
 
@@ -22,6 +23,7 @@ import numpy as np
 IDX_HEADS, IDX_DIM = 32, 128
 MLA_HEADS, LATENT, VALUE = 96, 576, 512
 KEY_BYTES = {0: 132, 1: 68}
+LATENT_BYTES = {0: 576, 1: 352}
 
 
 def visible_lengths(seq_lens, nq: int) -> np.ndarray:
@@ -30,12 +32,12 @@ def visible_lengths(seq_lens, nq: int) -> np.ndarray:
     return np.maximum(L - (nq - 1) + j, 0)
 
 
-def step_bytes(seq_lens, nq: int = 1, topk: int = 2048, key_format: int = 0) -> dict:
+def step_bytes(seq_lens, nq: int = 1, topk: int = 2048, key_format: int = 0, latent_format: int = 0) -> dict:
     seq_lens = np.asarray(seq_lens, dtype=np.int64)
     vis = visible_lengths(seq_lens, nq)
     rows = len(vis)
     keys = int(KEY_BYTES[key_format] * seq_lens.sum())
-    latents = int(LATENT * np.minimum(vis, topk).sum())
+    latents = int(LATENT_BYTES[latent_format] * np.minimum(vis, topk).sum())
     q_in = rows * (IDX_HEADS * IDX_DIM + IDX_HEADS * 4 + MLA_HEADS * LATENT * 2)
     out = rows * (MLA_HEADS * VALUE * 2 + MLA_HEADS * 4)
     return dict(keys=keys, latents=latents, queries=q_in, outputs=out,
@@ -48,10 +50,10 @@ def indexer_bytes(seq_lens, nq: int = 1, key_format: int = 0) -> int:
     return int(KEY_BYTES[key_format] * seq_lens.sum() + rows * (IDX_HEADS * IDX_DIM + IDX_HEADS * 4))
 
 
-def mla_bytes(seq_lens, nq: int = 1, topk: int = 2048) -> int:
+def mla_bytes(seq_lens, nq: int = 1, topk: int = 2048, latent_format: int = 0) -> int:
     vis = visible_lengths(seq_lens, nq)
     rows = len(vis)
-    return int(LATENT * np.minimum(vis, topk).sum()
+    return int(LATENT_BYTES[latent_format] * np.minimum(vis, topk).sum()
                + rows * (MLA_HEADS * LATENT * 2 + MLA_HEADS * VALUE * 2 + MLA_HEADS * 4))
 
 

@@ -44,7 +44,7 @@
 extern "C" {
 #endif
 
-#define DSA_API_VERSION 1
+#define DSA_API_VERSION 2
 #define DSA_BLOCK_SIZE 64        /* tokens per page */
 #define DSA_INDEX_HEADS 32       /* light indexer heads */
 #define DSA_INDEX_DIM 128        /* indexer head dim */
@@ -74,16 +74,27 @@ typedef enum dsa_key_format {
                                 no per-token fp32 scale (AMD section: 132 B -> 68 B) */
 } dsa_key_format_t;
 
+typedef enum dsa_latent_format {
+  DSA_LATENT_FP8_E4M3 = 0,   /* 576 B/token: page = 64 records of 576 E4M3 codes */
+  DSA_LATENT_NVFP4 = 1       /* 352 B/token (packed-cache section: NVFP4 latents): page = 64 records of
+                                256 B packed E2M1 for dims 0..511 (element 2i in the low nibble of
+                                byte i), 32 E4M3 block scales (one per 16 dims of 0..511), and 64
+                                E4M3 codes for dims 512..575 */
+} dsa_latent_format_t;
+
 /* One layer's view of the packed paged cache. */
 typedef struct dsa_paged_cache {
   void* base;              /* device address of block row 0; 128-byte aligned */
   int64_t row_stride;      /* bytes between block rows; multiple of 128 */
-  int64_t latent_off;      /* byte offset of the latent page in a row (64 x 576 E4M3); multiple of 128 */
+  int64_t latent_off;      /* byte offset of the latent page in a row (64 records); multiple of 128 */
   int64_t index_off;       /* byte offset of the index-key page in a row; multiple of 128 */
   int32_t block_size;      /* tokens per page; must be DSA_BLOCK_SIZE */
   int32_t num_blocks;      /* block rows in the pool (valid table entries are 0..num_blocks-1) */
   int32_t key_format;      /* dsa_key_format_t */
-  float latent_scale;      /* per-layer dequantisation scale of the E4M3 latents */
+  float latent_scale;      /* per-layer dequantisation scale of the latents: value = latent_scale *
+                              e4m3(code), or for NVFP4 dims 0..511 latent_scale * e4m3(block scale)
+                              * e2m1(code) */
+  int32_t latent_format;   /* dsa_latent_format_t (0 = FP8, the zero-initialised default) */
 } dsa_paged_cache_t;
 
 /* The batch of one decode step. */

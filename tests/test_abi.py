@@ -33,7 +33,7 @@ def test_every_declared_symbol_is_exported(lib):
 
 
 def test_version_and_status_strings(lib):
-    assert lib.dsa_api_version() == 1
+    assert lib.dsa_api_version() == 2
     for code in range(7):
         assert binding.status_string(code).startswith("DSA_")
     assert "unknown" in binding.status_string(99)
@@ -74,6 +74,15 @@ def test_host_validation_without_device(lib):
                             None) == B.ERR_UNSUPPORTED
     assert lib.dsa_dcp_topk(None, 0, None, 1, 10, 2048, 0, None, None, None, 0, st, None) == B.ERR_INVALID_ARG
     assert lib.dsa_dcp_topk(128, 16, 256, 1, 10, 2048, 8, 512, None, None, 0, st, None) == B.ERR_WORKSPACE
+    # latent formats: FP8 (0) and NVFP4 (1, 352-byte records: a smaller row fits); nothing else
+    c.latent_format = 2
+    assert lib.dsa_index_scores(ctypes.byref(c), ctypes.byref(b), 1024, 2048, 4096, 104, st,
+                                None) == B.ERR_INVALID_ARG
+    c.latent_format, c.row_stride = B.LATENT_NVFP4, 64 * 352 + 64 * 132 + 128
+    c.index_off = 64 * 352 + 64                     # not a multiple of 128
+    assert lib.dsa_index_scores(ctypes.byref(c), ctypes.byref(b), 1024, 2048, 4096, 104, st,
+                                None) == B.ERR_INVALID_ARG
+    c.latent_format, c.row_stride, c.index_off = 0, 45312, 36864
     # bf16 scores: rows of a multiple of 8 elements
     assert lib.dsa_topk_bf16(128, 12, 256, 1, 10, 2048, 512, st, None) == B.ERR_INVALID_ARG
     assert lib.dsa_topk_bf16(128, 16, 256, 1, 10, 0, 512, st, None) == B.ERR_INVALID_ARG

@@ -43,3 +43,16 @@ def test_step_bytes_counts_each_sequence_key_once():
     assert list(vis) == [997, 998, 999, 1000, 2997, 2998, 2999, 3000]
     assert b["latents"] == 576 * int(np.minimum(vis, 2048).sum())
     assert roofline.mla_flops([4096]) == 2 * 96 * 2048 * (576 + 512)
+
+
+def test_nvfp4_latent_record_and_the_420_byte_configuration():
+    """352 B NVFP4 latents: the generator's record and page, and with MXFP4
+    keys a pool row of 420 B a token (24 layers: the printed 10,080 B)."""
+    rec = synth.LATENT_RECORD[synth.LATENT_NVFP4]
+    assert rec == G["latent_bytes"]["nvfp4"] == 512 // 2 + 512 // 16 + 64
+    c = synth.make_case("nvg", seq_lens=[130], key_format=synth.KEY_MXFP4, latent_format=synth.LATENT_NVFP4, seed=1)
+    assert c.row_stride == synth.BLOCK * (rec + G["index_key_bytes"]["mxfp4"])
+    assert G["layers"] * c.row_stride // synth.BLOCK == G["per_token_bytes_24_layers"]["k31_nvfp4_latent_mxfp4_key"]
+    assert c.row_stride % 128 == 0 and c.index_off % 128 == 0
+    b = roofline.step_bytes([1000], topk=2048, key_format=1, latent_format=1)
+    assert b["keys"] == 68 * 1000 and b["latents"] == 352 * 1000

@@ -31,11 +31,21 @@ def _new_rows(rows, seed, extreme_latents=True):
     return _bf16_bits(lat), _bf16_bits(key)
 
 
-@pytest.mark.parametrize("fmt", [synth.KEY_FP8, synth.KEY_MXFP4])
+@pytest.mark.parametrize("fmt,lfmt", [(synth.KEY_FP8, synth.LATENT_FP8), (synth.KEY_MXFP4, synth.LATENT_FP8),
+                                       (synth.KEY_MXFP4, synth.LATENT_NVFP4), (synth.KEY_FP8, synth.LATENT_NVFP4)])
 @pytest.mark.parametrize("lens,nq", [([1000, 64, 777], 1), ([5000, 130], 4), ([3000], 64)])
-def test_cache_append_matches_oracle(fmt, lens, nq):
-    case = synth.make_case("ap", seq_lens=lens, nq=nq, key_format=fmt, seed=nq + fmt, spare_blocks=2)
+def test_cache_append_matches_oracle(fmt, lfmt, lens, nq):
+    case = synth.make_case("ap", seq_lens=lens, nq=nq, key_format=fmt, seed=nq + fmt, spare_blocks=2,
+                           latent_format=lfmt)
     lat, key = _new_rows(case.rows, seed=len(lens) + nq)
+    if lfmt == synth.LATENT_NVFP4 and case.rows >= 2:
+        # NVFP4 blocks with a wide spread, an all-zero block and a tiny one
+        rng = np.random.default_rng(nq)
+        x = (rng.standard_normal((case.rows, 576)) * np.exp(rng.uniform(-6, 6, (case.rows, 36, 1))).repeat(16, 2)
+             .reshape(case.rows, 576)).astype(np.float32)
+        x[1, 32:48] = 0.0
+        x[1, 48:64] *= 1e-30
+        lat = _bf16_bits(x)
     ref = oracle.cache_append(case, lat, key)
     dc = synth.device_case(case)
     st = _status()
@@ -76,11 +86,13 @@ def test_quantize_index_query_matches_oracle():
     np.testing.assert_array_equal(w_out.cpu().numpy(), w_ref)
 
 
-@pytest.mark.parametrize("fmt,nq", [(synth.KEY_FP8, 1), (synth.KEY_FP8, 4), (synth.KEY_MXFP4, 1)])
-def test_step_that_owns_its_cache_update(fmt, nq):
+@pytest.mark.parametrize("fmt,nq,lfmt", [(synth.KEY_FP8, 1, synth.LATENT_FP8), (synth.KEY_FP8, 4, synth.LATENT_FP8),
+                                         (synth.KEY_MXFP4, 1, synth.LATENT_FP8),
+                                         (synth.KEY_MXFP4, 1, synth.LATENT_NVFP4)])
+def test_step_that_owns_its_cache_update(fmt, nq, lfmt):
     """Write the step's new tokens, quantise the indexer query, then run the
     fused step; every stage against the oracle on the updated cache."""
-    case = synth.make_case("own", seq_lens=[9000, 4100], nq=nq, key_format=fmt, seed=31 + nq)
+    case = synth.make_case("own", seq_lens=[9000, 4100], nq=nq, key_format=fmt, seed=31 + nq, latent_format=lfmt)
     rng = np.random.default_rng(7)
     # no saturating latents here: one selected +-448 code would make the MLA's
     # error scale with its value (the attended values' spread), not with 1e-2
@@ -92,7 +104,7 @@ def test_step_that_owns_its_cache_update(fmt, nq):
     case.q_index, case.head_w = oracle.quantize_query(q_b, w)
     # the GPU's view: the original pool, updated and quantised on the device
     dc_pool = torch.from_numpy(synth.make_case("own", seq_lens=[9000, 4100], nq=nq, key_format=fmt,
-                                               seed=31 + nq).pool).cuda()
+                                               seed=31 + nq, latent_format=lfmt).pool).cuda()
     dc = synth.device_case(case)
     dc.cache.pool.copy_(dc_pool)
     st = _status()

@@ -8,6 +8,7 @@ Workloads (seeded as the benchmark seeds them):
   speculative decode   8 sequences x 4 causal draft rows, 32,768 tokens each
   long-context batch   32 sequences, 64K-160K tokens, heavy-tailed keys
   1M-token decode      4 sequences of 1,048,576 tokens, MXFP4 index keys
+  420 B/token batch    the long-context batch with NVFP4 latents and MXFP4 keys
 """
 import dataclasses
 
@@ -26,6 +27,7 @@ SAMPLES = {
     "specdecode_b8x4_l32768": (0, 3, 13, 30),   # first and last draft rows of several sequences
     "longctx_b32_l64k-160k": (0, 11, 31),
     "mxfp4_b4_l1m": (0, 3),
+    "longctx_b32_l64k-160k_nvfp4": (5, 31),
 }
 
 
@@ -55,7 +57,7 @@ def _check_rows(case, res, rows):
         check_mla(rc, idx[r:r + 1], o[r:r + 1], l[r:r + 1])
 
 
-@pytest.mark.parametrize("name", ["specdecode_b8x4_l32768", "mxfp4_b4_l1m"])
+@pytest.mark.parametrize("name", ["specdecode_b8x4_l32768", "mxfp4_b4_l1m", "longctx_b32_l64k-160k_nvfp4"])
 def test_full_size_decode_step_sampled_rows(name):
     case = synth.workload(name, seed=0)
     _check_rows(case, _run_step(case), SAMPLES[name])
