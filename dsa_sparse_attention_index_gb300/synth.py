@@ -295,6 +295,8 @@ WORKLOADS = {
     # smaller cases of the same shapes for profiler captures (inputs still larger than L2)
     "longctx_b32_l64k": dict(seq_lens=[65536] * 32, nq=1, heavy_tail=0.1),
     "mxfp4_b8_l256k": dict(seq_lens=[1 << 18] * 8, nq=1, key_format=KEY_MXFP4),
+    "longctx_b32_l64k_nvfp4": dict(seq_lens=[65536] * 32, nq=1, heavy_tail=0.1, key_format=KEY_MXFP4,
+                                   latent_format=LATENT_NVFP4),
     # chunked-prefill append: 2048 new query rows on a 151,552-token prefix
     "prefill_q2048_l153600": dict(seq_lens=[153600], nq=2048),
 }
