@@ -1,10 +1,13 @@
 """GPU parity: every stage of the CUDA path against the fp64 oracle on the
 same seeded inputs, called through the C ABI.
 
-Tolerances (written here, derived in the design doc):
-  scores   |gpu - ref| <= 1e-5 * max(|ref|, A_t), A_t = sum_h |w_h| |scale_t| sum_d |q_hd k_td|
+Tolerances:
+  scores   |gpu - ref| <= 1e-5 * max(|ref|, A_t), A_t = sum_h |w_h| |scale_t| sum_d |q_hd k_td|:
+           the weights mix signs, so a score can be near 0 and a purely relative
+           bound is ill-posed; an fp32 dot of 128 terms is within 128 * 2^-24 * A_t
   top-k    bit-exact (both sides select on the same fp32 scores)
-  MLA      |out - ref| <= 1e-2 (bf16 output), |lse - ref| <= 1e-4
+  MLA      |out - ref| <= 1e-2 (bf16 output with |O| below about 2, and P
+           rounded to bf16 before the PV product), |lse - ref| <= 1e-4
 """
 import numpy as np
 import pytest
