@@ -173,18 +173,54 @@ def cpu_baseline(case, max_rows: int = 4):
                       f"{dt:.2f} s"}
 
 
+# ---------------------------------------------------------------- replicas
+class Replicas:
+    """This process among torchrun's ranks (RANK, LOCAL_RANK, WORLD_SIZE): one
+    independent replica of the step per GPU.  The data path has no exchange;
+    the ranks only meet at barriers around the timed region and in the max
+    over ranks of the measured times."""
+
+    def __init__(self, backend: str):
+        self.world = int(os.environ.get("WORLD_SIZE", "1"))
+        self.rank = int(os.environ.get("RANK", "0"))
+        self.local = int(os.environ.get("LOCAL_RANK", "0"))
+        if self.world > 1:
+            import torch.distributed as dist
+
+            dist.init_process_group(backend)
+
+    def barrier(self):
+        if self.world > 1:
+            import torch.distributed as dist
+
+            dist.barrier()
+
+    def max(self, x: float, device="cpu") -> float:
+        """The largest x over the ranks (every rank gets it)."""
+        if self.world == 1:
+            return float(x)
+        import torch
+        import torch.distributed as dist
+
+        t = torch.tensor([float(x)], dtype=torch.float64, device=device)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        return float(t.item())
+
+    def close(self):
+        if self.world > 1:
+            import torch.distributed as dist
+
+            dist.destroy_process_group()
+
+
 # ---------------------------------------------------------------- GPU arm
 def main_ours(args):
     import torch
-    import torch.distributed as dist
 
     from dsa_sparse_attention_index_gb300 import binding
 
-    world = int(os.environ.get("WORLD_SIZE", "1"))
-    rank = int(os.environ.get("RANK", "0"))
-    local = int(os.environ.get("LOCAL_RANK", "0"))
-    if world > 1:
-        dist.init_process_group("nccl")
+    reps = Replicas("nccl")
+    world, rank, local = reps.world, reps.rank, reps.local
     torch.cuda.set_device(local)
     binding.lib()  # fail loudly if the CUDA library is missing
 
@@ -218,8 +254,7 @@ def main_ours(args):
                             status, stream=stream)
 
     def barrier():
-        if world > 1:
-            dist.barrier()
+        reps.barrier()
         torch.cuda.synchronize()
 
     for _ in range(args.warmup):
@@ -250,11 +285,7 @@ def main_ours(args):
         t_wall = time.perf_counter() - t_wall
     clocks = clk.summary()
     step_ms = [e0.elapsed_time(e1) for e0, e1 in ev]
-    ms = statistics.mean(step_ms)
-    if world > 1:
-        t = torch.tensor([ms], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        ms = float(t.item())
+    ms = reps.max(statistics.mean(step_ms), dev)
     assert status.item() == 0, binding.status_string(status.item())
 
     # ---- per-stage attribution (same kernels through the three stage entry points)
@@ -379,11 +410,7 @@ def main_ours(args):
             torch.cuda.synchronize()
             if it >= args.warmup:
                 e2e_ms.append(e0.elapsed_time(e1))
-        e2e_t = statistics.mean(e2e_ms)
-        if world > 1:
-            t = torch.tensor([e2e_t], device=dev)
-            dist.all_reduce(t, op=dist.ReduceOp.MAX)
-            e2e_t = float(t.item())
+        e2e_t = reps.max(statistics.mean(e2e_ms), dev)
 
     b = roofline.step_bytes(case.seq_lens, case.nq, k, case.key_format, case.latent_format)
     total_bytes = b["total"] * world
@@ -458,8 +485,7 @@ def main_ours(args):
         line["cpu_baseline"] = cpu_baseline(case)
     if rank == 0:
         print(json.dumps(line), flush=True)
-    if world > 1:
-        dist.destroy_process_group()
+    reps.close()
 
 
 def load_traffic(workload):
