@@ -14,7 +14,7 @@ import torch
 
 import oracle
 from dsa_sparse_attention_index_gb300 import binding, synth
-from test_gpu_parity import LSE_ATOL, OUT_ATOL, _gpu_mla, _status, check_mla, gpu_scores
+from test_gpu_parity import LSE_ATOL, OUT_ATOL, _gpu_mla, _status, gpu_scores
 
 pytestmark = pytest.mark.gpu
 
