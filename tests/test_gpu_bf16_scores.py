@@ -174,3 +174,13 @@ def test_decode_step_bf16_matches_oracle(name, kw):
         kth = np.sort(vals[r, :vis])[::-1][case.topk - 1]
         diff = set(idx[r][idx[r] >= 0]) ^ set(idx32[r][idx32[r] >= 0])
         assert all(vals[r, t] == kth for t in diff), r
+
+
+def test_decode_step_bf16_in_the_420_byte_configuration():
+    """BF16 scores with MXFP4 keys and NVFP4 latents."""
+    case = synth.make_case("b16nv", seq_lens=[20000, 3000], seed=29, key_format=synth.KEY_MXFP4,
+                           latent_format=synth.LATENT_NVFP4, heavy_tail=0.1)
+    dc, scores, idx, o, l = _run_step_bf16(case)
+    check_scores_bf16(case, scores)
+    np.testing.assert_array_equal(idx, oracle.topk(_values(scores), case.row_lens(), case.topk))
+    check_mla(case, idx, o, l)

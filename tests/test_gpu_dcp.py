@@ -39,7 +39,7 @@ def _check(m, lens, k, shards):
     ref, ref_stats = oracle.dcp_topk(m, lens, k, shards)
     np.testing.assert_array_equal(got, ref)
     np.testing.assert_array_equal(stats, ref_stats.astype(np.int32))
-    return stats
+    return got, stats
 
 
 @pytest.mark.parametrize("shards", [1, 2, 3, 5, 8])
@@ -72,7 +72,7 @@ def test_dcp_topk_resend(shards):
     m[1, 0::shards] += 50.0
     m[1, (shards - 1)::shards] += 50.0
     lens = np.array([n, n, n - 11], dtype=np.int32)
-    stats = _check(m, lens, 2048, shards)
+    _, stats = _check(m, lens, 2048, shards)
     assert stats[0, 1] >= 1 and stats[2, 1] == 0
 
 
@@ -191,3 +191,16 @@ def test_dcp_sparse_mla_small_k_and_empty_rows(k):
     o, l, po, pl = _gpu_dcp_mla(case, dc, idx, 5)
     check_dcp_mla(case, idx, 5, o, l, po, pl)
     assert np.all(o[1] == 0) and np.all(np.isneginf(l[1]))
+
+
+def test_dcp_merge_then_combine_on_speculative_rows():
+    """Draft rows (4 per sequence, each seeing one more token): the merged
+    top-k of 3 shards from the indexer's scores, then the shards' partial
+    attention and LSE combine, each against the oracle."""
+    case = synth.make_case("dcpspec", seq_lens=[9000, 4100], nq=4, seed=77)
+    dc = synth.device_case(case)
+    s = gpu_scores(case, dc, extra=0)
+    m = s.cpu().numpy()
+    idx, _ = _check(m, case.row_lens(), 2048, 3)
+    o, l, po, pl = _gpu_dcp_mla(case, dc, idx, 3)
+    check_dcp_mla(case, idx, 3, o, l, po, pl)
