@@ -263,9 +263,9 @@ dsa_status_t sparse_mla_decode(const dsa_paged_cache_t* cache, const dsa_batch_t
                                int32_t* dev_status, void* stream);
 
 /*
- * Batch-invariant mode (Day-0 post, section on RL without train/rollout
- * mismatch: with batch-invariant kernels a token's log-prob does not depend
- * on the batch it is computed in).  The indexer and the top-k already give
+ * Batch-invariant mode (Day-0 post, section "day 0 的零失配 RL", zero-mismatch
+ * RL: with batch-invariant kernels a token's log-prob does not depend on the
+ * batch it is computed in).  The indexer and the top-k already give
  * each row the same result whatever the batch; the sparse MLA splits a row's
  * tokens into chunks whose number depends on the number of rows (to fill the
  * SMs), and the merge of the chunks rounds differently for a different split.
