@@ -1,8 +1,9 @@
 """Batch invariance (Day-0 post, section "day 0 的零失配 RL", zero-mismatch
-RL: a token's log-prob must not depend on the batch it is computed in).  With the batch-invariant mode on, every row of a batch gets bitwise the
-same scores, indices, output and LSE as when it is decoded alone; with it
-off, the sparse MLA's split into chunks follows the number of rows and the
-outputs differ in the last bits.
+RL: a token's log-prob must not depend on the batch it is computed in).
+With the batch-invariant mode on, every row of a batch gets bitwise the same
+scores, indices, output and LSE as when it is decoded alone; with it off, the
+sparse MLA's split into chunks follows the number of rows and the outputs
+differ in the last bits.
 """
 import dataclasses
 
