@@ -17,8 +17,9 @@
 // all sequences are split evenly across CTAs ("key-balanced", Day-0 post,
 // fused decode section).  Per CTA:
 //   warp 0  TMA producer: per unit, four 64-token code pages (3-D tensor map
-//           over the block pool, 128-byte swizzle; MXFP4 nibbles are unpacked
-//           by the copy into byte containers) into a 5-6 stage code ring, and
+//           over the block pool, 128-byte swizzle; MXFP4 codes land as
+//           8-byte packed chunks 16 bytes apart, the layout the block-scaled
+//           MMA reads) into a 5-6 stage code ring, and
 //           the four pages' scale rows in one tile::gather4 copy into a
 //           deeper scale ring.  The two half-warps issue two units at once;
 //           the lanes resolve the block-table rows of the next 32 units; the
@@ -552,7 +553,7 @@ dsa_status_t launch_index_scores(const dsa_paged_cache_t& c, const dsa_batch_t& 
   const int code_bytes = mx ? kIdxDim / 2 : kIdxDim;  // per token
   CUtensorMap keys, scales, qmap;
   // codes: the pool as [num_blocks][64 tokens][128 elements], one 64-row box per page; MXFP4
-  // nibbles are unpacked by the copy into one byte per element (8 data + 8 gap bytes per 16)
+  // codes land as 8-byte packed chunks with 8-byte gaps (16 elements per 16 bytes)
   {
     const uint64_t dims[3] = {(uint64_t)kIdxDim, (uint64_t)kBlock, (uint64_t)c.num_blocks};
     const uint64_t strides[2] = {(uint64_t)code_bytes, (uint64_t)c.row_stride};
