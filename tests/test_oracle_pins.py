@@ -647,3 +647,22 @@ def test_cache_append_nvfp4_latents():
             changed[r, case.index_off + slot * 64:case.index_off + (slot + 1) * 64] = True
             changed[r, case.index_off + 64 * 64 + 4 * slot:case.index_off + 64 * 64 + 4 * slot + 4] = True
     np.testing.assert_array_equal(pool[~changed], case.pool[~changed])
+
+
+def test_cache_append_nvfp4_agrees_with_the_input_generator():
+    """The oracle's NVFP4 write (C, brute-force nearest codes) and the input
+    generator's NVFP4 encoder (numpy/torch, midpoint search) implement the
+    same rule independently: on bf16-valued latents they write the same
+    352 bytes."""
+    case = synth.make_case("nvx", seq_lens=[70], nq=1, key_format=synth.KEY_FP8, seed=9,
+                           latent_format=synth.LATENT_NVFP4)
+    rng = np.random.default_rng(9)
+    lat = (rng.standard_normal((1, 576)) * np.exp(rng.uniform(-5, 5, (1, 36, 1))).repeat(16, 2).reshape(1, 576))
+    lat_b = _bf16_bits(lat.astype(np.float32))
+    key_b = _bf16_bits(rng.standard_normal((1, 128)).astype(np.float32))
+    pool = oracle.cache_append(case, lat_b, key_b)
+    t = 69
+    r = case.block_table[0, t // 64]
+    rec = pool[r, case.latent_off + (t % 64) * 352:case.latent_off + (t % 64 + 1) * 352]
+    want = synth.nvfp4_latent_encode(_bf16_value(lat_b), case.latent_scale)[0]
+    np.testing.assert_array_equal(rec, want)
