@@ -97,6 +97,12 @@ def test_host_validation_without_device(lib):
     assert dm(8, 1032, 2048, None, 0) == B.ERR_INVALID_ARG        # q_mla not 16-byte aligned
     assert dm(8, 1024, 2052, None, 0) == B.ERR_INVALID_ARG        # out not 8-byte aligned
     assert dm(8, 1024, 2048, 4096, 100) == B.ERR_WORKSPACE
+    # partial outputs, when given, 8-byte aligned like the output
+    assert lib.dsa_dcp_sparse_mla(ctypes.byref(c), ctypes.byref(b), 1024, 256, 2048, 4, 1.0, 2048, 512, 3076, None,
+                                  4096, 1 << 40, st, None) == B.ERR_INVALID_ARG
+    # bf16 fused step: a caller's score buffer needs a row stride that is a multiple of 8
+    assert lib.dsa_decode_step_bf16(ctypes.byref(c), ctypes.byref(b), 1024, 2048, 4096, 2048, 1.0, 8192, 512, 16384,
+                                    100, None, 4096, 1 << 40, st, None) == B.ERR_INVALID_ARG
 
 
 def test_workspace_sizes(lib):
