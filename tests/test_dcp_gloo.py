@@ -6,7 +6,9 @@ everyone's words, select the same global top-k, detect a shard that may hold
 more of it, let that shard resend its full local top-k, and select again.
 The result and the words-sent statistics equal the oracle's single-process
 model of the protocol (and the library's one-GPU emulation is tested against
-that model).  Runs on CPU; the rendezvous is on 127.0.0.1."""
+that model).  The LSE combine likewise: each rank's partial attention over
+the selected tokens it holds, gathered as bf16 outputs and LSEs and merged,
+equals the oracle's.  Runs on CPU; the rendezvous is on 127.0.0.1."""
 import multiprocessing as mp
 import os
 import socket
@@ -122,3 +124,65 @@ def test_dcp_exchange_over_two_gloo_ranks_matches_the_oracle():
         np.testing.assert_array_equal(idx, ref.astype(np.int64))
         np.testing.assert_array_equal(stats, ref_stats)
     assert ref_stats[2, 1] == 1 and ref_stats[0, 1] == 0   # the dominated row made shard 0 resend
+
+
+def _rank_combine(rank, world, port, q):
+    os.environ.update(RANK=str(rank), WORLD_SIZE=str(world), MASTER_ADDR="127.0.0.1", MASTER_PORT=str(port))
+    sys.path.insert(0, ROOT)
+    import torch
+    import torch.distributed as dist
+
+    import oracle
+    from dsa_sparse_attention_index_gb300 import synth
+
+    dist.init_process_group("gloo")
+    case, idx = _combine_case(synth)
+    # this rank's partial attention over the selected tokens it holds, sent as
+    # bf16 outputs and fp64 LSEs
+    own = np.where((idx >= 0) & (idx % world == rank), idx, -1).astype(np.int32)
+    o, l = oracle.sparse_mla(case, own)
+    o16 = torch.from_numpy(oracle.round_bf16(o))
+    parts_o = [torch.empty_like(o16) for _ in range(world)]
+    parts_l = [torch.empty_like(torch.from_numpy(l)) for _ in range(world)]
+    dist.all_gather(parts_o, o16)
+    dist.all_gather(parts_l, torch.from_numpy(l))
+    O = torch.stack(parts_o).numpy()
+    L = torch.stack(parts_l).numpy()
+    lse = np.logaddexp.reduce(L, axis=0)             # -inf where no rank holds a token
+    with np.errstate(invalid="ignore"):
+        w = np.where(np.isfinite(L), np.exp(L - np.where(np.isfinite(lse), lse, 0.0)), 0.0)
+    out = (w[..., None] * O).sum(axis=0)
+    q.put((rank, out, lse))
+    dist.destroy_process_group()
+
+
+def _combine_case(synth):
+    case = synth.make_case("gloo_mla", seq_lens=[400, 90], nq=1, topk=64, seed=21)
+    rng = np.random.default_rng(21)
+    idx = np.full((2, 64), -1, dtype=np.int32)
+    idx[0] = np.sort(rng.choice(400, 64, replace=False))
+    idx[1, :30] = np.sort(rng.choice(90, 30, replace=False))
+    return case, idx
+
+
+def test_dcp_lse_combine_over_two_gloo_ranks_matches_the_oracle():
+    sys.path.insert(0, ROOT)
+    import oracle
+    from dsa_sparse_attention_index_gb300 import synth
+
+    oracle.build()
+    ctx = mp.get_context("spawn")
+    q = ctx.Queue()
+    port = _free_port()
+    procs = [ctx.Process(target=_rank_combine, args=(r, 2, port, q)) for r in range(2)]
+    for p in procs:
+        p.start()
+    res = [q.get(timeout=180) for _ in procs]
+    for p in procs:
+        p.join(timeout=60)
+        assert p.exitcode == 0
+    case, idx = _combine_case(synth)
+    ref_out, ref_lse, _, _ = oracle.dcp_sparse_mla(case, idx, 2)
+    for _, out, lse in res:
+        np.testing.assert_allclose(out, ref_out, rtol=1e-12, atol=1e-14)
+        np.testing.assert_allclose(lse, ref_lse, rtol=1e-13)
