@@ -43,7 +43,7 @@ L2_FLUSH_BYTES = 256 << 20   # > 129 MB L2; flushed by READING it (clean lines, 
 def parse():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--steps", type=int, default=50)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", default=DEFAULT_WORKLOAD, choices=sorted(synth.WORKLOADS))
@@ -160,6 +160,34 @@ def run_oracle(sub):
     return time.perf_counter() - t0
 
 
+def host_cpu() -> str:
+    """The host's CPU model (x86 `model name`; on Arm the implementer and part
+    numbers) and its logical core count."""
+    model = ""
+    try:
+        with open("/proc/cpuinfo") as f:
+            info = f.read()
+        for key in ("model name", "Model name", "CPU part"):
+            for line in info.splitlines():
+                if line.split(":")[0].strip() == key:
+                    model = (key + " " if key == "CPU part" else "") + line.split(":", 1)[1].strip()
+                    break
+            if model:
+                break
+    except OSError:
+        pass
+    import platform
+
+    return f"{model or platform.processor() or 'unknown'} ({platform.machine()}, {os.cpu_count()} logical cores)"
+
+
+def step_percentiles(step_ms) -> dict:
+    """Median and p10/p90 of the per-step times (ms)."""
+    a = np.asarray(step_ms, dtype=np.float64)
+    return {"ms_p10": round(float(np.percentile(a, 10)), 5), "ms_p50": round(float(np.percentile(a, 50)), 5),
+            "ms_p90": round(float(np.percentile(a, 90)), 5)}
+
+
 def cpu_baseline(case, max_rows: int = 4, min_seconds: float = 10.0, max_runs: int = 50):
     """The oracle's decode step on a bounded sample of the workload, repeated
     until about min_seconds of CPU work (at most max_runs passes)."""
@@ -172,6 +200,7 @@ def cpu_baseline(case, max_rows: int = 4, min_seconds: float = 10.0, max_runs: i
         runs += 1
     b = roofline.step_bytes(sub.seq_lens, sub.nq, sub.topk, sub.key_format, sub.latent_format)["total"]
     return {"value": b * runs / dt / 1e9, "unit": "GB/s", "cores": oracle.num_threads(), "kind": "oracle",
+            "cpu": host_cpu(),
             "sample": f"{sub.batch} of {case.batch} sequences ({sub.rows} query rows, "
                       f"{int(sub.seq_lens.sum())} context tokens) of the same workload, fp64 C oracle, "
                       f"{runs} passes in {dt:.1f} s"}
@@ -457,6 +486,7 @@ def main_ours(args):
         "steps": args.steps,
         "warmup": args.warmup,
         "ms_per_step": round(ms, 5),
+        **step_percentiles(step_ms),
         "us_per_layer_step": round(ms * 1e3, 2),
         "tokens_per_s": round(rows * world / (ms * 1e-3), 1),
         "frac_of_8TBps": round(value / world / NOMINAL_HBM_GBS, 4),
@@ -522,6 +552,7 @@ def main_reference(args):
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
         "config": {"workload": args.workload, "sample": f"{sub.batch} sequence(s), {sub.rows} query row(s)"},
         "cpu_baseline": {"value": round(v, 4), "unit": "GB/s", "cores": oracle.num_threads(), "kind": "oracle",
+                         "cpu": host_cpu(),
                          "sample": f"first {sub.batch} sequence(s) of the workload per step"},
         "e2e": {"value": round(v, 4), "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }

@@ -90,5 +90,24 @@ def test_reference_arm_prints_the_contract_line():
                 "scaling", "vs_baseline", "dtype", "data", "config", "cpu_baseline", "e2e"):
         assert key in d, key
     assert d["impl"] == "reference" and d["config"]["workload"] == "decode_b1_l4096" and d["value"] > 0
-    assert d["cpu_baseline"]["kind"] == "oracle" and d["cpu_baseline"]["cores"] >= 1
+    assert d["cpu_baseline"]["kind"] == "oracle" and d["cpu_baseline"]["cores"] >= 1 and d["cpu_baseline"]["cpu"]
     assert d["e2e"]["h2d_bytes_per_step"] == 0 and d["e2e"]["value"] == d["value"]
+
+
+def test_step_percentiles_and_host_cpu():
+    sys.path.insert(0, ROOT)
+    import bench
+
+    p = bench.step_percentiles([0.2, 0.1, 0.4, 0.3, 0.5])
+    assert p == {"ms_p10": 0.14, "ms_p50": 0.3, "ms_p90": 0.46}
+    assert "logical cores" in bench.host_cpu()
+
+
+def test_cpu_baseline_line():
+    sys.path.insert(0, ROOT)
+    import bench
+    from dsa_sparse_attention_index_gb300 import synth
+
+    d = bench.cpu_baseline(synth.make_case("cb", seq_lens=[3000, 700], seed=1), min_seconds=0.0)
+    assert d["kind"] == "oracle" and d["value"] > 0 and d["cores"] >= 1 and d["cpu"]
+    assert "1 passes" in d["sample"] and "2 of 2 sequences" in d["sample"]
