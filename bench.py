@@ -181,6 +181,14 @@ def host_cpu() -> str:
     return f"{model or platform.processor() or 'unknown'} ({platform.machine()}, {os.cpu_count()} logical cores)"
 
 
+def l2_label(step_bytes: int, l2_bytes: int = 129 << 20) -> str:
+    """How the timed steps treat L2: flushed between steps either way; says
+    whether a step's inputs alone would fit in it."""
+    side = "above" if step_bytes > l2_bytes else "below"
+    return (f"L2 flushed by a 256 MB read between timed steps (outside the step events); a step's algorithmic "
+            f"bytes {step_bytes / 1e6:.1f} MB, {side} the 129 MB L2")
+
+
 def step_percentiles(step_ms) -> dict:
     """Median and p10/p90 of the per-step times (ms)."""
     a = np.asarray(step_ms, dtype=np.float64)
@@ -501,7 +509,7 @@ def main_ours(args):
             "seq_len_max": int(case.seq_lens.max()), "topk": k, "key_bytes": case.token_bytes(),
             "latent_bytes": case.latent_bytes(), "heads": 96, "index_heads": 32, "block": 64,
             "algorithmic_bytes_per_step": b["total"], "parallelism": f"replicas x{world}",
-            "l2": "inputs > L2; L2 flushed by a 256 MB read between timed steps (outside the step events)",
+            "l2": l2_label(b["total"]),
         },
         "stage_us": {kk: round(v * 1e3, 2) for kk, v in st_ms.items()},
         "stages": stages,

@@ -111,3 +111,11 @@ def test_cpu_baseline_line():
     d = bench.cpu_baseline(synth.make_case("cb", seq_lens=[3000, 700], seed=1), min_seconds=0.0)
     assert d["kind"] == "oracle" and d["value"] > 0 and d["cores"] >= 1 and d["cpu"]
     assert "1 passes" in d["sample"] and "2 of 2 sequences" in d["sample"]
+
+
+def test_l2_label_says_which_side_of_l2_a_step_is():
+    sys.path.insert(0, ROOT)
+    import bench
+
+    assert "above the 129 MB L2" in bench.l2_label(522_000_000)
+    assert "below the 129 MB L2" in bench.l2_label(1_720_000)
