@@ -6,7 +6,8 @@
  * K3.1 Pro): a small lightning indexer scores every prior token with 32 light
  * heads over a 132-byte FP8 key (128 E4M3 codes + fp32 scale), the 2,048
  * best tokens are kept, and exact MLA attention then runs only over those
- * tokens' 576-byte FP8 latents.  The indexer score is DeepSeek-V3.2's
+ * tokens' 576-byte FP8 latents (or 352-byte NVFP4 latents, see
+ * dsa_latent_format_t).  The indexer score is DeepSeek-V3.2's
  *     s[t] = sum_h w[h] * max(0, scale_t * (q_h . k_t))
  * (32 heads x 128 dims, fp32 accumulation and a weighted reduction across
  * heads — same post, AMD section "量化：原生 MXFP4 索引器").
@@ -15,6 +16,18 @@
  * a pool of block rows, each holding one layer's latent page and index-key
  * page for 64 tokens; a block table maps (sequence, logical block) to a row,
  * and the library translates it to page addresses itself on every call.
+ *
+ * Entry points
+ *   dsa_translate_pages      block table -> page addresses
+ *   dsa_index_scores(_bf16)  indexer scores (FP8 or MXFP4 keys; fp32 or bf16 out)
+ *   dsa_topk(_bf16, _noalloc) top-k per row, ties to the lower index
+ *   sparse_mla_decode        exact sparse MLA over the selected tokens
+ *   dsa_decode_step(_bf16)   the three stages fused on one stream
+ *   dsa_cache_append, dsa_quantize_index_query   the step's front end
+ *   dsa_dcp_topk, dsa_dcp_sparse_mla   decode context parallelism (top-k
+ *                            merge, partial attention + LSE combine) of W
+ *                            token shards, emulated on one GPU
+ *   dsa_batch_invariant, dsa_topk_force_multipass   process-wide switches
  *
  * Conventions for every entry point
  *   - All pointers to tensors are DEVICE pointers unless stated otherwise;
