@@ -108,6 +108,25 @@ def test_index_scores_exact_integer_dot(small_case):
                 assert s[b, t] == float(want)
 
 
+def test_index_score_bounds_are_the_absolute_sums(small_case):
+    """A_t = sum_h |w_h| |scale_t| sum_d |q_hd k_td| (the tolerances' scale):
+    exact integer sums of absolute products, and never below |s_t|."""
+    c = small_case
+    bnd = oracle.index_score_bounds(c)
+    s = oracle.index_scores(c)
+    for b in range(c.batch):
+        for t in (0, 5, 64, int(c.seq_lens[b]) - 1):
+            codes, scale = _decode_key_fp8(c, b, t)
+            k = _e4m3_int(codes)
+            want = Fraction(0)
+            for h in range(32):
+                qi = _e4m3_int(c.q_index[b, h])
+                want += abs(Fraction(float(c.head_w[b, h]))) * abs(Fraction(scale)) * Fraction(
+                    sum(abs(a * x) for a, x in zip(qi, k)), 512 * 512)
+            assert bnd[b, t] == pytest.approx(float(want), rel=1e-14)
+            assert abs(s[b, t]) <= bnd[b, t] * (1 + 1e-14)
+
+
 def test_index_scores_one_hot_closed_form(small_case):
     c = copy.deepcopy(small_case)
     h, d = 5, 77
