@@ -195,6 +195,7 @@ def test_index_scores_mxfp4_exact_rational():
     c.head_w = np.zeros_like(c.head_w)
     c.head_w[:, 9] = 1.0
     s = oracle.index_scores(c)
+    bnd = oracle.index_score_bounds(c)
     qi = _e4m3_int(c.q_index[0, 9])
     for t in (0, 5, 64, 129):
         r = c.block_table[0, t // 64]
@@ -208,6 +209,8 @@ def test_index_scores_mxfp4_exact_rational():
             two_k.append(Fraction(mag, 2) * Fraction(2) ** (int(e8[d // 32]) - 127))
         dot = sum(Fraction(a, 512) * k for a, k in zip(qi, two_k))
         assert s[0, t] == float(max(Fraction(0), dot))
+        # the tolerance scale: the sum of absolute products (scale_t = 1)
+        assert bnd[0, t] == pytest.approx(float(sum(abs(Fraction(a, 512) * k) for a, k in zip(qi, two_k))), rel=1e-14)
 
 
 # --------------------------------------------------------------- top-k
