@@ -531,12 +531,20 @@ def main_ours(args):
 
 
 def load_traffic(workload):
-    """DRAM bytes per indexer launch from the committed ncu summary, if any."""
+    """DRAM bytes per indexer launch from the committed ncu summary, if any,
+    and only while the indexer's source is the one the counters were taken
+    from (its sha256 is recorded beside them)."""
+    import hashlib
+
     p = os.path.join(ROOT, "profiles", "indexer_traffic.json")
-    if os.path.exists(p):
-        d = json.load(open(p))
-        return d.get(workload)
-    return None
+    if not os.path.exists(p):
+        return None
+    d = json.load(open(p))
+    src = os.path.join(ROOT, "dsa_sparse_attention_index_gb300", "csrc", "indexer.cu")
+    with open(src, "rb") as f:
+        if hashlib.sha256(f.read()).hexdigest() != d.get("indexer_source_sha256"):
+            return None
+    return d.get(workload)
 
 
 # ---------------------------------------------------------------- reference arm
