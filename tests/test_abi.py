@@ -128,3 +128,20 @@ def test_workspace_sizes(lib):
     finally:
         assert lib.dsa_batch_invariant(0) == 1
     assert lib.sparse_mla_workspace_size(200, 2048) < 200 * 4 * 96 * 512 * 4
+
+
+def test_oracle_and_product_share_no_code():
+    """The product (package and CUDA sources) never imports or includes the
+    oracle, and the oracle never imports the product."""
+    pkg = os.path.join(ROOT, "dsa_sparse_attention_index_gb300")
+    for dirpath, _, files in os.walk(pkg):
+        for f in files:
+            if f.endswith((".py", ".cu", ".cuh", ".h")):
+                src = open(os.path.join(dirpath, f)).read()
+                assert not re.search(r"^\s*(import|from)\s+oracle\b", src, flags=re.M), f
+                assert not re.search(r'#include\s+[<"][^>"]*oracle', src), f
+    for f in os.listdir(os.path.join(ROOT, "oracle")):
+        if f.endswith((".py", ".c", ".h")):
+            src = open(os.path.join(ROOT, "oracle", f)).read()
+            assert not re.search(r"^\s*(import|from)\s+dsa_sparse_attention_index_gb300\b", src, flags=re.M), f
+            assert not re.search(r'#include\s+[<"][^>"]*(csrc|dsa\.h|common\.cuh)', src), f
