@@ -38,6 +38,10 @@ METRIC = "DSA decode µs/layer-step & achieved HBM GB/s (fraction of 8 TB/s) at 
 DEFAULT_WORKLOAD = "longctx_b32_l64k-160k"
 NOMINAL_HBM_GBS = 8000.0
 L2_FLUSH_BYTES = 256 << 20   # > 129 MB L2; flushed by READING it (clean lines, no write-back)
+# The other configurations of the target statement, measured after the headline
+# one with the same protocol (fewer steps) and reported in the line's
+# "workloads" block: speculative verify, 1M-token MXFP4 keys, chunked prefill.
+EXTRA_WORKLOADS = ("specdecode_b8x4_l32768", "mxfp4_b4_l1m", "prefill_q2048_l153600")
 
 
 def parse():
@@ -51,6 +55,8 @@ def parse():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--soak-s", type=float, default=1.5, help="seconds of identical steps before the timed region")
+    ap.add_argument("--workloads", default=",".join(EXTRA_WORKLOADS),
+                    help="other workloads measured after the headline one (comma-separated, 'none' for none)")
     return ap.parse_args()
 
 
@@ -212,6 +218,40 @@ def cpu_baseline(case, max_rows: int = 4, min_seconds: float = 10.0, max_runs: i
             "sample": f"{sub.batch} of {case.batch} sequences ({sub.rows} query rows, "
                       f"{int(sub.seq_lens.sum())} context tokens) of the same workload, fp64 C oracle, "
                       f"{runs} passes in {dt:.1f} s"}
+
+
+def stage_roofline(case, st_ms, traffic=None):
+    """Per-stage figures and the dominant kernel's roofline for one workload
+    from its median stage times (ms): a prefill chunk or a step whose MLA
+    outlasts the indexer against the tensor peak (the indexer's fp8 at the
+    measured bf16 peak x 2, the nominal ratio), else the indexer against the
+    measured HBM copy bandwidth."""
+    k = case.topk
+    peak, peak_kind = peaks()
+    bf16_peak, bf16_kind = tensor_peak()
+    idx_bytes = roofline.indexer_bytes(case.seq_lens, case.nq, case.key_format)
+    idx_gbs = idx_bytes / (st_ms["index"] * 1e-3) / 1e9
+    idx_fl = roofline.indexer_flops(case.seq_lens, case.nq)
+    mla_fl = roofline.mla_flops(case.seq_lens, case.nq, k)
+    idx_tf = idx_fl / (st_ms["index"] * 1e-3) / 1e12
+    mla_tf = mla_fl / (st_ms["mla"] * 1e-3) / 1e12
+    mla_gbs = roofline.mla_bytes(case.seq_lens, case.nq, k, case.latent_format) / (st_ms["mla"] * 1e-3) / 1e9
+    stages = {"index": {"us": round(st_ms["index"] * 1e3, 2), "GB/s": round(idx_gbs, 1), "TFLOP/s": round(idx_tf, 1)},
+              "topk": {"us": round(st_ms["topk"] * 1e3, 2)},
+              "mla": {"us": round(st_ms["mla"] * 1e3, 2), "GB/s": round(mla_gbs, 1), "TFLOP/s": round(mla_tf, 1)}}
+    if case.nq > 4 and st_ms["index"] >= st_ms["mla"]:
+        roof = {"kernel": "indexer_kernel (dsa_index_scores)", "bound": "tensor", "achieved": round(idx_tf, 1),
+                "peak": 2 * bf16_peak, "peak_kind": bf16_kind + " bf16 x 2 (fp8)", "unit": "TFLOP/s",
+                "frac": round(idx_tf / (2 * bf16_peak), 4), "traffic": None, "algorithmic_flops": idx_fl}
+    elif st_ms["mla"] > st_ms["index"]:
+        roof = {"kernel": "sparse_mla_kernel (sparse_mla_decode)", "bound": "tensor", "achieved": round(mla_tf, 1),
+                "peak": bf16_peak, "peak_kind": bf16_kind + " bf16", "unit": "TFLOP/s",
+                "frac": round(mla_tf / bf16_peak, 4), "traffic": None, "algorithmic_flops": mla_fl}
+    else:
+        roof = {"kernel": "indexer_kernel (dsa_index_scores)", "bound": "hbm", "achieved": round(idx_gbs, 1),
+                "peak": peak, "peak_kind": peak_kind, "unit": "GB/s", "frac": round(idx_gbs / peak, 4),
+                "traffic": traffic, "algorithmic_bytes": idx_bytes}
+    return stages, roof
 
 
 # ---------------------------------------------------------------- replicas
@@ -456,36 +496,8 @@ def main_ours(args):
     b = roofline.step_bytes(case.seq_lens, case.nq, k, case.key_format, case.latent_format)
     total_bytes = b["total"] * world
     value = total_bytes / (ms * 1e-3) / 1e9
-    peak, peak_kind = peaks()
-    idx_bytes = roofline.indexer_bytes(case.seq_lens, case.nq, case.key_format)
-    idx_gbs = idx_bytes / (st_ms["index"] * 1e-3) / 1e9
-    traffic = load_traffic(args.workload)
-    bf16_peak, bf16_kind = tensor_peak()
-    idx_tf = roofline.indexer_flops(case.seq_lens, case.nq) / (st_ms["index"] * 1e-3) / 1e12
-    mla_tf = roofline.mla_flops(case.seq_lens, case.nq, k) / (st_ms["mla"] * 1e-3) / 1e12
-    mla_gbs = roofline.mla_bytes(case.seq_lens, case.nq, k, case.latent_format) / (st_ms["mla"] * 1e-3) / 1e9
-    stages = {"index": {"us": round(st_ms["index"] * 1e3, 2), "GB/s": round(idx_gbs, 1), "TFLOP/s": round(idx_tf, 1)},
-              "topk": {"us": round(st_ms["topk"] * 1e3, 2)},
-              "mla": {"us": round(st_ms["mla"] * 1e3, 2), "GB/s": round(mla_gbs, 1), "TFLOP/s": round(mla_tf, 1)}}
-    if case.nq > 4:
-        # a prefill chunk is tensor-bound: the slower of the two contractions against the
-        # measured bf16 peak (fp8: that peak x 2, the nominal fp8/bf16 ratio)
-        if st_ms["index"] >= st_ms["mla"]:
-            rl = {"kernel": "indexer_kernel (dsa_index_scores)", "achieved": idx_tf, "peak": 2 * bf16_peak,
-                  "peak_kind": bf16_kind + " bf16 x 2 (fp8)",
-                  "flops": roofline.indexer_flops(case.seq_lens, case.nq)}
-        else:
-            rl = {"kernel": "sparse_mla_kernel (sparse_mla_decode)", "achieved": mla_tf, "peak": bf16_peak,
-                  "peak_kind": bf16_kind + " bf16", "flops": roofline.mla_flops(case.seq_lens, case.nq, k)}
-        roof = {"kernel": rl["kernel"], "bound": "tensor", "achieved": round(rl["achieved"], 1),
-                "peak": rl["peak"], "peak_kind": rl["peak_kind"], "unit": "TFLOP/s",
-                "frac": round(rl["achieved"] / rl["peak"], 4), "traffic": None, "algorithmic_flops": rl["flops"]}
-    else:
-        roof = {"kernel": "indexer_kernel (dsa_index_scores)", "bound": "hbm",
-                "achieved": round(idx_gbs, 1), "peak": peak, "peak_kind": peak_kind, "unit": "GB/s",
-                "frac": round(idx_gbs / peak, 4),
-                "traffic": traffic, "algorithmic_bytes": idx_bytes,
-                "step_frac": round(value / world / peak, 4)}
+    stages, roof = stage_roofline(case, st_ms, load_traffic(args.workload))
+    roof["step_frac"] = round(value / world / peaks()[0], 4)
     line = {
         "metric": METRIC,
         "value": round(value, 1),
@@ -525,9 +537,93 @@ def main_ours(args):
                        "ms_per_step": round(e2e_t, 5), "h2d_bytes_per_step": bi, "d2h_bytes_per_step": bo}
     if rank == 0 and not args.no_cpu_baseline:
         line["cpu_baseline"] = cpu_baseline(case)
+    extra = [w for w in args.workloads.split(",") if w and w != "none" and w != args.workload]
+    if rank == 0 and extra:  # the headline's buffers stay: HBM holds both
+        line["workloads"] = {w: measure_workload(w, args, dev, flush, stream, max(5, min(args.steps, 20)))
+                             for w in extra}
     if rank == 0:
         print(json.dumps(line), flush=True)
     reps.close()
+
+
+def measure_workload(name, args, dev, flush, stream, steps):
+    """One more workload with the headline's protocol: warm-up steps, a soak
+    under the clock sampler, `steps` fused steps each bracketed by its own
+    events with L2 flushed in between, then the three stages enqueued back to
+    back.  Returns its block of the JSON line; frees its buffers."""
+    import torch
+
+    from dsa_sparse_attention_index_gb300 import binding
+
+    case = synth.workload(name, seed=args.seed)
+    dc = synth.device_case(case, dev)
+    k, rows = case.topk, case.rows
+    ld = (case.max_len + 3) // 4 * 4
+    out = torch.empty((rows, 96, 512), dtype=torch.int16, device=dev)
+    lse = torch.empty((rows, 96), dtype=torch.float32, device=dev)
+    scores = torch.empty((rows, ld), dtype=torch.float32, device=dev)
+    idx = torch.empty((rows, k), dtype=torch.int32, device=dev)
+    ws = binding.workspace(binding.workspace_size(dc.batch, k), dev)
+    tk_ws = binding.workspace(binding.topk_workspace_size(rows, case.max_len, k), dev)
+    mla_ws = binding.workspace(binding.sparse_mla_workspace_size(rows, k), dev)
+    status = torch.zeros(1, dtype=torch.int32, device=dev)
+
+    def step():
+        binding.decode_step(dc.cache, dc.batch, dc.q_index, dc.head_w, dc.q_mla, k, case.sm_scale, out, lse, ws,
+                            status, stream=stream)
+
+    for _ in range(args.warmup):
+        flush.zero_()
+        step()
+    torch.cuda.synchronize()
+    assert status.item() == 0, binding.status_string(status.item())
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(steps)]
+    with ClockSampler(torch.cuda.current_device()) as clk:
+        t0 = time.perf_counter()
+        while time.perf_counter() - t0 < min(args.soak_s, 0.5):
+            for _ in range(5):
+                flush.zero_()
+                step()
+            torch.cuda.synchronize()
+        n0 = binding.kernel_launches()
+        for e0, e1 in ev:
+            flush.zero_()
+            e0.record(stream)
+            step()
+            e1.record(stream)
+        n_launches = binding.kernel_launches() - n0
+        torch.cuda.synchronize()
+    step_ms = [e0.elapsed_time(e1) for e0, e1 in ev]
+    assert status.item() == 0, binding.status_string(status.item())
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(steps)]
+    for e in evs:
+        flush.zero_()
+        e[0].record(stream)
+        binding.index_scores(dc.cache, dc.batch, dc.q_index, dc.head_w, scores, status, stream)
+        e[1].record(stream)
+        binding.topk(scores, dc.row_lens, case.max_len, k, idx, tk_ws, status, stream)
+        e[2].record(stream)
+        binding.sparse_mla_decode(dc.cache, dc.batch, dc.q_mla, idx, case.sm_scale, out, lse, mla_ws, status, stream)
+        e[3].record(stream)
+    torch.cuda.synchronize()
+    assert status.item() == 0, binding.status_string(status.item())
+    st_ms = {kk: statistics.median(e[j].elapsed_time(e[j + 1]) for e in evs)
+             for j, kk in enumerate(("index", "topk", "mla"))}
+    ms = statistics.mean(step_ms)
+    b = roofline.step_bytes(case.seq_lens, case.nq, k, case.key_format, case.latent_format)["total"]
+    stages, roof = stage_roofline(case, st_ms, load_traffic(name))
+    roof["step_frac"] = round(b / (ms * 1e-3) / 1e9 / peaks()[0], 4)
+    res = {"ms_per_step": round(ms, 5), **step_percentiles(step_ms), "us_per_layer_step": round(ms * 1e3, 2),
+           "value": round(b / (ms * 1e-3) / 1e9, 1), "unit": "GB/s", "tokens_per_s": round(rows / (ms * 1e-3), 1),
+           "steps": steps, "gpu_launches": n_launches,
+           "config": {"batch": case.batch, "queries_per_seq": case.nq, "seq_len_mean": float(np.mean(case.seq_lens)),
+                      "topk": k, "key_bytes": case.token_bytes(), "latent_bytes": case.latent_bytes(),
+                      "algorithmic_bytes_per_step": b, "l2": l2_label(b)},
+           "stage_us": {kk: round(v * 1e3, 2) for kk, v in st_ms.items()}, "stages": stages, "roofline": roof,
+           "clocks": clk.summary()}
+    del dc, out, lse, scores, idx, ws, tk_ws, mla_ws
+    torch.cuda.empty_cache()
+    return res
 
 
 def load_traffic(workload):

@@ -12,7 +12,7 @@
 namespace dsa {
 
 int num_sms() {
-  static int cache[64] = {};
+  static std::atomic<int> cache[64];  // zero: not yet asked
   int dev = 0;
   cudaGetDevice(&dev);
   if (dev >= 0 && dev < 64 && cache[dev]) return cache[dev];

@@ -42,6 +42,7 @@
 // All draft rows of a sequence share one key read (AMD section: keys are
 // reused across query rows during speculative verify).
 #include <algorithm>
+#include <atomic>
 
 #include <cuda_bf16.h>
 
@@ -520,7 +521,7 @@ __global__ void __launch_bounds__(idx_threads<MX>(), 1)
 template <int NQ, bool MX>
 dsa_status_t launch_nq(const IdxParams& p, const CUtensorMap& keys, const CUtensorMap& scales,
                        const CUtensorMap& q, cudaStream_t st) {
-  static bool attr_set[64] = {};
+  static std::atomic<bool> attr_set[64];
   int dev = 0;
   cudaGetDevice(&dev);
   const size_t smem = IdxSmem<NQ>::bytes(kMaxBatch);

@@ -8,32 +8,33 @@
 // prefill section gives the 96 heads).  The selected rows are read straight
 // from the packed paged cache through the block table.
 //
-// GB300 design (one CTA per (query row, token chunk), 11 warps):
+// GB300 design (one CTA per (query row, token chunk), 12 warps):
 //   * Q [96 x 576] bf16 is the A operand of S = Q K^T with the heads on the
 //     MMA's M = 128 rows (rows 96..127 are ignored): dims 0..447 loaded once
 //     by TMA into shared memory (84 KB, 128-byte swizzle, K-major), dims
 //     448..575 written by the softmax warps into TMEM (A from TMEM).  That
-//     leaves room for three latent tile buffers and spares the tensor core
-//     the shared-memory reads of those Q blocks, the limit of these
-//     small-N MMAs.
-//   * warps 4..9 gather 32 latent rows per tile (16-byte loads, four tiles in
-//     flight), widen E4M3 -> bf16 exactly in registers and store the tile
+//     leaves room for two latent tile buffers of 48 tokens.
+//   * warps 4..9 gather 48 latent rows per tile (16-byte loads, three tiles
+//     in flight in registers), widen E4M3 -> bf16 exactly and store the tile
 //     once, 128-byte swizzled.  That single tile is the B operand of QK^T
-//     (K-major, N = 32 tokens) and the A operand of P V (MN-major, M = 128
+//     (K-major, N = 48 tokens) and the A operand of P V (MN-major, M = 128
 //     value dims), so V needs no second copy.
 //   * two warps issue tcgen05.mma (kind::f16, fp32 accumulation): warp 10
-//     S = Q K^T into a double-buffered 32-column TMEM tile, warp 11
-//     O^T = V^T P^T into 4 x 96 TMEM columns (dims on lanes, heads on
-//     columns).  The two products of neighbouring tiles are issued at the
-//     same time, and the softmax of tile i overlaps both.
+//     S = Q K^T into a 48-column TMEM tile, warp 11 O^T = V^T P^T into
+//     4 x 96 TMEM columns (dims on lanes, heads on columns).  The per-MMA
+//     cost barely grows with N up to 64, so 48-token tiles issue a third
+//     fewer QK^T instructions per token than 32-token ones; TMEM (384 + 48 +
+//     64 of 512 columns) then holds one S tile, which the softmax reads out
+//     at once so the next QK^T can start.
 //   * warps 0..3 (one thread per head) run the online softmax on the S row
-//     in registers (exp2 with the scale folded in), write P as bf16 (64-byte
+//     in registers (exp2 with the scale folded in), write P as bf16 (128-byte
 //     swizzled rows, the K-major B operand of PV), and rescale O^T only when
 //     a head's running maximum grows by more than 2^8 (exact either way: the
 //     final normalisation uses the same reference maximum).
 //   * Partial (unnormalised O, max, sums) per chunk go to the workspace and
-//     a combine kernel merges the chunks through their log-sum-exp (Day-0
-//     post, DCP section: partial outputs are combined by LSE).
+//     are merged through their log-sum-exp (Day-0 post, DCP section: partial
+//     outputs are combined by LSE), inside the row's cluster or by a combine
+//     kernel.
 #include <algorithm>
 #include <atomic>
 #include <cmath>
@@ -47,17 +48,19 @@ namespace dsa {
 
 namespace {
 
-constexpr int kTileTok = 32;
+constexpr int kTileTok = 48;
 constexpr int kDBlocks = kLatent / 64;                 // 9 blocks of 64 dims (128 B of bf16)
 constexpr int kQTmemBlocks = 2;                        // Q dims 448..575 in TMEM
 constexpr int kQSmemBlocks = kDBlocks - kQTmemBlocks;  // Q dims 0..447 in shared memory
 constexpr int kQBlockBytes = kHeads * 128;             // 12,288
 constexpr int kQBytes = kQSmemBlocks * kQBlockBytes;   // 86,016
-constexpr int kTileBufs = 3;
-constexpr int kTileDBlockBytes = kTileTok * 128;       // 4,096
-constexpr int kTileBytes = kDBlocks * kTileDBlockBytes;  // 36,864
-constexpr int kPBytes = kHeads * kTileTok * 2;         // 6,144
-constexpr int kMaxChunk = 1024;                        // tokens per CTA
+constexpr int kTileBufs = 2;
+constexpr int kTileDBlockBytes = kTileTok * 128;       // 6,144
+constexpr int kTileBytes = kDBlocks * kTileDBlockBytes;  // 55,296
+constexpr int kPRowBytes = 128;                        // a head's P row: 48 bf16 in a 128-byte swizzle row
+constexpr int kPBytes = kHeads * kPRowBytes;           // 12,288
+constexpr int kMaxChunk = 22 * kTileTok;               // 1,056 tokens per CTA
+constexpr int kMaskWords = kMaxChunk / 32 + 1;         // token validity bits (+1: tile masks read two words)
 constexpr int kInvariantChunk = 512;                   // tokens per CTA in the batch-invariant mode
 constexpr int kNvRecord = kValue / 2 + kValue / 16 + (kLatent - kValue);  // 352 B: NVFP4 latent record
 constexpr int kNvUnits = kValue / 16;                  // 16-dim units of E2M1 codes (the rest are E4M3)
@@ -69,25 +72,27 @@ constexpr int kThreads = 12 * 32;
 constexpr int kLoaderThreads = 192;
 constexpr int kMmaWarp = 10;
 constexpr int kPvWarp = 11;
-constexpr int kChunksPerThread = kTileTok * (kLatent / 16) / kLoaderThreads;  // 6 of the 1,152 16-B chunks
+constexpr int kChunksPerThread = kTileTok * (kLatent / 16) / kLoaderThreads;  // 9 of the 1,728 16-B units
+static_assert(kChunksPerThread * kLoaderThreads == kTileTok * (kLatent / 16), "loader split");
 constexpr int kOCols = 4 * kHeads;                     // 384 TMEM columns of O^T
-constexpr int kSCol = kOCols;                          // S buffers at 384 and 416
-constexpr int kQ8Col = kSCol + 2 * kTileTok;           // Q dims 448..575: 64 columns at 448
+constexpr int kSCol = kOCols;                          // the S tile: columns 384..431
+constexpr int kQ8Col = kSCol + 64;                     // Q dims 448..575: 64 columns at 448
 constexpr int kTmemCols = 512;
-static_assert(kQ8Col + 32 * kQTmemBlocks <= kTmemCols, "TMEM columns");
+static_assert(kSCol + kTileTok <= kQ8Col && kQ8Col + 32 * kQTmemBlocks <= kTmemCols, "TMEM columns");
 constexpr float kRescaleThreshold = 8.0f;              // log2 units
 
 constexpr int kOffQ = 0;
 constexpr int kOffTile = kOffQ + kQBytes;                    // 86,016
 constexpr int kOffP = kOffTile + kTileBufs * kTileBytes;     // 196,608
-constexpr int kOffAlpha = kOffP + 2 * kPBytes;               // 208,896
-constexpr int kOffBars = kOffAlpha + 128 * 4;                // 209,408
+constexpr int kOffAlpha = kOffP + 2 * kPBytes;               // 221,184
+constexpr int kOffBars = kOffAlpha + 128 * 4;                // 221,696
+static_assert(kOffTile % 1024 == 0 && kOffP % 1024 == 0 && kTileDBlockBytes % 1024 == 0, "swizzle atoms");
 // q, q8, tiles full/empty, s full/empty, p full, PV done per P buffer, PV drain
-constexpr int kNumBars = 2 + 2 * kTileBufs + 2 + 2 + 2 + 2 + 1;
+constexpr int kNumBars = 2 + 2 * kTileBufs + 2 + 2 + 2 + 1;
 constexpr int kOffMisc = kOffBars + kNumBars * 8;
 constexpr int kOffTok = kOffMisc + 16;                       // int32 per token: block row * 64 + slot, or -1
 constexpr int kOffMask = kOffTok + 4 * kMaxChunk;            // one validity bit per token
-constexpr size_t kSmemBytes = 1024 + kOffMask + (size_t)kMaxChunk / 8;
+constexpr size_t kSmemBytes = 1024 + kOffMask + (size_t)kMaskWords * 4;
 static_assert(kSmemBytes <= 232448, "shared memory");
 
 struct MlaParams {
@@ -101,7 +106,7 @@ struct MlaParams {
   int32_t cap;
   const int32_t* idx;
   int32_t k;
-  int32_t chunk;    // tokens per CTA (multiple of 32)
+  int32_t chunk;    // tokens per CTA
   int32_t nsplit;
   float logit_scale_log2;  // sm_scale * latent_scale * log2(e)
   const uint16_t* q_mla;   // bf16 [rows][96][576]
@@ -135,6 +140,56 @@ __device__ __forceinline__ bool bar_or_softmax(bool v) {
   return r != 0;
 }
 
+// The in-cluster merge of a row's NS chunks for this CTA's share [v0, v1) of
+// the row's output float4s: every chunk's partial is read from the workspace
+// (L2; U x NS 16-byte loads in flight per thread), weighted and summed in
+// chunk order with the combine kernel's arithmetic, and written as bf16.  A
+// zero weight skips its chunk.  (Reading the peers' partials from their shared
+// memory instead was measured slower.)
+template <int NS>
+__device__ __forceinline__ void merge_share(const float* opart_row, const float* wgt, int v0, int v1,
+                                            uint16_t* out_row) {
+  constexpr int U = NS >= 8 ? 2 : NS >= 4 ? 4 : NS >= 2 ? 8 : 16;
+  for (int vb = v0 + (int)threadIdx.x; vb < v1; vb += U * kThreads) {
+    float4 x[U][NS];
+#pragma unroll
+    for (int u = 0; u < U; ++u) {
+      const int v = vb + u * kThreads;
+      if (v < v1) {
+        const int hh = v / (kValue / 4), d = (v % (kValue / 4)) * 4;
+#pragma unroll
+        for (int s = 0; s < NS; ++s)
+          if (wgt[hh * kMaxFusedSplit + s] != 0.f)
+            x[u][s] = *reinterpret_cast<const float4*>(opart_row + ((int64_t)s * kHeads + hh) * kValue + d);
+      }
+    }
+#pragma unroll
+    for (int u = 0; u < U; ++u) {
+      const int v = vb + u * kThreads;
+      if (v < v1) {
+        const int hh = v / (kValue / 4), d = (v % (kValue / 4)) * 4;
+        float4 a = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+        for (int s = 0; s < NS; ++s) {
+          const float w = wgt[hh * kMaxFusedSplit + s];
+          if (w != 0.f) {
+            a.x = fmaf(w, x[u][s].x, a.x);
+            a.y = fmaf(w, x[u][s].y, a.y);
+            a.z = fmaf(w, x[u][s].z, a.z);
+            a.w = fmaf(w, x[u][s].w, a.w);
+          }
+        }
+        const __nv_bfloat162 lo = __floats2bfloat162_rn(a.x, a.y);
+        const __nv_bfloat162 hi = __floats2bfloat162_rn(a.z, a.w);
+        uint2 pk;
+        pk.x = *reinterpret_cast<const uint32_t*>(&lo);
+        pk.y = *reinterpret_cast<const uint32_t*>(&hi);
+        *reinterpret_cast<uint2*>(out_row + hh * kValue + d) = pk;
+      }
+    }
+  }
+}
+
 // kNV: NVFP4 latent records (352 B: E2M1 dims 0..511 with an E4M3 scale per
 // 16 dims, E4M3 dims 512..575), else E4M3 records (576 B).  Both are widened
 // to the same bf16 tile, exactly.
@@ -142,7 +197,7 @@ template <bool kNV>
 __global__ void __launch_bounds__(kThreads, 1)
     sparse_mla_kernel(const __grid_constant__ CUtensorMap tmap_q, const MlaParams p) {
   constexpr int kRec = kNV ? kNvRecord : kLatent;  // bytes per token record
-  // S = Q K^T: A = Q (K-major), B = latent tile (K-major); M = 128, N = 32.
+  // S = Q K^T: A = Q (K-major), B = latent tile (K-major); M = 128, N = 48.
   constexpr uint32_t kIdescQK = make_idesc(kFmtBF16, kFmtBF16, 0, 0, 128, kTileTok);
   // O^T = V^T P^T: A = latent tile (MN-major, M = dims), B = P (K-major); M = 128, N = 96.
   constexpr uint32_t kIdescPV = make_idesc(kFmtBF16, kFmtBF16, 1, 0, 128, kHeads);
@@ -155,11 +210,11 @@ __global__ void __launch_bounds__(kThreads, 1)
   const uint32_t q8_full = bars + 8u;  // Q dims 448..575 written to TMEM by the softmax warps
   auto tile_full = [&](int b) { return bars + 8u * (2 + b); };
   auto tile_empty = [&](int b) { return bars + 8u * (2 + kTileBufs + b); };
-  auto s_full = [&](int b) { return bars + 8u * (2 + 2 * kTileBufs + b); };
-  auto s_empty = [&](int b) { return bars + 8u * (4 + 2 * kTileBufs + b); };
-  auto p_full = [&](int b) { return bars + 8u * (6 + 2 * kTileBufs + b); };
-  auto pv_done = [&](int b) { return bars + 8u * (8 + 2 * kTileBufs + b); };  // PV of the tiles using P buffer b
-  const uint32_t pv_drain = bars + 8u * (10 + 2 * kTileBufs);
+  const uint32_t s_full = bars + 8u * (2 + 2 * kTileBufs);
+  const uint32_t s_empty = bars + 8u * (3 + 2 * kTileBufs);
+  auto p_full = [&](int b) { return bars + 8u * (4 + 2 * kTileBufs + b); };
+  auto pv_done = [&](int b) { return bars + 8u * (6 + 2 * kTileBufs + b); };  // PV of the tiles using P buffer b
+  const uint32_t pv_drain = bars + 8u * (8 + 2 * kTileBufs);
   // the MMA issuer's teardown barrier reuses q_full's slot after Q has landed
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + kOffMisc);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + kOffMisc + 4);
@@ -185,9 +240,9 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(tile_full(b), kLoaderThreads / 32);
       mbar_init(tile_empty(b), 1);
     }
+    mbar_init(s_full, 1);
+    mbar_init(s_empty, 4);
     for (int b = 0; b < 2; ++b) {
-      mbar_init(s_full(b), 1);
-      mbar_init(s_empty(b), 4);
       mbar_init(p_full(b), 4);
       mbar_init(pv_done(b), 1);
     }
@@ -200,6 +255,46 @@ __global__ void __launch_bounds__(kThreads, 1)
     tmem_alloc(smem_u32(tmem_slot), kTmemCols);
     tmem_relinquish();
   }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+  // Q is an input of the step, not an output of the previous kernel, so its
+  // loads go out before the wait below when the chunk's size is known without
+  // the previous kernel's output (no chunk table): dims 0..447 by TMA into
+  // shared memory (the MMA issuer waits for them), dims 448..575 of head h by
+  // thread h into TMEM, all sixteen 16-byte loads in flight before the first
+  // store.  With a chunk table they go out after the wait, and only for a
+  // chunk that is not empty.
+  auto issue_q = [&]() {
+    if (threadIdx.x == kMmaWarp * 32) {
+      mbar_arrive_expect_tx(q_full, kQBytes);
+      for (int kb = 0; kb < kQSmemBlocks; ++kb)
+        tma_load_2d(sbase + kOffQ + kb * kQBlockBytes, &tmap_q, kb * 64, row * kHeads, q_full);
+    }
+    if (warp < 4) {
+      const int h = threadIdx.x;
+      const bool live = h < kHeads;
+      const uint4* src = reinterpret_cast<const uint4*>(p.q_mla + ((int64_t)row * kHeads + (live ? h : 0)) * kLatent +
+                                                        64 * kQSmemBlocks);
+      uint4 v[8 * kQTmemBlocks];
+#pragma unroll
+      for (int c = 0; c < 8 * kQTmemBlocks; ++c) v[c] = live ? __ldg(src + c) : make_uint4(0, 0, 0, 0);
+#pragma unroll
+      for (int c = 0; c < 4 * kQTmemBlocks; ++c)
+        asm volatile("tcgen05.st.sync.aligned.32x32b.x8.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8};"
+                     ::"r"(tmem + ((uint32_t)(warp * 32) << 16) + kQ8Col + 8 * c), "r"(v[2 * c].x), "r"(v[2 * c].y),
+                     "r"(v[2 * c].z), "r"(v[2 * c].w), "r"(v[2 * c + 1].x), "r"(v[2 * c + 1].y),
+                     "r"(v[2 * c + 1].z), "r"(v[2 * c + 1].w)
+                     : "memory");
+      tmem_st_wait();
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(q8_full);
+    }
+  };
+  const bool q_early = p.seg == nullptr && count > 0;
+  if (q_early) issue_q();
   grid_dep_wait();    // the indices come from the previous kernel
   grid_dep_launch();
   if (p.seg) {
@@ -208,36 +303,53 @@ __global__ void __launch_bounds__(kThreads, 1)
     count = max(0, min(min(sg[1] - c0, p.chunk), p.k - c0));
   }
   const int ntiles = (count + kTileTok - 1) / kTileTok;
+  if (!q_early && ntiles > 0) issue_q();
   // physical slots of the chunk's latent rows, block row * 64 + slot (-1: a -1
-  // index or padding)
-  for (int i = threadIdx.x; i < ntiles * kTileTok; i += kThreads) {
-    int32_t phys = -1;
-    if (i < count) {
-      const int t = p.idx[(int64_t)row * p.k + c0 + i];
-      if (t >= 0) {
-        const int r = (t < vis) ? p.block_table[(int64_t)b_seq * p.max_blocks + t / kBlock] : -1;
-        if (r >= 0 && r < p.num_blocks)
-          phys = r * kBlock + t % kBlock;
+  // index or padding), and one validity bit per token in 32-token words, by
+  // warps 4..11 (warps 0..3 load Q into TMEM meanwhile): every index of a
+  // thread is loaded before its block-table entries.  Whole warps run each
+  // pass (the bound is a multiple of 32, within kMaxChunk).
+  if (warp >= 4) {
+    constexpr int kTr = kThreads - 128;
+    constexpr int kPer = (kMaxChunk + kTr - 1) / kTr;  // 5
+    const int bound = (ntiles * kTileTok + 31) / 32 * 32;
+    const int i0 = threadIdx.x - 128;
+    int t[kPer], r[kPer];
+#pragma unroll
+    for (int j = 0; j < kPer; ++j) {
+      const int i = i0 + j * kTr;
+      t[j] = i < count ? p.idx[(int64_t)row * p.k + c0 + i] : -1;
+    }
+#pragma unroll
+    for (int j = 0; j < kPer; ++j)
+      r[j] = (t[j] >= 0 && t[j] < vis) ? p.block_table[(int64_t)b_seq * p.max_blocks + t[j] / kBlock] : -1;
+#pragma unroll
+    for (int j = 0; j < kPer; ++j) {
+      const int i = i0 + j * kTr;
+      if (i - lane >= bound) break;  // warp-uniform
+      int32_t phys = -1;
+      if (t[j] >= 0) {
+        if (r[j] >= 0 && r[j] < p.num_blocks)
+          phys = r[j] * kBlock + t[j] % kBlock;
         else
           report(p.status, DSA_ERR_BOUNDS);
       }
+      tok_phys[i] = phys;
+      const uint32_t bits = __ballot_sync(0xffffffffu, phys >= 0);  // a warp pass covers 32 consecutive tokens
+      if (lane == 0) tile_mask[i >> 5] = bits;
     }
-    tok_phys[i] = phys;
-    const uint32_t bits = __ballot_sync(0xffffffffu, phys >= 0);  // a warp pass covers 32 consecutive tokens
-    if ((threadIdx.x & 31) == 0) tile_mask[i >> 5] = bits;
   }
-  tc_fence_before();
+  if (threadIdx.x == 0) tile_mask[(ntiles * kTileTok + 31) / 32] = 0u;  // the word after the last one read
   __syncthreads();
-  tc_fence_after();
-  const uint32_t tmem = *tmem_slot;
 
+  // this chunk's (running max in log2 units, sum of the rounded p, sum of p)
+  // per head, kept by the softmax thread of the head; an empty chunk
+  // contributes nothing
+  float4 ml_mine = make_float4(-INFINITY, 0.f, 0.f, 0.f);
   if (ntiles > 0) {
     if (warp == kMmaWarp) {
       if (lane == 0) {
-        // ------------------------------------------------ Q load + MMA issuer
-        mbar_arrive_expect_tx(q_full, kQBytes);
-        for (int kb = 0; kb < kQSmemBlocks; ++kb)
-          tma_load_2d(sbase + kOffQ + kb * kQBlockBytes, &tmap_q, kb * 64, row * kHeads, q_full);
+        // ------------------------------------------------ QK issuer
         bool ok = mbar_wait(q_full, 0, abort_flag, p.status);
         ok = ok && mbar_wait(q8_full, 0, abort_flag, p.status);
         // Shared-memory descriptors: the start address is the low 14 bits (in
@@ -247,8 +359,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         const uint32_t q_lo = (uint32_t)q_desc, sw128_hi = (uint32_t)(q_desc >> 32);
         const uint32_t t_lo0 = (uint32_t)smem_desc(sbase + kOffTile, 16, 1024, kLayoutSw128);
         auto issue_qk = [&](int i) {
-          const int b = i & 1;
-          const uint32_t d = tmem + kSCol + kTileTok * b;
+          const uint32_t d = tmem + kSCol;
           const uint32_t t_lo = t_lo0 + (uint32_t)((i % kTileBufs) * kTileBytes / 16);
 #pragma unroll
           for (int kb = 0; kb < kQSmemBlocks; ++kb) {
@@ -263,12 +374,12 @@ __global__ void __launch_bounds__(kThreads, 1)
             mma_bf16_tmem_a(d, tmem + kQ8Col + 8 * kk,
                             desc64(t_lo + ((kQSmemBlocks + kk / 4) * kTileDBlockBytes + 32 * (kk % 4)) / 16, sw128_hi),
                             kIdescQK, 1u);
-          mma_commit(s_full(b));
+          mma_commit(s_full);
         };
         for (int i = 0; ok && i < ntiles; ++i) {
-          // tile i landed; S buffer i & 1 read out by the softmax of tile i - 2
+          // tile i landed; the S tile read out by the softmax of tile i - 1
           ok = mbar_wait(tile_full(i % kTileBufs), (i / kTileBufs) & 1, abort_flag, p.status) &&
-               mbar_wait(s_empty(i & 1), ((i >> 1) & 1) ^ 1, abort_flag, p.status);
+               mbar_wait(s_empty, (i & 1) ^ 1, abort_flag, p.status);
           if (!ok) break;
           tc_fence_after();
           issue_qk(i);
@@ -283,7 +394,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         // descriptors as in the QK issuer: offsets go to the low word
         const uint64_t a_desc = smem_desc(sbase + kOffTile, kTileDBlockBytes, 1024, kLayoutSw128);
         const uint32_t a_lo0 = (uint32_t)a_desc, a_hi = (uint32_t)(a_desc >> 32);
-        const uint64_t p_desc = smem_desc(sbase + kOffP, 16, 512, kLayoutSw64);
+        const uint64_t p_desc = smem_desc(sbase + kOffP, 16, 1024, kLayoutSw128);
         const uint32_t p_lo0 = (uint32_t)p_desc, p_hi = (uint32_t)(p_desc >> 32);
         for (int i = 0; i < ntiles; ++i) {
           const int b = i & 1;
@@ -309,9 +420,10 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
     } else if (warp >= 4) {
       // ------------------------------------------------ gather + E4M3 -> bf16
+      constexpr int kThreadsPerTok = kLoaderThreads / kTileTok;  // 4
       const int lt = threadIdx.x - 128;                 // 0..191
-      const int tok = lt / kChunksPerThread;             // token row of the tile, 0..31
-      const int g = lt % kChunksPerThread;               // chunks g, g+6, ..., g+30 of the 36
+      const int tok = lt / kThreadsPerTok;               // token row of the tile, 0..47
+      const int g = lt % kThreadsPerTok;                 // units g, g+4, ..., g+32 of the 36
       // three tiles in flight per thread (a register ring), so the gather of
       // tile i+3 overlaps the rest; each tile is widened to bf16 in registers
       // before its buffer is free, so only the shared-memory stores wait
@@ -325,7 +437,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         const uint8_t* rec = p.latent_base + (int64_t)(phys >> 6) * p.row_stride + (phys & (kBlock - 1)) * kRec;
 #pragma unroll
         for (int c = 0; c < kChunksPerThread; ++c) {
-          const int u = g + kChunksPerThread * c;
+          const int u = g + kThreadsPerTok * c;
           buf[c] = make_uint4(0, 0, 0, 0);
           if (phys < 0) continue;
           if (!kNV) {
@@ -338,33 +450,29 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
         }
       };
+      // widen each unit after the buffer is free (the register ring already
+      // holds three raw tiles), then store it 128-byte swizzled
       auto store = [&](int i, const uint4 (&buf)[kChunksPerThread]) -> bool {
         if (i >= ntiles) return true;
-        uint4 cv[2 * kChunksPerThread];  // the widened units: 32 bytes of bf16 each
-#pragma unroll
-        for (int c = 0; c < kChunksPerThread; ++c) {
-          uint32_t o[8];
-          if (kNV && g + kChunksPerThread * c < kNvUnits) {
-            nvfp4x16_to_bf16x16(buf[c].x, buf[c].y, buf[c].z, o);
-          } else {
-            const uint32_t w[4] = {buf[c].x, buf[c].y, buf[c].z, buf[c].w};
-#pragma unroll
-            for (int q = 0; q < 4; ++q) e4m3x4_to_bf16x4(w[q], o[2 * q], o[2 * q + 1]);
-          }
-          cv[2 * c] = make_uint4(o[0], o[1], o[2], o[3]);
-          cv[2 * c + 1] = make_uint4(o[4], o[5], o[6], o[7]);
-        }
         const int b = i % kTileBufs;
         const bool ok = mbar_wait(tile_empty(b), ((i / kTileBufs) & 1) ^ 1, abort_flag, p.status);
         if (!__all_sync(0xffffffffu, ok)) return false;
         uint8_t* tile = smem + kOffTile + b * kTileBytes;
 #pragma unroll
         for (int c = 0; c < kChunksPerThread; ++c) {
-          const int ch = g + kChunksPerThread * c;  // 16-byte chunk of the 576-byte row: dims [16 ch, +16)
+          const int ch = g + kThreadsPerTok * c;  // 16-dim unit of the 576-dim row: dims [16 ch, +16)
+          uint32_t o[8];
+          if (kNV && ch < kNvUnits) {
+            nvfp4x16_to_bf16x16(buf[c].x, buf[c].y, buf[c].z, o);
+          } else {
+            const uint32_t w[4] = {buf[c].x, buf[c].y, buf[c].z, buf[c].w};
+#pragma unroll
+            for (int q = 0; q < 4; ++q) e4m3x4_to_bf16x4(w[q], o[2 * q], o[2 * q + 1]);
+          }
           uint8_t* blk = tile + (ch >> 2) * kTileDBlockBytes;
           const uint32_t inner = (uint32_t)((ch & 3) * 32);
-          *reinterpret_cast<uint4*>(blk + swz128(tok * 128 + inner)) = cv[2 * c];
-          *reinterpret_cast<uint4*>(blk + swz128(tok * 128 + inner + 16)) = cv[2 * c + 1];
+          *reinterpret_cast<uint4*>(blk + swz128(tok * 128 + inner)) = make_uint4(o[0], o[1], o[2], o[3]);
+          *reinterpret_cast<uint4*>(blk + swz128(tok * 128 + inner + 16)) = make_uint4(o[4], o[5], o[6], o[7]);
         }
         fence_proxy_async_smem();
         __syncwarp();
@@ -386,44 +494,32 @@ __global__ void __launch_bounds__(kThreads, 1)
       // ------------------------------------------------ softmax (thread = head)
       const int h = threadIdx.x;  // TMEM lane
       const bool live = h < kHeads;
-      {
-        // Q dims 448..575 of head h into TMEM (the A operand of the last eight
-        // QK steps), 8 columns (16 dims) at a time
-        const uint4* src = reinterpret_cast<const uint4*>(p.q_mla + ((int64_t)row * kHeads + h) * kLatent +
-                                                          64 * kQSmemBlocks);
-#pragma unroll 1
-        for (int c = 0; c < 4 * kQTmemBlocks; ++c) {
-          const uint4 v0 = live ? __ldg(src + 2 * c) : make_uint4(0, 0, 0, 0);
-          const uint4 v1 = live ? __ldg(src + 2 * c + 1) : make_uint4(0, 0, 0, 0);
-          asm volatile("tcgen05.st.sync.aligned.32x32b.x8.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8};"
-                       ::"r"(tmem + ((uint32_t)(warp * 32) << 16) + kQ8Col + 8 * c), "r"(v0.x), "r"(v0.y),
-                       "r"(v0.z), "r"(v0.w), "r"(v1.x), "r"(v1.y), "r"(v1.z), "r"(v1.w)
-                       : "memory");
-        }
-        tmem_st_wait();
-        tc_fence_before();
-        __syncwarp();
-        if (lane == 0) mbar_arrive(q8_full);
-      }
       float m_used = -INFINITY, l_round = 0.f, l_exact = 0.f;
       bool ok = true;
       for (int i = 0; i < ntiles; ++i) {
         const int b = i & 1;
-        ok = mbar_wait(s_full(b), (i >> 1) & 1, abort_flag, p.status);
+        ok = mbar_wait(s_full, i & 1, abort_flag, p.status);
         if (bar_or_softmax(!ok)) { ok = false; break; }   // uniform over the 128 softmax threads
         tc_fence_after();
-        uint32_t r[32];
-        tmem_ld32(tmem + ((uint32_t)(warp * 32) << 16) + kSCol + kTileTok * b, r);
+        uint32_t r[kTileTok];
+        {
+          const uint32_t ta = tmem + ((uint32_t)(warp * 32) << 16) + kSCol;
+          tmem_ld32(ta, *reinterpret_cast<uint32_t(*)[32]>(r));
+          tmem_ld16(ta + 32, r + 32);
+        }
         tmem_ld_wait();
         tc_fence_before();
         __syncwarp();
-        if (lane == 0) mbar_arrive(s_empty(b));  // the QK issuer may overwrite this S buffer
-        float x[32];
-        const uint32_t vmask = tile_mask[i];
+        if (lane == 0) mbar_arrive(s_empty);  // the QK issuer may overwrite the S tile
+        float x[kTileTok];
+        // validity bits of tokens [48 i, 48 i + 48) from the 32-token words
+        const int t0 = i * kTileTok;
+        const uint64_t vmask =
+            ((((uint64_t)tile_mask[(t0 >> 5) + 1]) << 32) | (uint64_t)tile_mask[t0 >> 5]) >> (t0 & 31);
         float m0 = -INFINITY, m1 = -INFINITY;
 #pragma unroll
-        for (int j = 0; j < 32; ++j) {
-          x[j] = ((vmask >> j) & 1u) ? __uint_as_float(r[j]) * p.logit_scale_log2 : -INFINITY;
+        for (int j = 0; j < kTileTok; ++j) {
+          x[j] = ((vmask >> j) & 1ull) ? __uint_as_float(r[j]) * p.logit_scale_log2 : -INFINITY;
           if (j & 1) m1 = fmaxf(m1, x[j]); else m0 = fmaxf(m0, x[j]);
         }
         const float m_tile = fmaxf(m0, m1);
@@ -454,12 +550,12 @@ __global__ void __launch_bounds__(kThreads, 1)
             tmem_st_wait();
           }
         }
-        // probabilities -> bf16 P row h (64 bytes, 64-byte swizzle)
-        uint32_t pk[16];
+        // probabilities -> bf16 P row h (96 of 128 bytes, 128-byte swizzle)
+        uint32_t pk[kTileTok / 2];
         float srnd = 0.f, sex = 0.f;
         if (m_used != -INFINITY) {
 #pragma unroll
-          for (int j = 0; j < 32; j += 2) {
+          for (int j = 0; j < kTileTok; j += 2) {
             const float p0 = ex2(x[j] - m_used), p1 = ex2(x[j + 1] - m_used);  // 2^-inf = 0 when masked
             const __nv_bfloat162 bb = __floats2bfloat162_rn(p0, p1);
             const float2 back = __bfloat1622float2(bb);
@@ -469,7 +565,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
         } else {
 #pragma unroll
-          for (int j = 0; j < 16; ++j) pk[j] = 0;
+          for (int j = 0; j < kTileTok / 2; ++j) pk[j] = 0;
         }
         l_round += srnd;
         l_exact += sex;
@@ -479,8 +575,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (live) {
           uint8_t* prow = smem + kOffP + b * kPBytes;
 #pragma unroll
-          for (int c = 0; c < 4; ++c)
-            *reinterpret_cast<uint4*>(prow + swz64(h * 64 + c * 16)) =
+          for (int c = 0; c < kTileTok / 8; ++c)
+            *reinterpret_cast<uint4*>(prow + swz128(h * kPRowBytes + c * 16)) =
                 make_uint4(pk[4 * c], pk[4 * c + 1], pk[4 * c + 2], pk[4 * c + 3]);
         }
         fence_proxy_async_smem();
@@ -490,15 +586,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       // ---- this chunk's running max and sums per head
       ok = !bar_or_softmax(!ok);
-      if (ok && live) {
-        const int64_t part = (int64_t)row * p.nsplit + split;
-        reinterpret_cast<float4*>(p.ml)[part * kHeads + h] = make_float4(m_used, l_round, l_exact, 0.f);
-      }
+      if (ok && live) ml_mine = make_float4(m_used, l_round, l_exact, 0.f);
     }
-  } else if (threadIdx.x < kHeads) {
-    // empty chunk: contributes nothing
-    const int64_t part = (int64_t)row * p.nsplit + split;
-    reinterpret_cast<float4*>(p.ml)[part * kHeads + threadIdx.x] = make_float4(-INFINITY, 0.f, 0.f, 0.f);
   }
   // ---- epilogue: the chunk's unnormalised O^T to the workspace, by all twelve
   //      warps.  Every MMA has completed: both issuers waited for theirs before
@@ -508,8 +597,9 @@ __global__ void __launch_bounds__(kThreads, 1)
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
+  const int64_t part = (int64_t)row * p.nsplit + split;
+  if (threadIdx.x < kHeads) reinterpret_cast<float4*>(p.ml)[part * kHeads + threadIdx.x] = ml_mine;
   if (ntiles > 0 && *abort_flag == 0) {
-    const int64_t part = (int64_t)row * p.nsplit + split;
     float* op = p.opart + part * kHeads * kValue;
     const int quarter = warp & 3, hg = warp >> 2;
     const uint32_t lane_base = tmem + ((uint32_t)(quarter * 32) << 16) + hg * 32;
@@ -535,17 +625,26 @@ __global__ void __launch_bounds__(kThreads, 1)
     // ---- the row's chunks are the cluster: once every chunk's partials are
     //      written (the cluster barrier orders them), each CTA merges a share of
     //      the row's outputs through the chunks' log-sum-exp, as the combine
-    //      kernel does
+    //      kernel does.  A zero weight (an empty chunk, or one whose maximum
+    //      lies far below) skips its partial, which an empty chunk never wrote.
     cooperative_groups::this_cluster().sync();
-    const float4* mlr = reinterpret_cast<const float4*>(p.ml) + (int64_t)row * p.nsplit * kHeads;
     float* wgt = reinterpret_cast<float*>(smem + kOffTile);  // [96][kMaxFusedSplit]; the tiles are free
     if (threadIdx.x < kHeads) {
       const int h = threadIdx.x;
+      const float4* mlr = reinterpret_cast<const float4*>(p.ml) + (int64_t)row * p.nsplit * kHeads;
+      float4 mv[kMaxFusedSplit];
+#pragma unroll
+      for (int s = 0; s < kMaxFusedSplit; ++s)
+        if (s < p.nsplit) mv[s] = mlr[s * kHeads + h];
       float M = -INFINITY;
-      for (int s = 0; s < p.nsplit; ++s) M = fmaxf(M, mlr[s * kHeads + h].x);
+#pragma unroll
+      for (int s = 0; s < kMaxFusedSplit; ++s)
+        if (s < p.nsplit) M = fmaxf(M, mv[s].x);
       float den = 0.f, ex = 0.f;
-      for (int s = 0; s < p.nsplit; ++s) {
-        const float4 v = mlr[s * kHeads + h];
+#pragma unroll
+      for (int s = 0; s < kMaxFusedSplit; ++s) {
+        if (s >= p.nsplit) break;
+        const float4 v = mv[s];
         const float w = (M == -INFINITY || v.x == -INFINITY) ? 0.f : ex2(v.x - M);
         den += w * v.y;
         ex += w * v.z;
@@ -560,29 +659,17 @@ __global__ void __launch_bounds__(kThreads, 1)
     __syncthreads();
     constexpr int kVec = kHeads * kValue / 4;  // float4s of the row's output
     const int v0 = (int)((int64_t)kVec * split / p.nsplit), v1 = (int)((int64_t)kVec * (split + 1) / p.nsplit);
-    for (int v = v0 + (int)threadIdx.x; v < v1; v += kThreads) {
-      const int hh = v / (kValue / 4), d = (v % (kValue / 4)) * 4;
-      const float* src = p.opart + ((int64_t)row * p.nsplit * kHeads + hh) * kValue + d;
-      float4 x[kMaxFusedSplit];
-#pragma unroll
-      for (int s = 0; s < kMaxFusedSplit; ++s)
-        if (s < p.nsplit) x[s] = *reinterpret_cast<const float4*>(src + (int64_t)s * kHeads * kValue);
-      float4 a = make_float4(0.f, 0.f, 0.f, 0.f);
-#pragma unroll
-      for (int s = 0; s < kMaxFusedSplit; ++s)
-        if (s < p.nsplit) {
-          const float w = wgt[hh * kMaxFusedSplit + s];
-          a.x = fmaf(w, x[s].x, a.x);
-          a.y = fmaf(w, x[s].y, a.y);
-          a.z = fmaf(w, x[s].z, a.z);
-          a.w = fmaf(w, x[s].w, a.w);
-        }
-      const __nv_bfloat162 lo = __floats2bfloat162_rn(a.x, a.y);
-      const __nv_bfloat162 hi = __floats2bfloat162_rn(a.z, a.w);
-      uint2 pk;
-      pk.x = *reinterpret_cast<const uint32_t*>(&lo);
-      pk.y = *reinterpret_cast<const uint32_t*>(&hi);
-      *reinterpret_cast<uint2*>(p.out + ((int64_t)row * kHeads + hh) * kValue + d) = pk;
+    uint16_t* out_row = p.out + (int64_t)row * kHeads * kValue;
+    const float* opart_row = p.opart + (int64_t)row * p.nsplit * kHeads * kValue;
+    switch (p.nsplit) {
+      case 1: merge_share<1>(opart_row, wgt, v0, v1, out_row); break;
+      case 2: merge_share<2>(opart_row, wgt, v0, v1, out_row); break;
+      case 3: merge_share<3>(opart_row, wgt, v0, v1, out_row); break;
+      case 4: merge_share<4>(opart_row, wgt, v0, v1, out_row); break;
+      case 5: merge_share<5>(opart_row, wgt, v0, v1, out_row); break;
+      case 6: merge_share<6>(opart_row, wgt, v0, v1, out_row); break;
+      case 7: merge_share<7>(opart_row, wgt, v0, v1, out_row); break;
+      default: merge_share<8>(opart_row, wgt, v0, v1, out_row); break;
     }
   }
 }
@@ -623,11 +710,11 @@ __global__ void __launch_bounds__(256) mla_combine_kernel(const float* __restric
     float4 x[kMaxSplit];
 #pragma unroll
     for (int s = 0; s < kMaxSplit; ++s)
-      if (s < nsplit) x[s] = *reinterpret_cast<const float4*>(src + (int64_t)s * kHeads * kValue);
+      if (s < nsplit && wgt[hl][s] != 0.f) x[s] = *reinterpret_cast<const float4*>(src + (int64_t)s * kHeads * kValue);
     float4 a = make_float4(0.f, 0.f, 0.f, 0.f);
 #pragma unroll
     for (int s = 0; s < kMaxSplit; ++s)
-      if (s < nsplit) {
+      if (s < nsplit && wgt[hl][s] != 0.f) {
         const float w = wgt[hl][s];
         a.x = fmaf(w, x[s].x, a.x); a.y = fmaf(w, x[s].y, a.y);
         a.z = fmaf(w, x[s].z, a.z); a.w = fmaf(w, x[s].w, a.w);
@@ -647,7 +734,7 @@ __global__ void __launch_bounds__(256) mla_combine_kernel(const float* __restric
 // device (asked once per device and size).
 template <bool kNV>
 bool fused_cluster_ok(int nsplit) {
-  static int known[64][kMaxFusedSplit + 1] = {};  // 0 unknown, 1 yes, 2 no
+  static std::atomic<int> known[64][kMaxFusedSplit + 1];  // 0 unknown, 1 yes, 2 no
   int dev = 0;
   cudaGetDevice(&dev);
   if (dev < 0 || dev >= 64 || nsplit < 1 || nsplit > kMaxFusedSplit) return false;
@@ -736,7 +823,7 @@ bool mla_setup(const dsa_paged_cache_t& c, const dsa_batch_t& bt, const uint16_t
                  out,
                  lse,
                  nullptr};
-  static bool attr_set[64] = {};
+  static std::atomic<bool> attr_set[64];
   int dev = 0;
   cudaGetDevice(&dev);
   if (dev < 64 && !attr_set[dev]) {

@@ -1132,7 +1132,7 @@ __global__ void __launch_bounds__(kResThreads, kStream ? 1 : 2)
 template <int C, bool kStream, typename In>
 dsa_status_t launch_cluster(const In* scores, int64_t ld, const int32_t* row_lens, const int32_t* seq_lens,
                             int nq, int rows, int cap, int k, int32_t* out, int32_t* status, cudaStream_t st) {
-  static bool attr_set[64] = {};
+  static std::atomic<bool> attr_set[64];
   int dev = 0;
   cudaGetDevice(&dev);
   if (dev < 64 && !attr_set[dev]) {
@@ -1173,7 +1173,7 @@ dsa_status_t launch_cluster(const In* scores, int64_t ld, const int32_t* row_len
 // (asked once per device; a cluster of 16 needs the non-portable size).
 template <int C, typename In>
 bool stream_cluster_ok() {
-  static int known[64] = {};  // 0 unknown, 1 yes, 2 no
+  static std::atomic<int> known[64];  // 0 unknown, 1 yes, 2 no
   int dev = 0;
   cudaGetDevice(&dev);
   if (dev >= 64) return false;
@@ -1313,7 +1313,7 @@ dsa_status_t launch_topk(const float* scores, int64_t ld, const int32_t* row_len
     topk_threshold_kernel<<<rows, kThreads, 0, st>>>(row_lens, seq_lens, nq, cap, k, ws);
     topk_collect_kernel<<<grid, kThreads, 0, st>>>(scores, ld, row_lens, seq_lens, nq, cap, k, ws, status);
   }
-  static bool attr_set[64] = {};
+  static std::atomic<bool> attr_set[64];
   int dev = 0;
   cudaGetDevice(&dev);
   const size_t smem = topk_final_smem_bytes();

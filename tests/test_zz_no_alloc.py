@@ -1,61 +1,98 @@
 """The top-k entry point that allocates nothing (dsa_topk_noalloc).
 
-Some callers cannot call cudaMalloc (a framework that owns the device memory
-pool, or a loop where allocation could block or synchronise the device); this
-variant keeps its scratch in a device array built into the library.  The test
-calls it through the C ABI twice in a row, on different inputs, and checks
-each result against the workspace-taking dsa_topk (top-k is bit-exact), so a
-second call that saw stale scratch from the first would fail.  This file is
-collected last on purpose.
+Some callers cannot call cudaMalloc: a host framework that owns the whole
+device memory pool, or a serving loop where an allocation could block or
+synchronise the device.  This variant keeps its scratch in a device array
+built into the library, so it takes no workspace argument.
+
+The scratch is only touched by the four-kernel top-k (histograms, counters,
+selected and candidate lists), which runs for rows too long to hold on chip
+when the streaming cluster is not used.  The tests therefore force that path
+with dsa_topk_force_multipass and use rows longer than 245,760 tokens, and
+call the entry point twice in a row on different inputs: the first call
+leaves its histograms, counters and candidates behind, so a second call that
+read stale scratch (a missed clear, a wrong offset) would select differently.
+Each call is checked bit for bit against the oracle and against dsa_topk with
+a caller-owned workspace.  This file is collected last on purpose.
 """
 import numpy as np
 import pytest
 import torch
 
+import oracle
 from dsa_sparse_attention_index_gb300 import binding
 
 pytestmark = pytest.mark.gpu
 
+K = 2048
 
-def _inputs(seed, rows, L):
+
+def _long_rows(seed, rows=6, n=300_000):
+    """Rows past the on-chip limit: ties on the k-th key, an all-equal row
+    (its candidates overflow the candidate list), a row shorter than k, and
+    rows of mixed lengths."""
     rng = np.random.default_rng(seed)
-    m = rng.standard_normal((rows, L)).astype(np.float32)
-    m[1, ::5] = 0.25                      # heavy ties in one row
-    m[2] = 3.0                            # all equal (candidate overflow path)
-    lens = rng.integers(1, L + 1, rows).astype(np.int32)
-    lens[0], lens[3] = L, 100             # a full row and a row shorter than k
-    return torch.from_numpy(m).cuda(), torch.from_numpy(lens).cuda()
+    m = rng.standard_normal((rows, n)).astype(np.float32)
+    m[0] = rng.integers(0, 40, n)                  # ties on the k-th key
+    m[1] = 3.0 + seed                              # all equal: the lowest k indices
+    m[2, ::5] = 0.25                               # a tied run inside a normal row
+    lens = np.array([n, n, n - 7, 100, 260_001, n - 2], dtype=np.int32)[:rows]
+    return m, lens
 
 
-def _with_workspace(scores, lens, L, k):
+def _workspace_topk(scores, lens, max_len):
     rows = scores.shape[0]
-    ws = binding.workspace(binding.topk_workspace_size(rows, L, k))
-    out = torch.empty((rows, k), dtype=torch.int32, device="cuda")
+    ws = binding.workspace(binding.topk_workspace_size(rows, max_len, K))
+    out = torch.empty((rows, K), dtype=torch.int32, device="cuda")
     st = torch.zeros(1, dtype=torch.int32, device="cuda")
-    binding.topk(scores, lens, L, k, out, ws, st)
+    binding.topk(scores, lens, max_len, K, out, ws, st)
     torch.cuda.synchronize()
-    assert st.item() == 0
-    return out
+    assert st.item() == 0, binding.status_string(st.item())
+    return out.cpu().numpy()
 
 
-def test_topk_noalloc_matches_workspace_entry_point_on_two_calls():
-    rows, L, k = 48, 20000, 2048
-    for call, seed in enumerate((5, 6)):
-        scores, lens = _inputs(seed, rows, L)
-        want = _with_workspace(scores, lens, L, k)
-        got = torch.full((rows, k), -7, dtype=torch.int32, device="cuda")
-        st = torch.zeros(1, dtype=torch.int32, device="cuda")
-        binding.topk_noalloc(scores, lens, L, k, got, st)
-        torch.cuda.synchronize()
-        assert st.item() == 0, f"call {call}: {binding.status_string(st.item())}"
-        assert torch.equal(got, want), f"call {call}: differs from dsa_topk"
+def _noalloc_topk(scores, lens, max_len):
+    rows = scores.shape[0]
+    out = torch.full((rows, K), -7, dtype=torch.int32, device="cuda")
+    st = torch.zeros(1, dtype=torch.int32, device="cuda")
+    binding.topk_noalloc(scores, lens, max_len, K, out, st)
+    torch.cuda.synchronize()
+    assert st.item() == 0, binding.status_string(st.item())
+    return out.cpu().numpy()
+
+
+def test_topk_noalloc_uses_its_scratch_correctly_on_two_calls():
+    prev = binding.topk_force_multipass(True)
+    try:
+        for call, seed in enumerate((5, 6)):
+            m, lens = _long_rows(seed)
+            scores, d_lens = torch.from_numpy(m).cuda(), torch.from_numpy(lens).cuda()
+            n0 = binding.kernel_launches()
+            got = _noalloc_topk(scores, d_lens, m.shape[1])
+            assert binding.kernel_launches() - n0 == 4, "the four-kernel path (the one with scratch) must run"
+            want = oracle.topk(m.astype(np.float64), lens, K)
+            np.testing.assert_array_equal(got, want, err_msg=f"call {call}: differs from the oracle")
+            np.testing.assert_array_equal(got, _workspace_topk(scores, d_lens, m.shape[1]),
+                                          err_msg=f"call {call}: differs from dsa_topk")
+    finally:
+        binding.topk_force_multipass(prev)
+
+
+def test_topk_noalloc_rows_no_longer_than_k():
+    """Every row fits in k: the entry point still goes through its scratch
+    set-up, and the final kernel writes 0..len-1 with -1 padding."""
+    rng = np.random.default_rng(3)
+    m = rng.standard_normal((5, K)).astype(np.float32)
+    lens = np.array([K, 1, 0, 777, K - 1], dtype=np.int32)
+    got = _noalloc_topk(torch.from_numpy(m).cuda(), torch.from_numpy(lens).cuda(), K)
+    np.testing.assert_array_equal(got, oracle.topk(m.astype(np.float64), lens, K))
 
 
 def test_topk_noalloc_rejects_more_rows_than_its_scratch_holds():
     scores = torch.zeros((65, 4096), dtype=torch.float32, device="cuda")
     lens = torch.full((65,), 4096, dtype=torch.int32, device="cuda")
-    out = torch.empty((65, 2048), dtype=torch.int32, device="cuda")
+    out = torch.empty((65, K), dtype=torch.int32, device="cuda")
     st = torch.zeros(1, dtype=torch.int32, device="cuda")
     with pytest.raises(binding.DsaError) as e:
-        binding.topk_noalloc(scores, lens, 4096, 2048, out, st)
+        binding.topk_noalloc(scores, lens, 4096, K, out, st)
     assert e.value.code == binding.ERR_UNSUPPORTED
