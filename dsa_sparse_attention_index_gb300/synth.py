@@ -345,3 +345,45 @@ def device_case(case: Case, device="cuda") -> DeviceCase:
                           queries_per_seq=case.nq, max_seq_len=max(case.max_len, 0))
     return DeviceCase(cache=cache, batch=batch, q_index=t(case.q_index), head_w=t(case.head_w),
                       q_mla=t(case.q_mla.view(np.int16)), row_lens=t(case.row_lens()))
+
+
+# ---------------------------------------------------------------------------
+# the fused indexer front end's inputs
+# ---------------------------------------------------------------------------
+
+# Width of the compressed query that the indexer front end normalises and
+# projects.  The pages do not give it; 1,536 is the compressed-query width of
+# the DeepSeek-style MLA that DSA comes from.
+QUERY_RANK = 1536
+NORM_EPS = 1e-6
+INDEX_Q_OUT = IDX_HEADS * IDX_DIM   # 4,096 projected query values per row
+
+
+@dataclasses.dataclass
+class FrontendInputs:
+    """One step's inputs to the fused indexer front end, for `rows` query rows:
+    what the packed input projection hands it (the compressed query, the raw
+    head weights, the new token's index key and latent) and the layer's norm
+    and projection weights.  bf16 tensors are stored as their 16-bit patterns."""
+
+    c_q: np.ndarray         # uint16 [rows, D]      compressed query
+    gamma: np.ndarray       # uint16 [D]            RMSNorm weight
+    w_iq: np.ndarray        # uint16 [4096, D]      indexer query projection (row o = head * 128 + dim)
+    head_w: np.ndarray      # float32 [rows, 32]    head weights before the query scale is folded in
+    new_latent: np.ndarray  # uint16 [rows, 576]    the new token's latent
+    new_key: np.ndarray     # uint16 [rows, 128]    the new token's index key
+    eps: float = NORM_EPS
+
+
+def make_frontend(rows: int, dim: int = QUERY_RANK, seed: int = 0) -> FrontendInputs:
+    """Seeded front-end inputs.  Draw order: compressed queries N(0, 1), the
+    norm weight U(0.5, 1.5), the projection N(0, 1/D) (unit-variance outputs),
+    head weights N(0, 0.1), new latents N(0, 1), new index keys N(0, 1)."""
+    rng = np.random.Generator(np.random.PCG64(seed + 2000))
+    c_q = bf16_encode(rng.standard_normal((rows, dim)).astype(np.float32))
+    gamma = bf16_encode(rng.uniform(0.5, 1.5, dim).astype(np.float32))
+    w_iq = bf16_encode((rng.standard_normal((INDEX_Q_OUT, dim)) / math.sqrt(dim)).astype(np.float32))
+    head_w = (rng.standard_normal((rows, IDX_HEADS)) * 0.1).astype(np.float32)
+    new_latent = bf16_encode(rng.standard_normal((rows, LATENT)).astype(np.float32))
+    new_key = bf16_encode(rng.standard_normal((rows, IDX_DIM)).astype(np.float32))
+    return FrontendInputs(c_q=c_q, gamma=gamma, w_iq=w_iq, head_w=head_w, new_latent=new_latent, new_key=new_key)

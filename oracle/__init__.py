@@ -77,6 +77,12 @@ def _load():
             lib.oracle_cache_append.restype = i32
             lib.oracle_quantize_query.argtypes = [P, P, i32, P, P]
             lib.oracle_quantize_query.restype = i32
+            lib.oracle_rms_norm_bf16.argtypes = [P, P, i32, i32, f64, P]
+            lib.oracle_rms_norm_bf16.restype = i32
+            lib.oracle_index_query_proj.argtypes = [P, P, i32, i32, i32, P]
+            lib.oracle_index_query_proj.restype = i32
+            lib.oracle_quantize_query_f32.argtypes = [P, P, i32, P, P]
+            lib.oracle_quantize_query_f32.restype = i32
             _lib = lib
     return _lib
 
@@ -252,6 +258,46 @@ def quantize_query(q_bf16: np.ndarray, head_w: np.ndarray):
     codes = np.empty((rows, IDX_HEADS, IDX_DIM), dtype=np.uint8)
     w_out = np.empty((rows, IDX_HEADS), dtype=np.float32)
     _check(_load().oracle_quantize_query(_ptr(q), _ptr(w), rows, _ptr(codes), _ptr(w_out)), "quantize_query")
+    return codes, w_out
+
+
+def rms_norm_bf16(c_bf16: np.ndarray, gamma_bf16: np.ndarray, eps: float) -> np.ndarray:
+    """The front end's query norm (Day-0 post, fused-decode section: "query
+    norm"; read as RMSNorm with a learned weight): xn = c / sqrt(mean(c^2) +
+    eps) * gamma per row, in fp64, rounded to bf16.  Inputs and result are
+    bf16 bits [rows, D]."""
+    c = np.ascontiguousarray(c_bf16, dtype=np.uint16)
+    g = np.ascontiguousarray(gamma_bf16, dtype=np.uint16)
+    rows, dim = c.shape
+    out = np.empty_like(c)
+    _check(_load().oracle_rms_norm_bf16(_ptr(c), _ptr(g), rows, dim, float(eps), _ptr(out)), "rms_norm_bf16")
+    return out
+
+
+def index_query_proj(xn_bf16: np.ndarray, w_bf16: np.ndarray) -> np.ndarray:
+    """The indexer's query projection (Day-0 post, fused-decode section):
+    q[r, o] = sum_i W[o, i] xn[r, i] in fp64 over bf16 operands, o = head *
+    128 + dim.  xn [rows, D], W [outs, D] bf16 bits; returns float64 [rows, outs]."""
+    xn = np.ascontiguousarray(xn_bf16, dtype=np.uint16)
+    w = np.ascontiguousarray(w_bf16, dtype=np.uint16)
+    rows, dim = xn.shape
+    outs = w.shape[0]
+    assert w.shape[1] == dim
+    q = np.empty((rows, outs), dtype=np.float64)
+    _check(_load().oracle_index_query_proj(_ptr(xn), _ptr(w), rows, dim, outs, _ptr(q)), "index_query_proj")
+    return q
+
+
+def quantize_query_f32(q_f32: np.ndarray, head_w: np.ndarray):
+    """quantize_query from fp32 query values [rows, 32, 128] (the front end's
+    projection accumulates in fp32): codes uint8 [rows, 32, 128] and the
+    head weights times the scales, float32 [rows, 32]."""
+    q = np.ascontiguousarray(q_f32, dtype=np.float32).reshape(-1, IDX_HEADS, IDX_DIM)
+    w = np.ascontiguousarray(head_w, dtype=np.float32)
+    rows = q.shape[0]
+    codes = np.empty((rows, IDX_HEADS, IDX_DIM), dtype=np.uint8)
+    w_out = np.empty((rows, IDX_HEADS), dtype=np.float32)
+    _check(_load().oracle_quantize_query_f32(_ptr(q), _ptr(w), rows, _ptr(codes), _ptr(w_out)), "quantize_query_f32")
     return codes, w_out
 
 

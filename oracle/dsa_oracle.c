@@ -681,3 +681,83 @@ int oracle_quantize_query(const uint16_t* q, const float* w, int32_t rows, uint8
   }
   return ORACLE_OK;
 }
+
+/* ------------------------------------------------------------------ */
+/* Fused indexer front end.                                             */
+/* ------------------------------------------------------------------ */
+/*
+ * [K31] "低延迟解码：融合的 DSA 解码路径", second bullet: one kernel does the
+ * query norm, the indexer's query projection, its FP8 quantisation with the
+ * scale folded into the head weights, and the new token's index key.  The
+ * pages name the steps, not their formulas.  Readings:
+ *   norm        RMSNorm of the row's compressed query c (width D) with a
+ *               learned weight gamma:  xn[i] = c[i] / sqrt(mean_j c[j]^2 + eps)
+ *               * gamma[i], rounded to bf16 (the projection's operand type);
+ *   projection  q[o] = sum_i W[o][i] * xn[i] for the 32 x 128 outputs
+ *               o = h * 128 + d (W: bf16, row-major [4096][D]);
+ *   quantise    per (row, head) as oracle_quantize_query, from the fp32 value
+ *               of q (the projection's accumulator type): s = amax/448,
+ *               codes e4m3(q / s), w_out = w * s, all in single precision;
+ *   index key   written with the new latent by oracle_cache_append.
+ * Norm and projection are in double precision.
+ */
+
+/* fp64 -> nearest bf16 (ties to even), as bf16 bits; values here are far
+   from the bf16 range's end (no overflow handling). */
+static uint16_t bf16_bits_rne(double x) {
+  double r = x;
+  if (isfinite(x) && x != 0.0) {
+    int e;
+    frexp(x, &e);                       /* |x| = m 2^e, m in [0.5, 1) */
+    int qe = e - 8;                     /* bf16 keeps 8 significant bits */
+    if (qe < -133) qe = -133;           /* subnormal spacing 2^-133 */
+    r = rint(ldexp(x, -qe));            /* exact scaling, round half to even */
+    r = ldexp(r, qe);
+  }
+  const float f = (float)r;            /* exact: r is a bf16 value */
+  uint32_t u;
+  memcpy(&u, &f, 4);
+  return (uint16_t)(u >> 16);
+}
+
+int oracle_rms_norm_bf16(const uint16_t* c, const uint16_t* gamma, int32_t rows, int32_t dim, double eps,
+                         uint16_t* xn) {
+  if (!c || !gamma || !xn || rows < 0 || dim < 1 || !(eps >= 0.0)) return ORACLE_BAD_ARG;
+  for (int64_t r = 0; r < rows; ++r) {
+    double ss = 0.0;
+    for (int i = 0; i < dim; ++i) {
+      const double v = oracle_bf16_to_double(c[r * dim + i]);
+      ss += v * v;
+    }
+    const double inv = 1.0 / sqrt(ss / dim + eps);
+    for (int i = 0; i < dim; ++i)
+      xn[r * dim + i] = bf16_bits_rne(oracle_bf16_to_double(c[r * dim + i]) * inv * oracle_bf16_to_double(gamma[i]));
+  }
+  return ORACLE_OK;
+}
+
+int oracle_index_query_proj(const uint16_t* xn, const uint16_t* w, int32_t rows, int32_t dim, int32_t outs,
+                            double* q) {
+  if (!xn || !w || !q || rows < 0 || dim < 1 || outs < 1) return ORACLE_BAD_ARG;
+#pragma omp parallel for collapse(2) schedule(static)
+  for (int64_t r = 0; r < rows; ++r)
+    for (int64_t o = 0; o < outs; ++o) {
+      double acc = 0.0;
+      for (int i = 0; i < dim; ++i)
+        acc += oracle_bf16_to_double(w[o * dim + i]) * oracle_bf16_to_double(xn[r * dim + i]);
+      q[r * outs + o] = acc;
+    }
+  return ORACLE_OK;
+}
+
+/* oracle_quantize_query on fp32 query values */
+int oracle_quantize_query_f32(const float* q, const float* w, int32_t rows, uint8_t* codes, float* w_out) {
+  if (!q || !w || !codes || !w_out || rows < 0) return ORACLE_BAD_ARG;
+  for (int64_t rh = 0; rh < (int64_t)rows * ORACLE_IDX_HEADS; ++rh) {
+    const float* x = q + rh * ORACLE_IDX_DIM;
+    const float s = fp8_scale(x, ORACLE_IDX_DIM);
+    for (int d = 0; d < ORACLE_IDX_DIM; ++d) codes[rh * ORACLE_IDX_DIM + d] = oracle_e4m3_encode((double)(x[d] / s));
+    w_out[rh] = w[rh] * s;
+  }
+  return ORACLE_OK;
+}

@@ -688,3 +688,87 @@ def test_cache_append_nvfp4_agrees_with_the_input_generator():
     rec = pool[r, case.latent_off + (t % 64) * 352:case.latent_off + (t % 64 + 1) * 352]
     want = synth.nvfp4_latent_encode(_bf16_value(lat_b), case.latent_scale)[0]
     np.testing.assert_array_equal(rec, want)
+
+
+# ---------------------------------------------------------------- fused indexer front end
+def _bf16_from_f64_torch(x):
+    """bf16 bits of fp64 values through torch's float64 -> bfloat16 rounding."""
+    return torch.from_numpy(np.ascontiguousarray(x, dtype=np.float64)).to(torch.bfloat16).view(torch.int16).numpy().view(np.uint16)
+
+
+def test_rms_norm_matches_the_definition_through_torch():
+    """xn = c / sqrt(mean(c^2) + eps) * gamma in fp64, rounded to bf16: the
+    same values through torch's fp64 arithmetic and its bf16 rounding."""
+    fe = synth.make_frontend(7, dim=256, seed=3)
+    got = oracle.rms_norm_bf16(fe.c_q, fe.gamma, fe.eps)
+    c = _bf16_value(fe.c_q).astype(np.float64)
+    g = _bf16_value(fe.gamma).astype(np.float64)
+    ct = torch.from_numpy(c)
+    ref = ct / torch.sqrt((ct * ct).mean(dim=1, keepdim=True) + fe.eps) * torch.from_numpy(g)
+    np.testing.assert_array_equal(got, _bf16_from_f64_torch(ref.numpy()))
+
+
+def test_rms_norm_closed_forms():
+    """A constant row a gives gamma * a / sqrt(a^2 + eps); eps = 0 makes the
+    norm scale-invariant (rows c and 4c give the same xn); the sign of c
+    carries through; gamma = 1, eps = 0 on a row of +-1 returns the row."""
+    D = 64
+    gamma = _bf16_bits(np.linspace(0.5, 1.5, D).astype(np.float32))
+    g = _bf16_value(gamma).astype(np.float64)
+    c = _bf16_bits(np.full((1, D), 3.0, dtype=np.float32))
+    got = _bf16_value(oracle.rms_norm_bf16(c, gamma, 1e-6)[0]).astype(np.float64)
+    want = _bf16_value(_bf16_from_f64_torch(g * 3.0 / math.sqrt(9.0 + 1e-6))).astype(np.float64)
+    np.testing.assert_array_equal(got, want)
+    rng = np.random.default_rng(5)
+    x = rng.standard_normal((2, D)).astype(np.float32)
+    c2 = _bf16_bits(np.stack([x[0], 4.0 * x[0], -x[1]]))
+    out = oracle.rms_norm_bf16(c2, gamma, 0.0)
+    np.testing.assert_array_equal(out[0], out[1])
+    signs = np.sign(_bf16_value(out[2])) == np.sign(_bf16_value(c2[2]))   # gamma > 0: xn keeps c's sign
+    assert signs[_bf16_value(c2[2]) != 0].all()
+    ones = _bf16_bits(np.where(rng.random((1, D)) < 0.5, -1.0, 1.0).astype(np.float32))
+    unit = _bf16_bits(np.ones(D, dtype=np.float32))
+    np.testing.assert_array_equal(oracle.rms_norm_bf16(ones, unit, 0.0), ones)
+
+
+def test_index_query_projection_exact_integers_and_one_hot_rows():
+    """Small-integer operands make every dot product an exact integer (Python
+    ints); a one-hot weight row copies one input; a row scaled by -2 flips the
+    sign and doubles; against torch's fp64 matmul on random bf16 operands."""
+    rng = np.random.default_rng(11)
+    rows, D, outs = 3, 96, 40
+    xi = rng.integers(-8, 9, (rows, D))
+    wi = rng.integers(-8, 9, (outs, D))
+    wi[5] = 0
+    wi[5, 17] = 1                                          # one-hot: q[:, 5] = x[:, 17]
+    wi[6] = -2 * wi[7]
+    q = oracle.index_query_proj(_bf16_bits(xi.astype(np.float32)), _bf16_bits(wi.astype(np.float32)))
+    want = [[sum(int(a) * int(b) for a, b in zip(xi[r], wi[o])) for o in range(outs)] for r in range(rows)]
+    np.testing.assert_array_equal(q, np.array(want, dtype=np.float64))
+    np.testing.assert_array_equal(q[:, 5], xi[:, 17].astype(np.float64))
+    np.testing.assert_array_equal(q[:, 6], -2 * q[:, 7])
+    fe = synth.make_frontend(4, dim=512, seed=9)
+    xn = oracle.rms_norm_bf16(fe.c_q, fe.gamma, fe.eps)
+    w = fe.w_iq[:200]
+    got = oracle.index_query_proj(xn, w)
+    ref = torch.from_numpy(_bf16_value(xn).astype(np.float64)) @ torch.from_numpy(_bf16_value(w).astype(np.float64)).T
+    np.testing.assert_allclose(got, ref.numpy(), rtol=1e-12, atol=1e-12)
+
+
+def test_quantize_query_f32_folds_the_scale():
+    """From fp32 query values: s = amax / 448 in fp32, codes = torch's E4M3 of
+    q / s (fp32), w_out = w * s; an all-zero head takes s = 1; the bf16 entry
+    point agrees on bf16-valued inputs."""
+    rng = np.random.default_rng(13)
+    q = (rng.standard_normal((4, 32, 128)) * np.exp(rng.uniform(-5, 5, (4, 32, 1)))).astype(np.float32)
+    q[1, 2] = 0.0
+    q[2, 3, :2] = [-0.0, 3.0e38]
+    w = rng.standard_normal((4, 32)).astype(np.float32)
+    codes, w_out = oracle.quantize_query_f32(q, w)
+    amax = np.abs(q).max(axis=2)
+    s = np.where(amax > 0, amax / np.float32(448.0), np.float32(1.0)).astype(np.float32)
+    np.testing.assert_array_equal(codes, _torch_e4m3(q / s[..., None]))
+    np.testing.assert_array_equal(w_out, (w * s).astype(np.float32))
+    assert (codes[1, 2] == 0).all() and w_out[1, 2] == w[1, 2]
+    qb = _bf16_bits(q)
+    np.testing.assert_array_equal(oracle.quantize_query_f32(_bf16_value(qb), w)[0], oracle.quantize_query(qb, w)[0])
