@@ -52,6 +52,7 @@ EXPORTS = ["dsa_api_version", "dsa_status_string", "dsa_last_cuda_error", "dsa_k
            "dsa_dcp_topk_workspace_size", "dsa_dcp_topk", "sparse_mla_workspace_size",
            "sparse_mla_decode", "dsa_dcp_sparse_mla_workspace_size", "dsa_dcp_sparse_mla", "dsa_batch_invariant",
            "dsa_workspace_size", "dsa_decode_step", "dsa_cache_append", "dsa_quantize_index_query",
+           "dsa_index_frontend", "dsa_frontend_workspace_size", "dsa_decode_step_frontend",
            "dsa_selftest_wait_timeout"]
 
 
@@ -90,6 +91,10 @@ def lib():
             "dsa_topk_bf16": (i32, [P, i64, P, i32, i32, i32, P, P, P]),
             "dsa_cache_append": (i32, [pc, pb, P, P, P, P]),
             "dsa_quantize_index_query": (i32, [P, P, i32, P, P, P]),
+            "dsa_index_frontend": (i32, [pc, pb, P, i32, P, f32, P, P, P, P, P, P, P, P, P]),
+            "dsa_frontend_workspace_size": (sz, [pb, i32]),
+            "dsa_decode_step_frontend": (i32, [pc, pb, P, i32, P, f32, P, P, P, P, P, i32, f32, P, P, P, i64, P, P,
+                                               sz, P, P]),
             "dsa_selftest_wait_timeout": (i32, [i64, P, P]),
         }
         for name, (res, args) in sig.items():
@@ -307,6 +312,38 @@ def quantize_index_query(q_bf16, head_w, q_index, head_w_out, stream=None):
     rows = int(q_bf16.shape[0])
     _check(lib().dsa_quantize_index_query(_ptr(q_bf16), _ptr(head_w), rows, _ptr(q_index), _ptr(head_w_out),
                                           _stream(stream)), "dsa_quantize_index_query")
+
+
+def index_frontend(cache: PagedCache, batch: Batch, c_q, gamma, eps: float, w_iq, head_w, new_latent, new_index_key,
+                   q_index, head_w_out, status, q_proj=None, stream=None):
+    """The fused indexer front end: RMSNorm of c_q (bf16 bits [rows, D]), the
+    projection by w_iq (bf16 bits [4096, D]), the FP8 query (q_index [rows, 32,
+    128]) with its scale folded into head_w_out, optionally the fp32 projected
+    values (q_proj [rows, 4096]), and the new tokens into the cache."""
+    c, b = cache.struct(), batch.struct()
+    _check(lib().dsa_index_frontend(ctypes.byref(c), ctypes.byref(b), _ptr(c_q), int(c_q.shape[1]), _ptr(gamma),
+                                    float(eps), _ptr(w_iq), _ptr(head_w), _ptr(new_latent), _ptr(new_index_key),
+                                    _ptr(q_index), _ptr(head_w_out), _ptr(q_proj), _ptr(status), _stream(stream)),
+           "dsa_index_frontend")
+
+
+def frontend_workspace_size(batch: Batch, k: int) -> int:
+    b = batch.struct()
+    return int(lib().dsa_frontend_workspace_size(ctypes.byref(b), int(k)))
+
+
+def decode_step_frontend(cache: PagedCache, batch: Batch, c_q, gamma, eps: float, w_iq, head_w, new_latent,
+                         new_index_key, q_mla, k: int, sm_scale: float, out, lse, workspace, status, scores_out=None,
+                         idx_out=None, stream=None):
+    """The front end, then the fused step over the updated cache (one call)."""
+    c, b = cache.struct(), batch.struct()
+    ld = int(scores_out.shape[1]) if scores_out is not None else 0
+    _check(lib().dsa_decode_step_frontend(ctypes.byref(c), ctypes.byref(b), _ptr(c_q), int(c_q.shape[1]), _ptr(gamma),
+                                          float(eps), _ptr(w_iq), _ptr(head_w), _ptr(new_latent),
+                                          _ptr(new_index_key), _ptr(q_mla), int(k), float(sm_scale), _ptr(out),
+                                          _ptr(lse), _ptr(scores_out), ld, _ptr(idx_out), _ptr(workspace),
+                                          workspace.numel() * workspace.element_size(), _ptr(status),
+                                          _stream(stream)), "dsa_decode_step_frontend")
 
 
 def selftest_wait_timeout(limit_ns: int, status, stream=None):

@@ -392,6 +392,77 @@ dsa_status_t dsa_quantize_index_query(const uint16_t* q_bf16, const float* head_
   return launch_quantize_query(q_bf16, head_w, rows, q_index, head_w_out, static_cast<cudaStream_t>(stream));
 }
 
+namespace {
+dsa_status_t check_frontend(const uint16_t* c_q, int32_t q_rank, const uint16_t* gamma, float eps,
+                            const uint16_t* w_iq, const float* head_w, const uint16_t* new_latent,
+                            const uint16_t* new_index_key) {
+  if (q_rank % 64 || q_rank < 64 || q_rank > 16384) return DSA_ERR_UNSUPPORTED;
+  if (!c_q || !gamma || !w_iq || !head_w || !new_latent || !new_index_key || !(eps >= 0.f)) return DSA_ERR_INVALID_ARG;
+  if (!aligned(c_q, 16) || !aligned(gamma, 16) || !aligned(w_iq, 16) || !aligned(head_w, 4) || !aligned(new_latent, 2) ||
+      !aligned(new_index_key, 2))
+    return DSA_ERR_INVALID_ARG;
+  return DSA_OK;
+}
+}  // namespace
+
+dsa_status_t dsa_index_frontend(const dsa_paged_cache_t* cache, const dsa_batch_t* batch, const uint16_t* c_q,
+                                int32_t q_rank, const uint16_t* gamma, float eps, const uint16_t* w_iq,
+                                const float* head_w, const uint16_t* new_latent, const uint16_t* new_index_key,
+                                uint8_t* q_index, float* head_w_out, float* q_proj, int32_t* dev_status,
+                                void* stream) {
+  dsa_status_t s;
+  if ((s = check_cache(cache)) != DSA_OK) return s;
+  if ((s = check_batch(batch)) != DSA_OK) return s;
+  if (!dev_status) return DSA_ERR_INVALID_ARG;
+  if (batch->batch == 0) return DSA_OK;
+  if ((s = check_frontend(c_q, q_rank, gamma, eps, w_iq, head_w, new_latent, new_index_key)) != DSA_OK) return s;
+  if (!q_index || !head_w_out || !aligned(head_w_out, 4) || (q_proj && !aligned(q_proj, 4))) return DSA_ERR_INVALID_ARG;
+  return launch_frontend(*cache, *batch, c_q, q_rank, gamma, eps, w_iq, head_w, new_latent, new_index_key, q_index,
+                         head_w_out, q_proj, dev_status, static_cast<cudaStream_t>(stream));
+}
+
+size_t dsa_frontend_workspace_size(const dsa_batch_t* batch, int32_t k) {
+  const size_t step = dsa_workspace_size(batch, k);
+  if (!step) return 0;
+  const size_t rows = (size_t)batch->batch * std::max(1, batch->queries_per_seq);
+  return al256(rows * kIdxHeads * kIdxDim) + al256(rows * kIdxHeads * 4) + step;
+}
+
+dsa_status_t dsa_decode_step_frontend(const dsa_paged_cache_t* cache, const dsa_batch_t* batch,
+                                      const uint16_t* c_q, int32_t q_rank, const uint16_t* gamma, float eps,
+                                      const uint16_t* w_iq, const float* head_w, const uint16_t* new_latent,
+                                      const uint16_t* new_index_key, const uint16_t* q_mla, int32_t k,
+                                      float sm_scale, uint16_t* out, float* lse, float* scores_out,
+                                      int64_t ld_scores, int32_t* idx_out, void* workspace, size_t workspace_bytes,
+                                      int32_t* dev_status, void* stream) {
+  dsa_status_t s;
+  if ((s = check_cache(cache)) != DSA_OK) return s;
+  if ((s = check_batch(batch)) != DSA_OK) return s;
+  if ((s = check_index_rows(cache, batch)) != DSA_OK) return s;
+  if (k < 1 || k > DSA_MAX_TOPK || !dev_status) return DSA_ERR_INVALID_ARG;
+  if (batch->batch == 0) return DSA_OK;
+  if ((s = check_frontend(c_q, q_rank, gamma, eps, w_iq, head_w, new_latent, new_index_key)) != DSA_OK) return s;
+  if (!workspace || !aligned(workspace, 256) || workspace_bytes < dsa_frontend_workspace_size(batch, k))
+    return DSA_ERR_WORKSPACE;
+  const size_t rows = (size_t)batch->batch * batch->queries_per_seq;
+  uint8_t* w = static_cast<uint8_t*>(workspace);
+  uint8_t* q_index = w;
+  w += al256(rows * kIdxHeads * kIdxDim);
+  float* head_w_out = reinterpret_cast<float*>(w);
+  w += al256(rows * kIdxHeads * 4);
+  // validate the step's own arguments before the front end writes the cache
+  if (!q_mla || !out || !lse || !aligned(q_mla, 16) || !aligned(out, 8)) return DSA_ERR_INVALID_ARG;
+  if (scores_out && (!aligned(scores_out, 16) || ld_scores < batch->max_seq_len || (ld_scores % 4)))
+    return DSA_ERR_INVALID_ARG;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  if ((s = launch_frontend(*cache, *batch, c_q, q_rank, gamma, eps, w_iq, head_w, new_latent, new_index_key, q_index,
+                           head_w_out, nullptr, dev_status, st)) != DSA_OK)
+    return s;
+  return dsa_decode_step(cache, batch, q_index, head_w_out, q_mla, k, sm_scale, out, lse, scores_out, ld_scores,
+                         idx_out, w, workspace_bytes - (size_t)(w - static_cast<uint8_t*>(workspace)), dev_status,
+                         stream);
+}
+
 dsa_status_t dsa_selftest_wait_timeout(int64_t limit_ns, int32_t* dev_status, void* stream) {
   if (!dev_status) return DSA_ERR_INVALID_ARG;
   return launch_wait_selftest(limit_ns, dev_status, static_cast<cudaStream_t>(stream));

@@ -78,6 +78,13 @@ dsa_status_t launch_sparse_mla(const dsa_paged_cache_t& c, const dsa_batch_t& bt
 dsa_status_t launch_wait_selftest(int64_t limit_ns, int32_t* status, cudaStream_t st);
 dsa_status_t launch_cache_append(const dsa_paged_cache_t& c, const dsa_batch_t& bt, const uint16_t* new_latent,
                                  const uint16_t* new_key, int32_t* status, cudaStream_t st);
+// The fused indexer front end: RMSNorm of c_q [rows][dim], the projection by
+// w_iq [4096][dim] (bf16), FP8 query codes and folded head weights, optional
+// fp32 projected values, and the new tokens into the cache; one launch.
+dsa_status_t launch_frontend(const dsa_paged_cache_t& c, const dsa_batch_t& bt, const uint16_t* c_q, int dim,
+                             const uint16_t* gamma, float eps, const uint16_t* w_iq, const float* head_w,
+                             const uint16_t* new_latent, const uint16_t* new_key, uint8_t* q_index, float* head_w_out,
+                             float* q_proj, int32_t* status, cudaStream_t st);
 dsa_status_t launch_quantize_query(const uint16_t* q, const float* w, int rows, uint8_t* codes, float* w_out,
                                    cudaStream_t st);
 

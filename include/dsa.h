@@ -24,6 +24,9 @@
  *   sparse_mla_decode        exact sparse MLA over the selected tokens
  *   dsa_decode_step(_bf16)   the three stages fused on one stream
  *   dsa_cache_append, dsa_quantize_index_query   the step's front end
+ *   dsa_index_frontend       the fused indexer front end (norm, projection,
+ *                            FP8 query, new tokens into the cache)
+ *   dsa_decode_step_frontend the front end and the fused step, one call
  *   dsa_dcp_topk, dsa_dcp_sparse_mla   decode context parallelism (top-k
  *                            merge, partial attention + LSE combine) of W
  *                            token shards, emulated on one GPU
@@ -406,6 +409,57 @@ dsa_status_t dsa_cache_append(const dsa_paged_cache_t* cache, const dsa_batch_t*
  */
 dsa_status_t dsa_quantize_index_query(const uint16_t* q_bf16, const float* head_w, int32_t rows,
                                       uint8_t* q_index, float* head_w_out, void* stream);
+
+/*
+ * The fused indexer front end (Day-0 post, fused-decode section, second
+ * bullet: the query norm, the indexer's query projection, its FP8
+ * quantisation folded into the head weights, and the new token's index key,
+ * in one kernel).  For every row r = b * queries_per_seq + j of the batch:
+ *   xn[r][i]     = bf16( c_q[r][i] * (1 / sqrt(mean_i c_q[r][i]^2 + eps)) * gamma[i] )
+ *                  (RMSNorm in fp32, the product rounded to bf16; the post
+ *                  names a "query norm", read as RMSNorm)
+ *   q[r][o]      = sum_i w_iq[o][i] * xn[r][i]   for o = h * 128 + d (bf16
+ *                  operands, fp32 accumulation)
+ *   q_index[r][h][d], head_w_out[r][h]   as dsa_quantize_index_query, from the
+ *                  fp32 q: s = amax_d |q| / 448, codes e4m3(q / s), head_w * s
+ *   the row's new token written to the cache exactly as dsa_cache_append does
+ *                  (new_latent[r], new_index_key[r])
+ * One launch; tcgen05 does the projection.
+ *   c_q         device bf16 bits [rows][q_rank], 16-B aligned
+ *   q_rank      the compressed query's width D: a multiple of 64, 64 .. 16384,
+ *               else DSA_ERR_UNSUPPORTED
+ *   gamma       device bf16 bits [q_rank], 16-B aligned;  eps >= 0
+ *   w_iq        device bf16 bits [4096][q_rank] (row o = h * 128 + d), 16-B aligned
+ *   head_w      device fp32 [rows][32], the head weights before the scale is folded in
+ *   new_latent, new_index_key   as for dsa_cache_append
+ *   q_index     device [rows][32][128] E4M3 codes;  head_w_out device fp32 [rows][32]
+ *   q_proj      device fp32 [rows][4096] or NULL: the projected q (for checks)
+ * A block-table entry outside the pool raises DSA_ERR_BOUNDS in *dev_status.
+ */
+dsa_status_t dsa_index_frontend(const dsa_paged_cache_t* cache, const dsa_batch_t* batch, const uint16_t* c_q,
+                                int32_t q_rank, const uint16_t* gamma, float eps, const uint16_t* w_iq,
+                                const float* head_w, const uint16_t* new_latent, const uint16_t* new_index_key,
+                                uint8_t* q_index, float* head_w_out, float* q_proj, int32_t* dev_status,
+                                void* stream);
+
+/*
+ * A decode step that owns its cache update: dsa_index_frontend (the new
+ * tokens into the cache, the indexer query from the compressed query) and
+ * then dsa_decode_step over the updated cache, on one stream with no host
+ * synchronisation (Day-0 post, fused-decode section: the front end, then the
+ * fused indexer and the sparse attention).  The FP8 query and folded head
+ * weights live in the workspace.  Arguments as for the two calls; the step's
+ * optional outputs as for dsa_decode_step.
+ *   workspace >= dsa_frontend_workspace_size(batch, k) bytes, 256-B aligned
+ */
+size_t dsa_frontend_workspace_size(const dsa_batch_t* batch, int32_t k);
+dsa_status_t dsa_decode_step_frontend(const dsa_paged_cache_t* cache, const dsa_batch_t* batch,
+                                      const uint16_t* c_q, int32_t q_rank, const uint16_t* gamma, float eps,
+                                      const uint16_t* w_iq, const float* head_w, const uint16_t* new_latent,
+                                      const uint16_t* new_index_key, const uint16_t* q_mla, int32_t k,
+                                      float sm_scale, uint16_t* out, float* lse, float* scores_out,
+                                      int64_t ld_scores, int32_t* idx_out, void* workspace, size_t workspace_bytes,
+                                      int32_t* dev_status, void* stream);
 
 /*
  * Self-test of the bounded in-kernel wait used by every pipelined kernel:

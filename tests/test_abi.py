@@ -145,3 +145,27 @@ def test_oracle_and_product_share_no_code():
             src = open(os.path.join(ROOT, "oracle", f)).read()
             assert not re.search(r"^\s*(import|from)\s+dsa_sparse_attention_index_gb300\b", src, flags=re.M), f
             assert not re.search(r'#include\s+[<"][^>"]*(csrc|dsa\.h|common\.cuh)', src), f
+
+
+def test_frontend_host_validation_without_device(lib):
+    """The fused front end refuses a compressed-query width that is not a
+    multiple of 64 (DSA_ERR_UNSUPPORTED) and missing or misaligned buffers
+    (DSA_ERR_INVALID_ARG) before any launch; the step variant checks its
+    workspace the same way."""
+    B = binding
+    c = B.PagedCacheT(128 * 1000, 45312, 0, 36864, 64, 10, 0, 1.0)
+    b = B.BatchT(128 * 2000, 128 * 3000, 4, 1, 1, 100)
+    st = 128 * 4000
+    fake = 128 * 5000
+    args = lambda rank, cq=fake, g=fake, eps=1e-6: (ctypes.byref(c), ctypes.byref(b), cq, rank, g, eps, fake, fake,
+                                                     fake, fake, fake, fake, None, st, None)
+    assert lib.dsa_index_frontend(*args(1000)) == B.ERR_UNSUPPORTED
+    assert lib.dsa_index_frontend(*args(0)) == B.ERR_UNSUPPORTED
+    assert lib.dsa_index_frontend(*args(1536, cq=None)) == B.ERR_INVALID_ARG
+    assert lib.dsa_index_frontend(*args(1536, g=fake + 2)) == B.ERR_INVALID_ARG   # gamma not 16-B aligned
+    assert lib.dsa_index_frontend(*args(1536, eps=-1.0)) == B.ERR_INVALID_ARG
+    need = lib.dsa_frontend_workspace_size(ctypes.byref(b), 2048)
+    assert need >= lib.dsa_workspace_size(ctypes.byref(b), 2048) + 4096
+    assert lib.dsa_decode_step_frontend(ctypes.byref(c), ctypes.byref(b), fake, 1536, fake, 1e-6, fake, fake, fake,
+                                        fake, fake, 2048, 1.0, fake, fake, None, 0, None, fake, need - 1, st,
+                                        None) == B.ERR_WORKSPACE
