@@ -48,7 +48,7 @@ _lib = None
 EXPORTS = ["dsa_api_version", "dsa_status_string", "dsa_last_cuda_error", "dsa_kernel_launches",
            "dsa_translate_pages", "dsa_index_scores", "dsa_index_scores_bf16", "dsa_topk_bf16",
            "dsa_decode_step_bf16",
-           "dsa_topk_workspace_size", "dsa_topk", "dsa_topk_noalloc", "dsa_topk_force_multipass",
+           "dsa_topk_workspace_size", "dsa_topk", "dsa_topk_noalloc", "dsa_topk_force_multipass", "dsa_topk_paged",
            "dsa_dcp_topk_workspace_size", "dsa_dcp_topk", "sparse_mla_workspace_size",
            "sparse_mla_decode", "dsa_dcp_sparse_mla_workspace_size", "dsa_dcp_sparse_mla", "dsa_batch_invariant",
            "dsa_workspace_size", "dsa_decode_step", "dsa_cache_append", "dsa_quantize_index_query",
@@ -85,8 +85,9 @@ def lib():
             "dsa_batch_invariant": (i32, [i32]),
             "dsa_dcp_sparse_mla": (i32, [pc, pb, P, P, i32, i32, f32, P, P, P, P, P, sz, P, P]),
             "dsa_workspace_size": (sz, [pb, i32]),
-            "dsa_decode_step": (i32, [pc, pb, P, P, P, i32, f32, P, P, P, i64, P, P, sz, P, P]),
-            "dsa_decode_step_bf16": (i32, [pc, pb, P, P, P, i32, f32, P, P, P, i64, P, P, sz, P, P]),
+            "dsa_decode_step": (i32, [pc, pb, P, P, P, i32, f32, P, P, P, i64, P, P, P, sz, P, P]),
+            "dsa_decode_step_bf16": (i32, [pc, pb, P, P, P, i32, f32, P, P, P, i64, P, P, P, sz, P, P]),
+            "dsa_topk_paged": (i32, [pc, pb, P, i64, i32, P, P, P, sz, P, P]),
             "dsa_index_scores_bf16": (i32, [pc, pb, P, P, P, i64, P, P]),
             "dsa_topk_bf16": (i32, [P, i64, P, i32, i32, i32, P, P, P]),
             "dsa_cache_append": (i32, [pc, pb, P, P, P, P]),
@@ -94,7 +95,7 @@ def lib():
             "dsa_index_frontend": (i32, [pc, pb, P, i32, P, f32, P, P, P, P, P, P, P, P, P]),
             "dsa_frontend_workspace_size": (sz, [pb, i32]),
             "dsa_decode_step_frontend": (i32, [pc, pb, P, i32, P, f32, P, P, P, P, P, i32, f32, P, P, P, i64, P, P,
-                                               sz, P, P]),
+                                               P, sz, P, P]),
             "dsa_selftest_wait_timeout": (i32, [i64, P, P]),
         }
         for name, (res, args) in sig.items():
@@ -279,24 +280,37 @@ def workspace_size(batch: Batch, k: int) -> int:
 
 
 def decode_step(cache: PagedCache, batch: Batch, q_index, head_w, q_mla, k: int, sm_scale: float, out, lse,
-                workspace, status, scores_out=None, idx_out=None, stream=None):
+                workspace, status, scores_out=None, idx_out=None, stream=None, phys_out=None):
     c, b = cache.struct(), batch.struct()
     ld = int(scores_out.shape[1]) if scores_out is not None else 0
     _check(lib().dsa_decode_step(ctypes.byref(c), ctypes.byref(b), _ptr(q_index), _ptr(head_w), _ptr(q_mla),
                                  int(k), float(sm_scale), _ptr(out), _ptr(lse), _ptr(scores_out), ld,
-                                 _ptr(idx_out), _ptr(workspace), workspace.numel() * workspace.element_size(),
-                                 _ptr(status), _stream(stream)), "dsa_decode_step")
+                                 _ptr(idx_out), _ptr(phys_out), _ptr(workspace),
+                                 workspace.numel() * workspace.element_size(), _ptr(status), _stream(stream)),
+           "dsa_decode_step")
+
+
+def topk_paged(cache: PagedCache, batch: Batch, scores, k: int, idx_out, workspace, status, phys_out=None,
+               stream=None):
+    """The fused step's top-k on its own (row lengths from the batch), with the
+    selected tokens' physical KV rows when phys_out is given."""
+    c, b = cache.struct(), batch.struct()
+    nbytes = workspace.numel() * workspace.element_size() if workspace is not None else 0
+    _check(lib().dsa_topk_paged(ctypes.byref(c), ctypes.byref(b), _ptr(scores), int(scores.shape[1]), int(k),
+                                _ptr(idx_out), _ptr(phys_out), _ptr(workspace), nbytes, _ptr(status),
+                                _stream(stream)), "dsa_topk_paged")
 
 
 def decode_step_bf16(cache: PagedCache, batch: Batch, q_index, head_w, q_mla, k: int, sm_scale: float, out, lse,
-                     workspace, status, scores_out=None, idx_out=None, stream=None):
+                     workspace, status, scores_out=None, idx_out=None, stream=None, phys_out=None):
     """The fused step with bf16 scores between the indexer and the top-k."""
     c, b = cache.struct(), batch.struct()
     ld = int(scores_out.shape[1]) if scores_out is not None else 0
     _check(lib().dsa_decode_step_bf16(ctypes.byref(c), ctypes.byref(b), _ptr(q_index), _ptr(head_w), _ptr(q_mla),
                                       int(k), float(sm_scale), _ptr(out), _ptr(lse), _ptr(scores_out), ld,
-                                      _ptr(idx_out), _ptr(workspace), workspace.numel() * workspace.element_size(),
-                                      _ptr(status), _stream(stream)), "dsa_decode_step_bf16")
+                                      _ptr(idx_out), _ptr(phys_out), _ptr(workspace),
+                                      workspace.numel() * workspace.element_size(), _ptr(status), _stream(stream)),
+           "dsa_decode_step_bf16")
 
 
 def cache_append(cache: PagedCache, batch: Batch, new_latent, new_index_key, status, stream=None):
@@ -334,14 +348,15 @@ def frontend_workspace_size(batch: Batch, k: int) -> int:
 
 def decode_step_frontend(cache: PagedCache, batch: Batch, c_q, gamma, eps: float, w_iq, head_w, new_latent,
                          new_index_key, q_mla, k: int, sm_scale: float, out, lse, workspace, status, scores_out=None,
-                         idx_out=None, stream=None):
+                         idx_out=None, stream=None, phys_out=None):
     """The front end, then the fused step over the updated cache (one call)."""
     c, b = cache.struct(), batch.struct()
     ld = int(scores_out.shape[1]) if scores_out is not None else 0
     _check(lib().dsa_decode_step_frontend(ctypes.byref(c), ctypes.byref(b), _ptr(c_q), int(c_q.shape[1]), _ptr(gamma),
                                           float(eps), _ptr(w_iq), _ptr(head_w), _ptr(new_latent),
                                           _ptr(new_index_key), _ptr(q_mla), int(k), float(sm_scale), _ptr(out),
-                                          _ptr(lse), _ptr(scores_out), ld, _ptr(idx_out), _ptr(workspace),
+                                          _ptr(lse), _ptr(scores_out), ld, _ptr(idx_out), _ptr(phys_out),
+                                          _ptr(workspace),
                                           workspace.numel() * workspace.element_size(), _ptr(status),
                                           _stream(stream)), "dsa_decode_step_frontend")
 

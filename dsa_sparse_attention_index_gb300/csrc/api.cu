@@ -298,7 +298,7 @@ dsa_status_t sparse_mla_decode(const dsa_paged_cache_t* cache, const dsa_batch_t
 size_t dsa_workspace_size(const dsa_batch_t* batch, int32_t k) {
   if (!batch || batch->batch < 0 || k < 1 || k > DSA_MAX_TOPK) return 0;
   const int rows = batch->batch * std::max(1, batch->queries_per_seq);
-  return al256((size_t)rows * round_ld(batch->max_seq_len) * 4) + al256((size_t)rows * k * 4) +
+  return al256((size_t)rows * round_ld(batch->max_seq_len) * 4) + 2 * al256((size_t)rows * k * 4) +
          al256(topk_workspace_bytes(rows, batch->max_seq_len, k)) + al256(mla_workspace_bytes(rows, k));
 }
 
@@ -307,7 +307,8 @@ namespace {
 dsa_status_t decode_step_impl(const dsa_paged_cache_t* cache, const dsa_batch_t* batch, const uint8_t* q_index,
                               const float* head_w, const uint16_t* q_mla, int32_t k, float sm_scale, uint16_t* out,
                               float* lse, void* scores_out, bool bf16, int64_t ld_scores, int32_t* idx_out,
-                              void* workspace, size_t workspace_bytes, int32_t* dev_status, void* stream) {
+                              int32_t* phys_out, void* workspace, size_t workspace_bytes, int32_t* dev_status,
+                              void* stream) {
   dsa_status_t s;
   if ((s = check_cache(cache)) != DSA_OK) return s;
   if ((s = check_batch(batch)) != DSA_OK) return s;
@@ -334,6 +335,9 @@ dsa_status_t decode_step_impl(const dsa_paged_cache_t* cache, const dsa_batch_t*
   w += scores_bytes;
   int32_t* idx = idx_out ? idx_out : reinterpret_cast<int32_t*>(w);
   w += al256((size_t)rows * k * 4);
+  // the selected tokens' physical KV rows: written by the top-k, read by the MLA
+  int32_t* phys = phys_out ? phys_out : reinterpret_cast<int32_t*>(w);
+  w += al256((size_t)rows * k * 4);
   void* topk_ws = w;
   w += al256(topk_workspace_bytes(rows, batch->max_seq_len, k));
   void* mla_ws = w;
@@ -341,33 +345,61 @@ dsa_status_t decode_step_impl(const dsa_paged_cache_t* cache, const dsa_batch_t*
   if ((s = launch_index_scores(*cache, *batch, q_index, head_w, scores, bf16, ld, dev_status, st)) != DSA_OK)
     return s;
   const int cap = std::min(batch->max_blocks_per_seq * kBlock, batch->max_seq_len);
+  TopkPhys po;
+  po.phys = phys;
+  po.block_table = batch->block_table;
+  po.max_blocks = batch->max_blocks_per_seq;
+  po.num_blocks = cache->num_blocks;
   if (bf16)
     s = launch_topk_bf16(static_cast<const uint16_t*>(scores), ld, nullptr, batch->seq_lens,
-                         batch->queries_per_seq, rows, cap, k, idx, dev_status, st);
+                         batch->queries_per_seq, rows, cap, k, idx, dev_status, st, po);
   else
     s = launch_topk(static_cast<const float*>(scores), ld, nullptr, batch->seq_lens, batch->queries_per_seq, rows,
-                    cap, k, idx, topk_ws, dev_status, st);
+                    cap, k, idx, topk_ws, dev_status, st, po);
   if (s != DSA_OK) return s;
-  return launch_sparse_mla(*cache, *batch, q_mla, idx, k, sm_scale, out, lse, mla_ws, dev_status, st);
+  return launch_sparse_mla(*cache, *batch, q_mla, idx, k, sm_scale, out, lse, mla_ws, dev_status, st, phys);
 }
 
 }  // namespace
 
 dsa_status_t dsa_decode_step(const dsa_paged_cache_t* cache, const dsa_batch_t* batch, const uint8_t* q_index,
                              const float* head_w, const uint16_t* q_mla, int32_t k, float sm_scale, uint16_t* out,
-                             float* lse, float* scores_out, int64_t ld_scores, int32_t* idx_out, void* workspace,
-                             size_t workspace_bytes, int32_t* dev_status, void* stream) {
+                             float* lse, float* scores_out, int64_t ld_scores, int32_t* idx_out, int32_t* phys_out,
+                             void* workspace, size_t workspace_bytes, int32_t* dev_status, void* stream) {
   return decode_step_impl(cache, batch, q_index, head_w, q_mla, k, sm_scale, out, lse, scores_out, false, ld_scores,
-                          idx_out, workspace, workspace_bytes, dev_status, stream);
+                          idx_out, phys_out, workspace, workspace_bytes, dev_status, stream);
+}
+
+dsa_status_t dsa_topk_paged(const dsa_paged_cache_t* cache, const dsa_batch_t* batch, const float* scores,
+                            int64_t ld_scores, int32_t k, int32_t* idx_out, int32_t* phys_out, void* workspace,
+                            size_t workspace_bytes, int32_t* dev_status, void* stream) {
+  dsa_status_t s;
+  if ((s = check_cache(cache)) != DSA_OK) return s;
+  if ((s = check_batch(batch)) != DSA_OK) return s;
+  if (k < 1 || k > DSA_MAX_TOPK || !dev_status) return DSA_ERR_INVALID_ARG;
+  const int rows = batch->batch * batch->queries_per_seq;
+  if (rows == 0) return DSA_OK;
+  if (!scores || !idx_out || !aligned(scores, 16) || ld_scores < batch->max_seq_len || (ld_scores % 4))
+    return DSA_ERR_INVALID_ARG;
+  const size_t need = topk_workspace_bytes(rows, batch->max_seq_len, k);
+  if (need && (!workspace || !aligned(workspace, 256) || workspace_bytes < need)) return DSA_ERR_WORKSPACE;
+  TopkPhys po;
+  po.phys = phys_out;
+  po.block_table = batch->block_table;
+  po.max_blocks = batch->max_blocks_per_seq;
+  po.num_blocks = cache->num_blocks;
+  const int cap = std::min(batch->max_blocks_per_seq * kBlock, batch->max_seq_len);
+  return launch_topk(scores, ld_scores, nullptr, batch->seq_lens, batch->queries_per_seq, rows, cap, k, idx_out,
+                     workspace, dev_status, static_cast<cudaStream_t>(stream), po);
 }
 
 dsa_status_t dsa_decode_step_bf16(const dsa_paged_cache_t* cache, const dsa_batch_t* batch, const uint8_t* q_index,
                                   const float* head_w, const uint16_t* q_mla, int32_t k, float sm_scale,
                                   uint16_t* out, float* lse, uint16_t* scores_out, int64_t ld_scores,
-                                  int32_t* idx_out, void* workspace, size_t workspace_bytes, int32_t* dev_status,
-                                  void* stream) {
+                                  int32_t* idx_out, int32_t* phys_out, void* workspace, size_t workspace_bytes,
+                                  int32_t* dev_status, void* stream) {
   return decode_step_impl(cache, batch, q_index, head_w, q_mla, k, sm_scale, out, lse, scores_out, true, ld_scores,
-                          idx_out, workspace, workspace_bytes, dev_status, stream);
+                          idx_out, phys_out, workspace, workspace_bytes, dev_status, stream);
 }
 
 dsa_status_t dsa_cache_append(const dsa_paged_cache_t* cache, const dsa_batch_t* batch, const uint16_t* new_latent,
@@ -433,8 +465,8 @@ dsa_status_t dsa_decode_step_frontend(const dsa_paged_cache_t* cache, const dsa_
                                       const uint16_t* w_iq, const float* head_w, const uint16_t* new_latent,
                                       const uint16_t* new_index_key, const uint16_t* q_mla, int32_t k,
                                       float sm_scale, uint16_t* out, float* lse, float* scores_out,
-                                      int64_t ld_scores, int32_t* idx_out, void* workspace, size_t workspace_bytes,
-                                      int32_t* dev_status, void* stream) {
+                                      int64_t ld_scores, int32_t* idx_out, int32_t* phys_out, void* workspace,
+                                      size_t workspace_bytes, int32_t* dev_status, void* stream) {
   dsa_status_t s;
   if ((s = check_cache(cache)) != DSA_OK) return s;
   if ((s = check_batch(batch)) != DSA_OK) return s;
@@ -459,8 +491,8 @@ dsa_status_t dsa_decode_step_frontend(const dsa_paged_cache_t* cache, const dsa_
                            head_w_out, nullptr, dev_status, st)) != DSA_OK)
     return s;
   return dsa_decode_step(cache, batch, q_index, head_w_out, q_mla, k, sm_scale, out, lse, scores_out, ld_scores,
-                         idx_out, w, workspace_bytes - (size_t)(w - static_cast<uint8_t*>(workspace)), dev_status,
-                         stream);
+                         idx_out, phys_out, w, workspace_bytes - (size_t)(w - static_cast<uint8_t*>(workspace)),
+                         dev_status, stream);
 }
 
 dsa_status_t dsa_selftest_wait_timeout(int64_t limit_ns, int32_t* dev_status, void* stream) {

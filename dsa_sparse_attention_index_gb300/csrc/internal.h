@@ -36,16 +36,25 @@ dsa_status_t launch_index_scores(const dsa_paged_cache_t& c, const dsa_batch_t& 
                                  const float* head_w, void* scores, bool bf16, int64_t ld, int32_t* status,
                                  cudaStream_t st);
 size_t topk_workspace_bytes(int rows, int max_row_len, int k);
+// Optional physical KV rows beside the top-k's token indices: phys[r][p] =
+// block_table[r / nq][t / 64] * 64 + t % 64 for the index t at position p
+// (-1 for padding; an entry outside 0..num_blocks-1 is reported as
+// DSA_ERR_BOUNDS and gives -1).  phys == nullptr: none.
+struct TopkPhys {
+  int32_t* phys = nullptr;
+  const int32_t* block_table = nullptr;
+  int32_t max_blocks = 0, num_blocks = 0;
+};
 // Process-wide choice of the four-kernel top-k for rows too long for shared memory.
 int topk_force_multipass(int on);
 dsa_status_t launch_topk(const float* scores, int64_t ld, const int32_t* row_lens, const int32_t* seq_lens, int nq,
                          int rows, int max_row_len, int k, int32_t* out, void* workspace, int32_t* status,
-                         cudaStream_t st);
+                         cudaStream_t st, const TopkPhys& po = TopkPhys{});
 // The same top-k over bf16 scores (bits, widened exactly): the cluster paths
 // only (DSA_ERR_UNSUPPORTED where no cluster can be scheduled); no workspace.
 dsa_status_t launch_topk_bf16(const uint16_t* scores, int64_t ld, const int32_t* row_lens, const int32_t* seq_lens,
                               int nq, int rows, int max_row_len, int k, int32_t* out, int32_t* status,
-                              cudaStream_t st);
+                              cudaStream_t st, const TopkPhys& po = TopkPhys{});
 // The same top-k with its scratch in a file-scope device array (no allocation).
 dsa_status_t launch_topk_noalloc(const float* scores, int64_t ld, const int32_t* row_lens, int rows, int max_row_len,
                                  int k, int32_t* out, int32_t* status, cudaStream_t st);
@@ -72,9 +81,11 @@ int mla_max_chunk();
 dsa_status_t launch_sparse_mla_partials(const dsa_paged_cache_t& c, const dsa_batch_t& bt, const uint16_t* q_mla,
                                         const int32_t* idx, int k, const int32_t* seg, int nseg, float sm_scale,
                                         float* opart, float* ml, int32_t* status, cudaStream_t st);
+// phys: the top-k's physical KV rows for idx ([rows][k], -1 padding, already
+// bounds-checked and visible) or nullptr: the kernel translates idx itself.
 dsa_status_t launch_sparse_mla(const dsa_paged_cache_t& c, const dsa_batch_t& bt, const uint16_t* q_mla,
                                const int32_t* idx, int k, float sm_scale, uint16_t* out, float* lse,
-                               void* workspace, int32_t* status, cudaStream_t st);
+                               void* workspace, int32_t* status, cudaStream_t st, const int32_t* phys = nullptr);
 dsa_status_t launch_wait_selftest(int64_t limit_ns, int32_t* status, cudaStream_t st);
 dsa_status_t launch_cache_append(const dsa_paged_cache_t& c, const dsa_batch_t& bt, const uint16_t* new_latent,
                                  const uint16_t* new_key, int32_t* status, cudaStream_t st);

@@ -122,6 +122,10 @@ struct MlaParams {
   // `split` is [seg[split], seg[split + 1]), at most `chunk` long), or null:
   // chunk `split` is [split * chunk, (split + 1) * chunk)
   const int32_t* seg;
+  // the top-k's physical KV rows beside idx ([rows][k], block row * 64 + slot,
+  // -1 padding; visible and bounds-checked by the top-k), or null: the kernel
+  // translates idx through the block table itself
+  const int32_t* phys;
 };
 
 __device__ __forceinline__ float ex2(float x) {
@@ -315,14 +319,25 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int bound = (ntiles * kTileTok + 31) / 32 * 32;
     const int i0 = threadIdx.x - 128;
     int t[kPer], r[kPer];
+    if (p.phys) {
+      // the top-k's physical rows: visible and bounds-checked already
 #pragma unroll
-    for (int j = 0; j < kPer; ++j) {
-      const int i = i0 + j * kTr;
-      t[j] = i < count ? p.idx[(int64_t)row * p.k + c0 + i] : -1;
+      for (int j = 0; j < kPer; ++j) {
+        const int i = i0 + j * kTr;
+        const int ph = i < count ? p.phys[(int64_t)row * p.k + c0 + i] : -1;
+        t[j] = ph < 0 ? -1 : ph % kBlock;
+        r[j] = ph < 0 ? -1 : ph / kBlock;
+      }
+    } else {
+#pragma unroll
+      for (int j = 0; j < kPer; ++j) {
+        const int i = i0 + j * kTr;
+        t[j] = i < count ? p.idx[(int64_t)row * p.k + c0 + i] : -1;
+      }
+#pragma unroll
+      for (int j = 0; j < kPer; ++j)
+        r[j] = (t[j] >= 0 && t[j] < vis) ? p.block_table[(int64_t)b_seq * p.max_blocks + t[j] / kBlock] : -1;
     }
-#pragma unroll
-    for (int j = 0; j < kPer; ++j)
-      r[j] = (t[j] >= 0 && t[j] < vis) ? p.block_table[(int64_t)b_seq * p.max_blocks + t[j] / kBlock] : -1;
 #pragma unroll
     for (int j = 0; j < kPer; ++j) {
       const int i = i0 + j * kTr;
@@ -822,6 +837,7 @@ bool mla_setup(const dsa_paged_cache_t& c, const dsa_batch_t& bt, const uint16_t
                  c.latent_scale,
                  out,
                  lse,
+                 nullptr,
                  nullptr};
   static std::atomic<bool> attr_set[64];
   int dev = 0;
@@ -874,7 +890,7 @@ dsa_status_t launch_sparse_mla_partials(const dsa_paged_cache_t& c, const dsa_ba
 
 dsa_status_t launch_sparse_mla(const dsa_paged_cache_t& c, const dsa_batch_t& bt, const uint16_t* q_mla,
                                const int32_t* idx, int k, float sm_scale, uint16_t* out, float* lse,
-                               void* workspace, int32_t* status, cudaStream_t st) {
+                               void* workspace, int32_t* status, cudaStream_t st, const int32_t* phys) {
   const int rows = bt.batch * bt.queries_per_seq;
   if (rows == 0) return DSA_OK;
   const bool inv = batch_invariant();  // read once: the split and the workspace layout agree
@@ -890,6 +906,7 @@ dsa_status_t launch_sparse_mla(const dsa_paged_cache_t& c, const dsa_batch_t& bt
   MlaParams p;
   if (!mla_setup(c, bt, q_mla, idx, k, chunk, nsplit, sm_scale, opart, ml, out, lse, status, &qmap, &p))
     return DSA_ERR_CUDA;
+  p.phys = phys;
   // Up to kMaxFusedSplit chunks per row: the row's CTAs form a cluster and
   // merge the chunks themselves; more chunks take the combine kernel.
   const bool nv = c.latent_format == DSA_LATENT_NVFP4;

@@ -77,6 +77,18 @@ __device__ __forceinline__ int row_len(const int32_t* row_lens, const int32_t* s
   return len;
 }
 
+// The physical KV row of token t of row r's sequence (block row * 64 + slot),
+// -1 for padding; an entry outside the pool is reported and gives -1.
+__device__ __forceinline__ int32_t phys_row(const TopkPhys& po, int nq, int r, int t, int32_t* status) {
+  if (t < 0) return -1;
+  const int32_t b = po.block_table[(int64_t)(r / nq) * po.max_blocks + t / kBlock];
+  if (b < 0 || b >= po.num_blocks) {
+    report(status, DSA_ERR_BOUNDS);
+    return -1;
+  }
+  return b * kBlock + t % kBlock;
+}
+
 __global__ void __launch_bounds__(kThreads) topk_hist_kernel(const float* __restrict__ scores, int64_t ld,
                                                               const int32_t* row_lens, const int32_t* seq_lens,
                                                               int nq, int cap, int k, TopkWs ws, int32_t* status) {
@@ -323,7 +335,8 @@ __device__ void pick_digit(const uint32_t* hist, int nbins, uint32_t* sh, uint32
 __global__ void __launch_bounds__(kFinalThreads) topk_final_kernel(const float* __restrict__ scores, int64_t ld,
                                                                     const int32_t* row_lens,
                                                                     const int32_t* seq_lens, int nq, int cap, int k,
-                                                                    TopkWs ws, int32_t* out, int32_t* status) {
+                                                                    TopkWs ws, int32_t* out, int32_t* status,
+                                                                    const TopkPhys po) {
   extern __shared__ uint8_t smem_raw[];
   // bitmap[kWindowBits/32] u32 | cand[kCandCap] u64 | chosen[kMaxTopk] i32 | hist[kBins] u32 | scan[32] u32
   uint32_t* bitmap = reinterpret_cast<uint32_t*>(smem_raw);
@@ -336,8 +349,12 @@ __global__ void __launch_bounds__(kFinalThreads) topk_final_kernel(const float* 
   const int r = blockIdx.x, tid = threadIdx.x;
   const int len = row_len(row_lens, seq_lens, nq, r, cap, nullptr);
   int32_t* o = out + (int64_t)r * k;
+  auto emit = [&](int64_t pos_, int t_) {  // index t_ at output position pos_, and its physical row
+    o[pos_] = t_;
+    if (po.phys) po.phys[(int64_t)r * k + pos_] = phys_row(po, nq, r, t_, status);
+  };
   if (len <= k) {
-    for (int i = tid; i < k; i += kFinalThreads) o[i] = i < len ? i : -1;
+    for (int i = tid; i < k; i += kFinalThreads) emit(i, i < len ? i : -1);
     return;
   }
   const uint32_t* cnt = ws.counts + 4 * (int64_t)r;
@@ -345,7 +362,7 @@ __global__ void __launch_bounds__(kFinalThreads) topk_final_kernel(const float* 
   const int T = (int)cnt[2];
   if (n_sel >= (uint32_t)k || n_cand == 0) {  // impossible with a consistent histogram
     report(status, DSA_ERR_BOUNDS);
-    for (int i = tid; i < k; i += kFinalThreads) o[i] = -1;
+    for (int i = tid; i < k; i += kFinalThreads) emit(i, -1);
     return;
   }
   // rows up to one bitmap window set their bits directly; longer rows collect a list first
@@ -483,7 +500,7 @@ __global__ void __launch_bounds__(kFinalThreads) topk_final_kernel(const float* 
       while (bits) {
         const int b = __ffs(bits) - 1;
         bits &= bits - 1;
-        if (pos < (uint32_t)k) o[pos] = (int32_t)(w0 + (int64_t)wi * 32 + b);
+        if (pos < (uint32_t)k) emit(pos, (int32_t)(w0 + (int64_t)wi * 32 + b));
         ++pos;
       }
     }
@@ -491,7 +508,7 @@ __global__ void __launch_bounds__(kFinalThreads) topk_final_kernel(const float* 
     __syncthreads();
   }
   if (direct && written != (uint32_t)k) report(status, DSA_ERR_BOUNDS);  // internal consistency check
-  for (int i = (int)written + tid; i < k; i += kFinalThreads) o[i] = -1;
+  for (int i = (int)written + tid; i < k; i += kFinalThreads) emit(i, -1);
 }
 
 // ---------------------------------------------------------------- row-resident path
@@ -625,7 +642,7 @@ template <int C, bool kStream, typename In>
 __global__ void __launch_bounds__(kResThreads, kStream ? 1 : 2)
     topk_cluster_kernel(const In* __restrict__ scores, int64_t ld, const int32_t* row_lens,
                         const int32_t* seq_lens, int nq, int cap, int k, int32_t* out, int32_t* status,
-                        int slice_cap) {
+                        int slice_cap, const TopkPhys po) {
   constexpr bool kF32 = std::is_same<In, float>::value;
   using G = typename std::conditional<kStream, float4, uint4>::type;  // a group of 4 elements
   cg::cluster_group cluster = cg::this_cluster();
@@ -648,11 +665,15 @@ __global__ void __launch_bounds__(kResThreads, kStream ? 1 : 2)
 
   const int len = row_len(row_lens, seq_lens, nq, r, cap, c == 0 ? status : nullptr);
   int32_t* o = out + (int64_t)r * k;
+  auto emit = [&](int64_t pos_, int t_) {  // index t_ at output position pos_, and its physical row
+    o[pos_] = t_;
+    if (po.phys) po.phys[(int64_t)r * k + pos_] = phys_row(po, nq, r, t_, status);
+  };
   grid_dep_wait();  // the scores come from the previous kernel, which may still read `out`
   grid_dep_launch();
   if (len <= k) {  // the same branch for every CTA of the cluster
     if (c == 0)
-      for (int i = tid; i < k; i += kResThreads) o[i] = i < len ? i : -1;
+      for (int i = tid; i < k; i += kResThreads) emit(i, i < len ? i : -1);
     return;
   }
   // this CTA's slice of the row: S tokens from `start` (S a multiple of 4)
@@ -969,7 +990,7 @@ __global__ void __launch_bounds__(kResThreads, kStream ? 1 : 2)
         }
       }
       if (take) {
-        if (p < (uint32_t)k) o[p] = start + 4 * q0 + b;
+        if (p < (uint32_t)k) emit(p, start + 4 * q0 + b);
         ++p;
       }
     }
@@ -1088,7 +1109,7 @@ __global__ void __launch_bounds__(kResThreads, kStream ? 1 : 2)
       }
       const uint32_t take_mask = __ballot_sync(0xffffffffu, take);
       const uint32_t p = pos + __popc(take_mask & lanes_below);
-      if (take && p < (uint32_t)k) o[p] = start + (int)(e & 0x7FFFFFFFu);
+      if (take && p < (uint32_t)k) emit(p, start + (int)(e & 0x7FFFFFFFu));
       pos += __popc(take_mask);
     }
     return;
@@ -1120,7 +1141,7 @@ __global__ void __launch_bounds__(kResThreads, kStream ? 1 : 2)
 #pragma unroll
         for (int j = 0; j < 4; ++j)
           if ((take >> j) & 1u) {
-            if (p < (uint32_t)k) o[p] = start + 4 * i + j;
+            if (p < (uint32_t)k) emit(p, start + 4 * i + j);
             ++p;
           }
         pos += t_tot;
@@ -1131,7 +1152,8 @@ __global__ void __launch_bounds__(kResThreads, kStream ? 1 : 2)
 
 template <int C, bool kStream, typename In>
 dsa_status_t launch_cluster(const In* scores, int64_t ld, const int32_t* row_lens, const int32_t* seq_lens,
-                            int nq, int rows, int cap, int k, int32_t* out, int32_t* status, cudaStream_t st) {
+                            int nq, int rows, int cap, int k, int32_t* out, int32_t* status, cudaStream_t st,
+                            const TopkPhys& po) {
   static std::atomic<bool> attr_set[64];
   int dev = 0;
   cudaGetDevice(&dev);
@@ -1164,7 +1186,7 @@ dsa_status_t launch_cluster(const In* scores, int64_t ld, const int32_t* row_len
   cfg.numAttrs = 2;
   count_launches(1);
   if (cuda_status(cudaLaunchKernelEx(&cfg, topk_cluster_kernel<C, kStream, In>, scores, ld, row_lens, seq_lens, nq, cap,
-                                     k, out, status, slice)) != DSA_OK)
+                                     k, out, status, slice, po)) != DSA_OK)
     return DSA_ERR_CUDA;
   return launch_status();
 }
@@ -1227,7 +1249,7 @@ namespace {
 template <typename In>
 bool launch_topk_cluster(const In* scores, int64_t ld, const int32_t* row_lens, const int32_t* seq_lens, int nq,
                          int rows, int max_row_len, int k, int32_t* out, int32_t* status, cudaStream_t st,
-                         dsa_status_t* res) {
+                         dsa_status_t* res, const TopkPhys& po) {
   // row-resident path: one cluster per row, enough CTAs to hold the row, small
   // enough slices for two CTAs per SM where a cluster of 8 allows it, and for
   // few rows enough CTAs to spread them over the SMs (at least 8,192 keys per CTA)
@@ -1239,7 +1261,7 @@ bool launch_topk_cluster(const In* scores, int64_t ld, const int32_t* row_lens, 
   const int cluster = std::min(kResMaxCluster, std::max(std::max(c_min, c_pair), std::max(c_fill, 1)));
   if (max_row_len > k && c_min <= kResMaxCluster) {
     // row-resident path: one cluster of `cluster` CTAs per row, no workspace
-#define DSA_RES(C) launch_cluster<C, false, In>(scores, ld, row_lens, seq_lens, nq, rows, max_row_len, k, out, status, st)
+#define DSA_RES(C) launch_cluster<C, false, In>(scores, ld, row_lens, seq_lens, nq, rows, max_row_len, k, out, status, st, po)
     switch (cluster) {
       case 1: *res = DSA_RES(1); break;
       case 2: *res = DSA_RES(2); break;
@@ -1257,11 +1279,11 @@ bool launch_topk_cluster(const In* scores, int64_t ld, const int32_t* row_lens, 
     // rows too long to hold on chip: the streaming cluster kernel, 16 CTAs per
     // row where the device schedules such clusters, else 8
     if (stream_cluster_ok<16, In>()) {
-      *res = launch_cluster<16, true, In>(scores, ld, row_lens, seq_lens, nq, rows, max_row_len, k, out, status, st);
+      *res = launch_cluster<16, true, In>(scores, ld, row_lens, seq_lens, nq, rows, max_row_len, k, out, status, st, po);
       return true;
     }
     if (stream_cluster_ok<8, In>()) {
-      *res = launch_cluster<8, true, In>(scores, ld, row_lens, seq_lens, nq, rows, max_row_len, k, out, status, st);
+      *res = launch_cluster<8, true, In>(scores, ld, row_lens, seq_lens, nq, rows, max_row_len, k, out, status, st, po);
       return true;
     }
   }
@@ -1272,13 +1294,13 @@ bool launch_topk_cluster(const In* scores, int64_t ld, const int32_t* row_lens, 
 
 dsa_status_t launch_topk_bf16(const uint16_t* scores, int64_t ld, const int32_t* row_lens, const int32_t* seq_lens,
                               int nq, int rows, int max_row_len, int k, int32_t* out, int32_t* status,
-                              cudaStream_t st) {
+                              cudaStream_t st, const TopkPhys& po) {
   if (rows == 0) return DSA_OK;
   dsa_status_t res = DSA_OK;
   if (max_row_len <= k)  // nothing to select: the kernel writes 0..len-1 and the padding, reading no score
     return launch_cluster<1, false, uint16_t>(scores, ld, row_lens, seq_lens, nq, rows, max_row_len, k, out, status,
-                                              st);
-  if (launch_topk_cluster(scores, ld, row_lens, seq_lens, nq, rows, max_row_len, k, out, status, st, &res))
+                                              st, po);
+  if (launch_topk_cluster(scores, ld, row_lens, seq_lens, nq, rows, max_row_len, k, out, status, st, &res, po))
     return res;
   // long rows with the four-kernel path forced, or no cluster schedulable: that path reads fp32 scores only
   return DSA_ERR_UNSUPPORTED;
@@ -1286,10 +1308,10 @@ dsa_status_t launch_topk_bf16(const uint16_t* scores, int64_t ld, const int32_t*
 
 dsa_status_t launch_topk(const float* scores, int64_t ld, const int32_t* row_lens, const int32_t* seq_lens, int nq,
                          int rows, int max_row_len, int k, int32_t* out, void* workspace, int32_t* status,
-                         cudaStream_t st) {
+                         cudaStream_t st, const TopkPhys& po) {
   if (rows == 0) return DSA_OK;
   dsa_status_t res = DSA_OK;
-  if (launch_topk_cluster(scores, ld, row_lens, seq_lens, nq, rows, max_row_len, k, out, status, st, &res))
+  if (launch_topk_cluster(scores, ld, row_lens, seq_lens, nq, rows, max_row_len, k, out, status, st, &res, po))
     return res;
   auto al = [](size_t x) { return (x + 255) & ~size_t(255); };
   uint8_t* w = static_cast<uint8_t*>(workspace);
@@ -1324,7 +1346,7 @@ dsa_status_t launch_topk(const float* scores, int64_t ld, const int32_t* row_len
     attr_set[dev] = true;
   }
   count_launches(1);
-  topk_final_kernel<<<rows, kFinalThreads, smem, st>>>(scores, ld, row_lens, seq_lens, nq, cap, k, ws, out, status);
+  topk_final_kernel<<<rows, kFinalThreads, smem, st>>>(scores, ld, row_lens, seq_lens, nq, cap, k, ws, out, status, po);
   return launch_status();
 }
 
@@ -1363,7 +1385,7 @@ dsa_status_t launch_topk_noalloc(const float* scores, int64_t ld, const int32_t*
     }
     scratch = g_scratch_addr[dev];
   }
-  return launch_topk(scores, ld, row_lens, nullptr, 1, rows, max_row_len, k, out, scratch, status, st);
+  return launch_topk(scores, ld, row_lens, nullptr, 1, rows, max_row_len, k, out, scratch, status, st, TopkPhys{});
 }
 
 }  // namespace dsa

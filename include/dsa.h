@@ -21,6 +21,7 @@
  *   dsa_translate_pages      block table -> page addresses
  *   dsa_index_scores(_bf16)  indexer scores (FP8 or MXFP4 keys; fp32 or bf16 out)
  *   dsa_topk(_bf16, _noalloc) top-k per row, ties to the lower index
+ *   dsa_topk_paged           the step's top-k, with the selected tokens' physical KV rows
  *   sparse_mla_decode        exact sparse MLA over the selected tokens
  *   dsa_decode_step(_bf16)   the three stages fused on one stream
  *   dsa_cache_append, dsa_quantize_index_query   the step's front end
@@ -60,7 +61,7 @@
 extern "C" {
 #endif
 
-#define DSA_API_VERSION 2
+#define DSA_API_VERSION 3
 #define DSA_BLOCK_SIZE 64        /* tokens per page */
 #define DSA_INDEX_HEADS 32       /* light indexer heads */
 #define DSA_INDEX_DIM 128        /* indexer head dim */
@@ -326,8 +327,12 @@ dsa_status_t dsa_dcp_sparse_mla(const dsa_paged_cache_t* cache, const dsa_batch_
  * one stream with no host synchronisation (Day-0 post, fused low-latency
  * decode section: a key-balanced scorer and an exact top-k in two kernels,
  * then sparse attention).  Arguments as above; scores_out (fp32
- * [rows][ld_scores]) and idx_out (int32 [rows][k]) are optional (NULL: kept
- * in the workspace only).
+ * [rows][ld_scores]), idx_out (int32 [rows][k]) and phys_out (int32 [rows][k])
+ * are optional (NULL: kept in the workspace only).  phys_out receives the
+ * physical KV row of each selected token, block_table[b][t / 64] * 64 + t % 64
+ * (-1 beside -1 padding): the rows the attention reads (same section: the
+ * fused indexer outputs the physical KV rows that attention reads).  The MLA
+ * kernel reads those rows instead of translating the indices again.
  *   workspace >= dsa_workspace_size(batch, k) bytes, 256-B aligned
  */
 size_t dsa_workspace_size(const dsa_batch_t* batch, int32_t k);
@@ -335,9 +340,24 @@ dsa_status_t dsa_decode_step(const dsa_paged_cache_t* cache, const dsa_batch_t* 
                              const uint8_t* q_index, const float* head_w,
                              const uint16_t* q_mla, int32_t k, float sm_scale,
                              uint16_t* out, float* lse,
-                             float* scores_out, int64_t ld_scores, int32_t* idx_out,
+                             float* scores_out, int64_t ld_scores, int32_t* idx_out, int32_t* phys_out,
                              void* workspace, size_t workspace_bytes,
                              int32_t* dev_status, void* stream);
+
+/*
+ * The top-k of the fused step as a call of its own: rows r = b *
+ * queries_per_seq + j of the batch with their visible lengths (row j of
+ * sequence b sees seq_len_b - (queries_per_seq - 1) + j tokens), the same
+ * selection as dsa_topk, and optionally the physical KV rows of the selected
+ * tokens through the cache's block table (as phys_out of dsa_decode_step;
+ * a table entry outside the pool gives -1 and DSA_ERR_BOUNDS in *dev_status).
+ *   scores    device fp32 [rows][ld_scores], ld_scores >= batch->max_seq_len, a multiple of 4
+ *   idx_out   device int32 [rows][k];  phys_out device int32 [rows][k] or NULL
+ *   workspace >= dsa_topk_workspace_size(rows, batch->max_seq_len, k) bytes, 256-B aligned
+ */
+dsa_status_t dsa_topk_paged(const dsa_paged_cache_t* cache, const dsa_batch_t* batch, const float* scores,
+                            int64_t ld_scores, int32_t k, int32_t* idx_out, int32_t* phys_out, void* workspace,
+                            size_t workspace_bytes, int32_t* dev_status, void* stream);
 
 /*
  * BF16 scores (Day-0 post, decode-context-parallelism section: candidates
@@ -369,7 +389,7 @@ dsa_status_t dsa_decode_step_bf16(const dsa_paged_cache_t* cache, const dsa_batc
                                   const uint8_t* q_index, const float* head_w,
                                   const uint16_t* q_mla, int32_t k, float sm_scale,
                                   uint16_t* out, float* lse,
-                                  uint16_t* scores_out, int64_t ld_scores, int32_t* idx_out,
+                                  uint16_t* scores_out, int64_t ld_scores, int32_t* idx_out, int32_t* phys_out,
                                   void* workspace, size_t workspace_bytes,
                                   int32_t* dev_status, void* stream);
 
@@ -458,8 +478,8 @@ dsa_status_t dsa_decode_step_frontend(const dsa_paged_cache_t* cache, const dsa_
                                       const uint16_t* w_iq, const float* head_w, const uint16_t* new_latent,
                                       const uint16_t* new_index_key, const uint16_t* q_mla, int32_t k,
                                       float sm_scale, uint16_t* out, float* lse, float* scores_out,
-                                      int64_t ld_scores, int32_t* idx_out, void* workspace, size_t workspace_bytes,
-                                      int32_t* dev_status, void* stream);
+                                      int64_t ld_scores, int32_t* idx_out, int32_t* phys_out, void* workspace,
+                                      size_t workspace_bytes, int32_t* dev_status, void* stream);
 
 /*
  * Self-test of the bounded in-kernel wait used by every pipelined kernel:

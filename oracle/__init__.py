@@ -83,6 +83,8 @@ def _load():
             lib.oracle_index_query_proj.restype = i32
             lib.oracle_quantize_query_f32.argtypes = [P, P, i32, P, P]
             lib.oracle_quantize_query_f32.restype = i32
+            lib.oracle_phys_rows.argtypes = [P, i32, i32, i32, P, i32, i32, P]
+            lib.oracle_phys_rows.restype = i32
             _lib = lib
     return _lib
 
@@ -299,6 +301,20 @@ def quantize_query_f32(q_f32: np.ndarray, head_w: np.ndarray):
     w_out = np.empty((rows, IDX_HEADS), dtype=np.float32)
     _check(_load().oracle_quantize_query_f32(_ptr(q), _ptr(w), rows, _ptr(codes), _ptr(w_out)), "quantize_query_f32")
     return codes, w_out
+
+
+def phys_rows(case, idx: np.ndarray) -> np.ndarray:
+    """The physical KV rows (block row * 64 + slot) of the selected tokens idx
+    [rows, k] through the case's block table, -1 beside -1 (Day-0 post,
+    fused-decode section: the fused indexer outputs the physical KV rows that
+    attention reads).  Raises on a table entry outside the pool."""
+    ix = np.ascontiguousarray(idx, dtype=np.int32)
+    rows, k = ix.shape
+    out = np.empty_like(ix)
+    bt = np.ascontiguousarray(case.block_table, dtype=np.int32)
+    _check(_load().oracle_phys_rows(_ptr(bt), int(bt.shape[1]), int(case.num_blocks), int(case.nq), _ptr(ix), rows,
+                                    int(k), _ptr(out)), "phys_rows")
+    return out
 
 
 def round_bf16(x: np.ndarray) -> np.ndarray:

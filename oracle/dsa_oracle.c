@@ -761,3 +761,36 @@ int oracle_quantize_query_f32(const float* q, const float* w, int32_t rows, uint
   }
   return ORACLE_OK;
 }
+
+/*
+ * Physical KV rows of selected tokens ([K31] "低延迟解码：融合的 DSA 解码路径",
+ * fourth bullet: the fused indexer outputs the physical KV rows that the
+ * attention reads; "为三类状态服务的 KV 缓存": a block table maps each
+ * sequence's logical blocks to pool rows).  Row r belongs to sequence r / nq;
+ * token t of it lives in pool row block_table[b][t / 64], slot t % 64, read as
+ * the physical row number block_row * 64 + slot.  -1 stays -1.  Returns 3 for
+ * a table entry outside 0..num_blocks-1 (that output is -1).
+ */
+int oracle_phys_rows(const int32_t* block_table, int32_t max_blocks, int32_t num_blocks, int32_t nq,
+                     const int32_t* idx, int32_t rows, int32_t k, int32_t* phys) {
+  if (!block_table || !idx || !phys || nq < 1 || rows < 0 || k < 1) return ORACLE_BAD_ARG;
+  int bad = 0;
+  for (int64_t r = 0; r < rows; ++r)
+    for (int64_t p = 0; p < k; ++p) {
+      const int32_t t = idx[r * k + p];
+      int32_t v = -1;
+      if (t >= 0) {
+        if (t / ORACLE_BLOCK >= max_blocks) {
+          bad = 1;
+        } else {
+          const int32_t row = block_table[(r / nq) * max_blocks + t / ORACLE_BLOCK];
+          if (row < 0 || row >= num_blocks)
+            bad = 1;
+          else
+            v = row * ORACLE_BLOCK + t % ORACLE_BLOCK;
+        }
+      }
+      phys[r * k + p] = v;
+    }
+  return bad ? ORACLE_BAD_BLOCK : ORACLE_OK;
+}

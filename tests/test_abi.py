@@ -33,7 +33,7 @@ def test_every_declared_symbol_is_exported(lib):
 
 
 def test_version_and_status_strings(lib):
-    assert lib.dsa_api_version() == 2
+    assert lib.dsa_api_version() == 3
     for code in range(7):
         assert binding.status_string(code).startswith("DSA_")
     assert "unknown" in binding.status_string(99)
@@ -58,7 +58,7 @@ def test_host_validation_without_device(lib):
     for nq in (5, 2049, 0):  # > 4 rows must come in groups of 4; at most 2048; at least 1
         b.queries_per_seq = nq
         assert lib.dsa_decode_step(ctypes.byref(c), ctypes.byref(b), None, None, None, 2048, 1.0, None, None, None,
-                                   0, None, None, 0, None, None) == B.ERR_UNSUPPORTED
+                                   0, None, None, None, 0, None, None) == B.ERR_UNSUPPORTED
     b.queries_per_seq = 2
     c.key_format = B.KEY_MXFP4  # MXFP4 keys: one row per sequence
     c.row_stride, c.index_off = 41216, 36864
@@ -102,7 +102,7 @@ def test_host_validation_without_device(lib):
                                   4096, 1 << 40, st, None) == B.ERR_INVALID_ARG
     # bf16 fused step: a caller's score buffer needs a row stride that is a multiple of 8
     assert lib.dsa_decode_step_bf16(ctypes.byref(c), ctypes.byref(b), 1024, 2048, 4096, 2048, 1.0, 8192, 512, 16384,
-                                    100, None, 4096, 1 << 40, st, None) == B.ERR_INVALID_ARG
+                                    100, None, None, 4096, 1 << 40, st, None) == B.ERR_INVALID_ARG
 
 
 def test_workspace_sizes(lib):
@@ -167,5 +167,5 @@ def test_frontend_host_validation_without_device(lib):
     need = lib.dsa_frontend_workspace_size(ctypes.byref(b), 2048)
     assert need >= lib.dsa_workspace_size(ctypes.byref(b), 2048) + 4096
     assert lib.dsa_decode_step_frontend(ctypes.byref(c), ctypes.byref(b), fake, 1536, fake, 1e-6, fake, fake, fake,
-                                        fake, fake, 2048, 1.0, fake, fake, None, 0, None, fake, need - 1, st,
+                                        fake, fake, 2048, 1.0, fake, fake, None, 0, None, None, fake, need - 1, st,
                                         None) == B.ERR_WORKSPACE

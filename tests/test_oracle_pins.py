@@ -772,3 +772,29 @@ def test_quantize_query_f32_folds_the_scale():
     assert (codes[1, 2] == 0).all() and w_out[1, 2] == w[1, 2]
     qb = _bf16_bits(q)
     np.testing.assert_array_equal(oracle.quantize_query_f32(_bf16_value(qb), w)[0], oracle.quantize_query(qb, w)[0])
+
+
+# ---------------------------------------------------------------- physical KV rows
+def test_phys_rows_identity_table_and_permutation():
+    """With the identity block table of one sequence the physical row of token
+    t is t itself; with a permuted table it is perm[t // 64] * 64 + t % 64
+    (checked against a Python loop over the same table), -1 stays -1, and
+    rows of the same sequence (draft rows) share the sequence's table row."""
+    ident = synth.make_case("pi", seq_lens=[3000], seed=1, permute_blocks=False)
+    idx = np.array([[0, 1, 63, 64, 2999, -1]], dtype=np.int32)
+    np.testing.assert_array_equal(oracle.phys_rows(ident, idx), idx)
+    case = synth.make_case("pp", seq_lens=[700, 1300], nq=2, seed=4)
+    rng = np.random.default_rng(2)
+    idx = np.full((4, 50), -1, dtype=np.int32)
+    for r, L in enumerate(case.row_lens()):
+        idx[r, :40] = np.sort(rng.choice(int(L), 40, replace=False))
+    got = oracle.phys_rows(case, idx)
+    for r in range(4):
+        for p in range(50):
+            t = int(idx[r, p])
+            want = -1 if t < 0 else int(case.block_table[r // 2, t // 64]) * 64 + t % 64
+            assert got[r, p] == want
+    case.block_table[1, 0] = case.num_blocks   # outside the pool
+    idx2 = np.zeros((4, 1), dtype=np.int32)
+    with pytest.raises(RuntimeError):
+        oracle.phys_rows(case, idx2)
