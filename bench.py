@@ -468,29 +468,51 @@ def main_ours(args):
             "partial_bytes_per_shard_and_row": 96 * 512 * 2 + 96 * 4,
             "max_abs_vs_unsharded": round(diff, 5)}
 
-    # ---- end to end through the public call, host buffers, copies inside the timed region
+    # ---- end to end through the public call, host buffers, copies inside the timed region:
+    #      the step's host inputs packed in one pinned buffer (one host->device copy into a
+    #      device buffer whose views are the step's arguments), its outputs in one device
+    #      buffer (one device->host copy into pinned memory)
     e2e_ms = []
     if not args.no_e2e:
-        pin = lambda t: t.cpu().pin_memory()
-        h_in = [pin(dc.q_index), pin(dc.head_w), pin(dc.q_mla), pin(dc.batch.block_table), pin(dc.batch.seq_lens)]
-        d_in = [dc.q_index, dc.head_w, dc.q_mla, dc.batch.block_table, dc.batch.seq_lens]
-        h_out = [torch.empty_like(out, device="cpu").pin_memory(), torch.empty_like(lse, device="cpu").pin_memory()]
-        bi = sum(t.numel() * t.element_size() for t in h_in)
-        bo = sum(t.numel() * t.element_size() for t in h_out)
-        e2e_ms = []
+        from dsa_sparse_attention_index_gb300 import binding as B
+
+        srcs = [dc.q_index, dc.head_w, dc.q_mla, dc.batch.block_table, dc.batch.seq_lens]
+        al = lambda n: (n + 255) // 256 * 256
+        offs, tot = [], 0
+        for t in srcs:
+            offs.append(tot)
+            tot += al(t.numel() * t.element_size())
+        h_in = torch.empty(tot, dtype=torch.uint8).pin_memory()
+        d_in = torch.empty(tot, dtype=torch.uint8, device=dev)
+        views = []
+        for t, o in zip(srcs, offs):
+            n = t.numel() * t.element_size()
+            h_in[o:o + n].copy_(t.contiguous().view(-1).view(torch.uint8).cpu())
+            views.append(d_in[o:o + n].view(t.dtype).view(t.shape))
+        e_qi, e_w, e_qm, e_bt, e_sl = views
+        e_batch = B.Batch(block_table=e_bt, seq_lens=e_sl, queries_per_seq=case.nq, max_seq_len=max(case.max_len, 0))
+        o_bytes = al(out.numel() * 2)
+        d_out = torch.empty(o_bytes + lse.numel() * 4, dtype=torch.uint8, device=dev)
+        e_out = d_out[:out.numel() * 2].view(torch.int16).view(out.shape)
+        e_lse = d_out[o_bytes:].view(torch.float32).view(lse.shape)
+        h_out = torch.empty(d_out.numel(), dtype=torch.uint8).pin_memory()
+        bi, bo = tot, d_out.numel()
         for it in range(args.warmup + args.steps):
             flush.zero_()
             e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
             e0.record(stream)
-            for h, d in zip(h_in, d_in):
-                d.copy_(h, non_blocking=True)
-            step()
-            h_out[0].copy_(out, non_blocking=True)
-            h_out[1].copy_(lse, non_blocking=True)
+            d_in.copy_(h_in, non_blocking=True)
+            B.decode_step(dc.cache, e_batch, e_qi, e_w, e_qm, k, case.sm_scale, e_out, e_lse, ws, status,
+                          stream=stream)
+            h_out.copy_(d_out, non_blocking=True)
             e1.record(stream)
             torch.cuda.synchronize()
             if it >= args.warmup:
                 e2e_ms.append(e0.elapsed_time(e1))
+        step()  # the device-resident step once more: the e2e call computed the same outputs
+        torch.cuda.synchronize()
+        assert status.item() == 0, binding.status_string(status.item())
+        assert torch.equal(e_out, out) and torch.equal(e_lse, lse)
         e2e_t = reps.max(statistics.mean(e2e_ms), dev)
 
     b = roofline.step_bytes(case.seq_lens, case.nq, k, case.key_format, case.latent_format)

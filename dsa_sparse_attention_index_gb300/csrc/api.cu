@@ -298,7 +298,7 @@ dsa_status_t sparse_mla_decode(const dsa_paged_cache_t* cache, const dsa_batch_t
 size_t dsa_workspace_size(const dsa_batch_t* batch, int32_t k) {
   if (!batch || batch->batch < 0 || k < 1 || k > DSA_MAX_TOPK) return 0;
   const int rows = batch->batch * std::max(1, batch->queries_per_seq);
-  return al256((size_t)rows * round_ld(batch->max_seq_len) * 4) + 2 * al256((size_t)rows * k * 4) +
+  return al256((size_t)rows * round_ld(batch->max_seq_len) * 4) + al256((size_t)rows * k * 4) +
          al256(topk_workspace_bytes(rows, batch->max_seq_len, k)) + al256(mla_workspace_bytes(rows, k));
 }
 
@@ -335,9 +335,10 @@ dsa_status_t decode_step_impl(const dsa_paged_cache_t* cache, const dsa_batch_t*
   w += scores_bytes;
   int32_t* idx = idx_out ? idx_out : reinterpret_cast<int32_t*>(w);
   w += al256((size_t)rows * k * 4);
-  // the selected tokens' physical KV rows: written by the top-k, read by the MLA
-  int32_t* phys = phys_out ? phys_out : reinterpret_cast<int32_t*>(w);
-  w += al256((size_t)rows * k * 4);
+  // the selected tokens' physical KV rows, when the caller asks for them: written
+  // by the top-k and read by the MLA (which otherwise translates the indices
+  // itself, beside its Q loads, off the critical path)
+  int32_t* phys = phys_out;
   void* topk_ws = w;
   w += al256(topk_workspace_bytes(rows, batch->max_seq_len, k));
   void* mla_ws = w;

@@ -398,7 +398,7 @@ constexpr int kDcpMaxPieces = 16;
 // inside, natural log stored).  part_out / part_lse (nullable) receive the
 // shards' outputs, [W][rows][96][512] bf16 and [W][rows][96] fp32.
 template <int P>
-__global__ void __launch_bounds__(256) dcp_combine_kernel(const float* __restrict__ opart,
+__global__ void __launch_bounds__(256) dcp_combine_kernel(const uint16_t* __restrict__ opart,
                                                            const float* __restrict__ ml, int W, int rows,
                                                            float latent_scale, uint16_t* __restrict__ out,
                                                            float* __restrict__ lse, uint16_t* __restrict__ part_out,
@@ -426,7 +426,7 @@ __global__ void __launch_bounds__(256) dcp_combine_kernel(const float* __restric
         const float w = (M == -INFINITY || v.x == -INFINITY) ? 0.f : dcp_ex2(v.x - M);
         den += w * v.y;
         ex += w * v.z;
-        wgt[hl][r * P + j] = w;
+        wgt[hl][r * P + j] = w * v.y;  // the piece's partial is normalised by v.y
       }
       const float inv = den > 0.f ? latent_scale / den : 0.f;
       for (int j = 0; j < P; ++j) wgt[hl][r * P + j] *= inv;
@@ -450,12 +450,17 @@ __global__ void __launch_bounds__(256) dcp_combine_kernel(const float* __restric
   constexpr int kVec = kDcpCombineHeads * kValue / 4;  // 1024 float4s per CTA
   for (int v = threadIdx.x; v < kVec; v += blockDim.x) {
     const int hl = v / (kValue / 4), d = (v % (kValue / 4)) * 4;
-    const float* src = opart + ((int64_t)row * nseg * kHeads + h0 + hl) * kValue + d;
+    const uint16_t* src = opart + ((int64_t)row * nseg * kHeads + h0 + hl) * kValue + d;
     // an empty piece wrote no partial: only pieces with weight are read
     float4 x[DSA_DCP_MAX_SHARDS * P];
 #pragma unroll
     for (int s = 0; s < DSA_DCP_MAX_SHARDS * P; ++s)
-      if (s < nseg && wgt[hl][s] != 0.f) x[s] = *reinterpret_cast<const float4*>(src + (int64_t)s * kHeads * kValue);
+      if (s < nseg && wgt[hl][s] != 0.f) {
+        const uint2 hv = *reinterpret_cast<const uint2*>(src + (int64_t)s * kHeads * kValue);
+        const float2 a = __half22float2(*reinterpret_cast<const __half2*>(&hv.x));
+        const float2 b = __half22float2(*reinterpret_cast<const __half2*>(&hv.y));
+        x[s] = make_float4(a.x, a.y, b.x, b.y);
+      }
     float4 a = make_float4(0.f, 0.f, 0.f, 0.f);
 #pragma unroll
     for (int r = 0; r < DSA_DCP_MAX_SHARDS; ++r) {
@@ -566,7 +571,7 @@ static int dcp_pieces(int k) { return (k + mla_max_chunk() - 1) / mla_max_chunk(
 size_t dcp_mla_workspace_bytes(int rows, int k, int shards) {
   auto al = [](size_t x) { return (x + 255) & ~size_t(255); };
   const size_t nseg = (size_t)shards * dcp_pieces(k);
-  return al((size_t)rows * k * 4) + al((size_t)rows * (nseg + 1) * 4) + al((size_t)rows * nseg * kHeads * kValue * 4) +
+  return al((size_t)rows * k * 4) + al((size_t)rows * (nseg + 1) * 4) + al((size_t)rows * nseg * kHeads * kValue * 2) +
          al((size_t)rows * nseg * kHeads * 16);
 }
 
@@ -584,8 +589,8 @@ dsa_status_t launch_dcp_sparse_mla(const dsa_paged_cache_t& c, const dsa_batch_t
   w += al((size_t)rows * k * 4);
   int32_t* seg = reinterpret_cast<int32_t*>(w);
   w += al((size_t)rows * (nseg + 1) * 4);
-  float* opart = reinterpret_cast<float*>(w);
-  w += al((size_t)rows * nseg * kHeads * kValue * 4);
+  uint16_t* opart = reinterpret_cast<uint16_t*>(w);
+  w += al((size_t)rows * nseg * kHeads * kValue * 2);
   float* ml = reinterpret_cast<float*>(w);
   count_launches(1);
   dcp_group_kernel<<<dim3((unsigned)W, (unsigned)rows), kDcpThreads, 0, st>>>(idx, k, W, P, mla_max_chunk(), gidx,
@@ -605,9 +610,9 @@ dsa_status_t launch_dcp_sparse_mla(const dsa_paged_cache_t& c, const dsa_batch_t
   cfg.numAttrs = 1;
   count_launches(1);
   const cudaError_t e =
-      P == 1 ? cudaLaunchKernelEx(&cfg, dcp_combine_kernel<1>, (const float*)opart, (const float*)ml, W, rows,
+      P == 1 ? cudaLaunchKernelEx(&cfg, dcp_combine_kernel<1>, (const uint16_t*)opart, (const float*)ml, W, rows,
                                   c.latent_scale, out, lse, part_out, part_lse)
-             : cudaLaunchKernelEx(&cfg, dcp_combine_kernel<2>, (const float*)opart, (const float*)ml, W, rows,
+             : cudaLaunchKernelEx(&cfg, dcp_combine_kernel<2>, (const uint16_t*)opart, (const float*)ml, W, rows,
                                   c.latent_scale, out, lse, part_out, part_lse);
   if (cuda_status(e) != DSA_OK) return DSA_ERR_CUDA;
   return launch_status();

@@ -237,7 +237,6 @@ __global__ void __launch_bounds__(idx_threads<MX>(), 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
-  grid_dep_launch();  // the top-k may launch and wait for this grid on its own
 
   const int64_t total = prefix[nb];
   const int64_t u_begin = total * blockIdx.x / gridDim.x;
@@ -515,6 +514,11 @@ __global__ void __launch_bounds__(idx_threads<MX>(), 1)
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
+  // The top-k is launched once every CTA of this grid gets here, i.e. with the
+  // scan all but done: its clusters then find the SMs free and are all placed
+  // in one wave.  (Triggered at the start, they were placed while the SMs
+  // emptied one by one, and the last clusters waited for the first to finish.)
+  grid_dep_launch();
   if (warp == 1) tmem_dealloc(tmem, kTmemCols);
 }
 

@@ -76,11 +76,12 @@ int mla_batch_invariant(int on);
 int mla_max_chunk();
 // The MLA kernel alone over per-row chunk tables: nseg chunks per row,
 // boundaries seg[row][0..nseg] in idx[row], each at most mla_max_chunk()
-// tokens; unnormalised partials to opart [rows][nseg][96][512] and (max, sum
-// of rounded p, sum of p) to ml [rows][nseg][96][4].
+// tokens; partials normalised by their sum of rounded p to opart (fp16 bits)
+// [rows][nseg][96][512] and (max, sum of rounded p, sum of p) to ml
+// [rows][nseg][96][4].
 dsa_status_t launch_sparse_mla_partials(const dsa_paged_cache_t& c, const dsa_batch_t& bt, const uint16_t* q_mla,
                                         const int32_t* idx, int k, const int32_t* seg, int nseg, float sm_scale,
-                                        float* opart, float* ml, int32_t* status, cudaStream_t st);
+                                        uint16_t* opart, float* ml, int32_t* status, cudaStream_t st);
 // phys: the top-k's physical KV rows for idx ([rows][k], -1 padding, already
 // bounds-checked and visible) or nullptr: the kernel translates idx itself.
 dsa_status_t launch_sparse_mla(const dsa_paged_cache_t& c, const dsa_batch_t& bt, const uint16_t* q_mla,

@@ -110,7 +110,7 @@ struct MlaParams {
   int32_t nsplit;
   float logit_scale_log2;  // sm_scale * latent_scale * log2(e)
   const uint16_t* q_mla;   // bf16 [rows][96][576]
-  float* opart;     // [rows][nsplit][96][512]
+  uint16_t* opart;  // fp16 [rows][nsplit][96][512]: the chunk's output normalised by its own sum of bf16(p)
   float* ml;        // [rows][nsplit][96][4]: max (log2), sum of bf16(p), sum of p
   int32_t* status;
   // combining in the kernel: a row's nsplit CTAs form a cluster (fuse = 1)
@@ -144,14 +144,21 @@ __device__ __forceinline__ bool bar_or_softmax(bool v) {
   return r != 0;
 }
 
+// Four fp16 values (bits, low half first) as floats.
+__device__ __forceinline__ float4 half4_to_float4(uint2 v) {
+  const float2 a = __half22float2(*reinterpret_cast<const __half2*>(&v.x));
+  const float2 b = __half22float2(*reinterpret_cast<const __half2*>(&v.y));
+  return make_float4(a.x, a.y, b.x, b.y);
+}
+
 // The in-cluster merge of a row's NS chunks for this CTA's share [v0, v1) of
 // the row's output float4s: every chunk's partial is read from the workspace
-// (L2; U x NS 16-byte loads in flight per thread), weighted and summed in
+// (L2; U x NS 8-byte loads in flight per thread), weighted and summed in
 // chunk order with the combine kernel's arithmetic, and written as bf16.  A
 // zero weight skips its chunk.  (Reading the peers' partials from their shared
 // memory instead was measured slower.)
 template <int NS>
-__device__ __forceinline__ void merge_share(const float* opart_row, const float* wgt, int v0, int v1,
+__device__ __forceinline__ void merge_share(const uint16_t* opart_row, const float* wgt, int v0, int v1,
                                             uint16_t* out_row) {
   constexpr int U = NS >= 8 ? 2 : NS >= 4 ? 4 : NS >= 2 ? 8 : 16;
   for (int vb = v0 + (int)threadIdx.x; vb < v1; vb += U * kThreads) {
@@ -164,7 +171,7 @@ __device__ __forceinline__ void merge_share(const float* opart_row, const float*
 #pragma unroll
         for (int s = 0; s < NS; ++s)
           if (wgt[hh * kMaxFusedSplit + s] != 0.f)
-            x[u][s] = *reinterpret_cast<const float4*>(opart_row + ((int64_t)s * kHeads + hh) * kValue + d);
+            x[u][s] = half4_to_float4(*reinterpret_cast<const uint2*>(opart_row + ((int64_t)s * kHeads + hh) * kValue + d));
       }
     }
 #pragma unroll
@@ -602,9 +609,14 @@ __global__ void __launch_bounds__(kThreads, 1)
       // ---- this chunk's running max and sums per head
       ok = !bar_or_softmax(!ok);
       if (ok && live) ml_mine = make_float4(m_used, l_round, l_exact, 0.f);
+      // the epilogue normalises the chunk's output by its own sum (alpha_s is
+      // free now: the softmax threads are its only users)
+      alpha_s[h] = (live && l_round > 0.f) ? 1.f / l_round : 0.f;
     }
   }
-  // ---- epilogue: the chunk's unnormalised O^T to the workspace, by all twelve
+  // ---- epilogue: the chunk's O^T, normalised by the chunk's sum of the rounded
+  //      probabilities, to the workspace as fp16 (values below 448 x the latent
+  //      scale: 11 significant bits, far inside the bf16 output's 8), by all twelve
   //      warps.  Every MMA has completed: both issuers waited for theirs before
   //      this barrier.  Warp w reads TMEM lanes 32 (w % 4) .. + 31 (dims of each
   //      128-dim block) and the 32-head column groups w / 4 of the four blocks,
@@ -615,7 +627,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int64_t part = (int64_t)row * p.nsplit + split;
   if (threadIdx.x < kHeads) reinterpret_cast<float4*>(p.ml)[part * kHeads + threadIdx.x] = ml_mine;
   if (ntiles > 0 && *abort_flag == 0) {
-    float* op = p.opart + part * kHeads * kValue;
+    uint16_t* op = p.opart + part * kHeads * kValue;
     const int quarter = warp & 3, hg = warp >> 2;
     const uint32_t lane_base = tmem + ((uint32_t)(quarter * 32) << 16) + hg * 32;
     const int dim_in_block = quarter * 32 + lane;
@@ -627,8 +639,11 @@ __global__ void __launch_bounds__(kThreads, 1)
       tmem_ld_wait();
 #pragma unroll
       for (int j = 0; j < 32; ++j) {
-        op[(int64_t)(hg * 32 + j) * kValue + mb * 128 + dim_in_block] = __uint_as_float(o0[j]);
-        op[(int64_t)(hg * 32 + j) * kValue + (mb + 1) * 128 + dim_in_block] = __uint_as_float(o1[j]);
+        const float il = alpha_s[hg * 32 + j];
+        op[(int64_t)(hg * 32 + j) * kValue + mb * 128 + dim_in_block] =
+            __half_as_ushort(__float2half_rn(__uint_as_float(o0[j]) * il));
+        op[(int64_t)(hg * 32 + j) * kValue + (mb + 1) * 128 + dim_in_block] =
+            __half_as_ushort(__float2half_rn(__uint_as_float(o1[j]) * il));
       }
     }
   }
@@ -663,7 +678,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         const float w = (M == -INFINITY || v.x == -INFINITY) ? 0.f : ex2(v.x - M);
         den += w * v.y;
         ex += w * v.z;
-        wgt[h * kMaxFusedSplit + s] = w;
+        wgt[h * kMaxFusedSplit + s] = w * v.y;  // the partial is normalised by v.y
       }
       const float inv = den > 0.f ? p.latent_scale / den : 0.f;
       for (int s = 0; s < p.nsplit; ++s) wgt[h * kMaxFusedSplit + s] *= inv;
@@ -675,7 +690,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     constexpr int kVec = kHeads * kValue / 4;  // float4s of the row's output
     const int v0 = (int)((int64_t)kVec * split / p.nsplit), v1 = (int)((int64_t)kVec * (split + 1) / p.nsplit);
     uint16_t* out_row = p.out + (int64_t)row * kHeads * kValue;
-    const float* opart_row = p.opart + (int64_t)row * p.nsplit * kHeads * kValue;
+    const uint16_t* opart_row = p.opart + (int64_t)row * p.nsplit * kHeads * kValue;
     switch (p.nsplit) {
       case 1: merge_share<1>(opart_row, wgt, v0, v1, out_row); break;
       case 2: merge_share<2>(opart_row, wgt, v0, v1, out_row); break;
@@ -693,7 +708,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 // fp32 LSE (natural log).  CTA (row, group) covers 8 heads; every split's
 // partial of a float4 is loaded before any is added (loads in flight).
 constexpr int kCombineHeads = 8;
-__global__ void __launch_bounds__(256) mla_combine_kernel(const float* __restrict__ opart,
+__global__ void __launch_bounds__(256) mla_combine_kernel(const uint16_t* __restrict__ opart,
                                                            const float* __restrict__ ml, int nsplit,
                                                            float latent_scale, uint16_t* out, float* lse) {
   const int row = blockIdx.y, h0 = blockIdx.x * kCombineHeads;
@@ -711,6 +726,7 @@ __global__ void __launch_bounds__(256) mla_combine_kernel(const float* __restric
       w[s] = (M == -INFINITY || v.x == -INFINITY) ? 0.f : ex2(v.x - M);
       den += w[s] * v.y;
       ex += w[s] * v.z;
+      w[s] *= v.y;  // the partial is normalised by v.y
     }
     const float inv = den > 0.f ? latent_scale / den : 0.f;
     for (int s = 0; s < nsplit; ++s) wgt[threadIdx.x][s] = w[s] * inv;
@@ -721,11 +737,11 @@ __global__ void __launch_bounds__(256) mla_combine_kernel(const float* __restric
   constexpr int kVec = kCombineHeads * kValue / 4;  // 1024 float4s per CTA
   for (int v = threadIdx.x; v < kVec; v += blockDim.x) {
     const int hl = v / (kValue / 4), d = (v % (kValue / 4)) * 4;
-    const float* src = opart + ((int64_t)row * nsplit * kHeads + h0 + hl) * kValue + d;
+    const uint16_t* src = opart + ((int64_t)row * nsplit * kHeads + h0 + hl) * kValue + d;
     float4 x[kMaxSplit];
 #pragma unroll
     for (int s = 0; s < kMaxSplit; ++s)
-      if (s < nsplit && wgt[hl][s] != 0.f) x[s] = *reinterpret_cast<const float4*>(src + (int64_t)s * kHeads * kValue);
+      if (s < nsplit && wgt[hl][s] != 0.f) x[s] = half4_to_float4(*reinterpret_cast<const uint2*>(src + (int64_t)s * kHeads * kValue));
     float4 a = make_float4(0.f, 0.f, 0.f, 0.f);
 #pragma unroll
     for (int s = 0; s < kMaxSplit; ++s)
@@ -799,7 +815,7 @@ static bool batch_invariant() { return g_batch_invariant.load(std::memory_order_
 size_t mla_workspace_bytes(int rows, int k) {
   auto al = [](size_t x) { return (x + 255) & ~size_t(255); };
   const size_t parts = (size_t)rows * mla_nsplit_max(rows, k, batch_invariant());
-  return al(parts * kHeads * kValue * 4) + al(parts * kHeads * 16);
+  return al(parts * kHeads * kValue * 2) + al(parts * kHeads * 16);
 }
 
 namespace {
@@ -808,7 +824,7 @@ namespace {
 // `nsplit` chunks of `chunk` tokens; false if the tensor map cannot be made or
 // the shared-memory size cannot be set.
 bool mla_setup(const dsa_paged_cache_t& c, const dsa_batch_t& bt, const uint16_t* q_mla, const int32_t* idx, int k,
-               int chunk, int nsplit, float sm_scale, float* opart, float* ml, uint16_t* out, float* lse,
+               int chunk, int nsplit, float sm_scale, uint16_t* opart, float* ml, uint16_t* out, float* lse,
                int32_t* status, CUtensorMap* qmap, MlaParams* p) {
   const int rows = bt.batch * bt.queries_per_seq;
   const uint64_t dims[2] = {(uint64_t)kLatent, (uint64_t)rows * kHeads};
@@ -864,7 +880,7 @@ int mla_max_chunk() { return kMaxChunk; }
 
 dsa_status_t launch_sparse_mla_partials(const dsa_paged_cache_t& c, const dsa_batch_t& bt, const uint16_t* q_mla,
                                         const int32_t* idx, int k, const int32_t* seg, int nseg, float sm_scale,
-                                        float* opart, float* ml, int32_t* status, cudaStream_t st) {
+                                        uint16_t* opart, float* ml, int32_t* status, cudaStream_t st) {
   const int rows = bt.batch * bt.queries_per_seq;
   if (rows == 0) return DSA_OK;
   if (nseg < 1 || nseg > kMaxSplit) return DSA_ERR_UNSUPPORTED;
@@ -899,9 +915,9 @@ dsa_status_t launch_sparse_mla(const dsa_paged_cache_t& c, const dsa_batch_t& bt
   const int chunk = ((tiles + nsplit0 - 1) / nsplit0) * kTileTok;
   const int nsplit = (k + chunk - 1) / chunk;
   auto al = [](size_t x) { return (x + 255) & ~size_t(255); };
-  float* opart = static_cast<float*>(workspace);
+  uint16_t* opart = static_cast<uint16_t*>(workspace);
   float* ml = reinterpret_cast<float*>(static_cast<uint8_t*>(workspace) +
-                                       al((size_t)rows * mla_nsplit_max(rows, k, inv) * kHeads * kValue * 4));
+                                       al((size_t)rows * mla_nsplit_max(rows, k, inv) * kHeads * kValue * 2));
   CUtensorMap qmap;
   MlaParams p;
   if (!mla_setup(c, bt, q_mla, idx, k, chunk, nsplit, sm_scale, opart, ml, out, lse, status, &qmap, &p))
@@ -935,7 +951,7 @@ dsa_status_t launch_sparse_mla(const dsa_paged_cache_t& c, const dsa_batch_t& bt
   cfg2.blockDim = dim3(256);
   cfg2.dynamicSmemBytes = 0;
   count_launches(1);
-  if (cuda_status(cudaLaunchKernelEx(&cfg2, mla_combine_kernel, (const float*)opart, (const float*)ml, nsplit,
+  if (cuda_status(cudaLaunchKernelEx(&cfg2, mla_combine_kernel, (const uint16_t*)opart, (const float*)ml, nsplit,
                                      c.latent_scale, out, lse)) != DSA_OK)
     return DSA_ERR_CUDA;
   return launch_status();

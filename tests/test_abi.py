@@ -110,21 +110,21 @@ def test_workspace_sizes(lib):
     ws = lib.dsa_workspace_size(ctypes.byref(b), 2048)
     assert ws >= 32 * 163840 * 4  # holds the scores
     assert lib.dsa_topk_workspace_size(4, 1 << 20, 2048) > 0
-    assert lib.sparse_mla_workspace_size(32, 2048) >= 32 * 96 * 512 * 4
+    assert lib.sparse_mla_workspace_size(32, 2048) >= 32 * 96 * 512 * 2  # fp16 partials
     assert lib.dsa_topk_workspace_size(32, 163840, 2048) == 0  # rows held in shared memory
     assert lib.dsa_topk_workspace_size(4, 100, 0) == 0
     # DCP: one candidate slot of max(ceil(1.5 k / W), k) words per (row, shard), plus counters
     assert lib.dsa_dcp_topk_workspace_size(32, 2048, 8) >= 32 * 8 * 2048 * 4
     assert lib.dsa_dcp_topk_workspace_size(4, 2048, 1) >= 4 * 3072 * 4
     assert lib.dsa_dcp_topk_workspace_size(4, 2048, 9) == 0
-    # DCP LSE combine: the grouped indices plus fp32 partials of 2 pieces per shard (k = 2048)
-    assert lib.dsa_dcp_sparse_mla_workspace_size(32, 2048, 8) >= 32 * 16 * 96 * 512 * 4 + 32 * 2048 * 4
-    assert lib.dsa_dcp_sparse_mla_workspace_size(4, 1024, 3) >= 4 * 3 * 96 * 512 * 4
+    # DCP LSE combine: the grouped indices plus fp16 partials of 2 pieces per shard (k = 2048)
+    assert lib.dsa_dcp_sparse_mla_workspace_size(32, 2048, 8) >= 32 * 16 * 96 * 512 * 2 + 32 * 2048 * 4
+    assert lib.dsa_dcp_sparse_mla_workspace_size(4, 1024, 3) >= 4 * 3 * 96 * 512 * 2
     assert lib.dsa_dcp_sparse_mla_workspace_size(4, 2048, 9) == 0
     # batch-invariant mode: 512-token chunks, so the partials of 200 rows need 4 slots a row
     assert lib.dsa_batch_invariant(1) == 0
     try:
-        assert lib.sparse_mla_workspace_size(200, 2048) >= 200 * 4 * 96 * 512 * 4
+        assert lib.sparse_mla_workspace_size(200, 2048) >= 200 * 4 * 96 * 512 * 2
     finally:
         assert lib.dsa_batch_invariant(0) == 1
     assert lib.sparse_mla_workspace_size(200, 2048) < 200 * 4 * 96 * 512 * 4
