@@ -468,6 +468,49 @@ def main_ours(args):
             "partial_bytes_per_shard_and_row": 96 * 512 * 2 + 96 * 4,
             "max_abs_vs_unsharded": round(diff, 5)}
 
+    # ---- the fused indexer front end on this batch (RMSNorm, the 4096 x 1536 query projection,
+    #      FP8 query, the new tokens into the cache) alone, and the step that owns its cache
+    #      update (front end + step, one call); both write the cache, so they run on a copy
+    fe_block = None
+    if rank == 0:
+        fe = synth.make_frontend(rows, seed=args.seed)
+        t = lambda a: torch.from_numpy(np.ascontiguousarray(a).view(np.int16) if a.dtype == np.uint16
+                                       else np.ascontiguousarray(a)).to(dev)
+        f_cq, f_g, f_w, f_hw, f_lat, f_key = (t(fe.c_q), t(fe.gamma), t(fe.w_iq), t(fe.head_w), t(fe.new_latent),
+                                              t(fe.new_key))
+        pool_copy = dc.cache.pool.clone()
+        f_cache = binding.PagedCache(pool=pool_copy, row_stride=dc.cache.row_stride, latent_off=dc.cache.latent_off,
+                                     index_off=dc.cache.index_off, key_format=dc.cache.key_format,
+                                     latent_scale=dc.cache.latent_scale, latent_format=dc.cache.latent_format)
+        f_qi = torch.empty_like(dc.q_index)
+        f_wo = torch.empty_like(dc.head_w)
+        f_ws = binding.workspace(binding.frontend_workspace_size(dc.batch, k), dev)
+        evf = [[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(n_att)]
+        for e in evf:
+            flush.zero_()
+            e[0].record(stream)
+            binding.index_frontend(f_cache, dc.batch, f_cq, f_g, fe.eps, f_w, f_hw, f_lat, f_key, f_qi, f_wo, status,
+                                   stream=stream)
+            e[1].record(stream)
+        evs2 = [[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(n_att)]
+        for e in evs2:
+            flush.zero_()
+            e[0].record(stream)
+            binding.decode_step_frontend(f_cache, dc.batch, f_cq, f_g, fe.eps, f_w, f_hw, f_lat, f_key, dc.q_mla, k,
+                                         case.sm_scale, out, lse, f_ws, status, stream=stream)
+            e[1].record(stream)
+        torch.cuda.synchronize()
+        assert status.item() == 0, binding.status_string(status.item())
+        fe_us = statistics.median(e[0].elapsed_time(e[1]) for e in evf) * 1e3
+        # bytes the front end must move: the projection weights once, the queries, the
+        # outputs and the new tokens' cache records
+        fe_bytes = (fe.w_iq.nbytes + fe.gamma.nbytes + fe.c_q.nbytes + fe.head_w.nbytes + fe.new_latent.nbytes +
+                    fe.new_key.nbytes + rows * (4096 + 128) + rows * (case.latent_bytes() + case.token_bytes()))
+        fe_block = {"us": round(fe_us, 2), "algorithmic_bytes": int(fe_bytes), "GB/s": round(fe_bytes / fe_us / 1e3, 1),
+                    "q_rank": int(fe.c_q.shape[1]), "launches": 1,
+                    "step_with_frontend_us": round(statistics.median(e[0].elapsed_time(e[1]) for e in evs2) * 1e3, 2)}
+        del pool_copy, f_cache
+
     # ---- end to end through the public call, host buffers, copies inside the timed region:
     #      the step's host inputs packed in one pinned buffer (one host->device copy into a
     #      device buffer whose views are the step's arguments), its outputs in one device
@@ -550,6 +593,7 @@ def main_ours(args):
         "roofline": roof,
         "gpu_launches": n_launches,
         "dcp_topk": dcp,
+        "frontend": fe_block,
         "bf16_scores": b16,
         "clocks": clocks,
         "wall_s_timed_region": round(t_wall, 4),

@@ -181,29 +181,45 @@ __global__ void __launch_bounds__(128)
 
 
 // ---------------------------------------------------------------- fused indexer front end
-// Grid (33, ceil(rows / 64)).  CTA (h < 32, g): the 128 projected values of
-// head h for rows 64 g .. 64 g + 63, as one tcgen05 GEMM D[128 dims x N rows]
-// = W_h[128 x D] xn^T[D x N] (M = 128, N = the rows rounded up to 16, K in
-// 64-element stages): warp 0 streams W_h by TMA (128-byte swizzle), warps 2..5
-// normalise the rows and write each stage's xn tile (the same swizzle), warp 1
-// issues the MMAs; then warps 2..5 (one TMEM lane quarter each: 32 dims) read
-// the fp32 accumulators, take each row's amax over the head's 128 dims and
-// write the FP8 codes and the folded head weight.  CTA (32, g): the new
-// tokens of rows 64 g .. 64 g + 63 into the cache (threads 0..127).
+// Grid (32 * 4 + 64, ceil(rows / 64)), clusters of 4 CTAs along x.  Cluster h
+// (CTAs 4h .. 4h + 3) computes the 128 projected values of head h for rows
+// 64 g .. 64 g + 63 as one tcgen05 GEMM D[128 dims x N rows] = W_h[128 x D]
+// xn^T[D x N] (M = 128, N = the rows rounded up to 16), split over K: CTA rank
+// s takes the 64-element K stages [nk s / 4, nk (s + 1) / 4), so 128 CTAs (two
+// per SM) stream the weights.  In each CTA warp 0 streams its W_h stages and
+// the rows' compressed-query tiles by TMA (128-byte swizzle; rows past the
+// batch read as zeros), warp 1 issues the MMAs, and warps 2..5 first sum the
+// squares of their K range per row (the four ranks' sums are exchanged through
+// distributed shared memory and added in rank order), then turn each stage's
+// query tile into xn in place (scale, gamma, bf16; stage j by warp 2 + j % 4),
+// and finally write their fp32 accumulators to shared memory.  After a cluster
+// barrier rank s adds the four ranks' accumulators (in rank order) for rows
+// 16 s .. 16 s + 15, takes each row's amax over the head's 128 dims and writes
+// the FP8 codes and the folded head weight.  CTA (128 + j, g): the new token of
+// row 64 g + j into the cache (threads 0..127).
 constexpr int kFeRows = 64;
+constexpr int kFeSplit = 4;                               // K ranks per head (the cluster)
 constexpr int kFeStages = 4;
 constexpr int kFeK = 64;                                  // K elements per stage: one 128-byte swizzle row
 constexpr int kFeWBytes = 128 * kFeK * 2;                 // 16 KB
 constexpr int kFeXBytes = kFeRows * kFeK * 2;             // 8 KB
 constexpr int kFeThreads = 192;
+constexpr int kFeMaxDim = 16384;
 constexpr int kFeOffW = 0;
 constexpr int kFeOffX = kFeOffW + kFeStages * kFeWBytes;  // 65,536
 constexpr int kFeOffBars = kFeOffX + kFeStages * kFeXBytes;  // 98,304
-constexpr int kFeNumBars = 3 * kFeStages + 1;             // W full, xn full, stage empty; done
-constexpr int kFeOffNorm = kFeOffBars + kFeNumBars * 8;
-constexpr int kFeOffAmax = kFeOffNorm + kFeRows * 4;
-constexpr int kFeOffMisc = kFeOffAmax + 4 * kFeRows * 4;
+constexpr int kFeNumBars = 4 * kFeStages + 1;             // W full, xn full, stage empty, query tile landed; done
+constexpr int kFeOffSs = (kFeOffBars + kFeNumBars * 8 + 127) / 128 * 128;  // partial sums of squares [64]
+constexpr int kFeOffNorm = kFeOffSs + kFeRows * 4;                        // RMS factors [64]
+constexpr int kFeOffAmax = kFeOffNorm + kFeRows * 4;                      // [4 warps][16 rows]; the writers' amax
+constexpr int kFeOffGamma = kFeOffAmax + 4 * kFeRows * 4;                 // gamma of this rank's K range, bf16
+constexpr int kFeOffMisc = kFeOffGamma + (kFeMaxDim / kFeSplit) * 2;
 constexpr size_t kFeSmem = 1024 + kFeOffMisc + 32;
+constexpr int kFePartBytes = kFeRows * 128 * 4;           // this rank's fp32 accumulators [64 rows][128 dims]
+static_assert(kFePartBytes <= kFeOffBars, "the accumulators reuse the stage buffers");
+static_assert(kFeOffSs % 16 == 0 && kFeOffNorm % 16 == 0 && kFeOffAmax % 16 == 0 && kFeOffGamma % 16 == 0,
+              "16-byte vector accesses");
+static_assert(2 * kFeSmem <= 233472, "two CTAs per SM");
 constexpr int kFeTmemCols = 64;
 
 struct FeParams {
@@ -221,22 +237,35 @@ struct FeParams {
 
 // Named barrier 2 over warps 2..5.
 __device__ __forceinline__ void bar_fe() { asm volatile("bar.sync 2, 128;" ::: "memory"); }
+// The cluster barrier in two halves (every thread of the cluster arrives, then
+// waits), so that warps with other work can arrive early and wait late.
+__device__ __forceinline__ void cluster_arrive() { asm volatile("barrier.cluster.arrive.release.aligned;" ::: "memory"); }
+__device__ __forceinline__ void cluster_wait() { asm volatile("barrier.cluster.wait.acquire.aligned;" ::: "memory"); }
+__device__ __forceinline__ float ld_cluster_f32(uint32_t addr) {
+  float v;
+  asm volatile("ld.shared::cluster.f32 %0, [%1];" : "=f"(v) : "r"(addr) : "memory");
+  return v;
+}
+__device__ __forceinline__ uint32_t cluster_addr(uint32_t saddr, uint32_t rank) {
+  uint32_t r;
+  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(saddr), "r"(rank));
+  return r;
+}
 
-__global__ void __launch_bounds__(kFeThreads, 1)
-    frontend_kernel(const __grid_constant__ CUtensorMap tmap_w, const FeParams p) {
+__global__ void __launch_bounds__(kFeThreads, 2)
+    frontend_kernel(const __grid_constant__ CUtensorMap tmap_w, const __grid_constant__ CUtensorMap tmap_c,
+                    const FeParams p) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int row0 = blockIdx.y * kFeRows;
   const int nrow = min(kFeRows, p.rows - row0);
-  if (blockIdx.x == kIdxHeads) {
-    // ---- the new tokens of this CTA's rows into the cache
+  if (blockIdx.x >= kIdxHeads * kFeSplit) {
+    // ---- the new token of one row into the cache (no cluster barrier here)
+    const int r = blockIdx.x - kIdxHeads * kFeSplit;
     float* warp_amax = reinterpret_cast<float*>(smem + kFeOffAmax);
-    if (threadIdx.x < kAppendThreads)
-      for (int r = 0; r < nrow; ++r) {
-        append_row(p.app, row0 + r, threadIdx.x, warp_amax, [] { bar_append(); });
-        bar_append();  // warp_amax is rewritten by the next row
-      }
+    if (r < nrow && threadIdx.x < kAppendThreads)
+      append_row(p.app, row0 + r, threadIdx.x, warp_amax, [] { bar_append(); });
     return;
   }
   const uint32_t sbase = smem_u32(smem);
@@ -244,24 +273,31 @@ __global__ void __launch_bounds__(kFeThreads, 1)
   auto full_w = [&](int s) { return bars + 8u * s; };
   auto full_x = [&](int s) { return bars + 8u * (kFeStages + s); };
   auto empty = [&](int s) { return bars + 8u * (2 * kFeStages + s); };
-  const uint32_t done = bars + 8u * (3 * kFeStages);
+  auto raw_x = [&](int s) { return bars + 8u * (3 * kFeStages + s); };  // the stage's query tile landed
+  const uint32_t done = bars + 8u * (4 * kFeStages);
+  float* ss_s = reinterpret_cast<float*>(smem + kFeOffSs);
   float* norm = reinterpret_cast<float*>(smem + kFeOffNorm);
-  float* amax_s = reinterpret_cast<float*>(smem + kFeOffAmax);  // [4 warps][64 rows]
+  float* amax_s = reinterpret_cast<float*>(smem + kFeOffAmax);
+  uint16_t* gamma_s = reinterpret_cast<uint16_t*>(smem + kFeOffGamma);
+  float* part = reinterpret_cast<float*>(smem + kFeOffW);    // [64 rows][128 dims], after the MMAs
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + kFeOffMisc);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + kFeOffMisc + 4);
-  const int h = blockIdx.x;
+  const int h = blockIdx.x / kFeSplit, rank = blockIdx.x % kFeSplit;  // clusters are 4 consecutive CTAs along x
   const int n_mma = max(16, (nrow + 15) & ~15);
   const int nk = p.dim / kFeK;
+  const int kc0 = nk * rank / kFeSplit, nkm = nk * (rank + 1) / kFeSplit - kc0;  // this rank's K stages
   if (threadIdx.x == 0) {
     for (int s = 0; s < kFeStages; ++s) {
       mbar_init(full_w(s), 1);
-      mbar_init(full_x(s), 4);
+      mbar_init(full_x(s), 1);
       mbar_init(empty(s), 1);
+      mbar_init(raw_x(s), 1);
     }
     mbar_init(done, 1);
     *abort_flag = 0;
     fence_mbar_init();
     prefetch_tmap(&tmap_w);
+    prefetch_tmap(&tmap_c);
   }
   if (warp == 1) {
     tmem_alloc(smem_u32(tmem_slot), kFeTmemCols);
@@ -272,133 +308,195 @@ __global__ void __launch_bounds__(kFeThreads, 1)
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
 
-  if (warp == 0) {
-    if (lane == 0) {
-      // ------------------------------------------------ W_h stages by TMA
+  if (warp < 2) {
+    cluster_arrive();  // phase 1 (the sums of squares): nothing to give
+    if (warp == 0 && lane == 0) {
+      // ------------------------------------------------ this rank's W_h and query stages by TMA
       int issued = 0;
-      for (int kc = 0; kc < nk; ++kc) {
-        const int s = kc % kFeStages;
-        if (!mbar_wait(empty(s), ((kc / kFeStages) & 1) ^ 1, abort_flag, p.app.status)) break;
+      for (int j = 0; j < nkm; ++j) {
+        const int s = j % kFeStages, kc = kc0 + j;
+        if (!mbar_wait(empty(s), ((j / kFeStages) & 1) ^ 1, abort_flag, p.app.status)) break;
         mbar_arrive_expect_tx(full_w(s), kFeWBytes);
         tma_load_2d(sbase + kFeOffW + s * kFeWBytes, &tmap_w, kc * kFeK, h * 128, full_w(s));
+        mbar_arrive_expect_tx(raw_x(s), kFeXBytes);
+        tma_load_2d(sbase + kFeOffX + s * kFeXBytes, &tmap_c, kc * kFeK, row0, raw_x(s));
         ++issued;
       }
-      // the copies still in flight land before the CTA exits (all of them have
-      // landed already unless another role gave up)
-      for (int kc = max(0, issued - kFeStages); kc < issued; ++kc)
-        mbar_wait_drain(full_w(kc % kFeStages), (kc / kFeStages) & 1, 100000000ull);
-    }
-  } else if (warp == 1) {
-    if (lane == 0) {
+      // the copies still in flight land before the buffers are reused (all of
+      // them have landed already unless another role gave up)
+      for (int j = max(0, issued - kFeStages); j < issued; ++j) {
+        mbar_wait_drain(full_w(j % kFeStages), (j / kFeStages) & 1, 100000000ull);
+        mbar_wait_drain(raw_x(j % kFeStages), (j / kFeStages) & 1, 100000000ull);
+      }
+    } else if (warp == 1 && lane == 0) {
       // ------------------------------------------------ MMA issuer
       const uint32_t idesc = make_idesc(kFmtBF16, kFmtBF16, 0, 0, 128, (uint32_t)n_mma);
-      bool ok = true;
-      for (int kc = 0; kc < nk && ok; ++kc) {
-        const int s = kc % kFeStages;
-        ok = mbar_wait(full_w(s), (kc / kFeStages) & 1, abort_flag, p.app.status) &&
-             mbar_wait(full_x(s), (kc / kFeStages) & 1, abort_flag, p.app.status);
-        if (!ok) break;
+      for (int j = 0; j < nkm; ++j) {
+        const int s = j % kFeStages;
+        if (!(mbar_wait(full_w(s), (j / kFeStages) & 1, abort_flag, p.app.status) &&
+              mbar_wait(full_x(s), (j / kFeStages) & 1, abort_flag, p.app.status)))
+          break;
         tc_fence_after();
         const uint32_t a0 = sbase + kFeOffW + s * kFeWBytes, b0 = sbase + kFeOffX + s * kFeXBytes;
 #pragma unroll
         for (int kk = 0; kk < kFeK / 16; ++kk)
           mma_bf16(tmem, smem_desc(a0 + 32 * kk, 16, 1024, kLayoutSw128), smem_desc(b0 + 32 * kk, 16, 1024, kLayoutSw128),
-                   idesc, (kc | kk) ? 1u : 0u);
+                   idesc, (j | kk) ? 1u : 0u);
         mma_commit(empty(s));
       }
       mma_commit(done);  // also after an abort: every issued MMA completes before TMEM is released
     }
+    __syncwarp();
+    cluster_wait();    // phase 1
+    cluster_arrive();  // phase 2 (the accumulators): nothing to give
+    cluster_wait();
+    cluster_arrive();  // phase 3 (the peers have read the accumulators)
+    cluster_wait();
   } else {
-    // ------------------------------------------------ norm, xn stages, epilogue
+    // ------------------------------------------------ warps 2..5
     const int t = threadIdx.x - 64, eq = warp - 2;
-    // 1 / sqrt(mean(c^2) + eps) per row, one warp per row
-    for (int r = eq; r < nrow; r += 4) {
-      const uint16_t* c = p.c_q + (int64_t)(row0 + r) * p.dim;
-      float ss = 0.f;
-      for (int i = 8 * lane; i < p.dim; i += 256) {
-        const uint4 v = *reinterpret_cast<const uint4*>(c + i);
-        const uint32_t w4[4] = {v.x, v.y, v.z, v.w};
+    const float hw_t = t < nrow ? p.head_w[(int64_t)(row0 + t) * kIdxHeads + h] : 0.f;
+    // gamma of this rank's K range into shared memory
+    for (int i = t; i < nkm * (kFeK / 8); i += 128)
+      reinterpret_cast<uint4*>(gamma_s)[i] = reinterpret_cast<const uint4*>(p.gamma + kc0 * kFeK)[i];
+    // this rank's part of sum(c^2) per row: a warp takes four rows at a time,
+    // every lane's 16-byte loads of all four (up to 6 of each) in flight first
+    auto sq_acc = [](const uint4& v, float& ss) {
+      const uint32_t w4[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+      for (int q = 0; q < 4; ++q) {
+        const float lo = __uint_as_float(w4[q] << 16), hi = __uint_as_float(w4[q] & 0xFFFF0000u);
+        ss = fmaf(lo, lo, ss);
+        ss = fmaf(hi, hi, ss);
+      }
+    };
+    const int nv = nkm * (kFeK / 8);  // 16-byte chunks of a row in this rank's range
+    for (int rb = eq; rb < kFeRows; rb += 16) {
+      float ss[4] = {0.f, 0.f, 0.f, 0.f};
+      for (int j0 = lane; j0 < nv; j0 += 6 * 32) {
+        uint4 v[4][6];
 #pragma unroll
         for (int q = 0; q < 4; ++q) {
-          const float lo = __uint_as_float(w4[q] << 16), hi = __uint_as_float(w4[q] & 0xFFFF0000u);
-          ss = fmaf(lo, lo, ss);
-          ss = fmaf(hi, hi, ss);
+          const int r = rb + 4 * q;
+          const uint4* c = reinterpret_cast<const uint4*>(p.c_q + (int64_t)(row0 + min(r, nrow - 1)) * p.dim + kc0 * kFeK);
+#pragma unroll
+          for (int j = 0; j < 6; ++j) {
+            const int jj = j0 + 32 * j;
+            v[q][j] = (r < nrow && jj < nv) ? c[jj] : make_uint4(0u, 0u, 0u, 0u);
+          }
         }
+#pragma unroll
+        for (int q = 0; q < 4; ++q)
+#pragma unroll
+          for (int j = 0; j < 6; ++j) sq_acc(v[q][j], ss[q]);
       }
 #pragma unroll
-      for (int o = 16; o > 0; o >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, o);
-      if (lane == 0) norm[r] = 1.0f / sqrtf(ss / (float)p.dim + p.eps);
+      for (int q = 0; q < 4; ++q) {
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) ss[q] += __shfl_xor_sync(0xffffffffu, ss[q], o);
+        if (lane == 0) ss_s[rb + 4 * q] = ss[q];
+      }
+    }
+    cluster_arrive();  // phase 1: this rank's sums of squares are written
+    cluster_wait();
+    // the RMS factors from the four ranks' sums, added in rank order (0 for the
+    // zero rows past the batch)
+    if (t < kFeRows) {
+      float tot = 0.f;
+#pragma unroll
+      for (int q = 0; q < kFeSplit; ++q) tot += ld_cluster_f32(cluster_addr(smem_u32(ss_s + t), (uint32_t)q));
+      norm[t] = t < nrow ? 1.0f / sqrtf(tot / (float)p.dim + p.eps) : 0.f;
     }
     bar_fe();
-    // xn stages: row r, 16-byte chunk cc (8 elements) of the stage's 64
+    // xn stages: each landed query tile (rows x 64 elements, 128-byte swizzle)
+    // is scaled in place by one warp (stage j by warp 2 + j % 4, so that the
+    // proxy fences of four stages overlap).  Lane l takes the 16-byte chunks at
+    // physical column pc = l % 8 of rows l / 8 + 4 i, whose logical column is
+    // pc ^ (row % 8).
+    const int pc = lane & 7;
     bool ok = true;
-    for (int kc = 0; kc < nk; ++kc) {
-      const int s = kc % kFeStages;
-      ok = mbar_wait(empty(s), ((kc / kFeStages) & 1) ^ 1, abort_flag, p.app.status);
+    for (int j = eq; j < nkm; j += 4) {
+      const int s = j % kFeStages;
+      ok = mbar_wait(raw_x(s), (j / kFeStages) & 1, abort_flag, p.app.status);
       if (!__all_sync(0xffffffffu, ok)) { ok = false; break; }
       uint8_t* xs = smem + kFeOffX + s * kFeXBytes;
-      for (int idx = t; idx < n_mma * 8; idx += 128) {
-        const int r = idx >> 3, cc = idx & 7;
-        uint4 o = make_uint4(0u, 0u, 0u, 0u);
-        if (r < nrow) {
-          const int e0 = kc * kFeK + 8 * cc;
-          const uint4 cv = *reinterpret_cast<const uint4*>(p.c_q + (int64_t)(row0 + r) * p.dim + e0);
-          const uint4 gv = *reinterpret_cast<const uint4*>(p.gamma + e0);
-          const float nr = norm[r];
-          const uint32_t c4[4] = {cv.x, cv.y, cv.z, cv.w}, g4[4] = {gv.x, gv.y, gv.z, gv.w};
-          uint32_t o4[4];
+      const uint4* gk = reinterpret_cast<const uint4*>(gamma_s + j * kFeK);
+#pragma unroll 4
+      for (int r = lane >> 3; r < n_mma; r += 4) {
+        uint4* cell = reinterpret_cast<uint4*>(xs + r * 128 + pc * 16);
+        const uint4 cv = *cell;
+        const uint4 gv = gk[pc ^ (r & 7)];
+        const float nr = norm[r];
+        const uint32_t c4[4] = {cv.x, cv.y, cv.z, cv.w}, g4[4] = {gv.x, gv.y, gv.z, gv.w};
+        uint32_t o4[4];
 #pragma unroll
-          for (int q = 0; q < 4; ++q) {
-            const float lo = __uint_as_float(c4[q] << 16) * nr * __uint_as_float(g4[q] << 16);
-            const float hi = __uint_as_float(c4[q] & 0xFFFF0000u) * nr * __uint_as_float(g4[q] & 0xFFFF0000u);
-            const __nv_bfloat162 b2 = __floats2bfloat162_rn(lo, hi);
-            o4[q] = *reinterpret_cast<const uint32_t*>(&b2);
-          }
-          o = make_uint4(o4[0], o4[1], o4[2], o4[3]);
+        for (int q = 0; q < 4; ++q) {
+          const float lo = __uint_as_float(c4[q] << 16) * nr * __uint_as_float(g4[q] << 16);
+          const float hi = __uint_as_float(c4[q] & 0xFFFF0000u) * nr * __uint_as_float(g4[q] & 0xFFFF0000u);
+          const __nv_bfloat162 b2 = __floats2bfloat162_rn(lo, hi);
+          o4[q] = *reinterpret_cast<const uint32_t*>(&b2);
         }
-        *reinterpret_cast<uint4*>(xs + swz128((uint32_t)(r * 128 + cc * 16))) = o;
+        *cell = make_uint4(o4[0], o4[1], o4[2], o4[3]);
       }
       fence_proxy_async_smem();
       __syncwarp();
       if (lane == 0) mbar_arrive(full_x(s));
     }
-    // ---- epilogue: TMEM lane = dim 32 (warp % 4) + lane of the head, column = row
+    ok = !__any_sync(0xffffffffu, !ok);
+    // ---- this rank's accumulators into shared memory (zeros for a rank with no
+    //      K stage): TMEM lane = dim 32 (warp % 4) + lane, column = row
     const bool fin = mbar_wait(done, 0, abort_flag, p.app.status) && ok;
     tc_fence_after();
     const int quarter = warp & 3, d = quarter * 32 + lane;
-    float v[kFeRows];
     {
       uint32_t r0[32], r1[32];
       const uint32_t ta = tmem + ((uint32_t)(quarter * 32) << 16);
       tmem_ld32(ta, r0);
       tmem_ld32(ta + 32, r1);
       tmem_ld_wait();
+      const bool have = fin && nkm > 0;
 #pragma unroll
       for (int j = 0; j < 32; ++j) {
-        v[j] = __uint_as_float(r0[j]);
-        v[32 + j] = __uint_as_float(r1[j]);
+        part[j * 128 + d] = have ? __uint_as_float(r0[j]) : 0.f;
+        part[(32 + j) * 128 + d] = have ? __uint_as_float(r1[j]) : 0.f;
       }
     }
-    if (fin) {
+    cluster_arrive();  // phase 2: this rank's accumulators are written
+    cluster_wait();
+    // ---- rows 16 rank .. + 15: the four ranks' accumulators added in rank
+    //      order, each row's amax over the head's 128 dims, the FP8 codes and
+    //      the folded head weight
+    const uint32_t part_u = smem_u32(part);
+    float v[16];
 #pragma unroll
-      for (int r = 0; r < kFeRows; ++r) {
-        if (r >= nrow) break;
-        if (p.q_proj) p.q_proj[(int64_t)(row0 + r) * (kIdxHeads * kIdxDim) + h * kIdxDim + d] = v[r];
-        const uint32_t m = __reduce_max_sync(0xffffffffu, __float_as_uint(fabsf(v[r])));  // |v| bits order as |v|
-        if (lane == 0) amax_s[quarter * kFeRows + r] = __uint_as_float(m);
-      }
+    for (int i = 0; i < 16; ++i) {
+      const int r = 16 * rank + i;
+      float a = 0.f;
+#pragma unroll
+      for (int q = 0; q < kFeSplit; ++q) a += ld_cluster_f32(cluster_addr(part_u + (uint32_t)(r * 128 + d) * 4u, (uint32_t)q));
+      v[i] = a;
+    }
+    cluster_arrive();  // phase 3: the peers' accumulators are read
+#pragma unroll
+    for (int i = 0; i < 16; ++i) {
+      const int r = 16 * rank + i;
+      if (r >= nrow) break;
+      if (p.q_proj) p.q_proj[(int64_t)(row0 + r) * (kIdxHeads * kIdxDim) + h * kIdxDim + d] = v[i];
+      const uint32_t m = __reduce_max_sync(0xffffffffu, __float_as_uint(fabsf(v[i])));  // |v| bits order as |v|
+      if (lane == 0) amax_s[eq * 16 + i] = __uint_as_float(m);
     }
     bar_fe();
-    if (fin) {
+    const bool good = !*abort_flag;
 #pragma unroll
-      for (int r = 0; r < kFeRows; ++r) {
-        if (r >= nrow) break;
-        const float amax = fmaxf(fmaxf(amax_s[r], amax_s[kFeRows + r]), fmaxf(amax_s[2 * kFeRows + r], amax_s[3 * kFeRows + r]));
-        const float sc = amax > 0.f ? amax / 448.0f : 1.0f;
-        p.q_index[(int64_t)(row0 + r) * (kIdxHeads * kIdxDim) + h * kIdxDim + d] = e4m3(v[r] / sc);
-        if (t == r) p.head_w_out[(int64_t)(row0 + r) * kIdxHeads + h] = p.head_w[(int64_t)(row0 + r) * kIdxHeads + h] * sc;
-      }
+    for (int i = 0; i < 16; ++i) {
+      const int r = 16 * rank + i;
+      if (r >= nrow || !good) break;
+      const float amax = fmaxf(fmaxf(amax_s[i], amax_s[16 + i]), fmaxf(amax_s[32 + i], amax_s[48 + i]));
+      const float sc = amax > 0.f ? amax / 448.0f : 1.0f;
+      p.q_index[(int64_t)(row0 + r) * (kIdxHeads * kIdxDim) + h * kIdxDim + d] = e4m3(v[i] / sc);
+      if (t == r) p.head_w_out[(int64_t)(row0 + r) * kIdxHeads + h] = hw_t * sc;
     }
+    cluster_wait();    // phase 3: no peer reads this rank's accumulators any more
   }
   tc_fence_before();
   __syncthreads();
@@ -443,6 +541,12 @@ dsa_status_t launch_frontend(const dsa_paged_cache_t& c, const dsa_batch_t& bt, 
   const uint32_t box[2] = {(uint32_t)kFeK, 128u};
   if (!encode_tmap(&wmap, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, w_iq, dims, strides, box, CU_TENSOR_MAP_SWIZZLE_128B))
     return DSA_ERR_CUDA;
+  // the compressed queries, 64 rows x 64 elements a box; rows past the batch read as zeros
+  CUtensorMap cmap;
+  const uint64_t cdims[2] = {(uint64_t)dim, (uint64_t)rows};
+  const uint32_t cbox[2] = {(uint32_t)kFeK, (uint32_t)kFeRows};
+  if (!encode_tmap(&cmap, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, c_q, cdims, strides, cbox, CU_TENSOR_MAP_SWIZZLE_128B))
+    return DSA_ERR_CUDA;
   static std::atomic<bool> attr_set[64];
   int dev = 0;
   cudaGetDevice(&dev);
@@ -467,9 +571,20 @@ dsa_status_t launch_frontend(const dsa_paged_cache_t& c, const dsa_batch_t& bt, 
                      c.latent_format, c.latent_scale, bt.block_table, bt.max_blocks_per_seq, bt.seq_lens,
                      bt.queries_per_seq, std::min(bt.max_blocks_per_seq * kBlock, bt.max_seq_len), new_latent,
                      new_key, status};
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = kFeSplit;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(kIdxHeads * kFeSplit + kFeRows, (unsigned)((rows + kFeRows - 1) / kFeRows));
+  cfg.blockDim = dim3(kFeThreads);
+  cfg.dynamicSmemBytes = kFeSmem;
+  cfg.stream = st;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
   count_launches(1);
-  frontend_kernel<<<dim3(kIdxHeads + 1, (unsigned)((rows + kFeRows - 1) / kFeRows)), kFeThreads, kFeSmem, st>>>(
-      wmap, p);
+  if (cuda_status(cudaLaunchKernelEx(&cfg, frontend_kernel, wmap, cmap, p)) != DSA_OK) return DSA_ERR_CUDA;
   return launch_status();
 }
 

@@ -299,6 +299,8 @@ WORKLOADS = {
                                    latent_format=LATENT_NVFP4),
     # chunked-prefill append: 2048 new query rows on a 151,552-token prefix
     "prefill_q2048_l153600": dict(seq_lens=[153600], nq=2048),
+    # a smaller chunk of the same context for profiler captures (scores still larger than L2)
+    "prefill_q256_l153600": dict(seq_lens=[153600], nq=256),
 }
 
 
