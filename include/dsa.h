@@ -331,8 +331,9 @@ dsa_status_t dsa_dcp_sparse_mla(const dsa_paged_cache_t* cache, const dsa_batch_
  * are optional (NULL: kept in the workspace only).  phys_out receives the
  * physical KV row of each selected token, block_table[b][t / 64] * 64 + t % 64
  * (-1 beside -1 padding): the rows the attention reads (same section: the
- * fused indexer outputs the physical KV rows that attention reads).  The MLA
- * kernel reads those rows instead of translating the indices again.
+ * fused indexer outputs the physical KV rows that attention reads).  When
+ * phys_out is given the MLA kernel reads those rows instead of translating the
+ * indices again.
  *   workspace >= dsa_workspace_size(batch, k) bytes, 256-B aligned
  */
 size_t dsa_workspace_size(const dsa_batch_t* batch, int32_t k);
