@@ -240,7 +240,7 @@ def stage_roofline(case, st_ms, traffic=None):
               "topk": {"us": round(st_ms["topk"] * 1e3, 2)},
               "mla": {"us": round(st_ms["mla"] * 1e3, 2), "GB/s": round(mla_gbs, 1), "TFLOP/s": round(mla_tf, 1)}}
     if case.nq > 4 and st_ms["index"] >= st_ms["mla"]:
-        roof = {"kernel": "indexer_kernel (dsa_index_scores)", "bound": "tensor", "achieved": round(idx_tf, 1),
+        roof = {"kernel": "prefill_indexer_kernel (dsa_index_scores)", "bound": "tensor", "achieved": round(idx_tf, 1),
                 "peak": 2 * bf16_peak, "peak_kind": bf16_kind + " bf16 x 2 (fp8)", "unit": "TFLOP/s",
                 "frac": round(idx_tf / (2 * bf16_peak), 4), "traffic": None, "algorithmic_flops": idx_fl}
     elif st_ms["mla"] > st_ms["index"]:

@@ -86,12 +86,12 @@ dsa_status_t check_batch(const dsa_batch_t* b) {
 }
 
 // Row shapes the indexer takes: MXFP4 keys one row per sequence; more than 4
-// rows per sequence (a prefill chunk) in groups of 4, at most 4096 groups.
+// rows per sequence (a prefill chunk) a multiple of 4; at most 4096 sequences.
 dsa_status_t check_index_rows(const dsa_paged_cache_t* c, const dsa_batch_t* b) {
   const int nq = b->queries_per_seq;
   if (c->key_format == DSA_KEY_MXFP4 && nq != 1) return DSA_ERR_UNSUPPORTED;
   if (nq > 4 && nq % 4 != 0) return DSA_ERR_UNSUPPORTED;
-  if ((int64_t)b->batch * (nq > 4 ? nq / 4 : 1) > 4096) return DSA_ERR_UNSUPPORTED;
+  if (b->batch > 4096) return DSA_ERR_UNSUPPORTED;
   return DSA_OK;
 }
 

@@ -76,13 +76,6 @@ struct IdxParams {
   float* scores;
   int64_t ld;
   int32_t* status;
-  // A sequence with nq_real query rows runs as `groups` pseudo-sequences of NQ
-  // rows each (decode: groups = 1, nq_real = NQ).  Pseudo-sequence b of real
-  // sequence b / groups has length L - nq_real + NQ * (b % groups + 1), so its
-  // row q sees L - (nq_real - 1) + NQ * (b % groups) + q tokens: the causal
-  // rows of a prefill chunk.
-  int32_t groups;
-  int32_t nq_real;
   int32_t score_bf16;  // scores are bf16 (round to nearest even) at (uint16_t*)scores, else fp32
 };
 
@@ -198,19 +191,11 @@ __global__ void __launch_bounds__(idx_threads<MX>(), 1)
     tmem_alloc(smem_u32(tmem_slot), kTmemCols);
     tmem_relinquish();
   }
-  const int nb = p.batch * p.groups;  // pseudo-sequences
-  // length of pseudo-sequence b (the real length clamped to [0, cap], then the
-  // group's causal prefix)
-  const bool grouped = p.groups > 1;
-  auto real_seq = [&](int b) { return grouped ? b / p.groups : b; };
+  const int nb = p.batch;
+  // length of sequence b, clamped to [0, cap]
   auto seq_len_of = [&](int b) {
-    int len = p.seq_lens[real_seq(b)];
-    len = len < 0 ? 0 : (len > cap ? cap : len);
-    if (grouped) {
-      len += NQ * (b % p.groups + 1) - p.nq_real;
-      len = len < 0 ? 0 : len;
-    }
-    return len;
+    const int len = p.seq_lens[b];
+    return len < 0 ? 0 : (len > cap ? cap : len);
   };
   if (warp == 0) {
     int run = 0;
@@ -218,7 +203,7 @@ __global__ void __launch_bounds__(idx_threads<MX>(), 1)
       int b = b0 + lane;
       int units = 0;
       if (b < nb) {
-        const int raw = p.seq_lens[real_seq(b)];
+        const int raw = p.seq_lens[b];
         if (raw < 0 || raw > cap) report(p.status, DSA_ERR_BOUNDS);
         units = (seq_len_of(b) + kUnitKeys - 1) / kUnitKeys;
       }
@@ -271,7 +256,7 @@ __global__ void __launch_bounds__(idx_threads<MX>(), 1)
           const int j = (int)(u - prefix[rb]);
           const int rem = seq_len_of(rb) - kUnitKeys * j;
           rnp = min(kPagesPerUnit, (rem + kBlock - 1) / kBlock);
-          const int32_t* bt = p.block_table + (int64_t)real_seq(rb) * p.max_blocks + kPagesPerUnit * j;
+          const int32_t* bt = p.block_table + (int64_t)rb * p.max_blocks + kPagesPerUnit * j;
 #pragma unroll
           for (int q = 0; q < kPagesPerUnit; ++q) rr[q] = q < rnp ? bt[q] : 0;
         }
@@ -535,10 +520,10 @@ dsa_status_t launch_nq(const IdxParams& p, const CUtensorMap& keys, const CUtens
       return DSA_ERR_CUDA;
     attr_set[dev] = true;
   }
-  const int64_t units_bound = (int64_t)p.batch * p.groups * ((p.max_seq_len + kUnitKeys - 1) / kUnitKeys);
+  const int64_t units_bound = (int64_t)p.batch * ((p.max_seq_len + kUnitKeys - 1) / kUnitKeys);
   const int grid = (int)std::max<int64_t>(1, std::min<int64_t>(units_bound, num_sms()));
   count_launches(1);
-  indexer_kernel<NQ, MX><<<grid, idx_threads<MX>(), IdxSmem<NQ>::bytes(p.batch * p.groups), st>>>(keys, scales, q, p);
+  indexer_kernel<NQ, MX><<<grid, idx_threads<MX>(), IdxSmem<NQ>::bytes(p.batch), st>>>(keys, scales, q, p);
   return launch_status();
 }
 
@@ -550,10 +535,11 @@ dsa_status_t launch_index_scores(const dsa_paged_cache_t& c, const dsa_batch_t& 
   const bool mx = c.key_format == DSA_KEY_MXFP4;
   const int nq = bt.queries_per_seq;
   if (mx && nq != 1) return DSA_ERR_UNSUPPORTED;
-  // more than 4 rows per sequence (a prefill chunk): groups of 4 causal rows
+  // more than 4 rows per sequence (a prefill chunk): a multiple of 4 rows, scored by
+  // the dense-contraction kernel of prefill.cu
   if (nq > 4 && nq % 4 != 0) return DSA_ERR_UNSUPPORTED;
-  const int nq_k = nq > 4 ? 4 : nq, groups = nq / nq_k;
-  if ((int64_t)bt.batch * groups > kMaxBatch) return DSA_ERR_UNSUPPORTED;
+  if (nq > 4) return launch_prefill_scores(c, bt, q_index, head_w, scores, bf16, ld, status, st);
+  if (bt.batch > kMaxBatch) return DSA_ERR_UNSUPPORTED;
   const uint8_t* index_base = static_cast<const uint8_t*>(c.base) + c.index_off;
   const int code_bytes = mx ? kIdxDim / 2 : kIdxDim;  // per token
   CUtensorMap keys, scales, qmap;
@@ -580,16 +566,15 @@ dsa_status_t launch_index_scores(const dsa_paged_cache_t& c, const dsa_batch_t& 
     const uint64_t rows = (uint64_t)bt.batch * nq * kIdxHeads;
     const uint64_t dims[2] = {(uint64_t)kIdxDim, rows};
     const uint64_t strides[1] = {(uint64_t)kIdxDim};
-    const uint32_t box[2] = {(uint32_t)kIdxDim, (uint32_t)(kIdxHeads * nq_k)};
+    const uint32_t box[2] = {(uint32_t)kIdxDim, (uint32_t)(kIdxHeads * nq)};
     if (!encode_tmap(&qmap, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, q_index, dims, strides, box,
                      CU_TENSOR_MAP_SWIZZLE_128B))
       return DSA_ERR_CUDA;
   }
   IdxParams p{index_base, c.row_stride, c.num_blocks, bt.block_table, bt.max_blocks_per_seq, bt.seq_lens,
-              bt.batch, bt.max_seq_len, head_w, static_cast<float*>(scores), ld, status, groups, nq,
-              bf16 ? 1 : 0};
+              bt.batch, bt.max_seq_len, head_w, static_cast<float*>(scores), ld, status, bf16 ? 1 : 0};
   if (mx) return launch_nq<1, true>(p, keys, scales, qmap, st);
-  switch (nq_k) {
+  switch (nq) {
     case 1: return launch_nq<1, false>(p, keys, scales, qmap, st);
     case 2: return launch_nq<2, false>(p, keys, scales, qmap, st);
     case 3: return launch_nq<3, false>(p, keys, scales, qmap, st);

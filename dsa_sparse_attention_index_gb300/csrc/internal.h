@@ -35,6 +35,11 @@ dsa_status_t launch_translate_pages(const dsa_paged_cache_t& c, const dsa_batch_
 dsa_status_t launch_index_scores(const dsa_paged_cache_t& c, const dsa_batch_t& bt, const uint8_t* q_index,
                                  const float* head_w, void* scores, bool bf16, int64_t ld, int32_t* status,
                                  cudaStream_t st);
+// The same scores for a prefill chunk (FP8 keys, at least 8 rows per sequence):
+// the dense-contraction kernel of prefill.cu.
+dsa_status_t launch_prefill_scores(const dsa_paged_cache_t& c, const dsa_batch_t& bt, const uint8_t* q_index,
+                                   const float* head_w, void* scores, bool bf16, int64_t ld, int32_t* status,
+                                   cudaStream_t st);
 size_t topk_workspace_bytes(int rows, int max_row_len, int k);
 // Optional physical KV rows beside the top-k's token indices: phys[r][p] =
 // block_table[r / nq][t / 64] * 64 + t % 64 for the index t at position p

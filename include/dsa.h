@@ -166,7 +166,11 @@ dsa_status_t dsa_translate_pages(const dsa_paged_cache_t* cache, const dsa_batch
  * and scale_t = 1.  Tensor-core accumulation is fp32.
  * rows = batch * queries_per_seq.  MXFP4 keys take one row per sequence, and
  * more than 4 rows per sequence must be a multiple of 4; otherwise, and when
- * batch * queries_per_seq / 4 exceeds 4096, DSA_ERR_UNSUPPORTED.
+ * batch exceeds 4096 sequences, DSA_ERR_UNSUPPORTED.  Up to 4 rows per
+ * sequence share each key read in the decode kernel; a prefill chunk (more
+ * than 4 rows, FP8 keys) runs as a dense contraction of 8-row query groups
+ * against 512-key blocks (prefill section: the indexer scores every query row
+ * of the chunk against the whole context).
  */
 dsa_status_t dsa_index_scores(const dsa_paged_cache_t* cache, const dsa_batch_t* batch,
                               const uint8_t* q_index, const float* head_w,
