@@ -32,14 +32,15 @@ import numpy as np
 BLOCK = 64
 IDX_HEADS, IDX_DIM = 32, 128
 MLA_HEADS, LATENT, VALUE = 96, 576, 512
-KEY_FP8, KEY_MXFP4 = 0, 1
+KEY_FP8, KEY_MXFP4, KEY_MXFP4_NATIVE = 0, 1, 2   # native: MXFP4 keys and an MXFP4 query
 LATENT_FP8, LATENT_NVFP4 = 0, 1
 
 LATENT_RECORD = {LATENT_FP8: LATENT,              # 576 B: E4M3 codes
                  LATENT_NVFP4: VALUE // 2 + VALUE // 16 + (LATENT - VALUE)}  # 352 B: E2M1 + E4M3 scales + E4M3 tail
 LATENT_PAGE = BLOCK * LATENT                      # 36,864 B (FP8 latents)
 INDEX_PAGE = {KEY_FP8: BLOCK * (IDX_DIM + 4),     # 8,448 B
-              KEY_MXFP4: BLOCK * (IDX_DIM // 2 + 4)}  # 4,352 B
+              KEY_MXFP4: BLOCK * (IDX_DIM // 2 + 4),  # 4,352 B
+              KEY_MXFP4_NATIVE: BLOCK * (IDX_DIM // 2 + 4)}
 
 _E2M1_GRID = np.array([0.0, 0.5, 1.0, 1.5, 2.0, 3.0, 4.0, 6.0])
 _E2M1_MID = (_E2M1_GRID[1:] + _E2M1_GRID[:-1]) / 2   # 0.25 0.75 1.25 1.75 2.5 3.5 5
@@ -53,7 +54,7 @@ class Case:
     batch: int
     nq: int                     # query rows per sequence (speculative draft size)
     seq_lens: np.ndarray        # int32 [batch], context incl. the current token(s)
-    key_format: int             # KEY_FP8 or KEY_MXFP4
+    key_format: int             # KEY_FP8, KEY_MXFP4 or KEY_MXFP4_NATIVE
     topk: int
     pool: np.ndarray            # uint8 [num_blocks, row_stride]
     row_stride: int
@@ -61,7 +62,7 @@ class Case:
     index_off: int
     latent_scale: float
     block_table: np.ndarray     # int32 [batch, max_blocks]; -1 = unallocated
-    q_index: np.ndarray         # uint8 (E4M3 codes) [rows, 32, 128]
+    q_index: np.ndarray         # uint8: E4M3 codes [rows, 32, 128]; native FP4: codes [rows, 32, 64] then E8M0 [rows, 32, 4], flat
     head_w: np.ndarray          # float32 [rows, 32]
     q_mla: np.ndarray           # uint16 (bf16 bits) [rows, 96, 576]
     sm_scale: float
@@ -135,6 +136,15 @@ def mxfp4_encode(x: np.ndarray):
     return packed, e8m0
 
 
+def mxfp4_query_encode(q: np.ndarray) -> np.ndarray:
+    """An indexer query [rows, 32, 128] in the native-FP4 layout: each head's
+    128 values quantised as one MXFP4 key (mxfp4_encode); the buffer holds the
+    packed codes [rows, 32, 64] followed by the E8M0 scales [rows, 32, 4]."""
+    rows = q.shape[0]
+    packed, e8 = mxfp4_encode(np.asarray(q).reshape(rows * IDX_HEADS, IDX_DIM))
+    return np.concatenate([packed.reshape(-1), e8.reshape(-1)]).astype(np.uint8)
+
+
 def e2m1_codes(mag_signed: "torch.Tensor") -> "torch.Tensor":
     """Nearest E2M1 codes (ties to even, |x| >= 6 -> 6) of a float64 tensor,
     as int64 nibbles with the sign in bit 3."""
@@ -188,7 +198,8 @@ def make_case(name: str, seq_lens, nq: int = 1, key_format: int = KEY_FP8, topk:
     latent scale U(0.5, 2); indexer queries E4M3(N(0,1)) [32, 128]; head
     weights N(0, 0.1^2) fp32; MLA queries bf16(N(0,1)) [96, 576].  With
     ``heavy_tail`` = f, a fraction f of tokens have their key values x4 before
-    rounding.  MXFP4 keys quantise the same N(0,1) draws per OCP MX; NVFP4
+    rounding.  MXFP4 keys quantise the same N(0,1) draws per OCP MX (and, for
+    KEY_MXFP4_NATIVE, the query draws likewise, per head); NVFP4
     latents quantise the same latent draws as ``nvfp4_latent_encode``.
     """
     rng = np.random.Generator(np.random.PCG64(seed))
@@ -266,7 +277,8 @@ def make_case(name: str, seq_lens, nq: int = 1, key_format: int = KEY_FP8, topk:
         pool[spare] = rng.integers(0, 256, size=(len(spare), row_stride), dtype=np.uint8)
 
     rows = batch * nq
-    q_index = e4m3_encode(rng.standard_normal((rows, IDX_HEADS, IDX_DIM), dtype=np.float32))
+    q_draw = rng.standard_normal((rows, IDX_HEADS, IDX_DIM), dtype=np.float32)
+    q_index = e4m3_encode(q_draw) if key_format != KEY_MXFP4_NATIVE else mxfp4_query_encode(q_draw)
     head_w = (rng.standard_normal((rows, IDX_HEADS)) * 0.1).astype(np.float32)
     q_mla = bf16_encode(rng.standard_normal((rows, MLA_HEADS, LATENT), dtype=np.float32))
     return Case(name=name, batch=batch, nq=nq, seq_lens=seq_lens, key_format=key_format, topk=topk,
@@ -288,6 +300,8 @@ WORKLOADS = {
     "longctx_b32_l64k-160k": dict(seq_lens=None, nq=1, heavy_tail=0.10),
     # 1M-token decode with MXFP4 index keys: batch 4
     "mxfp4_b4_l1m": dict(seq_lens=[1 << 20] * 4, nq=1, key_format=KEY_MXFP4),
+    # the same with the query in MXFP4 too, scored by the native FP4 x FP4 MMA
+    "mxfp4n_b4_l1m": dict(seq_lens=[1 << 20] * 4, nq=1, key_format=KEY_MXFP4_NATIVE),
     # the long-context batch in the 10,080 B/token configuration: NVFP4
     # latents (352 B) and MXFP4 keys (68 B), 420 B a token and layer
     "longctx_b32_l64k-160k_nvfp4": dict(seq_lens=None, nq=1, heavy_tail=0.10, key_format=KEY_MXFP4,
@@ -295,6 +309,7 @@ WORKLOADS = {
     # smaller cases of the same shapes for profiler captures (inputs still larger than L2)
     "longctx_b32_l64k": dict(seq_lens=[65536] * 32, nq=1, heavy_tail=0.1),
     "mxfp4_b8_l256k": dict(seq_lens=[1 << 18] * 8, nq=1, key_format=KEY_MXFP4),
+    "mxfp4n_b8_l256k": dict(seq_lens=[1 << 18] * 8, nq=1, key_format=KEY_MXFP4_NATIVE),
     "longctx_b32_l64k_nvfp4": dict(seq_lens=[65536] * 32, nq=1, heavy_tail=0.1, key_format=KEY_MXFP4,
                                    latent_format=LATENT_NVFP4),
     # chunked-prefill append: 2048 new query rows on a 151,552-token prefix
@@ -327,7 +342,7 @@ def workload(name: str, seed: int = 0, **overrides) -> Case:
 class DeviceCase:
     cache: object        # binding.PagedCache
     batch: object        # binding.Batch
-    q_index: object      # uint8 [rows, 32, 128]
+    q_index: object      # uint8, the case's query layout
     head_w: object       # float32 [rows, 32]
     q_mla: object        # int16 (bf16 bits) [rows, 96, 576]
     row_lens: object     # int32 [rows]

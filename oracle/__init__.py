@@ -83,6 +83,8 @@ def _load():
             lib.oracle_index_query_proj.restype = i32
             lib.oracle_quantize_query_f32.argtypes = [P, P, i32, P, P]
             lib.oracle_quantize_query_f32.restype = i32
+            lib.oracle_quantize_query_mxfp4.argtypes = [P, P, i32, P, P]
+            lib.oracle_quantize_query_mxfp4.restype = i32
             lib.oracle_phys_rows.argtypes = [P, i32, i32, i32, P, i32, i32, P]
             lib.oracle_phys_rows.restype = i32
             _lib = lib
@@ -144,7 +146,9 @@ def index_scores(case, rows_ld: int | None = None) -> np.ndarray:
     Follows the Kimi K3.1 Pro Day-0 post, section on sparse attention (32
     light heads score every prior token with a 132-byte FP8 key) and its AMD
     MXFP4-indexer section (68-byte keys, FP32 accumulation, weighted head
-    reduction).  Entries beyond a row's visible length are NaN.
+    reduction; key_format 2: the MXFP4 keys against a native-FP4 query, whose
+    buffer is codes [rows, 32, 64] then E8M0 scales [rows, 32, 4]).  Entries
+    beyond a row's visible length are NaN.
     """
     ld = int(rows_ld or case.max_len)
     out = np.full((case.rows, ld), np.nan, dtype=np.float64)
@@ -301,6 +305,23 @@ def quantize_query_f32(q_f32: np.ndarray, head_w: np.ndarray):
     w_out = np.empty((rows, IDX_HEADS), dtype=np.float32)
     _check(_load().oracle_quantize_query_f32(_ptr(q), _ptr(w), rows, _ptr(codes), _ptr(w_out)), "quantize_query_f32")
     return codes, w_out
+
+
+def quantize_query_mxfp4(q_f32: np.ndarray, head_w: np.ndarray):
+    """The indexer query in native FP4 (Day-0 post, fused-decode section: FP8
+    or MXFP4 quantisation; MXFP4-indexer section: native FP4 scoring), from
+    fp32 values [rows, 32, 128]: per 32-dim block the OCP MX shared exponent
+    floor(log2 amax) - 2 and E2M1 codes, as the MXFP4 keys.  Returns the query
+    buffer (uint8: codes [rows, 32, 64] then E8M0 scales [rows, 32, 4], flat)
+    and the head weights, unchanged (float32 [rows, 32])."""
+    q = np.ascontiguousarray(q_f32, dtype=np.float32).reshape(-1, IDX_HEADS, IDX_DIM)
+    w = np.ascontiguousarray(head_w, dtype=np.float32)
+    rows = q.shape[0]
+    out = np.empty(rows * IDX_HEADS * (IDX_DIM // 2 + 4), dtype=np.uint8)
+    w_out = np.empty((rows, IDX_HEADS), dtype=np.float32)
+    _check(_load().oracle_quantize_query_mxfp4(_ptr(q), _ptr(w), rows, _ptr(out), _ptr(w_out)),
+           "quantize_query_mxfp4")
+    return out, w_out
 
 
 def phys_rows(case, idx: np.ndarray) -> np.ndarray:

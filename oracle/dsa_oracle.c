@@ -30,6 +30,14 @@
  *   MXFP4 keys    k[d] = 2^(E[d/32]-127) * e2m1(code[d]), 128 elements +
  *                 4 E8M0 scales = 68 B per token, no per-token fp32 scale
  *                 ([K31] MXFP4 indexer section: 132 B -> 68 B).
+ *   native FP4    MXFP4 keys scored against an MXFP4 query ([K31] MXFP4
+ *                 indexer section: scoring uses native FP4 matrix
+ *                 instructions; fused-decode section: the front end quantises
+ *                 the query to FP8 or MXFP4): q[h][d] = 2^(Q[h][d/32]-127) *
+ *                 e2m1(qcode[h][d]).  The query buffer is then codes
+ *                 [rows][32][64] (two per byte, low nibble first) followed by
+ *                 the E8M0 scales [rows][32][4]; the head weights are used as
+ *                 given (the block scales stay with the codes).
  *   top-k         keep the k highest-scoring visible tokens (k = 2048 in the
  *                 model, [K31]); ties go to the lower token index; output in
  *                 ascending token order, padded with -1.
@@ -141,6 +149,42 @@ static const uint8_t* block_row(const uint8_t* pool, int64_t row_stride, int32_t
 /* Lightning indexer scores.                                           */
 /* ------------------------------------------------------------------ */
 
+/* The query head (row, h) as 128 doubles.  key_format 0 and 1: E4M3 codes
+ * [rows][32][128]; key_format 2 (native FP4): E2M1 codes [rows][32][64]
+ * followed by E8M0 scales [rows][32][4]. */
+static void query_head(const uint8_t* q_codes, int64_t rows, int32_t key_format, int64_t row, int h,
+                       double qv[ORACLE_IDX_DIM]) {
+  const int64_t rh = row * ORACLE_IDX_HEADS + h;
+  if (key_format != 2) {
+    for (int d = 0; d < ORACLE_IDX_DIM; ++d) qv[d] = oracle_e4m3_to_double(q_codes[rh * ORACLE_IDX_DIM + d]);
+    return;
+  }
+  const uint8_t* packed = q_codes + rh * (ORACLE_IDX_DIM / 2);
+  const uint8_t* e8 = q_codes + rows * ORACLE_IDX_HEADS * (ORACLE_IDX_DIM / 2) + rh * 4;
+  for (int d = 0; d < ORACLE_IDX_DIM; ++d) {
+    const uint8_t nib = (d % 2 == 0) ? (packed[d / 2] & 0xF) : (packed[d / 2] >> 4);
+    qv[d] = oracle_e8m0_to_double(e8[d / 32]) * oracle_e2m1_to_double(nib);
+  }
+}
+
+/* raw[h] = q_h . k_t for an MXFP4 key against a native-FP4 query (the
+ * products are exact in double; the sum over the four blocks, whose scales
+ * may differ widely, is rounded once per addition in double). */
+static void raw_dots_native(const uint8_t* q_codes, int64_t rows, int64_t row, const uint8_t* packed,
+                            const uint8_t* e8m0, double raw[ORACLE_IDX_HEADS]) {
+  double k[ORACLE_IDX_DIM];
+  for (int d = 0; d < ORACLE_IDX_DIM; ++d) {
+    const uint8_t nib = (d % 2 == 0) ? (packed[d / 2] & 0xF) : (packed[d / 2] >> 4);
+    k[d] = oracle_e8m0_to_double(e8m0[d / 32]) * oracle_e2m1_to_double(nib);
+  }
+  for (int h = 0; h < ORACLE_IDX_HEADS; ++h) {
+    double qv[ORACLE_IDX_DIM], acc = 0.0;
+    query_head(q_codes, rows, 2, row, h, qv);
+    for (int d = 0; d < ORACLE_IDX_DIM; ++d) acc += qv[d] * k[d];
+    raw[h] = acc;
+  }
+}
+
 /* raw[h] = q_h . k_t  for the FP8 key of token t (exact in double: every
  * e4m3 value is a multiple of 2^-9 below 2^9, so each product is a multiple
  * of 2^-18 below 2^18 and a 128-term sum stays far inside 53 bits). */
@@ -178,6 +222,7 @@ static void raw_dots_mxfp4(const uint8_t* q, const uint8_t* packed /*[64]*/,
 /* Scores of every visible token for every query row.
  *   key_format 0: FP8 page = 64 x 128 B codes, then 64 fp32 scales.
  *   key_format 1: MXFP4 page = 64 x 64 B packed codes, then 64 x 4 E8M0.
+ *   key_format 2: the MXFP4 page against a native-FP4 query (query_head).
  * scores[row * ld + t] is written for t < visible length; other entries are
  * left untouched.  Returns ORACLE_BAD_BLOCK if a visible token's block-table
  * entry is outside the pool. */
@@ -188,14 +233,14 @@ int oracle_index_scores(const uint8_t* pool, int64_t row_stride, int64_t index_o
                         double* scores, int64_t ld) {
   if (!pool || !block_table || !seq_lens || !q_codes || !head_w || !scores || nq < 1 || batch < 0)
     return ORACLE_BAD_ARG;
-  if (key_format != 0 && key_format != 1) return ORACLE_BAD_ARG;
+  if (key_format < 0 || key_format > 2) return ORACLE_BAD_ARG;
   int bad = 0;
   int64_t rows = (int64_t)batch * nq;
   for (int64_t row = 0; row < rows; ++row) {
     int b = (int)(row / nq), j = (int)(row % nq);
     int64_t vis = visible_len(seq_lens[b], nq, j);
     if (vis > ld) return ORACLE_BAD_ARG;
-    const uint8_t* q = q_codes + row * ORACLE_IDX_HEADS * ORACLE_IDX_DIM;
+    const uint8_t* q = q_codes + (key_format == 2 ? 0 : row * ORACLE_IDX_HEADS * ORACLE_IDX_DIM);
     const float* w = head_w + row * ORACLE_IDX_HEADS;
 #pragma omp parallel for schedule(static) reduction(| : bad)
     for (int64_t t = 0; t < vis; ++t) {
@@ -208,6 +253,10 @@ int oracle_index_scores(const uint8_t* pool, int64_t row_stride, int64_t index_o
       if (key_format == 0) {
         raw_dots_fp8(q, page + slot * ORACLE_IDX_DIM, raw);
         scale = (double)load_f32(page + ORACLE_BLOCK * ORACLE_IDX_DIM + slot * 4);
+      } else if (key_format == 2) {
+        raw_dots_native(q_codes, rows, row, page + slot * (ORACLE_IDX_DIM / 2),
+                        page + ORACLE_BLOCK * (ORACLE_IDX_DIM / 2) + slot * 4, raw);
+        scale = 1.0;
       } else {
         raw_dots_mxfp4(q, page + slot * (ORACLE_IDX_DIM / 2),
                        page + ORACLE_BLOCK * (ORACLE_IDX_DIM / 2) + slot * 4, raw);
@@ -231,14 +280,16 @@ int oracle_index_score_bounds(const uint8_t* pool, int64_t row_stride, int64_t i
                               const int32_t* seq_lens, int32_t batch, int32_t nq,
                               const uint8_t* q_codes, const float* head_w, double* bounds, int64_t ld) {
   if (!pool || !block_table || !seq_lens || !q_codes || !head_w || !bounds || nq < 1) return ORACLE_BAD_ARG;
+  if (key_format < 0 || key_format > 2) return ORACLE_BAD_ARG;
   int bad = 0;
   int64_t rows = (int64_t)batch * nq;
   for (int64_t row = 0; row < rows; ++row) {
     int b = (int)(row / nq), j = (int)(row % nq);
     int64_t vis = visible_len(seq_lens[b], nq, j);
     if (vis > ld) return ORACLE_BAD_ARG;
-    const uint8_t* q = q_codes + row * ORACLE_IDX_HEADS * ORACLE_IDX_DIM;
     const float* w = head_w + row * ORACLE_IDX_HEADS;
+    double qv[ORACLE_IDX_HEADS][ORACLE_IDX_DIM];
+    for (int h = 0; h < ORACLE_IDX_HEADS; ++h) query_head(q_codes, rows, key_format, row, h, qv[h]);
 #pragma omp parallel for schedule(static) reduction(| : bad)
     for (int64_t t = 0; t < vis; ++t) {
       const uint8_t* rowp = block_row(pool, row_stride, num_blocks, block_table, max_blocks, b, t);
@@ -261,7 +312,7 @@ int oracle_index_score_bounds(const uint8_t* pool, int64_t row_stride, int64_t i
       double a = 0.0;
       for (int h = 0; h < ORACLE_IDX_HEADS; ++h) {
         double acc = 0.0;
-        for (int d = 0; d < ORACLE_IDX_DIM; ++d) acc += fabs(oracle_e4m3_to_double(q[h * ORACLE_IDX_DIM + d]) * k[d]);
+        for (int d = 0; d < ORACLE_IDX_DIM; ++d) acc += fabs(qv[h][d] * k[d]);
         a += fabs((double)w[h]) * fabs(scale) * acc;
       }
       bounds[row * ld + t] = a;
@@ -567,6 +618,27 @@ uint8_t oracle_e2m1_encode(double x) {
   return (uint8_t)(mag | (signbit(x) ? 0x8 : 0));
 }
 
+/* One OCP MX block of 32 values: the shared exponent E = floor(log2 amax) - 2
+ * (E2M1's largest exponent is 2) clamped to [-127, 127], -127 for an all-zero
+ * block; codes e2m1(x * 2^-E) (exact scaling), two per byte, low nibble
+ * first; the scale byte E + 127. */
+static void mx_block_encode(const float* x /*[32]*/, uint8_t* packed /*[16]*/, uint8_t* e8) {
+  double amax = 0.0;
+  for (int d = 0; d < 32; ++d) amax = fmax(amax, fabs((double)x[d]));
+  int e = -127;
+  if (amax > 0.0) {
+    int ex;
+    frexp(amax, &ex);  /* amax = m * 2^ex, m in [0.5, 1): floor(log2 amax) = ex - 1 */
+    e = ex - 1 - 2;
+    if (e < -127) e = -127;
+    if (e > 127) e = 127;
+  }
+  uint8_t codes[32];
+  for (int d = 0; d < 32; ++d) codes[d] = oracle_e2m1_encode(ldexp((double)x[d], -e));
+  for (int d = 0; d < 32; d += 2) packed[d / 2] = (uint8_t)(codes[d] | (codes[d + 1] << 4));
+  *e8 = (uint8_t)(e + 127);
+}
+
 /* float amax / 448 in single precision; 1 for an all-zero vector */
 static float fp8_scale(const float* x, int n) {
   float amax = 0.f;
@@ -642,24 +714,10 @@ int oracle_cache_append(uint8_t* pool, int64_t row_stride, int64_t latent_off, i
         for (int d = 0; d < ORACLE_IDX_DIM; ++d)
           page[(int64_t)slot * ORACLE_IDX_DIM + d] = oracle_e4m3_encode((double)(k[d] / s));
         memcpy(page + ORACLE_BLOCK * ORACLE_IDX_DIM + 4 * slot, &s, 4);
-      } else {
-        for (int blk = 0; blk < ORACLE_IDX_DIM / 32; ++blk) {
-          double amax = 0.0;
-          for (int d = 0; d < 32; ++d) amax = fmax(amax, fabs((double)k[32 * blk + d]));
-          int e = -127;
-          if (amax > 0.0) {
-            int ex;
-            frexp(amax, &ex);  /* amax = m * 2^ex, m in [0.5, 1): floor(log2 amax) = ex - 1 */
-            e = ex - 1 - 2;
-            if (e < -127) e = -127;
-            if (e > 127) e = 127;
-          }
-          uint8_t codes[32];
-          for (int d = 0; d < 32; ++d) codes[d] = oracle_e2m1_encode(ldexp((double)k[32 * blk + d], -e));
-          for (int d = 0; d < 32; d += 2)
-            page[(int64_t)slot * (ORACLE_IDX_DIM / 2) + 16 * blk + d / 2] = (uint8_t)(codes[d] | (codes[d + 1] << 4));
-          page[ORACLE_BLOCK * (ORACLE_IDX_DIM / 2) + 4 * slot + blk] = (uint8_t)(e + 127);
-        }
+      } else {  /* MXFP4 keys (key_format 1 and 2) */
+        for (int blk = 0; blk < ORACLE_IDX_DIM / 32; ++blk)
+          mx_block_encode(k + 32 * blk, page + (int64_t)slot * (ORACLE_IDX_DIM / 2) + 16 * blk,
+                          page + ORACLE_BLOCK * (ORACLE_IDX_DIM / 2) + 4 * slot + blk);
       }
     }
   }
@@ -758,6 +816,27 @@ int oracle_quantize_query_f32(const float* q, const float* w, int32_t rows, uint
     const float s = fp8_scale(x, ORACLE_IDX_DIM);
     for (int d = 0; d < ORACLE_IDX_DIM; ++d) codes[rh * ORACLE_IDX_DIM + d] = oracle_e4m3_encode((double)(x[d] / s));
     w_out[rh] = w[rh] * s;
+  }
+  return ORACLE_OK;
+}
+
+/*
+ * The indexer query in native FP4 ([K31] fused-decode section: the front end
+ * quantises the query to FP8 or MXFP4; MXFP4 indexer section: native FP4
+ * scoring), from fp32 values q [rows][32][128]: per (row, head) and 32-dim
+ * block the OCP MX encoding of mx_block_encode, as the MXFP4 keys are
+ * written.  out: codes [rows][32][64], then E8M0 scales [rows][32][4].  The
+ * block scales stay with the codes (the block-scaled product applies them), so
+ * the head weights pass through unchanged: w_out = w.
+ */
+int oracle_quantize_query_mxfp4(const float* q, const float* w, int32_t rows, uint8_t* out, float* w_out) {
+  if (!q || !w || !out || !w_out || rows < 0) return ORACLE_BAD_ARG;
+  const int64_t heads = (int64_t)rows * ORACLE_IDX_HEADS;
+  for (int64_t rh = 0; rh < heads; ++rh) {
+    for (int blk = 0; blk < ORACLE_IDX_DIM / 32; ++blk)
+      mx_block_encode(q + rh * ORACLE_IDX_DIM + 32 * blk, out + rh * (ORACLE_IDX_DIM / 2) + 16 * blk,
+                      out + heads * (ORACLE_IDX_DIM / 2) + rh * 4 + blk);
+    w_out[rh] = w[rh];
   }
   return ORACLE_OK;
 }

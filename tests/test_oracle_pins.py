@@ -798,3 +798,89 @@ def test_phys_rows_identity_table_and_permutation():
     idx2 = np.zeros((4, 1), dtype=np.int32)
     with pytest.raises(RuntimeError):
         oracle.phys_rows(case, idx2)
+
+
+# --------------------------------------------------------------- native FP4 scoring
+def _mx_values(packed, e8):
+    """Exact values of MX-coded rows (codes [n, 64] packed, E8M0 [n, 4]) as Fractions."""
+    out = []
+    for p, e in zip(packed, e8):
+        row = []
+        for d in range(128):
+            nib = p[d // 2] & 0xF if d % 2 == 0 else p[d // 2] >> 4
+            mag = [0, 1, 2, 3, 4, 6, 8, 12][nib & 7] * (-1 if nib & 8 else 1)  # 2 x E2M1
+            row.append(Fraction(mag, 2) * Fraction(2) ** (int(e[d // 32]) - 127))
+        out.append(row)
+    return out
+
+
+def test_index_scores_native_fp4_exact_rational():
+    """MXFP4 keys against an MXFP4 query (the native FP4 x FP4 product): with
+    w = e_h the score is max(0, q_h . k_t), both sides decoded exactly from
+    their E2M1 codes and E8M0 block scales."""
+    c = synth.make_case("mxn", seq_lens=[130], key_format=synth.KEY_MXFP4_NATIVE, seed=4)
+    rows = c.rows
+    assert c.q_index.size == rows * 32 * 68
+    qp = c.q_index[:rows * 32 * 64].reshape(rows * 32, 64)
+    qe = c.q_index[rows * 32 * 64:].reshape(rows * 32, 4)
+    for h in (0, 9, 31):
+        c.head_w = np.zeros_like(c.head_w)
+        c.head_w[:, h] = 1.0
+        s = oracle.index_scores(c)
+        bnd = oracle.index_score_bounds(c)
+        qv = _mx_values(qp[h:h + 1], qe[h:h + 1])[0]
+        for t in (0, 5, 64, 129):
+            r = c.block_table[0, t // 64]
+            page = c.pool[r, c.index_off:]
+            kv = _mx_values([page[(t % 64) * 64:(t % 64) * 64 + 64]], [page[64 * 64 + (t % 64) * 4:64 * 64 + (t % 64) * 4 + 4]])[0]
+            dot = sum(a * b for a, b in zip(qv, kv))
+            assert s[0, t] == float(max(Fraction(0), dot))
+            assert bnd[0, t] == pytest.approx(float(sum(abs(a * b) for a, b in zip(qv, kv))), rel=1e-14)
+
+
+def test_index_scores_native_fp4_equals_fp8_query_when_the_query_is_exact():
+    """When every query value is representable in both formats (E2M1 values
+    times a power of two per block that E4M3 also holds exactly), the native
+    and the FP8-query scores of the same keys are equal."""
+    c8 = synth.make_case("mxe", seq_lens=[200, 70], key_format=synth.KEY_MXFP4, seed=9)
+    rng = np.random.default_rng(2)
+    rows = c8.rows
+    vals = rng.choice([0.0, 0.5, 1.0, 1.5, 2.0, 3.0, 4.0, 6.0], size=(rows, 32, 128)) * rng.choice([-1, 1], size=(rows, 32, 128))
+    vals = vals * (2.0 ** rng.integers(-3, 3, size=(rows, 32, 4))).repeat(32, axis=2)
+    c8.q_index = synth.e4m3_encode(vals.astype(np.float32))
+    cn = synth.make_case("mxe", seq_lens=[200, 70], key_format=synth.KEY_MXFP4_NATIVE, seed=9)
+    cn.q_index = synth.mxfp4_query_encode(vals.astype(np.float32))
+    cn.head_w = c8.head_w
+    np.testing.assert_array_equal(oracle.index_scores(cn), oracle.index_scores(c8))
+
+
+def test_quantize_query_mxfp4_is_the_mx_encoding_per_head():
+    """Per (row, head) and 32-dim block: E = floor(log2 amax) - 2 (clamped to
+    [-127, 127]; byte 0 for an all-zero block), codes the nearest E2M1 of
+    x 2^-E with ties to even (brute force), head weights unchanged."""
+    rng = np.random.default_rng(13)
+    q = rng.standard_normal((2, 32, 128)).astype(np.float32) * np.exp(rng.uniform(-4, 4, (2, 32, 1))).astype(np.float32)
+    q[0, 3] = 0.0                      # an all-zero head
+    q[1, 7, 32:64] *= np.float32(1e-38)  # a block of tiny values
+    q[1, 8, :32] = 6.0 * 2.0 ** 5      # amax exactly 6 x 2^E: the top code
+    q[1, 9, 64:96] = np.float32(2.0 ** 120)   # E clamps at 127
+    w = rng.standard_normal((2, 32)).astype(np.float32)
+    buf, w_out = oracle.quantize_query_mxfp4(q, w)
+    np.testing.assert_array_equal(w_out, w)
+    rows = 2
+    packed = buf[:rows * 32 * 64].reshape(rows, 32, 64)
+    e8 = buf[rows * 32 * 64:].reshape(rows, 32, 4)
+    for r in range(rows):
+        for h in range(32):
+            for blk in range(4):
+                xs = q[r, h, 32 * blk:32 * blk + 32].astype(np.float64)
+                amax = np.abs(xs).max()
+                e = -127 if amax == 0 else max(-127, min(127, math.frexp(amax)[1] - 1 - 2))
+                assert e8[r, h, blk] == e + 127, (r, h, blk)
+                p = packed[r, h, 16 * blk:16 * blk + 16]
+                codes = np.stack([p & 0xF, p >> 4], axis=1).reshape(-1)
+                assert [int(c) for c in codes] == [_e2m1_brute(float(v) * 2.0 ** -e) for v in xs], (r, h, blk)
+    assert e8[0, 3].tolist() == [0, 0, 0, 0] and not packed[0, 3].any()
+    assert (packed[1, 8, :16] == 0x77).all()          # +6 in both nibbles
+    # the query generator's native layout is this encoding of its draws
+    np.testing.assert_array_equal(synth.mxfp4_query_encode(q), buf)
