@@ -41,7 +41,7 @@ L2_FLUSH_BYTES = 256 << 20   # > 129 MB L2; flushed by READING it (clean lines, 
 # The other configurations of the target statement, measured after the headline
 # one with the same protocol (fewer steps) and reported in the line's
 # "workloads" block: speculative verify, 1M-token MXFP4 keys, chunked prefill.
-EXTRA_WORKLOADS = ("specdecode_b8x4_l32768", "mxfp4_b4_l1m", "prefill_q2048_l153600")
+EXTRA_WORKLOADS = ("specdecode_b8x4_l32768", "mxfp4_b4_l1m", "mxfp4n_b4_l1m", "prefill_q2048_l153600")
 
 
 def parse():

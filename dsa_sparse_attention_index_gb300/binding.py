@@ -17,7 +17,7 @@ _HERE = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(_HERE, "libdsa.so")
 
 OK, ERR_INVALID_ARG, ERR_UNSUPPORTED, ERR_BOUNDS, ERR_TIMEOUT, ERR_CUDA, ERR_WORKSPACE = range(7)
-KEY_FP8_E4M3, KEY_MXFP4 = 0, 1
+KEY_FP8_E4M3, KEY_MXFP4, KEY_MXFP4_NATIVE = 0, 1, 2
 LATENT_FP8_E4M3, LATENT_NVFP4 = 0, 1
 BLOCK, IDX_HEADS, IDX_DIM, MLA_HEADS, LATENT, VALUE, MAX_TOPK = 64, 32, 128, 96, 576, 512, 2048
 

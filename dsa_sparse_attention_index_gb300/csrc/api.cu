@@ -67,7 +67,8 @@ int index_page_bytes(int key_format) {
 dsa_status_t check_cache(const dsa_paged_cache_t* c) {
   if (!c || !c->base || !aligned(c->base, 128)) return DSA_ERR_INVALID_ARG;
   if (c->block_size != kBlock) return DSA_ERR_UNSUPPORTED;
-  if (c->key_format != DSA_KEY_FP8_E4M3 && c->key_format != DSA_KEY_MXFP4) return DSA_ERR_INVALID_ARG;
+  if (c->key_format != DSA_KEY_FP8_E4M3 && c->key_format != DSA_KEY_MXFP4 && c->key_format != DSA_KEY_MXFP4_NATIVE)
+    return DSA_ERR_INVALID_ARG;
   if (c->latent_format != DSA_LATENT_FP8_E4M3 && c->latent_format != DSA_LATENT_NVFP4) return DSA_ERR_INVALID_ARG;
   if (c->num_blocks <= 0 || c->row_stride <= 0 || (c->row_stride % 128) || (c->latent_off % 128) ||
       (c->index_off % 128) || c->latent_off < 0 || c->index_off < 0)
@@ -85,11 +86,11 @@ dsa_status_t check_batch(const dsa_batch_t* b) {
   return DSA_OK;
 }
 
-// Row shapes the indexer takes: MXFP4 keys one row per sequence; more than 4
+// Row shapes the indexer takes: MXFP4 keys (either query format) one row per sequence; more than 4
 // rows per sequence (a prefill chunk) a multiple of 4; at most 4096 sequences.
 dsa_status_t check_index_rows(const dsa_paged_cache_t* c, const dsa_batch_t* b) {
   const int nq = b->queries_per_seq;
-  if (c->key_format == DSA_KEY_MXFP4 && nq != 1) return DSA_ERR_UNSUPPORTED;
+  if (c->key_format != DSA_KEY_FP8_E4M3 && nq != 1) return DSA_ERR_UNSUPPORTED;
   if (nq > 4 && nq % 4 != 0) return DSA_ERR_UNSUPPORTED;
   if (b->batch > 4096) return DSA_ERR_UNSUPPORTED;
   return DSA_OK;

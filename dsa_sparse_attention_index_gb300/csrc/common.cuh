@@ -216,6 +216,17 @@ __device__ __forceinline__ void mma_mxf8f6f4(uint32_t d, uint64_t a, uint64_t b,
       ::"r"(d), "l"(a), "l"(b), "r"(idesc), "r"(sfa), "r"(sfb), "r"(accumulate)
       : "memory");
 }
+// The same with packed E2M1 operands on both sides (kind::mxf4, K = 64 per
+// instruction, two E8M0 scales per row: bytes sf_id and sf_id + 1 of the
+// scale word, sf_id 0 or 2).
+__device__ __forceinline__ void mma_mxf4(uint32_t d, uint64_t a, uint64_t b, uint32_t idesc, uint32_t sfa,
+                                         uint32_t sfb, uint32_t accumulate) {
+  asm volatile(
+      "{\n .reg .pred p;\n setp.ne.b32 p, %6, 0;\n"
+      " tcgen05.mma.cta_group::1.kind::mxf4.block_scale.scale_vec::2X [%0], %1, %2, %3, [%4], [%5], p;\n}\n"
+      ::"r"(d), "l"(a), "l"(b), "r"(idesc), "r"(sfa), "r"(sfb), "r"(accumulate)
+      : "memory");
+}
 // Arrive once on `bar` when every tcgen05.mma issued so far by this thread completes.
 __device__ __forceinline__ void mma_commit(uint32_t bar) {
   asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar) : "memory");
@@ -256,6 +267,10 @@ __device__ __forceinline__ void tmem_st32(uint32_t taddr, const uint32_t (&r)[32
       DSA_W32(r)
       : "memory");
 }
+// One 32-bit TMEM column of this thread's lane (warp-collective).
+__device__ __forceinline__ void tmem_st1(uint32_t taddr, uint32_t v) {
+  asm volatile("tcgen05.st.sync.aligned.32x32b.x1.b32 [%0], {%1};" ::"r"(taddr), "r"(v) : "memory");
+}
 // Four consecutive 32-bit TMEM columns of this thread's lane (warp-collective).
 __device__ __forceinline__ void tmem_st4(uint32_t taddr, uint32_t v0, uint32_t v1, uint32_t v2, uint32_t v3) {
   asm volatile("tcgen05.st.sync.aligned.32x32b.x4.b32 [%0], {%1, %2, %3, %4};" ::"r"(taddr), "r"(v0), "r"(v1),
@@ -283,6 +298,8 @@ __device__ __forceinline__ uint64_t desc64(uint32_t lo, uint32_t hi) { return ((
 // Instruction descriptor (kind::f16 and kind::f8f6f4): fp32 accumulator,
 // operand formats, K-major (0) / MN-major (1) per operand, N >> 3, M >> 4.
 enum : uint32_t { kFmtE4M3 = 0, kFmtE2M1 = 5, kFmtBF16 = 1 };
+// E2M1 in the operand-format field of kind::mxf4 (the only format of that kind)
+constexpr uint32_t kFmtMxf4E2M1 = 1;
 // Instruction descriptor of kind::mxf8f6f4.block_scale (fp32 accumulator
 // implied): operand formats, K-major operands, N >> 3, E8M0 scale type (bit
 // 23), M >> 4; the per-MMA scale-factor byte ids are ORed in with mx_sf_ids.

@@ -29,8 +29,13 @@
 //           double-buffered TMEM tile.  FP8: tcgen05.mma kind::f8f6f4.
 //           MXFP4: kind::mxf8f6f4.block_scale, E2M1 x E4M3 with the keys'
 //           E8M0 block scales read from TMEM (queries: scale 2^0), so one
-//           accumulator per sub-tile already holds q . k.  The code stage
-//           is released by tcgen05.commit as soon as its MMAs complete;
+//           accumulator per sub-tile already holds q . k.  Native FP4 (an
+//           MXFP4 query too; AMD section: native FP4 matrix instructions):
+//           kind::mxf4.block_scale, both operands packed E2M1 (64-byte rows,
+//           64-byte swizzle), two K = 64 steps, both sides' E8M0 scales from
+//           TMEM; the packed stage is half the FP8 one, so 11 stages hold
+//           the keys in flight that HBM needs.  The code stage is released by
+//           tcgen05.commit as soon as its MMAs complete;
 //   warps 2-5 epilogue: each thread owns two key rows (one per sub-tile),
 //           reads their 32*NQ accumulators with tcgen05.ld, applies the FP8
 //           scale, ReLU and the head weights, sums the heads in registers
@@ -38,7 +43,9 @@
 //   warps 6-9 (MXFP4 only) scale staging: per unit, copy the 256 keys' E8M0
 //           words from the scale ring into TMEM, laid out as the
 //           block-scaled MMA reads them (key row m: lane m % 32, column
-//           m / 32, byte = 32-element block).
+//           m / 32, byte = 32-element block); native FP4 also writes the
+//           unit's query words (head n: lane n, one column per slot, the
+//           slots 32 columns apart as the keys' are).
 // All draft rows of a sequence share one key read (AMD section: keys are
 // reused across query rows during speculative verify).
 #include <algorithm>
@@ -58,6 +65,7 @@ constexpr int kPagesPerUnit = kUnitKeys / kBlock;       // 4
 constexpr int kSubTileBytes = 128 * kIdxDim;            // 16 KB: one M = 128 MMA tile (one byte per element)
 constexpr int kATileBytes = kUnitKeys * kIdxDim;        // 32 KB of codes per unit in shared memory
 constexpr int kPageCodeBytes = kBlock * kIdxDim;        // 8 KB in shared memory (MXFP4: 4 KB read)
+constexpr int kPagePackedBytes = kBlock * kIdxDim / 2;  // 4 KB: a page of packed E2M1 codes (native FP4)
 constexpr int kPageScaleBytes = kBlock * 4;             // 256 B
 constexpr int kUnitScaleBytes = kPagesPerUnit * kPageScaleBytes;  // 1 KB (one gather4)
 constexpr int kMaxBatch = 4096;
@@ -77,17 +85,23 @@ struct IdxParams {
   int64_t ld;
   int32_t* status;
   int32_t score_bf16;  // scores are bf16 (round to nearest even) at (uint16_t*)scores, else fp32
+  const uint32_t* q_scales;  // native FP4: the query's E8M0 words [rows][32] (4 blocks a word), else null
 };
 
 constexpr int kSfSlots = 4;  // MXFP4: TMEM scale-factor slots, decoupled from the accumulators
 
-template <int NQ>
+// Shared memory of the indexer.  NAT (native FP4): the code stages hold packed
+// E2M1 (16 KB a unit), so nearly twice as many fit and twice the keys are in
+// flight for the same bytes.
+template <int NQ, bool NAT = false>
 struct IdxSmem {
-  static constexpr int kStages = NQ == 1 ? 6 : 5;       // code ring; keeps the CTA within 227 KB
+  static constexpr int kATile = NAT ? kUnitKeys * kIdxDim / 2 : kATileBytes;  // bytes of one code stage
+  static constexpr int kPageSmem = NAT ? kPagePackedBytes : kPageCodeBytes;   // bytes of one page in a stage
+  static constexpr int kStages = NAT ? 11 : (NQ == 1 ? 6 : 5);  // code ring; keeps the CTA within 227 KB
   static constexpr int kScaleStages = kStages + 2;      // scale slots are held until the epilogue ends
-  static constexpr int kQSlot = 32 * NQ * kIdxDim;      // bytes
+  static constexpr int kQSlot = NAT ? 32 * kIdxDim / 2 : 32 * NQ * kIdxDim;  // bytes
   static constexpr int kOffA = 0;
-  static constexpr int kOffQ = kOffA + kStages * kATileBytes;
+  static constexpr int kOffQ = kOffA + kStages * kATile;
   static constexpr int kOffScales = kOffQ + 2 * kQSlot;
   static constexpr int kOffBars = kOffScales + kScaleStages * kUnitScaleBytes;
   // barriers: code full/empty [S], scale full/empty [SS], acc full/empty [2],
@@ -116,25 +130,31 @@ __device__ __forceinline__ void tma_gather4(uint32_t dst, const void* map, int c
       : "memory");
 }
 
-// MX = false: FP8 keys (E4M3 codes + fp32 scale).  MX = true: MXFP4 keys
-// (E2M1 codes + E8M0 block scales, applied by the block-scaled MMA).
-template <int NQ, bool MX>
-__global__ void __launch_bounds__(idx_threads<MX>(), 1)
+// KF = 0: FP8 keys (E4M3 codes + fp32 scale).  KF = 1: MXFP4 keys (E2M1 codes
+// + E8M0 block scales, applied by the block-scaled MMA) against the E4M3
+// query.  KF = 2: the MXFP4 keys against an MXFP4 query, both packed, on the
+// native FP4 x FP4 MMA.
+template <int NQ, int KF>
+__global__ void __launch_bounds__(idx_threads<KF != 0>(), 1)
     indexer_kernel(const __grid_constant__ CUtensorMap tmap_keys, const __grid_constant__ CUtensorMap tmap_scales,
                    const __grid_constant__ CUtensorMap tmap_q, const IdxParams p) {
-  using L = IdxSmem<NQ>;
+  constexpr bool MX = KF != 0, NAT = KF == 2;
+  using L = IdxSmem<NQ, NAT>;
   static_assert(!MX || NQ == 1, "MXFP4 keys: one query row per sequence");
   constexpr int kStages = L::kStages;
   constexpr int kSS = L::kScaleStages;
   constexpr int N = 32 * NQ;
   // TMEM: accumulators [2 slots][2 sub-tiles][N] at column 0; MXFP4 adds the
   // keys' scale factors (4 columns per sub-tile, at 32-column steps, in
-  // kSfSlots slots) and the queries' (2^0)
+  // kSfSlots slots) and the queries' (2^0; native FP4: the query's words, one
+  // column per slot, at 32-column steps like the keys': a scale-factor address
+  // off that grid faults)
   constexpr uint32_t kTmemCols = MX ? 512 : ((4 * N <= 128) ? 128 : (4 * N <= 256 ? 256 : 512));
   constexpr uint32_t kSfaCol = 128, kSfbCol = kSfaCol + 64 * kSfSlots;
-  static_assert(!MX || kSfbCol + 4 <= kTmemCols, "TMEM columns");
-  constexpr uint32_t kIdesc = MX ? make_idesc_mx(kFmtE2M1, kFmtE4M3, 128, N)
-                                 : make_idesc(kFmtE4M3, kFmtE4M3, 0, 0, 128, N);
+  static_assert(!MX || kSfbCol + 32 * (kSfSlots - 1) + 1 <= kTmemCols, "TMEM columns");
+  constexpr uint32_t kIdesc = NAT  ? make_idesc_mx(kFmtMxf4E2M1, kFmtMxf4E2M1, 128, N)
+                              : MX ? make_idesc_mx(kFmtE2M1, kFmtE4M3, 128, N)
+                                   : make_idesc(kFmtE4M3, kFmtE4M3, 0, 0, 128, N);
 
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -322,8 +342,8 @@ __global__ void __launch_bounds__(idx_threads<MX>(), 1)
             okh = mbar_wait(empty_bar(s), ((uit / kStages) & 1) ^ 1, abort_flag, p.status) &&
                   mbar_wait(sce_bar(s2), ((uit / kSS) & 1) ^ 1, abort_flag, p.status);
             if (okh) {
-              // an unpacking MXFP4 copy counts its packed source bytes (half what it writes)
-              mbar_arrive_expect_tx(full_bar(s), npages * (MX ? kPageCodeBytes / 2 : kPageCodeBytes));
+              // MXFP4 pages are 4 KB in HBM (the unpacking copy of KF = 1 counts its source bytes)
+              mbar_arrive_expect_tx(full_bar(s), npages * (MX ? kPagePackedBytes : kPageCodeBytes));
               mbar_arrive_expect_tx(scf_bar(s2), kUnitScaleBytes);
             }
           }
@@ -332,7 +352,7 @@ __global__ void __launch_bounds__(idx_threads<MX>(), 1)
           // lane hl < npages of each half loads page hl; lane 4 of each half gathers the scale rows
           if (hl < npages) {
             const int rq = hl == 0 ? r[0] : (hl == 1 ? r[1] : (hl == 2 ? r[2] : r[3]));
-            tma_load_3d_hint(sbase + L::kOffA + s * kATileBytes + hl * kPageCodeBytes, &tmap_keys, 0, 0, rq,
+            tma_load_3d_hint(sbase + L::kOffA + s * L::kATile + hl * L::kPageSmem, &tmap_keys, 0, 0, rq,
                              full_bar(s), stream_policy);
           } else if (hl == kPagesPerUnit && valid) {
             tma_gather4(sbase + L::kOffScales + s2 * kUnitScaleBytes, &tmap_scales, 0, r[0], r[1], r[2], r[3],
@@ -373,6 +393,17 @@ __global__ void __launch_bounds__(idx_threads<MX>(), 1)
         const uint32_t b_base = sbase + L::kOffQ + ((qn - 1) & 1) * L::kQSlot;
 #pragma unroll
         for (int sub = 0; sub < 2; ++sub) {
+          if constexpr (NAT) {
+            // packed E2M1, 64-byte rows with the 64-byte swizzle (8-row groups 512 B apart);
+            // K = 64 per MMA: E8M0 bytes 2 kk and 2 kk + 1 of the scale words
+            const uint32_t a_base = sbase + L::kOffA + s * L::kATile + sub * (128 * kIdxDim / 2);
+#pragma unroll
+            for (int kk = 0; kk < kIdxDim / 64; ++kk)
+              mma_mxf4(tmem + (2 * a + sub) * N, smem_desc(a_base + 32 * kk, 16, 512, kLayoutSw64),
+                       smem_desc(b_base + 32 * kk, 16, 512, kLayoutSw64), kIdesc | mx_sf_ids(2 * kk, 2 * kk),
+                       tmem + kSfaCol + 32 * (2 * f + sub), tmem + kSfbCol + 32 * f, kk > 0 ? 1u : 0u);
+            continue;
+          }
           const uint32_t a_base = sbase + L::kOffA + s * kATileBytes + sub * kSubTileBytes;
 #pragma unroll
           for (int kk = 0; kk < kIdxDim / 32; ++kk) {
@@ -471,10 +502,13 @@ __global__ void __launch_bounds__(idx_threads<MX>(), 1)
       // column m / 32; every warp writes the same words into its own lane
       // quarter.  The queries' scale words (2^0 in every byte) are written once.
       const uint32_t lane_base = tmem + ((uint32_t)((warp & 3) * 32) << 16);
-      tmem_st4(lane_base + kSfbCol, 0x7F7F7F7Fu, 0x7F7F7F7Fu, 0x7F7F7F7Fu, 0x7F7F7F7Fu);
+      if (!NAT) tmem_st4(lane_base + kSfbCol, 0x7F7F7F7Fu, 0x7F7F7F7Fu, 0x7F7F7F7Fu, 0x7F7F7F7Fu);
+      int cursor = first_seq(u_begin);
       uint32_t it = 0;
       for (int64_t u = u_begin; u < u_end; ++u, ++it) {
         const int s2 = it % kSS, f = it % kSfSlots;
+        // native FP4: head `lane` of the unit's query row (the query's words come from global memory)
+        const uint32_t qw = NAT ? __ldg(p.q_scales + (int64_t)seq_of_unit(prefix, nb, u, cursor) * 32 + lane) : 0u;
         bool ok = mbar_wait(scf_bar(s2), (it / kSS) & 1, abort_flag, p.status);
         // slot f's scale factors were last read by the MMAs of unit it - kSfSlots
         ok = ok && mbar_wait(sfe_bar(f), ((it / kSfSlots) & 1) ^ 1, abort_flag, p.status);
@@ -486,6 +520,7 @@ __global__ void __launch_bounds__(idx_threads<MX>(), 1)
           const uint32_t* ws = wsrc + 128 * sub + lane;
           tmem_st4(lane_base + kSfaCol + 32 * (2 * f + sub), ws[0], ws[32], ws[64], ws[96]);
         }
+        if (NAT) tmem_st1(lane_base + kSfbCol + 32 * f, qw);
         tmem_st_wait();
         tc_fence_before();
         __syncwarp();
@@ -507,15 +542,16 @@ __global__ void __launch_bounds__(idx_threads<MX>(), 1)
   if (warp == 1) tmem_dealloc(tmem, kTmemCols);
 }
 
-template <int NQ, bool MX>
+template <int NQ, int KF>
 dsa_status_t launch_nq(const IdxParams& p, const CUtensorMap& keys, const CUtensorMap& scales,
                        const CUtensorMap& q, cudaStream_t st) {
+  using L = IdxSmem<NQ, KF == 2>;
   static std::atomic<bool> attr_set[64];
   int dev = 0;
   cudaGetDevice(&dev);
-  const size_t smem = IdxSmem<NQ>::bytes(kMaxBatch);
+  const size_t smem = L::bytes(kMaxBatch);
   if (dev < 64 && !attr_set[dev]) {
-    if (cuda_status(cudaFuncSetAttribute(indexer_kernel<NQ, MX>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+    if (cuda_status(cudaFuncSetAttribute(indexer_kernel<NQ, KF>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          (int)smem)) != DSA_OK)
       return DSA_ERR_CUDA;
     attr_set[dev] = true;
@@ -523,7 +559,7 @@ dsa_status_t launch_nq(const IdxParams& p, const CUtensorMap& keys, const CUtens
   const int64_t units_bound = (int64_t)p.batch * ((p.max_seq_len + kUnitKeys - 1) / kUnitKeys);
   const int grid = (int)std::max<int64_t>(1, std::min<int64_t>(units_bound, num_sms()));
   count_launches(1);
-  indexer_kernel<NQ, MX><<<grid, idx_threads<MX>(), IdxSmem<NQ>::bytes(p.batch), st>>>(keys, scales, q, p);
+  indexer_kernel<NQ, KF><<<grid, idx_threads<KF != 0>(), L::bytes(p.batch), st>>>(keys, scales, q, p);
   return launch_status();
 }
 
@@ -532,7 +568,8 @@ dsa_status_t launch_nq(const IdxParams& p, const CUtensorMap& keys, const CUtens
 dsa_status_t launch_index_scores(const dsa_paged_cache_t& c, const dsa_batch_t& bt, const uint8_t* q_index,
                                  const float* head_w, void* scores, bool bf16, int64_t ld, int32_t* status,
                                  cudaStream_t st) {
-  const bool mx = c.key_format == DSA_KEY_MXFP4;
+  const bool nat = c.key_format == DSA_KEY_MXFP4_NATIVE;
+  const bool mx = c.key_format == DSA_KEY_MXFP4 || nat;
   const int nq = bt.queries_per_seq;
   if (mx && nq != 1) return DSA_ERR_UNSUPPORTED;
   // more than 4 rows per sequence (a prefill chunk): a multiple of 4 rows, scored by
@@ -541,16 +578,21 @@ dsa_status_t launch_index_scores(const dsa_paged_cache_t& c, const dsa_batch_t& 
   if (nq > 4) return launch_prefill_scores(c, bt, q_index, head_w, scores, bf16, ld, status, st);
   if (bt.batch > kMaxBatch) return DSA_ERR_UNSUPPORTED;
   const uint8_t* index_base = static_cast<const uint8_t*>(c.base) + c.index_off;
-  const int code_bytes = mx ? kIdxDim / 2 : kIdxDim;  // per token
+  const int code_bytes = mx ? kIdxDim / 2 : kIdxDim;  // per token in the cache
+  const uint64_t rows = (uint64_t)bt.batch * nq;
   CUtensorMap keys, scales, qmap;
-  // codes: the pool as [num_blocks][64 tokens][128 elements], one 64-row box per page; MXFP4
-  // codes land as 8-byte packed chunks with 8-byte gaps (16 elements per 16 bytes)
+  // codes: the pool as [num_blocks][64 tokens][128 elements], one 64-row box per page.  FP8:
+  // 128-byte rows, 128-byte swizzle.  MXFP4 against the E4M3 query: the copy unpacks the codes
+  // into 8-byte chunks with 8-byte gaps (16 elements per 16 bytes), 128-byte swizzle.  Native
+  // FP4: the packed 64-byte rows as they are, 64-byte swizzle.
   {
-    const uint64_t dims[3] = {(uint64_t)kIdxDim, (uint64_t)kBlock, (uint64_t)c.num_blocks};
+    const uint64_t dims[3] = {(uint64_t)(nat ? code_bytes : kIdxDim), (uint64_t)kBlock, (uint64_t)c.num_blocks};
     const uint64_t strides[2] = {(uint64_t)code_bytes, (uint64_t)c.row_stride};
-    const uint32_t box[3] = {(uint32_t)kIdxDim, (uint32_t)kBlock, 1};
-    if (!encode_tmap(&keys, mx ? CU_TENSOR_MAP_DATA_TYPE_16U4_ALIGN16B : CU_TENSOR_MAP_DATA_TYPE_UINT8, 3, index_base,
-                     dims, strides, box, CU_TENSOR_MAP_SWIZZLE_128B))
+    const uint32_t box[3] = {(uint32_t)(nat ? code_bytes : kIdxDim), (uint32_t)kBlock, 1};
+    const CUtensorMapDataType type =
+        (mx && !nat) ? CU_TENSOR_MAP_DATA_TYPE_16U4_ALIGN16B : CU_TENSOR_MAP_DATA_TYPE_UINT8;
+    if (!encode_tmap(&keys, type, 3, index_base, dims, strides, box,
+                     nat ? CU_TENSOR_MAP_SWIZZLE_64B : CU_TENSOR_MAP_SWIZZLE_128B))
       return DSA_ERR_CUDA;
   }
   // per-token scales (fp32, or four E8M0 bytes): the pool as [num_blocks][256 B], one-row boxes for gather4
@@ -562,23 +604,28 @@ dsa_status_t launch_index_scores(const dsa_paged_cache_t& c, const dsa_batch_t& 
                      CU_TENSOR_MAP_SWIZZLE_NONE))
       return DSA_ERR_CUDA;
   }
+  // the query: E4M3 [rows * 32][128] (128-byte swizzle), or native FP4 packed [rows * 32][64]
+  // (64-byte swizzle) with its E8M0 words after the codes
   {
-    const uint64_t rows = (uint64_t)bt.batch * nq * kIdxHeads;
-    const uint64_t dims[2] = {(uint64_t)kIdxDim, rows};
-    const uint64_t strides[1] = {(uint64_t)kIdxDim};
-    const uint32_t box[2] = {(uint32_t)kIdxDim, (uint32_t)(kIdxHeads * nq)};
+    const uint64_t qrow = nat ? kIdxDim / 2 : kIdxDim;
+    const uint64_t dims[2] = {qrow, rows * kIdxHeads};
+    const uint64_t strides[1] = {qrow};
+    const uint32_t box[2] = {(uint32_t)qrow, (uint32_t)(kIdxHeads * nq)};
     if (!encode_tmap(&qmap, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, q_index, dims, strides, box,
-                     CU_TENSOR_MAP_SWIZZLE_128B))
+                     nat ? CU_TENSOR_MAP_SWIZZLE_64B : CU_TENSOR_MAP_SWIZZLE_128B))
       return DSA_ERR_CUDA;
   }
+  const uint32_t* q_scales = nat ? reinterpret_cast<const uint32_t*>(q_index + rows * kIdxHeads * (kIdxDim / 2))
+                                 : nullptr;
   IdxParams p{index_base, c.row_stride, c.num_blocks, bt.block_table, bt.max_blocks_per_seq, bt.seq_lens,
-              bt.batch, bt.max_seq_len, head_w, static_cast<float*>(scores), ld, status, bf16 ? 1 : 0};
-  if (mx) return launch_nq<1, true>(p, keys, scales, qmap, st);
+              bt.batch, bt.max_seq_len, head_w, static_cast<float*>(scores), ld, status, bf16 ? 1 : 0, q_scales};
+  if (nat) return launch_nq<1, 2>(p, keys, scales, qmap, st);
+  if (mx) return launch_nq<1, 1>(p, keys, scales, qmap, st);
   switch (nq) {
-    case 1: return launch_nq<1, false>(p, keys, scales, qmap, st);
-    case 2: return launch_nq<2, false>(p, keys, scales, qmap, st);
-    case 3: return launch_nq<3, false>(p, keys, scales, qmap, st);
-    case 4: return launch_nq<4, false>(p, keys, scales, qmap, st);
+    case 1: return launch_nq<1, 0>(p, keys, scales, qmap, st);
+    case 2: return launch_nq<2, 0>(p, keys, scales, qmap, st);
+    case 3: return launch_nq<3, 0>(p, keys, scales, qmap, st);
+    case 4: return launch_nq<4, 0>(p, keys, scales, qmap, st);
     default: return DSA_ERR_UNSUPPORTED;
   }
 }

@@ -4,8 +4,8 @@
 the chip for one layer-step, independent of how the kernels are written:
 
 * index keys: every visible token's key once per sequence — 132 B (128 E4M3
-  codes + fp32 scale) or 68 B (128 E2M1 + 4 E8M0) — all draft rows of a
-  sequence share one read;
+  codes + fp32 scale) or 68 B (128 E2M1 + 4 E8M0, with an E4M3 or a native
+  MXFP4 query) — all draft rows of a sequence share one read;
 * latents: 576 B (E4M3) or 352 B (NVFP4) for each selected token of each
   query row (up to top-k);
 * queries and head weights in, attention output (bf16 [96, 512]) and LSE
@@ -22,7 +22,9 @@ import numpy as np
 
 IDX_HEADS, IDX_DIM = 32, 128
 MLA_HEADS, LATENT, VALUE = 96, 576, 512
-KEY_BYTES = {0: 132, 1: 68}
+KEY_BYTES = {0: 132, 1: 68, 2: 68}
+# indexer query bytes per row: E4M3 [32][128], or native FP4 codes [32][64] and E8M0 [32][4]
+QUERY_BYTES = {0: IDX_HEADS * IDX_DIM, 1: IDX_HEADS * IDX_DIM, 2: IDX_HEADS * (IDX_DIM // 2 + 4)}
 LATENT_BYTES = {0: 576, 1: 352}
 
 
@@ -38,7 +40,7 @@ def step_bytes(seq_lens, nq: int = 1, topk: int = 2048, key_format: int = 0, lat
     rows = len(vis)
     keys = int(KEY_BYTES[key_format] * seq_lens.sum())
     latents = int(LATENT_BYTES[latent_format] * np.minimum(vis, topk).sum())
-    q_in = rows * (IDX_HEADS * IDX_DIM + IDX_HEADS * 4 + MLA_HEADS * LATENT * 2)
+    q_in = rows * (QUERY_BYTES[key_format] + IDX_HEADS * 4 + MLA_HEADS * LATENT * 2)
     out = rows * (MLA_HEADS * VALUE * 2 + MLA_HEADS * 4)
     return dict(keys=keys, latents=latents, queries=q_in, outputs=out,
                 total=keys + latents + q_in + out, rows=rows)
@@ -47,7 +49,7 @@ def step_bytes(seq_lens, nq: int = 1, topk: int = 2048, key_format: int = 0, lat
 def indexer_bytes(seq_lens, nq: int = 1, key_format: int = 0) -> int:
     seq_lens = np.asarray(seq_lens, dtype=np.int64)
     rows = len(seq_lens) * nq
-    return int(KEY_BYTES[key_format] * seq_lens.sum() + rows * (IDX_HEADS * IDX_DIM + IDX_HEADS * 4))
+    return int(KEY_BYTES[key_format] * seq_lens.sum() + rows * (QUERY_BYTES[key_format] + IDX_HEADS * 4))
 
 
 def mla_bytes(seq_lens, nq: int = 1, topk: int = 2048, latent_format: int = 0) -> int:

@@ -61,7 +61,7 @@
 extern "C" {
 #endif
 
-#define DSA_API_VERSION 3
+#define DSA_API_VERSION 4
 #define DSA_BLOCK_SIZE 64        /* tokens per page */
 #define DSA_INDEX_HEADS 32       /* light indexer heads */
 #define DSA_INDEX_DIM 128        /* indexer head dim */
@@ -86,9 +86,16 @@ typedef enum dsa_status {
 
 typedef enum dsa_key_format {
   DSA_KEY_FP8_E4M3 = 0,      /* 132 B/token: page = 64 x 128 B E4M3 codes, then 64 fp32 scales */
-  DSA_KEY_MXFP4 = 1          /* 68 B/token: page = 64 x 64 B packed E2M1 (element 2i in the low
+  DSA_KEY_MXFP4 = 1,         /* 68 B/token: page = 64 x 64 B packed E2M1 (element 2i in the low
                                 nibble of byte i), then 64 x 4 E8M0 scales (one per 32 elements);
-                                no per-token fp32 scale (AMD section: 132 B -> 68 B) */
+                                no per-token fp32 scale (AMD section: 132 B -> 68 B); the query
+                                is E4M3 as for FP8 keys */
+  DSA_KEY_MXFP4_NATIVE = 2   /* the MXFP4 page of DSA_KEY_MXFP4 scored against an MXFP4 query by
+                                the FP4 x FP4 block-scaled MMA (AMD section: scoring uses native
+                                FP4 matrix instructions; fused-decode section: the front end
+                                quantises the query to FP8 or MXFP4).  q_index then holds the
+                                query's packed E2M1 codes [rows][32][64] followed by its E8M0
+                                scales [rows][32][4] (one per 32 dims); head_w is used as given */
 } dsa_key_format_t;
 
 typedef enum dsa_latent_format {

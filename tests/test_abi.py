@@ -33,7 +33,7 @@ def test_every_declared_symbol_is_exported(lib):
 
 
 def test_version_and_status_strings(lib):
-    assert lib.dsa_api_version() == 3
+    assert lib.dsa_api_version() == 4
     for code in range(7):
         assert binding.status_string(code).startswith("DSA_")
     assert "unknown" in binding.status_string(99)
