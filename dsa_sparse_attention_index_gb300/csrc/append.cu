@@ -19,11 +19,14 @@
 //   MXFP4 key per 32 elements E = floor(log2 amax) - 2 clamped to [-127, 127]
 //             (-127 for an all-zero block), code = e2m1(x * 2^-E), byte E + 127
 //   query     per (row, head) s = amax / 448, code = e4m3(q / s), w' = w * s
-//             (ReLU is positively homogeneous, so the score is unchanged).
+//             (ReLU is positively homogeneous, so the score is unchanged);
+//             for native FP4 keys (DSA_KEY_MXFP4_NATIVE) the query per head
+//             and 32 dims as an MXFP4 key, w' = w (the E8M0 scales stay with
+//             the codes and the block-scaled MMA applies them).
 //
 // The fused front end (same post, same section, second bullet: the query norm,
-// the indexer's query projection, its FP8 quantisation folded into the head
-// weights, and the new token's index key, in one kernel): per row the RMSNorm
+// the indexer's query projection, its FP8 or MXFP4 quantisation folded into
+// the head weights, and the new token's index key, in one kernel): per row the RMSNorm
 // of the compressed query c (xn = bf16(c * (1 / sqrt(mean(c^2) + eps)) *
 // gamma), fp32), the projection q = W xn (4,096 outputs, bf16 operands, fp32
 // accumulation on tcgen05), the query quantisation above from the fp32 q, and
@@ -195,7 +198,9 @@ __global__ void __launch_bounds__(128)
 // and finally write their fp32 accumulators to shared memory.  After a cluster
 // barrier rank s adds the four ranks' accumulators (in rank order) for rows
 // 16 s .. 16 s + 15, takes each row's amax over the head's 128 dims and writes
-// the FP8 codes and the folded head weight.  CTA (128 + j, g): the new token of
+// the FP8 codes and the folded head weight (native FP4 keys: per 32 dims, one
+// warp's, the MXFP4 codes and E8M0 scale; the head weight as given).
+// CTA (128 + j, g): the new token of
 // row 64 g + j into the cache (threads 0..127).
 constexpr int kFeRows = 64;
 constexpr int kFeSplit = 4;                               // K ranks per head (the cluster)
@@ -229,8 +234,9 @@ struct FeParams {
   float eps;
   const float* head_w;     // fp32 [rows][32]
   int32_t rows;
-  uint8_t* q_index;        // E4M3 [rows][32][128]
+  uint8_t* q_index;        // E4M3 [rows][32][128]; native FP4: E2M1 [rows][32][64] then E8M0 [rows][32][4]
   float* head_w_out;       // fp32 [rows][32]
+  int32_t native;          // the cache's keys are scored against an MXFP4 query (DSA_KEY_MXFP4_NATIVE)
   float* q_proj;           // fp32 [rows][4096] or null
   AppendArgs app;
 };
@@ -491,10 +497,25 @@ __global__ void __launch_bounds__(kFeThreads, 2)
     for (int i = 0; i < 16; ++i) {
       const int r = 16 * rank + i;
       if (r >= nrow || !good) break;
-      const float amax = fmaxf(fmaxf(amax_s[i], amax_s[16 + i]), fmaxf(amax_s[32 + i], amax_s[48 + i]));
-      const float sc = amax > 0.f ? amax / 448.0f : 1.0f;
-      p.q_index[(int64_t)(row0 + r) * (kIdxHeads * kIdxDim) + h * kIdxDim + d] = e4m3(v[i] / sc);
-      if (t == r) p.head_w_out[(int64_t)(row0 + r) * kIdxHeads + h] = hw_t * sc;
+      const int64_t rh = (int64_t)(row0 + r) * kIdxHeads + h;
+      if (p.native) {
+        // MXFP4: this warp's 32 dims are one block; E = floor(log2 amax) - 2
+        // clamped to [-127, 127] (-127 for an all-zero block), codes
+        // e2m1(q 2^-E), as the MXFP4 keys are written; the head weight as given
+        const float am = amax_s[eq * 16 + i];
+        const uint32_t ebits = (__float_as_uint(am) >> 23) & 0xFFu;  // floor(log2 amax) + 127 for normal amax
+        const int e = (am > 0.f && ebits > 0) ? max(-127, min(127, (int)ebits - 127 - 2)) : -127;
+        const uint32_t code = (uint32_t)__nv_cvt_float_to_fp4(ldexpf(v[i], -e), __NV_E2M1, cudaRoundNearest) & 0xFu;
+        const uint32_t hi = __shfl_down_sync(0xffffffffu, code, 1);  // element 2i in the low nibble of byte i
+        if ((lane & 1) == 0) p.q_index[rh * (kIdxDim / 2) + d / 2] = (uint8_t)(code | (hi << 4));
+        if (lane == 0) p.q_index[(int64_t)p.rows * kIdxHeads * (kIdxDim / 2) + rh * 4 + quarter] = (uint8_t)(e + 127);
+        if (t == r) p.head_w_out[rh] = hw_t;
+      } else {
+        const float amax = fmaxf(fmaxf(amax_s[i], amax_s[16 + i]), fmaxf(amax_s[32 + i], amax_s[48 + i]));
+        const float sc = amax > 0.f ? amax / 448.0f : 1.0f;
+        p.q_index[rh * kIdxDim + d] = e4m3(v[i] / sc);
+        if (t == r) p.head_w_out[rh] = hw_t * sc;
+      }
     }
     cluster_wait();    // phase 3: no peer reads this rank's accumulators any more
   }
@@ -566,6 +587,7 @@ dsa_status_t launch_frontend(const dsa_paged_cache_t& c, const dsa_batch_t& bt, 
   p.rows = rows;
   p.q_index = q_index;
   p.head_w_out = head_w_out;
+  p.native = c.key_format == DSA_KEY_MXFP4_NATIVE ? 1 : 0;
   p.q_proj = q_proj;
   p.app = AppendArgs{base + c.latent_off, base + c.index_off, c.row_stride, c.num_blocks, c.key_format,
                      c.latent_format, c.latent_scale, bt.block_table, bt.max_blocks_per_seq, bt.seq_lens,

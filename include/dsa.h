@@ -444,7 +444,7 @@ dsa_status_t dsa_quantize_index_query(const uint16_t* q_bf16, const float* head_
 
 /*
  * The fused indexer front end (Day-0 post, fused-decode section, second
- * bullet: the query norm, the indexer's query projection, its FP8
+ * bullet: the query norm, the indexer's query projection, its FP8 or MXFP4
  * quantisation folded into the head weights, and the new token's index key,
  * in one kernel).  For every row r = b * queries_per_seq + j of the batch:
  *   xn[r][i]     = bf16( c_q[r][i] * (1 / sqrt(mean_i c_q[r][i]^2 + eps)) * gamma[i] )
@@ -453,7 +453,12 @@ dsa_status_t dsa_quantize_index_query(const uint16_t* q_bf16, const float* head_
  *   q[r][o]      = sum_i w_iq[o][i] * xn[r][i]   for o = h * 128 + d (bf16
  *                  operands, fp32 accumulation)
  *   q_index[r][h][d], head_w_out[r][h]   as dsa_quantize_index_query, from the
- *                  fp32 q: s = amax_d |q| / 448, codes e4m3(q / s), head_w * s
+ *                  fp32 q: s = amax_d |q| / 448, codes e4m3(q / s), head_w * s;
+ *                  for cache->key_format == DSA_KEY_MXFP4_NATIVE the query in
+ *                  MXFP4 instead: per head and 32 dims E = floor(log2 amax) - 2
+ *                  clamped to [-127, 127] (-127 for an all-zero block), codes
+ *                  e2m1(q * 2^-E), scale byte E + 127 (as the MXFP4 keys are
+ *                  written), head_w_out = head_w
  *   the row's new token written to the cache exactly as dsa_cache_append does
  *                  (new_latent[r], new_index_key[r])
  * One launch; tcgen05 does the projection.
@@ -464,7 +469,8 @@ dsa_status_t dsa_quantize_index_query(const uint16_t* q_bf16, const float* head_
  *   w_iq        device bf16 bits [4096][q_rank] (row o = h * 128 + d), 16-B aligned
  *   head_w      device fp32 [rows][32], the head weights before the scale is folded in
  *   new_latent, new_index_key   as for dsa_cache_append
- *   q_index     device [rows][32][128] E4M3 codes;  head_w_out device fp32 [rows][32]
+ *   q_index     device [rows][32][128] E4M3 codes (native FP4: [rows][32][64] packed
+ *               E2M1, then [rows][32][4] E8M0);  head_w_out device fp32 [rows][32]
  *   q_proj      device fp32 [rows][4096] or NULL: the projected q (for checks)
  * A block-table entry outside the pool raises DSA_ERR_BOUNDS in *dev_status.
  */
@@ -479,8 +485,8 @@ dsa_status_t dsa_index_frontend(const dsa_paged_cache_t* cache, const dsa_batch_
  * tokens into the cache, the indexer query from the compressed query) and
  * then dsa_decode_step over the updated cache, on one stream with no host
  * synchronisation (Day-0 post, fused-decode section: the front end, then the
- * fused indexer and the sparse attention).  The FP8 query and folded head
- * weights live in the workspace.  Arguments as for the two calls; the step's
+ * fused indexer and the sparse attention).  The FP8 (or MXFP4) query and the
+ * head weights live in the workspace.  Arguments as for the two calls; the step's
  * optional outputs as for dsa_decode_step.
  *   workspace >= dsa_frontend_workspace_size(batch, k) bytes, 256-B aligned
  */

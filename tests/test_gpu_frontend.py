@@ -60,7 +60,10 @@ def _q_tolerance(fe, xn_bits):
 def _run_frontend(case, fe):
     dc = synth.device_case(case)
     rows = case.rows
-    q_index = torch.empty((rows, 32, 128), dtype=torch.uint8, device="cuda")
+    if case.key_format == synth.KEY_MXFP4_NATIVE:   # codes [rows][32][64], then E8M0 [rows][32][4]
+        q_index = torch.empty(rows * 32 * 68, dtype=torch.uint8, device="cuda")
+    else:
+        q_index = torch.empty((rows, 32, 128), dtype=torch.uint8, device="cuda")
     w_out = torch.empty((rows, 32), dtype=torch.float32, device="cuda")
     q_proj = torch.empty((rows, 4096), dtype=torch.float32, device="cuda")
     st = _status()
@@ -79,6 +82,8 @@ def _run_frontend(case, fe):
     ([5000] * 65, 1, 512, synth.KEY_MXFP4, synth.LATENT_FP8),            # 65 rows: a second group of 1
     ([4000] * 35, 4, 64, synth.KEY_FP8, synth.LATENT_NVFP4),             # 140 rows, one K stage
     ([300], 1, 2048, synth.KEY_MXFP4, synth.LATENT_NVFP4),               # 1 row, more stages than the ring
+    ([5000] * 65, 1, 512, synth.KEY_MXFP4_NATIVE, synth.LATENT_FP8),     # the query in MXFP4
+    ([700, 64, 65], 4, 1536, synth.KEY_MXFP4_NATIVE, synth.LATENT_NVFP4),
 ])
 def test_frontend_matches_oracle(lens, nq, dim, fmt, lfmt):
     case = synth.make_case("fe", seq_lens=lens, nq=nq, key_format=fmt, seed=len(lens) + dim, latent_format=lfmt)
@@ -92,7 +97,10 @@ def test_frontend_matches_oracle(lens, nq, dim, fmt, lfmt):
     err = np.abs(q_proj.astype(np.float64) - q_ref)
     assert (err <= tol).all(), f"max excess {np.max(err - tol)} at {np.unravel_index(np.argmax(err - tol), err.shape)}"
     # codes and folded weights: the oracle's quantisation of the kernel's own q, bit for bit
-    codes_ref, w_ref = oracle.quantize_query_f32(q_proj.reshape(-1, 32, 128), fe.head_w)
+    if fmt == synth.KEY_MXFP4_NATIVE:
+        codes_ref, w_ref = oracle.quantize_query_mxfp4(q_proj.reshape(-1, 32, 128), fe.head_w)
+    else:
+        codes_ref, w_ref = oracle.quantize_query_f32(q_proj.reshape(-1, 32, 128), fe.head_w)
     np.testing.assert_array_equal(codes, codes_ref)
     np.testing.assert_array_equal(w_out, w_ref)
     # the new tokens in the cache, bit for bit
@@ -115,7 +123,8 @@ def test_frontend_reports_a_bad_block():
     assert st.item() == binding.ERR_BOUNDS
 
 
-@pytest.mark.parametrize("fmt,nq", [(synth.KEY_FP8, 1), (synth.KEY_FP8, 4), (synth.KEY_MXFP4, 1)])
+@pytest.mark.parametrize("fmt,nq", [(synth.KEY_FP8, 1), (synth.KEY_FP8, 4), (synth.KEY_MXFP4, 1),
+                                    (synth.KEY_MXFP4_NATIVE, 1)])
 def test_step_that_owns_its_cache_update_in_one_call(fmt, nq):
     """dsa_decode_step_frontend: the front end then the fused step, one call,
     one launch more than the step; its outputs equal dsa_decode_step's on the front end's
