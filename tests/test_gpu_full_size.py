@@ -7,7 +7,8 @@ long-context batch's own scores.  Tolerances as in the small-case tests.
 Workloads (seeded as the benchmark seeds them):
   speculative decode   8 sequences x 4 causal draft rows, 32,768 tokens each
   long-context batch   32 sequences, 64K-160K tokens, heavy-tailed keys
-  1M-token decode      4 sequences of 1,048,576 tokens, MXFP4 index keys
+  1M-token decode      4 sequences of 1,048,576 tokens, MXFP4 index keys (E4M3
+                       query, and MXFP4 query on the native FP4 path)
   420 B/token batch    the long-context batch with NVFP4 latents and MXFP4 keys
 """
 import dataclasses
@@ -27,6 +28,7 @@ SAMPLES = {
     "specdecode_b8x4_l32768": (0, 3, 13, 30),   # first and last draft rows of several sequences
     "longctx_b32_l64k-160k": (0, 11, 31),
     "mxfp4_b4_l1m": (0, 3),
+    "mxfp4n_b4_l1m": (1, 2),
     "longctx_b32_l64k-160k_nvfp4": (5, 31),
 }
 
@@ -36,8 +38,13 @@ def _row_case(case, r):
     table, queries and weights)."""
     b, j = divmod(r, case.nq)
     L = int(case.seq_lens[b]) - (case.nq - 1) + j
+    if case.key_format == synth.KEY_MXFP4_NATIVE:   # codes [rows][32][64], then E8M0 [rows][32][4]
+        n = case.rows * 32 * 64
+        q = np.concatenate([case.q_index[:n].reshape(case.rows, -1)[r], case.q_index[n:].reshape(case.rows, -1)[r]])
+    else:
+        q = case.q_index[r:r + 1]
     return dataclasses.replace(case, batch=1, nq=1, seq_lens=np.array([L], dtype=np.int32),
-                               block_table=case.block_table[b:b + 1], q_index=case.q_index[r:r + 1],
+                               block_table=case.block_table[b:b + 1], q_index=q,
                                head_w=case.head_w[r:r + 1], q_mla=case.q_mla[r:r + 1])
 
 
@@ -57,7 +64,8 @@ def _check_rows(case, res, rows):
         check_mla(rc, idx[r:r + 1], o[r:r + 1], l[r:r + 1])
 
 
-@pytest.mark.parametrize("name", ["specdecode_b8x4_l32768", "mxfp4_b4_l1m", "longctx_b32_l64k-160k_nvfp4"])
+@pytest.mark.parametrize("name", ["specdecode_b8x4_l32768", "mxfp4_b4_l1m", "mxfp4n_b4_l1m",
+                                  "longctx_b32_l64k-160k_nvfp4"])
 def test_full_size_decode_step_sampled_rows(name):
     case = synth.workload(name, seed=0)
     _check_rows(case, _run_step(case), SAMPLES[name])
