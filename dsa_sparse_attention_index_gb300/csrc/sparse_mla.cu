@@ -705,9 +705,11 @@ __global__ void __launch_bounds__(kThreads, 1)
 }
 
 // Merge the chunks of one row through their log-sum-exp and write bf16 O and
-// fp32 LSE (natural log).  CTA (row, group) covers 8 heads; every split's
-// partial of a float4 is loaded before any is added (loads in flight).
-constexpr int kCombineHeads = 8;
+// fp32 LSE (natural log), with the in-cluster merge's arithmetic.  CTA (group,
+// row) covers 2 heads, one output float4 per thread; a head's (max, sums) of
+// every chunk are loaded before any is used, and so is every chunk's partial of
+// a float4 (the loads in flight, not one after another).
+constexpr int kCombineHeads = 2;
 __global__ void __launch_bounds__(256) mla_combine_kernel(const uint16_t* __restrict__ opart,
                                                            const float* __restrict__ ml, int nsplit,
                                                            float latent_scale, uint16_t* out, float* lse) {
@@ -717,24 +719,34 @@ __global__ void __launch_bounds__(256) mla_combine_kernel(const uint16_t* __rest
   const float4* mlr = reinterpret_cast<const float4*>(ml) + (int64_t)row * nsplit * kHeads;
   if (threadIdx.x < kCombineHeads) {
     const int h = h0 + threadIdx.x;
+    float4 mv[kMaxSplit];
+#pragma unroll
+    for (int s = 0; s < kMaxSplit; ++s)
+      if (s < nsplit) mv[s] = mlr[s * kHeads + h];
     float M = -INFINITY;
-    for (int s = 0; s < nsplit; ++s) M = fmaxf(M, mlr[s * kHeads + h].x);
+#pragma unroll
+    for (int s = 0; s < kMaxSplit; ++s)
+      if (s < nsplit) M = fmaxf(M, mv[s].x);
     float den = 0.f, ex = 0.f;
     float w[kMaxSplit];
-    for (int s = 0; s < nsplit; ++s) {
-      const float4 v = mlr[s * kHeads + h];
+#pragma unroll
+    for (int s = 0; s < kMaxSplit; ++s) {
+      w[s] = 0.f;
+      if (s >= nsplit) continue;
+      const float4 v = mv[s];
       w[s] = (M == -INFINITY || v.x == -INFINITY) ? 0.f : ex2(v.x - M);
       den += w[s] * v.y;
       ex += w[s] * v.z;
       w[s] *= v.y;  // the partial is normalised by v.y
     }
     const float inv = den > 0.f ? latent_scale / den : 0.f;
-    for (int s = 0; s < nsplit; ++s) wgt[threadIdx.x][s] = w[s] * inv;
+#pragma unroll
+    for (int s = 0; s < kMaxSplit; ++s) wgt[threadIdx.x][s] = w[s] * inv;
     lse[(int64_t)row * kHeads + h] =
         (M == -INFINITY || ex <= 0.f) ? -INFINITY : (M + log2f(ex)) * 0.69314718055994531f;
   }
   __syncthreads();
-  constexpr int kVec = kCombineHeads * kValue / 4;  // 1024 float4s per CTA
+  constexpr int kVec = kCombineHeads * kValue / 4;  // 256 float4s per CTA
   for (int v = threadIdx.x; v < kVec; v += blockDim.x) {
     const int hl = v / (kValue / 4), d = (v % (kValue / 4)) * 4;
     const uint16_t* src = opart + ((int64_t)row * nsplit * kHeads + h0 + hl) * kValue + d;
