@@ -107,7 +107,7 @@ def lib():
 
 
 def topk_force_multipass(on: bool) -> bool:
-    """Route rows longer than 327,680 tokens through the four-kernel top-k
+    """Route rows longer than 245,760 tokens through the four-kernel top-k
     (True) or the automatic choice (False); returns the previous setting."""
     return bool(lib().dsa_topk_force_multipass(int(bool(on))))
 

@@ -20,11 +20,20 @@
 // chosen indices in ascending order at a place from warp and cluster scans.
 // No workspace is used.
 //
-// Longer rows (the 1M-token rows) take the same kernel in its streaming form:
-// a cluster of 16 CTAs per row (8 where the device cannot schedule 16) that
-// reads its slice again from L2 in every pass and keeps only the histograms
-// in shared memory.  Where neither cluster can be scheduled, four kernels
-// over a workspace do the selection:
+// Longer rows (the 1M-token rows) with fp32 scores and a workspace take two
+// levels of the same kernel: pass 1 selects the top-k of every segment of at
+// most 163,840 tokens (one cluster per segment, as many segments as fill the
+// SMs, so few long rows still use them all) and writes it, with the scores,
+// into the row's compact candidate list in token order; pass 2 selects the
+// row's top-k among those candidates.  The result is exact: a token of the
+// row's top-k is also in its own segment's top-k, and the compact rows keep
+// token order, so ties still go to the lower index.
+// Without a workspace (bf16 scores, the no-allocation entry point) they take
+// the kernel's streaming form: a cluster of 16 CTAs per row (8 where the
+// device cannot schedule 16) that reads its slice again from L2 in every pass
+// and keeps only the histograms in shared memory.  Where the four-kernel form
+// is forced, or no cluster can be scheduled, four kernels over a workspace do
+// the selection:
 //   1. hist:    multi-CTA per row: 4096-bin histogram of the key's top 12
 //               bits, merged into a per-row global histogram.
 //   2. threshold: one CTA per row finds the bin T holding the k-th largest
@@ -638,16 +647,37 @@ __device__ __forceinline__ uint32_t warp_excl_scan(uint32_t v, uint32_t& total) 
 // registers); streaming: one.
 // In: the score element, float or uint16_t (bf16 bits, widened exactly to
 // fp32 as they are read; the selection is then the fp32 one).
+// The two-level form for long rows.  Pass 1 (nseg > 0): launch row v is
+// segment p = v % nseg of score row r = v / nseg, tokens [p seg, (p+1) seg),
+// and its top-k goes straight into row r's compact candidate list at
+// positions p k + i (every segment before p is full, so holds k of them):
+// the token index to cand_idx, its score to cand_score.  Pass 2 (pass2 set):
+// launch row r is that compact row, floor(len / seg) k + min(k, len % seg)
+// candidates for a score row of len tokens, and an output position i is
+// written as cand_idx[r][i], the candidate's token index.  The compact rows
+// are in token order.  All zero: the plain top-k of each score row.
+struct TopkSeg {
+  int32_t seg_tokens = 0;
+  int32_t nseg = 0;
+  bool pass2 = false;
+  float* cand_score = nullptr;
+  int32_t* cand_idx = nullptr;
+  int64_t ldc = 0;
+  int32_t longest = 0;  // the longest launch row (0: cap)
+};
+
 template <int C, bool kStream, typename In>
 __global__ void __launch_bounds__(kResThreads, kStream ? 1 : 2)
     topk_cluster_kernel(const In* __restrict__ scores, int64_t ld, const int32_t* row_lens,
                         const int32_t* seq_lens, int nq, int cap, int k, int32_t* out, int32_t* status,
-                        int slice_cap, const TopkPhys po) {
+                        int slice_cap, const TopkPhys po, const TopkSeg sg) {
   constexpr bool kF32 = std::is_same<In, float>::value;
   using G = typename std::conditional<kStream, float4, uint4>::type;  // a group of 4 elements
   cg::cluster_group cluster = cg::this_cluster();
   const int c = (int)cluster.block_rank();
-  const int r = blockIdx.x / C, tid = threadIdx.x, lane = tid & 31, wid = tid >> 5;
+  const int rv = blockIdx.x / C, tid = threadIdx.x, lane = tid & 31, wid = tid >> 5;  // the launch's row
+  const int r = sg.nseg ? rv / sg.nseg : rv;       // the score row
+  const int seg_p = sg.nseg ? rv % sg.nseg : 0;    // the segment of it (pass 1)
   auto csync = [&]() {  // a one-CTA cluster needs only the block barrier
     if (C == 1) __syncthreads();
     else cluster.sync();
@@ -663,14 +693,30 @@ __global__ void __launch_bounds__(kResThreads, kStream ? 1 : 2)
   uint32_t* misc = scan + 32;
   const uint32_t load_bars = smem_u32(misc + 32);  // kLoadChunks mbarriers, 8 bytes each
 
-  const int len = row_len(row_lens, seq_lens, nq, r, cap, c == 0 ? status : nullptr);
-  int32_t* o = out + (int64_t)r * k;
-  auto emit = [&](int64_t pos_, int t_) {  // index t_ at output position pos_, and its physical row
-    o[pos_] = t_;
-    if (po.phys) po.phys[(int64_t)r * k + pos_] = phys_row(po, nq, r, t_, status);
-  };
-  grid_dep_wait();  // the scores come from the previous kernel, which may still read `out`
+  // the scores (and in the two-level form's second pass the row lengths and
+  // index map) come from the previous kernel, which may also still read `out`
+  grid_dep_wait();
   grid_dep_launch();
+  int len = row_len(row_lens, seq_lens, nq, r, cap, (c == 0 && seg_p == 0 && !sg.pass2) ? status : nullptr);
+  if (sg.nseg) len = max(0, min(sg.seg_tokens, len - seg_p * sg.seg_tokens));
+  if (sg.pass2) len = (len / sg.seg_tokens) * k + min(k, len % sg.seg_tokens);
+  int32_t* o = sg.nseg ? nullptr : out + (int64_t)rv * k;  // pass 1 writes the candidate rows instead
+  auto emit = [&](int64_t pos_, int t_) {  // index t_ at output position pos_, and its physical row
+    if (sg.nseg) {  // pass 1: into the compact candidate row
+      if (t_ >= 0) {
+        const int64_t tok = (int64_t)seg_p * sg.seg_tokens + t_;
+        const int64_t at = (int64_t)r * sg.ldc + (int64_t)seg_p * k + pos_;
+        sg.cand_idx[at] = (int32_t)tok;
+        const In x = scores[(int64_t)r * ld + tok];
+        if constexpr (kF32) sg.cand_score[at] = x;
+        else sg.cand_score[at] = __uint_as_float((uint32_t)x << 16);
+      }
+      return;
+    }
+    if (sg.pass2 && t_ >= 0) t_ = sg.cand_idx[(int64_t)r * sg.ldc + t_];
+    o[pos_] = t_;
+    if (po.phys) po.phys[(int64_t)rv * k + pos_] = phys_row(po, nq, r, t_, status);
+  };
   if (len <= k) {  // the same branch for every CTA of the cluster
     if (c == 0)
       for (int i = tid; i < k; i += kResThreads) emit(i, i < len ? i : -1);
@@ -681,7 +727,7 @@ __global__ void __launch_bounds__(kResThreads, kStream ? 1 : 2)
   const int start = c * S;
   const int n = max(0, min(S, len - start));
   const int n4 = (n + 3) >> 2;  // groups of 4; the last one is padded with NaN / key 0 (never counted)
-  const In* row = scores + (int64_t)r * ld + start;
+  const In* row = scores + (int64_t)r * ld + (int64_t)seg_p * sg.seg_tokens + start;
   const int full4 = n >> 2;
   auto widen = [](In x) -> float {
     if constexpr (kF32) return x;
@@ -1153,7 +1199,7 @@ __global__ void __launch_bounds__(kResThreads, kStream ? 1 : 2)
 template <int C, bool kStream, typename In>
 dsa_status_t launch_cluster(const In* scores, int64_t ld, const int32_t* row_lens, const int32_t* seq_lens,
                             int nq, int rows, int cap, int k, int32_t* out, int32_t* status, cudaStream_t st,
-                            const TopkPhys& po) {
+                            const TopkPhys& po, const TopkSeg& sg = TopkSeg{}) {
   static std::atomic<bool> attr_set[64];
   int dev = 0;
   cudaGetDevice(&dev);
@@ -1168,10 +1214,11 @@ dsa_status_t launch_cluster(const In* scores, int64_t ld, const int32_t* row_len
       return DSA_ERR_CUDA;
     attr_set[dev] = true;
   }
-  // each CTA's slice of the longest row, rounded up to 4 keys
-  const int slice = (((cap + C - 1) / C) + 3) & ~3;
+  // each CTA's slice of the longest row (segment), rounded up to 4 keys
+  const int longest = sg.longest ? sg.longest : cap;
+  const int slice = (((longest + C - 1) / C) + 3) & ~3;
   cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3((unsigned)(rows * C));
+  cfg.gridDim = dim3((unsigned)(rows * (sg.nseg ? sg.nseg : 1) * C));
   cfg.blockDim = dim3(kResThreads);
   cfg.dynamicSmemBytes = res_smem(kStream ? 0 : slice);
   cfg.stream = st;
@@ -1186,7 +1233,7 @@ dsa_status_t launch_cluster(const In* scores, int64_t ld, const int32_t* row_len
   cfg.numAttrs = 2;
   count_launches(1);
   if (cuda_status(cudaLaunchKernelEx(&cfg, topk_cluster_kernel<C, kStream, In>, scores, ld, row_lens, seq_lens, nq, cap,
-                                     k, out, status, slice, po)) != DSA_OK)
+                                     k, out, status, slice, po, sg)) != DSA_OK)
     return DSA_ERR_CUDA;
   return launch_status();
 }
@@ -1227,12 +1274,35 @@ size_t ws_bytes(int rows, int k) {
          al((size_t)rows * kCandCap * 8);
 }
 
+// The two-level form for rows longer than a cluster holds: segments of at
+// most kSegMax tokens (8 CTAs of 20,480 keys, two CTAs per SM), more of them
+// where that fills the SMs better (down to kSegMin tokens), each reduced to
+// its top-k; then one more top-k over the rows' candidates.  Few long rows
+// then spread over all SMs.  The workspace holds the candidates of up to
+// kSlotsMax / 8 segments per row (or the fewest that cover the row).
+constexpr int kSegMax = 8 * 20480;
+constexpr int kSegMin = 8 * 4096;
+constexpr int kSlotsMax = 2 * 192;  // CTA slots the segment count aims at, on devices up to 192 SMs
+int two_level_max_nseg(int rows, int max_row_len) {
+  const int need = (max_row_len + kSegMax - 1) / kSegMax;
+  const int fill = std::min(kSlotsMax / (8 * std::max(rows, 1)), (max_row_len + kSegMin - 1) / kSegMin);
+  return std::max(need, fill);
+}
+int64_t two_level_ldc(int nseg, int k) { return ((int64_t)nseg * k + 3) & ~int64_t(3); }
+size_t two_level_bytes(int rows, int max_row_len, int k) {
+  auto al = [](size_t x) { return (x + 255) & ~size_t(255); };
+  const size_t plane = al((size_t)rows * two_level_ldc(two_level_max_nseg(rows, max_row_len), k) * 4);
+  return 2 * plane;  // candidate scores, then their token indices
+}
+
 }  // namespace
 
 size_t topk_workspace_bytes(int rows, int max_row_len, int k) {
-  // rows that fit a cluster's shared memory (or need no selection) use none
+  // rows that fit a cluster's shared memory (or need no selection) use none;
+  // longer rows: the two-level form, or the four-kernel form where clusters
+  // cannot be scheduled or it is forced
   if (max_row_len <= k || (max_row_len + kResKeys - 1) / kResKeys <= kResMaxCluster) return 0;
-  return ws_bytes(rows, k);
+  return std::max(ws_bytes(rows, k), two_level_bytes(rows, max_row_len, k));
 }
 
 namespace {
@@ -1245,34 +1315,88 @@ size_t topk_final_smem_bytes() { return (size_t)kWindowBits / 8 + 8 * kCandCap +
 
 namespace {
 
+// Cluster size of the row-resident form for `rows` rows of at most `len`
+// keys: enough CTAs to hold a row, small enough slices for two CTAs per SM
+// where a cluster of 8 allows it, and for few rows enough CTAs to spread them
+// over the SMs (at least 8,192 keys per CTA).
+int resident_cluster(int rows, int len) {
+  const int c_min = (len + kResKeys - 1) / kResKeys;
+  // two CTAs per SM pay off only while the grid stays within one wave
+  int c_pair = std::min(kResMaxCluster, (len + kResPairKeys - 1) / kResPairKeys);
+  if ((int64_t)rows * c_pair > 2 * (int64_t)num_sms()) c_pair = 1;
+  const int c_fill = std::min(num_sms() / std::max(rows, 1), len / 8192);
+  return std::min(kResMaxCluster, std::max(std::max(c_min, c_pair), std::max(c_fill, 1)));
+}
+
+template <bool kStream, typename In>
+dsa_status_t launch_cluster_sized(int cluster, const In* scores, int64_t ld, const int32_t* row_lens,
+                                  const int32_t* seq_lens, int nq, int rows, int cap, int k, int32_t* out,
+                                  int32_t* status, cudaStream_t st, const TopkPhys& po, const TopkSeg& sg) {
+#define DSA_RES(C) launch_cluster<C, kStream, In>(scores, ld, row_lens, seq_lens, nq, rows, cap, k, out, status, st, po, sg)
+  switch (cluster) {
+    case 1: return DSA_RES(1);
+    case 2: return DSA_RES(2);
+    case 3: return DSA_RES(3);
+    case 4: return DSA_RES(4);
+    case 5: return DSA_RES(5);
+    case 6: return DSA_RES(6);
+    case 7: return DSA_RES(7);
+    default: return DSA_RES(8);
+  }
+#undef DSA_RES
+}
+
+// Rows longer than a cluster holds (fp32 scores, a workspace): pass 1 reduces
+// every segment to its top-k, written into each row's compact candidate list
+// (token order, with the scores), and pass 2 selects the row's top-k among
+// them, writing token indices (and physical rows).  The result is the top-k
+// of the whole row: every token of it is among its own segment's top-k.  Two
+// launches, chained by programmatic dependent launch.  Both passes use
+// clusters of up to 8 CTAs, as many as two CTAs per SM allow.
+dsa_status_t launch_topk_two_level(const float* scores, int64_t ld, const int32_t* row_lens, const int32_t* seq_lens,
+                                   int nq, int rows, int max_row_len, int k, int32_t* out, void* workspace,
+                                   int32_t* status, cudaStream_t st, const TopkPhys& po) {
+  const int slots = 2 * num_sms();
+  const int need = (max_row_len + kSegMax - 1) / kSegMax;
+  const int nseg = std::min(two_level_max_nseg(rows, max_row_len),
+                            std::max(need, std::min(slots / (8 * rows), (max_row_len + kSegMin - 1) / kSegMin)));
+  const int seg = (((max_row_len + nseg - 1) / nseg) + 3) & ~3;  // bulk copies start on 16 bytes
+  const int64_t ldc = two_level_ldc(nseg, k);
+  const size_t plane = ((size_t)rows * ldc * 4 + 255) & ~size_t(255);
+  TopkSeg s1;
+  s1.seg_tokens = seg;
+  s1.nseg = nseg;
+  s1.cand_score = static_cast<float*>(workspace);
+  s1.cand_idx = reinterpret_cast<int32_t*>(static_cast<uint8_t*>(workspace) + plane);
+  s1.ldc = ldc;
+  s1.longest = std::min(max_row_len, seg);
+  auto cluster_for = [&](int vrows, int len) {
+    const int c_min = (len + kResKeys - 1) / kResKeys;
+    if ((int64_t)vrows * kResMaxCluster <= slots) return kResMaxCluster;
+    return std::max(c_min, resident_cluster(vrows, len));
+  };
+  dsa_status_t res = launch_cluster_sized<false, float>(cluster_for(rows * nseg, s1.longest), scores, ld, row_lens,
+                                                        seq_lens, nq, rows, max_row_len, k, nullptr, status, st,
+                                                        TopkPhys{}, s1);
+  if (res != DSA_OK) return res;
+  TopkSeg s2 = s1;
+  s2.nseg = 0;
+  s2.pass2 = true;
+  s2.longest = (max_row_len / seg) * k + std::min(k, max_row_len % seg);
+  return launch_cluster_sized<false, float>(cluster_for(rows, s2.longest), s1.cand_score, ldc, row_lens, seq_lens, nq,
+                                            rows, max_row_len, k, out, status, st, po, s2);
+}
+
 // The cluster paths: true with *res set when one of them took the rows.
 template <typename In>
 bool launch_topk_cluster(const In* scores, int64_t ld, const int32_t* row_lens, const int32_t* seq_lens, int nq,
                          int rows, int max_row_len, int k, int32_t* out, int32_t* status, cudaStream_t st,
                          dsa_status_t* res, const TopkPhys& po) {
-  // row-resident path: one cluster per row, enough CTAs to hold the row, small
-  // enough slices for two CTAs per SM where a cluster of 8 allows it, and for
-  // few rows enough CTAs to spread them over the SMs (at least 8,192 keys per CTA)
+  // row-resident path: one cluster per row (resident_cluster), no workspace
   const int c_min = (max_row_len + kResKeys - 1) / kResKeys;
-  // two CTAs per SM pay off only while the grid stays within one wave
-  int c_pair = std::min(kResMaxCluster, (max_row_len + kResPairKeys - 1) / kResPairKeys);
-  if ((int64_t)rows * c_pair > 2 * (int64_t)num_sms()) c_pair = 1;
-  const int c_fill = std::min(num_sms() / std::max(rows, 1), max_row_len / 8192);
-  const int cluster = std::min(kResMaxCluster, std::max(std::max(c_min, c_pair), std::max(c_fill, 1)));
   if (max_row_len > k && c_min <= kResMaxCluster) {
-    // row-resident path: one cluster of `cluster` CTAs per row, no workspace
-#define DSA_RES(C) launch_cluster<C, false, In>(scores, ld, row_lens, seq_lens, nq, rows, max_row_len, k, out, status, st, po)
-    switch (cluster) {
-      case 1: *res = DSA_RES(1); break;
-      case 2: *res = DSA_RES(2); break;
-      case 3: *res = DSA_RES(3); break;
-      case 4: *res = DSA_RES(4); break;
-      case 5: *res = DSA_RES(5); break;
-      case 6: *res = DSA_RES(6); break;
-      case 7: *res = DSA_RES(7); break;
-      default: *res = DSA_RES(8); break;
-    }
-#undef DSA_RES
+    *res = launch_cluster_sized<false, In>(resident_cluster(rows, max_row_len), scores, ld, row_lens, seq_lens, nq,
+                                           rows, max_row_len, k, out, status, st, po, TopkSeg{});
     return true;
   }
   if (max_row_len > k && !g_force_multipass.load(std::memory_order_relaxed)) {
@@ -1306,11 +1430,21 @@ dsa_status_t launch_topk_bf16(const uint16_t* scores, int64_t ld, const int32_t*
   return DSA_ERR_UNSUPPORTED;
 }
 
-dsa_status_t launch_topk(const float* scores, int64_t ld, const int32_t* row_lens, const int32_t* seq_lens, int nq,
-                         int rows, int max_row_len, int k, int32_t* out, void* workspace, int32_t* status,
-                         cudaStream_t st, const TopkPhys& po) {
+namespace {
+
+// two_level: rows longer than a cluster holds may take the two-level form
+// (the workspace then holds at least two_level(...).bytes); otherwise the
+// streaming cluster, or the four-kernel form where it is forced or no cluster
+// can be scheduled.
+dsa_status_t launch_topk_impl(const float* scores, int64_t ld, const int32_t* row_lens, const int32_t* seq_lens,
+                              int nq, int rows, int max_row_len, int k, int32_t* out, void* workspace,
+                              int32_t* status, cudaStream_t st, const TopkPhys& po, bool two_level_ok) {
   if (rows == 0) return DSA_OK;
   dsa_status_t res = DSA_OK;
+  if (two_level_ok && max_row_len > kResMaxCluster * kResKeys && workspace &&
+      !g_force_multipass.load(std::memory_order_relaxed))
+    return launch_topk_two_level(scores, ld, row_lens, seq_lens, nq, rows, max_row_len, k, out, workspace, status, st,
+                                 po);
   if (launch_topk_cluster(scores, ld, row_lens, seq_lens, nq, rows, max_row_len, k, out, status, st, &res, po))
     return res;
   auto al = [](size_t x) { return (x + 255) & ~size_t(255); };
@@ -1350,6 +1484,15 @@ dsa_status_t launch_topk(const float* scores, int64_t ld, const int32_t* row_len
   return launch_status();
 }
 
+}  // namespace
+
+dsa_status_t launch_topk(const float* scores, int64_t ld, const int32_t* row_lens, const int32_t* seq_lens, int nq,
+                         int rows, int max_row_len, int k, int32_t* out, void* workspace, int32_t* status,
+                         cudaStream_t st, const TopkPhys& po) {
+  return launch_topk_impl(scores, ld, row_lens, seq_lens, nq, rows, max_row_len, k, out, workspace, status, st, po,
+                          true);
+}
+
 // ---------------------------------------------------------------- top-k with built-in scratch
 // The scratch the top-k needs (histograms, counters, selected and candidate
 // lists) for up to kNoAllocMaxRows rows of any length with k <= 2048, kept in
@@ -1385,7 +1528,9 @@ dsa_status_t launch_topk_noalloc(const float* scores, int64_t ld, const int32_t*
     }
     scratch = g_scratch_addr[dev];
   }
-  return launch_topk(scores, ld, row_lens, nullptr, 1, rows, max_row_len, k, out, scratch, status, st, TopkPhys{});
+  // the streaming cluster for long rows (the scratch is sized for the four-kernel form)
+  return launch_topk_impl(scores, ld, row_lens, nullptr, 1, rows, max_row_len, k, out, scratch, status, st, TopkPhys{},
+                          false);
 }
 
 }  // namespace dsa

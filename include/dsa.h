@@ -205,12 +205,15 @@ dsa_status_t dsa_topk(const float* scores, int64_t ld_scores, const int32_t* row
 
 /*
  * Which top-k kernels serve rows longer than 245,760 tokens.  By default
- * (on = 0) such rows take one launch of a thread-block cluster per row (16
- * CTAs, or 8 where the device cannot schedule 16) and the workspace goes
- * unused; where neither cluster can be scheduled, four kernels over the
+ * (on = 0), in dsa_topk, dsa_topk_paged and the decode steps with fp32
+ * scores, such rows take two levels of the cluster kernel over the
+ * workspace: the top-k of every segment of at most 163,840 tokens, then the
+ * top-k of the row's candidates (two launches).  dsa_topk_noalloc takes one launch of a
+ * streaming cluster per row (16 CTAs, or 8 where the device cannot schedule
+ * 16); where neither cluster can be scheduled, four kernels over the
  * workspace do the selection.  on != 0 selects the four-kernel path for every
  * later call in this process (all threads and devices), for testing it or for
- * a device shared with work that clusters would contend with.  Both paths give
+ * a device shared with work that clusters would contend with.  All paths give
  * the same indices.  Returns the previous setting; never fails.
  */
 int32_t dsa_topk_force_multipass(int32_t on);

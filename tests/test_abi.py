@@ -110,6 +110,8 @@ def test_workspace_sizes(lib):
     ws = lib.dsa_workspace_size(ctypes.byref(b), 2048)
     assert ws >= 32 * 163840 * 4  # holds the scores
     assert lib.dsa_topk_workspace_size(4, 1 << 20, 2048) > 0
+    # two levels for long rows: at least 7 segments' candidates, their scores and tokens
+    assert lib.dsa_topk_workspace_size(4, 1 << 20, 2048) >= 2 * 4 * 7 * 2048 * 4
     assert lib.sparse_mla_workspace_size(32, 2048) >= 32 * 96 * 512 * 2  # fp16 partials
     assert lib.dsa_topk_workspace_size(32, 163840, 2048) == 0  # rows held in shared memory
     assert lib.dsa_topk_workspace_size(4, 100, 0) == 0

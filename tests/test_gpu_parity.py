@@ -182,14 +182,16 @@ def test_topk_cluster_sizes(n):
     np.testing.assert_array_equal(got, oracle.topk(m.astype(np.float64), lens, 2048))
 
 
-@pytest.mark.parametrize("multipass", [False, True])
+@pytest.mark.parametrize("path", ["two_level", "multipass", "streaming"])
 @pytest.mark.parametrize("n", [245_761, 1_000_000, 2_000_003])
-def test_topk_long_rows_on_both_paths(n, multipass):
-    """Rows past 8 x 30,720 tokens: the streaming cluster kernel (one launch)
-    and the four-kernel path (forced), bit-exact against the oracle, with rows
-    of mixed lengths in one call (one shorter than k, one far shorter than
-    the longest) and heavy ties on the k-th key."""
-    rng = np.random.default_rng(n + multipass)
+def test_topk_long_rows_on_all_paths(n, path):
+    """Rows past 8 x 30,720 tokens: the two-level cluster form (two
+    launches), the four-kernel path (forced) and the streaming cluster (the
+    no-allocation entry point, one launch), bit-exact against the oracle,
+    with rows of mixed lengths in one call (one shorter than k, one far
+    shorter than the longest, ties across segment boundaries) and heavy ties
+    on the k-th key."""
+    rng = np.random.default_rng(n + len(path))
     ld = (n + 3) // 4 * 4
     m = np.zeros((6, ld), dtype=np.float32)
     m[0, :n] = rng.integers(0, 50, n)                 # ties on the k-th key
@@ -202,21 +204,53 @@ def test_topk_long_rows_on_both_paths(n, multipass):
     m[5, :n] = -rng.exponential(1.0, n)             # all negative, top at the row's end
     m[5, n - 2048:n] = 1.0 + rng.random(2048)
     lens = np.array([n, n, n - 5, 1000, 50_001, n - 3], dtype=np.int32)
-    prev = binding.topk_force_multipass(multipass)
+    prev = binding.topk_force_multipass(path == "multipass")
     try:
         n0 = binding.kernel_launches()
-        got = _gpu_topk(torch.from_numpy(m).cuda(), torch.from_numpy(lens).cuda(), 2048, max_row_len=n)
+        if path == "streaming":
+            scores = torch.from_numpy(m).cuda()
+            idx = torch.full((6, 2048), -7, dtype=torch.int32, device="cuda")
+            st = _status()
+            binding.topk_noalloc(scores, torch.from_numpy(lens).cuda(), n, 2048, idx, st)
+            torch.cuda.synchronize()
+            assert st.item() == 0, binding.status_string(st.item())
+            got = idx.cpu().numpy()
+        else:
+            got = _gpu_topk(torch.from_numpy(m).cuda(), torch.from_numpy(lens).cuda(), 2048, max_row_len=n)
         launches = binding.kernel_launches() - n0
     finally:
         binding.topk_force_multipass(prev)
-    assert launches == (4 if multipass else 1)
+    assert launches == {"two_level": 2, "multipass": 4, "streaming": 1}[path]
+    np.testing.assert_array_equal(got, oracle.topk(m.astype(np.float64), lens, 2048))
+
+
+@pytest.mark.parametrize("n", [491_521, 1_048_579])
+def test_topk_two_level_segment_boundaries(n):
+    """The two-level form splits a row into segments: the row's top-k
+    concentrated in one segment (more than k of them there); 2,049 tokens
+    tied at the top spread over the whole row, so every segment keeps some
+    and the lowest 2,048 indices must win across segments; heavy ties
+    everywhere; NaN scores among them."""
+    ld = (n + 3) // 4 * 4
+    rng = np.random.default_rng(n)
+    m = np.full((4, ld), -1.0, dtype=np.float32)
+    m[0, :n] = rng.standard_normal(n)
+    m[0, 300_001:305_001] = 10.0 + rng.random(5000)
+    m[1, :n] = 0.5
+    m[1, np.linspace(0, n - 1, 2049).astype(np.int64)] = 5.0
+    m[2, :n] = rng.integers(0, 4, n)
+    m[3, :n] = rng.standard_normal(n)
+    m[3, :n:1000] = np.nan
+    m[3, n - 1] = np.inf
+    lens = np.array([n, n, n - 7, n], dtype=np.int32)
+    got = _gpu_topk(torch.from_numpy(m).cuda(), torch.from_numpy(lens).cuda(), 2048, max_row_len=n)
     np.testing.assert_array_equal(got, oracle.topk(m.astype(np.float64), lens, 2048))
 
 
 @pytest.mark.parametrize("lens,launches", [
     ([3000] * 32, 3),        # 4 chunks per row: the MLA merges them itself (a cluster per row)
     ([9000, 130], 4),        # 16 chunks per row: plus the combine kernel
-    ([400_000], 4),          # the streaming cluster top-k, 16 chunks
+    ([400_000], 5),          # the two-level top-k (two launches), 16 chunks
 ])
 def test_decode_step_launch_count(lens, launches):
     """A fused decode step launches the indexer, the top-k and the sparse MLA,

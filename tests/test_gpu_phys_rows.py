@@ -30,7 +30,8 @@ def _topk_paged(case, dc, scores, k=2048, with_phys=True):
 @pytest.mark.parametrize("lens,nq,multipass", [
     ([6000, 2500, 900, 40], 1, False),        # cluster top-k; a row shorter than k
     ([9000, 3000], 4, False),                 # draft rows share their sequence's table row
-    ([260_000, 3000], 1, False),              # the streaming cluster
+    ([260_000, 3000], 1, False),              # the two-level cluster form
+    ([200_000, 340_000], 2, False),           # two levels with draft rows (2 segments and 3)
     ([260_000, 3000], 1, True),               # the four-kernel path
 ])
 def test_topk_paged_rows_match_the_oracle(lens, nq, multipass):
