@@ -1274,6 +1274,427 @@ size_t ws_bytes(int rows, int k) {
          al((size_t)rows * kCandCap * 8);
 }
 
+// ------------------------------------------------------------ many rows
+// Many rows of at most kRowMaxLen tokens (a prefill chunk's rows): one CTA
+// per row at a time, persistent over the rows, each row streamed from global
+// memory rather than held on chip, so that a row per SM is in flight instead
+// of a row per cluster.
+//   1. One pass over the row: histogram of the keys' top 12 bits, and the bin
+//      holding the k-th key (the threshold group).
+//   2. While the group holds more than half the candidate buffer, one more
+//      pass refines it by the next 10 bits.
+//   3. One pass marks the keys above the group in bitmap A and moves the
+//      group's keys with their indices into shared memory, each warp into a
+//      region of its own (no shared counter); a group of one key value (all
+//      32 bits fixed) goes straight into bitmap B.  If a warp's region
+//      overflows, the group is refined once more and the pass repeated.
+//   4. The remaining digits over the candidates in shared memory give the
+//      exact k-th key; candidates above it go into A, those equal to it into B.
+//   5. B keeps its `need` lowest indices (ties to the lower index), and the
+//      indices of A | B are written in ascending order.
+constexpr int kRowThreads = 512;              // two CTAs per SM: one streams while the other selects
+constexpr int kRowWarps = kRowThreads / 32;
+constexpr int kRowMaxLen = 163840;           // bitmaps of 5,120 words each
+constexpr int kRowWords = kRowMaxLen / 32;
+constexpr int kRowB1 = 4096;                 // first digit: key bits 31..20
+constexpr int kRowD = 10;                    // later digits: bits 19..10, then 9..0
+constexpr int kRowCand = 6144;               // group keys held in shared memory, ...
+constexpr int kRowWarpCand = kRowCand / kRowWarps;  // ... in one region per warp
+constexpr int kRowGroupMax = kRowCand / 2;   // larger groups are narrowed first
+constexpr int kRowU = 4;                     // 16-byte loads in flight per thread
+constexpr size_t kRowSmem = (size_t)(kRowB1 + 2 * kRowWords + 2 * kRowCand + 96) * 4;
+static_assert(kRowWarps <= 32, "the block scan holds the warp totals in one warp's lanes");
+// a row of at most kRowCand tokens puts at most kRowWarpCand of them in each warp's stripe
+static_assert(kRowCand % (4 * kRowThreads) == 0, "whole passes of the stream loop");
+
+// Exclusive prefix sum of v over the CTA's threads in thread order; `total`
+// is the sum over all of them.  ws: kRowWarps words.  Two barriers.
+__device__ __forceinline__ uint32_t row_block_scan(uint32_t v, uint32_t* ws, uint32_t& total) {
+  const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5;
+  uint32_t x = v;
+#pragma unroll
+  for (int d = 1; d < 32; d <<= 1) {
+    const uint32_t y = __shfl_up_sync(0xffffffffu, x, d);
+    if (lane >= d) x += y;
+  }
+  __syncthreads();  // ws is free
+  if (lane == 31) ws[wid] = x;
+  __syncthreads();
+  const uint32_t w = lane < kRowWarps ? ws[lane] : 0u;
+  uint32_t wsum = w;
+#pragma unroll
+  for (int d = 1; d < 32; d <<= 1) {
+    const uint32_t y = __shfl_up_sync(0xffffffffu, wsum, d);
+    if (lane >= d) wsum += y;
+  }
+  total = __shfl_sync(0xffffffffu, wsum, 31);
+  return __shfl_sync(0xffffffffu, wsum - w, wid) + x - v;
+}
+
+// The bin of histogram h (nb bins, nb a multiple of the thread count) that
+// holds the need-th largest key counting from the top, need within it, and
+// its count.  Thread t sums the bins [nb - (t+1) per, nb - t per), so the
+// scan in thread order counts the keys above each thread's bins.  res: 3
+// words, read after the closing barrier.  Opens with a barrier, so the
+// histogram's last increments are complete.
+struct RowPick {
+  uint32_t bin, need, pop;
+};
+__device__ __forceinline__ RowPick row_pick(const uint32_t* h, int nb, uint32_t need, uint32_t* ws, uint32_t* res) {
+  const int per = nb / kRowThreads;
+  const int hi = nb - (int)threadIdx.x * per;
+  __syncthreads();  // the histogram is complete
+  if (threadIdx.x == 0) {  // only kept if the counts were inconsistent
+    res[0] = 0u;
+    res[1] = 1u;
+    res[2] = 0u;
+  }
+  uint32_t sum = 0;
+  for (int j = 1; j <= per; ++j) sum += h[hi - j];
+  uint32_t tot;
+  const uint32_t above = row_block_scan(sum, ws, tot);
+  if (above < need && need <= above + sum) {
+    uint32_t a = above;
+    for (int j = 1; j <= per; ++j) {
+      const uint32_t c = h[hi - j];
+      if (need <= a + c) {
+        res[0] = (uint32_t)(hi - j);
+        res[1] = need - a;
+        res[2] = c;
+        break;
+      }
+      a += c;
+    }
+  }
+  __syncthreads();
+  return RowPick{res[0], res[1], res[2]};
+}
+
+__global__ void __launch_bounds__(kRowThreads, 2)
+    topk_row_kernel(const float* __restrict__ scores, int64_t ld, const int32_t* row_lens, const int32_t* seq_lens,
+                    int nq, int rows, int cap, int k, int32_t* out, int32_t* status, const TopkPhys po) {
+  extern __shared__ __align__(16) uint32_t rsm[];
+  uint32_t* hist = rsm;               // kRowB1 bins (1,024 in the later digits)
+  uint32_t* bmA = hist + kRowB1;      // tokens above the k-th key
+  uint32_t* bmB = bmA + kRowWords;    // tokens equal to it
+  uint32_t* ckey = bmB + kRowWords;   // the group's keys ...
+  uint32_t* cidx = ckey + kRowCand;   // ... and their token indices
+  uint32_t* ws = cidx + kRowCand;     // 32 words: scan scratch
+  uint32_t* res = ws + 32;            // 0..2: a pick
+  uint32_t* wcnt = res + 32;          // kRowWarps words: candidates per warp region
+  const int tid = threadIdx.x, lane = tid & 31, wid = tid >> 5;
+  const uint32_t lanes_below = (1u << lane) - 1u;
+  grid_dep_wait();  // the scores come from the previous kernel, which may also still read `out`
+  grid_dep_launch();
+  for (int r = blockIdx.x; r < rows; r += gridDim.x) {
+    const int len = row_len(row_lens, seq_lens, nq, r, cap, status);
+    int32_t* o = out + (int64_t)r * k;
+    auto emit = [&](int pos, int t) {
+      o[pos] = t;
+      if (po.phys) po.phys[(int64_t)r * k + pos] = phys_row(po, nq, r, t, status);
+    };
+    if (len <= k) {  // every token, then padding; no shared memory used
+      for (int i = tid; i < k; i += kRowThreads) emit(i, i < len ? i : -1);
+      continue;
+    }
+    const float* row = scores + (int64_t)r * ld;
+    const int nw = (len + 31) >> 5;
+    const int full4 = len >> 2;
+    // body(t0, keys, valid) for every group of 4 tokens t0..t0+3 (valid: a bit
+    // per token of the row); every thread of a warp calls it equally often,
+    // so warp votes inside are allowed
+    const int n4 = (len + 3) >> 2;
+    // group i of the row (16-byte aligned; the ragged last one padded with NaN)
+    auto load_group = [&](int i) -> float4 {
+      if (i < full4) return reinterpret_cast<const float4*>(row)[i];
+      const float nan = __uint_as_float(0x7FC00000u);
+      if (i >= n4) return make_float4(nan, nan, nan, nan);
+      return make_float4(row[4 * i], 4 * i + 1 < len ? row[4 * i + 1] : nan, 4 * i + 2 < len ? row[4 * i + 2] : nan,
+                         nan);
+    };
+    auto group_valid = [&](int i) -> uint32_t {
+      return i < full4 ? 0xFu : (i < n4 ? (1u << (len - 4 * i)) - 1u : 0u);
+    };
+    auto group_keys = [](const float4& v) {
+      return make_uint4(score_key(v.x), score_key(v.y), score_key(v.z), score_key(v.w));
+    };
+    // four groups in flight per thread, held in named registers (no array)
+    static_assert(kRowU == 4, "stream() holds four groups");
+    auto stream = [&](auto&& body) {
+      for (int base = 0; base < n4; base += 4 * kRowThreads) {  // the same trip count in every thread
+        const int i0 = base + tid, i1 = i0 + kRowThreads, i2 = i0 + 2 * kRowThreads, i3 = i0 + 3 * kRowThreads;
+        const float4 v0 = load_group(i0), v1 = load_group(i1), v2 = load_group(i2), v3 = load_group(i3);
+        body(4 * i0, group_keys(v0), group_valid(i0));
+        body(4 * i1, group_keys(v1), group_valid(i1));
+        body(4 * i2, group_keys(v2), group_valid(i2));
+        body(4 * i3, group_keys(v3), group_valid(i3));
+      }
+    };
+
+    for (int i = tid; i < kRowB1; i += kRowThreads) hist[i] = 0u;
+    for (int i = tid; i < nw; i += kRowThreads) {
+      bmA[i] = 0u;
+      bmB[i] = 0u;
+    }
+    __syncthreads();
+    uint32_t* const wkey = ckey + wid * kRowWarpCand;  // this warp's candidate region
+    uint32_t* const widx = cidx + wid * kRowWarpCand;
+    // Stores the keys of the 4-token group at t0 flagged in `grp` in the
+    // warp's region from slot wc on (every lane of the warp calls it with the
+    // same wc, which then counts all of the warp's flagged keys).
+    auto store_cands = [&](int t0, const uint4& kk, uint32_t grp, uint32_t& wc) {
+      uint32_t tot;
+      uint32_t slot = wc + warp_excl_scan_small((uint32_t)__popc(grp), lanes_below, tot);
+      wc += tot;
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        if ((grp >> j) & 1u) {
+          if (slot < (uint32_t)kRowWarpCand) {
+            wkey[slot] = j == 0 ? kk.x : j == 1 ? kk.y : j == 2 ? kk.z : kk.w;
+            widx[slot] = (uint32_t)(t0 + j);
+          }
+          ++slot;
+        }
+      }
+    };
+    RowPick p;
+    uint32_t prefix = 0, need = 0, pop = 0;  // the threshold group: keys whose bits above `shift` equal `prefix`
+    int shift = 20;
+
+    // ---- 0. one pass, where a sample predicts the bar: the first 128 tokens
+    //         of every 1,024 estimate a first-digit bin L with about 1.3 k keys
+    //         above its lower edge; one pass then keeps every key of bin L or above as a
+    //         candidate (the sample's lines are still in L2).  If they number
+    //         at least k and fit their regions, the row's top-k is among them.
+    bool fast = false;
+    {
+      const int64_t n_s = (int64_t)(len / 1024) * 128 + min(128, len % 1024);  // sampled tokens
+      const int64_t need_s = (13 * (int64_t)k * n_s + 10 * (int64_t)len - 1) / (10 * (int64_t)len) + 32;
+      uint32_t bar = kRowB1;  // no candidates pass: go to the general steps
+      if (need_s <= n_s) {
+        const int nchunk = (len + 1023) / 1024;
+        // warp w reads chunks w, w + 32, ...: 32 groups (128 tokens) each
+        auto sample = [&](int c) { return load_group(c < nchunk ? c * 256 + lane : n4); };
+        auto count = [&](int c, const float4& v) {
+          const uint32_t valid = c < nchunk ? group_valid(c * 256 + lane) : 0u;
+          const uint4 kk = group_keys(v);
+          if (valid & 1u) atomicAdd(&hist[kk.x >> 20], 1u);
+          if (valid & 2u) atomicAdd(&hist[kk.y >> 20], 1u);
+          if (valid & 4u) atomicAdd(&hist[kk.z >> 20], 1u);
+          if (valid & 8u) atomicAdd(&hist[kk.w >> 20], 1u);
+        };
+        for (int c0 = wid; c0 < nchunk; c0 += 4 * kRowWarps) {
+          const int c1 = c0 + kRowWarps, c2 = c0 + 2 * kRowWarps, c3 = c0 + 3 * kRowWarps;
+          const float4 v0 = sample(c0), v1 = sample(c1), v2 = sample(c2), v3 = sample(c3);
+          count(c0, v0);
+          count(c1, v1);
+          count(c2, v2);
+          count(c3, v3);
+        }
+        bar = row_pick(hist, kRowB1, (uint32_t)need_s, ws, res).bin;
+      } else if (len <= kRowCand) {
+        bar = 0;  // every key: a warp's stripe of such a row holds at most kRowWarpCand tokens
+      }
+      if (bar < (uint32_t)kRowB1) {
+        for (int i = tid; i < kRowB1; i += kRowThreads) hist[i] = 0u;
+        __syncthreads();
+        uint32_t wc = 0;
+        stream([&](int t0, const uint4& kk, uint32_t valid) {
+          const uint32_t a[4] = {kk.x, kk.y, kk.z, kk.w};
+          uint32_t grp = 0;
+#pragma unroll
+          for (int j = 0; j < 4; ++j)
+            if ((a[j] >> 20) >= bar) grp |= 1u << j;
+          grp &= valid;
+#pragma unroll
+          for (int j = 0; j < 4; ++j)
+            if ((grp >> j) & 1u) atomicAdd(&hist[a[j] >> 20], 1u);
+          store_cands(t0, kk, grp, wc);
+        });
+        if (lane == 0) wcnt[wid] = wc;
+        __syncthreads();
+        bool over = false;
+        uint32_t total = 0;
+        for (int w = 0; w < kRowWarps; ++w) {
+          over |= wcnt[w] > (uint32_t)kRowWarpCand;
+          total += wcnt[w];
+        }
+        if (!over && total >= (uint32_t)k) {
+          fast = true;
+          p = row_pick(hist, kRowB1, (uint32_t)k, ws, res);
+          prefix = p.bin;
+          need = p.need;
+          pop = p.pop;
+        }
+      }
+    }
+
+    // ---- 1. first digit (where the one pass did not settle it)
+    if (!fast) {
+      for (int i = tid; i < kRowB1; i += kRowThreads) hist[i] = 0u;
+      __syncthreads();
+      stream([&](int, const uint4& kk, uint32_t valid) {
+        if (valid & 1u) atomicAdd(&hist[kk.x >> 20], 1u);
+        if (valid & 2u) atomicAdd(&hist[kk.y >> 20], 1u);
+        if (valid & 4u) atomicAdd(&hist[kk.z >> 20], 1u);
+        if (valid & 8u) atomicAdd(&hist[kk.w >> 20], 1u);
+      });
+      p = row_pick(hist, kRowB1, (uint32_t)k, ws, res);
+      prefix = p.bin;
+      need = p.need;
+      pop = p.pop;
+    }
+    bool narrow = false;  // a warp's candidate region overflowed: narrow the group once more
+    while (!fast) {
+      // ---- 2. narrower groups until the candidates fit comfortably
+      while ((pop > (uint32_t)kRowGroupMax || narrow) && shift > 0) {
+        narrow = false;
+        for (int i = tid; i < (1 << kRowD); i += kRowThreads) hist[i] = 0u;
+        __syncthreads();
+        const int s2 = shift - kRowD;
+        stream([&](int, const uint4& kk, uint32_t valid) {
+          const uint32_t a[4] = {kk.x, kk.y, kk.z, kk.w};
+#pragma unroll
+          for (int j = 0; j < 4; ++j)
+            if (((valid >> j) & 1u) && (a[j] >> shift) == prefix)
+              atomicAdd(&hist[(a[j] >> s2) & ((1u << kRowD) - 1u)], 1u);
+        });
+        p = row_pick(hist, 1 << kRowD, need, ws, res);
+        prefix = (prefix << kRowD) | p.bin;
+        need = p.need;
+        pop = p.pop;
+        shift = s2;
+      }
+      // ---- 3. keys above the group into A (a group's 4 tokens share a bitmap
+      //         word); the group into the warp's candidate region (or B)
+      uint32_t wc = 0;  // this warp's candidates so far (the same in every lane)
+      stream([&](int t0, const uint4& kk, uint32_t valid) {
+        const uint32_t a[4] = {kk.x, kk.y, kk.z, kk.w};
+        uint32_t above = 0, grp = 0;
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+          const uint32_t top = a[j] >> shift;
+          if (top > prefix) above |= 1u << j;
+          if (top == prefix) grp |= 1u << j;
+        }
+        above &= valid;
+        grp &= valid;
+        if (above) atomicOr(&bmA[t0 >> 5], above << (t0 & 31));
+        if (shift == 0) {
+          if (grp) atomicOr(&bmB[t0 >> 5], grp << (t0 & 31));
+        } else {
+          store_cands(t0, kk, grp, wc);
+        }
+      });
+      if (lane == 0) wcnt[wid] = wc;
+      __syncthreads();
+      if (shift == 0) break;
+      bool over = false;
+      for (int w = 0; w < kRowWarps; ++w) over |= wcnt[w] > (uint32_t)kRowWarpCand;
+      if (!over) break;
+      narrow = true;  // A keeps its bits: keys above this group are above any narrower one
+      __syncthreads();  // every thread has read the counts
+    }
+    // ---- 4. the last digits over the candidates: the exact k-th key (in
+    //         the one-pass case the candidates hold every key above the group
+    //         too, and they go into A with the others above it)
+    auto for_cands = [&](auto&& body) {  // body(key, token) for every stored candidate
+      for (int c = tid; c < kRowCand; c += kRowThreads)
+        if ((uint32_t)(c % kRowWarpCand) < wcnt[c / kRowWarpCand]) body(ckey[c], cidx[c]);
+    };
+    if (shift > 0) {
+      while (shift > 0) {
+        for (int i = tid; i < (1 << kRowD); i += kRowThreads) hist[i] = 0u;
+        __syncthreads();
+        const int s2 = shift - kRowD;
+        for_cands([&](uint32_t key, uint32_t) {
+          if ((key >> shift) == prefix) atomicAdd(&hist[(key >> s2) & ((1u << kRowD) - 1u)], 1u);
+        });
+        p = row_pick(hist, 1 << kRowD, need, ws, res);
+        prefix = (prefix << kRowD) | p.bin;
+        need = p.need;
+        pop = p.pop;
+        shift = s2;
+      }
+      for_cands([&](uint32_t key, uint32_t t) {
+        if (key > prefix) atomicOr(&bmA[t >> 5], 1u << (t & 31));
+        else if (key == prefix) atomicOr(&bmB[t >> 5], 1u << (t & 31));
+      });
+      __syncthreads();
+    }
+    // ---- 5. the lowest `need` of the tied indices, then the output in order;
+    //         thread t owns the bitmap words [w0, w1)
+    const int per = (nw + kRowThreads - 1) / kRowThreads;
+    const int w0 = min(nw, tid * per), w1 = min(nw, w0 + per);
+    uint32_t tot;
+    if (need < pop) {
+      uint32_t cnt = 0;
+      for (int w = w0; w < w1; ++w) cnt += __popc(bmB[w]);
+      uint32_t run = row_block_scan(cnt, ws, tot);
+      for (int w = w0; w < w1; ++w) {
+        uint32_t x = bmB[w], keep = 0;
+        while (x && run < need) {
+          const uint32_t b = x & (0u - x);
+          keep |= b;
+          x ^= b;
+          ++run;
+        }
+        bmB[w] = keep;
+      }
+      __syncthreads();
+    }
+    uint32_t cnt = 0;
+    for (int w = w0; w < w1; ++w) cnt += __popc(bmA[w] | bmB[w]);
+    uint32_t pos = row_block_scan(cnt, ws, tot);
+    for (int w = w0; w < w1; ++w) {
+      for (uint32_t x = bmA[w] | bmB[w]; x; x &= x - 1) {
+        if (pos < (uint32_t)k) emit((int)pos, w * 32 + __ffs(x) - 1);
+        ++pos;
+      }
+    }
+    if (tid == 0 && tot != (uint32_t)k) report(status, DSA_ERR_BOUNDS);  // consistency check
+    __syncthreads();  // shared memory is reused by the next row
+  }
+}
+
+// Whether the per-row CTA form serves these rows: more rows than one wave of
+// row-resident clusters holds (two CTAs of 20,480 keys per SM), and rows
+// short enough for its bitmaps.
+bool use_row_form(int rows, int max_row_len, int k) {
+  if (max_row_len <= k || max_row_len > kRowMaxLen) return false;
+  const int64_t ctas = (int64_t)rows * ((max_row_len + kResPairKeys - 1) / kResPairKeys);
+  return ctas > 2 * (int64_t)num_sms();
+}
+
+dsa_status_t launch_topk_rows(const float* scores, int64_t ld, const int32_t* row_lens, const int32_t* seq_lens,
+                              int nq, int rows, int cap, int k, int32_t* out, int32_t* status, cudaStream_t st,
+                              const TopkPhys& po) {
+  static std::atomic<bool> attr_set[64];
+  int dev = 0;
+  cudaGetDevice(&dev);
+  if (dev < 64 && !attr_set[dev]) {
+    if (cuda_status(cudaFuncSetAttribute(topk_row_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         (int)kRowSmem)) != DSA_OK)
+      return DSA_ERR_CUDA;
+    attr_set[dev] = true;
+  }
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3((unsigned)std::min(rows, 2 * num_sms()));  // two CTAs per SM, persistent over the rows
+  cfg.blockDim = dim3(kRowThreads);
+  cfg.dynamicSmemBytes = kRowSmem;
+  cfg.stream = st;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  count_launches(1);
+  if (cuda_status(cudaLaunchKernelEx(&cfg, topk_row_kernel, scores, ld, row_lens, seq_lens, nq, rows, cap, k, out,
+                                     status, po)) != DSA_OK)
+    return DSA_ERR_CUDA;
+  return launch_status();
+}
+
 // The two-level form for rows longer than a cluster holds: segments of at
 // most kSegMax tokens (8 CTAs of 20,480 keys, two CTAs per SM), more of them
 // where that fills the SMs better (down to kSegMin tokens), each reduced to
@@ -1441,10 +1862,14 @@ dsa_status_t launch_topk_impl(const float* scores, int64_t ld, const int32_t* ro
                               int32_t* status, cudaStream_t st, const TopkPhys& po, bool two_level_ok) {
   if (rows == 0) return DSA_OK;
   dsa_status_t res = DSA_OK;
-  if (two_level_ok && max_row_len > kResMaxCluster * kResKeys && workspace &&
-      !g_force_multipass.load(std::memory_order_relaxed))
+  const bool forced = g_force_multipass.load(std::memory_order_relaxed);
+  if (two_level_ok && max_row_len > kResMaxCluster * kResKeys && workspace && !forced)
     return launch_topk_two_level(scores, ld, row_lens, seq_lens, nq, rows, max_row_len, k, out, workspace, status, st,
                                  po);
+  // many rows: one CTA per row at a time (the forced four-kernel form keeps
+  // the rows longer than a cluster holds)
+  if (use_row_form(rows, max_row_len, k) && !(forced && max_row_len > kResMaxCluster * kResKeys))
+    return launch_topk_rows(scores, ld, row_lens, seq_lens, nq, rows, max_row_len, k, out, status, st, po);
   if (launch_topk_cluster(scores, ld, row_lens, seq_lens, nq, rows, max_row_len, k, out, status, st, &res, po))
     return res;
   auto al = [](size_t x) { return (x + 255) & ~size_t(255); };

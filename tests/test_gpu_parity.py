@@ -247,6 +247,64 @@ def test_topk_two_level_segment_boundaries(n):
     np.testing.assert_array_equal(got, oracle.topk(m.astype(np.float64), lens, 2048))
 
 
+def test_topk_many_rows_one_cta_per_row():
+    """More rows than one wave of row-resident clusters holds: one CTA per row
+    at a time, streaming the row.  Rows of mixed lengths (shorter than k,
+    k + 1, up to 60,000), all equal (the group narrows to one key value), a
+    threshold group larger than the candidate buffer (scores within one
+    12-bit bin), heavy ties, NaN and infinities, bit-exact against the
+    oracle; one launch."""
+    rng = np.random.default_rng(41)
+    rows, ld = 400, 60_000
+    lens = rng.integers(2_049, ld + 1, rows).astype(np.int32)
+    m = rng.standard_normal((rows, ld)).astype(np.float32)
+    lens[0], lens[1], lens[2] = 100, 2048, 2049
+    m[3, :] = 3.0                                            # all equal
+    m[4, :] = (1.0 + rng.random(ld) * 1e-4).astype(np.float32)   # one 12-bit bin, 60,000 keys
+    m[5, :] = rng.integers(0, 3, ld)                         # heavy ties
+    m[6, ::7] = np.nan
+    m[6, 5] = np.inf
+    m[6, 9] = -np.inf
+    m[7, :] = -np.abs(m[7, :])                               # all negative
+    m[7, 123] = -0.0
+    m[7, 456] = 0.0
+    lens[3:8] = ld
+    n0 = binding.kernel_launches()
+    got = _gpu_topk(torch.from_numpy(m).cuda(), torch.from_numpy(lens).cuda(), 2048, max_row_len=ld)
+    assert binding.kernel_launches() - n0 == 1
+    np.testing.assert_array_equal(got, oracle.topk(m.astype(np.float64), lens, 2048))
+
+
+def test_topk_many_rows_candidates_in_one_region():
+    """The per-row form stores the threshold group's keys per warp; here a
+    row's top keys (10,000 in one 12-bit bin) lie only where one warp reads
+    (the first 128 tokens of every 2,048), so that warp's region overflows:
+    the one-pass candidates and then the group are narrowed until they fit;
+    rows of 160,000 tokens."""
+    rng = np.random.default_rng(7)
+    rows, ld = 40, 160_000
+    m = (rng.standard_normal((rows, ld)) * 1e-3).astype(np.float32)
+    pos = np.nonzero(np.arange(ld) % 2048 < 128)[0]
+    for r in range(10):
+        m[r, pos] = (2.0 + rng.random(pos.size) * 0.01).astype(np.float32)
+    m[10, pos] = 2.0                                         # the same, all tied
+    lens = np.full(rows, ld, dtype=np.int32)
+    lens[20:] = rng.integers(80_000, ld + 1, rows - 20)
+    got = _gpu_topk(torch.from_numpy(m).cuda(), torch.from_numpy(lens).cuda(), 2048, max_row_len=ld)
+    np.testing.assert_array_equal(got, oracle.topk(m.astype(np.float64), lens, 2048))
+
+
+@pytest.mark.parametrize("k", [1, 100, 2047])
+def test_topk_many_rows_small_k(k):
+    rng = np.random.default_rng(k)
+    rows, ld = 320, 24_000
+    lens = rng.integers(1, ld + 1, rows).astype(np.int32)
+    m = rng.standard_normal((rows, ld)).astype(np.float32)
+    m[::5, ::3] = 0.25                                       # ties on many rows
+    got = _gpu_topk(torch.from_numpy(m).cuda(), torch.from_numpy(lens).cuda(), k, max_row_len=ld)
+    np.testing.assert_array_equal(got, oracle.topk(m.astype(np.float64), lens, k))
+
+
 @pytest.mark.parametrize("lens,launches", [
     ([3000] * 32, 3),        # 4 chunks per row: the MLA merges them itself (a cluster per row)
     ([9000, 130], 4),        # 16 chunks per row: plus the combine kernel

@@ -33,6 +33,7 @@ def _topk_paged(case, dc, scores, k=2048, with_phys=True):
     ([260_000, 3000], 1, False),              # the two-level cluster form
     ([200_000, 340_000], 2, False),           # two levels with draft rows (2 segments and 3)
     ([260_000, 3000], 1, True),               # the four-kernel path
+    ([50_000, 30_000], 160, False),           # many rows: one CTA per row
 ])
 def test_topk_paged_rows_match_the_oracle(lens, nq, multipass):
     case = synth.make_case("ph", seq_lens=lens, nq=nq, seed=len(lens) + nq)
