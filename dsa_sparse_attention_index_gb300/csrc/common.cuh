@@ -154,6 +154,11 @@ __device__ __forceinline__ void bulk_load(uint32_t dst, const void* src, uint32_
                ::"r"(dst), "l"(src), "r"(bytes), "r"(bar)
                : "memory");
 }
+// Asks L2 to fetch [src, src + bytes) (16-byte aligned, a multiple of 16 bytes)
+// without waiting for it.
+__device__ __forceinline__ void prefetch_l2(const void* src, uint32_t bytes) {
+  asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(src), "r"(bytes) : "memory");
+}
 // Make this thread's generic-proxy shared-memory writes visible to the async
 // proxy (tensor core / TMA) before signalling the consumer.
 __device__ __forceinline__ void fence_proxy_async_smem() {

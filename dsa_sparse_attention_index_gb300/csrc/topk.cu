@@ -1302,6 +1302,7 @@ constexpr int kRowCand = 6144;               // group keys held in shared memory
 constexpr int kRowWarpCand = kRowCand / kRowWarps;  // ... in one region per warp
 constexpr int kRowGroupMax = kRowCand / 2;   // larger groups are narrowed first
 constexpr int kRowU = 4;                     // 16-byte loads in flight per thread
+constexpr int kRowAhead = 4;                 // L2 prefetch distance in loop steps (32 KB each)
 constexpr size_t kRowSmem = (size_t)(kRowB1 + 2 * kRowWords + 2 * kRowCand + 96) * 4;
 static_assert(kRowWarps <= 32, "the block scan holds the warp totals in one warp's lanes");
 // a row of at most kRowCand tokens puts at most kRowWarpCand of them in each warp's stripe
@@ -1420,8 +1421,19 @@ __global__ void __launch_bounds__(kRowThreads, 2)
     };
     // four groups in flight per thread, held in named registers (no array)
     static_assert(kRowU == 4, "stream() holds four groups");
+    // L2 prefetch of step `it` of a pass (its 4 x kRowThreads groups), kRowAhead
+    // steps before the loads: the loads then mostly wait on L2, not HBM
+    auto prefetch = [&](int it) {
+      const int g0 = it * 4 * kRowThreads;
+      if (tid == 0 && g0 < full4) prefetch_l2(row + 4 * (int64_t)g0, (uint32_t)min(4 * kRowThreads, full4 - g0) * 16u);
+    };
+    bool primed = false;  // the row's first pass finds its first prefetches issued
     auto stream = [&](auto&& body) {
+      if (!primed)
+        for (int d = 0; d < kRowAhead; ++d) prefetch(d);
+      primed = false;
       for (int base = 0; base < n4; base += 4 * kRowThreads) {  // the same trip count in every thread
+        prefetch(base / (4 * kRowThreads) + kRowAhead);
         const int i0 = base + tid, i1 = i0 + kRowThreads, i2 = i0 + 2 * kRowThreads, i3 = i0 + 3 * kRowThreads;
         const float4 v0 = load_group(i0), v1 = load_group(i1), v2 = load_group(i2), v3 = load_group(i3);
         body(4 * i0, group_keys(v0), group_valid(i0));
@@ -1436,6 +1448,8 @@ __global__ void __launch_bounds__(kRowThreads, 2)
       bmA[i] = 0u;
       bmB[i] = 0u;
     }
+    for (int d = 0; d < kRowAhead; ++d) prefetch(d);  // the row's first pass, while the sample is read
+    primed = true;
     __syncthreads();
     uint32_t* const wkey = ckey + wid * kRowWarpCand;  // this warp's candidate region
     uint32_t* const widx = cidx + wid * kRowWarpCand;
@@ -1462,21 +1476,21 @@ __global__ void __launch_bounds__(kRowThreads, 2)
     int shift = 20;
 
     // ---- 0. one pass, where a sample predicts the bar: the first 128 tokens
-    //         of every 1,024 estimate a first-digit bin L with about 1.3 k keys
+    //         of every 2,048 estimate a first-digit bin L with about 1.3 k keys
     //         above its lower edge; one pass then keeps every key of bin L or above as a
     //         candidate (the sample's lines are still in L2).  If they number
     //         at least k and fit their regions, the row's top-k is among them.
     bool fast = false;
     {
-      const int64_t n_s = (int64_t)(len / 1024) * 128 + min(128, len % 1024);  // sampled tokens
+      const int64_t n_s = (int64_t)(len / 2048) * 128 + min(128, len % 2048);  // sampled tokens
       const int64_t need_s = (13 * (int64_t)k * n_s + 10 * (int64_t)len - 1) / (10 * (int64_t)len) + 32;
       uint32_t bar = kRowB1;  // no candidates pass: go to the general steps
       if (need_s <= n_s) {
-        const int nchunk = (len + 1023) / 1024;
-        // warp w reads chunks w, w + 32, ...: 32 groups (128 tokens) each
-        auto sample = [&](int c) { return load_group(c < nchunk ? c * 256 + lane : n4); };
+        const int nchunk = (len + 2047) / 2048;
+        // warp w reads chunks w, w + kRowWarps, ...: their first 32 groups (128 tokens)
+        auto sample = [&](int c) { return load_group(c < nchunk ? c * 512 + lane : n4); };
         auto count = [&](int c, const float4& v) {
-          const uint32_t valid = c < nchunk ? group_valid(c * 256 + lane) : 0u;
+          const uint32_t valid = c < nchunk ? group_valid(c * 512 + lane) : 0u;
           const uint4 kk = group_keys(v);
           if (valid & 1u) atomicAdd(&hist[kk.x >> 20], 1u);
           if (valid & 2u) atomicAdd(&hist[kk.y >> 20], 1u);
@@ -1498,19 +1512,51 @@ __global__ void __launch_bounds__(kRowThreads, 2)
       if (bar < (uint32_t)kRowB1) {
         for (int i = tid; i < kRowB1; i += kRowThreads) hist[i] = 0u;
         __syncthreads();
-        uint32_t wc = 0;
-        stream([&](int t0, const uint4& kk, uint32_t valid) {
-          const uint32_t a[4] = {kk.x, kk.y, kk.z, kk.w};
-          uint32_t grp = 0;
+        // keys of bin `bar` or above, compared as scores (score_range: NaN
+        // scores are below every bin but bin 0, where every score passes)
+        const KeyRange kr = key_range(bar, 20);
+        auto pass = [&](const float4& v, uint32_t valid) -> uint32_t {
+          return (kr.s.nan ? 0xFu : ((uint32_t)(v.x >= kr.s.lo) | ((uint32_t)(v.y >= kr.s.lo) << 1) |
+                                     ((uint32_t)(v.z >= kr.s.lo) << 2) | ((uint32_t)(v.w >= kr.s.lo) << 3))) &
+                 valid;
+        };
+        auto elem = [](const float4& v, int j) { return j == 0 ? v.x : j == 1 ? v.y : j == 2 ? v.z : v.w; };
+        uint32_t wc = 0;  // this warp's candidates so far (the same in every lane)
+        if (tid == 0 && !primed)
+          for (int d = 0; d < kRowAhead; ++d) prefetch(d);
+        primed = false;
+        for (int base = 0; base < n4; base += 4 * kRowThreads) {  // the same trip count in every thread
+          prefetch(base / (4 * kRowThreads) + kRowAhead);
+          const int i0 = base + tid;
+          const float4 v0 = load_group(i0), v1 = load_group(i0 + kRowThreads), v2 = load_group(i0 + 2 * kRowThreads),
+                       v3 = load_group(i0 + 3 * kRowThreads);
+          // bit 4u + j: element j of group i0 + u * kRowThreads passes
+          const uint32_t m = pass(v0, group_valid(i0)) | (pass(v1, group_valid(i0 + kRowThreads)) << 4) |
+                             (pass(v2, group_valid(i0 + 2 * kRowThreads)) << 8) |
+                             (pass(v3, group_valid(i0 + 3 * kRowThreads)) << 12);
+          // the warp's exclusive prefix of the lanes' counts (0..16: five bit planes)
+          const uint32_t c = (uint32_t)__popc(m);
+          uint32_t before = 0, tot = 0;
 #pragma unroll
-          for (int j = 0; j < 4; ++j)
-            if ((a[j] >> 20) >= bar) grp |= 1u << j;
-          grp &= valid;
-#pragma unroll
-          for (int j = 0; j < 4; ++j)
-            if ((grp >> j) & 1u) atomicAdd(&hist[a[j] >> 20], 1u);
-          store_cands(t0, kk, grp, wc);
-        });
+          for (int bit = 0; bit < 5; ++bit) {
+            const uint32_t plane = __ballot_sync(0xffffffffu, (c >> bit) & 1u);
+            before += (uint32_t)__popc(plane & lanes_below) << bit;
+            tot += (uint32_t)__popc(plane) << bit;
+          }
+          uint32_t slot = wc + before;
+          wc += tot;
+          for (uint32_t mm = m; mm; mm &= mm - 1) {
+            const int b = __ffs(mm) - 1, u = b >> 2, j = b & 3;
+            const float e0 = elem(v0, j), e1 = elem(v1, j), e2 = elem(v2, j), e3 = elem(v3, j);
+            const uint32_t key = score_key(u == 0 ? e0 : u == 1 ? e1 : u == 2 ? e2 : e3);
+            atomicAdd(&hist[key >> 20], 1u);
+            if (slot < (uint32_t)kRowWarpCand) {
+              wkey[slot] = key;
+              widx[slot] = (uint32_t)(4 * (i0 + u * kRowThreads) + j);
+            }
+            ++slot;
+          }
+        }
         if (lane == 0) wcnt[wid] = wc;
         __syncthreads();
         bool over = false;
