@@ -20,6 +20,16 @@
 // chosen indices in ascending order at a place from warp and cluster scans.
 // No workspace is used.
 //
+// Many rows of at most 163,840 tokens (more than one wave of clusters, such
+// as a prefill chunk's rows) take topk_row_kernel instead: one CTA per row at
+// a time, two per SM, persistent over the rows.  A sample of the row sets a
+// bar with about 1.3 k keys above it; one pass streams the row, comparing
+// scores against the bar as floats, and keeps every key above it as a
+// candidate in shared memory; the selection then runs over the candidates
+// and the output goes through bitmaps of the row.  If the sample misleads
+// (fewer than k keys pass, or more than fit), exact digit passes over the
+// row take over.
+//
 // Longer rows (the 1M-token rows) with fp32 scores and a workspace take two
 // levels of the same kernel: pass 1 selects the top-k of every segment of at
 // most 163,840 tokens (one cluster per segment, as many segments as fill the
