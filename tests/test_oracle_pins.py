@@ -266,6 +266,31 @@ def test_topk_matches_python_sort_on_random_rows():
         _is_valid_topk(s[r], n, 2048, got[r])
 
 
+@pytest.mark.parametrize("seg", [97, 500, 2048])
+def test_topk_of_segment_topks_is_the_topk(seg):
+    """The decomposition the two-level selection of long rows rests on: the
+    top-k of a row equals the top-k over the union of its segments' top-k,
+    with the union kept in token order so that ties still go to the lower
+    index (ties within and across segments, NaN, a short last segment)."""
+    rng = np.random.default_rng(seg)
+    k = 64
+    for trial in range(20):
+        n = int(rng.integers(1, 4000))
+        row = rng.choice([0.0, 1.0, 2.0, np.nan, -1.0], size=n) + (rng.random(n) < 0.5) * rng.standard_normal(n)
+        s = row[None, :]
+        want = oracle.topk(s, np.array([n]), k)[0]
+        cand = []
+        for p0 in range(0, n, seg):
+            part = row[p0:p0 + seg]
+            sel = oracle.topk(part[None, :], np.array([part.size]), k)[0]
+            cand += [p0 + int(t) for t in sel if t >= 0]
+        cand = np.array(cand)                        # ascending: segments in order, each ascending
+        assert np.all(np.diff(cand) > 0)
+        sub = oracle.topk(row[cand][None, :], np.array([cand.size]), k)[0]
+        got = np.array([cand[t] if t >= 0 else -1 for t in sub])
+        np.testing.assert_array_equal(got, want)
+
+
 # --------------------------------------------------------------- sparse MLA
 def _latent(case, b, t):
     r = case.block_table[b, t // 64]
