@@ -294,6 +294,39 @@ def test_topk_many_rows_candidates_in_one_region():
     np.testing.assert_array_equal(got, oracle.topk(m.astype(np.float64), lens, 2048))
 
 
+def test_topk_many_rows_without_allocation():
+    """The no-allocation entry point takes the per-row form too (64 rows of
+    up to 120,000 tokens are more than a wave of clusters): one launch, no
+    workspace, bit-exact against the oracle."""
+    rng = np.random.default_rng(64)
+    rows, ld = 64, 120_000
+    m = rng.standard_normal((rows, ld)).astype(np.float32)
+    m[1, :] = 0.0
+    m[2, ::5] = 9.0
+    lens = rng.integers(90_000, ld + 1, rows).astype(np.int32)
+    lens[3] = 2048
+    idx = torch.full((rows, 2048), -7, dtype=torch.int32, device="cuda")
+    st = _status()
+    n0 = binding.kernel_launches()
+    binding.topk_noalloc(torch.from_numpy(m).cuda(), torch.from_numpy(lens).cuda(), ld, 2048, idx, st)
+    torch.cuda.synchronize()
+    assert binding.kernel_launches() - n0 == 1
+    assert st.item() == 0, binding.status_string(st.item())
+    np.testing.assert_array_equal(idx.cpu().numpy(), oracle.topk(m.astype(np.float64), lens, 2048))
+
+
+def test_topk_many_long_rows_in_waves_of_clusters():
+    """Many rows longer than the per-row form takes (180,000 tokens): the
+    row-resident clusters in several waves, bit-exact against the oracle."""
+    rng = np.random.default_rng(180)
+    rows, ld = 200, 180_000
+    m = rng.standard_normal((rows, ld)).astype(np.float32)
+    m[::7, ::11] = 1.5
+    lens = rng.integers(164_000, ld + 1, rows).astype(np.int32)
+    got = _gpu_topk(torch.from_numpy(m).cuda(), torch.from_numpy(lens).cuda(), 2048, max_row_len=ld)
+    np.testing.assert_array_equal(got, oracle.topk(m.astype(np.float64), lens, 2048))
+
+
 @pytest.mark.parametrize("k", [1, 100, 2047])
 def test_topk_many_rows_small_k(k):
     rng = np.random.default_rng(k)
