@@ -83,6 +83,15 @@ def test_host_validation_without_device(lib):
     assert lib.dsa_index_scores(ctypes.byref(c), ctypes.byref(b), 1024, 2048, 4096, 104, st,
                                 None) == B.ERR_INVALID_ARG
     c.latent_format, c.row_stride, c.index_off = 0, 45312, 36864
+    # rows longer than a cluster holds need the two-level workspace: NULL, too small or
+    # misaligned is refused before anything is launched
+    need = lib.dsa_topk_workspace_size(4, 1 << 20, 2048)
+    assert lib.dsa_topk(128, 1 << 20, 256, 4, 1 << 20, 2048, 512, None, 0, st, None) == B.ERR_WORKSPACE
+    assert lib.dsa_topk(128, 1 << 20, 256, 4, 1 << 20, 2048, 512, 1 << 20, need - 1, st, None) == B.ERR_WORKSPACE
+    assert lib.dsa_topk(128, 1 << 20, 256, 4, 1 << 20, 2048, 512, (1 << 20) + 16, need, st, None) == B.ERR_WORKSPACE
+    assert lib.dsa_topk(128, (1 << 20) + 2, 256, 4, 1 << 20, 2048, 512, 1 << 20, need, st, None) == B.ERR_INVALID_ARG
+    # the no-allocation entry point: at most 64 rows
+    assert lib.dsa_topk_noalloc(128, 1 << 20, 256, 65, 1 << 20, 2048, 512, st, None) == B.ERR_UNSUPPORTED
     # bf16 scores: rows of a multiple of 8 elements
     assert lib.dsa_topk_bf16(128, 12, 256, 1, 10, 2048, 512, st, None) == B.ERR_INVALID_ARG
     assert lib.dsa_topk_bf16(128, 16, 256, 1, 10, 0, 512, st, None) == B.ERR_INVALID_ARG
